@@ -1,0 +1,187 @@
+/*
+ * prefill.h -- C ABI of the KV-shared prompt-prefill library (GB300, sm_103a).
+ *
+ * What it computes.  The prompt-prefill forward pass of a decoder-only
+ * transformer whose last layers are KV-shared:
+ *   - layers il < n_layer_kv_from_start compute Q/K/V for every prompt row and
+ *     write FP16 K/V into the KV cache;
+ *   - layers il >= n_layer_kv_from_start write nothing and attend to the cache
+ *     of an earlier layer (kv_src[il]); so, before the first such layer, the
+ *     rows no output needs are pruned: an intermediate ubatch stops there and
+ *     the final ubatch carries exactly one row (its last) through them.
+ *   ("llama.cpp Gemma 4 prefill KV graph optimization", devotd.net news,
+ *   section 1, with its listing of the pruning condition; outputs unchanged,
+ *   end of section 3.)
+ * The per-layer-embedding scaling (same page, section 1) is part of the pass,
+ * and the FP16 KV cache can be saved to and restored from a "KVCP" image to
+ * reuse a fixed system-prompt prefix ("PicoLM KV Cache persistence",
+ * xxqk.cn news 668802, "usage", "file" and "rules" paragraphs).
+ *
+ * Model, per layer (pre-norm):  y = rmsnorm(x)*(1+g);  q,k,v = y W^T;
+ * half-split RoPE on q,k;  o = causal GQA attention;  x += o Wo^T;
+ * y = rmsnorm(x)*(1+g);  x += (act(y Wg^T) * (y Wu^T)) Wd^T  (act = GELU-tanh
+ * or SiLU);  if ple_dim > 0:  x += (gelu(x Wpg^T) * ple[il]) Wpp^T, with
+ * ple[il] = E_ple[token, il, :] / sqrt(ple_dim).  Logits = rmsnorm(x_last)*(1+g)
+ * times the tied token-embedding matrix.
+ *
+ * Conventions.
+ *   - Every call returns an int status: 0 = PF_OK, negative = PF_E_*.  No
+ *     exception crosses the ABI; kernels never trap.  prefill_last_error()
+ *     gives a message for the last failure on a context.
+ *   - Device work is ordered on the stream given at create (or the legacy
+ *     default stream when NULL).  prefill_ubatch, kv_save and kv_load return
+ *     once the work is enqueued; prefill_sync() waits for it and reports a
+ *     device-side error (a bad token, a timed-out pipeline wait).
+ *   - A context holds one sequence (n_seq_max == 1).
+ */
+#ifndef PREFILL_KV_SHARED_H
+#define PREFILL_KV_SHARED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define PF_OK 0
+#define PF_E_ARG (-1)            /* bad argument, token, position or size */
+#define PF_E_KV_MAGIC (-2)       /* KV image does not start with "KVCP" */
+#define PF_E_KV_SHAPE (-3)       /* KV image layer count or kv_dim differs from the model */
+#define PF_E_KV_RANGE (-4)       /* n_pos beyond the image or the context; image too short */
+#define PF_E_CUDA (-5)           /* a CUDA call failed */
+#define PF_E_DEVICE_TIMEOUT (-6) /* a kernel gave up a bounded wait; results are invalid */
+#define PF_E_DEVICE_TOKEN (-7)   /* a device-resident token id was out of range */
+#define PF_E_NOMEM (-8)          /* device allocation failed */
+
+/* weight storage types */
+#define PF_W_F32 0  /* fp32 matrices (computed as bf16 on the GPU) */
+#define PF_W_Q4_0 2 /* Q4_0: 32-element blocks of 18 bytes: fp16 scale d (little
+                       endian), 16 bytes; byte j = element j (low nibble), element
+                       j+16 (high nibble); value d*(nibble-8) */
+
+/* feed-forward gate activation */
+#define PF_FFN_GEGLU 0  /* gelu_tanh(g) * u */
+#define PF_FFN_SWIGLU 1 /* silu(g) * u */
+
+typedef struct prefill_ctx prefill_ctx; /* opaque */
+
+typedef struct prefill_model_desc {
+  int32_t n_layer;
+  int32_t n_layer_kv_from_start; /* first KV-shared layer (== n_layer: none) */
+  int32_t d_model;
+  int32_t n_head;
+  int32_t n_head_kv;
+  int32_t head_dim; /* 64 or 256 */
+  int32_t ffn_dim;
+  int32_t vocab;
+  int32_t ple_dim; /* per-layer embedding width; 0 = no per-layer embeddings */
+  int32_t ffn_kind;  /* PF_FFN_* */
+  int32_t wtype;     /* PF_W_* for every matrix and embedding table */
+  float rms_eps;
+  float rope_base;
+  const int32_t* kv_src; /* [n_layer]: -1 for writing layers, else the writing layer
+                            whose cache the layer reads; copied at create */
+  int32_t max_ctx;        /* positions the KV cache holds */
+  int32_t ubatch_max;     /* largest n_tokens per prefill_ubatch */
+  int32_t prune_shared_enable; /* 1: prune before the first KV-shared layer when the
+                                  condition holds; 0: every row passes every layer */
+  int32_t n_seq_max;      /* sequences sharing the context; pruning needs 1 */
+  int32_t embeddings;     /* nonzero: an embeddings output is requested (disables pruning) */
+} prefill_model_desc;
+
+/* host pointers; the library copies (and repacks) everything at create.
+   Matrices are [out][in] row-major in the model's wtype; norm gains are fp32.
+   Absent tensors (wk/wv of KV-shared layers, ple_* when ple_dim == 0) are NULL. */
+typedef struct prefill_layer_weights {
+  const void *attn_norm, *wq, *wk, *wv, *wo, *ffn_norm, *w_gate, *w_up, *w_down, *ple_gate, *ple_proj;
+} prefill_layer_weights;
+
+typedef struct prefill_weights {
+  const void* tok_embd; /* [vocab][d_model]; also the LM head (tied) */
+  const void* ple_embd; /* [vocab][n_layer * ple_dim] or NULL */
+  const void* out_norm; /* fp32 [d_model] */
+  const prefill_layer_weights* layers; /* [n_layer] */
+} prefill_weights;
+
+/* Build a context on the current CUDA device: validates the description,
+   uploads and repacks the weights, allocates the FP16 KV cache
+   (2 x writing layers x max_ctx x kv_dim) and the activation buffers for
+   ubatch_max rows.  cuda_stream: a cudaStream_t or NULL.  On failure *out is
+   NULL and the status says why. */
+int prefill_create(const prefill_model_desc* desc, const prefill_weights* weights, void* cuda_stream,
+                   prefill_ctx** out);
+
+/* Run one ubatch of n_tokens tokens at positions pos0 .. pos0+n_tokens-1.
+   tokens: host memory (validated on the host: PF_E_ARG on an id outside
+   [0, vocab)) or device memory (validated on the device: PF_E_DEVICE_TOKEN at
+   prefill_sync).  pos0 must equal the context's position count (ubatches
+   continue the sequence), and pos0 + n_tokens <= max_ctx, 1 <= n_tokens <=
+   ubatch_max.  is_last: this ubatch ends the prompt; its last row's logits
+   (fp32 [vocab], device memory) are written to `logits`, which may be NULL
+   otherwise.  With pruning active, a non-final ubatch runs only the writing
+   layers.  Enqueue only: call prefill_sync to wait. */
+int prefill_ubatch(prefill_ctx* ctx, const int32_t* tokens, int32_t n_tokens, int64_t pos0, int32_t is_last,
+                   float* logits);
+
+/* Wait for the context's stream and report device-side errors. */
+int prefill_sync(prefill_ctx* ctx);
+
+/* Positions currently in the cache. */
+int64_t prefill_n_pos(const prefill_ctx* ctx);
+
+/* Forget the sequence (position count 0); the cache memory is kept. */
+int prefill_reset(prefill_ctx* ctx);
+
+/* Switch pruning on or off for later ubatches (the A/B switch); the pruning
+   condition itself still has to hold.  prefill_prune_active() says whether
+   ubatches are pruned with the current settings. */
+int prefill_set_prune(prefill_ctx* ctx, int32_t enable);
+int prefill_prune_active(const prefill_ctx* ctx);
+
+/* Size in bytes of a KV image of n_pos positions for this model:
+   16-byte header + 2 * writing_layers * n_pos * kv_dim * 2. */
+int64_t prefill_kv_image_bytes(const prefill_ctx* ctx, int64_t n_pos);
+
+/* Write the cache's first prefill_n_pos() positions as a KV image to dst
+   (device or host memory, 16-byte aligned, dst_bytes >= the image size).
+   Image: "KVCP", int32 n_pos, int32 writing layers, int32 kv_dim (little
+   endian), then FP16 keys [layer][pos][kv_dim], then FP16 values.  Only
+   prompt positions are ever in the cache. */
+int kv_save(prefill_ctx* ctx, void* dst, size_t dst_bytes);
+
+/* Restore the first n_pos positions of a KV image (device or host memory) and
+   set the position count to n_pos; the next ubatch continues at n_pos.  A
+   wrong magic (PF_E_KV_MAGIC), a layer/kv_dim mismatch (PF_E_KV_SHAPE), or
+   n_pos beyond the image's positions or max_ctx (PF_E_KV_RANGE) is refused
+   and leaves the cache and position count unchanged: the caller then runs a
+   full prefill.  Whether the image was made from the same prompt prefix is
+   the caller's contract (the image stores no tokens). */
+int kv_load(prefill_ctx* ctx, const void* src, size_t src_bytes, int64_t n_pos);
+
+void prefill_destroy(prefill_ctx* ctx);
+
+const char* prefill_last_error(const prefill_ctx* ctx);
+
+/* ---- host-only helpers (no GPU needed) ---- */
+
+/* The pruning condition for a description (n_seq_max == 1, no embeddings,
+   0 < n_layer_kv_from_start < n_layer, pruning enabled).  Returns 1 or 0, or
+   PF_E_ARG for a NULL description. */
+int prefill_prune_predicate(const prefill_model_desc* desc);
+
+/* Validate a 16-byte KV image header against a model (writing layers, kv_dim),
+   a requested n_pos, the context length and the image size.  Returns PF_OK or
+   PF_E_KV_MAGIC / PF_E_KV_SHAPE / PF_E_KV_RANGE. */
+int prefill_kv_header_check(const void* header16, int32_t n_layers_written, int32_t kv_dim, int64_t n_pos,
+                            int64_t max_ctx, size_t image_bytes);
+
+/* 16 + 2 * n_layers_written * n_pos * kv_dim * 2, or -1 on negative input. */
+int64_t prefill_kv_image_bytes_for(int32_t n_layers_written, int64_t n_pos, int32_t kv_dim);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PREFILL_KV_SHARED_H */

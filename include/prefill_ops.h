@@ -1,0 +1,86 @@
+/*
+ * prefill_ops.h -- per-kernel entry points of the KV-shared prefill library.
+ *
+ * Each call runs ONE of the library's CUDA kernels (the same launchers the
+ * prefill pass uses) on caller-provided device buffers, waits for it, and
+ * returns a status (PF_OK or a negative PF_E_* from prefill.h).  They exist
+ * so that every step of the pass can be checked on its own against a
+ * reference.  Weights are passed as host pointers and uploaded for the call.
+ * Calls are synchronous on `stream` (a cudaStream_t or NULL).
+ *
+ * Matrices are row-major.  bf16/fp16 buffers hold raw 16-bit values.  The A
+ * operand of every GEMM (a_dev, bf16 [a_rows][K]) must have a_rows >= 128
+ * rows allocated (rows beyond M are read but their results are dropped) and
+ * K a multiple of 64.
+ */
+#ifndef PREFILL_OPS_H
+#define PREFILL_OPS_H
+
+#include <stdint.h>
+
+#include "prefill.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* out[m][n] = sum_k A[m][k] W[n][k] (fp32 [M][N]); W [N][K] in wtype
+   (PF_W_Q4_0 blocks or fp32, computed as bf16).  bn: N-tile, 128 or 256. */
+int pfop_linear_f32(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn, const void* a_dev,
+                    int32_t a_rows, int32_t M, float* out_dev, void* stream);
+
+/* x[m][n] += (A W^T)[m][n] (fp32 [M][N], in place); if xb_dev != NULL also
+   xb[m][n] = bf16(new x[m][n]).  N must be a multiple of 32. */
+int pfop_linear_resid(int32_t wtype, const void* w_host, int32_t N, int32_t K, const void* a_dev, int32_t a_rows,
+                      int32_t M, float* x_dev, void* xb_dev, void* stream);
+
+/* h[m][f] = act(A Wg^T)[m][f] * (A Wu^T)[m][f] (bf16 [M][F]); act 0 =
+   gelu_tanh (GeGLU), 1 = silu (SwiGLU).  F a multiple of 64. */
+int pfop_linear_glu(int32_t wtype, const void* wg_host, const void* wu_host, int32_t F, int32_t K, int32_t act,
+                    const void* a_dev, int32_t a_rows, int32_t M, void* h_dev, void* stream);
+
+/* out[m][p] = bf16(gelu_tanh((A W^T)[m][p]) * ple[m*ple_stride + p]) (bf16
+   [M][P]); ple bf16.  P a multiple of 32 (the per-layer-embedding gate). */
+int pfop_linear_ple(int32_t wtype, const void* w_host, int32_t P, int32_t K, const void* a_dev, int32_t a_rows,
+                    int32_t M, const void* ple_dev, int32_t ple_stride, void* out_dev, void* stream);
+
+/* Q/K/V projection with half-split RoPE at positions pos0+m (angle
+   pos * base^(-2i/hd), i < hd/2, pairing i with i+hd/2):
+   q_out fp16 [M][Hq*hd]; if wk_host/wv_host are not NULL, K (rotated) and V
+   go to the fp16 caches kc/vc [max_ctx][Hkv*hd] at rows pos0+m. */
+int pfop_linear_qkv(int32_t wtype, const void* wq_host, const void* wk_host, const void* wv_host, int32_t Hq,
+                    int32_t Hkv, int32_t hd, int32_t K, float rope_base, const void* a_dev, int32_t a_rows,
+                    int32_t M, int32_t pos0, int32_t max_ctx, void* q_dev, void* kc_dev, void* vc_dev, void* stream);
+
+/* Causal GQA attention: q fp16 [M][Hq*hd] at positions pos_base+m, K/V fp16
+   [positions][Hkv*hd] with keys [0, kv_len) valid; out bf16 [M][Hq*hd].
+   mode 0: all rows, in-CTA ordered chunk fold; mode 1: one row (M == 1),
+   split-K chunk partials + ordered warp merge. */
+int pfop_attention(int32_t mode, const void* q_dev, const void* k_dev, const void* v_dev, int32_t M, int32_t Hq,
+                   int32_t Hkv, int32_t hd, int32_t pos_base, int32_t kv_len, void* out_dev, void* stream);
+
+/* y[i] = bf16(rmsnorm(x[row0+i]) * (1 + g)) for i < M (x fp32 [.][D]); if
+   xcopy_dev != NULL, xcopy[i] = x[row0+i]. */
+int pfop_rmsnorm(const float* x_dev, int32_t row0, int32_t M, int32_t D, const float* g_host, float eps, void* y_dev,
+                 float* xcopy_dev, void* stream);
+
+/* x[t] = E[tok_t] (fp32 [T][D]); if ple_host != NULL, ple[t] = bf16(E_ple[tok_t] *
+   ple_scale) (bf16 [T][LP]).  Tables in wtype.  tok_dev: int32 device. */
+int pfop_embed(int32_t wtype, const void* tok_host, const void* ple_host, int32_t vocab, int32_t D, int32_t LP,
+               float ple_scale, const int32_t* tok_dev, int32_t T, float* x_dev, void* ple_dev, void* stream);
+
+/* The KV image copy kernel.  dir 0: cache -> image (writes the 16-byte header
+   `header`, then n_seg segments of copy_bytes); dir 1: image -> cache.
+   Segment s is at s*cache_seg_halves halves in the cache and at
+   16 + s*img_seg_bytes bytes in the image. */
+int pfop_kv_copy(int32_t dir, void* cache_dev, int64_t cache_seg_halves, void* image_dev, int64_t img_seg_bytes,
+                 int32_t n_seg, int64_t copy_bytes, const int32_t* header4, void* stream);
+
+/* Last error message of a pfop_* call on this thread. */
+const char* pfop_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PREFILL_OPS_H */

@@ -33,11 +33,12 @@ def q4_0_decode(blocks: np.ndarray) -> np.ndarray:
     blocks = np.asarray(blocks, dtype=np.uint8)
     d = blocks[..., 0:2].copy().view(np.float16)[..., 0].astype(F32)
     qs = blocks[..., 2:18]
-    lo = (qs & 0x0F).astype(np.int16) - 8
-    hi = (qs >> 4).astype(np.int16) - 8
-    q = np.concatenate([lo, hi], axis=-1).astype(F32)   # [..., nb, 32]
-    vals = d[..., None] * q
-    return vals.reshape(*blocks.shape[:-2], blocks.shape[-2] * 32)
+    q = np.empty(blocks.shape[:-1] + (32,), dtype=F32)
+    q[..., :16] = qs & 0x0F          # element j: low nibble of byte j
+    q[..., 16:] = qs >> 4            # element j+16: high nibble of byte j
+    q -= F32(8.0)
+    q *= d[..., None]
+    return q.reshape(*blocks.shape[:-2], blocks.shape[-2] * 32)
 
 
 def as_f32_matrix(w: np.ndarray) -> np.ndarray:

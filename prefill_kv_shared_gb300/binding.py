@@ -1,0 +1,271 @@
+"""ctypes binding of the C ABI (include/prefill.h, include/prefill_ops.h).
+
+Argument marshalling only: every step of the prefill pass runs in the CUDA
+library.  There is no fallback: if the library is missing or a call fails,
+the binding raises.  PyTorch is used by callers for device memory and
+streams; this module passes raw pointers and sizes.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libprefill_kv_shared.so")
+
+PF_OK = 0
+PF_E_ARG = -1
+PF_E_KV_MAGIC = -2
+PF_E_KV_SHAPE = -3
+PF_E_KV_RANGE = -4
+PF_E_CUDA = -5
+PF_E_DEVICE_TIMEOUT = -6
+PF_E_DEVICE_TOKEN = -7
+PF_E_NOMEM = -8
+
+PF_W_F32 = 0
+PF_W_Q4_0 = 2
+PF_FFN_GEGLU = 0
+PF_FFN_SWIGLU = 1
+
+# every symbol the headers declare
+EXPORTS = (
+    "prefill_create", "prefill_ubatch", "prefill_sync", "prefill_n_pos", "prefill_reset",
+    "prefill_set_prune", "prefill_prune_active", "prefill_kv_image_bytes", "kv_save", "kv_load",
+    "prefill_destroy", "prefill_last_error", "prefill_prune_predicate", "prefill_kv_header_check",
+    "prefill_kv_image_bytes_for",
+    "pfop_linear_f32", "pfop_linear_resid", "pfop_linear_glu", "pfop_linear_ple", "pfop_linear_qkv",
+    "pfop_attention", "pfop_rmsnorm", "pfop_embed", "pfop_kv_copy", "pfop_last_error",
+)
+
+
+class PrefillError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"status {code}: {msg}")
+        self.code = code
+
+
+class ModelDesc(C.Structure):
+    _fields_ = [
+        ("n_layer", C.c_int32), ("n_layer_kv_from_start", C.c_int32), ("d_model", C.c_int32),
+        ("n_head", C.c_int32), ("n_head_kv", C.c_int32), ("head_dim", C.c_int32),
+        ("ffn_dim", C.c_int32), ("vocab", C.c_int32), ("ple_dim", C.c_int32),
+        ("ffn_kind", C.c_int32), ("wtype", C.c_int32), ("rms_eps", C.c_float),
+        ("rope_base", C.c_float), ("kv_src", C.POINTER(C.c_int32)), ("max_ctx", C.c_int32),
+        ("ubatch_max", C.c_int32), ("prune_shared_enable", C.c_int32), ("n_seq_max", C.c_int32),
+        ("embeddings", C.c_int32),
+    ]
+
+
+class LayerWeights(C.Structure):
+    _fields_ = [(k, C.c_void_p) for k in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate",
+                                          "w_up", "w_down", "ple_gate", "ple_proj")]
+
+
+class Weights(C.Structure):
+    _fields_ = [("tok_embd", C.c_void_p), ("ple_embd", C.c_void_p), ("out_norm", C.c_void_p),
+                ("layers", C.POINTER(LayerWeights))]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> C.CDLL:
+    """Load the library (building it first if the sources are newer)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path) or os.environ.get("PREFILL_REBUILD"):
+        from . import build as _b
+        _b.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not found: {path}")
+    lib = C.CDLL(path)
+    vp, i32, i64, f32, sz = C.c_void_p, C.c_int32, C.c_int64, C.c_float, C.c_size_t
+    sig = {
+        "prefill_create": (C.c_int, [C.POINTER(ModelDesc), C.POINTER(Weights), vp, C.POINTER(vp)]),
+        "prefill_ubatch": (C.c_int, [vp, vp, i32, i64, i32, vp]),
+        "prefill_sync": (C.c_int, [vp]),
+        "prefill_n_pos": (i64, [vp]),
+        "prefill_reset": (C.c_int, [vp]),
+        "prefill_set_prune": (C.c_int, [vp, i32]),
+        "prefill_prune_active": (C.c_int, [vp]),
+        "prefill_kv_image_bytes": (i64, [vp, i64]),
+        "kv_save": (C.c_int, [vp, vp, sz]),
+        "kv_load": (C.c_int, [vp, vp, sz, i64]),
+        "prefill_destroy": (None, [vp]),
+        "prefill_last_error": (C.c_char_p, [vp]),
+        "prefill_prune_predicate": (C.c_int, [C.POINTER(ModelDesc)]),
+        "prefill_kv_header_check": (C.c_int, [vp, i32, i32, i64, i64, sz]),
+        "prefill_kv_image_bytes_for": (i64, [i32, i64, i32]),
+        "pfop_linear_f32": (C.c_int, [i32, vp, i32, i32, i32, vp, i32, i32, vp, vp]),
+        "pfop_linear_resid": (C.c_int, [i32, vp, i32, i32, vp, i32, i32, vp, vp, vp]),
+        "pfop_linear_glu": (C.c_int, [i32, vp, vp, i32, i32, i32, vp, i32, i32, vp, vp]),
+        "pfop_linear_ple": (C.c_int, [i32, vp, i32, i32, vp, i32, i32, vp, i32, vp, vp]),
+        "pfop_linear_qkv": (C.c_int, [i32, vp, vp, vp, i32, i32, i32, i32, f32, vp, i32, i32, i32, i32,
+                                      vp, vp, vp, vp]),
+        "pfop_attention": (C.c_int, [i32, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]),
+        "pfop_rmsnorm": (C.c_int, [vp, i32, i32, i32, vp, f32, vp, vp, vp]),
+        "pfop_embed": (C.c_int, [i32, vp, vp, i32, i32, i32, f32, vp, i32, vp, vp, vp]),
+        "pfop_kv_copy": (C.c_int, [i32, vp, i64, vp, i64, i32, i64, vp, vp]),
+        "pfop_last_error": (C.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(a) -> int | None:
+    """Address of a numpy array, a torch tensor or an int; None stays None."""
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    if isinstance(a, np.ndarray):
+        return a.ctypes.data
+    return a.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def check_op(rc: int):
+    if rc != PF_OK:
+        raise PrefillError(rc, load().pfop_last_error().decode())
+
+
+# ---------------------------------------------------------------------------
+# model description from a config dict
+
+
+def make_desc(cfg: dict, max_ctx: int, ubatch_max: int, prune: bool = True, n_seq_max: int = 1,
+              embeddings: bool = False):
+    kv_src = (C.c_int32 * cfg["n_layer"])(*cfg["kv_src"])
+    d = ModelDesc(
+        n_layer=cfg["n_layer"], n_layer_kv_from_start=cfg["n_layer_kv_from_start"],
+        d_model=cfg["d_model"], n_head=cfg["n_head"], n_head_kv=cfg["n_head_kv"],
+        head_dim=cfg["head_dim"], ffn_dim=cfg["ffn_dim"], vocab=cfg["vocab"],
+        ple_dim=cfg["ple_dim"], ffn_kind=PF_FFN_GEGLU if cfg["ffn"] == "geglu" else PF_FFN_SWIGLU,
+        wtype=PF_W_Q4_0 if cfg["wtype"] == "q4_0" else PF_W_F32, rms_eps=cfg["rms_eps"],
+        rope_base=cfg["rope_base"], kv_src=C.cast(kv_src, C.POINTER(C.c_int32)), max_ctx=max_ctx,
+        ubatch_max=ubatch_max, prune_shared_enable=1 if prune else 0, n_seq_max=n_seq_max,
+        embeddings=1 if embeddings else 0)
+    d._keep = kv_src
+    return d
+
+
+def prune_predicate(cfg: dict, prune: bool = True, n_seq_max: int = 1, embeddings: bool = False) -> bool:
+    d = make_desc(cfg, 16, 16, prune, n_seq_max, embeddings)
+    rc = load().prefill_prune_predicate(C.byref(d))
+    if rc < 0:
+        raise PrefillError(rc, "bad description")
+    return bool(rc)
+
+
+def kv_image_bytes_for(n_layers_written: int, n_pos: int, kv_dim: int) -> int:
+    return int(load().prefill_kv_image_bytes_for(n_layers_written, n_pos, kv_dim))
+
+
+def kv_header_check(header: bytes, n_layers_written: int, kv_dim: int, n_pos: int, max_ctx: int,
+                    image_bytes: int) -> int:
+    buf = (C.c_uint8 * 16).from_buffer_copy(header[:16].ljust(16, b"\0"))
+    return int(load().prefill_kv_header_check(buf, n_layers_written, kv_dim, n_pos, max_ctx, image_bytes))
+
+
+# ---------------------------------------------------------------------------
+# a prefill context
+
+
+class PrefillContext:
+    """One sequence on the current CUDA device (see prefill.h)."""
+
+    def __init__(self, weights, max_ctx: int, ubatch_max: int, prune: bool = True, stream=None,
+                 n_seq_max: int = 1, embeddings: bool = False):
+        lib = load()
+        cfg = weights.cfg
+        self.cfg = cfg
+        self._desc = make_desc(cfg, max_ctx, ubatch_max, prune, n_seq_max, embeddings)
+        keep = []
+
+        def p(a):
+            if a is None:
+                return None
+            a = np.ascontiguousarray(a)
+            keep.append(a)
+            return a.ctypes.data
+
+        layers = (LayerWeights * cfg["n_layer"])()
+        for il, lw in enumerate(weights.layers):
+            for k in LayerWeights._fields_:
+                setattr(layers[il], k[0], p(lw[k[0]]))
+        w = Weights(tok_embd=p(weights.tok_embd), ple_embd=p(weights.ple_embd),
+                    out_norm=p(weights.out_norm), layers=C.cast(layers, C.POINTER(LayerWeights)))
+        h = C.c_void_p()
+        rc = lib.prefill_create(C.byref(self._desc), C.byref(w), _stream(stream), C.byref(h))
+        if rc != PF_OK:
+            raise PrefillError(rc, lib.prefill_last_error(None).decode())
+        self._h = h
+        self._lib = lib
+        self.vocab = cfg["vocab"]
+
+    def _check(self, rc):
+        if rc != PF_OK:
+            raise PrefillError(rc, self._lib.prefill_last_error(self._h).decode())
+
+    def ubatch(self, tokens, pos0: int, is_last: bool, logits=None):
+        """tokens: numpy int32 (host) or an int32 device tensor; logits: fp32
+        device tensor [vocab] (needed when is_last)."""
+        if isinstance(tokens, np.ndarray):
+            tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+            n = len(tokens)
+        else:
+            n = tokens.numel()
+        self._check(self._lib.prefill_ubatch(self._h, _ptr(tokens), n, pos0, 1 if is_last else 0,
+                                             _ptr(logits)))
+
+    def sync(self):
+        self._check(self._lib.prefill_sync(self._h))
+
+    def reset(self):
+        self._check(self._lib.prefill_reset(self._h))
+
+    @property
+    def n_pos(self) -> int:
+        return int(self._lib.prefill_n_pos(self._h))
+
+    def set_prune(self, enable: bool):
+        self._check(self._lib.prefill_set_prune(self._h, 1 if enable else 0))
+
+    @property
+    def prune_active(self) -> bool:
+        return bool(self._lib.prefill_prune_active(self._h))
+
+    def kv_image_bytes(self, n_pos: int) -> int:
+        return int(self._lib.prefill_kv_image_bytes(self._h, n_pos))
+
+    def kv_save(self, dst, nbytes: int):
+        self._check(self._lib.kv_save(self._h, _ptr(dst), nbytes))
+
+    def kv_load(self, src, nbytes: int, n_pos: int):
+        self._check(self._lib.kv_load(self._h, _ptr(src), nbytes, n_pos))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.prefill_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,130 @@
+// Host-side declarations of the CUDA kernels' launchers and the data layouts
+// they share with the runtime.  Internal to the library (not part of the
+// C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+namespace pf {
+
+// ---------------------------------------------------------------------------
+// GEMM: out = A[M, K] (bf16, row-major) x W[N, K]^T, fused epilogues
+
+enum WKind : int { W_BF16 = 0, W_Q4 = 1 };
+
+enum EpiKind : int {
+  EPI_F32 = 0,    // out_f32[m, n] = acc
+  EPI_RESID = 1,  // out_f32[m, n] += acc; if out_bf16: out_bf16[m, n] = bf16(new value)
+  EPI_GLU = 2,    // W rows interleaved per tile (gate half, up half):
+                  //   out_bf16[m, f] = act(gate) * up
+  EPI_QKV = 3,    // columns [0,q) Q, [q,q+kv) K, [q+kv,q+2kv) V; RoPE on Q and K;
+                  //   Q -> q_out fp16 [m][q], K/V -> fp16 cache rows at pos0+m
+  EPI_PLE = 4,    // out_bf16[m, n] = bf16(gelu_tanh(acc) * ple[m*ple_stride + n])
+};
+
+struct EpiParams {
+  int kind = EPI_F32;
+  int N = 0;  // logical output columns (GLU: ffn dim)
+  float* out_f32 = nullptr;
+  int ld_f32 = 0;
+  __nv_bfloat16* out_bf16 = nullptr;
+  int ld_bf16 = 0;
+  const __nv_bfloat16* ple = nullptr;
+  int ple_stride = 0;
+  int act = 0;  // GLU: 0 = gelu_tanh, 1 = silu
+  __half* q_out = nullptr;
+  __half* k_cache = nullptr;  // row p = position p, kv_dim halves per row
+  __half* v_cache = nullptr;
+  int q_dim = 0, kv_dim = 0, head_dim = 0;
+  int pos0 = 0;                  // position of GEMM row 0
+  const float2* rope = nullptr;  // [position][head_dim/2] = (cos, sin)
+};
+
+// A weight matrix in device memory, in the GEMM's tile order.
+//  W_BF16: bf16 [N_rows][K] row-major (rows already in tile order), TMA-read.
+//  W_Q4:   tiles (n-tile t, k-block kb) at byte (t*nkb + kb) * BN*36:
+//          [half h][row r] 16 nibble bytes, then [half h][row r] fp16 scales,
+//          where half h is the Q4_0 block of k in [64kb+32h, 64kb+32h+32).
+struct WeightMat {
+  int kind = W_Q4;
+  int N_rows = 0;  // stored rows (multiple of BN)
+  int K = 0;
+  int BN = 128;
+  void* dev = nullptr;
+  size_t bytes = 0;
+  alignas(64) CUtensorMap tmap;
+};
+
+// A bf16 activation matrix used as the GEMM's A operand.
+struct ActMat {
+  const __nv_bfloat16* dev = nullptr;
+  int rows = 0, K = 0;
+  alignas(64) CUtensorMap tmap;
+};
+
+bool make_act_map(ActMat& a, std::string* err);
+bool make_weight_map(WeightMat& w, std::string* err);
+
+cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err_word,
+                        cudaStream_t s);
+
+// Host repack.  `rows[i]` points at the i-th stored row's source (Q4_0: K/32
+// blocks of 18 bytes; F32: K floats) or is null for a zero padding row.
+std::vector<uint8_t> repack_q4_tiles(const std::vector<const uint8_t*>& rows, int K, int BN);
+std::vector<uint16_t> repack_bf16_rows(const std::vector<const float*>& rows, int K);
+
+// ---------------------------------------------------------------------------
+// attention (fp16 Q and KV cache, fp32 accumulation, 64-key chunks)
+
+struct AttnArgs {
+  const __half* q = nullptr;  // [M][Hq*hd]
+  const __half* k = nullptr;  // [position][Hkv*hd]
+  const __half* v = nullptr;
+  __nv_bfloat16* out = nullptr;  // [M][Hq*hd]
+  int M = 0, Hq = 0, Hkv = 0, hd = 0;
+  int pos_base = 0;  // position of row 0
+  int kv_len = 0;    // keys [0, kv_len) exist in the cache
+};
+
+// every row folds its chunks in ascending order inside one CTA
+cudaError_t launch_attn_prefill(const AttnArgs& a, cudaStream_t s);
+// one row (M == 1): chunk partials in parallel, then an ordered merge
+cudaError_t launch_attn_split(const AttnArgs& a, float* partials, cudaStream_t s);
+size_t attn_partials_floats(int Hq, int hd, int max_ctx);
+
+// ---------------------------------------------------------------------------
+// per-row kernels
+
+struct EmbedArgs {
+  const int32_t* tok = nullptr;
+  int T = 0, vocab = 0, D = 0;
+  int wq4 = 1;
+  const void* tok_table = nullptr;  // Q4_0 rows [V][D/32][18] or f32 [V][D]
+  float* x = nullptr;               // [T][D]
+  const void* ple_table = nullptr;  // Q4_0 rows [V][LP/32][18] or f32 [V][LP] (null: none)
+  int LP = 0;
+  float ple_scale = 1.0f;
+  __nv_bfloat16* ple = nullptr;  // [T][LP]
+  int* err = nullptr;
+};
+cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t s);
+
+// y[i] = rmsnorm(x[row0 + i]) * (1 + g) for i < M; optionally x_copy[i] = x[row0 + i]
+cudaError_t launch_rmsnorm(const float* x, int row0, int M, int D, const float* g, float eps,
+                           __nv_bfloat16* y, float* x_copy, cudaStream_t s);
+
+// KV image body <-> cache.  n_seg segments (keys of each writing layer, then
+// values); each copies copy_bytes, from/to the cache at seg * cache_seg_stride
+// halves and the image body (16 bytes after `image`) at seg * img_seg_bytes.
+// dir 0: cache -> image (also writes the 16-byte header), dir 1: image -> cache.
+cudaError_t launch_kv_copy(int dir, __half* cache, int64_t cache_seg_stride, uint8_t* image, int64_t img_seg_bytes,
+                           int n_seg, int64_t copy_bytes, const int32_t header[4], cudaStream_t s);
+
+}  // namespace pf

@@ -1,0 +1,646 @@
+// Runtime behind the C ABI (include/prefill.h): context creation (weight
+// repack and upload, KV cache and activation buffers), the ubatch schedule
+// with the pruning decision, and the KV image save/restore.
+//
+// The pruning follows the Gemma 4 prefill change (devotd.net llama.cpp Gemma 4
+// prefill news, section 1 and its listing): when 0 < n_layer_kv_from_start <
+// n_layer, one sequence, no embeddings output, the rows no output needs are
+// dropped before the first KV-shared layer; an intermediate ubatch ends there
+// and the final ubatch carries its last row only.  The KV image follows the
+// PicoLM KV cache article ("file" and "rules" paragraphs).
+#include "../../include/prefill.h"
+#include "common.cuh"
+#include "kernels.h"
+
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <memory>
+#include <string>
+#include <vector>
+
+using namespace pf;
+
+namespace {
+
+struct DevBuf {
+  void* p = nullptr;
+  size_t bytes = 0;
+};
+
+struct LayerW {
+  WeightMat qkv;  // writing layers: [Wq; Wk; Wv]; KV-shared layers: Wq
+  WeightMat o, gu, down, pg, pp;
+  float* attn_norm = nullptr;
+  float* ffn_norm = nullptr;
+};
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+}  // namespace
+
+struct prefill_ctx {
+  prefill_model_desc d{};
+  std::vector<int32_t> kv_src;
+  int L = 0, S = 0, L_w = 0, D = 0, Hq = 0, Hkv = 0, hd = 0, q = 0, kv = 0, F = 0, V = 0, P = 0;
+  int rows_alloc = 0;
+  cudaStream_t stream = nullptr;
+  int device = 0;
+  std::vector<void*> allocs;
+
+  std::vector<LayerW> layers;
+  WeightMat head;
+  const void* tok_table = nullptr;  // gather copy (original Q4_0 rows or fp32)
+  const void* ple_table = nullptr;
+  float* out_norm = nullptr;
+
+  int32_t* tok = nullptr;
+  float* x = nullptr;
+  float* xr = nullptr;
+  __nv_bfloat16 *y = nullptr, *att = nullptr, *h = nullptr, *xb = nullptr, *pg = nullptr, *ple = nullptr;
+  __half* q16 = nullptr;
+  float* partials = nullptr;
+  __half* cache = nullptr;  // [2][L_w][max_ctx][kv]
+  float2* rope = nullptr;
+  int* err = nullptr;
+  ActMat a_y, a_att, a_h, a_xb, a_pg;
+
+  int64_t n_pos = 0;
+  int prune_enable = 1;
+  std::string last_error;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(prefill_ctx* c, int code, const std::string& msg) {
+  if (c)
+    c->last_error = msg;
+  else
+    g_last_error = msg;
+  return code;
+}
+
+int cuda_fail(prefill_ctx* c, cudaError_t e, const char* what) {
+  return fail(c, PF_E_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define PF_CUDA(ctx, call)                                    \
+  do {                                                        \
+    cudaError_t e_ = (call);                                  \
+    if (e_ != cudaSuccess) return cuda_fail(ctx, e_, #call); \
+  } while (0)
+
+template <class T>
+int dev_alloc(prefill_ctx* c, T** out, size_t bytes, bool zero = true) {
+  void* p = nullptr;
+  cudaError_t e = cudaMalloc(&p, bytes ? bytes : 16);
+  if (e != cudaSuccess) return fail(c, PF_E_NOMEM, std::string("cudaMalloc: ") + cudaGetErrorString(e));
+  c->allocs.push_back(p);
+  if (zero) {
+    e = cudaMemset(p, 0, bytes ? bytes : 16);
+    if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemset");
+  }
+  *out = static_cast<T*>(p);
+  return PF_OK;
+}
+
+template <class T>
+int upload(prefill_ctx* c, T** out, const void* host, size_t bytes) {
+  int rc = dev_alloc(c, out, bytes, false);
+  if (rc) return rc;
+  PF_CUDA(c, cudaMemcpy(*out, host, bytes, cudaMemcpyHostToDevice));
+  return PF_OK;
+}
+
+size_t row_bytes(int wtype, int K) { return wtype == PF_W_Q4_0 ? static_cast<size_t>(K / 32) * 18 : static_cast<size_t>(K) * 4; }
+
+// rows: sources of the stored rows in tile order (null = zero row)
+int build_weight(prefill_ctx* c, WeightMat& w, const std::vector<const void*>& rows, int K, int BN) {
+  w.K = K;
+  w.BN = BN;
+  w.N_rows = static_cast<int>(rows.size());
+  if (w.N_rows % BN != 0 || K % 64 != 0) return fail(c, PF_E_ARG, "weight shape not tileable");
+  std::string err;
+  if (c->d.wtype == PF_W_Q4_0) {
+    w.kind = W_Q4;
+    std::vector<const uint8_t*> r(rows.size());
+    for (size_t i = 0; i < rows.size(); ++i) r[i] = static_cast<const uint8_t*>(rows[i]);
+    std::vector<uint8_t> t = repack_q4_tiles(r, K, BN);
+    w.bytes = t.size();
+    int rc = upload(c, &w.dev, t.data(), t.size());
+    if (rc) return rc;
+  } else {
+    w.kind = W_BF16;
+    std::vector<const float*> r(rows.size());
+    for (size_t i = 0; i < rows.size(); ++i) r[i] = static_cast<const float*>(rows[i]);
+    std::vector<uint16_t> t = repack_bf16_rows(r, K);
+    w.bytes = t.size() * 2;
+    int rc = upload(c, &w.dev, t.data(), w.bytes);
+    if (rc) return rc;
+  }
+  if (!make_weight_map(w, &err)) return fail(c, PF_E_CUDA, err);
+  return PF_OK;
+}
+
+// plain matrix [N][K], rows in order, padded to BN
+std::vector<const void*> plain_rows(const void* m, int N, int K, int wtype, int BN) {
+  std::vector<const void*> r(round_up(N, BN), nullptr);
+  const uint8_t* b = static_cast<const uint8_t*>(m);
+  for (int n = 0; n < N; ++n) r[n] = b + n * row_bytes(wtype, K);
+  return r;
+}
+
+int check_desc(const prefill_model_desc* d, std::string* why) {
+  auto bad = [&](const char* m) {
+    *why = m;
+    return PF_E_ARG;
+  };
+  if (!d) return bad("null description");
+  if (d->n_layer < 1) return bad("n_layer < 1");
+  if (d->n_layer_kv_from_start < 0 || d->n_layer_kv_from_start > d->n_layer)
+    return bad("n_layer_kv_from_start outside [0, n_layer]");
+  if (d->n_layer_kv_from_start == 0) return bad("at least one layer must write the KV cache");
+  if (d->head_dim != 64 && d->head_dim != 256) return bad("head_dim must be 64 or 256");
+  if (d->n_head < 1 || d->n_head_kv < 1 || d->n_head % d->n_head_kv) return bad("n_head must be a multiple of n_head_kv");
+  const int G = d->n_head / d->n_head_kv;
+  if (G > 16 || 16 % G) return bad("n_head / n_head_kv must divide 16");
+  if (d->d_model < 64 || d->d_model % 64) return bad("d_model must be a multiple of 64");
+  if (d->ffn_dim < 64 || d->ffn_dim % 64) return bad("ffn_dim must be a multiple of 64");
+  if (d->ple_dim < 0 || d->ple_dim % 64) return bad("ple_dim must be 0 or a multiple of 64");
+  if (d->vocab < 1) return bad("vocab < 1");
+  if (d->ffn_kind != PF_FFN_GEGLU && d->ffn_kind != PF_FFN_SWIGLU) return bad("ffn_kind");
+  if (d->wtype != PF_W_F32 && d->wtype != PF_W_Q4_0) return bad("wtype");
+  if (d->max_ctx < 1 || d->ubatch_max < 1) return bad("max_ctx and ubatch_max must be >= 1");
+  if (!d->kv_src) return bad("kv_src is null");
+  for (int il = 0; il < d->n_layer; ++il) {
+    const int s = d->kv_src[il];
+    if (il < d->n_layer_kv_from_start) {
+      if (s != -1) return bad("kv_src of a writing layer must be -1");
+    } else if (s < 0 || s >= d->n_layer_kv_from_start) {
+      return bad("kv_src of a KV-shared layer must name a writing layer");
+    }
+  }
+  return PF_OK;
+}
+
+bool predicate(const prefill_model_desc& d, int enable) {
+  // the NextN crop is always allowed here (no multi-token-prediction head)
+  return enable && d.n_layer_kv_from_start > 0 && d.n_layer_kv_from_start < d.n_layer && !d.embeddings &&
+         d.n_seq_max == 1;
+}
+
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+int check_device_error(prefill_ctx* c) {
+  int e = 0;
+  PF_CUDA(c, cudaMemcpy(&e, c->err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (e == 0) return PF_OK;
+  PF_CUDA(c, cudaMemset(c->err, 0, sizeof(int)));
+  if (e == PF_DEV_BAD_TOKEN) return fail(c, PF_E_DEVICE_TOKEN, "a token id was outside [0, vocab)");
+  return fail(c, PF_E_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (code " + std::to_string(e) + ")");
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// create / destroy
+
+extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weights* w, void* stream,
+                              prefill_ctx** out) {
+  if (!out) return fail(nullptr, PF_E_ARG, "out is null");
+  *out = nullptr;
+  std::string why;
+  if (check_desc(desc, &why) != PF_OK) return fail(nullptr, PF_E_ARG, why);
+  if (!w || !w->tok_embd || !w->out_norm || !w->layers) return fail(nullptr, PF_E_ARG, "missing weights");
+  if (desc->ple_dim > 0 && !w->ple_embd) return fail(nullptr, PF_E_ARG, "missing ple_embd");
+
+  std::unique_ptr<prefill_ctx> c(new prefill_ctx());
+  prefill_ctx* C = c.get();
+  C->d = *desc;
+  C->kv_src.assign(desc->kv_src, desc->kv_src + desc->n_layer);
+  C->d.kv_src = C->kv_src.data();
+  C->L = desc->n_layer;
+  C->S = desc->n_layer_kv_from_start;
+  C->L_w = C->S;
+  C->D = desc->d_model;
+  C->Hq = desc->n_head;
+  C->Hkv = desc->n_head_kv;
+  C->hd = desc->head_dim;
+  C->q = C->Hq * C->hd;
+  C->kv = C->Hkv * C->hd;
+  C->F = desc->ffn_dim;
+  C->V = desc->vocab;
+  C->P = desc->ple_dim;
+  C->stream = static_cast<cudaStream_t>(stream);
+  C->prune_enable = desc->prune_shared_enable ? 1 : 0;
+  C->rows_alloc = round_up(desc->ubatch_max, 128);
+  cudaGetDevice(&C->device);
+  const int wt = desc->wtype;
+  int rc;
+
+  // layers
+  C->layers.resize(C->L);
+  for (int il = 0; il < C->L; ++il) {
+    const prefill_layer_weights& lw = w->layers[il];
+    LayerW& L = C->layers[il];
+    const bool writes = il < C->S;
+    if (!lw.attn_norm || !lw.wq || !lw.wo || !lw.ffn_norm || !lw.w_gate || !lw.w_up || !lw.w_down)
+      return fail(nullptr, PF_E_ARG, "missing layer weight");
+    if (writes && (!lw.wk || !lw.wv)) return fail(nullptr, PF_E_ARG, "writing layer without wk/wv");
+    if (C->P > 0 && (!lw.ple_gate || !lw.ple_proj)) return fail(nullptr, PF_E_ARG, "missing ple_gate/ple_proj");
+    // QKV (or Q): one tile holds whole heads so RoPE pairs stay in the tile
+    const int bn_qkv = C->hd > 128 ? 256 : 128;
+    {
+      const size_t rb = row_bytes(wt, C->D);
+      std::vector<const void*> rows;
+      for (int n = 0; n < C->q; ++n) rows.push_back(static_cast<const uint8_t*>(lw.wq) + n * rb);
+      if (writes) {
+        for (int n = 0; n < C->kv; ++n) rows.push_back(static_cast<const uint8_t*>(lw.wk) + n * rb);
+        for (int n = 0; n < C->kv; ++n) rows.push_back(static_cast<const uint8_t*>(lw.wv) + n * rb);
+      }
+      rows.resize(round_up(static_cast<int>(rows.size()), bn_qkv), nullptr);
+      if ((rc = build_weight(C, L.qkv, rows, C->D, bn_qkv))) return fail(nullptr, rc, C->last_error);
+    }
+    if ((rc = build_weight(C, L.o, plain_rows(lw.wo, C->D, C->q, wt, 128), C->q, 128)))
+      return fail(nullptr, rc, C->last_error);
+    {
+      // gate/up interleaved per 128-row tile: 64 gate rows, then the same 64 up rows
+      const size_t rb = row_bytes(wt, C->D);
+      std::vector<const void*> rows;
+      for (int t = 0; t < C->F / 64; ++t) {
+        for (int i = 0; i < 64; ++i) rows.push_back(static_cast<const uint8_t*>(lw.w_gate) + (t * 64 + i) * rb);
+        for (int i = 0; i < 64; ++i) rows.push_back(static_cast<const uint8_t*>(lw.w_up) + (t * 64 + i) * rb);
+      }
+      if ((rc = build_weight(C, L.gu, rows, C->D, 128))) return fail(nullptr, rc, C->last_error);
+    }
+    if ((rc = build_weight(C, L.down, plain_rows(lw.w_down, C->D, C->F, wt, 128), C->F, 128)))
+      return fail(nullptr, rc, C->last_error);
+    if (C->P > 0) {
+      if ((rc = build_weight(C, L.pg, plain_rows(lw.ple_gate, C->P, C->D, wt, 128), C->D, 128)))
+        return fail(nullptr, rc, C->last_error);
+      if ((rc = build_weight(C, L.pp, plain_rows(lw.ple_proj, C->D, C->P, wt, 128), C->P, 128)))
+        return fail(nullptr, rc, C->last_error);
+    }
+    if ((rc = upload(C, &L.attn_norm, lw.attn_norm, C->D * 4))) return fail(nullptr, rc, C->last_error);
+    if ((rc = upload(C, &L.ffn_norm, lw.ffn_norm, C->D * 4))) return fail(nullptr, rc, C->last_error);
+  }
+  // head (tied embedding), gather tables, final norm
+  if ((rc = build_weight(C, C->head, plain_rows(w->tok_embd, C->V, C->D, wt, 128), C->D, 128)))
+    return fail(nullptr, rc, C->last_error);
+  {
+    void* p = nullptr;
+    if ((rc = upload(C, &p, w->tok_embd, static_cast<size_t>(C->V) * row_bytes(wt, C->D))))
+      return fail(nullptr, rc, C->last_error);
+    C->tok_table = p;
+    if (C->P > 0) {
+      if ((rc = upload(C, &p, w->ple_embd, static_cast<size_t>(C->V) * row_bytes(wt, C->L * C->P))))
+        return fail(nullptr, rc, C->last_error);
+      C->ple_table = p;
+    }
+    if ((rc = upload(C, &C->out_norm, w->out_norm, C->D * 4))) return fail(nullptr, rc, C->last_error);
+  }
+
+  // buffers
+  const size_t R = C->rows_alloc;
+  if ((rc = dev_alloc(C, &C->tok, R * 4)) || (rc = dev_alloc(C, &C->x, R * C->D * 4)) ||
+      (rc = dev_alloc(C, &C->xr, 128 * C->D * 4)) || (rc = dev_alloc(C, &C->y, R * C->D * 2)) ||
+      (rc = dev_alloc(C, &C->att, R * C->q * 2)) || (rc = dev_alloc(C, &C->h, R * C->F * 2)) ||
+      (rc = dev_alloc(C, &C->xb, R * C->D * 2)) || (rc = dev_alloc(C, &C->q16, R * C->q * 2)) ||
+      (rc = dev_alloc(C, &C->err, 16)))
+    return fail(nullptr, rc, C->last_error);
+  if (C->P > 0) {
+    if ((rc = dev_alloc(C, &C->pg, R * C->P * 2)) || (rc = dev_alloc(C, &C->ple, R * C->L * C->P * 2)))
+      return fail(nullptr, rc, C->last_error);
+  }
+  if ((rc = dev_alloc(C, &C->partials, attn_partials_floats(C->Hq, C->hd, C->d.max_ctx) * 4)))
+    return fail(nullptr, rc, C->last_error);
+  if ((rc = dev_alloc(C, &C->cache, static_cast<size_t>(2) * C->L_w * C->d.max_ctx * C->kv * 2)))
+    return fail(nullptr, rc, C->last_error);
+  {
+    // RoPE table: angle pos * base^(-2i/hd) in double, cos/sin rounded to fp32
+    const int half = C->hd / 2;
+    std::vector<float2> tab(static_cast<size_t>(C->d.max_ctx) * half);
+    for (int p = 0; p < C->d.max_ctx; ++p)
+      for (int i = 0; i < half; ++i) {
+        const double th = static_cast<double>(p) * std::pow(static_cast<double>(C->d.rope_base), -2.0 * i / C->hd);
+        tab[static_cast<size_t>(p) * half + i] = make_float2(static_cast<float>(std::cos(th)), static_cast<float>(std::sin(th)));
+      }
+    if ((rc = upload(C, &C->rope, tab.data(), tab.size() * sizeof(float2)))) return fail(nullptr, rc, C->last_error);
+  }
+  std::string err;
+  auto mk = [&](ActMat& a, const __nv_bfloat16* p, int K) {
+    a.dev = p;
+    a.rows = C->rows_alloc;
+    a.K = K;
+    return make_act_map(a, &err);
+  };
+  if (!mk(C->a_y, C->y, C->D) || !mk(C->a_att, C->att, C->q) || !mk(C->a_h, C->h, C->F) ||
+      !mk(C->a_xb, C->xb, C->D) || (C->P > 0 && !mk(C->a_pg, C->pg, C->P)))
+    return fail(nullptr, PF_E_CUDA, err);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "create");
+  *out = c.release();
+  return PF_OK;
+}
+
+extern "C" void prefill_destroy(prefill_ctx* c) {
+  if (!c) return;
+  cudaStreamSynchronize(c->stream);
+  for (void* p : c->allocs) cudaFree(p);
+  delete c;
+}
+
+extern "C" const char* prefill_last_error(const prefill_ctx* c) {
+  return c ? c->last_error.c_str() : g_last_error.c_str();
+}
+
+// ---------------------------------------------------------------------------
+// the ubatch
+
+extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, int64_t pos0, int32_t is_last,
+                              float* logits) {
+  if (!c) return fail(nullptr, PF_E_ARG, "null context");
+  if (!tokens || T < 1 || T > c->d.ubatch_max) return fail(c, PF_E_ARG, "n_tokens outside [1, ubatch_max]");
+  if (pos0 != c->n_pos) return fail(c, PF_E_ARG, "pos0 must equal the cached position count");
+  if (pos0 + T > c->d.max_ctx) return fail(c, PF_E_ARG, "positions would exceed max_ctx");
+  if (is_last && !logits) return fail(c, PF_E_ARG, "logits is null on the last ubatch");
+  cudaStream_t s = c->stream;
+  if (is_device_ptr(tokens)) {
+    PF_CUDA(c, cudaMemcpyAsync(c->tok, tokens, T * 4, cudaMemcpyDeviceToDevice, s));
+  } else {
+    for (int i = 0; i < T; ++i)
+      if (tokens[i] < 0 || tokens[i] >= c->V) return fail(c, PF_E_ARG, "token id outside [0, vocab)");
+    PF_CUDA(c, cudaMemcpyAsync(c->tok, tokens, T * 4, cudaMemcpyHostToDevice, s));
+  }
+
+  const bool prune = predicate(c->d, c->prune_enable);
+  const int L = c->L, S = c->S, D = c->D, LP = L * c->P;
+  const int kv_len = static_cast<int>(pos0) + T;
+  const size_t seg = static_cast<size_t>(c->d.max_ctx) * c->kv;
+
+  EmbedArgs ea;
+  ea.tok = c->tok;
+  ea.T = T;
+  ea.vocab = c->V;
+  ea.D = D;
+  ea.wq4 = c->d.wtype == PF_W_Q4_0;
+  ea.tok_table = c->tok_table;
+  ea.x = c->x;
+  ea.ple_table = c->P > 0 ? c->ple_table : nullptr;
+  ea.LP = LP;
+  ea.ple_scale = c->P > 0 ? static_cast<float>(1.0 / std::sqrt(static_cast<double>(c->P))) : 1.0f;
+  ea.ple = c->ple;
+  ea.err = c->err;
+  PF_CUDA(c, launch_embed(ea, s));
+
+  float* xcur = c->x;
+  int M = T;
+  int pos_base = static_cast<int>(pos0);
+  const __nv_bfloat16* ple_view = c->ple;
+  bool gathered = false;
+  bool stopped = false;
+
+  for (int il = 0; il < L; ++il) {
+    const LayerW& W = c->layers[il];
+    if (prune && il == S) {
+      if (!is_last) {
+        stopped = true;
+        break;
+      }
+      // keep the output row only: gather it inside the norm
+      PF_CUDA(c, launch_rmsnorm(c->x, T - 1, 1, D, W.attn_norm, c->d.rms_eps, c->y, c->xr, s));
+      xcur = c->xr;
+      M = 1;
+      pos_base = static_cast<int>(pos0) + T - 1;
+      ple_view = c->ple + static_cast<size_t>(T - 1) * LP;
+      gathered = true;
+    } else {
+      PF_CUDA(c, launch_rmsnorm(xcur, 0, M, D, W.attn_norm, c->d.rms_eps, c->y, nullptr, s));
+    }
+    const bool writes = il < S;
+    const int src = writes ? il : c->kv_src[il];
+    {
+      EpiParams e;
+      e.kind = EPI_QKV;
+      e.q_out = c->q16;
+      e.q_dim = c->q;
+      e.kv_dim = writes ? c->kv : 0;
+      e.head_dim = c->hd;
+      e.pos0 = pos_base;
+      e.rope = c->rope;
+      e.k_cache = c->cache + static_cast<size_t>(il) * seg;
+      e.v_cache = c->cache + static_cast<size_t>(c->L_w + il) * seg;
+      PF_CUDA(c, launch_gemm(c->a_y, M, W.qkv, e, c->err, s));
+    }
+    {
+      AttnArgs a;
+      a.q = c->q16;
+      a.k = c->cache + static_cast<size_t>(src) * seg;
+      a.v = c->cache + static_cast<size_t>(c->L_w + src) * seg;
+      a.out = c->att;
+      a.M = M;
+      a.Hq = c->Hq;
+      a.Hkv = c->Hkv;
+      a.hd = c->hd;
+      a.pos_base = pos_base;
+      a.kv_len = kv_len;
+      if (gathered)
+        PF_CUDA(c, launch_attn_split(a, c->partials, s));
+      else
+        PF_CUDA(c, launch_attn_prefill(a, s));
+    }
+    {
+      EpiParams e;
+      e.kind = EPI_RESID;
+      e.N = D;
+      e.out_f32 = xcur;
+      e.ld_f32 = D;
+      PF_CUDA(c, launch_gemm(c->a_att, M, W.o, e, c->err, s));
+    }
+    PF_CUDA(c, launch_rmsnorm(xcur, 0, M, D, W.ffn_norm, c->d.rms_eps, c->y, nullptr, s));
+    {
+      EpiParams e;
+      e.kind = EPI_GLU;
+      e.N = c->F;
+      e.out_bf16 = c->h;
+      e.ld_bf16 = c->F;
+      e.act = c->d.ffn_kind == PF_FFN_GEGLU ? 0 : 1;
+      PF_CUDA(c, launch_gemm(c->a_y, M, W.gu, e, c->err, s));
+    }
+    {
+      EpiParams e;
+      e.kind = EPI_RESID;
+      e.N = D;
+      e.out_f32 = xcur;
+      e.ld_f32 = D;
+      if (c->P > 0) {
+        e.out_bf16 = c->xb;
+        e.ld_bf16 = D;
+      }
+      PF_CUDA(c, launch_gemm(c->a_h, M, W.down, e, c->err, s));
+    }
+    if (c->P > 0) {
+      EpiParams e;
+      e.kind = EPI_PLE;
+      e.N = c->P;
+      e.out_bf16 = c->pg;
+      e.ld_bf16 = c->P;
+      e.ple = ple_view + static_cast<size_t>(il) * c->P;
+      e.ple_stride = LP;
+      PF_CUDA(c, launch_gemm(c->a_xb, M, W.pg, e, c->err, s));
+      EpiParams r;
+      r.kind = EPI_RESID;
+      r.N = D;
+      r.out_f32 = xcur;
+      r.ld_f32 = D;
+      PF_CUDA(c, launch_gemm(c->a_pg, M, W.pp, r, c->err, s));
+    }
+  }
+  (void)stopped;
+  if (is_last) {
+    const int row = gathered ? 0 : T - 1;
+    PF_CUDA(c, launch_rmsnorm(xcur, row, 1, D, c->out_norm, c->d.rms_eps, c->y, nullptr, s));
+    EpiParams e;
+    e.kind = EPI_F32;
+    e.N = c->V;
+    e.out_f32 = logits;
+    e.ld_f32 = c->V;
+    PF_CUDA(c, launch_gemm(c->a_y, 1, c->head, e, c->err, s));
+  }
+  c->n_pos = kv_len;
+  return PF_OK;
+}
+
+extern "C" int prefill_sync(prefill_ctx* c) {
+  if (!c) return fail(nullptr, PF_E_ARG, "null context");
+  PF_CUDA(c, cudaStreamSynchronize(c->stream));
+  return check_device_error(c);
+}
+
+extern "C" int64_t prefill_n_pos(const prefill_ctx* c) { return c ? c->n_pos : -1; }
+
+extern "C" int prefill_reset(prefill_ctx* c) {
+  if (!c) return fail(nullptr, PF_E_ARG, "null context");
+  c->n_pos = 0;
+  return PF_OK;
+}
+
+extern "C" int prefill_set_prune(prefill_ctx* c, int32_t enable) {
+  if (!c) return fail(nullptr, PF_E_ARG, "null context");
+  c->prune_enable = enable ? 1 : 0;
+  return PF_OK;
+}
+
+extern "C" int prefill_prune_active(const prefill_ctx* c) { return c ? (predicate(c->d, c->prune_enable) ? 1 : 0) : 0; }
+
+// ---------------------------------------------------------------------------
+// KV image
+
+extern "C" int64_t prefill_kv_image_bytes_for(int32_t n_layers_written, int64_t n_pos, int32_t kv_dim) {
+  if (n_layers_written < 0 || n_pos < 0 || kv_dim < 0) return -1;
+  return 16 + 2 * static_cast<int64_t>(n_layers_written) * n_pos * kv_dim * 2;
+}
+
+extern "C" int64_t prefill_kv_image_bytes(const prefill_ctx* c, int64_t n_pos) {
+  if (!c) return -1;
+  return prefill_kv_image_bytes_for(c->L_w, n_pos, c->kv);
+}
+
+extern "C" int prefill_kv_header_check(const void* header16, int32_t n_layers_written, int32_t kv_dim, int64_t n_pos,
+                                       int64_t max_ctx, size_t image_bytes) {
+  if (!header16 || image_bytes < 16) return PF_E_KV_MAGIC;
+  const uint8_t* h = static_cast<const uint8_t*>(header16);
+  if (std::memcmp(h, "KVCP", 4) != 0) return PF_E_KV_MAGIC;
+  int32_t f[3];
+  for (int i = 0; i < 3; ++i)
+    f[i] = static_cast<int32_t>(static_cast<uint32_t>(h[4 + 4 * i]) | (static_cast<uint32_t>(h[5 + 4 * i]) << 8) |
+                                (static_cast<uint32_t>(h[6 + 4 * i]) << 16) | (static_cast<uint32_t>(h[7 + 4 * i]) << 24));
+  const int32_t n_img = f[0], l_img = f[1], kv_img = f[2];
+  if (l_img != n_layers_written || kv_img != kv_dim) return PF_E_KV_SHAPE;
+  if (n_img < 0 || n_pos < 0 || n_pos > n_img || n_pos > max_ctx) return PF_E_KV_RANGE;
+  if (static_cast<int64_t>(image_bytes) < prefill_kv_image_bytes_for(l_img, n_img, kv_img)) return PF_E_KV_RANGE;
+  return PF_OK;
+}
+
+extern "C" int kv_save(prefill_ctx* c, void* dst, size_t dst_bytes) {
+  if (!c || !dst) return fail(c, PF_E_ARG, "null argument");
+  const int64_t n = c->n_pos;
+  const int64_t need = prefill_kv_image_bytes(c, n);
+  if (static_cast<int64_t>(dst_bytes) < need) return fail(c, PF_E_ARG, "destination smaller than the image");
+  if (reinterpret_cast<uintptr_t>(dst) % 16 != 0) return fail(c, PF_E_ARG, "destination not 16-byte aligned");
+  int32_t h4[4];
+  std::memcpy(h4, "KVCP", 4);
+  h4[1] = static_cast<int32_t>(n);
+  h4[2] = c->L_w;
+  h4[3] = c->kv;
+  const size_t seg_bytes = static_cast<size_t>(n) * c->kv * 2;
+  const size_t cache_pitch = static_cast<size_t>(c->d.max_ctx) * c->kv * 2;
+  if (is_device_ptr(dst)) {
+    PF_CUDA(c, launch_kv_copy(0, c->cache, static_cast<int64_t>(c->d.max_ctx) * c->kv, static_cast<uint8_t*>(dst),
+                              static_cast<int64_t>(seg_bytes), 2 * c->L_w, static_cast<int64_t>(seg_bytes), h4,
+                              c->stream));
+  } else {
+    std::memcpy(dst, h4, 16);
+    if (seg_bytes > 0)
+      PF_CUDA(c, cudaMemcpy2DAsync(static_cast<uint8_t*>(dst) + 16, seg_bytes, c->cache, cache_pitch, seg_bytes,
+                                   2 * c->L_w, cudaMemcpyDeviceToHost, c->stream));
+    PF_CUDA(c, cudaStreamSynchronize(c->stream));
+  }
+  if (std::getenv("PREFILL_LOG")) std::fprintf(stderr, "KV cache saved: %lld positions\n", (long long)n);
+  return PF_OK;
+}
+
+extern "C" int kv_load(prefill_ctx* c, const void* src, size_t src_bytes, int64_t n_pos) {
+  if (!c || !src) return fail(c, PF_E_ARG, "null argument");
+  const bool dev = is_device_ptr(src);
+  uint8_t hdr[16] = {0};
+  if (src_bytes >= 16) {
+    if (dev) {
+      PF_CUDA(c, cudaStreamSynchronize(c->stream));
+      PF_CUDA(c, cudaMemcpy(hdr, src, 16, cudaMemcpyDeviceToHost));
+    } else {
+      std::memcpy(hdr, src, 16);
+    }
+  }
+  const int rc = prefill_kv_header_check(hdr, c->L_w, c->kv, n_pos, c->d.max_ctx, src_bytes);
+  if (rc == PF_E_KV_MAGIC) return fail(c, rc, "not a KV image (magic)");
+  if (rc == PF_E_KV_SHAPE) return fail(c, rc, "KV image layers or kv_dim do not match the model");
+  if (rc != PF_OK) return fail(c, rc, "KV image position count out of range");
+  if (dev && reinterpret_cast<uintptr_t>(src) % 16 != 0) return fail(c, PF_E_ARG, "source not 16-byte aligned");
+  int32_t n_img;
+  std::memcpy(&n_img, hdr + 4, 4);
+  const size_t img_seg = static_cast<size_t>(n_img) * c->kv * 2;
+  const size_t copy = static_cast<size_t>(n_pos) * c->kv * 2;
+  const size_t cache_pitch = static_cast<size_t>(c->d.max_ctx) * c->kv * 2;
+  if (copy > 0) {
+    if (dev) {
+      PF_CUDA(c, launch_kv_copy(1, c->cache, static_cast<int64_t>(c->d.max_ctx) * c->kv,
+                                const_cast<uint8_t*>(static_cast<const uint8_t*>(src)), static_cast<int64_t>(img_seg),
+                                2 * c->L_w, static_cast<int64_t>(copy), reinterpret_cast<const int32_t*>(hdr),
+                                c->stream));
+    } else {
+      PF_CUDA(c, cudaMemcpy2DAsync(c->cache, cache_pitch, static_cast<const uint8_t*>(src) + 16, img_seg, copy,
+                                   2 * c->L_w, cudaMemcpyHostToDevice, c->stream));
+    }
+  }
+  c->n_pos = n_pos;
+  if (std::getenv("PREFILL_LOG"))
+    std::fprintf(stderr, "KV cache loaded: %lld positions; skipping %lld cached prompt tokens\n", (long long)n_pos,
+                 (long long)n_pos);
+  return PF_OK;
+}
+
+extern "C" int prefill_prune_predicate(const prefill_model_desc* d) {
+  if (!d) return PF_E_ARG;
+  return predicate(*d, d->prune_shared_enable) ? 1 : 0;
+}

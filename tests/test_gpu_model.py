@@ -1,0 +1,206 @@
+"""Whole prefill through the C ABI against the CPU oracle.
+
+Acceptance: the output row's logits within 2e-2 * max|oracle logit| with the
+same argmax (when the oracle's top two are further apart than twice that
+tolerance; otherwise the GPU's argmax must be one of the oracle's logits
+within the tolerance of the top), and the pruned pass bit-identical to the
+unpruned one."""
+import numpy as np
+import pytest
+
+from oracle.prefill import OracleContext
+from prefill_kv_shared_gb300 import binding, synth
+from tests.gpu_util import need_gpu, torch
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+
+
+def check_logits(got, want):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    assert np.isfinite(got).all()
+    tol = TOL * np.abs(want).max()
+    err = np.abs(got - want).max()
+    assert err <= tol, f"max|err| {err:.4g} > {tol:.4g}"
+    top = np.sort(want)[::-1]
+    if top[0] - top[1] > 2 * tol:
+        assert int(np.argmax(got)) == int(np.argmax(want))
+    else:
+        assert want[int(np.argmax(got))] >= top[0] - tol
+    return err / np.abs(want).max()
+
+
+def run_gpu(weights, tokens, ubatch, prune, max_ctx=None, ctx=None):
+    cfg = weights.cfg
+    own = ctx is None
+    if own:
+        ctx = binding.PrefillContext(weights, max_ctx=max_ctx or len(tokens), ubatch_max=ubatch, prune=prune)
+    logits = torch.empty(cfg["vocab"], dtype=torch.float32, device="cuda")
+    chunks = synth.split_ubatches(tokens, ubatch)
+    pos = ctx.n_pos
+    for i, c in enumerate(chunks):
+        ctx.ubatch(c, pos, i == len(chunks) - 1, logits)
+        pos += len(c)
+    ctx.sync()
+    out = logits.cpu().numpy()
+    if own:
+        ctx.close()
+    return out
+
+
+@pytest.fixture(scope="module")
+def gpu():
+    need_gpu()
+    from prefill_kv_shared_gb300 import build
+    build.build()
+    binding.load()
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    cfg = synth.config("tiny")
+    return synth.make_weights(cfg)
+
+
+@pytest.fixture(scope="module")
+def e2b():
+    return synth.make_weights(synth.config("e2b"))
+
+
+def test_tiny_matches_oracle(gpu, tiny):
+    tok = synth.make_tokens(tiny.cfg, 64)
+    want = OracleContext(tiny.cfg, tiny, 128).ubatch(tok, True)
+    on = run_gpu(tiny, tok, 64, True)
+    off = run_gpu(tiny, tok, 64, False)
+    check_logits(on, want)
+    np.testing.assert_array_equal(on, off)
+
+
+def test_tiny_ubatches_and_ragged(gpu, tiny):
+    tok = synth.make_tokens(tiny.cfg, 61, seed=7)
+    want = OracleContext(tiny.cfg, tiny, 128).prefill(tok, 16)
+    on = run_gpu(tiny, tok, 16, True, max_ctx=128)
+    off = run_gpu(tiny, tok, 16, False, max_ctx=128)
+    check_logits(on, want)
+    np.testing.assert_array_equal(on, off)
+
+
+def test_tiny_device_tokens(gpu, tiny):
+    tok = synth.make_tokens(tiny.cfg, 64)
+    host = run_gpu(tiny, tok, 64, True)
+    ctx = binding.PrefillContext(tiny, max_ctx=64, ubatch_max=64)
+    logits = torch.empty(tiny.cfg["vocab"], dtype=torch.float32, device="cuda")
+    ctx.ubatch(torch.from_numpy(tok).cuda(), 0, True, logits)
+    ctx.sync()
+    np.testing.assert_array_equal(logits.cpu().numpy(), host)
+    ctx.reset()
+    bad = torch.from_numpy(tok).cuda()
+    bad[5] = tiny.cfg["vocab"]
+    ctx.ubatch(bad, 0, True, logits)
+    with pytest.raises(binding.PrefillError) as e:
+        ctx.sync()
+    assert e.value.code == binding.PF_E_DEVICE_TOKEN
+    ctx.close()
+
+
+def test_e2b_512_matches_oracle(gpu, e2b):
+    tok = synth.make_tokens(e2b.cfg, 512)
+    on = run_gpu(e2b, tok, 512, True)
+    off = run_gpu(e2b, tok, 512, False)
+    np.testing.assert_array_equal(on, off)
+    want = OracleContext(e2b.cfg, e2b, 512).ubatch(tok, True, prune=True)
+    check_logits(on, want)
+
+
+@pytest.mark.parametrize("n", [2048, 8192])
+def test_e2b_prune_bit_identical(gpu, e2b, n):
+    tok = synth.make_tokens(e2b.cfg, n)
+    on = run_gpu(e2b, tok, 512, True)
+    off = run_gpu(e2b, tok, 512, False)
+    assert np.isfinite(on).all()
+    np.testing.assert_array_equal(on, off)
+
+
+def test_e4b_8192_prune_bit_identical(gpu):
+    w = synth.make_weights(synth.config("e4b"))
+    tok = synth.make_tokens(w.cfg, 8192)
+    on = run_gpu(w, tok, 1024, True)
+    off = run_gpu(w, tok, 1024, False)
+    assert np.isfinite(on).all()
+    np.testing.assert_array_equal(on, off)
+
+
+@pytest.fixture(scope="module")
+def tinyllama():
+    return synth.make_weights(synth.config("tinyllama"))
+
+
+def test_kv_restore_suffix_equals_full(gpu, tinyllama):
+    """Cache a 500-token prefix as a KV image, restore it, prefill a 32-token
+    suffix: same logits as the full 532-token prefill (bit-identical on the
+    GPU) and within tolerance of the oracle."""
+    cfg = tinyllama.cfg
+    prefix = synth.make_tokens(cfg, 500, seed=1)
+    ctx = binding.PrefillContext(tinyllama, max_ctx=532, ubatch_max=512)
+    assert not ctx.prune_active
+    logits = torch.empty(cfg["vocab"], dtype=torch.float32, device="cuda")
+    ctx.ubatch(prefix, 0, False)
+    nbytes = ctx.kv_image_bytes(500)
+    assert nbytes == 16 + 2 * 22 * 500 * 256 * 2
+    img = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    ctx.kv_save(img, nbytes)
+    ctx.sync()
+    host_img = np.empty(nbytes, dtype=np.uint8)
+    ctx.kv_save(host_img, nbytes)
+    np.testing.assert_array_equal(host_img, img.cpu().numpy())
+    orc = OracleContext(cfg, tinyllama, 532)
+    orc.prefill(prefix, 512)
+    for i in range(3):
+        suffix = synth.make_tokens(cfg, 32, seed=2 + i)
+        full = run_gpu(tinyllama, np.concatenate([prefix, suffix]), 512, True, max_ctx=532)
+        ctx.reset()
+        ctx.kv_load(img if i % 2 == 0 else host_img, nbytes, 500)
+        assert ctx.n_pos == 500
+        ctx.ubatch(suffix, 500, True, logits)
+        ctx.sync()
+        got = logits.cpu().numpy()
+        np.testing.assert_array_equal(got, full)
+        o2 = OracleContext(cfg, tinyllama, 532)
+        o2.kv_load(orc.kv_save(), 500)
+        check_logits(got, o2.ubatch(suffix, True))
+    ctx.close()
+
+
+def test_errors_leave_state(gpu, tiny):
+    cfg = tiny.cfg
+    ctx = binding.PrefillContext(tiny, max_ctx=64, ubatch_max=32)
+    logits = torch.empty(cfg["vocab"], dtype=torch.float32, device="cuda")
+    tok = synth.make_tokens(cfg, 40)
+    with pytest.raises(binding.PrefillError) as e:
+        ctx.ubatch(tok, 0, True, logits)          # more than ubatch_max
+    assert e.value.code == binding.PF_E_ARG
+    bad = tok[:10].copy()
+    bad[3] = -1
+    with pytest.raises(binding.PrefillError):
+        ctx.ubatch(bad, 0, True, logits)          # token out of range
+    ctx.ubatch(tok[:20], 0, False)
+    with pytest.raises(binding.PrefillError):
+        ctx.ubatch(tok[20:30], 5, True, logits)   # pos0 gap
+    ctx.ubatch(tok[20:40], 20, True, logits)
+    ctx.sync()
+    n = ctx.kv_image_bytes(40)
+    img = np.empty(n, dtype=np.uint8)
+    ctx.kv_save(img, n)
+    ctx.reset()
+    for blob, npos, code in [(b"KVCQ" + img[4:].tobytes(), 10, binding.PF_E_KV_MAGIC),
+                             (img[:8].tobytes() + np.int32(3).tobytes() + img[12:].tobytes(), 10, binding.PF_E_KV_SHAPE),
+                             (img.tobytes(), 41, binding.PF_E_KV_RANGE),
+                             (img[:200].tobytes(), 10, binding.PF_E_KV_RANGE)]:
+        arr = np.frombuffer(blob, dtype=np.uint8).copy()
+        with pytest.raises(binding.PrefillError) as e:
+            ctx.kv_load(arr, len(arr), npos)
+        assert e.value.code == code
+        assert ctx.n_pos == 0
+    ctx.close()

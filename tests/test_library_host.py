@@ -1,0 +1,96 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports
+every symbol the headers declare, and its host-only helpers agree with the
+pages' facts and the oracle."""
+import os
+import re
+import struct
+import subprocess
+
+import pytest
+
+import oracle
+from prefill_kv_shared_gb300 import binding, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from prefill_kv_shared_gb300 import build
+    build.build()
+    return binding.load()
+
+
+def _declared_functions():
+    names = set()
+    for h in ("prefill.h", "prefill_ops.h"):
+        src = open(os.path.join(ROOT, "include", h)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M):
+            name = m.group(1)
+            if name not in ("defined",):
+                names.add(name)
+    return names
+
+
+def test_headers_are_plain_c():
+    for h in ("prefill.h", "prefill_ops.h"):
+        r = subprocess.run(["gcc", "-fsyntax-only", "-std=c99", "-Wall", "-Werror", "-x", "c",
+                            os.path.join(ROOT, "include", h)], capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_functions()
+    assert "prefill_ubatch" in declared and "kv_load" in declared and "pfop_attention" in declared
+    assert declared == set(binding.EXPORTS), declared ^ set(binding.EXPORTS)
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    missing = declared - exported
+    assert not missing, missing
+
+
+def test_kv_image_size_pin(lib):
+    kv = {}
+    for ln in open(os.path.join(GOLDEN, "kv_image_size.txt")):
+        if ln.strip() and not ln.startswith("#"):
+            k, v = ln.split()
+            kv[k] = int(v)
+    n = binding.kv_image_bytes_for(kv["layers"], kv["n_pos"], kv["kv_dim"])
+    assert n - 16 == kv["body_bytes"]
+    assert n == oracle.kv_image_bytes(kv["layers"], kv["n_pos"], kv["kv_dim"])
+    assert binding.kv_image_bytes_for(-1, 3, 4) == -1
+
+
+def test_prune_predicate_matches_listing(lib):
+    base = synth.config("e2b")
+    for ln in open(os.path.join(GOLDEN, "prune_predicate.txt")):
+        if not ln.strip() or ln.startswith("#"):
+            continue
+        L, S, nseq, emb, idx, want = (int(v) for v in ln.split())
+        if idx >= 0:
+            continue  # the library exposes no per-layer embedding outputs
+        cfg = dict(base, n_layer=L, n_layer_kv_from_start=S,
+                   kv_src=[-1 if i < S else max(S - 1, 0) for i in range(L)])
+        assert binding.prune_predicate(cfg, True, nseq, bool(emb)) == bool(want), ln
+        assert oracle.prune_shared(L, S, n_seq_max=nseq, embeddings=bool(emb)) == bool(want)
+    assert binding.prune_predicate(base, prune=False) is False
+
+
+def _hdr(n, layers, kv, magic=b"KVCP"):
+    return magic + struct.pack("<iii", n, layers, kv)
+
+
+def test_kv_header_check(lib):
+    size = binding.kv_image_bytes_for(22, 500, 256)
+    ok = binding.kv_header_check(_hdr(500, 22, 256), 22, 256, 500, 2048, size)
+    assert ok == binding.PF_OK
+    assert binding.kv_header_check(_hdr(500, 22, 256), 22, 256, 25, 2048, size) == binding.PF_OK
+    assert binding.kv_header_check(_hdr(500, 22, 256, b"KVCQ"), 22, 256, 500, 2048, size) == binding.PF_E_KV_MAGIC
+    assert binding.kv_header_check(_hdr(500, 21, 256), 22, 256, 500, 2048, size) == binding.PF_E_KV_SHAPE
+    assert binding.kv_header_check(_hdr(500, 22, 128), 22, 256, 500, 2048, size) == binding.PF_E_KV_SHAPE
+    assert binding.kv_header_check(_hdr(500, 22, 256), 22, 256, 501, 2048, size) == binding.PF_E_KV_RANGE
+    assert binding.kv_header_check(_hdr(500, 22, 256), 22, 256, 500, 499, size) == binding.PF_E_KV_RANGE
+    assert binding.kv_header_check(_hdr(500, 22, 256), 22, 256, 500, 2048, size - 1) == binding.PF_E_KV_RANGE
+    assert binding.kv_header_check(b"KV", 22, 256, 0, 2048, 2) == binding.PF_E_KV_MAGIC
