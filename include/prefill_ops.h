@@ -76,6 +76,14 @@ int pfop_embed(int32_t wtype, const void* tok_host, const void* ple_host, int32_
 int pfop_kv_copy(int32_t dir, void* cache_dev, int64_t cache_seg_halves, void* image_dev, int64_t img_seg_bytes,
                  int32_t n_seg, int64_t copy_bytes, const int32_t* header4, void* stream);
 
+/* Time the GEMM kernel: upload W once, run `warmup` then `iters` launches of
+   out = A W^T (fp32 [M][N]) and return the mean device time per launch in
+   *us (CUDA events on `stream`).  split: k-splits (0 = the library's choice
+   for this shape). */
+int pfop_linear_bench(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn, int32_t split,
+                      const void* a_dev, int32_t a_rows, int32_t M, float* out_dev, int32_t warmup, int32_t iters,
+                      float* us, void* stream);
+
 /* Last error message of a pfop_* call on this thread. */
 const char* pfop_last_error(void);
 

@@ -37,7 +37,7 @@ EXPORTS = (
     "prefill_destroy", "prefill_last_error", "prefill_prune_predicate", "prefill_kv_header_check",
     "prefill_kv_image_bytes_for",
     "pfop_linear_f32", "pfop_linear_resid", "pfop_linear_glu", "pfop_linear_ple", "pfop_linear_qkv",
-    "pfop_attention", "pfop_rmsnorm", "pfop_embed", "pfop_kv_copy", "pfop_last_error",
+    "pfop_attention", "pfop_rmsnorm", "pfop_embed", "pfop_kv_copy", "pfop_last_error", "pfop_linear_bench",
 )
 
 
@@ -111,6 +111,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "pfop_embed": (C.c_int, [i32, vp, vp, i32, i32, i32, f32, vp, i32, vp, vp, vp]),
         "pfop_kv_copy": (C.c_int, [i32, vp, i64, vp, i64, i32, i64, vp, vp]),
         "pfop_last_error": (C.c_char_p, []),
+        "pfop_linear_bench": (C.c_int, [i32, vp, i32, i32, i32, i32, vp, i32, i32, vp, i32, i32,
+                                        C.POINTER(C.c_float), vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -5,21 +5,32 @@
 //   out = A[M, K] (bf16, K-major) x W[N, K]^T, fp32 accumulation in TMEM.
 //
 // Weights are Q4_0 (32-element blocks, fp16 scale d, value d*(nibble-8)) or
-// bf16.  Q4_0 tiles are fetched with one bulk copy per k-block and expanded
-// to bf16 in shared memory by eight dequant warps, written directly in the
-// 128-byte-swizzled K-major layout the MMA reads; A (and bf16 W) tiles come
-// in by TMA with the same swizzle.
+// bf16.  Q4_0 tiles arrive by one bulk copy per 64-wide k-block into a raw
+// ring; dequant warps expand them to bf16 straight into the 128-byte-swizzled
+// K-major layout the MMA reads (B ring).  A (and bf16 W) tiles come in by TMA
+// with the same swizzle (A ring).  The three rings are released separately:
+// the raw ring by the dequant warps, the A and B rings by the MMA commits,
+// so weight fetches run far ahead of the tensor cores.
 //
-// CTA: 128*MT rows x BN columns, K in blocks of 64.
-//   warp 0      TMA / bulk-copy producer (one lane issues)
+// Persistent CTAs (one per SM) walk work units (m-block, n-tile, k-split):
+//   warp 0      TMA / bulk-copy producer
 //   warp 1      TMEM allocation, MMA issue (one lane), commits
-//   warps 2..9  Q4_0 -> bf16 dequant per stage, then the fused epilogue
-//               (TMEM -> registers -> global), 4 lane quarters x 2
+//   warps 2..5  epilogue (one TMEM lane quarter each): TMEM -> registers ->
+//               fused epilogue -> global; TMEM accumulators are double
+//               buffered when they fit, so a unit's epilogue overlaps the
+//               next unit's main loop
+//   warps 6..13 Q4_0 -> bf16 dequant
+//
+// Split-K: a weight matrix may be cut into S k-ranges (S fixed per matrix
+// shape, never per M), run by the S CTAs of a thread-block cluster; ranks
+// 1..S-1 store their fp32 partial tiles into rank 0's shared memory
+// (distributed shared memory), and rank 0 adds them to its own in ascending
+// rank order before the epilogue.
 //
 // Determinism: every output element is produced by the same sequence of
-// MMAs over k (64-wide blocks in ascending order, four K=16 steps each)
-// whatever M is, so a row's result does not depend on how many rows the
-// launch carries (M = 1 and M = 512 give bit-identical rows).
+// MMAs over k (64-wide blocks in ascending order, four K=16 steps each, the
+// same split boundaries and the same split order) whatever M is, so a row's
+// result does not depend on how many rows the launch carries.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -28,26 +39,35 @@
 
 namespace pf {
 
-constexpr int GEMM_THREADS = 320;
+constexpr int GEMM_WARPS = 14;
+constexpr int GEMM_THREADS = GEMM_WARPS * 32;
+constexpr int EPI_WARP0 = 2;
+constexpr int DQ_WARP0 = 6;
+constexpr int DQ_THREADS = 256;
+constexpr int SMEM_LIMIT = 232448;
+
+__host__ __device__ constexpr int pow2_cols(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
 
 template <int WK, int BN, int MT>
 struct GemmCfg {
-  static constexpr int BM = 128, BK = 64;
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int RAW_BYTES = (WK == W_Q4) ? BN * 36 : 0;
-  static constexpr int RAW_SLOT = (RAW_BYTES + 1023) / 1024 * 1024;
-  static constexpr int STAGE_BYTES = MT * A_BYTES + B_BYTES + RAW_SLOT;
-  static constexpr int SMEM_BUDGET = 232448 - 2048;
-  static constexpr int STAGES_FIT = SMEM_BUDGET / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
-  static constexpr int ACC_COLS = MT * BN;
-  static constexpr int TMEM_COLS = ACC_COLS <= 32 ? 32 : ACC_COLS <= 64 ? 64 : ACC_COLS <= 128 ? 128
-                                                                      : ACC_COLS <= 256 ? 256 : 512;
-  static_assert(STAGES >= 2, "shared memory too small for two stages");
-  static_assert(ACC_COLS <= 512, "accumulators exceed TMEM");
-  static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "MMA N");
+  static constexpr bool Q4 = WK == W_Q4;
+  static constexpr int A_BYTES = MT * 128 * 128;  // MT tiles of 128 rows x 64 bf16
+  static constexpr int BT_BYTES = BN * 128;       // one bf16 B tile (BN rows x 64)
+  static constexpr int RAW_BYTES = Q4 ? BN * 36 : 0;
+  static constexpr int A_STAGE = A_BYTES + (Q4 ? 0 : BT_BYTES);
+  static constexpr int S_B = Q4 ? (BN >= 256 ? 2 : (BN >= 128 ? 3 : 4)) : 0;
+  static constexpr int S_R = Q4 ? (BN >= 256 ? 6 : 8) : 0;
+  static constexpr int RAW_RING = (S_R * RAW_BYTES + 1023) / 1024 * 1024;
+  static constexpr int FIXED = S_B * BT_BYTES + RAW_RING + 1024 + 512;
+  static constexpr int S_A_FIT = (SMEM_LIMIT - FIXED) / A_STAGE;
+  static constexpr int S_A = S_A_FIT > 8 ? 8 : S_A_FIT;
+  static constexpr int SMEM_BYTES = S_A * A_STAGE + FIXED;
+  static constexpr int ACC = MT * BN;
+  static constexpr int ACC_BUFS = (2 * ACC <= 512) ? 2 : 1;
+  static constexpr int TMEM_COLS = pow2_cols(ACC * ACC_BUFS);
+  static_assert(S_A >= 2, "shared memory too small for two A stages");
+  static_assert(ACC <= 512, "accumulators exceed TMEM");
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "MMA N");
 };
 
 // ---------------------------------------------------------------------------
@@ -92,9 +112,7 @@ __device__ __forceinline__ void dequant_block32(uint4 nib, __half d, uint8_t* ro
 }
 
 // ---------------------------------------------------------------------------
-// epilogue helpers
-
-__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+// epilogue
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -112,27 +130,27 @@ __device__ __forceinline__ void store32x16(void* dst, const uint32_t (&w)[16]) {
   for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
 }
 
-template <int BN>
-__device__ __forceinline__ void epilogue(const EpiParams& ep, uint32_t tmem_acc, int m, bool row_ok,
-                                         int n_tile, int ew) {
+// The fused epilogue for one row of one tile.  load(c, v) fills v with the 32
+// fp32 results of the tile's column chunk c (columns 32c .. 32c+31) for this
+// thread's row; it is called in a warp-uniform way.
+template <int BN, class Load>
+__device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m, bool row_ok, int n_tile, Load&& load) {
   constexpr int NCH = BN / 32;
   const int n0 = n_tile * BN;
-  uint32_t v[32], u[32];
+  float v[32], u[32];
   if (ep.kind == EPI_GLU) {
     constexpr int HALF_CH = NCH / 2;
-    for (int c = ew; c < HALF_CH; c += 2) {
-      tmem_ld32(tmem_acc + 32 * c, v);
-      tmem_ld32(tmem_acc + 32 * (c + HALF_CH), u);
-      tmem_ld_wait();
+    for (int c = 0; c < HALF_CH; ++c) {
+      load(c, v);
+      load(c + HALF_CH, u);
       if (!row_ok) continue;
       const int f0 = n_tile * (BN / 2) + 32 * c;
       uint32_t w[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        float g0 = u2f(v[2 * j]), g1 = u2f(v[2 * j + 1]);
-        float a0 = ep.act == 0 ? gelu_tanh_f(g0) : silu_f(g0);
-        float a1 = ep.act == 0 ? gelu_tanh_f(g1) : silu_f(g1);
-        w[j] = pack_bf16x2(a0 * u2f(u[2 * j]), a1 * u2f(u[2 * j + 1]));
+        const float a0 = ep.act == 0 ? gelu_tanh_f(v[2 * j]) : silu_f(v[2 * j]);
+        const float a1 = ep.act == 0 ? gelu_tanh_f(v[2 * j + 1]) : silu_f(v[2 * j + 1]);
+        w[j] = pack_bf16x2(a0 * u[2 * j], a1 * u[2 * j + 1]);
       }
       if (f0 + 32 <= ep.N) store32x16(ep.out_bf16 + (size_t)m * ep.ld_bf16 + f0, w);
     }
@@ -142,16 +160,15 @@ __device__ __forceinline__ void epilogue(const EpiParams& ep, uint32_t tmem_acc,
     const int hd = ep.head_dim, half = hd / 2, pair_ch = half / 32;
     const int q_end = ep.q_dim, k_end = ep.q_dim + ep.kv_dim, v_end = ep.q_dim + 2 * ep.kv_dim;
     const int pos = ep.pos0 + m;
-    for (int c = ew; c < NCH; c += 2) {
+    for (int c = 0; c < NCH; ++c) {
       const int n = n0 + 32 * c;
-      if (n >= v_end) break;  // padding columns (uniform across the warp)
+      if (n >= v_end) break;  // padding columns
       if (n >= k_end) {       // V: no rotation
-        tmem_ld32(tmem_acc + 32 * c, v);
-        tmem_ld_wait();
+        load(c, v);
         if (!row_ok) continue;
         uint32_t w[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) w[j] = pack_half2(u2f(v[2 * j]), u2f(v[2 * j + 1]));
+        for (int j = 0; j < 16; ++j) w[j] = pack_half2(v[2 * j], v[2 * j + 1]);
         store32x16(ep.v_cache + (size_t)pos * ep.kv_dim + (n - k_end), w);
         continue;
       }
@@ -159,9 +176,8 @@ __device__ __forceinline__ void epilogue(const EpiParams& ep, uint32_t tmem_acc,
       const int rel = is_q ? n : n - q_end;
       const int i0 = rel % hd;
       if (i0 >= half) continue;  // handled together with its partner chunk
-      tmem_ld32(tmem_acc + 32 * c, v);
-      tmem_ld32(tmem_acc + 32 * (c + pair_ch), u);
-      tmem_ld_wait();
+      load(c, v);
+      load(c + pair_ch, u);
       if (!row_ok) continue;
       const int head = rel / hd;
       const float2* cs = ep.rope + (size_t)pos * half + i0;
@@ -169,10 +185,8 @@ __device__ __forceinline__ void epilogue(const EpiParams& ep, uint32_t tmem_acc,
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const float2 c0 = cs[2 * j], c1 = cs[2 * j + 1];
-        const float x0 = u2f(v[2 * j]), x1 = u2f(v[2 * j + 1]);
-        const float y0 = u2f(u[2 * j]), y1 = u2f(u[2 * j + 1]);
-        w1[j] = pack_half2(x0 * c0.x - y0 * c0.y, x1 * c1.x - y1 * c1.y);
-        w2[j] = pack_half2(x0 * c0.y + y0 * c0.x, x1 * c1.y + y1 * c1.x);
+        w1[j] = pack_half2(v[2 * j] * c0.x - u[2 * j] * c0.y, v[2 * j + 1] * c1.x - u[2 * j + 1] * c1.y);
+        w2[j] = pack_half2(v[2 * j] * c0.y + u[2 * j] * c0.x, v[2 * j + 1] * c1.y + u[2 * j + 1] * c1.x);
       }
       __half* dst = is_q ? ep.q_out + (size_t)m * ep.q_dim + head * hd
                          : ep.k_cache + (size_t)pos * ep.kv_dim + head * hd;
@@ -182,11 +196,10 @@ __device__ __forceinline__ void epilogue(const EpiParams& ep, uint32_t tmem_acc,
     return;
   }
   // F32, RESID, PLE: one 32-column chunk at a time
-  for (int c = ew; c < NCH; c += 2) {
+  for (int c = 0; c < NCH; ++c) {
     const int n = n0 + 32 * c;
     if (n >= ep.N) break;
-    tmem_ld32(tmem_acc + 32 * c, v);
-    tmem_ld_wait();
+    load(c, v);
     if (!row_ok) continue;
     const bool full = n + 32 <= ep.N;
     if (ep.kind == EPI_F32) {
@@ -194,27 +207,29 @@ __device__ __forceinline__ void epilogue(const EpiParams& ep, uint32_t tmem_acc,
       if (full) {
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          reinterpret_cast<float4*>(dst)[j] =
-              make_float4(u2f(v[4 * j]), u2f(v[4 * j + 1]), u2f(v[4 * j + 2]), u2f(v[4 * j + 3]));
+          reinterpret_cast<float4*>(dst)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
       } else {
-        for (int j = 0; j < 32 && n + j < ep.N; ++j) dst[j] = u2f(v[j]);
+        for (int j = 0; j < 32 && n + j < ep.N; ++j) dst[j] = v[j];
       }
     } else if (ep.kind == EPI_RESID) {
       float* xr = ep.out_f32 + (size_t)m * ep.ld_f32 + n;
-      float nv[32];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         float4 x4 = reinterpret_cast<const float4*>(xr)[j];
-        nv[4 * j] = x4.x + u2f(v[4 * j]);
-        nv[4 * j + 1] = x4.y + u2f(v[4 * j + 1]);
-        nv[4 * j + 2] = x4.z + u2f(v[4 * j + 2]);
-        nv[4 * j + 3] = x4.w + u2f(v[4 * j + 3]);
-        reinterpret_cast<float4*>(xr)[j] = make_float4(nv[4 * j], nv[4 * j + 1], nv[4 * j + 2], nv[4 * j + 3]);
+        x4.x += v[4 * j];
+        x4.y += v[4 * j + 1];
+        x4.z += v[4 * j + 2];
+        x4.w += v[4 * j + 3];
+        v[4 * j] = x4.x;
+        v[4 * j + 1] = x4.y;
+        v[4 * j + 2] = x4.z;
+        v[4 * j + 3] = x4.w;
+        reinterpret_cast<float4*>(xr)[j] = x4;
       }
       if (ep.out_bf16) {
         uint32_t w[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(nv[2 * j], nv[2 * j + 1]);
+        for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
         store32x16(ep.out_bf16 + (size_t)m * ep.ld_bf16 + n, w);
       }
     } else {  // EPI_PLE
@@ -223,8 +238,7 @@ __device__ __forceinline__ void epilogue(const EpiParams& ep, uint32_t tmem_acc,
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const __nv_bfloat162 p2 = reinterpret_cast<const __nv_bfloat162*>(pl)[j];
-        w[j] = pack_bf16x2(gelu_tanh_f(u2f(v[2 * j])) * __low2float(p2),
-                           gelu_tanh_f(u2f(v[2 * j + 1])) * __high2float(p2));
+        w[j] = pack_bf16x2(gelu_tanh_f(v[2 * j]) * __low2float(p2), gelu_tanh_f(v[2 * j + 1]) * __high2float(p2));
       }
       store32x16(ep.out_bf16 + (size_t)m * ep.ld_bf16 + n, w);
     }
@@ -234,44 +248,89 @@ __device__ __forceinline__ void epilogue(const EpiParams& ep, uint32_t tmem_acc,
 // ---------------------------------------------------------------------------
 // the kernel
 
-// wait with a time limit but without giving up on another thread's error:
-// used to let in-flight copies land before the CTA exits on an error path
+// Let copies already issued land before the CTA exits on an error path
+// (bounded in time, ignoring the error flag).
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(a, parity)) {
-    if (globaltimer_ns() - t0 > 200000000ull) return;  // 200 ms
+    if (globaltimer_ns() - t0 > 200000000ull) return;
   }
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local_smem, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+struct GemmShape {
+  int M, K;
+  int n_tiles, m_blocks, splits, kb_per_split, n_units;
+};
+
+// Byte offset of (chunk c, row r, 16-byte piece q) in a split partial slot:
+// [chunk][row][32 floats], pieces XOR-swizzled by row so that a warp's
+// 16-byte accesses hit all banks.
+__device__ __forceinline__ uint32_t slot_off(int c, int r, int q) {
+  return static_cast<uint32_t>(((c * 128 + r) << 7) + ((q ^ (r & 7)) << 4));
 }
 
 template <int WK, int BN, int MT>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const uint8_t* __restrict__ wq4, int M, int K, const __grid_constant__ EpiParams ep,
-                   int* err) {
+                   const uint8_t* __restrict__ wq4, const __grid_constant__ GemmShape sh,
+                   const __grid_constant__ EpiParams ep, int* err) {
   using C = GemmCfg<WK, BN, MT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
-  uint64_t* empty = full + C::STAGES;
-  uint64_t* bready = empty + C::STAGES;
-  uint64_t* accum = bready + C::STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  uint8_t* a_ring = smem;
+  uint8_t* b_ring = a_ring + C::S_A * C::A_STAGE;
+  uint8_t* r_ring = b_ring + C::S_B * C::BT_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(r_ring + C::RAW_RING);
+  uint64_t* full_a = bars;
+  uint64_t* empty_a = full_a + C::S_A;
+  uint64_t* full_r = empty_a + C::S_A;
+  uint64_t* empty_r = full_r + (C::S_R > 0 ? C::S_R : 1);
+  uint64_t* bfull = empty_r + (C::S_R > 0 ? C::S_R : 1);
+  uint64_t* bempty = bfull + (C::S_B > 0 ? C::S_B : 1);
+  uint64_t* tfull = bempty + (C::S_B > 0 ? C::S_B : 1);
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_tile = blockIdx.x;
-  const int m_base = blockIdx.y * (MT * 128);
-  const int nkb = K / 64;
-  int mt_valid = (M - m_base + 127) / 128;
-  if (mt_valid > MT) mt_valid = MT;
+  const int nkb = sh.kb_per_split;
+  const bool split_mode = sh.splits > 1;  // one unit per CTA, a cluster per tile
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-      mbar_init(&bready[s], 8);
+    for (int s = 0; s < C::S_A; ++s) {
+      mbar_init(&full_a[s], 1);
+      mbar_init(&empty_a[s], 1);
     }
-    mbar_init(accum, 1);
+    for (int s = 0; s < C::S_R; ++s) {
+      mbar_init(&full_r[s], 1);
+      mbar_init(&empty_r[s], DQ_THREADS / 32);
+    }
+    for (int s = 0; s < C::S_B; ++s) {
+      mbar_init(&bfull[s], DQ_THREADS / 32);
+      mbar_init(&bempty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -283,108 +342,218 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  bool epi_ok = true;
 
   if (warp == 0) {
     // ---------------- producer
-    int issued = 0;
+    uint32_t g = 0;
     bool ok = true;
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int s = kb % C::STAGES;
-      const uint32_t ph = (kb / C::STAGES) & 1;
-      if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (lane == 0) {
-        uint8_t* st = smem + s * C::STAGE_BYTES;
-        const uint32_t tx = mt_valid * C::A_BYTES + (WK == W_BF16 ? C::B_BYTES : C::RAW_BYTES);
-        mbar_arrive_expect_tx(&full[s], tx);
-        for (int mt = 0; mt < mt_valid; ++mt)
-          tma_load_2d(st + mt * C::A_BYTES, &tmA, &full[s], kb * 64, m_base + mt * 128);
-        if (WK == W_BF16) {
-          tma_load_2d(st + MT * C::A_BYTES, &tmB, &full[s], kb * 64, n_tile * BN);
-        } else {
-          bulk_load(st + MT * C::A_BYTES + C::B_BYTES, wq4 + ((size_t)n_tile * nkb + kb) * C::RAW_BYTES,
-                    C::RAW_BYTES, &full[s]);
+    for (int u = blockIdx.x; u < sh.n_units && ok; u += gridDim.x) {
+      const int ks = u % sh.splits, t = u / sh.splits;
+      const int nt = t % sh.n_tiles, mb = t / sh.n_tiles;
+      const int m_base = mb * MT * 128;
+      int mt_valid = (sh.M - m_base + 127) / 128;
+      if (mt_valid > MT) mt_valid = MT;
+      for (int i = 0; i < nkb; ++i, ++g) {
+        const int kb = ks * nkb + i;
+        const int sa = g % C::S_A;
+        if (lane == 0) ok = mbar_wait(&empty_a[sa], ((g / C::S_A) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
+        if (C::Q4 && lane == 0 && ok)
+          ok = mbar_wait(&empty_r[g % C::S_R], ((g / C::S_R) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (lane == 0) {
+          uint8_t* st = a_ring + sa * C::A_STAGE;
+          mbar_arrive_expect_tx(&full_a[sa], mt_valid * 128 * 128 + (C::Q4 ? 0 : C::BT_BYTES));
+          for (int mt = 0; mt < mt_valid; ++mt)
+            tma_load_2d(st + mt * 128 * 128, &tmA, &full_a[sa], kb * 64, m_base + mt * 128);
+          if (C::Q4) {
+            const int sr = g % C::S_R;
+            mbar_arrive_expect_tx(&full_r[sr], C::RAW_BYTES);
+            bulk_load(r_ring + sr * C::RAW_BYTES,
+                      wq4 + ((size_t)nt * (sh.splits * nkb) + kb) * C::RAW_BYTES, C::RAW_BYTES, &full_r[sr]);
+          } else {
+            tma_load_2d(st + C::A_BYTES, &tmB, &full_a[sa], kb * 64, nt * BN);
+          }
         }
+        __syncwarp();
       }
-      __syncwarp();
-      issued = kb + 1;
     }
     if (!ok && lane == 0) {
-      // let the copies already issued land before shared memory goes away
-      const int first = issued > C::STAGES ? issued - C::STAGES : 0;
-      for (int kb = first; kb < issued; ++kb) mbar_drain(&full[kb % C::STAGES], (kb / C::STAGES) & 1);
+      // the last S_A / S_R issues may still be in flight
+      const uint32_t ga = g > (uint32_t)C::S_A ? g - C::S_A : 0;
+      for (uint32_t x = ga; x < g; ++x) mbar_drain(&full_a[x % C::S_A], (x / C::S_A) & 1);
+      if (C::Q4) {
+        const uint32_t gr = g > (uint32_t)C::S_R ? g - C::S_R : 0;
+        for (uint32_t x = gr; x < g; ++x) mbar_drain(&full_r[x % C::S_R], (x / C::S_R) & 1);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issue
     constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
+    uint32_t g = 0, j = 0;
     bool ok = true;
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int s = kb % C::STAGES;
-      const uint32_t ph = (kb / C::STAGES) & 1;
-      if (lane == 0) {
-        ok = mbar_wait(&full[s], ph, err, PF_DEV_TIMEOUT_MMA);
-        if (ok && WK == W_Q4) ok = mbar_wait(&bready[s], ph, err, PF_DEV_TIMEOUT_MMA);
-      }
+    for (int u = blockIdx.x; u < sh.n_units && ok; u += gridDim.x, ++j) {
+      const int t = u / sh.splits;
+      const int mb = t / sh.n_tiles;
+      int mt_valid = (sh.M - mb * MT * 128 + 127) / 128;
+      if (mt_valid > MT) mt_valid = MT;
+      const int buf = C::ACC_BUFS == 2 ? (j & 1) : 0;
+      const uint32_t tacc = tmem_base + buf * C::ACC;
+      if (lane == 0)
+        ok = mbar_wait(&tempty[buf], ((j / C::ACC_BUFS) & 1) ^ 1, err, PF_DEV_TIMEOUT_MMA);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      if (lane == 0) {
-        const uint8_t* st = smem + s * C::STAGE_BYTES;
-        const uint32_t a0 = smem_u32(st);
-        const uint32_t b0 = smem_u32(st + MT * C::A_BYTES);
-        for (int mt = 0; mt < mt_valid; ++mt) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sdesc_sw128(a0 + mt * C::A_BYTES + kk * 32);
-            const uint64_t bd = sdesc_sw128(b0 + kk * 32);
-            tc_mma_f16(tmem_base + mt * BN, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-          }
+      for (int i = 0; i < nkb; ++i, ++g) {
+        const int sa = g % C::S_A;
+        const int sb = C::Q4 ? g % C::S_B : 0;
+        if (lane == 0) {
+          ok = mbar_wait(&full_a[sa], (g / C::S_A) & 1, err, PF_DEV_TIMEOUT_MMA);
+          if (ok && C::Q4) ok = mbar_wait(&bfull[sb], (g / C::S_B) & 1, err, PF_DEV_TIMEOUT_MMA);
         }
-        tc_commit(&empty[s]);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a0 = smem_u32(a_ring + sa * C::A_STAGE);
+          const uint32_t b0 = C::Q4 ? smem_u32(b_ring + sb * C::BT_BYTES) : a0 + C::A_BYTES;
+          for (int mt = 0; mt < mt_valid; ++mt) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sdesc_sw128(a0 + mt * 128 * 128 + kk * 32);
+              const uint64_t bd = sdesc_sw128(b0 + kk * 32);
+              tc_mma_f16(tacc + mt * BN, ad, bd, idesc, (i | kk) != 0 ? 1u : 0u);
+            }
+          }
+          tc_commit(&empty_a[sa]);
+          if (C::Q4) tc_commit(&bempty[sb]);
+        }
+        __syncwarp();
       }
+      if (lane == 0) tc_commit(&tfull[buf]);  // the unit's accumulator is complete
       __syncwarp();
     }
-    if (lane == 0) tc_commit(accum);  // fires once every MMA issued above has completed
+    if (!ok && lane == 0) {
+      // wait for the MMAs already issued before TMEM is freed
+      tc_commit(&tfull[0]);
+      mbar_drain(&tfull[0], 0);
+      mbar_drain(&tfull[0], 1);
+    }
     __syncwarp();
-  } else {
-    // ---------------- dequant, then epilogue
-    const int t = threadIdx.x - 64;  // 0..255
+  } else if (warp < DQ_WARP0) {
+    // ---------------- epilogue
+    const int qw = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = 32 * qw + lane;
+    uint32_t j = 0;
+    for (int u = blockIdx.x; u < sh.n_units; u += gridDim.x, ++j) {
+      const int t = u / sh.splits;
+      const int nt = t % sh.n_tiles, mb = t / sh.n_tiles;
+      const int m_base = mb * MT * 128;
+      int mt_valid = (sh.M - m_base + 127) / 128;
+      if (mt_valid > MT) mt_valid = MT;
+      const int buf = C::ACC_BUFS == 2 ? (j & 1) : 0;
+      bool ok = mbar_wait(&tfull[buf], (j / C::ACC_BUFS) & 1, err, PF_DEV_TIMEOUT_EPILOGUE);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        epi_ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (split_mode) break;  // the cluster reduction below takes it from here
+      const uint32_t tq = tmem_base + (static_cast<uint32_t>(32 * qw) << 16) + buf * C::ACC;
+      for (int mt = 0; mt < mt_valid; ++mt) {
+        const int m = m_base + mt * 128 + r;
+        run_epilogue<BN>(ep, m, m < sh.M, nt, [&](int c, float(&v)[32]) {
+          uint32_t x[32];
+          tmem_ld32(tq + mt * BN + 32 * c, x);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(x[q]);
+        });
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+    }
+  } else if (C::Q4) {
+    // ---------------- dequant
+    const int t = threadIdx.x - DQ_WARP0 * 32;  // 0..255
+    uint32_t g = 0;
     bool ok = true;
-    if (WK == W_Q4) {
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % C::STAGES;
-        const uint32_t ph = (kb / C::STAGES) & 1;
-        const bool w_ok = mbar_wait(&full[s], ph, err, PF_DEV_TIMEOUT_DEQUANT);
+    for (int u = blockIdx.x; u < sh.n_units && ok; u += gridDim.x) {
+      for (int i = 0; i < nkb; ++i, ++g) {
+        const int sr = g % C::S_R, sb = g % C::S_B;
+        bool w_ok = mbar_wait(&full_r[sr], (g / C::S_R) & 1, err, PF_DEV_TIMEOUT_DEQUANT);
+        if (w_ok) w_ok = mbar_wait(&bempty[sb], ((g / C::S_B) & 1) ^ 1, err, PF_DEV_TIMEOUT_DEQUANT);
         ok = __all_sync(0xffffffffu, w_ok);
         if (!ok) break;
-        uint8_t* bt = smem + s * C::STAGE_BYTES + MT * C::A_BYTES;
-        const uint8_t* raw = bt + C::B_BYTES;
-#pragma unroll
-        for (int it = t; it < BN * 2; it += 256) {
-          const int r = it % BN, h = it / BN;
-          const uint4 nib = *reinterpret_cast<const uint4*>(raw + (size_t)(h * BN + r) * 16);
-          const __half d = *reinterpret_cast<const __half*>(raw + BN * 32 + (h * BN + r) * 2);
-          dequant_block32(nib, d, bt + r * 128, h, r & 7);
+        uint8_t* bt = b_ring + sb * C::BT_BYTES;
+        const uint8_t* raw = r_ring + sr * C::RAW_BYTES;
+        for (int it = t; it < BN * 2; it += DQ_THREADS) {
+          const int rr = it % BN, h = it / BN;
+          const uint4 nib = *reinterpret_cast<const uint4*>(raw + (size_t)(h * BN + rr) * 16);
+          const __half d = *reinterpret_cast<const __half*>(raw + BN * 32 + (h * BN + rr) * 2);
+          dequant_block32(nib, d, bt + rr * 128, h, rr & 7);
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bready[s]);
+        if (lane == 0) {
+          mbar_arrive(&bfull[sb]);
+          mbar_arrive(&empty_r[sr]);
+        }
       }
     }
-    bool acc_ok = ok ? mbar_wait(accum, 0, err, PF_DEV_TIMEOUT_EPILOGUE) : false;
-    acc_ok = __all_sync(0xffffffffu, acc_ok);
-    if (acc_ok) {
-      tc_fence_after();
-      const int qw = warp & 3;         // TMEM lane quarter this warp may access
-      const int ew = (warp - 2) >> 2;  // which of the two warps on that quarter
-      const int r = 32 * qw + lane;
-      for (int mt = 0; mt < mt_valid; ++mt) {
-        const int m = m_base + mt * 128 + r;
-        const uint32_t tacc = tmem_base + (static_cast<uint32_t>(32 * qw) << 16) + mt * BN;
-        epilogue<BN>(ep, tacc, m, m < M, n_tile, ew);
+  }
+
+  if (split_mode) {
+    // Split-K over the cluster: CTA rank r holds the partial of k-range r.
+    // Ranks 1.. write theirs into rank 0's (now idle) ring memory; rank 0
+    // adds them to its own in ascending rank order and runs the epilogue.
+    cluster_sync_all();
+    const uint32_t rank = cluster_ctarank();
+    const bool epi_warp = warp >= EPI_WARP0 && warp < DQ_WARP0;
+    const int qw = warp & 3;
+    const int r = 32 * qw + lane;
+    const uint32_t tq = tmem_base + (static_cast<uint32_t>(32 * qw) << 16);
+    const uint32_t slot_bytes = 128u * BN * 4u;
+    if (epi_warp && epi_ok && rank != 0) {
+      const uint32_t remote = map_to_rank(smem_u32(a_ring), 0) + (rank - 1) * slot_bytes;
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t x[32];
+        tmem_ld32(tq + 32 * c, x);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          st_cluster_v4(remote + slot_off(c, r, q), __uint_as_float(x[4 * q]), __uint_as_float(x[4 * q + 1]),
+                        __uint_as_float(x[4 * q + 2]), __uint_as_float(x[4 * q + 3]));
       }
+    }
+    cluster_sync_all();
+    if (epi_warp && epi_ok && rank == 0) {
+      const int t = blockIdx.x / sh.splits;
+      const int nt = t % sh.n_tiles, mb = t / sh.n_tiles;
+      const int m = mb * MT * 128 + r;
+      const uint8_t* slots = a_ring;
+      run_epilogue<BN>(ep, m, m < sh.M, nt, [&](int c, float(&v)[32]) {
+        uint32_t x[32];
+        tmem_ld32(tq + 32 * c, x);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(x[q]);
+        for (int s = 1; s < sh.splits; ++s) {
+          const uint8_t* sl = slots + (s - 1) * slot_bytes;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 p = *reinterpret_cast<const float4*>(sl + slot_off(c, r, q));
+            v[4 * q] += p.x;
+            v[4 * q + 1] += p.y;
+            v[4 * q + 2] += p.z;
+            v[4 * q + 3] += p.w;
+          }
+        }
+      });
     }
   }
 
@@ -452,6 +621,42 @@ bool make_weight_map(WeightMat& w, std::string* err) {
   return encode_2d_bf16(&w.tmap, w.dev, (uint64_t)w.K, (uint64_t)w.N_rows, 64, (uint32_t)w.BN, err);
 }
 
+static int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+template <int WK, int BN, int MT>
+static size_t ring_bytes() {
+  using C = GemmCfg<WK, BN, MT>;
+  return static_cast<size_t>(C::S_A) * C::A_STAGE + static_cast<size_t>(C::S_B) * C::BT_BYTES + C::RAW_RING;
+}
+
+static size_t ring_bytes_mt1(int kind, int BN) {
+  if (kind == W_Q4) return BN == 256 ? ring_bytes<W_Q4, 256, 1>() : ring_bytes<W_Q4, 128, 1>();
+  return BN == 256 ? ring_bytes<W_BF16, 256, 1>() : ring_bytes<W_BF16, 128, 1>();
+}
+
+int choose_split(int kind, int N_rows, int BN, int K, int max_rows) {
+  // Split the k-range over a cluster of CTAs when the tile grid (one 128-row
+  // block per tile) would leave SMs idle.  Depends on the matrix shape and
+  // the context's largest ubatch only, never on a launch's M.
+  const int units1 = (N_rows / BN) * ((max_rows + 127) / 128);
+  const int nkb = K / 64;
+  const size_t ring = ring_bytes_mt1(kind, BN);
+  int s = 1;
+  while (units1 * s < 128 && nkb % (2 * s) == 0 && nkb / (2 * s) >= 4 && 2 * s <= 2 &&
+         static_cast<size_t>(2 * s - 1) * 128 * BN * 4 <= ring)
+    s *= 2;
+  return s;
+}
+
 template <int WK, int BN, int MT>
 static cudaError_t launch_t(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err,
                             cudaStream_t s) {
@@ -463,17 +668,46 @@ static cudaError_t launch_t(const ActMat& A, int M, const WeightMat& W, const Ep
                                     C::SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  dim3 grid(W.N_rows / BN, (M + MT * 128 - 1) / (MT * 128));
-  gemm_tc_kernel<WK, BN, MT><<<grid, GEMM_THREADS, C::SMEM_BYTES, s>>>(
-      A.tmap, W.tmap, static_cast<const uint8_t*>(W.dev), M, W.K, ep, err);
-  return cudaGetLastError();
+  GemmShape sh;
+  sh.M = M;
+  sh.K = W.K;
+  sh.n_tiles = W.N_rows / BN;
+  sh.m_blocks = (M + MT * 128 - 1) / (MT * 128);
+  sh.splits = W.split;
+  sh.kb_per_split = (W.K / 64) / W.split;
+  sh.n_units = sh.n_tiles * sh.m_blocks * sh.splits;
+  if (W.split > 1 && static_cast<size_t>(W.split - 1) * 128 * BN * 4 > ring_bytes<WK, BN, MT>())
+    return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(GEMM_THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = s;
+  if (W.split > 1) {
+    // one unit per CTA, the W.split k-ranges of a tile in one cluster
+    cfg.gridDim = dim3(sh.n_units);
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = W.split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  } else {
+    cfg.gridDim = dim3(sh.n_units < sm_count() ? sh.n_units : sm_count());
+    cfg.numAttrs = 0;
+  }
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<WK, BN, MT>, A.tmap, W.tmap, static_cast<const uint8_t*>(W.dev), sh,
+                            ep, err);
 }
 
-cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err,
-                        cudaStream_t s) {
+cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  if (A.K != W.K || W.K % 64 != 0 || W.N_rows % W.BN != 0 || M > A.rows) return cudaErrorInvalidValue;
-  const bool two = M > 128;
+  if (A.K != W.K || W.K % 64 != 0 || W.N_rows % W.BN != 0 || M > A.rows || W.split < 1 ||
+      (W.K / 64) % W.split != 0)
+    return cudaErrorInvalidValue;
+  // two 128-row M tiles per CTA for large M (not in split mode, whose
+  // partial slots hold one)
+  const bool two = M > 128 && W.split == 1;
 #define PF_GEMM_CASE(WKV, BNV)                                                    \
   if (W.kind == WKV && W.BN == BNV)                                               \
     return two ? launch_t<WKV, BNV, 2>(A, M, W, ep, err, s) : launch_t<WKV, BNV, 1>(A, M, W, ep, err, s);

@@ -57,20 +57,25 @@ struct WeightMat {
   int N_rows = 0;  // stored rows (multiple of BN)
   int K = 0;
   int BN = 128;
+  int split = 1;   // k-splits (fixed per matrix shape; K/64 divisible by it)
   void* dev = nullptr;
   size_t bytes = 0;
-  alignas(64) CUtensorMap tmap;
+  CUtensorMap tmap;
 };
 
 // A bf16 activation matrix used as the GEMM's A operand.
 struct ActMat {
   const __nv_bfloat16* dev = nullptr;
   int rows = 0, K = 0;
-  alignas(64) CUtensorMap tmap;
+  CUtensorMap tmap;
 };
 
 bool make_act_map(ActMat& a, std::string* err);
 bool make_weight_map(WeightMat& w, std::string* err);
+
+// k-splits (cluster size) for a weight shape, chosen from the shape and the
+// largest M the context runs; never from a launch's M
+int choose_split(int kind, int N_rows, int BN, int K, int max_rows);
 
 cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err_word,
                         cudaStream_t s);

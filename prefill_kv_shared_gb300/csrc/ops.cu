@@ -50,6 +50,9 @@ int make_weight(Scope& sc, WeightMat& w, int wtype, const std::vector<const void
   w.K = K;
   w.BN = BN;
   w.N_rows = static_cast<int>(rows.size());
+  // the split depends on the matrix shape only (as in a context with
+  // ubatch_max = 512), so one row gives the same bits whatever M is
+  w.split = choose_split(wtype == PF_W_Q4_0 ? W_Q4 : W_BF16, w.N_rows, BN, K, 512);
   if (wtype == PF_W_Q4_0) {
     w.kind = W_Q4;
     std::vector<const uint8_t*> r(rows.size());
@@ -121,6 +124,50 @@ extern "C" int pfop_linear_f32(int32_t wtype, const void* w_host, int32_t N, int
   return run_gemm(sc, A, M, W, e, static_cast<cudaStream_t>(stream));
 }
 
+extern "C" int pfop_linear_bench(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn, int32_t split,
+                                 const void* a_dev, int32_t a_rows, int32_t M, float* out_dev, int32_t warmup,
+                                 int32_t iters, float* us, void* stream) {
+  if (!w_host || !a_dev || !out_dev || !us || N < 1 || N % 4 || M < 1 || M > a_rows || (bn != 128 && bn != 256) ||
+      iters < 1 || warmup < 0 || split < 0)
+    return op_fail(PF_E_ARG, "bad argument");
+  Scope sc;
+  WeightMat W;
+  ActMat A;
+  int rc;
+  if ((rc = make_weight(sc, W, wtype, rows_of(w_host, N, K, wtype, bn), K, bn))) return rc;
+  if (split > 0) {
+    if ((K / 64) % split) return op_fail(PF_E_ARG, "split must divide K/64");
+    W.split = split;
+  }
+  if ((rc = make_act(A, a_dev, a_rows, K))) return rc;
+  EpiParams e;
+  e.kind = EPI_F32;
+  e.N = N;
+  e.out_f32 = out_dev;
+  e.ld_f32 = N;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* err = nullptr;
+  OP_CUDA(sc.alloc(&err, 16));
+  OP_CUDA(cudaMemsetAsync(err, 0, 16, s));
+  for (int i = 0; i < warmup; ++i) OP_CUDA(launch_gemm(A, M, W, e, err, s));
+  cudaEvent_t e0, e1;
+  OP_CUDA(cudaEventCreate(&e0));
+  OP_CUDA(cudaEventCreate(&e1));
+  OP_CUDA(cudaEventRecord(e0, s));
+  for (int i = 0; i < iters; ++i) OP_CUDA(launch_gemm(A, M, W, e, err, s));
+  OP_CUDA(cudaEventRecord(e1, s));
+  OP_CUDA(cudaEventSynchronize(e1));
+  float ms = 0.f;
+  OP_CUDA(cudaEventElapsedTime(&ms, e0, e1));
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  *us = ms * 1000.f / iters;
+  int h = 0;
+  OP_CUDA(cudaMemcpy(&h, err, 4, cudaMemcpyDeviceToHost));
+  if (h) return op_fail(PF_E_DEVICE_TIMEOUT, "GEMM gave up a bounded wait, code " + std::to_string(h));
+  return PF_OK;
+}
+
 extern "C" int pfop_linear_resid(int32_t wtype, const void* w_host, int32_t N, int32_t K, const void* a_dev,
                                  int32_t a_rows, int32_t M, float* x_dev, void* xb_dev, void* stream) {
   if (!w_host || !a_dev || !x_dev || N < 32 || N % 32 || M < 1 || M > a_rows) return op_fail(PF_E_ARG, "bad argument");
@@ -149,12 +196,13 @@ extern "C" int pfop_linear_glu(int32_t wtype, const void* wg_host, const void* w
   ActMat A;
   int rc;
   const size_t rb = rbytes(wtype, K);
+  const int bn = F % 128 == 0 ? 256 : 128, half = bn / 2;
   std::vector<const void*> rows;
-  for (int t = 0; t < F / 64; ++t) {
-    for (int i = 0; i < 64; ++i) rows.push_back(static_cast<const uint8_t*>(wg_host) + (t * 64 + i) * rb);
-    for (int i = 0; i < 64; ++i) rows.push_back(static_cast<const uint8_t*>(wu_host) + (t * 64 + i) * rb);
+  for (int t = 0; t < F / half; ++t) {
+    for (int i = 0; i < half; ++i) rows.push_back(static_cast<const uint8_t*>(wg_host) + (t * half + i) * rb);
+    for (int i = 0; i < half; ++i) rows.push_back(static_cast<const uint8_t*>(wu_host) + (t * half + i) * rb);
   }
-  if ((rc = make_weight(sc, W, wtype, rows, K, 128))) return rc;
+  if ((rc = make_weight(sc, W, wtype, rows, K, bn))) return rc;
   if ((rc = make_act(A, a_dev, a_rows, K))) return rc;
   EpiParams e;
   e.kind = EPI_GLU;

@@ -12,6 +12,7 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -123,6 +124,7 @@ int build_weight(prefill_ctx* c, WeightMat& w, const std::vector<const void*>& r
   w.BN = BN;
   w.N_rows = static_cast<int>(rows.size());
   if (w.N_rows % BN != 0 || K % 64 != 0) return fail(c, PF_E_ARG, "weight shape not tileable");
+  w.split = choose_split(c->d.wtype == PF_W_Q4_0 ? W_Q4 : W_BF16, w.N_rows, BN, K, c->d.ubatch_max);
   std::string err;
   if (c->d.wtype == PF_W_Q4_0) {
     w.kind = W_Q4;
@@ -274,14 +276,15 @@ extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weig
     if ((rc = build_weight(C, L.o, plain_rows(lw.wo, C->D, C->q, wt, 128), C->q, 128)))
       return fail(nullptr, rc, C->last_error);
     {
-      // gate/up interleaved per 128-row tile: 64 gate rows, then the same 64 up rows
+      // gate/up interleaved per tile: BN/2 gate rows, then the same BN/2 up rows
+      const int bn = C->F % 128 == 0 ? 256 : 128, half = bn / 2;
       const size_t rb = row_bytes(wt, C->D);
       std::vector<const void*> rows;
-      for (int t = 0; t < C->F / 64; ++t) {
-        for (int i = 0; i < 64; ++i) rows.push_back(static_cast<const uint8_t*>(lw.w_gate) + (t * 64 + i) * rb);
-        for (int i = 0; i < 64; ++i) rows.push_back(static_cast<const uint8_t*>(lw.w_up) + (t * 64 + i) * rb);
+      for (int t = 0; t < C->F / half; ++t) {
+        for (int i = 0; i < half; ++i) rows.push_back(static_cast<const uint8_t*>(lw.w_gate) + (t * half + i) * rb);
+        for (int i = 0; i < half; ++i) rows.push_back(static_cast<const uint8_t*>(lw.w_up) + (t * half + i) * rb);
       }
-      if ((rc = build_weight(C, L.gu, rows, C->D, 128))) return fail(nullptr, rc, C->last_error);
+      if ((rc = build_weight(C, L.gu, rows, C->D, bn))) return fail(nullptr, rc, C->last_error);
     }
     if ((rc = build_weight(C, L.down, plain_rows(lw.w_down, C->D, C->F, wt, 128), C->F, 128)))
       return fail(nullptr, rc, C->last_error);
