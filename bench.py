@@ -1,0 +1,404 @@
+#!/usr/bin/env python3
+"""Prompt-prefill benchmark of the KV-shared library on GB300.
+
+Workload: the E2B-shaped synthetic model (24 layers, layers 16-23 KV-shared,
+d_model 1536, 8/1 heads of 256, GeGLU 6144, vocab 32768, per-layer embedding
+256, Q4_0 weights drawn from seed 0) prefilling one sequence of 512 random
+tokens (seed 1) in one ubatch, with the KV-shared row pruning on.  A "step" is
+one whole prefill pass of that prompt (every layer, the pruning, the head)
+from tokens resident in device memory to the last row's logits.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the
+same workload instead.  Multi-GPU runs are independent replicas (one
+sequence per GPU, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill tokens/s (1 seq) at 512/2048/8192 prompt, pruning on vs off, % roofline"
+UNIT = "tokens/s"
+WORKLOAD = "e2b-512"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sweep-steps", type=int, default=5)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: barrier + max of the timings only)
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if os.environ.get("PREFILL_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append((time.time(), ln.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.t:
+                self.t.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ts, ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1] or rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (cpu_baseline and the reference arm)
+
+
+def oracle_rate(cfg, weights, tokens, budget_s: float, min_steps: int = 1, warm: bool = True):
+    """Tokens/s of the oracle's pruned prefill of `tokens`, timed on the host
+    cores for at least min_steps passes and about budget_s seconds."""
+    import numpy as np
+    from oracle.prefill import OracleContext
+    ctx = OracleContext(cfg, weights, len(tokens))
+    if warm:  # decodes and caches the weights
+        ctx.prefill(tokens, 512, prune=True)
+        ctx.reset()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        ctx.reset()
+        out = ctx.prefill(tokens, 512, prune=True)
+        n += 1
+        el = time.perf_counter() - t0
+        if n >= min_steps and el >= budget_s:
+            break
+    assert np.isfinite(out).all()
+    return n * len(tokens) / el, el / n, n
+
+
+def cpu_threads() -> int:
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(k, "").isdigit():
+            return int(os.environ[k])
+    return os.cpu_count() or 1
+
+
+def run_reference(args, dist: Dist):
+    """The oracle on the host cores.  A step is one pruned prefill pass over a
+    prompt sample: the whole 512-token prompt when K such passes fit in about
+    two minutes, else its first S tokens with S sized to fit."""
+    if dist.rank != 0:
+        return
+    from oracle.prefill import OracleContext
+    from prefill_kv_shared_gb300 import synth
+    cfg = synth.config("e2b")
+    w = synth.make_weights(cfg)
+    tok = synth.make_tokens(cfg, 512)
+    ctx = OracleContext(cfg, w, 512)
+    t0 = time.perf_counter()
+    ctx.prefill(tok, 512, prune=True)  # decodes and caches the weights
+    ctx.reset()
+    t0 = time.perf_counter()
+    ctx.prefill(tok, 512, prune=True)
+    t512 = time.perf_counter() - t0
+    budget = 120.0
+    S = 512 if args.steps * t512 <= budget else max(16, int(512 * budget / (args.steps * t512)))
+    sample = tok[:S]
+    for _ in range(args.warmup):
+        ctx.reset()
+        ctx.prefill(sample, 512, prune=True)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ctx.reset()
+        ctx.prefill(sample, 512, prune=True)
+    el = time.perf_counter() - t0
+    value = args.steps * S / el
+    cores = cpu_threads()
+    desc = (f"{args.steps} pruned prefill passes over the first {S} tokens of the 512-token prompt"
+            + ("" if S == 512 else f" (a full 512-token pass takes {t512:.2f} s)"))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "prompt": 512, "prompt_sample": S, "ubatch": 512, "pruning": True,
+                   "program": "numpy fp32 oracle (CPU)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+
+def run_ours(args, dist: Dist):
+    import numpy as np
+    import torch
+
+    from prefill_kv_shared_gb300 import binding, synth
+
+    torch.cuda.set_device(dist.local)
+    dev = torch.device("cuda", dist.local)
+    binding.load()
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
+    cfg = synth.config("e2b")
+    w = synth.make_weights(cfg)
+    N, UB = 512, 512
+    tok_host = synth.make_tokens(cfg, N)
+    tok = torch.from_numpy(tok_host).to(dev)
+    ctx = binding.PrefillContext(w, max_ctx=N, ubatch_max=UB, prune=True, stream=stream)
+    logits = torch.empty(cfg["vocab"], dtype=torch.float32, device=dev)
+
+    def step():
+        ctx.reset()
+        ctx.ubatch(tok, 0, True, logits)
+
+    clocks = ClockSampler(dist.local)
+    clocks.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
+    ctx.sync()
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    ctx.sync()
+    dist.barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    time.sleep(0.25)
+    clocks.stop()
+    ms = dist.max(ms)
+    value = dist.world * N / (ms * 1e-3)
+    clk = clocks.summary(t_wall0 - 0.3, t_wall1 + 0.3)
+
+    # the same steps again with CUDA events around every launch: per-class
+    # device time and algorithmic work
+    ctx.reset_stats()
+    ctx.set_timing(True)
+    for _ in range(args.steps):
+        step()
+    st = ctx.stats()
+    ctx.set_timing(False)
+    ctx.reset_stats()
+    launches_per_step = sum(v["launches"] for v in st.values()) / args.steps
+
+    peaks, peak_src = load_peaks()
+    g = st["gemm"]
+    gemm_ms_avg = g["ms"] / max(g["timed"], 1)
+    gemm_flops_avg = g["flops"] / max(g["launches"], 1)
+    achieved = gemm_flops_avg / (gemm_ms_avg * 1e-3) / 1e12 if gemm_ms_avg > 0 else None
+    peak = peaks["bf16_tflops_sustained"]
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "gemm_traffic_e2b512.json")
+    if os.path.exists(tr_path):
+        try:
+            traffic = json.load(open(tr_path)).get("dram_bytes_per_launch")
+        except (OSError, ValueError):
+            traffic = None
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": (achieved / peak) if achieved else None, "traffic": traffic,
+                "kernel": "gemm_tc_kernel (all projection/head launches of a step)",
+                "peak_source": f"{peak_src} bf16 sustained",
+                "classes": {k: {"launches_per_step": v["launches"] / args.steps,
+                                "ms_per_step": v["ms"] / args.steps,
+                                "tflops": (v["flops"] / (v["ms"] * 1e-3) / 1e12) if v["ms"] > 0 and v["flops"] > 0 else None,
+                                "gbs": (v["bytes"] / (v["ms"] * 1e-3) / 1e9) if v["ms"] > 0 else None}
+                            for k, v in st.items()}}
+    # whole-pass roofline: sum over classes of max(flops/P, bytes/BW)
+    ideal_ms = sum(max(v["flops"] / (peaks["bf16_tflops_sustained"] * 1e12),
+                       v["bytes"] / (peaks["hbm_gbs"] * 1e9)) for v in st.values()) * 1e3 / args.steps
+    roofline["pass_frac"] = ideal_ms / ms
+
+    # end to end through the C ABI with host buffers: tokens from pinned host
+    # memory each step, logits read back to pinned host memory each step
+    tok_pinned = torch.from_numpy(tok_host.copy()).pin_memory()
+    out_pinned = torch.empty(cfg["vocab"], dtype=torch.float32).pin_memory()
+    tok_np = tok_pinned.numpy()
+    for _ in range(3):
+        ctx.reset()
+        ctx.ubatch(tok_np, 0, True, logits)
+        out_pinned.copy_(logits, non_blocking=True)
+        torch.cuda.synchronize(dev)
+    dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ctx.reset()
+        ctx.ubatch(tok_np, 0, True, logits)
+        out_pinned.copy_(logits, non_blocking=True)
+        torch.cuda.synchronize(dev)
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    e2e_s = dist.max(e2e_s)
+    e2e = {"value": dist.world * N / e2e_s, "unit": UNIT, "h2d_bytes_per_step": N * 4,
+           "d2h_bytes_per_step": cfg["vocab"] * 4}
+    assert np.isfinite(out_pinned.numpy()).all()
+    ctx.close()
+
+    # pruning on/off at 512/2048/8192 (ubatches of 512), rank 0's GPU only
+    sweep = None
+    if not args.no_sweep and dist.rank == 0:
+        sweep = {}
+        big = binding.PrefillContext(w, max_ctx=8192, ubatch_max=UB, prune=True, stream=stream)
+        for n in (512, 2048, 8192):
+            t = torch.from_numpy(synth.make_tokens(cfg, n)).to(dev)
+            for prune in (True, False):
+                big.set_prune(prune)
+
+                def sweep_step():
+                    big.reset()
+                    for i in range(0, n, UB):
+                        big.ubatch(t[i:i + UB], i, i + UB >= n, logits)
+                sweep_step()
+                big.sync()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(args.sweep_steps):
+                    sweep_step()
+                b.record(stream)
+                torch.cuda.synchronize(dev)
+                sms = a.elapsed_time(b) / args.sweep_steps
+                sweep[f"{n}_{'on' if prune else 'off'}"] = {"ms": sms, "tokens_per_s": n / (sms * 1e-3)}
+            sweep[f"{n}_speedup"] = sweep[f"{n}_off"]["ms"] / sweep[f"{n}_on"]["ms"]
+        big.close()
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        rate, per, n = oracle_rate(cfg, w, tok_host, budget_s=10.0)
+        cpu = {"value": rate, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+               "sample": f"{n} pruned prefill passes of the same 512-token prompt ({per:.2f} s each), weights decoded once before timing"}
+
+    if dist.rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "model": "E2B-shaped synthetic, Q4_0 weights", "prompt": N,
+                       "ubatch": UB, "pruning": True, "global_batch": dist.world, "seq_len": N,
+                       "parallelism": f"replicas x{dist.world}",
+                       "l2": "inputs larger than L2 (488 MB of Q4_0 weights streamed every step)"},
+            "gpu_launches": int(round(launches_per_step * args.steps)),
+            "e2e": e2e, "roofline": roofline, "clocks": clk, "cpu_baseline": cpu, "sweep": sweep,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist)
+        else:
+            run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -160,6 +160,33 @@ int kv_save(prefill_ctx* ctx, void* dst, size_t dst_bytes);
    the caller's contract (the image stores no tokens). */
 int kv_load(prefill_ctx* ctx, const void* src, size_t src_bytes, int64_t n_pos);
 
+/* ---- launch accounting and per-class kernel timing ----
+   Every kernel the context launches is counted by class, with the
+   algorithmic work it does (FLOPs: 2*M*N*K for a projection, 4*hd per
+   (query head, visible key) for attention; bytes: what the step must move
+   at least).  With timing on, each launch is bracketed by CUDA events on
+   the context's stream (this adds host overhead; use it on a separate run
+   from throughput measurements). */
+#define PF_KC_GEMM 0  /* projections and the LM head (tcgen05) */
+#define PF_KC_ATTN 1  /* attention, chunk merge */
+#define PF_KC_NORM 2  /* RMSNorm (+ row gather) */
+#define PF_KC_OTHER 3 /* embedding gather, KV image copies */
+#define PF_KC_COUNT 4
+
+typedef struct prefill_stats {
+  int64_t launches[PF_KC_COUNT];
+  double flops[PF_KC_COUNT];
+  double bytes[PF_KC_COUNT];
+  int64_t timed[PF_KC_COUNT]; /* launches with event timing */
+  double ms[PF_KC_COUNT];     /* summed device time of the timed launches */
+} prefill_stats;
+
+int prefill_set_timing(prefill_ctx* ctx, int32_t enable);
+/* Waits for the stream when timing is on; fills *out with the totals since
+   the last prefill_reset_stats. */
+int prefill_get_stats(prefill_ctx* ctx, prefill_stats* out);
+int prefill_reset_stats(prefill_ctx* ctx);
+
 void prefill_destroy(prefill_ctx* ctx);
 
 const char* prefill_last_error(const prefill_ctx* ctx);

@@ -35,7 +35,7 @@ EXPORTS = (
     "prefill_create", "prefill_ubatch", "prefill_sync", "prefill_n_pos", "prefill_reset",
     "prefill_set_prune", "prefill_prune_active", "prefill_kv_image_bytes", "kv_save", "kv_load",
     "prefill_destroy", "prefill_last_error", "prefill_prune_predicate", "prefill_kv_header_check",
-    "prefill_kv_image_bytes_for",
+    "prefill_kv_image_bytes_for", "prefill_set_timing", "prefill_get_stats", "prefill_reset_stats",
     "pfop_linear_f32", "pfop_linear_resid", "pfop_linear_glu", "pfop_linear_ple", "pfop_linear_qkv",
     "pfop_attention", "pfop_rmsnorm", "pfop_embed", "pfop_kv_copy", "pfop_last_error", "pfop_linear_bench",
 )
@@ -57,6 +57,15 @@ class ModelDesc(C.Structure):
         ("ubatch_max", C.c_int32), ("prune_shared_enable", C.c_int32), ("n_seq_max", C.c_int32),
         ("embeddings", C.c_int32),
     ]
+
+
+KC_GEMM, KC_ATTN, KC_NORM, KC_OTHER = 0, 1, 2, 3
+KC_NAMES = ("gemm", "attention", "norm", "other")
+
+
+class Stats(C.Structure):
+    _fields_ = [("launches", C.c_int64 * 4), ("flops", C.c_double * 4), ("bytes", C.c_double * 4),
+                ("timed", C.c_int64 * 4), ("ms", C.c_double * 4)]
 
 
 class LayerWeights(C.Structure):
@@ -100,6 +109,9 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "prefill_prune_predicate": (C.c_int, [C.POINTER(ModelDesc)]),
         "prefill_kv_header_check": (C.c_int, [vp, i32, i32, i64, i64, sz]),
         "prefill_kv_image_bytes_for": (i64, [i32, i64, i32]),
+        "prefill_set_timing": (C.c_int, [vp, i32]),
+        "prefill_get_stats": (C.c_int, [vp, C.POINTER(Stats)]),
+        "prefill_reset_stats": (C.c_int, [vp]),
         "pfop_linear_f32": (C.c_int, [i32, vp, i32, i32, i32, vp, i32, i32, vp, vp]),
         "pfop_linear_resid": (C.c_int, [i32, vp, i32, i32, vp, i32, i32, vp, vp, vp]),
         "pfop_linear_glu": (C.c_int, [i32, vp, vp, i32, i32, i32, vp, i32, i32, vp, vp]),
@@ -260,6 +272,18 @@ class PrefillContext:
 
     def kv_load(self, src, nbytes: int, n_pos: int):
         self._check(self._lib.kv_load(self._h, _ptr(src), nbytes, n_pos))
+
+    def set_timing(self, enable: bool):
+        self._check(self._lib.prefill_set_timing(self._h, 1 if enable else 0))
+
+    def stats(self) -> dict:
+        st = Stats()
+        self._check(self._lib.prefill_get_stats(self._h, C.byref(st)))
+        return {name: dict(launches=st.launches[i], flops=st.flops[i], bytes=st.bytes[i],
+                           timed=st.timed[i], ms=st.ms[i]) for i, name in enumerate(KC_NAMES)}
+
+    def reset_stats(self):
+        self._check(self._lib.prefill_reset_stats(self._h))
 
     def close(self):
         if getattr(self, "_h", None):

@@ -229,6 +229,8 @@ __global__ void __launch_bounds__(NW * 32, 1) attn_prefill_kernel(AttnArgs a) {
   using S = ChunkSmem<HD>;
   using C = PrefillCfg<HD, NW>;
   extern __shared__ __align__(16) uint8_t smem[];
+  pdl_launch();
+  pdl_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tq = lane & 3;
   const int G = a.Hq / a.Hkv;
@@ -339,6 +341,8 @@ __global__ void __launch_bounds__(32) attn_split_kernel(AttnArgs a, float* __res
   using S = ChunkSmem<HD>;
   using C = SplitCfg<HD>;
   extern __shared__ __align__(16) uint8_t smem[];
+  pdl_launch();
+  pdl_wait();
   const int lane = threadIdx.x;
   const int g = lane >> 2, tq = lane & 3;
   const int ch = blockIdx.x, kvh = blockIdx.y;
@@ -388,6 +392,8 @@ template <int HD>
 __global__ void __launch_bounds__(32) attn_merge_kernel(const float* __restrict__ part, int n_chunks, int Hq,
                                                         __nv_bfloat16* __restrict__ out) {
   constexpr int PER = HD / 32;
+  pdl_launch();
+  pdl_wait();
   const int head = blockIdx.x, lane = threadIdx.x;
   const float* base = part + (size_t)head * n_chunks * (HD + 2);
   float m = -INFINITY, l = 0.f, o[PER];
@@ -430,8 +436,7 @@ static cudaError_t launch_prefill_t(const AttnArgs& a, cudaStream_t s) {
   const int G = a.Hq / a.Hkv;
   const int rows = a.M * G;
   dim3 grid((rows + C::ROWS - 1) / C::ROWS, a.Hkv);
-  attn_prefill_kernel<HD, NW><<<grid, NW * 32, C::SMEM, s>>>(a);
-  return cudaGetLastError();
+  return launch_k(attn_prefill_kernel<HD, NW>, grid, dim3(NW * 32), C::SMEM, s, 1, a);
 }
 
 static bool attn_shape_ok(const AttnArgs& a) {
@@ -459,11 +464,10 @@ static cudaError_t launch_split_t(const AttnArgs& a, float* part, cudaStream_t s
     attr = true;
   }
   const int n_chunks = a.pos_base / CHUNK + 1;
-  attn_split_kernel<HD><<<dim3(n_chunks, a.Hkv), 32, C::SMEM, s>>>(a, part, n_chunks);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_k(attn_split_kernel<HD>, dim3(n_chunks, a.Hkv), dim3(32), C::SMEM, s, 1, a, part, n_chunks);
   if (e != cudaSuccess) return e;
-  attn_merge_kernel<HD><<<a.Hq, 32, 0, s>>>(part, n_chunks, a.Hq, a.out);
-  return cudaGetLastError();
+  return launch_k(attn_merge_kernel<HD>, dim3(a.Hq), dim3(32), 0, s, 1, static_cast<const float*>(part), n_chunks,
+                  a.Hq, a.out);
 }
 
 cudaError_t launch_attn_split(const AttnArgs& a, float* part, cudaStream_t s) {

@@ -1,7 +1,7 @@
 // Device helpers shared by the sm_103a kernels: mbarriers, TMA bulk copies,
 // tcgen05 (TMEM alloc / MMA / commit / load), proxy fences and bounded waits.
 //
-// Every wait on an mbarrier is bounded in time: after PF_WAIT_NS nanoseconds
+// Every wait on an mbarrier is bounded in time: after about 2 s of SM cycles
 // (or as soon as another thread has flagged an error) the wait gives up,
 // records an error code in the context's device error word and returns false.
 // Kernels never trap.
@@ -10,7 +10,11 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <cstdlib>
+#include <utility>
 
 namespace pf {
 
@@ -23,10 +27,6 @@ enum : int {
   PF_DEV_TIMEOUT_EPILOGUE = 4,
   PF_DEV_BAD_TOKEN = 5,
 };
-
-#ifndef PF_WAIT_NS
-#define PF_WAIT_NS 2000000000ull  // 2 s
-#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -44,6 +44,49 @@ __device__ __forceinline__ void set_error(int* err, int code) {
 
 __device__ __forceinline__ int read_error(const int* err) {
   return err ? *(volatile const int*)err : 0;
+}
+
+// ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel lets the next one in the stream be
+// scheduled as soon as it starts (pdl_launch), and waits for the previous
+// one's completion and memory (pdl_wait) only before it touches data that
+// kernel produces or reads.
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+inline bool pdl_enabled() {
+  static const bool on = std::getenv("PREFILL_NO_PDL") == nullptr;
+  return on;
+}
+
+// cudaLaunchKernelEx with programmatic stream serialization (and an optional
+// cluster size)
+template <class... KArgs, class... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            int cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // ---------------------------------------------------------------------------
@@ -79,20 +122,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 }
 
 // Wait until the phase with the given parity has completed.  Bounded: returns
-// false (after flagging `code`) on timeout or when another thread has already
-// flagged an error.
+// false (after flagging `code`) when about PF_WAIT_CYCLES SM cycles have passed
+// or when another thread has already flagged an error.  The timeout and the
+// error word are looked at only every 4096 polls, so a wait that ends soon
+// costs nothing but the polls themselves.
+#ifndef PF_WAIT_CYCLES
+#define PF_WAIT_CYCLES 4000000000ll  // about 2 s
+#endif
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  long long t0 = 0;
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(a, parity)) return true;
-    if ((i & 255u) == 0u) {
-      if (read_error(err) != 0) return false;
-      if (globaltimer_ns() - t0 > PF_WAIT_NS) {
+    if ((i & 4095u) == 0u) {
+      const long long now = clock64();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > PF_WAIT_CYCLES) {
         set_error(err, code);
         return false;
       }
+      if (read_error(err) != 0) return false;
     }
   }
 }

@@ -252,9 +252,9 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m, bool ro
 // (bounded in time, ignoring the error flag).
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
-  const uint64_t t0 = globaltimer_ns();
+  const long long t0 = clock64();
   while (!mbar_try_wait(a, parity)) {
-    if (globaltimer_ns() - t0 > 200000000ull) return;
+    if (clock64() - t0 > 400000000ll) return;  // about 0.2 s
   }
 }
 
@@ -343,9 +343,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   bool epi_ok = true;
+  pdl_launch();
 
   if (warp == 0) {
     // ---------------- producer
+    // Weights do not depend on the previous kernel: the first raw stages are
+    // fetched before waiting for it.
+    uint32_t pre = 0;
+    if (C::Q4 && lane == 0 && blockIdx.x < sh.n_units) {
+      const int u = blockIdx.x;
+      const int ks = u % sh.splits, t = u / sh.splits;
+      const int nt = t % sh.n_tiles;
+      pre = nkb < C::S_R ? nkb : C::S_R;
+      for (uint32_t x = 0; x < pre; ++x) {
+        mbar_arrive_expect_tx(&full_r[x], C::RAW_BYTES);
+        bulk_load(r_ring + x * C::RAW_BYTES,
+                  wq4 + ((size_t)nt * (sh.splits * nkb) + ks * nkb + x) * C::RAW_BYTES, C::RAW_BYTES, &full_r[x]);
+      }
+    }
+    pre = __shfl_sync(0xffffffffu, pre, 0);
+    pdl_wait();
     uint32_t g = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < sh.n_units && ok; u += gridDim.x) {
@@ -358,7 +375,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int kb = ks * nkb + i;
         const int sa = g % C::S_A;
         if (lane == 0) ok = mbar_wait(&empty_a[sa], ((g / C::S_A) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
-        if (C::Q4 && lane == 0 && ok)
+        if (C::Q4 && lane == 0 && ok && g >= pre)
           ok = mbar_wait(&empty_r[g % C::S_R], ((g / C::S_R) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
@@ -367,12 +384,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           mbar_arrive_expect_tx(&full_a[sa], mt_valid * 128 * 128 + (C::Q4 ? 0 : C::BT_BYTES));
           for (int mt = 0; mt < mt_valid; ++mt)
             tma_load_2d(st + mt * 128 * 128, &tmA, &full_a[sa], kb * 64, m_base + mt * 128);
-          if (C::Q4) {
+          if (C::Q4 && g >= pre) {
             const int sr = g % C::S_R;
             mbar_arrive_expect_tx(&full_r[sr], C::RAW_BYTES);
             bulk_load(r_ring + sr * C::RAW_BYTES,
                       wq4 + ((size_t)nt * (sh.splits * nkb) + kb) * C::RAW_BYTES, C::RAW_BYTES, &full_r[sr]);
-          } else {
+          } else if (!C::Q4) {
             tma_load_2d(st + C::A_BYTES, &tmB, &full_a[sa], kb * 64, nt * BN);
           }
         }
@@ -444,6 +461,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     __syncwarp();
   } else if (warp < DQ_WARP0) {
     // ---------------- epilogue
+    pdl_wait();
     const int qw = warp & 3;  // TMEM lane quarter this warp may access
     const int r = 32 * qw + lane;
     uint32_t j = 0;
@@ -678,26 +696,10 @@ static cudaError_t launch_t(const ActMat& A, int M, const WeightMat& W, const Ep
   sh.n_units = sh.n_tiles * sh.m_blocks * sh.splits;
   if (W.split > 1 && static_cast<size_t>(W.split - 1) * 128 * BN * 4 > ring_bytes<WK, BN, MT>())
     return cudaErrorInvalidValue;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(GEMM_THREADS);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
-  cfg.stream = s;
-  if (W.split > 1) {
-    // one unit per CTA, the W.split k-ranges of a tile in one cluster
-    cfg.gridDim = dim3(sh.n_units);
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = W.split;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  } else {
-    cfg.gridDim = dim3(sh.n_units < sm_count() ? sh.n_units : sm_count());
-    cfg.numAttrs = 0;
-  }
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<WK, BN, MT>, A.tmap, W.tmap, static_cast<const uint8_t*>(W.dev), sh,
-                            ep, err);
+  const int cluster = W.split > 1 ? W.split : 1;
+  const int grid = W.split > 1 ? sh.n_units : (sh.n_units < sm_count() ? sh.n_units : sm_count());
+  return launch_k(gemm_tc_kernel<WK, BN, MT>, dim3(grid), dim3(GEMM_THREADS), C::SMEM_BYTES, s, cluster, A.tmap,
+                  W.tmap, static_cast<const uint8_t*>(W.dev), sh, ep, err);
 }
 
 cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err, cudaStream_t s) {

@@ -32,6 +32,8 @@ __device__ __forceinline__ void decode_q4_block(const uint8_t* blk, float (&out)
 }
 
 __global__ void __launch_bounds__(128) embed_kernel(EmbedArgs a) {
+  pdl_launch();
+  pdl_wait();
   const int t = blockIdx.x;
   int tok = a.tok[t];
   if (tok < 0 || tok >= a.vocab) {
@@ -87,8 +89,7 @@ __global__ void __launch_bounds__(128) embed_kernel(EmbedArgs a) {
 cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t s) {
   if (a.T <= 0) return cudaSuccess;
   if (a.D % 32 != 0 || a.LP % 32 != 0) return cudaErrorInvalidValue;
-  embed_kernel<<<a.T, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_k(embed_kernel, dim3(a.T), dim3(128), 0, s, 1, a);
 }
 
 // ---------------------------------------------------------------------------
@@ -101,6 +102,8 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(const float* __re
                                                                __nv_bfloat16* __restrict__ y,
                                                                float* __restrict__ x_copy) {
   __shared__ float red[NORM_THREADS / 32];
+  pdl_launch();
+  pdl_wait();
   const int i = blockIdx.x;
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)(row0 + i) * D);
   const int nv = D / 4;
@@ -139,8 +142,7 @@ cudaError_t launch_rmsnorm(const float* x, int row0, int M, int D, const float* 
                            float* x_copy, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
   if (D % 4 != 0) return cudaErrorInvalidValue;
-  rmsnorm_kernel<<<M, NORM_THREADS, 0, s>>>(x, row0, D, g, eps, y, x_copy);
-  return cudaGetLastError();
+  return launch_k(rmsnorm_kernel, dim3(M), dim3(NORM_THREADS), 0, s, 1, x, row0, D, g, eps, y, x_copy);
 }
 
 // ---------------------------------------------------------------------------
@@ -159,6 +161,8 @@ __device__ __forceinline__ void kv_vec_index(int64_t v, int64_t copy_vec, int64_
 __global__ void __launch_bounds__(256) kv_copy_kernel(int dir, uint4* __restrict__ cache, int64_t cache_stride_vec,
                                                       uint8_t* __restrict__ image, int64_t img_stride_vec,
                                                       int64_t copy_vec, int64_t n_vec, int4 header) {
+  pdl_launch();
+  pdl_wait();
   if (dir == 0 && blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int4*>(image) = header;
   uint4* body = reinterpret_cast<uint4*>(image + 16);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -206,9 +210,9 @@ cudaError_t launch_kv_copy(int dir, __half* cache, int64_t cache_seg_stride, uin
   int64_t blocks = (n_vec + 255) / 256;
   const int64_t cap = (int64_t)sms * 8;
   if (blocks > cap) blocks = cap;
-  kv_copy_kernel<<<(unsigned)blocks, 256, 0, s>>>(dir, reinterpret_cast<uint4*>(cache), cache_seg_stride / 8, image,
-                                                  img_seg_bytes / 16, copy_vec, n_vec, h);
-  return cudaGetLastError();
+  return launch_k(kv_copy_kernel, dim3((unsigned)blocks), dim3(256), 0, s, 1, dir, reinterpret_cast<uint4*>(cache),
+                  static_cast<int64_t>(cache_seg_stride / 8), image, static_cast<int64_t>(img_seg_bytes / 16), copy_vec,
+                  n_vec, h);
 }
 
 }  // namespace pf

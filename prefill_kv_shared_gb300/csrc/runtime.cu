@@ -70,6 +70,16 @@ struct prefill_ctx {
   int64_t n_pos = 0;
   int prune_enable = 1;
   std::string last_error;
+
+  // launch accounting
+  prefill_stats stats{};
+  bool timing = false;
+  struct Timed {
+    int kc;
+    cudaEvent_t e0, e1;
+  };
+  std::vector<Timed> timed;
+  std::vector<cudaEvent_t> event_pool;
 };
 
 namespace {
@@ -210,6 +220,44 @@ int check_device_error(prefill_ctx* c) {
   PF_CUDA(c, cudaMemset(c->err, 0, sizeof(int)));
   if (e == PF_DEV_BAD_TOKEN) return fail(c, PF_E_DEVICE_TOKEN, "a token id was outside [0, vocab)");
   return fail(c, PF_E_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (code " + std::to_string(e) + ")");
+}
+
+cudaEvent_t take_event(prefill_ctx* c) {
+  if (!c->event_pool.empty()) {
+    cudaEvent_t e = c->event_pool.back();
+    c->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Launch one step's kernel(s) through `fn`, counting them (n kernels) and
+// their algorithmic work; with timing on, bracket them with events.
+template <class F>
+cudaError_t counted(prefill_ctx* c, int kc, int n, double flops, double bytes, F&& fn) {
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (c->timing) {
+    e0 = take_event(c);
+    e1 = take_event(c);
+    cudaEventRecord(e0, c->stream);
+  }
+  const cudaError_t e = fn();
+  if (c->timing) {
+    cudaEventRecord(e1, c->stream);
+    c->timed.push_back({kc, e0, e1});
+  }
+  if (e == cudaSuccess) {
+    c->stats.launches[kc] += n;
+    c->stats.flops[kc] += flops;
+    c->stats.bytes[kc] += bytes;
+  }
+  return e;
+}
+
+double gemm_wbytes(const prefill_ctx* c, double n, double k) {
+  return c->d.wtype == PF_W_Q4_0 ? n * k * 18.0 / 32.0 : n * k * 4.0;
 }
 
 }  // namespace
@@ -356,9 +404,47 @@ extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weig
   return PF_OK;
 }
 
+extern "C" int prefill_set_timing(prefill_ctx* c, int32_t enable) {
+  if (!c) return fail(nullptr, PF_E_ARG, "null context");
+  c->timing = enable != 0;
+  return PF_OK;
+}
+
+extern "C" int prefill_get_stats(prefill_ctx* c, prefill_stats* out) {
+  if (!c || !out) return fail(c, PF_E_ARG, "null argument");
+  if (!c->timed.empty()) {
+    PF_CUDA(c, cudaStreamSynchronize(c->stream));
+    for (auto& t : c->timed) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, t.e0, t.e1) == cudaSuccess) {
+        c->stats.ms[t.kc] += ms;
+        c->stats.timed[t.kc] += 1;
+      }
+      c->event_pool.push_back(t.e0);
+      c->event_pool.push_back(t.e1);
+    }
+    c->timed.clear();
+  }
+  *out = c->stats;
+  return PF_OK;
+}
+
+extern "C" int prefill_reset_stats(prefill_ctx* c) {
+  if (!c) return fail(nullptr, PF_E_ARG, "null context");
+  prefill_stats tmp;
+  prefill_get_stats(c, &tmp);
+  c->stats = prefill_stats{};
+  return PF_OK;
+}
+
 extern "C" void prefill_destroy(prefill_ctx* c) {
   if (!c) return;
   cudaStreamSynchronize(c->stream);
+  for (auto& t : c->timed) {
+    cudaEventDestroy(t.e0);
+    cudaEventDestroy(t.e1);
+  }
+  for (cudaEvent_t e : c->event_pool) cudaEventDestroy(e);
   for (void* p : c->allocs) cudaFree(p);
   delete c;
 }
@@ -404,7 +490,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
   ea.ple_scale = c->P > 0 ? static_cast<float>(1.0 / std::sqrt(static_cast<double>(c->P))) : 1.0f;
   ea.ple = c->ple;
   ea.err = c->err;
-  PF_CUDA(c, launch_embed(ea, s));
+  PF_CUDA(c, counted(c, PF_KC_OTHER, 1, 0.0, T * (4.0 + D * 4.0 + LP * 2.0), [&] { return launch_embed(ea, s); }));
 
   float* xcur = c->x;
   int M = T;
@@ -421,14 +507,18 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
         break;
       }
       // keep the output row only: gather it inside the norm
-      PF_CUDA(c, launch_rmsnorm(c->x, T - 1, 1, D, W.attn_norm, c->d.rms_eps, c->y, c->xr, s));
+      PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, D * 10.0, [&] {
+                 return launch_rmsnorm(c->x, T - 1, 1, D, W.attn_norm, c->d.rms_eps, c->y, c->xr, s);
+               }));
       xcur = c->xr;
       M = 1;
       pos_base = static_cast<int>(pos0) + T - 1;
       ple_view = c->ple + static_cast<size_t>(T - 1) * LP;
       gathered = true;
     } else {
-      PF_CUDA(c, launch_rmsnorm(xcur, 0, M, D, W.attn_norm, c->d.rms_eps, c->y, nullptr, s));
+      PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, M * D * 6.0, [&] {
+                 return launch_rmsnorm(xcur, 0, M, D, W.attn_norm, c->d.rms_eps, c->y, nullptr, s);
+               }));
     }
     const bool writes = il < S;
     const int src = writes ? il : c->kv_src[il];
@@ -443,7 +533,9 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.rope = c->rope;
       e.k_cache = c->cache + static_cast<size_t>(il) * seg;
       e.v_cache = c->cache + static_cast<size_t>(c->L_w + il) * seg;
-      PF_CUDA(c, launch_gemm(c->a_y, M, W.qkv, e, c->err, s));
+      const double n_out = c->q + 2.0 * e.kv_dim;
+      PF_CUDA(c, counted(c, PF_KC_GEMM, 1, 2.0 * M * n_out * D, M * D * 2.0 + gemm_wbytes(c, n_out, D) + M * n_out * 2.0,
+                         [&] { return launch_gemm(c->a_y, M, W.qkv, e, c->err, s); }));
     }
     {
       AttnArgs a;
@@ -457,10 +549,15 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       a.hd = c->hd;
       a.pos_base = pos_base;
       a.kv_len = kv_len;
+      // (query head, visible key) pairs: rows at positions pos_base .. pos_base+M-1
+      const double pairs = static_cast<double>(M) * pos_base + 0.5 * M * (M + 1.0);
+      const double aflops = pairs * c->Hq * 4.0 * c->hd;
       if (gathered)
-        PF_CUDA(c, launch_attn_split(a, c->partials, s));
+        PF_CUDA(c, counted(c, PF_KC_ATTN, 2, aflops, kv_len * c->kv * 4.0 + M * c->q * 4.0,
+                           [&] { return launch_attn_split(a, c->partials, s); }));
       else
-        PF_CUDA(c, launch_attn_prefill(a, s));
+        PF_CUDA(c, counted(c, PF_KC_ATTN, 1, aflops, kv_len * c->kv * 4.0 + M * c->q * 4.0,
+                           [&] { return launch_attn_prefill(a, s); }));
     }
     {
       EpiParams e;
@@ -468,9 +565,12 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.N = D;
       e.out_f32 = xcur;
       e.ld_f32 = D;
-      PF_CUDA(c, launch_gemm(c->a_att, M, W.o, e, c->err, s));
+      PF_CUDA(c, counted(c, PF_KC_GEMM, 1, 2.0 * M * D * c->q, M * c->q * 2.0 + gemm_wbytes(c, D, c->q) + M * D * 8.0,
+                         [&] { return launch_gemm(c->a_att, M, W.o, e, c->err, s); }));
     }
-    PF_CUDA(c, launch_rmsnorm(xcur, 0, M, D, W.ffn_norm, c->d.rms_eps, c->y, nullptr, s));
+    PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, M * D * 6.0, [&] {
+               return launch_rmsnorm(xcur, 0, M, D, W.ffn_norm, c->d.rms_eps, c->y, nullptr, s);
+             }));
     {
       EpiParams e;
       e.kind = EPI_GLU;
@@ -478,7 +578,8 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.out_bf16 = c->h;
       e.ld_bf16 = c->F;
       e.act = c->d.ffn_kind == PF_FFN_GEGLU ? 0 : 1;
-      PF_CUDA(c, launch_gemm(c->a_y, M, W.gu, e, c->err, s));
+      PF_CUDA(c, counted(c, PF_KC_GEMM, 1, 4.0 * M * c->F * D, M * D * 2.0 + gemm_wbytes(c, 2.0 * c->F, D) + M * c->F * 2.0,
+                         [&] { return launch_gemm(c->a_y, M, W.gu, e, c->err, s); }));
     }
     {
       EpiParams e;
@@ -490,7 +591,8 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
         e.out_bf16 = c->xb;
         e.ld_bf16 = D;
       }
-      PF_CUDA(c, launch_gemm(c->a_h, M, W.down, e, c->err, s));
+      PF_CUDA(c, counted(c, PF_KC_GEMM, 1, 2.0 * M * D * c->F, M * c->F * 2.0 + gemm_wbytes(c, D, c->F) + M * D * 8.0,
+                         [&] { return launch_gemm(c->a_h, M, W.down, e, c->err, s); }));
     }
     if (c->P > 0) {
       EpiParams e;
@@ -500,25 +602,30 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.ld_bf16 = c->P;
       e.ple = ple_view + static_cast<size_t>(il) * c->P;
       e.ple_stride = LP;
-      PF_CUDA(c, launch_gemm(c->a_xb, M, W.pg, e, c->err, s));
+      PF_CUDA(c, counted(c, PF_KC_GEMM, 1, 2.0 * M * c->P * D, M * D * 2.0 + gemm_wbytes(c, c->P, D) + M * c->P * 4.0,
+                         [&] { return launch_gemm(c->a_xb, M, W.pg, e, c->err, s); }));
       EpiParams r;
       r.kind = EPI_RESID;
       r.N = D;
       r.out_f32 = xcur;
       r.ld_f32 = D;
-      PF_CUDA(c, launch_gemm(c->a_pg, M, W.pp, r, c->err, s));
+      PF_CUDA(c, counted(c, PF_KC_GEMM, 1, 2.0 * M * D * c->P, M * c->P * 2.0 + gemm_wbytes(c, D, c->P) + M * D * 8.0,
+                         [&] { return launch_gemm(c->a_pg, M, W.pp, r, c->err, s); }));
     }
   }
   (void)stopped;
   if (is_last) {
     const int row = gathered ? 0 : T - 1;
-    PF_CUDA(c, launch_rmsnorm(xcur, row, 1, D, c->out_norm, c->d.rms_eps, c->y, nullptr, s));
+    PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, D * 6.0, [&] {
+               return launch_rmsnorm(xcur, row, 1, D, c->out_norm, c->d.rms_eps, c->y, nullptr, s);
+             }));
     EpiParams e;
     e.kind = EPI_F32;
     e.N = c->V;
     e.out_f32 = logits;
     e.ld_f32 = c->V;
-    PF_CUDA(c, launch_gemm(c->a_y, 1, c->head, e, c->err, s));
+    PF_CUDA(c, counted(c, PF_KC_GEMM, 1, 2.0 * c->V * D, D * 2.0 + gemm_wbytes(c, c->V, D) + c->V * 4.0,
+                       [&] { return launch_gemm(c->a_y, 1, c->head, e, c->err, s); }));
   }
   c->n_pos = kv_len;
   return PF_OK;
@@ -589,9 +696,11 @@ extern "C" int kv_save(prefill_ctx* c, void* dst, size_t dst_bytes) {
   const size_t seg_bytes = static_cast<size_t>(n) * c->kv * 2;
   const size_t cache_pitch = static_cast<size_t>(c->d.max_ctx) * c->kv * 2;
   if (is_device_ptr(dst)) {
-    PF_CUDA(c, launch_kv_copy(0, c->cache, static_cast<int64_t>(c->d.max_ctx) * c->kv, static_cast<uint8_t*>(dst),
-                              static_cast<int64_t>(seg_bytes), 2 * c->L_w, static_cast<int64_t>(seg_bytes), h4,
-                              c->stream));
+    PF_CUDA(c, counted(c, PF_KC_OTHER, 1, 0.0, 2.0 * seg_bytes * 2 * c->L_w, [&] {
+               return launch_kv_copy(0, c->cache, static_cast<int64_t>(c->d.max_ctx) * c->kv, static_cast<uint8_t*>(dst),
+                                     static_cast<int64_t>(seg_bytes), 2 * c->L_w, static_cast<int64_t>(seg_bytes), h4,
+                                     c->stream);
+             }));
   } else {
     std::memcpy(dst, h4, 16);
     if (seg_bytes > 0)
@@ -627,10 +736,12 @@ extern "C" int kv_load(prefill_ctx* c, const void* src, size_t src_bytes, int64_
   const size_t cache_pitch = static_cast<size_t>(c->d.max_ctx) * c->kv * 2;
   if (copy > 0) {
     if (dev) {
-      PF_CUDA(c, launch_kv_copy(1, c->cache, static_cast<int64_t>(c->d.max_ctx) * c->kv,
-                                const_cast<uint8_t*>(static_cast<const uint8_t*>(src)), static_cast<int64_t>(img_seg),
-                                2 * c->L_w, static_cast<int64_t>(copy), reinterpret_cast<const int32_t*>(hdr),
-                                c->stream));
+      PF_CUDA(c, counted(c, PF_KC_OTHER, 1, 0.0, 2.0 * copy * 2 * c->L_w, [&] {
+                 return launch_kv_copy(1, c->cache, static_cast<int64_t>(c->d.max_ctx) * c->kv,
+                                       const_cast<uint8_t*>(static_cast<const uint8_t*>(src)),
+                                       static_cast<int64_t>(img_seg), 2 * c->L_w, static_cast<int64_t>(copy),
+                                       reinterpret_cast<const int32_t*>(hdr), c->stream);
+               }));
     } else {
       PF_CUDA(c, cudaMemcpy2DAsync(c->cache, cache_pitch, static_cast<const uint8_t*>(src) + 16, img_seg, copy,
                                    2 * c->L_w, cudaMemcpyHostToDevice, c->stream));
