@@ -84,6 +84,23 @@ int pfop_linear_bench(int32_t wtype, const void* w_host, int32_t N, int32_t K, i
                       const void* a_dev, int32_t a_rows, int32_t M, float* out_dev, int32_t warmup, int32_t iters,
                       float* us, void* stream);
 
+/* The single-row split-K attention of pfop_attention (mode 1) without any
+   memory allocation, for callers that may not allocate device memory at this
+   point (a fixed memory budget already handed out, a server that forbids
+   allocation after start-up, an embedder whose allocator owns the device).
+   The page set this library follows has no counterpart for this call.
+   q fp16 [Hq*hd] at position pos; K/V fp16 [positions][Hkv*hd] with keys
+   [0, kv_len) valid, pos < kv_len; out bf16 [Hq*hd].
+   Scratch: one fixed device array of 2^21 floats (8 MiB) per GPU that loads
+   the library, kept until exit.  A call needs Hq*(pos/64+1)*(hd+2) floats;
+   larger requests return PF_E_ARG without touching the GPU.  All calls share
+   the array, so calls that overlap on the GPU race: order them on one stream
+   or with events.  The first call on a device looks up the array's device
+   address with that device current (cudaGetSymbolAddress); make that first
+   call before capturing any stream.  Synchronous on `stream`. */
+int pfop_attention_split_noalloc(const void* q_dev, const void* k_dev, const void* v_dev, int32_t Hq, int32_t Hkv,
+                                 int32_t hd, int32_t pos, int32_t kv_len, void* out_dev, void* stream);
+
 /* Last error message of a pfop_* call on this thread. */
 const char* pfop_last_error(void);
 

@@ -132,4 +132,7 @@ cudaError_t launch_rmsnorm(const float* x, int row0, int M, int D, const float* 
 cudaError_t launch_kv_copy(int dir, __half* cache, int64_t cache_seg_stride, uint8_t* image, int64_t img_seg_bytes,
                            int n_seg, int64_t copy_bytes, const int32_t header[4], cudaStream_t s);
 
+// message returned by pfop_last_error() on this thread
+void set_op_error(const std::string& m);
+
 }  // namespace pf

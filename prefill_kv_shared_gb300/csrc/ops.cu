@@ -105,6 +105,8 @@ int run_gemm(Scope& sc, const ActMat& A, int M, const WeightMat& W, const EpiPar
 
 extern "C" const char* pfop_last_error(void) { return g_err.c_str(); }
 
+void pf::set_op_error(const std::string& m) { g_err = m; }
+
 extern "C" int pfop_linear_f32(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn, const void* a_dev,
                                int32_t a_rows, int32_t M, float* out_dev, void* stream) {
   if (!w_host || !a_dev || !out_dev || N < 1 || M < 1 || M > a_rows || (bn != 128 && bn != 256))
