@@ -263,12 +263,21 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 // ---------------------------------------------------------------------------
 // small numerics shared by the epilogues
 
+// tanh from the SFU (tanh.approx.f32, relative error ~2^-11); the epilogues
+// that use it round their results to bf16 (2^-9) afterwards
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float gelu_tanh_f(float x) {
   const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
   const float k1 = 0.044715f;
-  return 0.5f * x * (1.0f + tanhf(k0 * (x + k1 * x * x * x)));
+  return 0.5f * x * (1.0f + tanh_fast(k0 * (x + k1 * x * x * x)));
 }
 
-__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+// x * sigmoid(x), with sigmoid(x) = (1 + tanh(x/2)) / 2
+__device__ __forceinline__ float silu_f(float x) { return 0.5f * x * (1.0f + tanh_fast(0.5f * x)); }
 
 }  // namespace pf

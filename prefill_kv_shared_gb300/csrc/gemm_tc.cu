@@ -15,11 +15,11 @@
 // Persistent CTAs (one per SM) walk work units (m-block, n-tile, k-split):
 //   warp 0      TMA / bulk-copy producer
 //   warp 1      TMEM allocation, MMA issue (one lane), commits
-//   warps 2..5  epilogue (one TMEM lane quarter each): TMEM -> registers ->
-//               fused epilogue -> global; TMEM accumulators are double
-//               buffered when they fit, so a unit's epilogue overlaps the
-//               next unit's main loop
-//   warps 6..13 Q4_0 -> bf16 dequant
+//   warps 2..9  epilogue (two per TMEM lane quarter, splitting the column
+//               chunks): TMEM -> registers -> fused epilogue -> global; TMEM
+//               accumulators are double buffered when they fit, so a unit's
+//               epilogue overlaps the next unit's main loop
+//   warps 10..11 Q4_0 -> bf16 dequant
 //
 // Split-K: a weight matrix may be cut into S k-ranges (S fixed per matrix
 // shape, never per M), run by the S CTAs of a thread-block cluster; ranks
@@ -41,9 +41,10 @@ namespace pf {
 
 constexpr int GEMM_WARPS = 14;
 constexpr int GEMM_THREADS = GEMM_WARPS * 32;
-constexpr int EPI_WARP0 = 2;
-constexpr int DQ_WARP0 = 6;
-constexpr int DQ_THREADS = 256;
+constexpr int EPI_WARP0 = 2;   // warps 2..9: epilogue, two per TMEM lane quarter
+constexpr int EPI_WARPS = 8;
+constexpr int DQ_WARP0 = 10;   // warps 10..13: Q4_0 dequant
+constexpr int DQ_THREADS = 128;
 constexpr int SMEM_LIMIT = 232448;
 
 __host__ __device__ constexpr int pow2_cols(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
@@ -55,8 +56,13 @@ struct GemmCfg {
   static constexpr int BT_BYTES = BN * 128;       // one bf16 B tile (BN rows x 64)
   static constexpr int RAW_BYTES = Q4 ? BN * 36 : 0;
   static constexpr int A_STAGE = A_BYTES + (Q4 ? 0 : BT_BYTES);
-  static constexpr int S_B = Q4 ? (BN >= 256 ? 2 : (BN >= 128 ? 3 : 4)) : 0;
-  static constexpr int S_R = Q4 ? (BN >= 256 ? 6 : 8) : 0;
+  // The dequantised B ring bounds how far the dequant warps run ahead of the
+  // MMAs (B stage k+S_B is written once the MMAs of stage k are done): deep
+  // for narrow tiles, at least 3 for wide ones; the A ring takes the rest.
+  static constexpr int S_B = Q4 ? (BN >= 256 ? 3 : 6) : 0;
+  static constexpr int S_R = Q4 ? (BN >= 256 ? 3 : 8) : 0;
+  static constexpr int NB = S_B > 0 ? S_B : 1;  // ring moduli (the rings are unused without Q4)
+  static constexpr int NR = S_R > 0 ? S_R : 1;
   static constexpr int RAW_RING = (S_R * RAW_BYTES + 1023) / 1024 * 1024;
   static constexpr int FIXED = S_B * BT_BYTES + RAW_RING + 1024 + 512;
   static constexpr int S_A_FIT = (SMEM_LIMIT - FIXED) / A_STAGE;
@@ -132,15 +138,17 @@ __device__ __forceinline__ void store32x16(void* dst, const uint32_t (&w)[16]) {
 
 // The fused epilogue for one row of one tile.  load(c, v) fills v with the 32
 // fp32 results of the tile's column chunk c (columns 32c .. 32c+31) for this
-// thread's row; it is called in a warp-uniform way.
+// thread's row; it is called in a warp-uniform way.  The two epilogue warps
+// of a lane quarter (ew = 0, 1) take alternate work items.
 template <int BN, class Load>
-__device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m, bool row_ok, int n_tile, Load&& load) {
+__device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m, bool row_ok, int n_tile, int ew,
+                                             Load&& load) {
   constexpr int NCH = BN / 32;
   const int n0 = n_tile * BN;
   float v[32], u[32];
   if (ep.kind == EPI_GLU) {
     constexpr int HALF_CH = NCH / 2;
-    for (int c = 0; c < HALF_CH; ++c) {
+    for (int c = ew; c < HALF_CH; c += 2) {
       load(c, v);
       load(c + HALF_CH, u);
       if (!row_ok) continue;
@@ -160,10 +168,12 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m, bool ro
     const int hd = ep.head_dim, half = hd / 2, pair_ch = half / 32;
     const int q_end = ep.q_dim, k_end = ep.q_dim + ep.kv_dim, v_end = ep.q_dim + 2 * ep.kv_dim;
     const int pos = ep.pos0 + m;
+    int item = 0;
     for (int c = 0; c < NCH; ++c) {
       const int n = n0 + 32 * c;
       if (n >= v_end) break;  // padding columns
       if (n >= k_end) {       // V: no rotation
+        if ((item++ & 1) != ew) continue;
         load(c, v);
         if (!row_ok) continue;
         uint32_t w[16];
@@ -176,17 +186,18 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m, bool ro
       const int rel = is_q ? n : n - q_end;
       const int i0 = rel % hd;
       if (i0 >= half) continue;  // handled together with its partner chunk
+      if ((item++ & 1) != ew) continue;
       load(c, v);
       load(c + pair_ch, u);
       if (!row_ok) continue;
       const int head = rel / hd;
-      const float2* cs = ep.rope + (size_t)pos * half + i0;
+      const float4* cs4 = reinterpret_cast<const float4*>(ep.rope + (size_t)pos * half + i0);
       uint32_t w1[16], w2[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const float2 c0 = cs[2 * j], c1 = cs[2 * j + 1];
-        w1[j] = pack_half2(v[2 * j] * c0.x - u[2 * j] * c0.y, v[2 * j + 1] * c1.x - u[2 * j + 1] * c1.y);
-        w2[j] = pack_half2(v[2 * j] * c0.y + u[2 * j] * c0.x, v[2 * j + 1] * c1.y + u[2 * j + 1] * c1.x);
+        const float4 c01 = cs4[j];  // (cos, sin) of columns 2j and 2j+1
+        w1[j] = pack_half2(v[2 * j] * c01.x - u[2 * j] * c01.y, v[2 * j + 1] * c01.z - u[2 * j + 1] * c01.w);
+        w2[j] = pack_half2(v[2 * j] * c01.y + u[2 * j] * c01.x, v[2 * j + 1] * c01.w + u[2 * j + 1] * c01.z);
       }
       __half* dst = is_q ? ep.q_out + (size_t)m * ep.q_dim + head * hd
                          : ep.k_cache + (size_t)pos * ep.kv_dim + head * hd;
@@ -195,12 +206,26 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m, bool ro
     }
     return;
   }
-  // F32, RESID, PLE: one 32-column chunk at a time
-  for (int c = 0; c < NCH; ++c) {
+  // F32, RESID, PLE: one 32-column chunk at a time; the chunk's global
+  // operands are requested before its TMEM load
+  auto fetch = [&](int c, float4 (&g)[8]) {
     const int n = n0 + 32 * c;
-    if (n >= ep.N) break;
+    if (!row_ok || n >= ep.N) return;
+    if (ep.kind == EPI_RESID) {
+      const float4* xr = reinterpret_cast<const float4*>(ep.out_f32 + (size_t)m * ep.ld_f32 + n);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) g[j] = xr[j];
+    } else if (ep.kind == EPI_PLE) {
+      const float4* pl = reinterpret_cast<const float4*>(ep.ple + (size_t)m * ep.ple_stride + n);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) g[j] = pl[j];
+    }
+  };
+  auto finish = [&](int c, float4 (&g)[8]) {
+    const int n = n0 + 32 * c;
+    if (n >= ep.N) return;
     load(c, v);
-    if (!row_ok) continue;
+    if (!row_ok) return;
     const bool full = n + 32 <= ep.N;
     if (ep.kind == EPI_F32) {
       float* dst = ep.out_f32 + (size_t)m * ep.ld_f32 + n;
@@ -212,10 +237,10 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m, bool ro
         for (int j = 0; j < 32 && n + j < ep.N; ++j) dst[j] = v[j];
       }
     } else if (ep.kind == EPI_RESID) {
-      float* xr = ep.out_f32 + (size_t)m * ep.ld_f32 + n;
+      float4* xr = reinterpret_cast<float4*>(ep.out_f32 + (size_t)m * ep.ld_f32 + n);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        float4 x4 = reinterpret_cast<const float4*>(xr)[j];
+        float4 x4 = g[j];
         x4.x += v[4 * j];
         x4.y += v[4 * j + 1];
         x4.z += v[4 * j + 2];
@@ -224,7 +249,7 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m, bool ro
         v[4 * j + 1] = x4.y;
         v[4 * j + 2] = x4.z;
         v[4 * j + 3] = x4.w;
-        reinterpret_cast<float4*>(xr)[j] = x4;
+        xr[j] = x4;
       }
       if (ep.out_bf16) {
         uint32_t w[16];
@@ -232,16 +257,23 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m, bool ro
         for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
         store32x16(ep.out_bf16 + (size_t)m * ep.ld_bf16 + n, w);
       }
-    } else {  // EPI_PLE
-      const __nv_bfloat16* pl = ep.ple + (size_t)m * ep.ple_stride + n;
+    } else {  // EPI_PLE: g holds 32 bf16 multipliers in g[0..3]
       uint32_t w[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const __nv_bfloat162 p2 = reinterpret_cast<const __nv_bfloat162*>(pl)[j];
-        w[j] = pack_bf16x2(gelu_tanh_f(v[2 * j]) * __low2float(p2), gelu_tanh_f(v[2 * j + 1]) * __high2float(p2));
+        const float4 q = g[j >> 2];
+        const float qf = (j & 3) == 0 ? q.x : (j & 3) == 1 ? q.y : (j & 3) == 2 ? q.z : q.w;
+        const uint32_t pw = __float_as_uint(qf);
+        const float plo = __uint_as_float(pw << 16), phi = __uint_as_float(pw & 0xFFFF0000u);  // bf16 -> f32
+        w[j] = pack_bf16x2(gelu_tanh_f(v[2 * j]) * plo, gelu_tanh_f(v[2 * j + 1]) * phi);
       }
       store32x16(ep.out_bf16 + (size_t)m * ep.ld_bf16 + n, w);
     }
+  };
+  for (int c = ew; c < NCH; c += 2) {
+    float4 g[8];
+    fetch(c, g);
+    finish(c, g);
   }
 }
 
@@ -291,9 +323,21 @@ __device__ __forceinline__ uint32_t slot_off(int c, int r, int q) {
 template <int WK, int BN, int MT>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const uint8_t* __restrict__ wq4, const __grid_constant__ GemmShape sh,
-                   const __grid_constant__ EpiParams ep, int* err) {
+                   const uint8_t* __restrict__ wq4, const GemmShape sh_in, const EpiParams ep_in, int* err) {
   using C = GemmCfg<WK, BN, MT>;
+  // The launch parameters are read from shared-memory copies: fields of a
+  // kernel parameter used through a reference are re-read from parameter
+  // memory inside the loops, and a local copy of a struct this size lands in
+  // local memory; both are slow next to a 220 KB shared-memory carve-out.
+  __shared__ GemmShape s_sh;
+  __shared__ EpiParams s_ep;
+  if (threadIdx.x == 0) {
+    s_sh = sh_in;
+    s_ep = ep_in;
+  }
+  __syncthreads();
+  const GemmShape& sh = s_sh;
+  const EpiParams& ep = s_ep;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* a_ring = smem;
@@ -303,10 +347,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint64_t* full_a = bars;
   uint64_t* empty_a = full_a + C::S_A;
   uint64_t* full_r = empty_a + C::S_A;
-  uint64_t* empty_r = full_r + (C::S_R > 0 ? C::S_R : 1);
-  uint64_t* bfull = empty_r + (C::S_R > 0 ? C::S_R : 1);
-  uint64_t* bempty = bfull + (C::S_B > 0 ? C::S_B : 1);
-  uint64_t* tfull = bempty + (C::S_B > 0 ? C::S_B : 1);
+  uint64_t* empty_r = full_r + C::NR;
+  uint64_t* bfull = empty_r + C::NR;
+  uint64_t* bempty = bfull + C::NB;
+  uint64_t* tfull = bempty + C::NB;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
 
@@ -329,7 +373,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tempty[b], EPI_WARPS);
     }
     fence_mbar_init();
   }
@@ -376,7 +420,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int sa = g % C::S_A;
         if (lane == 0) ok = mbar_wait(&empty_a[sa], ((g / C::S_A) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
         if (C::Q4 && lane == 0 && ok && g >= pre)
-          ok = mbar_wait(&empty_r[g % C::S_R], ((g / C::S_R) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
+          ok = mbar_wait(&empty_r[g % C::NR], ((g / C::NR) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (lane == 0) {
@@ -385,7 +429,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           for (int mt = 0; mt < mt_valid; ++mt)
             tma_load_2d(st + mt * 128 * 128, &tmA, &full_a[sa], kb * 64, m_base + mt * 128);
           if (C::Q4 && g >= pre) {
-            const int sr = g % C::S_R;
+            const int sr = g % C::NR;
             mbar_arrive_expect_tx(&full_r[sr], C::RAW_BYTES);
             bulk_load(r_ring + sr * C::RAW_BYTES,
                       wq4 + ((size_t)nt * (sh.splits * nkb) + kb) * C::RAW_BYTES, C::RAW_BYTES, &full_r[sr]);
@@ -402,7 +446,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       for (uint32_t x = ga; x < g; ++x) mbar_drain(&full_a[x % C::S_A], (x / C::S_A) & 1);
       if (C::Q4) {
         const uint32_t gr = g > (uint32_t)C::S_R ? g - C::S_R : 0;
-        for (uint32_t x = gr; x < g; ++x) mbar_drain(&full_r[x % C::S_R], (x / C::S_R) & 1);
+        for (uint32_t x = gr; x < g; ++x) mbar_drain(&full_r[x % C::NR], (x / C::NR) & 1);
       }
     }
     __syncwarp();
@@ -425,10 +469,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       tc_fence_after();
       for (int i = 0; i < nkb; ++i, ++g) {
         const int sa = g % C::S_A;
-        const int sb = C::Q4 ? g % C::S_B : 0;
+        const int sb = C::Q4 ? g % C::NB : 0;
         if (lane == 0) {
           ok = mbar_wait(&full_a[sa], (g / C::S_A) & 1, err, PF_DEV_TIMEOUT_MMA);
-          if (ok && C::Q4) ok = mbar_wait(&bfull[sb], (g / C::S_B) & 1, err, PF_DEV_TIMEOUT_MMA);
+          if (ok && C::Q4) ok = mbar_wait(&bfull[sb], (g / C::NB) & 1, err, PF_DEV_TIMEOUT_MMA);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
@@ -462,7 +506,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   } else if (warp < DQ_WARP0) {
     // ---------------- epilogue
     pdl_wait();
-    const int qw = warp & 3;  // TMEM lane quarter this warp may access
+    const int qw = warp & 3;                 // TMEM lane quarter this warp may access
+    const int ew = (warp - EPI_WARP0) >> 2;  // which of the quarter's two epilogue warps
     const int r = 32 * qw + lane;
     uint32_t j = 0;
     for (int u = blockIdx.x; u < sh.n_units; u += gridDim.x, ++j) {
@@ -483,7 +528,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const uint32_t tq = tmem_base + (static_cast<uint32_t>(32 * qw) << 16) + buf * C::ACC;
       for (int mt = 0; mt < mt_valid; ++mt) {
         const int m = m_base + mt * 128 + r;
-        run_epilogue<BN>(ep, m, m < sh.M, nt, [&](int c, float(&v)[32]) {
+        run_epilogue<BN>(ep, m, m < sh.M, nt, ew, [&](int c, float(&v)[32]) {
           uint32_t x[32];
           tmem_ld32(tq + mt * BN + 32 * c, x);
           tmem_ld_wait();
@@ -497,14 +542,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   } else if (C::Q4) {
     // ---------------- dequant
-    const int t = threadIdx.x - DQ_WARP0 * 32;  // 0..255
+    const int t = threadIdx.x - DQ_WARP0 * 32;  // 0..DQ_THREADS-1
     uint32_t g = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < sh.n_units && ok; u += gridDim.x) {
       for (int i = 0; i < nkb; ++i, ++g) {
-        const int sr = g % C::S_R, sb = g % C::S_B;
-        bool w_ok = mbar_wait(&full_r[sr], (g / C::S_R) & 1, err, PF_DEV_TIMEOUT_DEQUANT);
-        if (w_ok) w_ok = mbar_wait(&bempty[sb], ((g / C::S_B) & 1) ^ 1, err, PF_DEV_TIMEOUT_DEQUANT);
+        const int sr = g % C::NR, sb = g % C::NB;
+        bool w_ok = mbar_wait(&full_r[sr], (g / C::NR) & 1, err, PF_DEV_TIMEOUT_DEQUANT);
+        if (w_ok) w_ok = mbar_wait(&bempty[sb], ((g / C::NB) & 1) ^ 1, err, PF_DEV_TIMEOUT_DEQUANT);
         ok = __all_sync(0xffffffffu, w_ok);
         if (!ok) break;
         uint8_t* bt = b_ring + sb * C::BT_BYTES;
@@ -533,12 +578,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t rank = cluster_ctarank();
     const bool epi_warp = warp >= EPI_WARP0 && warp < DQ_WARP0;
     const int qw = warp & 3;
+    const int ew = (warp - EPI_WARP0) >> 2;
     const int r = 32 * qw + lane;
     const uint32_t tq = tmem_base + (static_cast<uint32_t>(32 * qw) << 16);
     const uint32_t slot_bytes = 128u * BN * 4u;
     if (epi_warp && epi_ok && rank != 0) {
       const uint32_t remote = map_to_rank(smem_u32(a_ring), 0) + (rank - 1) * slot_bytes;
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = ew; c < BN / 32; c += 2) {
         uint32_t x[32];
         tmem_ld32(tq + 32 * c, x);
         tmem_ld_wait();
@@ -554,7 +600,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int nt = t % sh.n_tiles, mb = t / sh.n_tiles;
       const int m = mb * MT * 128 + r;
       const uint8_t* slots = a_ring;
-      run_epilogue<BN>(ep, m, m < sh.M, nt, [&](int c, float(&v)[32]) {
+      run_epilogue<BN>(ep, m, m < sh.M, nt, ew, [&](int c, float(&v)[32]) {
         uint32_t x[32];
         tmem_ld32(tq + 32 * c, x);
         tmem_ld_wait();
