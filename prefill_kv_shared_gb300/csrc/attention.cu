@@ -122,7 +122,7 @@ __device__ __forceinline__ void attn_chunk(uint32_t sq, uint32_t sk, uint32_t sv
                                            float (&mj)[2], float (&lj)[2], Sink&& sink) {
   using S = ChunkSmem<HD>;
   const int lane = threadIdx.x & 31;
-  const int g = lane >> 2, tq = lane & 3;
+  const int tq = lane & 3;
   const int lm = lane >> 3, lr = lane & 7;
 
   // s = q k^T for 16 rows x 64 keys

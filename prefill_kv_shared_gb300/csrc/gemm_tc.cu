@@ -13,19 +13,21 @@
 // so weight fetches run far ahead of the tensor cores.
 //
 // Persistent CTAs (one per SM) walk work units (m-block, n-tile, k-split):
-//   warp 0      TMA / bulk-copy producer
-//   warp 1      TMEM allocation, MMA issue (one lane), commits
-//   warps 2..9  epilogue (two per TMEM lane quarter, splitting the column
-//               chunks): TMEM -> registers -> fused epilogue -> global; TMEM
-//               accumulators are double buffered when they fit, so a unit's
-//               epilogue overlaps the next unit's main loop
-//   warps 10..11 Q4_0 -> bf16 dequant
+//   warp 0        TMA / bulk-copy producer
+//   warp 1        TMEM allocation, MMA issue (one lane), commits
+//   warps 4..11   epilogue (two per TMEM lane quarter, splitting the column
+//                 chunks): TMEM -> registers -> shared-memory staging ->
+//                 fused epilogue with coalesced global accesses; TMEM
+//                 accumulators are double buffered when they fit, so a
+//                 unit's epilogue overlaps the next unit's main loop
+//   warps 2, 3, 12..15  Q4_0 -> bf16 dequant
 //
 // Split-K: a weight matrix may be cut into S k-ranges (S fixed per matrix
 // shape, never per M), run by the S CTAs of a thread-block cluster; ranks
-// 1..S-1 store their fp32 partial tiles into rank 0's shared memory
-// (distributed shared memory), and rank 0 adds them to its own in ascending
-// rank order before the epilogue.
+// 1..S-1 stage their fp32 partial tiles in their own shared memory and move
+// the real rows into rank 0's with bulk copies (distributed shared memory),
+// and rank 0 adds them to its own in ascending rank order before the
+// epilogue.
 //
 // Determinism: every output element is produced by the same sequence of
 // MMAs over k (64-wide blocks in ascending order, four K=16 steps each, the
@@ -39,12 +41,25 @@
 
 namespace pf {
 
-constexpr int GEMM_WARPS = 14;
+// Roles sit on warpgroup boundaries so that registers can be moved between
+// them (setmaxnreg): warpgroups 1 and 2 (warps 4..11) run the epilogue with
+// EPI_REGS registers a thread; warpgroups 0 and 3 (producer, MMA and the
+// dequant warps 2, 3, 12..15) give theirs up down to LEAN_REGS.  The launch
+// holds GEMM_THREADS x 128 = 65536 registers, and
+// 2 x 128 x (LEAN_REGS + EPI_REGS) must not exceed that.
+constexpr int GEMM_WARPS = 16;
 constexpr int GEMM_THREADS = GEMM_WARPS * 32;
-constexpr int EPI_WARP0 = 2;   // warps 2..9: epilogue, two per TMEM lane quarter
+constexpr int EPI_WARP0 = 4;  // warps 4..11: epilogue, two per TMEM lane quarter
 constexpr int EPI_WARPS = 8;
-constexpr int DQ_WARP0 = 10;   // warps 10..13: Q4_0 dequant
-constexpr int DQ_THREADS = 128;
+constexpr int DQ_THREADS = 192;  // warps 2, 3, 12..15: Q4_0 dequant
+constexpr int EPI_REGS = 176;
+constexpr int LEAN_REGS = 80;
+static_assert(2 * 128 * (EPI_REGS + LEAN_REGS) <= GEMM_THREADS * 128, "register split exceeds the launch's registers");
+static_assert(EPI_REGS % 8 == 0 && LEAN_REGS % 8 == 0 && LEAN_REGS >= 24 && EPI_REGS <= 256, "setmaxnreg range");
+
+__device__ __forceinline__ bool is_epi_warp(int w) { return w >= EPI_WARP0 && w < EPI_WARP0 + EPI_WARPS; }
+// dequant thread index 0..DQ_THREADS-1 of a thread in warps 2, 3, 12..15
+__device__ __forceinline__ int dq_index(int w, int lane) { return (w < 4 ? w - 2 : w - 10) * 32 + lane; }
 constexpr int SMEM_LIMIT = 232448;
 
 __host__ __device__ constexpr int pow2_cols(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
@@ -57,14 +72,15 @@ struct GemmCfg {
   static constexpr int RAW_BYTES = Q4 ? BN * 36 : 0;
   static constexpr int A_STAGE = A_BYTES + (Q4 ? 0 : BT_BYTES);
   // The dequantised B ring bounds how far the dequant warps run ahead of the
-  // MMAs (B stage k+S_B is written once the MMAs of stage k are done): deep
-  // for narrow tiles, at least 3 for wide ones; the A ring takes the rest.
-  static constexpr int S_B = Q4 ? (BN >= 256 ? 3 : 6) : 0;
-  static constexpr int S_R = Q4 ? (BN >= 256 ? 3 : 8) : 0;
+  // MMAs (B stage k+S_B is written once the MMAs of stage k are done); the
+  // A ring takes what the B and raw rings and the epilogue staging leave.
+  static constexpr int S_B = Q4 ? (BN >= 256 ? (MT == 2 ? 2 : 3) : 4) : 0;
+  static constexpr int S_R = Q4 ? (BN >= 256 ? 3 : 6) : 0;
   static constexpr int NB = S_B > 0 ? S_B : 1;  // ring moduli (the rings are unused without Q4)
   static constexpr int NR = S_R > 0 ? S_R : 1;
   static constexpr int RAW_RING = (S_R * RAW_BYTES + 1023) / 1024 * 1024;
-  static constexpr int FIXED = S_B * BT_BYTES + RAW_RING + 1024 + 512;
+  static constexpr int EPI_BYTES = EPI_WARPS * 32 * 32 * 4;  // one 4 KB staging buffer per epilogue warp
+  static constexpr int FIXED = S_B * BT_BYTES + RAW_RING + EPI_BYTES + 1024 + 512;
   static constexpr int S_A_FIT = (SMEM_LIMIT - FIXED) / A_STAGE;
   static constexpr int S_A = S_A_FIT > 8 ? 8 : S_A_FIT;
   static constexpr int SMEM_BYTES = S_A * A_STAGE + FIXED;
@@ -118,7 +134,31 @@ __device__ __forceinline__ void dequant_block32(uint4 nib, __half d, uint8_t* ro
 }
 
 // ---------------------------------------------------------------------------
-// epilogue
+// Epilogue.
+//
+// tcgen05.ld (32x32b) gives each thread one accumulator row: a warp holds a
+// 32-row x 32-column block, one row per lane.  Written to global memory in
+// that layout every 16-byte access of a warp instruction falls in a
+// different row, so a 128-byte row segment costs eight separate
+// transactions.  Each block therefore goes through a warp-private 4 KB
+// staging buffer in shared memory, and global memory is touched with lane l
+// at row 4i + l/8, columns 4(l%8) .. 4(l%8)+3 (i = 0..7): every instruction
+// covers four whole 128-byte (fp32) or 64-byte (16-bit) row segments.
+
+constexpr int EPI_STAGE_BYTES = 32 * 32 * 4;
+
+// Row r's 16-byte piece p (columns 4p .. 4p+3) sits at r*128 + 16*(p ^ (r & 7)):
+// both the row-per-lane writes and the transposed reads are free of bank
+// conflicts.
+__device__ __forceinline__ void stage_put(uint8_t* st, int r, const float (&v)[32]) {
+#pragma unroll
+  for (int p = 0; p < 8; ++p)
+    *reinterpret_cast<float4*>(st + r * 128 + ((p ^ (r & 7)) << 4)) =
+        make_float4(v[4 * p], v[4 * p + 1], v[4 * p + 2], v[4 * p + 3]);
+}
+__device__ __forceinline__ float4 stage_get(const uint8_t* st, int r, int p) {
+  return *reinterpret_cast<const float4*>(st + r * 128 + ((p ^ (r & 7)) << 4));
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -128,46 +168,83 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   __half2 v = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
 }
-
-// store 32 packed 16-bit values (16 words) to a 16-byte aligned address
-__device__ __forceinline__ void store32x16(void* dst, const uint32_t (&w)[16]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+__device__ __forceinline__ uint2 pack_bf16x4(float4 a) {
+  return make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+}
+__device__ __forceinline__ uint2 pack_half4(float4 a) { return make_uint2(pack_half2(a.x, a.y), pack_half2(a.z, a.w)); }
+__device__ __forceinline__ float comp(const float4& a, int e) { return e == 0 ? a.x : e == 1 ? a.y : e == 2 ? a.z : a.w; }
+__device__ __forceinline__ float4 bf16x4_to_f32(uint2 p) {
+  return make_float4(__uint_as_float(p.x << 16), __uint_as_float(p.x & 0xFFFF0000u), __uint_as_float(p.y << 16),
+                     __uint_as_float(p.y & 0xFFFF0000u));
 }
 
-// The fused epilogue for one row of one tile.  load(c, v) fills v with the 32
-// fp32 results of the tile's column chunk c (columns 32c .. 32c+31) for this
-// thread's row; it is called in a warp-uniform way.  The two epilogue warps
-// of a lane quarter (ew = 0, 1) take alternate work items.
+// The fused epilogue for one warp's 32 rows of one tile: output rows
+// m0 .. m0+31, of which the first rv are real (warp-uniform).  load(c, v)
+// fills v with this lane's row (m0 + lane) of the tile's column chunk c
+// (columns 32c .. 32c+31) and is called in a warp-uniform way.  The two
+// epilogue warps of a lane quarter (ew = 0, 1) take alternate work items.
+// st: the warp's staging buffer.
 template <int BN, class Load>
-__device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m, bool row_ok, int n_tile, int ew,
+__device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m0, int rv, int n_tile, int ew, uint8_t* st,
                                              Load&& load) {
   constexpr int NCH = BN / 32;
+  if (rv <= 0) return;
+  const int lane = threadIdx.x & 31;
+  const int rs = lane >> 3, p = lane & 7;  // transposed position: rows 4i + rs, columns 4p .. 4p+3
   const int n0 = n_tile * BN;
-  float v[32], u[32];
+  float v[32];
+  // Every kind below first computes all of a block's values into registers
+  // and only then stores them: a global load placed after a store in
+  // program order waits for it, which would put one memory round trip on
+  // every row of the block.
+
   if (ep.kind == EPI_GLU) {
+    // gate chunk c and up chunk c + NCH/2 of the interleaved tile -> output
+    // columns f0 .. f0+31
     constexpr int HALF_CH = NCH / 2;
     for (int c = ew; c < HALF_CH; c += 2) {
-      load(c, v);
-      load(c + HALF_CH, u);
-      if (!row_ok) continue;
       const int f0 = n_tile * (BN / 2) + 32 * c;
-      uint32_t w[16];
+      if (f0 >= ep.N) break;
+      load(c, v);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float a0 = ep.act == 0 ? gelu_tanh_f(v[2 * j]) : silu_f(v[2 * j]);
-        const float a1 = ep.act == 0 ? gelu_tanh_f(v[2 * j + 1]) : silu_f(v[2 * j + 1]);
-        w[j] = pack_bf16x2(a0 * u[2 * j], a1 * u[2 * j + 1]);
+      for (int j = 0; j < 32; ++j) v[j] = ep.act == 0 ? gelu_tanh_f(v[j]) : silu_f(v[j]);
+      {
+        float u[32];
+        load(c + HALF_CH, u);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= u[j];
       }
-      if (f0 + 32 <= ep.N) store32x16(ep.out_bf16 + (size_t)m * ep.ld_bf16 + f0, w);
+      stage_put(st, lane, v);
+      __syncwarp();
+      uint2 h[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) h[i] = pack_bf16x4(stage_get(st, 4 * i + rs, p));
+      __syncwarp();
+      const int col = f0 + 4 * p;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = 4 * i + rs;
+        if (r >= rv || col >= ep.N) continue;
+        __nv_bfloat16* dst = ep.out_bf16 + (size_t)(m0 + r) * ep.ld_bf16 + col;
+        if (col + 4 <= ep.N) {
+          *reinterpret_cast<uint2*>(dst) = h[i];
+        } else {
+          for (int e = 0; col + e < ep.N; ++e) {
+            const uint32_t w = e < 2 ? h[i].x : h[i].y;
+            dst[e] = __ushort_as_bfloat16(static_cast<unsigned short>(w >> (16 * (e & 1))));
+          }
+        }
+      }
     }
     return;
   }
+
   if (ep.kind == EPI_QKV) {
+    // Q | K | V columns; Q and K rotated (half-split RoPE at position
+    // pos0 + row) and written as fp16, V written as fp16 to the cache.  A
+    // rotated chunk is handled together with its partner half a head away.
     const int hd = ep.head_dim, half = hd / 2, pair_ch = half / 32;
     const int q_end = ep.q_dim, k_end = ep.q_dim + ep.kv_dim, v_end = ep.q_dim + 2 * ep.kv_dim;
-    const int pos = ep.pos0 + m;
     int item = 0;
     for (int c = 0; c < NCH; ++c) {
       const int n = n0 + 32 * c;
@@ -175,11 +252,19 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m, bool ro
       if (n >= k_end) {       // V: no rotation
         if ((item++ & 1) != ew) continue;
         load(c, v);
-        if (!row_ok) continue;
-        uint32_t w[16];
+        stage_put(st, lane, v);
+        __syncwarp();
+        uint2 h[8];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) w[j] = pack_half2(v[2 * j], v[2 * j + 1]);
-        store32x16(ep.v_cache + (size_t)pos * ep.kv_dim + (n - k_end), w);
+        for (int i = 0; i < 8; ++i) h[i] = pack_half4(stage_get(st, 4 * i + rs, p));
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = 4 * i + rs;
+          if (r >= rv) continue;
+          const int pos = ep.pos0 + m0 + r;
+          *reinterpret_cast<uint2*>(ep.v_cache + (size_t)pos * ep.kv_dim + (n - k_end) + 4 * p) = h[i];
+        }
         continue;
       }
       const bool is_q = n < q_end;
@@ -187,93 +272,129 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m, bool ro
       const int i0 = rel % hd;
       if (i0 >= half) continue;  // handled together with its partner chunk
       if ((item++ & 1) != ew) continue;
-      load(c, v);
-      load(c + pair_ch, u);
-      if (!row_ok) continue;
       const int head = rel / hd;
-      const float4* cs4 = reinterpret_cast<const float4*>(ep.rope + (size_t)pos * half + i0);
-      uint32_t w1[16], w2[16];
+      // two passes of 16 rows each keep the transposed halves in registers
+      for (int hp = 0; hp < 2; ++hp) {
+        float4 c01[4], c23[4];  // (cos, sin) of columns i0+4p .. i0+4p+3 at each row's position
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float4 c01 = cs4[j];  // (cos, sin) of columns 2j and 2j+1
-        w1[j] = pack_half2(v[2 * j] * c01.x - u[2 * j] * c01.y, v[2 * j + 1] * c01.z - u[2 * j + 1] * c01.w);
-        w2[j] = pack_half2(v[2 * j] * c01.y + u[2 * j] * c01.x, v[2 * j + 1] * c01.w + u[2 * j + 1] * c01.z);
+        for (int i = 0; i < 4; ++i) {
+          const int r = 16 * hp + 4 * i + rs;
+          const int pos = ep.pos0 + m0 + (r < rv ? r : 0);
+          const float4* cs = reinterpret_cast<const float4*>(ep.rope + (size_t)pos * half + i0 + 4 * p);
+          c01[i] = cs[0];
+          c23[i] = cs[1];
+        }
+        float4 vt[4], ut[4];
+        load(c, v);
+        stage_put(st, lane, v);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) vt[i] = stage_get(st, 16 * hp + 4 * i + rs, p);
+        __syncwarp();
+        load(c + pair_ch, v);
+        stage_put(st, lane, v);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ut[i] = stage_get(st, 16 * hp + 4 * i + rs, p);
+        __syncwarp();
+        uint2 o1[4], o2[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 a = vt[i], b = ut[i], x = c01[i], y = c23[i];
+          o1[i] = pack_half4(make_float4(a.x * x.x - b.x * x.y, a.y * x.z - b.y * x.w, a.z * y.x - b.z * y.y,
+                                         a.w * y.z - b.w * y.w));
+          o2[i] = pack_half4(make_float4(a.x * x.y + b.x * x.x, a.y * x.w + b.y * x.z, a.z * y.y + b.z * y.x,
+                                         a.w * y.w + b.w * y.z));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 16 * hp + 4 * i + rs;
+          if (r >= rv) continue;
+          const int m = m0 + r, pos = ep.pos0 + m;
+          __half* dst = is_q ? ep.q_out + (size_t)m * ep.q_dim + head * hd
+                             : ep.k_cache + (size_t)pos * ep.kv_dim + head * hd;
+          *reinterpret_cast<uint2*>(dst + i0 + 4 * p) = o1[i];
+          *reinterpret_cast<uint2*>(dst + i0 + half + 4 * p) = o2[i];
+        }
+        if (rv <= 16) break;
       }
-      __half* dst = is_q ? ep.q_out + (size_t)m * ep.q_dim + head * hd
-                         : ep.k_cache + (size_t)pos * ep.kv_dim + head * hd;
-      store32x16(dst + i0, w1);
-      store32x16(dst + i0 + half, w2);
     }
     return;
   }
-  // F32, RESID, PLE: one 32-column chunk at a time; the chunk's global
-  // operands are requested before its TMEM load
-  auto fetch = [&](int c, float4 (&g)[8]) {
-    const int n = n0 + 32 * c;
-    if (!row_ok || n >= ep.N) return;
-    if (ep.kind == EPI_RESID) {
-      const float4* xr = reinterpret_cast<const float4*>(ep.out_f32 + (size_t)m * ep.ld_f32 + n);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) g[j] = xr[j];
-    } else if (ep.kind == EPI_PLE) {
-      const float4* pl = reinterpret_cast<const float4*>(ep.ple + (size_t)m * ep.ple_stride + n);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) g[j] = pl[j];
-    }
-  };
-  auto finish = [&](int c, float4 (&g)[8]) {
-    const int n = n0 + 32 * c;
-    if (n >= ep.N) return;
-    load(c, v);
-    if (!row_ok) return;
-    const bool full = n + 32 <= ep.N;
-    if (ep.kind == EPI_F32) {
-      float* dst = ep.out_f32 + (size_t)m * ep.ld_f32 + n;
-      if (full) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          reinterpret_cast<float4*>(dst)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-      } else {
-        for (int j = 0; j < 32 && n + j < ep.N; ++j) dst[j] = v[j];
-      }
-    } else if (ep.kind == EPI_RESID) {
-      float4* xr = reinterpret_cast<float4*>(ep.out_f32 + (size_t)m * ep.ld_f32 + n);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float4 x4 = g[j];
-        x4.x += v[4 * j];
-        x4.y += v[4 * j + 1];
-        x4.z += v[4 * j + 2];
-        x4.w += v[4 * j + 3];
-        v[4 * j] = x4.x;
-        v[4 * j + 1] = x4.y;
-        v[4 * j + 2] = x4.z;
-        v[4 * j + 3] = x4.w;
-        xr[j] = x4;
-      }
-      if (ep.out_bf16) {
-        uint32_t w[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-        store32x16(ep.out_bf16 + (size_t)m * ep.ld_bf16 + n, w);
-      }
-    } else {  // EPI_PLE: g holds 32 bf16 multipliers in g[0..3]
-      uint32_t w[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float4 q = g[j >> 2];
-        const float qf = (j & 3) == 0 ? q.x : (j & 3) == 1 ? q.y : (j & 3) == 2 ? q.z : q.w;
-        const uint32_t pw = __float_as_uint(qf);
-        const float plo = __uint_as_float(pw << 16), phi = __uint_as_float(pw & 0xFFFF0000u);  // bf16 -> f32
-        w[j] = pack_bf16x2(gelu_tanh_f(v[2 * j]) * plo, gelu_tanh_f(v[2 * j + 1]) * phi);
-      }
-      store32x16(ep.out_bf16 + (size_t)m * ep.ld_bf16 + n, w);
-    }
-  };
+
+  // F32, RESID, PLE: one 32-column chunk at a time.  The chunk's global
+  // operand (RESID: the residual rows; PLE: the multipliers) is requested
+  // before the TMEM load so that its latency overlaps the staging.
   for (int c = ew; c < NCH; c += 2) {
-    float4 g[8];
-    fetch(c, g);
-    finish(c, g);
+    const int n = n0 + 32 * c;
+    if (n >= ep.N) break;
+    const int col = n + 4 * p;
+    const bool full = col + 4 <= ep.N;
+    float4 side[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = 4 * i + rs;
+      side[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r >= rv || col >= ep.N) continue;
+      if (ep.kind == EPI_RESID) {
+        const float* xr = ep.out_f32 + (size_t)(m0 + r) * ep.ld_f32 + col;
+        if (full) {
+          side[i] = *reinterpret_cast<const float4*>(xr);
+        } else {
+          side[i].x = xr[0];
+          if (col + 1 < ep.N) side[i].y = xr[1];
+          if (col + 2 < ep.N) side[i].z = xr[2];
+        }
+      } else if (ep.kind == EPI_PLE) {
+        const __nv_bfloat16* pl = ep.ple + (size_t)(m0 + r) * ep.ple_stride + col;
+        if (full) {
+          side[i] = bf16x4_to_f32(*reinterpret_cast<const uint2*>(pl));
+        } else {
+          side[i].x = __bfloat162float(pl[0]);
+          if (col + 1 < ep.N) side[i].y = __bfloat162float(pl[1]);
+          if (col + 2 < ep.N) side[i].z = __bfloat162float(pl[2]);
+        }
+      }
+    }
+    load(c, v);
+    stage_put(st, lane, v);
+    __syncwarp();
+    // values of the block in the transposed layout (RESID: the new residual;
+    // PLE: gelu(acc) * multiplier, before rounding)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 a = stage_get(st, 4 * i + rs, p);
+      const float4 g = side[i];
+      if (ep.kind == EPI_RESID) {
+        side[i] = make_float4(g.x + a.x, g.y + a.y, g.z + a.z, g.w + a.w);
+      } else if (ep.kind == EPI_PLE) {
+        side[i] = make_float4(gelu_tanh_f(a.x) * g.x, gelu_tanh_f(a.y) * g.y, gelu_tanh_f(a.z) * g.z,
+                              gelu_tanh_f(a.w) * g.w);
+      } else {
+        side[i] = a;
+      }
+    }
+    __syncwarp();
+    if (col < ep.N) {
+      float* of = ep.kind != EPI_PLE ? ep.out_f32 : nullptr;                        // fp32 result
+      __nv_bfloat16* ob = ep.kind != EPI_F32 ? ep.out_bf16 : nullptr;               // bf16 result (RESID: optional copy)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = 4 * i + rs;
+        if (r >= rv) continue;
+        const size_t m = static_cast<size_t>(m0 + r);
+        const float4 a = side[i];
+        if (full) {
+          if (of) *reinterpret_cast<float4*>(of + m * ep.ld_f32 + col) = a;
+          if (ob) *reinterpret_cast<uint2*>(ob + m * ep.ld_bf16 + col) = pack_bf16x4(a);
+        } else {
+          for (int e = 0; col + e < ep.N; ++e) {
+            if (of) of[m * ep.ld_f32 + col + e] = comp(a, e);
+            if (ob) ob[m * ep.ld_bf16 + col + e] = __float2bfloat16_rn(comp(a, e));
+          }
+        }
+      }
+    }
   }
 }
 
@@ -303,9 +424,17 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local_smem, uint32_t ra
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+// Bulk copy from this CTA's shared memory to a cluster peer's, completing
+// on the peer's mbarrier (both destination addresses from mapa).
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst),
+               "r"(src), "r"(bytes), "r"(bar)
                : "memory");
+}
+// barrier among the epilogue warps only
+__device__ __forceinline__ void epi_bar_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(EPI_WARPS * 32) : "memory");
 }
 
 struct GemmShape {
@@ -343,7 +472,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint8_t* a_ring = smem;
   uint8_t* b_ring = a_ring + C::S_A * C::A_STAGE;
   uint8_t* r_ring = b_ring + C::S_B * C::BT_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(r_ring + C::RAW_RING);
+  uint8_t* epi_stage = r_ring + C::RAW_RING;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + C::EPI_BYTES);
   uint64_t* full_a = bars;
   uint64_t* empty_a = full_a + C::S_A;
   uint64_t* full_r = empty_a + C::S_A;
@@ -352,7 +482,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint64_t* bempty = bfull + C::NB;
   uint64_t* tfull = bempty + C::NB;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* red_full = tempty + 2;  // split-K: rank 0's partials have landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_full + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = sh.kb_per_split;
@@ -375,6 +506,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], EPI_WARPS);
     }
+    mbar_init(red_full, 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -388,236 +520,285 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   bool epi_ok = true;
   pdl_launch();
-
-  if (warp == 0) {
-    // ---------------- producer
-    // Weights do not depend on the previous kernel: the first raw stages are
-    // fetched before waiting for it.
-    uint32_t pre = 0;
-    if (C::Q4 && lane == 0 && blockIdx.x < sh.n_units) {
-      const int u = blockIdx.x;
-      const int ks = u % sh.splits, t = u / sh.splits;
-      const int nt = t % sh.n_tiles;
-      pre = nkb < C::S_R ? nkb : C::S_R;
-      for (uint32_t x = 0; x < pre; ++x) {
-        mbar_arrive_expect_tx(&full_r[x], C::RAW_BYTES);
-        bulk_load(r_ring + x * C::RAW_BYTES,
-                  wq4 + ((size_t)nt * (sh.splits * nkb) + ks * nkb + x) * C::RAW_BYTES, C::RAW_BYTES, &full_r[x]);
+  // split-K: bytes of one column chunk's real rows in a partial tile (one
+  // 128-row unit per CTA in split mode)
+  uint32_t split_chunk_bytes = 0;
+  if (split_mode) {
+    const int mb = (blockIdx.x / sh.splits) / sh.n_tiles;
+    const int rows = sh.M - mb * 128 < 128 ? sh.M - mb * 128 : 128;
+    split_chunk_bytes = static_cast<uint32_t>(rows) * 128u;
+  }
+  const int wg = warp >> 2;
+  if (wg == 1 || wg == 2) {
+    // ================ epilogue warpgroups
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPI_REGS));
+    {
+      // ---------------- epilogue
+      pdl_wait();
+      const int qw = warp & 3;                 // TMEM lane quarter this warp may access
+      const int ew = (warp - EPI_WARP0) >> 2;  // which of the quarter's two epilogue warps
+      uint8_t* stage = epi_stage + (warp - EPI_WARP0) * EPI_STAGE_BYTES;
+      uint32_t j = 0;
+      for (int u = blockIdx.x; u < sh.n_units; u += gridDim.x, ++j) {
+        const int t = u / sh.splits;
+        const int nt = t % sh.n_tiles, mb = t / sh.n_tiles;
+        const int m_base = mb * MT * 128;
+        int mt_valid = (sh.M - m_base + 127) / 128;
+        if (mt_valid > MT) mt_valid = MT;
+        const int buf = C::ACC_BUFS == 2 ? (j & 1) : 0;
+        bool ok = mbar_wait(&tfull[buf], (j / C::ACC_BUFS) & 1, err, PF_DEV_TIMEOUT_EPILOGUE);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          epi_ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (split_mode) break;  // the cluster reduction below takes it from here
+        const uint32_t tq = tmem_base + (static_cast<uint32_t>(32 * qw) << 16) + buf * C::ACC;
+        for (int mt = 0; mt < mt_valid; ++mt) {
+          const int m0 = m_base + mt * 128 + 32 * qw;
+          const int rv = sh.M - m0 < 32 ? sh.M - m0 : 32;
+          run_epilogue<BN>(ep, m0, rv, nt, ew, stage, [&](int c, float(&v)[32]) {
+            uint32_t x[32];
+            tmem_ld32(tq + mt * BN + 32 * c, x);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(x[q]);
+          });
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
       }
     }
-    pre = __shfl_sync(0xffffffffu, pre, 0);
-    pdl_wait();
-    uint32_t g = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < sh.n_units && ok; u += gridDim.x) {
-      const int ks = u % sh.splits, t = u / sh.splits;
+    if (split_mode) {
+      // Split-K over the cluster: CTA rank r holds the partial of k-range r.
+      // Ranks 1.. stage theirs in their own (now idle) ring memory and send the
+      // real rows to rank 0's ring with bulk copies; rank 0 adds them to its
+      // own in ascending rank order and runs the epilogue.
+      const uint32_t rank = cluster_ctarank();
+      const int t = blockIdx.x / sh.splits;
       const int nt = t % sh.n_tiles, mb = t / sh.n_tiles;
-      const int m_base = mb * MT * 128;
-      int mt_valid = (sh.M - m_base + 127) / 128;
-      if (mt_valid > MT) mt_valid = MT;
-      for (int i = 0; i < nkb; ++i, ++g) {
-        const int kb = ks * nkb + i;
-        const int sa = g % C::S_A;
-        if (lane == 0) ok = mbar_wait(&empty_a[sa], ((g / C::S_A) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
-        if (C::Q4 && lane == 0 && ok && g >= pre)
-          ok = mbar_wait(&empty_r[g % C::NR], ((g / C::NR) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        if (lane == 0) {
-          uint8_t* st = a_ring + sa * C::A_STAGE;
-          mbar_arrive_expect_tx(&full_a[sa], mt_valid * 128 * 128 + (C::Q4 ? 0 : C::BT_BYTES));
-          for (int mt = 0; mt < mt_valid; ++mt)
-            tma_load_2d(st + mt * 128 * 128, &tmA, &full_a[sa], kb * 64, m_base + mt * 128);
-          if (C::Q4 && g >= pre) {
-            const int sr = g % C::NR;
-            mbar_arrive_expect_tx(&full_r[sr], C::RAW_BYTES);
-            bulk_load(r_ring + sr * C::RAW_BYTES,
-                      wq4 + ((size_t)nt * (sh.splits * nkb) + kb) * C::RAW_BYTES, C::RAW_BYTES, &full_r[sr]);
-          } else if (!C::Q4) {
-            tma_load_2d(st + C::A_BYTES, &tmB, &full_a[sa], kb * 64, nt * BN);
+      const int m_base = mb * 128;  // one 128-row tile per unit in split mode
+      const int rows = sh.M - m_base < 128 ? sh.M - m_base : 128;
+      const uint32_t chunk_bytes = split_chunk_bytes;
+      const uint32_t slot_bytes = 128u * BN * 4u;
+      cluster_sync_all();  // rank 0's expected byte count is posted by its producer warp
+      const bool epi_warp = true;
+      const int qw = warp & 3;
+      const int ew = (warp - EPI_WARP0) >> 2;
+      const int r = 32 * qw + lane;
+      const uint32_t tq = tmem_base + (static_cast<uint32_t>(32 * qw) << 16);
+      if (epi_warp && rank != 0) {
+        if (epi_ok && 32 * qw < rows) {
+          for (int c = ew; c < BN / 32; c += 2) {
+            uint32_t x[32];
+            tmem_ld32(tq + 32 * c, x);
+            tmem_ld_wait();
+            if (r < rows) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<float4*>(a_ring + slot_off(c, r, q)) =
+                    make_float4(__uint_as_float(x[4 * q]), __uint_as_float(x[4 * q + 1]), __uint_as_float(x[4 * q + 2]),
+                                __uint_as_float(x[4 * q + 3]));
+            }
           }
         }
-        __syncwarp();
-      }
-    }
-    if (!ok && lane == 0) {
-      // the last S_A / S_R issues may still be in flight
-      const uint32_t ga = g > (uint32_t)C::S_A ? g - C::S_A : 0;
-      for (uint32_t x = ga; x < g; ++x) mbar_drain(&full_a[x % C::S_A], (x / C::S_A) & 1);
-      if (C::Q4) {
-        const uint32_t gr = g > (uint32_t)C::S_R ? g - C::S_R : 0;
-        for (uint32_t x = gr; x < g; ++x) mbar_drain(&full_r[x % C::NR], (x / C::NR) & 1);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ---------------- MMA issue
-    constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
-    uint32_t g = 0, j = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < sh.n_units && ok; u += gridDim.x, ++j) {
-      const int t = u / sh.splits;
-      const int mb = t / sh.n_tiles;
-      int mt_valid = (sh.M - mb * MT * 128 + 127) / 128;
-      if (mt_valid > MT) mt_valid = MT;
-      const int buf = C::ACC_BUFS == 2 ? (j & 1) : 0;
-      const uint32_t tacc = tmem_base + buf * C::ACC;
-      if (lane == 0)
-        ok = mbar_wait(&tempty[buf], ((j / C::ACC_BUFS) & 1) ^ 1, err, PF_DEV_TIMEOUT_MMA);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      tc_fence_after();
-      for (int i = 0; i < nkb; ++i, ++g) {
-        const int sa = g % C::S_A;
-        const int sb = C::Q4 ? g % C::NB : 0;
-        if (lane == 0) {
-          ok = mbar_wait(&full_a[sa], (g / C::S_A) & 1, err, PF_DEV_TIMEOUT_MMA);
-          if (ok && C::Q4) ok = mbar_wait(&bfull[sb], (g / C::NB) & 1, err, PF_DEV_TIMEOUT_MMA);
+        fence_proxy_async_smem();
+        epi_bar_sync();
+        if (warp == EPI_WARP0 && lane == 0) {
+          // sent even after a failed wait, so that rank 0 is not left waiting
+          const uint32_t dst = map_to_rank(smem_u32(a_ring), 0) + (rank - 1) * slot_bytes;
+          const uint32_t bar = map_to_rank(smem_u32(red_full), 0);
+          for (int c = 0; c < BN / 32; ++c)
+            bulk_copy_to_cluster(dst + c * 16384u, smem_u32(a_ring) + c * 16384u, chunk_bytes, bar);
         }
+      }
+      if (epi_warp && rank == 0) {
+        bool ok = mbar_wait(red_full, 0, err, PF_DEV_TIMEOUT_EPILOGUE);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok && epi_ok) {
+          const uint8_t* slots = a_ring;
+          uint8_t* stage = epi_stage + (warp - EPI_WARP0) * EPI_STAGE_BYTES;
+          const int m0 = m_base + 32 * qw;
+          const int rv = sh.M - m0 < 32 ? sh.M - m0 : 32;
+          run_epilogue<BN>(ep, m0, rv, nt, ew, stage, [&](int c, float(&v)[32]) {
+            uint32_t x[32];
+            tmem_ld32(tq + 32 * c, x);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(x[q]);
+            for (int s = 1; s < sh.splits; ++s) {
+              const uint8_t* sl = slots + (s - 1) * slot_bytes;
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const float4 p = *reinterpret_cast<const float4*>(sl + slot_off(c, r, q));
+                v[4 * q] += p.x;
+                v[4 * q + 1] += p.y;
+                v[4 * q + 2] += p.z;
+                v[4 * q + 3] += p.w;
+              }
+            }
+          });
+        }
+      }
+      // ranks 1.. keep their shared memory (the copies' source) until rank 0
+      // has received everything
+      cluster_sync_all();
+    }
+  } else {
+    // ================ producer, MMA and dequant warpgroups
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(LEAN_REGS));
+    if (warp == 0) {
+      // ---------------- producer
+      // Weights do not depend on the previous kernel: the first raw stages are
+      // fetched before waiting for it.
+      uint32_t pre = 0;
+      if (C::Q4 && lane == 0 && blockIdx.x < sh.n_units) {
+        const int u = blockIdx.x;
+        const int ks = u % sh.splits, t = u / sh.splits;
+        const int nt = t % sh.n_tiles;
+        pre = nkb < C::S_R ? nkb : C::S_R;
+        for (uint32_t x = 0; x < pre; ++x) {
+          mbar_arrive_expect_tx(&full_r[x], C::RAW_BYTES);
+          bulk_load(r_ring + x * C::RAW_BYTES,
+                    wq4 + ((size_t)nt * (sh.splits * nkb) + ks * nkb + x) * C::RAW_BYTES, C::RAW_BYTES, &full_r[x]);
+        }
+      }
+      pre = __shfl_sync(0xffffffffu, pre, 0);
+      pdl_wait();
+      uint32_t g = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < sh.n_units && ok; u += gridDim.x) {
+        const int ks = u % sh.splits, t = u / sh.splits;
+        const int nt = t % sh.n_tiles, mb = t / sh.n_tiles;
+        const int m_base = mb * MT * 128;
+        int mt_valid = (sh.M - m_base + 127) / 128;
+        if (mt_valid > MT) mt_valid = MT;
+        for (int i = 0; i < nkb; ++i, ++g) {
+          const int kb = ks * nkb + i;
+          const int sa = g % C::S_A;
+          if (lane == 0) ok = mbar_wait(&empty_a[sa], ((g / C::S_A) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
+          if (C::Q4 && lane == 0 && ok && g >= pre)
+            ok = mbar_wait(&empty_r[g % C::NR], ((g / C::NR) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          if (lane == 0) {
+            uint8_t* st = a_ring + sa * C::A_STAGE;
+            mbar_arrive_expect_tx(&full_a[sa], mt_valid * 128 * 128 + (C::Q4 ? 0 : C::BT_BYTES));
+            for (int mt = 0; mt < mt_valid; ++mt)
+              tma_load_2d(st + mt * 128 * 128, &tmA, &full_a[sa], kb * 64, m_base + mt * 128);
+            if (C::Q4 && g >= pre) {
+              const int sr = g % C::NR;
+              mbar_arrive_expect_tx(&full_r[sr], C::RAW_BYTES);
+              bulk_load(r_ring + sr * C::RAW_BYTES,
+                        wq4 + ((size_t)nt * (sh.splits * nkb) + kb) * C::RAW_BYTES, C::RAW_BYTES, &full_r[sr]);
+            } else if (!C::Q4) {
+              tma_load_2d(st + C::A_BYTES, &tmB, &full_a[sa], kb * 64, nt * BN);
+            }
+          }
+          __syncwarp();
+        }
+      }
+      if (!ok && lane == 0) {
+        // the last S_A / S_R issues may still be in flight
+        const uint32_t ga = g > (uint32_t)C::S_A ? g - C::S_A : 0;
+        for (uint32_t x = ga; x < g; ++x) mbar_drain(&full_a[x % C::S_A], (x / C::S_A) & 1);
+        if (C::Q4) {
+          const uint32_t gr = g > (uint32_t)C::S_R ? g - C::S_R : 0;
+          for (uint32_t x = gr; x < g; ++x) mbar_drain(&full_r[x % C::NR], (x / C::NR) & 1);
+        }
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      // ---------------- MMA issue
+      constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
+      uint32_t g = 0, j = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < sh.n_units && ok; u += gridDim.x, ++j) {
+        const int t = u / sh.splits;
+        const int mb = t / sh.n_tiles;
+        int mt_valid = (sh.M - mb * MT * 128 + 127) / 128;
+        if (mt_valid > MT) mt_valid = MT;
+        const int buf = C::ACC_BUFS == 2 ? (j & 1) : 0;
+        const uint32_t tacc = tmem_base + buf * C::ACC;
+        if (lane == 0)
+          ok = mbar_wait(&tempty[buf], ((j / C::ACC_BUFS) & 1) ^ 1, err, PF_DEV_TIMEOUT_MMA);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a0 = smem_u32(a_ring + sa * C::A_STAGE);
-          const uint32_t b0 = C::Q4 ? smem_u32(b_ring + sb * C::BT_BYTES) : a0 + C::A_BYTES;
-          for (int mt = 0; mt < mt_valid; ++mt) {
+        for (int i = 0; i < nkb; ++i, ++g) {
+          const int sa = g % C::S_A;
+          const int sb = C::Q4 ? g % C::NB : 0;
+          if (lane == 0) {
+            ok = mbar_wait(&full_a[sa], (g / C::S_A) & 1, err, PF_DEV_TIMEOUT_MMA);
+            if (ok && C::Q4) ok = mbar_wait(&bfull[sb], (g / C::NB) & 1, err, PF_DEV_TIMEOUT_MMA);
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a0 = smem_u32(a_ring + sa * C::A_STAGE);
+            const uint32_t b0 = C::Q4 ? smem_u32(b_ring + sb * C::BT_BYTES) : a0 + C::A_BYTES;
+            for (int mt = 0; mt < mt_valid; ++mt) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = sdesc_sw128(a0 + mt * 128 * 128 + kk * 32);
-              const uint64_t bd = sdesc_sw128(b0 + kk * 32);
-              tc_mma_f16(tacc + mt * BN, ad, bd, idesc, (i | kk) != 0 ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = sdesc_sw128(a0 + mt * 128 * 128 + kk * 32);
+                const uint64_t bd = sdesc_sw128(b0 + kk * 32);
+                tc_mma_f16(tacc + mt * BN, ad, bd, idesc, (i | kk) != 0 ? 1u : 0u);
+              }
             }
+            tc_commit(&empty_a[sa]);
+            if (C::Q4) tc_commit(&bempty[sb]);
           }
-          tc_commit(&empty_a[sa]);
-          if (C::Q4) tc_commit(&bempty[sb]);
+          __syncwarp();
         }
+        if (lane == 0) tc_commit(&tfull[buf]);  // the unit's accumulator is complete
         __syncwarp();
       }
-      if (lane == 0) tc_commit(&tfull[buf]);  // the unit's accumulator is complete
+      if (!ok && lane == 0) {
+        // wait for the MMAs already issued before TMEM is freed
+        tc_commit(&tfull[0]);
+        mbar_drain(&tfull[0], 0);
+        mbar_drain(&tfull[0], 1);
+      }
       __syncwarp();
-    }
-    if (!ok && lane == 0) {
-      // wait for the MMAs already issued before TMEM is freed
-      tc_commit(&tfull[0]);
-      mbar_drain(&tfull[0], 0);
-      mbar_drain(&tfull[0], 1);
-    }
-    __syncwarp();
-  } else if (warp < DQ_WARP0) {
-    // ---------------- epilogue
-    pdl_wait();
-    const int qw = warp & 3;                 // TMEM lane quarter this warp may access
-    const int ew = (warp - EPI_WARP0) >> 2;  // which of the quarter's two epilogue warps
-    const int r = 32 * qw + lane;
-    uint32_t j = 0;
-    for (int u = blockIdx.x; u < sh.n_units; u += gridDim.x, ++j) {
-      const int t = u / sh.splits;
-      const int nt = t % sh.n_tiles, mb = t / sh.n_tiles;
-      const int m_base = mb * MT * 128;
-      int mt_valid = (sh.M - m_base + 127) / 128;
-      if (mt_valid > MT) mt_valid = MT;
-      const int buf = C::ACC_BUFS == 2 ? (j & 1) : 0;
-      bool ok = mbar_wait(&tfull[buf], (j / C::ACC_BUFS) & 1, err, PF_DEV_TIMEOUT_EPILOGUE);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) {
-        epi_ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (split_mode) break;  // the cluster reduction below takes it from here
-      const uint32_t tq = tmem_base + (static_cast<uint32_t>(32 * qw) << 16) + buf * C::ACC;
-      for (int mt = 0; mt < mt_valid; ++mt) {
-        const int m = m_base + mt * 128 + r;
-        run_epilogue<BN>(ep, m, m < sh.M, nt, ew, [&](int c, float(&v)[32]) {
-          uint32_t x[32];
-          tmem_ld32(tq + mt * BN + 32 * c, x);
-          tmem_ld_wait();
-#pragma unroll
-          for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(x[q]);
-        });
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
-    }
-  } else if (C::Q4) {
-    // ---------------- dequant
-    const int t = threadIdx.x - DQ_WARP0 * 32;  // 0..DQ_THREADS-1
-    uint32_t g = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < sh.n_units && ok; u += gridDim.x) {
-      for (int i = 0; i < nkb; ++i, ++g) {
-        const int sr = g % C::NR, sb = g % C::NB;
-        bool w_ok = mbar_wait(&full_r[sr], (g / C::NR) & 1, err, PF_DEV_TIMEOUT_DEQUANT);
-        if (w_ok) w_ok = mbar_wait(&bempty[sb], ((g / C::NB) & 1) ^ 1, err, PF_DEV_TIMEOUT_DEQUANT);
-        ok = __all_sync(0xffffffffu, w_ok);
-        if (!ok) break;
-        uint8_t* bt = b_ring + sb * C::BT_BYTES;
-        const uint8_t* raw = r_ring + sr * C::RAW_BYTES;
-        for (int it = t; it < BN * 2; it += DQ_THREADS) {
-          const int rr = it % BN, h = it / BN;
-          const uint4 nib = *reinterpret_cast<const uint4*>(raw + (size_t)(h * BN + rr) * 16);
-          const __half d = *reinterpret_cast<const __half*>(raw + BN * 32 + (h * BN + rr) * 2);
-          dequant_block32(nib, d, bt + rr * 128, h, rr & 7);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bfull[sb]);
-          mbar_arrive(&empty_r[sr]);
-        }
-      }
-    }
-  }
-
-  if (split_mode) {
-    // Split-K over the cluster: CTA rank r holds the partial of k-range r.
-    // Ranks 1.. write theirs into rank 0's (now idle) ring memory; rank 0
-    // adds them to its own in ascending rank order and runs the epilogue.
-    cluster_sync_all();
-    const uint32_t rank = cluster_ctarank();
-    const bool epi_warp = warp >= EPI_WARP0 && warp < DQ_WARP0;
-    const int qw = warp & 3;
-    const int ew = (warp - EPI_WARP0) >> 2;
-    const int r = 32 * qw + lane;
-    const uint32_t tq = tmem_base + (static_cast<uint32_t>(32 * qw) << 16);
-    const uint32_t slot_bytes = 128u * BN * 4u;
-    if (epi_warp && epi_ok && rank != 0) {
-      const uint32_t remote = map_to_rank(smem_u32(a_ring), 0) + (rank - 1) * slot_bytes;
-      for (int c = ew; c < BN / 32; c += 2) {
-        uint32_t x[32];
-        tmem_ld32(tq + 32 * c, x);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          st_cluster_v4(remote + slot_off(c, r, q), __uint_as_float(x[4 * q]), __uint_as_float(x[4 * q + 1]),
-                        __uint_as_float(x[4 * q + 2]), __uint_as_float(x[4 * q + 3]));
-      }
-    }
-    cluster_sync_all();
-    if (epi_warp && epi_ok && rank == 0) {
-      const int t = blockIdx.x / sh.splits;
-      const int nt = t % sh.n_tiles, mb = t / sh.n_tiles;
-      const int m = mb * MT * 128 + r;
-      const uint8_t* slots = a_ring;
-      run_epilogue<BN>(ep, m, m < sh.M, nt, ew, [&](int c, float(&v)[32]) {
-        uint32_t x[32];
-        tmem_ld32(tq + 32 * c, x);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(x[q]);
-        for (int s = 1; s < sh.splits; ++s) {
-          const uint8_t* sl = slots + (s - 1) * slot_bytes;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 p = *reinterpret_cast<const float4*>(sl + slot_off(c, r, q));
-            v[4 * q] += p.x;
-            v[4 * q + 1] += p.y;
-            v[4 * q + 2] += p.z;
-            v[4 * q + 3] += p.w;
+    } else if (C::Q4) {
+      // ---------------- dequant
+      const int t = dq_index(warp, lane);
+      uint32_t g = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < sh.n_units && ok; u += gridDim.x) {
+        for (int i = 0; i < nkb; ++i, ++g) {
+          const int sr = g % C::NR, sb = g % C::NB;
+          bool w_ok = mbar_wait(&full_r[sr], (g / C::NR) & 1, err, PF_DEV_TIMEOUT_DEQUANT);
+          if (w_ok) w_ok = mbar_wait(&bempty[sb], ((g / C::NB) & 1) ^ 1, err, PF_DEV_TIMEOUT_DEQUANT);
+          ok = __all_sync(0xffffffffu, w_ok);
+          if (!ok) break;
+          uint8_t* bt = b_ring + sb * C::BT_BYTES;
+          const uint8_t* raw = r_ring + sr * C::RAW_BYTES;
+          for (int it = t; it < BN * 2; it += DQ_THREADS) {
+            const int rr = it % BN, h = it / BN;
+            const uint4 nib = *reinterpret_cast<const uint4*>(raw + (size_t)(h * BN + rr) * 16);
+            const __half d = *reinterpret_cast<const __half*>(raw + BN * 32 + (h * BN + rr) * 2);
+            dequant_block32(nib, d, bt + rr * 128, h, rr & 7);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bfull[sb]);
+            mbar_arrive(&empty_r[sr]);
           }
         }
-      });
+      }
+    }
+    if (split_mode) {
+      // the epilogue warpgroups run the cluster reduction; these warps
+      // take part in its two cluster barriers
+      if (warp == 0 && lane == 0 && cluster_ctarank() == 0)
+        mbar_arrive_expect_tx(red_full, static_cast<uint32_t>(sh.splits - 1) * (BN / 32) * split_chunk_bytes);
+      cluster_sync_all();
+      cluster_sync_all();
     }
   }
 

@@ -497,13 +497,11 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
   int pos_base = static_cast<int>(pos0);
   const __nv_bfloat16* ple_view = c->ple;
   bool gathered = false;
-  bool stopped = false;
 
   for (int il = 0; il < L; ++il) {
     const LayerW& W = c->layers[il];
     if (prune && il == S) {
       if (!is_last) {
-        stopped = true;
         break;
       }
       // keep the output row only: gather it inside the norm
@@ -613,7 +611,6 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
                          [&] { return launch_gemm(c->a_pg, M, W.pp, r, c->err, s); }));
     }
   }
-  (void)stopped;
   if (is_last) {
     const int row = gathered ? 0 : T - 1;
     PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, D * 6.0, [&] {
