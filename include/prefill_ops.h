@@ -54,8 +54,11 @@ int pfop_linear_qkv(int32_t wtype, const void* wq_host, const void* wk_host, con
 
 /* Causal GQA attention: q fp16 [M][Hq*hd] at positions pos_base+m, K/V fp16
    [positions][Hkv*hd] with keys [0, kv_len) valid; out bf16 [M][Hq*hd].
-   mode 0: all rows, in-CTA ordered chunk fold; mode 1: one row (M == 1),
-   split-K chunk partials + ordered warp merge. */
+   Keys are folded in 64-key chunks, the chunks in groups of
+   ceil(ceil(kv_len/64)/16); one CTA per (64-row block, group), then an
+   ordered merge of the group states of rows whose keys span several groups.
+   mode 0: any M; mode 1: one row (M == 1), the KV-shared-layer form (the
+   same kernels; a row's result is the same in both modes). */
 int pfop_attention(int32_t mode, const void* q_dev, const void* k_dev, const void* v_dev, int32_t M, int32_t Hq,
                    int32_t Hkv, int32_t hd, int32_t pos_base, int32_t kv_len, void* out_dev, void* stream);
 
@@ -92,7 +95,8 @@ int pfop_linear_bench(int32_t wtype, const void* w_host, int32_t N, int32_t K, i
    q fp16 [Hq*hd] at position pos; K/V fp16 [positions][Hkv*hd] with keys
    [0, kv_len) valid, pos < kv_len; out bf16 [Hq*hd].
    Scratch: one fixed device array of 2^21 floats (8 MiB) per GPU that loads
-   the library, kept until exit.  A call needs Hq*(pos/64+1)*(hd+2) floats;
+   the library, kept until exit.  A call needs Hq*16*(hd+2) floats when the
+   row's keys span more than one chunk group (see pfop_attention), else none;
    larger requests return PF_E_ARG without touching the GPU.  All calls share
    the array, so calls that overlap on the GPU race: order them on one stream
    or with events.  The first call on a device looks up the array's device

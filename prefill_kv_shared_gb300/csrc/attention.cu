@@ -4,17 +4,23 @@
 // a left fold, in ascending chunk order, of per-chunk partials
 //     (m_j, l_j, o_j):  m_j = max_k s_k,  p_k = fp16(2^((s_k - m_j) c)),
 //                       l_j = sum_k p_k,  o_j = sum_k p_k V_k
-// (s = q.k, c = log2(e)/sqrt(hd)) combined by merge_state().  Two launch forms
-// compute exactly the same fold:
-//   attn_prefill  every row of a ubatch; a CTA walks the chunks in order and
-//                 merges each partial into registers (writing layers, and the
-//                 KV-shared layers when pruning is off);
-//   attn_split    one output row (KV-shared layers after pruning): one CTA per
-//                 chunk writes its partial to global memory, then a warp per
-//                 head folds them in order (a split-K warp reduction).
-// Both run the same warp routine, attn_chunk(), for a chunk, and the same
-// merge_state(); a row's partial does not depend on the other rows in its MMA
-// tile.  So the pruned output row is bit-identical to the unpruned one.
+// (s = q.k, c = log2(e)/sqrt(hd)) combined by merge_state().
+//
+// The chunks are taken in groups of gc consecutive chunks, gc fixed by the
+// number of keys in the launch (attn_group_chunks: at most 16 groups).  A CTA
+// handles one (64-row block, group) pair: it folds the group's chunks in
+// ascending order into a state (m, l, o).  A row whose keys lie in one group
+// writes o / l directly; otherwise each group's state goes to a partials
+// buffer and attn_merge folds the row's group states in ascending order.  So
+// the causal work spreads over many CTAs instead of piling up on the CTAs of
+// the last rows.
+//
+// A row's result depends only on its own position, the keys and gc: the MMA
+// rows of a tile are independent, chunks past a row's position leave its
+// state unchanged, and gc is the same for the ubatch's last row whether the
+// launch carries the whole ubatch (M = T) or that row alone (M = 1, the
+// KV-shared layers after pruning), because both see the same number of keys.
+// So the pruned output row is bit-identical to the unpruned one.
 //
 // MMA rows are (query, head-within-group) pairs: row R = t*G + g for query t
 // and query head kvh*G + g, so the G query heads that share a KV head share
@@ -215,17 +221,30 @@ __device__ __forceinline__ void attn_chunk(uint32_t sq, uint32_t sk, uint32_t sv
 // ---------------------------------------------------------------------------
 // attn_prefill: every row, in-CTA ordered fold
 
+// partials layout: [row t][query head][group (ATTN_MAX_GROUPS)][HD + 2] =
+// o[HD] (not normalised), m, l
+constexpr int ATTN_MAX_GROUPS = 16;
+
+int attn_group_chunks(int kv_len) {
+  const int n_chunks = (kv_len + CHUNK - 1) / CHUNK;
+  const int gc = (n_chunks + ATTN_MAX_GROUPS - 1) / ATTN_MAX_GROUPS;
+  return gc < 1 ? 1 : gc;
+}
+
+// groups that hold keys of the row at position pos
+__host__ __device__ __forceinline__ int attn_row_groups(int pos, int gc) { return (pos / CHUNK) / gc + 1; }
+
 template <int HD, int NW>
 struct PrefillCfg {
   using S = ChunkSmem<HD>;
   static constexpr int ROWS = 16 * NW;
   static constexpr int Q_BYTES = ROWS * S::ROW_BYTES;
   static constexpr int STAGE_BYTES = 2 * S::KV_BYTES;
-  static constexpr int SMEM = Q_BYTES + 2 * STAGE_BYTES;
+  static constexpr int SMEM = Q_BYTES + STAGE_BYTES;  // one K/V stage: two CTAs fit on an SM
 };
 
 template <int HD, int NW>
-__global__ void __launch_bounds__(NW * 32, 1) attn_prefill_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(NW * 32, 2) attn_prefill_kernel(AttnArgs a, float* __restrict__ part, int gc) {
   using S = ChunkSmem<HD>;
   using C = PrefillCfg<HD, NW>;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -234,11 +253,16 @@ __global__ void __launch_bounds__(NW * 32, 1) attn_prefill_kernel(AttnArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tq = lane & 3;
   const int G = a.Hq / a.Hkv;
-  const int kvh = blockIdx.y;
+  const int kvh = blockIdx.y, grp = blockIdx.z;
   const int R0 = blockIdx.x * C::ROWS;
   const int q_stride = a.Hq * HD, kv_stride = a.Hkv * HD;
   const __half* kbase = a.k + kvh * HD;
   const __half* vbase = a.v + kvh * HD;
+  const int t_last = min(a.M - 1, (R0 + C::ROWS - 1) / G);
+  const int last_ch = (a.pos_base + t_last) / CHUNK;
+  const int ch_first = grp * gc;
+  if (ch_first > last_ch) return;  // no keys of this group reach the block's rows
+  const int ch_end = min(last_ch, ch_first + gc - 1);
 
   // queries of this CTA
   const uint32_t sq = smem_u32(smem);
@@ -248,11 +272,7 @@ __global__ void __launch_bounds__(NW * 32, 1) attn_prefill_kernel(AttnArgs a) {
     const bool ok = t < a.M;
     cp_async16(sq + r * S::ROW_BYTES + c * 16, a.q + (size_t)(ok ? t : 0) * q_stride + head * HD + c * 8, ok);
   }
-  const int t_last = min(a.M - 1, (R0 + C::ROWS - 1) / G);
-  const int last_ch = (a.pos_base + t_last) / CHUNK;
-  const uint32_t skv0 = sq + C::Q_BYTES;
-  load_kv_chunk<HD>(skv0, skv0 + S::KV_BYTES, kbase, vbase, kv_stride, a.kv_len, 0, tid, NW * 32);
-  cp_async_commit();
+  const uint32_t sk = sq + C::Q_BYTES, sv = sk + S::KV_BYTES;
 
   // this thread's two rows
   const int Rw = R0 + warp * 16;
@@ -267,140 +287,87 @@ __global__ void __launch_bounds__(NW * 32, 1) attn_prefill_kernel(AttnArgs a) {
 #pragma unroll
   for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
-  for (int ch = 0; ch <= last_ch; ++ch) {
-    if (ch + 1 <= last_ch) {
-      const uint32_t nst = skv0 + ((ch + 1) & 1) * C::STAGE_BYTES;
-      load_kv_chunk<HD>(nst, nst + S::KV_BYTES, kbase, vbase, kv_stride, a.kv_len, ch + 1, tid, NW * 32);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+  for (int ch = ch_first; ch <= ch_end; ++ch) {
+    if (ch != ch_first) __syncthreads();  // every warp is done with the previous chunk
+    load_kv_chunk<HD>(sk, sv, kbase, vbase, kv_stride, a.kv_len, ch, tid, NW * 32);
+    cp_async_commit();
+    cp_async_wait<0>();
     __syncthreads();
     if (warp_pmax >= ch * CHUNK) {
-      const uint32_t st = skv0 + (ch & 1) * C::STAGE_BYTES;
       float mj[2], lj[2];
       MergeAB ab[2];
       bool act[2];
-      attn_chunk<HD>(sq + warp * 16 * S::ROW_BYTES, st, st + S::KV_BYTES, ch, posa, posb, mj, lj,
-                     [&](int grp, float(&oj)[8][4]) {
-                       if (grp == 0) {
-                         act[0] = mj[0] != -INFINITY;
-                         act[1] = mj[1] != -INFINITY;
-                         if (act[0]) ab[0] = merge_state<HD>(m[0], l[0], mj[0], lj[0]);
-                         if (act[1]) ab[1] = merge_state<HD>(m[1], l[1], mj[1], lj[1]);
-                       }
+      attn_chunk<HD>(sq + warp * 16 * S::ROW_BYTES, sk, sv, ch, posa, posb, mj, lj, [&](int dg, float(&oj)[8][4]) {
+        if (dg == 0) {
+          act[0] = mj[0] != -INFINITY;
+          act[1] = mj[1] != -INFINITY;
+          if (act[0]) ab[0] = merge_state<HD>(m[0], l[0], mj[0], lj[0]);
+          if (act[1]) ab[1] = merge_state<HD>(m[1], l[1], mj[1], lj[1]);
+        }
 #pragma unroll
-                       for (int dt = 0; dt < 8; ++dt) {
-                         float* od = o[grp * 8 + dt];
-                         if (act[0]) {
-                           od[0] = merge_o(od[0], oj[dt][0], ab[0]);
-                           od[1] = merge_o(od[1], oj[dt][1], ab[0]);
-                         }
-                         if (act[1]) {
-                           od[2] = merge_o(od[2], oj[dt][2], ab[1]);
-                           od[3] = merge_o(od[3], oj[dt][3], ab[1]);
-                         }
-                       }
-                     });
+        for (int dt = 0; dt < 8; ++dt) {
+          float* od = o[dg * 8 + dt];
+          if (act[0]) {
+            od[0] = merge_o(od[0], oj[dt][0], ab[0]);
+            od[1] = merge_o(od[1], oj[dt][1], ab[0]);
+          }
+          if (act[1]) {
+            od[2] = merge_o(od[2], oj[dt][2], ab[1]);
+            od[3] = merge_o(od[3], oj[dt][3], ab[1]);
+          }
+        }
+      });
     }
-    __syncthreads();
   }
 
-  // out = o / l
+  // a row with one group: out = o / l; otherwise the group state
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const int t = half ? tb : ta;
     if (t >= a.M) continue;
     const int R = Rw + g + 8 * half;
     const int head = kvh * G + R % G;
-    __nv_bfloat16* dst = a.out + (size_t)t * q_stride + head * HD;
+    const int n_g = attn_row_groups(a.pos_base + t, gc);
+    if (n_g == 1) {
+      __nv_bfloat16* dst = a.out + (size_t)t * q_stride + head * HD;
 #pragma unroll
-    for (int dt = 0; dt < HD / 8; ++dt) {
-      const float x0 = __fdiv_rn(o[dt][2 * half], l[half]);
-      const float x1 = __fdiv_rn(o[dt][2 * half + 1], l[half]);
-      *reinterpret_cast<__nv_bfloat162*>(dst + 8 * dt + 2 * tq) = __floats2bfloat162_rn(x0, x1);
+      for (int dt = 0; dt < HD / 8; ++dt) {
+        const float x0 = __fdiv_rn(o[dt][2 * half], l[half]);
+        const float x1 = __fdiv_rn(o[dt][2 * half + 1], l[half]);
+        *reinterpret_cast<__nv_bfloat162*>(dst + 8 * dt + 2 * tq) = __floats2bfloat162_rn(x0, x1);
+      }
+    } else if (grp < n_g) {
+      float* dst = part + (((size_t)t * a.Hq + head) * ATTN_MAX_GROUPS + grp) * (HD + 2);
+#pragma unroll
+      for (int dt = 0; dt < HD / 8; ++dt)
+        *reinterpret_cast<float2*>(dst + 8 * dt + 2 * tq) = make_float2(o[dt][2 * half], o[dt][2 * half + 1]);
+      if (tq == 0) {
+        dst[HD] = m[half];
+        dst[HD + 1] = l[half];
+      }
     }
   }
 }
 
-// ---------------------------------------------------------------------------
-// attn_split: one row; a CTA (one warp) per (chunk, KV head) writes its
-// partial, then attn_merge folds the partials of each head in chunk order.
-// partial layout: [head][chunk][HD + 2] = o_j[HD], m_j, l_j
-
+// Rows t0 .. M-1 (two or more groups): a warp per (row, query head) folds the
+// group states in ascending order; lane owns HD/32 consecutive dims.
 template <int HD>
-struct SplitCfg {
-  using S = ChunkSmem<HD>;
-  static constexpr int Q_BYTES = 16 * S::ROW_BYTES;
-  static constexpr int SMEM = Q_BYTES + 2 * S::KV_BYTES;
-};
-
-template <int HD>
-__global__ void __launch_bounds__(32) attn_split_kernel(AttnArgs a, float* __restrict__ part, int n_chunks) {
-  using S = ChunkSmem<HD>;
-  using C = SplitCfg<HD>;
-  extern __shared__ __align__(16) uint8_t smem[];
-  pdl_launch();
-  pdl_wait();
-  const int lane = threadIdx.x;
-  const int g = lane >> 2, tq = lane & 3;
-  const int ch = blockIdx.x, kvh = blockIdx.y;
-  const int G = a.Hq / a.Hkv;
-  const int kv_stride = a.Hkv * HD;
-  const uint32_t sq = smem_u32(smem);
-  const uint32_t sk = sq + C::Q_BYTES, sv = sk + S::KV_BYTES;
-  for (int i = lane; i < 16 * (HD / 8); i += 32) {
-    const int r = i / (HD / 8), c = i % (HD / 8);
-    const bool ok = r < G;
-    cp_async16(sq + r * S::ROW_BYTES + c * 16, a.q + (ok ? (kvh * G + r) * HD : 0) + c * 8, ok);
-  }
-  load_kv_chunk<HD>(sk, sv, a.k + kvh * HD, a.v + kvh * HD, kv_stride, a.kv_len, ch, lane, 32);
-  cp_async_commit();
-  cp_async_wait<0>();
-  __syncwarp();
-
-  const int pos = a.pos_base;  // the single row's position
-  const int pa = g < G ? pos : -1, pb = g + 8 < G ? pos : -1;
-  float mj[2], lj[2];
-  attn_chunk<HD>(sq, sk, sv, ch, pa, pb, mj, lj, [&](int grp, float(&oj)[8][4]) {
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int r = g + 8 * half;
-      if (r >= G) continue;
-      float* dst = part + ((size_t)(kvh * G + r) * n_chunks + ch) * (HD + 2);
-#pragma unroll
-      for (int dt = 0; dt < 8; ++dt)
-        *reinterpret_cast<float2*>(dst + 64 * grp + 8 * dt + 2 * tq) =
-            make_float2(oj[dt][2 * half], oj[dt][2 * half + 1]);
-    }
-  });
-  if (tq == 0) {
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int r = g + 8 * half;
-      if (r >= G) continue;
-      float* dst = part + ((size_t)(kvh * G + r) * n_chunks + ch) * (HD + 2);
-      dst[HD] = mj[half];
-      dst[HD + 1] = lj[half];
-    }
-  }
-}
-
-// one warp per head; lane owns HD/32 consecutive dims
-template <int HD>
-__global__ void __launch_bounds__(32) attn_merge_kernel(const float* __restrict__ part, int n_chunks, int Hq,
-                                                        __nv_bfloat16* __restrict__ out) {
+__global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict__ part, int M, int Hq, int pos_base,
+                                                         int gc, int t0, __nv_bfloat16* __restrict__ out) {
   constexpr int PER = HD / 32;
   pdl_launch();
   pdl_wait();
-  const int head = blockIdx.x, lane = threadIdx.x;
-  const float* base = part + (size_t)head * n_chunks * (HD + 2);
+  const int lane = threadIdx.x & 31;
+  const int pair = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int t = t0 + pair / Hq, head = pair % Hq;
+  if (t >= M) return;
+  const int n_g = attn_row_groups(pos_base + t, gc);
+  const float* base = part + ((size_t)t * Hq + head) * ATTN_MAX_GROUPS * (HD + 2);
   float m = -INFINITY, l = 0.f, o[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) o[i] = 0.f;
-  for (int ch = 0; ch < n_chunks; ++ch) {
-    const float* p = base + (size_t)ch * (HD + 2);
+  for (int gi = 0; gi < n_g; ++gi) {
+    const float* p = base + (size_t)gi * (HD + 2);
     const float mj = p[HD], lj = p[HD + 1];
     float oj[PER];
 #pragma unroll
@@ -414,7 +381,7 @@ __global__ void __launch_bounds__(32) attn_merge_kernel(const float* __restrict_
 #pragma unroll
     for (int i = 0; i < PER; ++i) o[i] = merge_o(o[i], oj[i], ab);
   }
-  __nv_bfloat16* dst = out + (size_t)head * HD + lane * PER;
+  __nv_bfloat16* dst = out + (size_t)t * Hq * HD + (size_t)head * HD + lane * PER;
 #pragma unroll
   for (int i = 0; i < PER; i += 2)
     *reinterpret_cast<__nv_bfloat162*>(dst + i) = __floats2bfloat162_rn(__fdiv_rn(o[i], l), __fdiv_rn(o[i + 1], l));
@@ -424,7 +391,7 @@ __global__ void __launch_bounds__(32) attn_merge_kernel(const float* __restrict_
 // launchers
 
 template <int HD, int NW>
-static cudaError_t launch_prefill_t(const AttnArgs& a, cudaStream_t s) {
+static cudaError_t launch_prefill_t(const AttnArgs& a, float* part, cudaStream_t s) {
   using C = PrefillCfg<HD, NW>;
   static bool attr = false;
   if (!attr) {
@@ -435,50 +402,49 @@ static cudaError_t launch_prefill_t(const AttnArgs& a, cudaStream_t s) {
   }
   const int G = a.Hq / a.Hkv;
   const int rows = a.M * G;
-  dim3 grid((rows + C::ROWS - 1) / C::ROWS, a.Hkv);
-  return launch_k(attn_prefill_kernel<HD, NW>, grid, dim3(NW * 32), C::SMEM, s, 1, a);
+  const int gc = attn_group_chunks(a.kv_len);
+  const int last_pos = a.pos_base + a.M - 1;
+  const int n_groups = attn_row_groups(last_pos, gc);
+  if (n_groups > 1 && !part) return cudaErrorInvalidValue;
+  dim3 grid((rows + C::ROWS - 1) / C::ROWS, a.Hkv, n_groups);
+  cudaError_t e = launch_k(attn_prefill_kernel<HD, NW>, grid, dim3(NW * 32), C::SMEM, s, 1, a, part, gc);
+  if (e != cudaSuccess || n_groups == 1) return e;
+  const int t0 = a.pos_base >= CHUNK * gc ? 0 : CHUNK * gc - a.pos_base;  // first row with two groups
+  const int pairs = (a.M - t0) * a.Hq;
+  return launch_k(attn_merge_kernel<HD>, dim3((pairs + 3) / 4), dim3(128), 0, s, 1,
+                  static_cast<const float*>(part), a.M, a.Hq, a.pos_base, gc, t0, a.out);
 }
 
 static bool attn_shape_ok(const AttnArgs& a) {
   if (a.Hkv <= 0 || a.Hq % a.Hkv != 0) return false;
   const int G = a.Hq / a.Hkv;
   if (G > 16 || (16 % G) != 0) return false;
+  if (a.pos_base < 0 || a.pos_base + a.M > a.kv_len) return false;
   return a.hd == 64 || a.hd == 256;
 }
 
-cudaError_t launch_attn_prefill(const AttnArgs& a, cudaStream_t s) {
+cudaError_t launch_attn_prefill(const AttnArgs& a, float* partials, cudaStream_t s) {
   if (a.M <= 0) return cudaSuccess;
   if (!attn_shape_ok(a)) return cudaErrorInvalidValue;
-  if (a.hd == 256) return launch_prefill_t<256, 4>(a, s);
-  return launch_prefill_t<64, 4>(a, s);
+  if (a.hd == 256) return launch_prefill_t<256, 4>(a, partials, s);
+  return launch_prefill_t<64, 4>(a, partials, s);
 }
 
-template <int HD>
-static cudaError_t launch_split_t(const AttnArgs& a, float* part, cudaStream_t s) {
-  using C = SplitCfg<HD>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(attn_split_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  const int n_chunks = a.pos_base / CHUNK + 1;
-  cudaError_t e = launch_k(attn_split_kernel<HD>, dim3(n_chunks, a.Hkv), dim3(32), C::SMEM, s, 1, a, part, n_chunks);
-  if (e != cudaSuccess) return e;
-  return launch_k(attn_merge_kernel<HD>, dim3(a.Hq), dim3(32), 0, s, 1, static_cast<const float*>(part), n_chunks,
-                  a.Hq, a.out);
+cudaError_t launch_attn_split(const AttnArgs& a, float* partials, cudaStream_t s) {
+  if (a.M != 1) return cudaErrorInvalidValue;
+  return launch_attn_prefill(a, partials, s);
 }
 
-cudaError_t launch_attn_split(const AttnArgs& a, float* part, cudaStream_t s) {
-  if (a.M != 1 || !attn_shape_ok(a)) return cudaErrorInvalidValue;
-  if (a.hd == 256) return launch_split_t<256>(a, part, s);
-  return launch_split_t<64>(a, part, s);
+int attn_launch_count(const AttnArgs& a) {
+  if (a.M <= 0) return 0;
+  return attn_row_groups(a.pos_base + a.M - 1, attn_group_chunks(a.kv_len)) > 1 ? 2 : 1;
 }
 
-size_t attn_partials_floats(int Hq, int hd, int max_ctx) {
-  const size_t n_chunks = (static_cast<size_t>(max_ctx) + CHUNK - 1) / CHUNK;
-  return static_cast<size_t>(Hq) * n_chunks * (hd + 2);
+size_t attn_partials_floats(int M, int Hq, int hd, int kv_len) {
+  const int gc = attn_group_chunks(kv_len > 0 ? kv_len : 1);
+  const int n_groups = attn_row_groups(kv_len > 0 ? kv_len - 1 : 0, gc);
+  if (n_groups <= 1) return 0;
+  return static_cast<size_t>(M > 0 ? M : 0) * Hq * ATTN_MAX_GROUPS * (hd + 2);
 }
 
 }  // namespace pf

@@ -98,11 +98,15 @@ struct AttnArgs {
   int kv_len = 0;    // keys [0, kv_len) exist in the cache
 };
 
-// every row folds its chunks in ascending order inside one CTA
-cudaError_t launch_attn_prefill(const AttnArgs& a, cudaStream_t s);
-// one row (M == 1): chunk partials in parallel, then an ordered merge
+// Causal attention over (64-row block, chunk group) CTAs; rows whose keys span
+// several groups go through the partials buffer (attn_partials_floats) and an
+// ordered merge.  launch_attn_split is the M == 1 form (same kernels).
+cudaError_t launch_attn_prefill(const AttnArgs& a, float* partials, cudaStream_t s);
 cudaError_t launch_attn_split(const AttnArgs& a, float* partials, cudaStream_t s);
-size_t attn_partials_floats(int Hq, int hd, int max_ctx);
+// floats of partials a launch of M rows over kv_len keys needs (0: none)
+size_t attn_partials_floats(int M, int Hq, int hd, int kv_len);
+int attn_group_chunks(int kv_len);
+int attn_launch_count(const AttnArgs& a);  // kernels launch_attn_prefill starts (1 or 2)
 
 // ---------------------------------------------------------------------------
 // per-row kernels

@@ -12,8 +12,9 @@
 // Limits and sharing:
 //   - the array holds PF_NOALLOC_SCRATCH_FLOATS floats (8 MiB); every GPU
 //     that loads this library keeps it until the process exits;
-//   - a request needs n_head * (pos / 64 + 1) * (head_dim + 2) floats and is
-//     refused (PF_E_ARG) when that is more;
+//   - a request needs n_head * 16 * (head_dim + 2) floats when the row's keys
+//     span more than one chunk group, none otherwise, and is refused
+//     (PF_E_ARG) when that is more than the array holds;
 //   - every call, on every stream, uses the same array: calls whose work
 //     overlaps on the GPU race and give wrong results, so callers must order
 //     them (one stream, or events);
@@ -68,7 +69,7 @@ extern "C" int pfop_attention_split_noalloc(const void* q_dev, const void* k_dev
                                             void* stream) {
   if (!q_dev || !k_dev || !v_dev || !out_dev || pos < 0 || pos >= kv_len || Hq < 1 || Hkv < 1)
     return fail(PF_E_ARG, "bad argument");
-  const size_t need = pf::attn_partials_floats(Hq, hd, pos + 1);
+  const size_t need = pf::attn_partials_floats(1, Hq, hd, kv_len);
   if (need > PF_NOALLOC_SCRATCH_FLOATS)
     return fail(PF_E_ARG, "request needs " + std::to_string(need) + " scratch floats; the fixed array holds " +
                               std::to_string(PF_NOALLOC_SCRATCH_FLOATS));

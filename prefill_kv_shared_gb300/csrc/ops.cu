@@ -302,11 +302,11 @@ extern "C" int pfop_attention(int32_t mode, const void* q_dev, const void* k_dev
   a.kv_len = kv_len;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Scope sc;
+  float* part = nullptr;
+  OP_CUDA(sc.alloc(&part, attn_partials_floats(M, Hq, hd, kv_len) * 4));
   if (mode == 0) {
-    OP_CUDA(launch_attn_prefill(a, s));
+    OP_CUDA(launch_attn_prefill(a, part, s));
   } else {
-    float* part = nullptr;
-    OP_CUDA(sc.alloc(&part, attn_partials_floats(Hq, hd, kv_len) * 4));
     OP_CUDA(launch_attn_split(a, part, s));
   }
   OP_CUDA(cudaStreamSynchronize(s));

@@ -373,7 +373,7 @@ extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weig
     if ((rc = dev_alloc(C, &C->pg, R * C->P * 2)) || (rc = dev_alloc(C, &C->ple, R * C->L * C->P * 2)))
       return fail(nullptr, rc, C->last_error);
   }
-  if ((rc = dev_alloc(C, &C->partials, attn_partials_floats(C->Hq, C->hd, C->d.max_ctx) * 4)))
+  if ((rc = dev_alloc(C, &C->partials, attn_partials_floats(R, C->Hq, C->hd, C->d.max_ctx) * 4)))
     return fail(nullptr, rc, C->last_error);
   if ((rc = dev_alloc(C, &C->cache, static_cast<size_t>(2) * C->L_w * C->d.max_ctx * C->kv * 2)))
     return fail(nullptr, rc, C->last_error);
@@ -551,11 +551,11 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       const double pairs = static_cast<double>(M) * pos_base + 0.5 * M * (M + 1.0);
       const double aflops = pairs * c->Hq * 4.0 * c->hd;
       if (gathered)
-        PF_CUDA(c, counted(c, PF_KC_ATTN, 2, aflops, kv_len * c->kv * 4.0 + M * c->q * 4.0,
+        PF_CUDA(c, counted(c, PF_KC_ATTN, attn_launch_count(a), aflops, kv_len * c->kv * 4.0 + M * c->q * 4.0,
                            [&] { return launch_attn_split(a, c->partials, s); }));
       else
-        PF_CUDA(c, counted(c, PF_KC_ATTN, 1, aflops, kv_len * c->kv * 4.0 + M * c->q * 4.0,
-                           [&] { return launch_attn_prefill(a, s); }));
+        PF_CUDA(c, counted(c, PF_KC_ATTN, attn_launch_count(a), aflops, kv_len * c->kv * 4.0 + M * c->q * 4.0,
+                           [&] { return launch_attn_prefill(a, c->partials, s); }));
     }
     {
       EpiParams e;
