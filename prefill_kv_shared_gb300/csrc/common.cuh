@@ -148,6 +148,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   }
 }
 
+// The same bounded wait for long waits (an epilogue warp waiting for a whole
+// main loop): between polls the thread sleeps about `ns` nanoseconds, so that
+// waiting warps do not take shared-memory and issue bandwidth from the warps
+// that feed the tensor cores.  Wakes at most about `ns` late.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, int* err, int code, uint32_t ns) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(ns);
+    if (mbar_try_wait(a, parity)) return true;
+    if ((i & 255u) == 0u) {
+      if (clock64() - t0 > PF_WAIT_CYCLES) {
+        set_error(err, code);
+        return false;
+      }
+      if (read_error(err) != 0) return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // TMA (bulk async copies into shared memory, completion counted in bytes on
 // an mbarrier)

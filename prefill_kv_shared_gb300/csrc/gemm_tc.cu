@@ -440,6 +440,7 @@ __device__ __forceinline__ void epi_bar_sync() {
 struct GemmShape {
   int M, K;
   int n_tiles, m_blocks, splits, kb_per_split, n_units;
+  int a_box_rows;  // rows of A one TMA box brings (16 for launches of at most 16 rows, else 128)
 };
 
 // Byte offset of (chunk c, row r, 16-byte piece q) in a split partial slot:
@@ -546,7 +547,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         int mt_valid = (sh.M - m_base + 127) / 128;
         if (mt_valid > MT) mt_valid = MT;
         const int buf = C::ACC_BUFS == 2 ? (j & 1) : 0;
-        bool ok = mbar_wait(&tfull[buf], (j / C::ACC_BUFS) & 1, err, PF_DEV_TIMEOUT_EPILOGUE);
+        bool ok = mbar_wait_sleep(&tfull[buf], (j / C::ACC_BUFS) & 1, err, PF_DEV_TIMEOUT_EPILOGUE, 128);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
           epi_ok = false;
@@ -653,91 +654,85 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       // ---------------- producer
       // Weights do not depend on the previous kernel: the first raw stages are
       // fetched before waiting for it.
-      uint32_t pre = 0;
-      if (C::Q4 && lane == 0 && blockIdx.x < sh.n_units) {
+      const uint32_t pre = (C::Q4 && blockIdx.x < sh.n_units) ? (nkb < C::S_R ? nkb : C::S_R) : 0;
+      // one stage per lane: copies issued by one thread are served one after
+      // another, copies issued by different threads overlap
+      if (C::Q4 && static_cast<uint32_t>(lane) < pre) {
         const int u = blockIdx.x;
         const int ks = u % sh.splits, t = u / sh.splits;
         const int nt = t % sh.n_tiles;
-        pre = nkb < C::S_R ? nkb : C::S_R;
-        for (uint32_t x = 0; x < pre; ++x) {
-          mbar_arrive_expect_tx(&full_r[x], C::RAW_BYTES);
-          bulk_load(r_ring + x * C::RAW_BYTES,
-                    wq4 + ((size_t)nt * (sh.splits * nkb) + ks * nkb + x) * C::RAW_BYTES, C::RAW_BYTES, &full_r[x]);
-        }
+        mbar_arrive_expect_tx(&full_r[lane], C::RAW_BYTES);
+        bulk_load(r_ring + lane * C::RAW_BYTES,
+                  wq4 + ((size_t)nt * (sh.splits * nkb) + ks * nkb + lane) * C::RAW_BYTES, C::RAW_BYTES,
+                  &full_r[lane]);
       }
-      pre = __shfl_sync(0xffffffffu, pre, 0);
+      __syncwarp();
       pdl_wait();
-      uint32_t g = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < sh.n_units && ok; u += gridDim.x) {
-        const int ks = u % sh.splits, t = u / sh.splits;
-        const int nt = t % sh.n_tiles, mb = t / sh.n_tiles;
-        const int m_base = mb * MT * 128;
-        int mt_valid = (sh.M - m_base + 127) / 128;
-        if (mt_valid > MT) mt_valid = MT;
-        for (int i = 0; i < nkb; ++i, ++g) {
-          const int kb = ks * nkb + i;
-          const int sa = g % C::S_A;
-          if (lane == 0) ok = mbar_wait(&empty_a[sa], ((g / C::S_A) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
-          if (C::Q4 && lane == 0 && ok && g >= pre)
-            ok = mbar_wait(&empty_r[g % C::NR], ((g / C::NR) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-          if (lane == 0) {
+      // The main loop runs in lane 0 alone: no warp-wide step per k-block.
+      if (lane == 0) {
+        uint32_t g = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < sh.n_units && ok; u += gridDim.x) {
+          const int ks = u % sh.splits, t = u / sh.splits;
+          const int nt = t % sh.n_tiles, mb = t / sh.n_tiles;
+          const int m_base = mb * MT * 128;
+          int mt_valid = (sh.M - m_base + 127) / 128;
+          if (mt_valid > MT) mt_valid = MT;
+          for (int i = 0; i < nkb; ++i, ++g) {
+            const int kb = ks * nkb + i;
+            const int sa = g % C::S_A;
+            ok = mbar_wait(&empty_a[sa], ((g / C::S_A) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
+            const bool raw_now = C::Q4 && g >= pre;
+            const int sr = g % C::NR;
+            if (ok && raw_now) ok = mbar_wait(&empty_r[sr], ((g / C::NR) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
+            if (!ok) break;
             uint8_t* st = a_ring + sa * C::A_STAGE;
-            mbar_arrive_expect_tx(&full_a[sa], mt_valid * 128 * 128 + (C::Q4 ? 0 : C::BT_BYTES));
+            mbar_arrive_expect_tx(&full_a[sa], mt_valid * sh.a_box_rows * 128 + (C::Q4 ? 0 : C::BT_BYTES));
             for (int mt = 0; mt < mt_valid; ++mt)
               tma_load_2d(st + mt * 128 * 128, &tmA, &full_a[sa], kb * 64, m_base + mt * 128);
-            if (C::Q4 && g >= pre) {
-              const int sr = g % C::NR;
+            if (raw_now) {
               mbar_arrive_expect_tx(&full_r[sr], C::RAW_BYTES);
-              bulk_load(r_ring + sr * C::RAW_BYTES,
-                        wq4 + ((size_t)nt * (sh.splits * nkb) + kb) * C::RAW_BYTES, C::RAW_BYTES, &full_r[sr]);
+              bulk_load(r_ring + sr * C::RAW_BYTES, wq4 + ((size_t)nt * (sh.splits * nkb) + kb) * C::RAW_BYTES,
+                        C::RAW_BYTES, &full_r[sr]);
             } else if (!C::Q4) {
               tma_load_2d(st + C::A_BYTES, &tmB, &full_a[sa], kb * 64, nt * BN);
             }
           }
-          __syncwarp();
         }
-      }
-      if (!ok && lane == 0) {
-        // the last S_A / S_R issues may still be in flight
-        const uint32_t ga = g > (uint32_t)C::S_A ? g - C::S_A : 0;
-        for (uint32_t x = ga; x < g; ++x) mbar_drain(&full_a[x % C::S_A], (x / C::S_A) & 1);
-        if (C::Q4) {
-          const uint32_t gr = g > (uint32_t)C::S_R ? g - C::S_R : 0;
-          for (uint32_t x = gr; x < g; ++x) mbar_drain(&full_r[x % C::NR], (x / C::NR) & 1);
+        if (!ok) {
+          // the last S_A / S_R issues may still be in flight
+          const uint32_t ga = g > (uint32_t)C::S_A ? g - C::S_A : 0;
+          for (uint32_t x = ga; x < g; ++x) mbar_drain(&full_a[x % C::S_A], (x / C::S_A) & 1);
+          if (C::Q4) {
+            const uint32_t gr = g > (uint32_t)C::S_R ? g - C::S_R : 0;
+            for (uint32_t x = gr; x < g; ++x) mbar_drain(&full_r[x % C::NR], (x / C::NR) & 1);
+          }
         }
       }
       __syncwarp();
     } else if (warp == 1) {
-      // ---------------- MMA issue
-      constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
-      uint32_t g = 0, j = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < sh.n_units && ok; u += gridDim.x, ++j) {
-        const int t = u / sh.splits;
-        const int mb = t / sh.n_tiles;
-        int mt_valid = (sh.M - mb * MT * 128 + 127) / 128;
-        if (mt_valid > MT) mt_valid = MT;
-        const int buf = C::ACC_BUFS == 2 ? (j & 1) : 0;
-        const uint32_t tacc = tmem_base + buf * C::ACC;
-        if (lane == 0)
+      // ---------------- MMA issue (lane 0 alone)
+      if (lane == 0) {
+        constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
+        uint32_t g = 0, j = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < sh.n_units && ok; u += gridDim.x, ++j) {
+          const int t = u / sh.splits;
+          const int mb = t / sh.n_tiles;
+          int mt_valid = (sh.M - mb * MT * 128 + 127) / 128;
+          if (mt_valid > MT) mt_valid = MT;
+          const int buf = C::ACC_BUFS == 2 ? (j & 1) : 0;
+          const uint32_t tacc = tmem_base + buf * C::ACC;
           ok = mbar_wait(&tempty[buf], ((j / C::ACC_BUFS) & 1) ^ 1, err, PF_DEV_TIMEOUT_MMA);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        tc_fence_after();
-        for (int i = 0; i < nkb; ++i, ++g) {
-          const int sa = g % C::S_A;
-          const int sb = C::Q4 ? g % C::NB : 0;
-          if (lane == 0) {
-            ok = mbar_wait(&full_a[sa], (g / C::S_A) & 1, err, PF_DEV_TIMEOUT_MMA);
-            if (ok && C::Q4) ok = mbar_wait(&bfull[sb], (g / C::NB) & 1, err, PF_DEV_TIMEOUT_MMA);
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           tc_fence_after();
-          if (lane == 0) {
+          for (int i = 0; i < nkb; ++i, ++g) {
+            const int sa = g % C::S_A;
+            const int sb = C::Q4 ? g % C::NB : 0;
+            ok = mbar_wait(&full_a[sa], (g / C::S_A) & 1, err, PF_DEV_TIMEOUT_MMA);
+            if (ok && C::Q4) ok = mbar_wait(&bfull[sb], (g / C::NB) & 1, err, PF_DEV_TIMEOUT_MMA);
+            if (!ok) break;
+            tc_fence_after();
             const uint32_t a0 = smem_u32(a_ring + sa * C::A_STAGE);
             const uint32_t b0 = C::Q4 ? smem_u32(b_ring + sb * C::BT_BYTES) : a0 + C::A_BYTES;
             for (int mt = 0; mt < mt_valid; ++mt) {
@@ -751,16 +746,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             tc_commit(&empty_a[sa]);
             if (C::Q4) tc_commit(&bempty[sb]);
           }
-          __syncwarp();
+          if (ok) tc_commit(&tfull[buf]);  // the unit's accumulator is complete
         }
-        if (lane == 0) tc_commit(&tfull[buf]);  // the unit's accumulator is complete
-        __syncwarp();
-      }
-      if (!ok && lane == 0) {
-        // wait for the MMAs already issued before TMEM is freed
-        tc_commit(&tfull[0]);
-        mbar_drain(&tfull[0], 0);
-        mbar_drain(&tfull[0], 1);
+        if (!ok) {
+          // wait for the MMAs already issued before TMEM is freed
+          tc_commit(&tfull[0]);
+          mbar_drain(&tfull[0], 0);
+          mbar_drain(&tfull[0], 1);
+        }
       }
       __syncwarp();
     } else if (C::Q4) {
@@ -857,7 +850,9 @@ bool make_act_map(ActMat& a, std::string* err) {
     return false;
   }
   std::memset(&a.tmap, 0, sizeof(a.tmap));
-  return encode_2d_bf16(&a.tmap, a.dev, (uint64_t)a.K, (uint64_t)a.rows, 64, 128, err);
+  std::memset(&a.tmap_small, 0, sizeof(a.tmap_small));
+  return encode_2d_bf16(&a.tmap, a.dev, (uint64_t)a.K, (uint64_t)a.rows, 64, 128, err) &&
+         encode_2d_bf16(&a.tmap_small, a.dev, (uint64_t)a.K, (uint64_t)a.rows, 64, 16, err);
 }
 
 bool make_weight_map(WeightMat& w, std::string* err) {
@@ -921,12 +916,17 @@ static cudaError_t launch_t(const ActMat& A, int M, const WeightMat& W, const Ep
   sh.splits = W.split;
   sh.kb_per_split = (W.K / 64) / W.split;
   sh.n_units = sh.n_tiles * sh.m_blocks * sh.splits;
+  // A launch of at most 16 rows fetches 16-row A boxes: the MMA still reads
+  // 128 rows, and rows 16..127 (stale shared memory) only reach accumulator
+  // rows that are never stored.
+  const bool small = MT == 1 && M <= 16;
+  sh.a_box_rows = small ? 16 : 128;
   if (W.split > 1 && static_cast<size_t>(W.split - 1) * 128 * BN * 4 > ring_bytes<WK, BN, MT>())
     return cudaErrorInvalidValue;
   const int cluster = W.split > 1 ? W.split : 1;
   const int grid = W.split > 1 ? sh.n_units : (sh.n_units < sm_count() ? sh.n_units : sm_count());
-  return launch_k(gemm_tc_kernel<WK, BN, MT>, dim3(grid), dim3(GEMM_THREADS), C::SMEM_BYTES, s, cluster, A.tmap,
-                  W.tmap, static_cast<const uint8_t*>(W.dev), sh, ep, err);
+  return launch_k(gemm_tc_kernel<WK, BN, MT>, dim3(grid), dim3(GEMM_THREADS), C::SMEM_BYTES, s, cluster,
+                  small ? A.tmap_small : A.tmap, W.tmap, static_cast<const uint8_t*>(W.dev), sh, ep, err);
 }
 
 cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err, cudaStream_t s) {

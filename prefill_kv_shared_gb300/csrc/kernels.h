@@ -67,7 +67,8 @@ struct WeightMat {
 struct ActMat {
   const __nv_bfloat16* dev = nullptr;
   int rows = 0, K = 0;
-  CUtensorMap tmap;
+  CUtensorMap tmap;        // 128-row boxes
+  CUtensorMap tmap_small;  // 16-row boxes, for launches of at most 16 rows
 };
 
 bool make_act_map(ActMat& a, std::string* err);
