@@ -67,15 +67,22 @@ __host__ __device__ constexpr int pow2_cols(int c) { return c <= 32 ? 32 : c <= 
 template <int WK, int BN, int MT>
 struct GemmCfg {
   static constexpr bool Q4 = WK == W_Q4;
-  static constexpr int A_BYTES = MT * 128 * 128;  // MT tiles of 128 rows x 64 bf16
-  static constexpr int BT_BYTES = BN * 128;       // one bf16 B tile (BN rows x 64)
-  static constexpr int RAW_BYTES = Q4 ? BN * 36 : 0;
+  // 64-wide k-blocks per pipeline stage: every stage costs the copy engine,
+  // the barriers and the dequant warps a fixed amount whatever its size, so
+  // narrow tiles take two k-blocks a stage where shared memory allows.
+  static constexpr int KS = (Q4 && BN == 128 && MT == 1) ? 2 : 1;
+  static constexpr int A_KB = MT * 128 * 128;  // one k-block of A: MT tiles of 128 rows x 64 bf16
+  static constexpr int BT_KB = BN * 128;       // one k-block of bf16 B (BN rows x 64)
+  static constexpr int RAW_KB = Q4 ? BN * 36 : 0;
+  static constexpr int A_BYTES = KS * A_KB;    // stage layouts: [k-block][M tile][128 x 128 B], [k-block][BN x 128 B]
+  static constexpr int BT_BYTES = KS * BT_KB;
+  static constexpr int RAW_BYTES = KS * RAW_KB;
   static constexpr int A_STAGE = A_BYTES + (Q4 ? 0 : BT_BYTES);
   // The dequantised B ring bounds how far the dequant warps run ahead of the
   // MMAs (B stage k+S_B is written once the MMAs of stage k are done); the
   // A ring takes what the B and raw rings and the epilogue staging leave.
-  static constexpr int S_B = Q4 ? (BN >= 256 ? (MT == 2 ? 2 : 3) : 4) : 0;
-  static constexpr int S_R = Q4 ? (BN >= 256 ? 3 : 6) : 0;
+  static constexpr int S_B = Q4 ? (BN >= 256 ? (MT == 2 ? 2 : 3) : (KS == 2 ? 2 : 4)) : 0;
+  static constexpr int S_R = Q4 ? (BN >= 256 ? 3 : (KS == 2 ? 3 : 6)) : 0;
   static constexpr int NB = S_B > 0 ? S_B : 1;  // ring moduli (the rings are unused without Q4)
   static constexpr int NR = S_R > 0 ? S_R : 1;
   static constexpr int RAW_RING = (S_R * RAW_BYTES + 1023) / 1024 * 1024;
@@ -654,16 +661,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       // ---------------- producer
       // Weights do not depend on the previous kernel: the first raw stages are
       // fetched before waiting for it.
-      const uint32_t pre = (C::Q4 && blockIdx.x < sh.n_units) ? (nkb < C::S_R ? nkb : C::S_R) : 0;
+      const int nst = (nkb + C::KS - 1) / C::KS;  // pipeline stages per unit
+      const uint32_t pre = (C::Q4 && blockIdx.x < sh.n_units) ? (nst < C::S_R ? nst : C::S_R) : 0;
       // one stage per lane: copies issued by one thread are served one after
       // another, copies issued by different threads overlap
       if (C::Q4 && static_cast<uint32_t>(lane) < pre) {
         const int u = blockIdx.x;
         const int ks = u % sh.splits, t = u / sh.splits;
         const int nt = t % sh.n_tiles;
-        mbar_arrive_expect_tx(&full_r[lane], C::RAW_BYTES);
+        const int kc = nkb - lane * C::KS < C::KS ? nkb - lane * C::KS : C::KS;
+        mbar_arrive_expect_tx(&full_r[lane], kc * C::RAW_KB);
         bulk_load(r_ring + lane * C::RAW_BYTES,
-                  wq4 + ((size_t)nt * (sh.splits * nkb) + ks * nkb + lane) * C::RAW_BYTES, C::RAW_BYTES,
+                  wq4 + ((size_t)nt * (sh.splits * nkb) + ks * nkb + lane * C::KS) * C::RAW_KB, kc * C::RAW_KB,
                   &full_r[lane]);
       }
       __syncwarp();
@@ -678,8 +687,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           const int m_base = mb * MT * 128;
           int mt_valid = (sh.M - m_base + 127) / 128;
           if (mt_valid > MT) mt_valid = MT;
-          for (int i = 0; i < nkb; ++i, ++g) {
-            const int kb = ks * nkb + i;
+          for (int i = 0; i < nst; ++i, ++g) {
+            const int kb = ks * nkb + i * C::KS;  // first k-block of the stage
+            const int kc = nkb - i * C::KS < C::KS ? nkb - i * C::KS : C::KS;
             const int sa = g % C::S_A;
             ok = mbar_wait(&empty_a[sa], ((g / C::S_A) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
             const bool raw_now = C::Q4 && g >= pre;
@@ -687,13 +697,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (ok && raw_now) ok = mbar_wait(&empty_r[sr], ((g / C::NR) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
             if (!ok) break;
             uint8_t* st = a_ring + sa * C::A_STAGE;
-            mbar_arrive_expect_tx(&full_a[sa], mt_valid * sh.a_box_rows * 128 + (C::Q4 ? 0 : C::BT_BYTES));
-            for (int mt = 0; mt < mt_valid; ++mt)
-              tma_load_2d(st + mt * 128 * 128, &tmA, &full_a[sa], kb * 64, m_base + mt * 128);
+            mbar_arrive_expect_tx(&full_a[sa], kc * mt_valid * sh.a_box_rows * 128 + (C::Q4 ? 0 : C::BT_BYTES));
+            for (int j = 0; j < kc; ++j)
+              for (int mt = 0; mt < mt_valid; ++mt)
+                tma_load_2d(st + (j * MT + mt) * 128 * 128, &tmA, &full_a[sa], (kb + j) * 64, m_base + mt * 128);
             if (raw_now) {
-              mbar_arrive_expect_tx(&full_r[sr], C::RAW_BYTES);
-              bulk_load(r_ring + sr * C::RAW_BYTES, wq4 + ((size_t)nt * (sh.splits * nkb) + kb) * C::RAW_BYTES,
-                        C::RAW_BYTES, &full_r[sr]);
+              mbar_arrive_expect_tx(&full_r[sr], kc * C::RAW_KB);
+              bulk_load(r_ring + sr * C::RAW_BYTES, wq4 + ((size_t)nt * (sh.splits * nkb) + kb) * C::RAW_KB,
+                        kc * C::RAW_KB, &full_r[sr]);
             } else if (!C::Q4) {
               tma_load_2d(st + C::A_BYTES, &tmB, &full_a[sa], kb * 64, nt * BN);
             }
@@ -726,7 +737,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           ok = mbar_wait(&tempty[buf], ((j / C::ACC_BUFS) & 1) ^ 1, err, PF_DEV_TIMEOUT_MMA);
           if (!ok) break;
           tc_fence_after();
-          for (int i = 0; i < nkb; ++i, ++g) {
+          const int nst = (nkb + C::KS - 1) / C::KS;
+          for (int i = 0; i < nst; ++i, ++g) {
+            const int kc = nkb - i * C::KS < C::KS ? nkb - i * C::KS : C::KS;
             const int sa = g % C::S_A;
             const int sb = C::Q4 ? g % C::NB : 0;
             ok = mbar_wait(&full_a[sa], (g / C::S_A) & 1, err, PF_DEV_TIMEOUT_MMA);
@@ -735,12 +748,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             tc_fence_after();
             const uint32_t a0 = smem_u32(a_ring + sa * C::A_STAGE);
             const uint32_t b0 = C::Q4 ? smem_u32(b_ring + sb * C::BT_BYTES) : a0 + C::A_BYTES;
-            for (int mt = 0; mt < mt_valid; ++mt) {
+            for (int j = 0; j < kc; ++j) {
+              const int kbl = i * C::KS + j;  // k-block within the unit
+              for (int mt = 0; mt < mt_valid; ++mt) {
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = sdesc_sw128(a0 + mt * 128 * 128 + kk * 32);
-                const uint64_t bd = sdesc_sw128(b0 + kk * 32);
-                tc_mma_f16(tacc + mt * BN, ad, bd, idesc, (i | kk) != 0 ? 1u : 0u);
+                for (int kk = 0; kk < 4; ++kk) {
+                  const uint64_t ad = sdesc_sw128(a0 + (j * MT + mt) * 128 * 128 + kk * 32);
+                  const uint64_t bd = sdesc_sw128(b0 + j * C::BT_KB + kk * 32);
+                  tc_mma_f16(tacc + mt * BN, ad, bd, idesc, (kbl | kk) != 0 ? 1u : 0u);
+                }
               }
             }
             tc_commit(&empty_a[sa]);
@@ -761,8 +777,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int t = dq_index(warp, lane);
       uint32_t g = 0;
       bool ok = true;
+      const int nst = (nkb + C::KS - 1) / C::KS;
       for (int u = blockIdx.x; u < sh.n_units && ok; u += gridDim.x) {
-        for (int i = 0; i < nkb; ++i, ++g) {
+        for (int i = 0; i < nst; ++i, ++g) {
+          const int kc = nkb - i * C::KS < C::KS ? nkb - i * C::KS : C::KS;
           const int sr = g % C::NR, sb = g % C::NB;
           bool w_ok = mbar_wait(&full_r[sr], (g / C::NR) & 1, err, PF_DEV_TIMEOUT_DEQUANT);
           if (w_ok) w_ok = mbar_wait(&bempty[sb], ((g / C::NB) & 1) ^ 1, err, PF_DEV_TIMEOUT_DEQUANT);
@@ -770,11 +788,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           if (!ok) break;
           uint8_t* bt = b_ring + sb * C::BT_BYTES;
           const uint8_t* raw = r_ring + sr * C::RAW_BYTES;
-          for (int it = t; it < BN * 2; it += DQ_THREADS) {
-            const int rr = it % BN, h = it / BN;
-            const uint4 nib = *reinterpret_cast<const uint4*>(raw + (size_t)(h * BN + rr) * 16);
-            const __half d = *reinterpret_cast<const __half*>(raw + BN * 32 + (h * BN + rr) * 2);
-            dequant_block32(nib, d, bt + rr * 128, h, rr & 7);
+          // items: (k-block j, half h, row rr); a thread takes two at a time
+          // so that their shared-memory loads overlap
+          const int items = kc * BN * 2;
+          for (int it = t; it < items; it += 2 * DQ_THREADS) {
+            const int it2 = it + DQ_THREADS;
+            const int j = it / (BN * 2), rr = it % BN, h = (it / BN) & 1;
+            const uint8_t* rj = raw + j * C::RAW_KB;
+            const uint4 nib = *reinterpret_cast<const uint4*>(rj + (size_t)(h * BN + rr) * 16);
+            const __half d = *reinterpret_cast<const __half*>(rj + BN * 32 + (h * BN + rr) * 2);
+            if (it2 < items) {
+              const int j2 = it2 / (BN * 2), rr2 = it2 % BN, h2 = (it2 / BN) & 1;
+              const uint8_t* rj2 = raw + j2 * C::RAW_KB;
+              const uint4 nib2 = *reinterpret_cast<const uint4*>(rj2 + (size_t)(h2 * BN + rr2) * 16);
+              const __half d2 = *reinterpret_cast<const __half*>(rj2 + BN * 32 + (h2 * BN + rr2) * 2);
+              dequant_block32(nib, d, bt + j * C::BT_KB + rr * 128, h, rr & 7);
+              dequant_block32(nib2, d2, bt + j2 * C::BT_KB + rr2 * 128, h2, rr2 & 7);
+            } else {
+              dequant_block32(nib, d, bt + j * C::BT_KB + rr * 128, h, rr & 7);
+            }
           }
           fence_proxy_async_smem();
           __syncwarp();
