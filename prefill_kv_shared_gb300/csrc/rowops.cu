@@ -97,6 +97,13 @@ cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t s) {
 
 constexpr int NORM_THREADS = 128;
 
+// One CTA per row.  Rows of up to NORM_THREADS*4*NORM_VEC elements are read
+// once and kept in registers between the sum of squares and the scaling;
+// longer rows are read twice.  The reduction order (per-thread fmaf over the
+// thread's vectors in index order, xor-shuffle tree, warps in order) is the
+// same either way.
+constexpr int NORM_VEC = 8;
+
 __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(const float* __restrict__ x, int row0, int D,
                                                                const float* __restrict__ gain, float eps,
                                                                __nv_bfloat16* __restrict__ y,
@@ -107,13 +114,32 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(const float* __re
   const int i = blockIdx.x;
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)(row0 + i) * D);
   const int nv = D / 4;
+  const bool in_regs = nv <= NORM_THREADS * NORM_VEC;
+  float4 keep[NORM_VEC];
   float ss = 0.f;
-  for (int v = threadIdx.x; v < nv; v += NORM_THREADS) {
-    const float4 a = xr[v];
-    ss = __fmaf_rn(a.x, a.x, ss);
-    ss = __fmaf_rn(a.y, a.y, ss);
-    ss = __fmaf_rn(a.z, a.z, ss);
-    ss = __fmaf_rn(a.w, a.w, ss);
+  if (in_regs) {
+#pragma unroll
+    for (int k = 0; k < NORM_VEC; ++k) {
+      const int v = threadIdx.x + k * NORM_THREADS;
+      keep[k] = v < nv ? xr[v] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < NORM_VEC; ++k) {
+      if (threadIdx.x + k * NORM_THREADS >= nv) break;
+      const float4 a = keep[k];
+      ss = __fmaf_rn(a.x, a.x, ss);
+      ss = __fmaf_rn(a.y, a.y, ss);
+      ss = __fmaf_rn(a.z, a.z, ss);
+      ss = __fmaf_rn(a.w, a.w, ss);
+    }
+  } else {
+    for (int v = threadIdx.x; v < nv; v += NORM_THREADS) {
+      const float4 a = xr[v];
+      ss = __fmaf_rn(a.x, a.x, ss);
+      ss = __fmaf_rn(a.y, a.y, ss);
+      ss = __fmaf_rn(a.z, a.z, ss);
+      ss = __fmaf_rn(a.w, a.w, ss);
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
@@ -125,8 +151,7 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(const float* __re
   const float r = rsqrtf(__fadd_rn(__fdiv_rn(tot, static_cast<float>(D)), eps));
   const float4* g4 = reinterpret_cast<const float4*>(gain);
   __nv_bfloat16* yr = y + (size_t)i * D;
-  for (int v = threadIdx.x; v < nv; v += NORM_THREADS) {
-    const float4 a = xr[v];
+  auto emit = [&](int v, const float4 a) {
     const float4 g = g4[v];
     const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * r * (1.f + g.x), a.y * r * (1.f + g.y));
     const __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * r * (1.f + g.z), a.w * r * (1.f + g.w));
@@ -135,6 +160,16 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(const float* __re
     w.y = *reinterpret_cast<const uint32_t*>(&hi);
     reinterpret_cast<uint2*>(yr)[v] = w;
     if (x_copy) reinterpret_cast<float4*>(x_copy + (size_t)i * D)[v] = a;
+  };
+  if (in_regs) {
+#pragma unroll
+    for (int k = 0; k < NORM_VEC; ++k) {
+      const int v = threadIdx.x + k * NORM_THREADS;
+      if (v >= nv) break;
+      emit(v, keep[k]);
+    }
+  } else {
+    for (int v = threadIdx.x; v < nv; v += NORM_THREADS) emit(v, xr[v]);
   }
 }
 
