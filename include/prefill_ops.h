@@ -25,7 +25,7 @@ extern "C" {
 #endif
 
 /* out[m][n] = sum_k A[m][k] W[n][k] (fp32 [M][N]); W [N][K] in wtype
-   (PF_W_Q4_0 blocks or fp32, computed as bf16).  bn: N-tile, 128 or 256. */
+   (PF_W_Q4_0 blocks or fp32, computed as bf16).  bn: N-tile, 64, 128 or 256. */
 int pfop_linear_f32(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn, const void* a_dev,
                     int32_t a_rows, int32_t M, float* out_dev, void* stream);
 

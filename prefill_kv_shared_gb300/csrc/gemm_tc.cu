@@ -70,7 +70,7 @@ struct GemmCfg {
   // 64-wide k-blocks per pipeline stage: every stage costs the copy engine,
   // the barriers and the dequant warps a fixed amount whatever its size, so
   // narrow tiles take two k-blocks a stage where shared memory allows.
-  static constexpr int KS = (Q4 && BN == 128 && MT == 1) ? 2 : 1;
+  static constexpr int KS = (Q4 && BN <= 128 && MT == 1) ? 2 : 1;
   static constexpr int A_KB = MT * 128 * 128;  // one k-block of A: MT tiles of 128 rows x 64 bf16
   static constexpr int BT_KB = BN * 128;       // one k-block of bf16 B (BN rows x 64)
   static constexpr int RAW_KB = Q4 ? BN * 36 : 0;
@@ -81,8 +81,8 @@ struct GemmCfg {
   // The dequantised B ring bounds how far the dequant warps run ahead of the
   // MMAs (B stage k+S_B is written once the MMAs of stage k are done); the
   // A ring takes what the B and raw rings and the epilogue staging leave.
-  static constexpr int S_B = Q4 ? (BN >= 256 ? (MT == 2 ? 2 : 3) : (KS == 2 ? 2 : 4)) : 0;
-  static constexpr int S_R = Q4 ? (BN >= 256 ? 3 : (KS == 2 ? 3 : 6)) : 0;
+  static constexpr int S_B = Q4 ? (BN >= 256 ? (MT == 2 ? 2 : 3) : KS == 2 ? (BN == 64 ? 4 : 2) : 4) : 0;
+  static constexpr int S_R = Q4 ? (BN >= 256 ? 3 : KS == 2 ? (BN == 64 ? 6 : 3) : 6) : 0;
   static constexpr int NB = S_B > 0 ? S_B : 1;  // ring moduli (the rings are unused without Q4)
   static constexpr int NR = S_R > 0 ? S_R : 1;
   static constexpr int RAW_RING = (S_R * RAW_BYTES + 1023) / 1024 * 1024;
@@ -911,8 +911,9 @@ static size_t ring_bytes() {
 }
 
 static size_t ring_bytes_mt1(int kind, int BN) {
-  if (kind == W_Q4) return BN == 256 ? ring_bytes<W_Q4, 256, 1>() : ring_bytes<W_Q4, 128, 1>();
-  return BN == 256 ? ring_bytes<W_BF16, 256, 1>() : ring_bytes<W_BF16, 128, 1>();
+  if (kind == W_Q4)
+    return BN == 256 ? ring_bytes<W_Q4, 256, 1>() : BN == 64 ? ring_bytes<W_Q4, 64, 1>() : ring_bytes<W_Q4, 128, 1>();
+  return BN == 256 ? ring_bytes<W_BF16, 256, 1>() : BN == 64 ? ring_bytes<W_BF16, 64, 1>() : ring_bytes<W_BF16, 128, 1>();
 }
 
 int choose_split(int kind, int N_rows, int BN, int K, int max_rows) {
@@ -973,8 +974,10 @@ cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiPar
 #define PF_GEMM_CASE(WKV, BNV)                                                    \
   if (W.kind == WKV && W.BN == BNV)                                               \
     return two ? launch_t<WKV, BNV, 2>(A, M, W, ep, err, s) : launch_t<WKV, BNV, 1>(A, M, W, ep, err, s);
+  PF_GEMM_CASE(W_Q4, 64)
   PF_GEMM_CASE(W_Q4, 128)
   PF_GEMM_CASE(W_Q4, 256)
+  PF_GEMM_CASE(W_BF16, 64)
   PF_GEMM_CASE(W_BF16, 128)
   PF_GEMM_CASE(W_BF16, 256)
 #undef PF_GEMM_CASE

@@ -109,7 +109,7 @@ void pf::set_op_error(const std::string& m) { g_err = m; }
 
 extern "C" int pfop_linear_f32(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn, const void* a_dev,
                                int32_t a_rows, int32_t M, float* out_dev, void* stream) {
-  if (!w_host || !a_dev || !out_dev || N < 1 || M < 1 || M > a_rows || (bn != 128 && bn != 256))
+  if (!w_host || !a_dev || !out_dev || N < 1 || M < 1 || M > a_rows || (bn != 64 && bn != 128 && bn != 256))
     return op_fail(PF_E_ARG, "bad argument");
   Scope sc;
   WeightMat W;
@@ -129,7 +129,7 @@ extern "C" int pfop_linear_f32(int32_t wtype, const void* w_host, int32_t N, int
 extern "C" int pfop_linear_bench(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn, int32_t split,
                                  const void* a_dev, int32_t a_rows, int32_t M, float* out_dev, int32_t warmup,
                                  int32_t iters, float* us, void* stream) {
-  if (!w_host || !a_dev || !out_dev || !us || N < 1 || N % 4 || M < 1 || M > a_rows || (bn != 128 && bn != 256) ||
+  if (!w_host || !a_dev || !out_dev || !us || N < 1 || N % 4 || M < 1 || M > a_rows || (bn != 64 && bn != 128 && bn != 256) ||
       iters < 1 || warmup < 0 || split < 0)
     return op_fail(PF_E_ARG, "bad argument");
   Scope sc;

@@ -337,7 +337,9 @@ extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weig
     if ((rc = build_weight(C, L.down, plain_rows(lw.w_down, C->D, C->F, wt, 128), C->F, 128)))
       return fail(nullptr, rc, C->last_error);
     if (C->P > 0) {
-      if ((rc = build_weight(C, L.pg, plain_rows(lw.ple_gate, C->P, C->D, wt, 128), C->D, 128)))
+      // the PLE gate has few output rows: 64-row tiles give it more CTAs
+      const int bn_pg = C->P <= 512 ? 64 : 128;
+      if ((rc = build_weight(C, L.pg, plain_rows(lw.ple_gate, C->P, C->D, wt, bn_pg), C->D, bn_pg)))
         return fail(nullptr, rc, C->last_error);
       if ((rc = build_weight(C, L.pp, plain_rows(lw.ple_proj, C->D, C->P, wt, 128), C->P, 128)))
         return fail(nullptr, rc, C->last_error);

@@ -47,6 +47,9 @@ GEMM_CASES = [
     (Q4, 257, 512, 2048, 256),
     (F32, 64, 256, 256, 128),
     (F32, 200, 384, 512, 256),
+    (Q4, 512, 256, 1536, 64),
+    (Q4, 3, 192, 512, 64),
+    (F32, 100, 128, 256, 64),
 ]
 
 
@@ -66,7 +69,7 @@ def test_linear_f32(lib, wtype, M, N, K, bn):
     assert rel_err(got, ref_exact) < 2e-2
 
 
-@pytest.mark.parametrize("wtype,bn", [(Q4, 128), (Q4, 256), (F32, 128)])
+@pytest.mark.parametrize("wtype,bn", [(Q4, 64), (Q4, 128), (Q4, 256), (F32, 128)])
 def test_linear_row_independent_of_m(lib, wtype, bn):
     """A row's result is bit-identical whether the launch carries 512 rows or 1."""
     rng = np.random.default_rng(3)
