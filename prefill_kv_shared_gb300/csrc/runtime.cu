@@ -33,11 +33,18 @@ struct DevBuf {
 struct LayerW {
   WeightMat qkv;  // writing layers: [Wq; Wk; Wv]; KV-shared layers: Wq
   WeightMat o, gu, down, pg, pp;
+  // KV-shared layers: the same matrices in 64-row tiles with the same k-split,
+  // for the single-row launches after pruning (more CTAs; a row's result
+  // does not depend on the tile width, so the pruned row keeps its bits)
+  WeightMat o1, gu1, down1, pp1;
   float* attn_norm = nullptr;
   float* ffn_norm = nullptr;
 };
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+// the weight a launch of M rows uses: the single-row copy when there is one
+const WeightMat& pick(const WeightMat& full, const WeightMat& one, int M) { return M == 1 && one.dev ? one : full; }
 
 }  // namespace
 
@@ -129,12 +136,14 @@ int upload(prefill_ctx* c, T** out, const void* host, size_t bytes) {
 size_t row_bytes(int wtype, int K) { return wtype == PF_W_Q4_0 ? static_cast<size_t>(K / 32) * 18 : static_cast<size_t>(K) * 4; }
 
 // rows: sources of the stored rows in tile order (null = zero row)
-int build_weight(prefill_ctx* c, WeightMat& w, const std::vector<const void*>& rows, int K, int BN) {
+// split_as: 0 = choose the k-split for this shape; otherwise use that split
+int build_weight(prefill_ctx* c, WeightMat& w, const std::vector<const void*>& rows, int K, int BN, int split_as = 0) {
   w.K = K;
   w.BN = BN;
   w.N_rows = static_cast<int>(rows.size());
   if (w.N_rows % BN != 0 || K % 64 != 0) return fail(c, PF_E_ARG, "weight shape not tileable");
-  w.split = choose_split(c->d.wtype == PF_W_Q4_0 ? W_Q4 : W_BF16, w.N_rows, BN, K, c->d.ubatch_max);
+  w.split = split_as > 0 ? split_as
+                         : choose_split(c->d.wtype == PF_W_Q4_0 ? W_Q4 : W_BF16, w.N_rows, BN, K, c->d.ubatch_max);
   std::string err;
   if (c->d.wtype == PF_W_Q4_0) {
     w.kind = W_Q4;
@@ -321,20 +330,34 @@ extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weig
       rows.resize(round_up(static_cast<int>(rows.size()), bn_qkv), nullptr);
       if ((rc = build_weight(C, L.qkv, rows, C->D, bn_qkv))) return fail(nullptr, rc, C->last_error);
     }
+    // KV-shared layers of a model that can prune also get 64-row copies
+    const bool single_row_copies = !writes && C->S > 0 && C->D % 64 == 0 && C->F % 32 == 0;
     if ((rc = build_weight(C, L.o, plain_rows(lw.wo, C->D, C->q, wt, 128), C->q, 128)))
+      return fail(nullptr, rc, C->last_error);
+    if (single_row_copies &&
+        (rc = build_weight(C, L.o1, plain_rows(lw.wo, C->D, C->q, wt, 64), C->q, 64, L.o.split)))
       return fail(nullptr, rc, C->last_error);
     {
       // gate/up interleaved per tile: BN/2 gate rows, then the same BN/2 up rows
-      const int bn = C->F % 128 == 0 ? 256 : 128, half = bn / 2;
-      const size_t rb = row_bytes(wt, C->D);
-      std::vector<const void*> rows;
-      for (int t = 0; t < C->F / half; ++t) {
-        for (int i = 0; i < half; ++i) rows.push_back(static_cast<const uint8_t*>(lw.w_gate) + (t * half + i) * rb);
-        for (int i = 0; i < half; ++i) rows.push_back(static_cast<const uint8_t*>(lw.w_up) + (t * half + i) * rb);
-      }
-      if ((rc = build_weight(C, L.gu, rows, C->D, bn))) return fail(nullptr, rc, C->last_error);
+      auto gu_rows = [&](int bn) {
+        const int half = bn / 2;
+        const size_t rb = row_bytes(wt, C->D);
+        std::vector<const void*> rows;
+        for (int t = 0; t < C->F / half; ++t) {
+          for (int i = 0; i < half; ++i) rows.push_back(static_cast<const uint8_t*>(lw.w_gate) + (t * half + i) * rb);
+          for (int i = 0; i < half; ++i) rows.push_back(static_cast<const uint8_t*>(lw.w_up) + (t * half + i) * rb);
+        }
+        return rows;
+      };
+      const int bn = C->F % 128 == 0 ? 256 : 128;
+      if ((rc = build_weight(C, L.gu, gu_rows(bn), C->D, bn))) return fail(nullptr, rc, C->last_error);
+      if (single_row_copies && (rc = build_weight(C, L.gu1, gu_rows(64), C->D, 64, L.gu.split)))
+        return fail(nullptr, rc, C->last_error);
     }
     if ((rc = build_weight(C, L.down, plain_rows(lw.w_down, C->D, C->F, wt, 128), C->F, 128)))
+      return fail(nullptr, rc, C->last_error);
+    if (single_row_copies &&
+        (rc = build_weight(C, L.down1, plain_rows(lw.w_down, C->D, C->F, wt, 64), C->F, 64, L.down.split)))
       return fail(nullptr, rc, C->last_error);
     if (C->P > 0) {
       // the PLE gate has few output rows: 64-row tiles give it more CTAs
@@ -342,6 +365,9 @@ extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weig
       if ((rc = build_weight(C, L.pg, plain_rows(lw.ple_gate, C->P, C->D, wt, bn_pg), C->D, bn_pg)))
         return fail(nullptr, rc, C->last_error);
       if ((rc = build_weight(C, L.pp, plain_rows(lw.ple_proj, C->D, C->P, wt, 128), C->P, 128)))
+        return fail(nullptr, rc, C->last_error);
+      if (single_row_copies &&
+          (rc = build_weight(C, L.pp1, plain_rows(lw.ple_proj, C->D, C->P, wt, 64), C->P, 64, L.pp.split)))
         return fail(nullptr, rc, C->last_error);
     }
     if ((rc = upload(C, &L.attn_norm, lw.attn_norm, C->D * 4))) return fail(nullptr, rc, C->last_error);
@@ -566,7 +592,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.out_f32 = xcur;
       e.ld_f32 = D;
       PF_CUDA(c, counted(c, PF_KC_GEMM, 1, 2.0 * M * D * c->q, M * c->q * 2.0 + gemm_wbytes(c, D, c->q) + M * D * 8.0,
-                         [&] { return launch_gemm(c->a_att, M, W.o, e, c->err, s); }));
+                         [&] { return launch_gemm(c->a_att, M, pick(W.o, W.o1, M), e, c->err, s); }));
     }
     PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, M * D * 6.0, [&] {
                return launch_rmsnorm(xcur, 0, M, D, W.ffn_norm, c->d.rms_eps, c->y, nullptr, s);
@@ -579,7 +605,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.ld_bf16 = c->F;
       e.act = c->d.ffn_kind == PF_FFN_GEGLU ? 0 : 1;
       PF_CUDA(c, counted(c, PF_KC_GEMM, 1, 4.0 * M * c->F * D, M * D * 2.0 + gemm_wbytes(c, 2.0 * c->F, D) + M * c->F * 2.0,
-                         [&] { return launch_gemm(c->a_y, M, W.gu, e, c->err, s); }));
+                         [&] { return launch_gemm(c->a_y, M, pick(W.gu, W.gu1, M), e, c->err, s); }));
     }
     {
       EpiParams e;
@@ -592,7 +618,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
         e.ld_bf16 = D;
       }
       PF_CUDA(c, counted(c, PF_KC_GEMM, 1, 2.0 * M * D * c->F, M * c->F * 2.0 + gemm_wbytes(c, D, c->F) + M * D * 8.0,
-                         [&] { return launch_gemm(c->a_h, M, W.down, e, c->err, s); }));
+                         [&] { return launch_gemm(c->a_h, M, pick(W.down, W.down1, M), e, c->err, s); }));
     }
     if (c->P > 0) {
       EpiParams e;
@@ -610,7 +636,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       r.out_f32 = xcur;
       r.ld_f32 = D;
       PF_CUDA(c, counted(c, PF_KC_GEMM, 1, 2.0 * M * D * c->P, M * c->P * 2.0 + gemm_wbytes(c, D, c->P) + M * D * 8.0,
-                         [&] { return launch_gemm(c->a_pg, M, W.pp, r, c->err, s); }));
+                         [&] { return launch_gemm(c->a_pg, M, pick(W.pp, W.pp1, M), r, c->err, s); }));
     }
   }
   if (is_last) {
