@@ -349,42 +349,70 @@ __global__ void __launch_bounds__(NW * 32, 2) attn_prefill_kernel(AttnArgs a, fl
   }
 }
 
-// Rows t0 .. M-1 (two or more groups): a warp per (row, query head) folds the
-// group states in ascending order; lane owns HD/32 consecutive dims.
+// Rows t0 .. M-1 (two or more groups): a warp per (row, query head) combines
+// the group states (m_g, l_g, o_g): m = max m_g, w_g = 2^((m_g - m) c),
+// l = sum w_g l_g, out = (sum w_g o_g) / l, sums in ascending group order.
+// Every load is issued before the values it feeds are combined, so a row
+// costs two memory round trips however many groups it has.  (The single-row
+// form of the KV-shared layers runs this same kernel, so the pruned row's
+// bits do not depend on the combination order chosen here.)  Lane owns HD/32
+// consecutive dims.
 template <int HD>
 __global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict__ part, int M, int Hq, int pos_base,
                                                          int gc, int t0, __nv_bfloat16* __restrict__ out) {
   constexpr int PER = HD / 32;
+  constexpr float c = 1.4426950408889634f / (HD == 256 ? 16.0f : HD == 128 ? 11.313708498984761f : 8.0f);
   pdl_launch();
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int pair = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int t = t0 + pair / Hq, head = pair % Hq;
   if (t >= M) return;
-  const int n_g = attn_row_groups(pos_base + t, gc);
+  const int n_g = attn_row_groups(pos_base + t, gc);  // 2 .. ATTN_MAX_GROUPS
   const float* base = part + ((size_t)t * Hq + head) * ATTN_MAX_GROUPS * (HD + 2);
-  float m = -INFINITY, l = 0.f, o[PER];
+  // lane g < n_g fetches group g's (m, l)
+  float mg = -INFINITY, lg = 0.f;
+  if (lane < n_g) {
+    const float2 ml = *reinterpret_cast<const float2*>(base + (size_t)lane * (HD + 2) + HD);
+    mg = ml.x;
+    lg = ml.y;
+  }
+  float m = mg;
 #pragma unroll
-  for (int i = 0; i < PER; ++i) o[i] = 0.f;
-  for (int gi = 0; gi < n_g; ++gi) {
-    const float* p = base + (size_t)gi * (HD + 2);
-    const float mj = p[HD], lj = p[HD + 1];
-    float oj[PER];
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float wg = mg == -INFINITY ? 0.f : ex2_approx(__fmul_rn(__fsub_rn(mg, m), c));
+  float acc[PER];
 #pragma unroll
-    for (int i = 0; i < PER; i += 2) {
-      const float2 v = *reinterpret_cast<const float2*>(p + lane * PER + i);
-      oj[i] = v.x;
-      oj[i + 1] = v.y;
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  float l = 0.f;
+  for (int g0 = 0; g0 < n_g; g0 += 4) {
+    float oj[4][PER];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float* p = base + (size_t)(g0 + k) * (HD + 2) + lane * PER;
+#pragma unroll
+      for (int i = 0; i < PER; i += 2) {
+        float2 v = make_float2(0.f, 0.f);
+        if (g0 + k < n_g) v = *reinterpret_cast<const float2*>(p + i);
+        oj[k][i] = v.x;
+        oj[k][i + 1] = v.y;
+      }
     }
-    if (mj == -INFINITY) continue;
-    const MergeAB ab = merge_state<HD>(m, l, mj, lj);
 #pragma unroll
-    for (int i = 0; i < PER; ++i) o[i] = merge_o(o[i], oj[i], ab);
+    for (int k = 0; k < 4; ++k) {
+      const float w = __shfl_sync(0xffffffffu, wg, (g0 + k) & 31);
+      const float lk = __shfl_sync(0xffffffffu, lg, (g0 + k) & 31);
+      if (g0 + k >= n_g) continue;
+      l = __fadd_rn(l, __fmul_rn(w, lk));
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(w, oj[k][i]));
+    }
   }
   __nv_bfloat16* dst = out + (size_t)t * Hq * HD + (size_t)head * HD + lane * PER;
 #pragma unroll
   for (int i = 0; i < PER; i += 2)
-    *reinterpret_cast<__nv_bfloat162*>(dst + i) = __floats2bfloat162_rn(__fdiv_rn(o[i], l), __fdiv_rn(o[i + 1], l));
+    *reinterpret_cast<__nv_bfloat162*>(dst + i) =
+        __floats2bfloat162_rn(__fdiv_rn(acc[i], l), __fdiv_rn(acc[i + 1], l));
 }
 
 // ---------------------------------------------------------------------------
