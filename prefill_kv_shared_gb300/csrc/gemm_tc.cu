@@ -249,8 +249,13 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m0, int rv
   if (ep.kind == EPI_QKV) {
     // Q | K | V columns; Q and K rotated (half-split RoPE at position
     // pos0 + row) and written as fp16, V written as fp16 to the cache.  A
-    // rotated chunk is handled together with its partner half a head away.
+    // rotated chunk is handled together with its partner half a head away:
+    // with whole heads in a tile (hd <= BN) the partner is half/32 chunks
+    // further; with heads wider than the tile, a tile holds BN/2 dims of the
+    // head's first half and the same BN/2 dims of its second half
+    // (qkv_tile_rows), and the partner is NCH/2 chunks further.
     const int hd = ep.head_dim, half = hd / 2, pair_ch = half / 32;
+    const bool split_heads = hd > BN;
     const int q_end = ep.q_dim, k_end = ep.q_dim + ep.kv_dim, v_end = ep.q_dim + 2 * ep.kv_dim;
     int item = 0;
     for (int c = 0; c < NCH; ++c) {
@@ -276,10 +281,20 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m0, int rv
       }
       const bool is_q = n < q_end;
       const int rel = is_q ? n : n - q_end;
-      const int i0 = rel % hd;
-      if (i0 >= half) continue;  // handled together with its partner chunk
+      int i0, head, partner;
+      if (split_heads) {
+        const int tile = rel / BN, x = rel % BN;
+        if (x >= BN / 2) continue;  // handled together with its partner chunk
+        head = tile / (hd / BN);
+        i0 = (tile % (hd / BN)) * (BN / 2) + x;
+        partner = c + NCH / 2;
+      } else {
+        i0 = rel % hd;
+        if (i0 >= half) continue;  // handled together with its partner chunk
+        head = rel / hd;
+        partner = c + pair_ch;
+      }
       if ((item++ & 1) != ew) continue;
-      const int head = rel / hd;
       // two passes of 16 rows each keep the transposed halves in registers
       for (int hp = 0; hp < 2; ++hp) {
         float4 c01[4], c23[4];  // (cos, sin) of columns i0+4p .. i0+4p+3 at each row's position
@@ -298,7 +313,7 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m0, int rv
 #pragma unroll
         for (int i = 0; i < 4; ++i) vt[i] = stage_get(st, 16 * hp + 4 * i + rs, p);
         __syncwarp();
-        load(c + pair_ch, v);
+        load(partner, v);
         stage_put(st, lane, v);
         __syncwarp();
 #pragma unroll
@@ -917,17 +932,42 @@ static size_t ring_bytes_mt1(int kind, int BN) {
 }
 
 int choose_split(int kind, int N_rows, int BN, int K, int max_rows) {
-  // Split the k-range over a cluster of CTAs when the tile grid (one 128-row
-  // block per tile) would leave SMs idle.  Depends on the matrix shape and
-  // the context's largest ubatch only, never on a launch's M.
+  // Split the k-range over a cluster of CTAs while the split tile grid (one
+  // 128-row block per tile) still fits on the SMs at once.  Depends on the
+  // matrix shape and the context's largest ubatch only, never on a launch's M.
   const int units1 = (N_rows / BN) * ((max_rows + 127) / 128);
   const int nkb = K / 64;
   const size_t ring = ring_bytes_mt1(kind, BN);
   int s = 1;
-  while (units1 * s < 128 && nkb % (2 * s) == 0 && nkb / (2 * s) >= 4 && 2 * s <= 2 &&
+  while (units1 * 2 * s <= sm_count() && nkb % (2 * s) == 0 && nkb / (2 * s) >= 4 && 2 * s <= 2 &&
          static_cast<size_t>(2 * s - 1) * 128 * BN * 4 <= ring)
     s *= 2;
   return s;
+}
+
+std::vector<const void*> qkv_tile_rows(const void* wq, const void* wk, const void* wv, int Hq, int Hkv, int hd,
+                                       size_t row_bytes, int BN) {
+  std::vector<const void*> rows;
+  auto region = [&](const void* w, int heads, bool rotated) {
+    const uint8_t* b = static_cast<const uint8_t*>(w);
+    if (!rotated || hd <= BN) {
+      for (int n = 0; n < heads * hd; ++n) rows.push_back(b + n * row_bytes);
+      return;
+    }
+    // heads wider than a tile: tile j of a head holds dims j*BN/2 .. +BN/2 of
+    // each half, so that every RoPE pair (i, i + hd/2) stays in one tile
+    const int half = hd / 2, per = BN / 2;
+    for (int h = 0; h < heads; ++h)
+      for (int j = 0; j < hd / BN; ++j) {
+        for (int i = 0; i < per; ++i) rows.push_back(b + (size_t)(h * hd + j * per + i) * row_bytes);
+        for (int i = 0; i < per; ++i) rows.push_back(b + (size_t)(h * hd + half + j * per + i) * row_bytes);
+      }
+  };
+  region(wq, Hq, true);
+  if (wk) region(wk, Hkv, true);
+  if (wv) region(wv, Hkv, false);
+  rows.resize((rows.size() + BN - 1) / BN * BN, nullptr);
+  return rows;
 }
 
 template <int WK, int BN, int MT>

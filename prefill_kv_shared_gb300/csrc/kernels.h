@@ -77,6 +77,12 @@ bool make_weight_map(WeightMat& w, std::string* err);
 // k-splits (cluster size) for a weight shape, chosen from the shape and the
 // largest M the context runs; never from a launch's M
 int choose_split(int kind, int N_rows, int BN, int K, int max_rows);
+// Q|K|V weight rows in GEMM tile order (128-row tiles; heads wider than a
+// tile are cut so that RoPE pairs share a tile; V in plain order), padded to
+// BN with NULL rows.  wk/wv may be NULL (a Q-only projection).
+constexpr int QKV_BN = 128;
+std::vector<const void*> qkv_tile_rows(const void* wq, const void* wk, const void* wv, int Hq, int Hkv, int hd,
+                                       size_t row_bytes, int BN);
 
 cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err_word,
                         cudaStream_t s);

@@ -249,15 +249,9 @@ extern "C" int pfop_linear_qkv(int32_t wtype, const void* wq_host, const void* w
   ActMat A;
   int rc;
   const int q = Hq * hd, kv = Hkv * hd;
-  const int bn = hd > 128 ? 256 : 128;
-  const size_t rb = rbytes(wtype, K);
-  std::vector<const void*> rows;
-  for (int n = 0; n < q; ++n) rows.push_back(static_cast<const uint8_t*>(wq_host) + n * rb);
-  if (kvw) {
-    for (int n = 0; n < kv; ++n) rows.push_back(static_cast<const uint8_t*>(wk_host) + n * rb);
-    for (int n = 0; n < kv; ++n) rows.push_back(static_cast<const uint8_t*>(wv_host) + n * rb);
-  }
-  rows.resize(rup(static_cast<int>(rows.size()), bn), nullptr);
+  const int bn = QKV_BN;
+  std::vector<const void*> rows =
+      qkv_tile_rows(wq_host, kvw ? wk_host : nullptr, kvw ? wv_host : nullptr, Hq, Hkv, hd, rbytes(wtype, K), bn);
   if ((rc = make_weight(sc, W, wtype, rows, K, bn))) return rc;
   if ((rc = make_act(A, a_dev, a_rows, K))) return rc;
   const int half = hd / 2;

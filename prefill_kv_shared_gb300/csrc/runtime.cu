@@ -318,17 +318,10 @@ extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weig
     if (writes && (!lw.wk || !lw.wv)) return fail(nullptr, PF_E_ARG, "writing layer without wk/wv");
     if (C->P > 0 && (!lw.ple_gate || !lw.ple_proj)) return fail(nullptr, PF_E_ARG, "missing ple_gate/ple_proj");
     // QKV (or Q): one tile holds whole heads so RoPE pairs stay in the tile
-    const int bn_qkv = C->hd > 128 ? 256 : 128;
     {
-      const size_t rb = row_bytes(wt, C->D);
-      std::vector<const void*> rows;
-      for (int n = 0; n < C->q; ++n) rows.push_back(static_cast<const uint8_t*>(lw.wq) + n * rb);
-      if (writes) {
-        for (int n = 0; n < C->kv; ++n) rows.push_back(static_cast<const uint8_t*>(lw.wk) + n * rb);
-        for (int n = 0; n < C->kv; ++n) rows.push_back(static_cast<const uint8_t*>(lw.wv) + n * rb);
-      }
-      rows.resize(round_up(static_cast<int>(rows.size()), bn_qkv), nullptr);
-      if ((rc = build_weight(C, L.qkv, rows, C->D, bn_qkv))) return fail(nullptr, rc, C->last_error);
+      std::vector<const void*> rows = qkv_tile_rows(lw.wq, writes ? lw.wk : nullptr, writes ? lw.wv : nullptr, C->Hq,
+                                                    C->Hkv, C->hd, row_bytes(wt, C->D), QKV_BN);
+      if ((rc = build_weight(C, L.qkv, rows, C->D, QKV_BN))) return fail(nullptr, rc, C->last_error);
     }
     // KV-shared layers of a model that can prune also get 64-row copies
     const bool single_row_copies = !writes && C->S > 0 && C->D % 64 == 0 && C->F % 32 == 0;
