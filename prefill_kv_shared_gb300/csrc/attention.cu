@@ -7,7 +7,7 @@
 // (s = q.k, c = log2(e)/sqrt(hd)) combined by merge_state().
 //
 // The chunks are taken in groups of gc consecutive chunks, gc fixed by the
-// number of keys in the launch (attn_group_chunks: at most 16 groups).  A CTA
+// number of keys in the launch (attn_group_chunks: at most 4 groups).  A CTA
 // handles one (64-row block, group) pair: it folds the group's chunks in
 // ascending order into a state (m, l, o).  A row whose keys lie in one group
 // writes o / l directly; otherwise each group's state goes to a partials
@@ -223,7 +223,7 @@ __device__ __forceinline__ void attn_chunk(uint32_t sq, uint32_t sk, uint32_t sv
 
 // partials layout: [row t][query head][group (ATTN_MAX_GROUPS)][HD + 2] =
 // o[HD] (not normalised), m, l
-constexpr int ATTN_MAX_GROUPS = 16;
+constexpr int ATTN_MAX_GROUPS = 4;
 
 int attn_group_chunks(int kv_len) {
   const int n_chunks = (kv_len + CHUNK - 1) / CHUNK;
