@@ -1,32 +1,42 @@
-// Causal grouped-query attention over the FP16 KV cache.
-//
-// Keys are cut into absolute 64-key chunks.  For one query row the result is
-// a left fold, in ascending chunk order, of per-chunk partials
-//     (m_j, l_j, o_j):  m_j = max_k s_k,  p_k = fp16(2^((s_k - m_j) c)),
-//                       l_j = sum_k p_k,  o_j = sum_k p_k V_k
-// (s = q.k, c = log2(e)/sqrt(hd)) combined by merge_state().
-//
-// The chunks are taken in groups of gc consecutive chunks, gc fixed by the
-// number of keys in the launch (attn_group_chunks: at most 4 groups).  A CTA
-// handles one (64-row block, group) pair: it folds the group's chunks in
-// ascending order into a state (m, l, o).  A row whose keys lie in one group
-// writes o / l directly; otherwise each group's state goes to a partials
-// buffer and attn_merge folds the row's group states in ascending order.  So
-// the causal work spreads over many CTAs instead of piling up on the CTAs of
-// the last rows.
-//
-// A row's result depends only on its own position, the keys and gc: the MMA
-// rows of a tile are independent, chunks past a row's position leave its
-// state unchanged, and gc is the same for the ubatch's last row whether the
-// launch carries the whole ubatch (M = T) or that row alone (M = 1, the
-// KV-shared layers after pruning), because both see the same number of keys.
-// So the pruned output row is bit-identical to the unpruned one.
+// Causal grouped-query attention over the FP16 KV cache, on the 5th-generation
+// tensor cores.
 //
 // MMA rows are (query, head-within-group) pairs: row R = t*G + g for query t
 // and query head kvh*G + g, so the G query heads that share a KV head share
-// the K/V tiles.
+// the K/V tiles.  A CTA takes 128 rows (128/G queries) of one KV head.
+//
+// Keys are cut into absolute 64-key chunks, and the chunks into groups of gc
+// consecutive chunks, gc fixed by a key count (attn_group_chunks: at most
+// ATTN_MAX_GROUPS groups): a context's capacity, or the launch's keys.  A CTA handles one
+// (128-row block, group) pair and runs the online softmax over the group's
+// chunks in ascending order:
+//     S = Q K^T (tcgen05.mma, TMEM), m' = max(m, max_k s_k),
+//     p_k = fp16(2^((s_k - m') c)), l' = l 2^((m - m') c) + sum_k p_k,
+//     O' = O 2^((m - m') c) + P V (the rescale in TMEM, P V by tcgen05.mma)
+// with c = log2(e)/sqrt(hd).  A row whose keys lie in one group writes O / l;
+// otherwise each group's (O, m, l) goes to a partials buffer and
+// attn_merge_kernel combines the row's group states.  So the causal work
+// spreads over many CTAs instead of piling up on those of the last rows.
+//
+// A row's result depends only on its own position, the keys and gc: the MMA
+// rows of a tile are independent and chunks past a row's position leave its
+// state unchanged.  A context fixes gc from its capacity, so the pruned output
+// row (M = 1, the KV-shared layers after pruning) is bit-identical to the
+// unpruned one, and a prompt gives the same bits however it is cut into
+// ubatches (a restored prefix plus a suffix included).
+//
+// CTA roles: warp 1 lane 0 issues the TMA copies (Q once; K and V per chunk,
+// double-buffered); warp 0 allocates TMEM and its lane 0 issues the MMAs;
+// warps 2..5 own the 128 rows (thread = TMEM lane = row): softmax, the P tile
+// (fp16, 128-byte-swizzled K-major: the A operand of P V), the O rescale and
+// the output.  The MMA thread issues S(j+1) = Q K(j+1)^T before P(j) V(j), so
+// the tensor cores work while the row warps run the softmax of chunk j.  All
+// waits are bounded (PF_WAIT_CYCLES); a timed-out wait flags the error word
+// and the CTA unwinds.
 #include "common.cuh"
 #include "kernels.h"
+
+#include <string>
 
 namespace pf {
 
@@ -37,189 +47,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  const int n = valid ? 16 : 0;  // 0: fill the 16 bytes with zeros
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
-  __half2 h = __floats2half2_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// Fold partial (mj, lj) into state (m, l); returns the scale factors a (old
-// state) and b (partial).  The state's o is updated by the caller as
-// o = a*o + b*o_j with merge_o().  An empty state (m = -inf, l = 0, o = 0)
-// merged with a partial gives the partial exactly.
-struct MergeAB {
-  float a, b;
-};
-template <int HD>
-__device__ __forceinline__ MergeAB merge_state(float& m, float& l, float mj, float lj) {
-  constexpr float c = 1.4426950408889634f / (HD == 256 ? 16.0f : HD == 128 ? 11.313708498984761f : 8.0f);
-  const float mn = fmaxf(m, mj);
-  MergeAB r;
-  r.a = ex2_approx(__fmul_rn(__fsub_rn(m, mn), c));
-  r.b = ex2_approx(__fmul_rn(__fsub_rn(mj, mn), c));
-  l = __fadd_rn(__fmul_rn(r.a, l), __fmul_rn(r.b, lj));
-  m = mn;
-  return r;
-}
-__device__ __forceinline__ float merge_o(float o, float oj, MergeAB ab) {
-  return __fadd_rn(__fmul_rn(ab.a, o), __fmul_rn(ab.b, oj));
-}
-
-template <int HD>
-struct ChunkSmem {
-  static constexpr int LD = HD + 8;  // halves per row; the pad removes ldmatrix bank conflicts
-  static constexpr int ROW_BYTES = LD * 2;
-  static constexpr int KV_BYTES = CHUNK * ROW_BYTES;  // one K or V chunk
-};
-
-// Stage chunk `ch` of K and V (keys [64ch, 64ch+64)) into shared memory;
-// keys >= kv_len read as zeros.
-template <int HD>
-__device__ __forceinline__ void load_kv_chunk(uint32_t sk, uint32_t sv, const __half* k, const __half* v,
-                                              int kv_stride, int kv_len, int ch, int tid, int nthreads) {
-  using S = ChunkSmem<HD>;
-  constexpr int VPR = HD / 8;  // 16-byte vectors per key row
-  for (int i = tid; i < CHUNK * VPR; i += nthreads) {
-    const int r = i / VPR, c = i % VPR;
-    const int key = ch * CHUNK + r;
-    const bool ok = key < kv_len;
-    const size_t off = (size_t)(ok ? key : 0) * kv_stride + c * 8;
-    cp_async16(sk + r * S::ROW_BYTES + c * 16, k + off, ok);
-    cp_async16(sv + r * S::ROW_BYTES + c * 16, v + off, ok);
-  }
-}
-
-// One warp, 16 MMA rows (q in shared memory, ld = HD+8), one 64-key chunk.
-// pos0/pos1: positions of the thread's rows g and g+8 (-1: row unused).
-// Produces, for both rows, mj/lj (identical across the row's 4 lanes) and the
-// fp16 probabilities; then calls sink(dt0, o) for each 64-dim group with the
-// group's o_j fragments o[8][4].
-template <int HD, class Sink>
-__device__ __forceinline__ void attn_chunk(uint32_t sq, uint32_t sk, uint32_t sv, int ch, int pos0, int pos1,
-                                           float (&mj)[2], float (&lj)[2], Sink&& sink) {
-  using S = ChunkSmem<HD>;
-  const int lane = threadIdx.x & 31;
-  const int tq = lane & 3;
-  const int lm = lane >> 3, lr = lane & 7;
-
-  // s = q k^T for 16 rows x 64 keys
-  float s[8][4];
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-  for (int ks = 0; ks < HD / 16; ks += 2) {
-    uint32_t qa[4], qb[4];
-    ldsm_x4(qa, sq + (lr + ((lm & 1) << 3)) * S::ROW_BYTES + (16 * ks + ((lm >> 1) << 3)) * 2);
-    ldsm_x4(qb, sq + (lr + ((lm & 1) << 3)) * S::ROW_BYTES + (16 * (ks + 1) + ((lm >> 1) << 3)) * 2);
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      uint32_t kb[4];  // b0,b1 for k-step ks, then b0,b1 for ks+1
-      ldsm_x4(kb, sk + (8 * nt + lr) * S::ROW_BYTES + (16 * ks + 8 * lm) * 2);
-      mma16816(s[nt], qa, kb[0], kb[1]);
-      mma16816(s[nt], qb, kb[2], kb[3]);
-    }
-  }
-
-  // causal mask, row max
-  const int kbase = ch * CHUNK + 2 * tq;
-  float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int key = kbase + 8 * nt + e;
-      if (key > pos0) s[nt][e] = -INFINITY;
-      if (key > pos1) s[nt][2 + e] = -INFINITY;
-      mx0 = fmaxf(mx0, s[nt][e]);
-      mx1 = fmaxf(mx1, s[nt][2 + e]);
-    }
-  }
-  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-
-  // probabilities, rounded to fp16; the sum adds the rounded values
-  constexpr float c = 1.4426950408889634f / (HD == 256 ? 16.0f : HD == 128 ? 11.313708498984761f : 8.0f);
-  uint32_t p[8][2];
-  float sum0 = 0.f, sum1 = 0.f;
-  const bool act0 = mx0 != -INFINITY, act1 = mx1 != -INFINITY;
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-    const float p0 = act0 ? ex2_approx(__fmul_rn(__fsub_rn(s[nt][0], mx0), c)) : 0.f;
-    const float p1 = act0 ? ex2_approx(__fmul_rn(__fsub_rn(s[nt][1], mx0), c)) : 0.f;
-    const float p2 = act1 ? ex2_approx(__fmul_rn(__fsub_rn(s[nt][2], mx1), c)) : 0.f;
-    const float p3 = act1 ? ex2_approx(__fmul_rn(__fsub_rn(s[nt][3], mx1), c)) : 0.f;
-    const __half2 h01 = __floats2half2_rn(p0, p1);
-    const __half2 h23 = __floats2half2_rn(p2, p3);
-    p[nt][0] = *reinterpret_cast<const uint32_t*>(&h01);
-    p[nt][1] = *reinterpret_cast<const uint32_t*>(&h23);
-    sum0 = __fadd_rn(__fadd_rn(sum0, __low2float(h01)), __high2float(h01));
-    sum1 = __fadd_rn(__fadd_rn(sum1, __low2float(h23)), __high2float(h23));
-  }
-  sum0 = __fadd_rn(sum0, __shfl_xor_sync(0xffffffffu, sum0, 1));
-  sum0 = __fadd_rn(sum0, __shfl_xor_sync(0xffffffffu, sum0, 2));
-  sum1 = __fadd_rn(sum1, __shfl_xor_sync(0xffffffffu, sum1, 1));
-  sum1 = __fadd_rn(sum1, __shfl_xor_sync(0xffffffffu, sum1, 2));
-  mj[0] = mx0;
-  mj[1] = mx1;
-  lj[0] = sum0;
-  lj[1] = sum1;
-
-  // o_j = P V, 64 output dims at a time
-#pragma unroll
-  for (int grp = 0; grp < HD / 64; ++grp) {
-    float o[8][4];
-#pragma unroll
-    for (int dt = 0; dt < 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const uint32_t pa[4] = {p[2 * kk][0], p[2 * kk][1], p[2 * kk + 1][0], p[2 * kk + 1][1]};
-#pragma unroll
-      for (int dp = 0; dp < 4; ++dp) {
-        const int dt = 2 * dp;
-        uint32_t vb[4];  // (keys +0, dims dt) (keys +8, dims dt) (keys +0, dims dt+1) (keys +8, dims dt+1)
-        ldsm_x4_t(vb, sv + (16 * kk + lr + ((lm & 1) << 3)) * S::ROW_BYTES +
-                          (64 * grp + 8 * dt + ((lm >> 1) << 3)) * 2);
-        mma16816(o[dt], pa, vb[0], vb[1]);
-        mma16816(o[dt + 1], pa, vb[2], vb[3]);
-      }
-    }
-    sink(grp, o);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// attn_prefill: every row, in-CTA ordered fold
 
 // partials layout: [row t][query head][group (ATTN_MAX_GROUPS)][HD + 2] =
 // o[HD] (not normalised), m, l
@@ -234,120 +61,350 @@ int attn_group_chunks(int kv_len) {
 // groups that hold keys of the row at position pos
 __host__ __device__ __forceinline__ int attn_row_groups(int pos, int gc) { return (pos / CHUNK) / gc + 1; }
 
-template <int HD, int NW>
-struct PrefillCfg {
-  using S = ChunkSmem<HD>;
-  static constexpr int ROWS = 16 * NW;
-  static constexpr int Q_BYTES = ROWS * S::ROW_BYTES;
-  static constexpr int STAGE_BYTES = 2 * S::KV_BYTES;
-  static constexpr int SMEM = Q_BYTES + STAGE_BYTES;  // one K/V stage: two CTAs fit on an SM
+template <int HD>
+__host__ __device__ constexpr float attn_c() {
+  return 1.4426950408889634f / (HD == 256 ? 16.0f : HD == 128 ? 11.313708498984761f : 8.0f);
+}
+
+// ---------------------------------------------------------------------------
+// the tcgen05 kernel
+
+template <int HD>
+struct AttnTcCfg {
+  static constexpr int NB = HD / 64;               // 64-dim (128-byte) boxes per row
+  static constexpr int Q_BYTES = 128 * HD * 2;      // [box][128 rows][128 B]
+  static constexpr int KV_BYTES = CHUNK * HD * 2;   // one K or V chunk: [box][64 keys][128 B]
+  static constexpr int P_BYTES = 128 * CHUNK * 2;   // [128 rows][64 keys fp16]
+  static constexpr int OFF_K = Q_BYTES;
+  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + barriers, + alignment slack
+  static constexpr int TMEM_S = 0;                  // two S buffers of 64 columns
+  static constexpr int TMEM_O = 2 * CHUNK;          // O: HD columns
+  static constexpr int TMEM_COLS = (TMEM_O + HD) <= 256 ? 256 : 512;
+  static constexpr int THREADS = 192;
+  static_assert(SMEM <= 232448, "shared memory");
 };
 
-template <int HD, int NW>
-__global__ void __launch_bounds__(NW * 32, 2) attn_prefill_kernel(AttnArgs a, float* __restrict__ part, int gc) {
-  using S = ChunkSmem<HD>;
-  using C = PrefillCfg<HD, NW>;
-  extern __shared__ __align__(16) uint8_t smem[];
-  pdl_launch();
-  pdl_wait();
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, tq = lane & 3;
-  const int G = a.Hq / a.Hkv;
-  const int kvh = blockIdx.y, grp = blockIdx.z;
-  const int R0 = blockIdx.x * C::ROWS;
-  const int q_stride = a.Hq * HD, kv_stride = a.Hkv * HD;
-  const __half* kbase = a.k + kvh * HD;
-  const __half* vbase = a.v + kvh * HD;
-  const int t_last = min(a.M - 1, (R0 + C::ROWS - 1) / G);
-  const int last_ch = (a.pos_base + t_last) / CHUNK;
-  const int ch_first = grp * gc;
-  if (ch_first > last_ch) return;  // no keys of this group reach the block's rows
-  const int ch_end = min(last_ch, ch_first + gc - 1);
+// 128-byte-swizzled operand descriptor with explicit leading / stride byte
+// offsets (MN-major: LBO = bytes between 64-element atoms along MN, SBO =
+// bytes between 8-row groups along K)
+__device__ __forceinline__ uint64_t sdesc_sw128_lbo_sbo(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(lbo >> 4) << 16;
+  d |= static_cast<uint64_t>(sbo >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
 
-  // queries of this CTA
-  const uint32_t sq = smem_u32(smem);
-  for (int i = tid; i < C::ROWS * (HD / 8); i += NW * 32) {
-    const int r = i / (HD / 8), c = i % (HD / 8);
-    const int R = R0 + r, t = R / G, head = kvh * G + R % G;
-    const bool ok = t < a.M;
-    cp_async16(sq + r * S::ROW_BYTES + c * 16, a.q + (size_t)(ok ? t : 0) * q_stride + head * HD + c * 8, ok);
-  }
-  const uint32_t sk = sq + C::Q_BYTES, sv = sk + S::KV_BYTES;
+// kind::f16 instruction descriptor, fp16 A and B, fp32 accumulator; b_mn:
+// B is MN-major (V stored [key][dim] is the B operand of P V)
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn) {
+  return (1u << 4) | (b_mn ? (1u << 16) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
 
-  // this thread's two rows
-  const int Rw = R0 + warp * 16;
-  const int ta = (Rw + g) / G, tb = (Rw + g + 8) / G;
-  const int posa = ta < a.M ? a.pos_base + ta : -1;
-  const int posb = tb < a.M ? a.pos_base + tb : -1;
-  const int warp_tmax = min(a.M - 1, (Rw + 15) / G);
-  const int warp_pmax = (Rw / G) < a.M ? a.pos_base + warp_tmax : -1;
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                            int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
 
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-  float o[HD / 8][4];
-#pragma unroll
-  for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+// 32 lanes x 32 consecutive 32-bit columns from registers (thread i -> lane i)
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-  for (int ch = ch_first; ch <= ch_end; ++ch) {
-    if (ch != ch_first) __syncthreads();  // every warp is done with the previous chunk
-    load_kv_chunk<HD>(sk, sv, kbase, vbase, kv_stride, a.kv_len, ch, tid, NW * 32);
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
-    if (warp_pmax >= ch * CHUNK) {
-      float mj[2], lj[2];
-      MergeAB ab[2];
-      bool act[2];
-      attn_chunk<HD>(sq + warp * 16 * S::ROW_BYTES, sk, sv, ch, posa, posb, mj, lj, [&](int dg, float(&oj)[8][4]) {
-        if (dg == 0) {
-          act[0] = mj[0] != -INFINITY;
-          act[1] = mj[1] != -INFINITY;
-          if (act[0]) ab[0] = merge_state<HD>(m[0], l[0], mj[0], lj[0]);
-          if (act[1]) ab[1] = merge_state<HD>(m[1], l[1], mj[1], lj[1]);
-        }
-#pragma unroll
-        for (int dt = 0; dt < 8; ++dt) {
-          float* od = o[dg * 8 + dt];
-          if (act[0]) {
-            od[0] = merge_o(od[0], oj[dt][0], ab[0]);
-            od[1] = merge_o(od[1], oj[dt][1], ab[0]);
-          }
-          if (act[1]) {
-            od[2] = merge_o(od[2], oj[dt][2], ab[1]);
-            od[3] = merge_o(od[3], oj[dt][3], ab[1]);
-          }
-        }
-      });
-    }
-  }
-
-  // a row with one group: out = o / l; otherwise the group state
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int t = half ? tb : ta;
-    if (t >= a.M) continue;
-    const int R = Rw + g + 8 * half;
-    const int head = kvh * G + R % G;
-    const int n_g = attn_row_groups(a.pos_base + t, gc);
-    if (n_g == 1) {
-      __nv_bfloat16* dst = a.out + (size_t)t * q_stride + head * HD;
-#pragma unroll
-      for (int dt = 0; dt < HD / 8; ++dt) {
-        const float x0 = __fdiv_rn(o[dt][2 * half], l[half]);
-        const float x1 = __fdiv_rn(o[dt][2 * half + 1], l[half]);
-        *reinterpret_cast<__nv_bfloat162*>(dst + 8 * dt + 2 * tq) = __floats2bfloat162_rn(x0, x1);
-      }
-    } else if (grp < n_g) {
-      float* dst = part + (((size_t)t * a.Hq + head) * ATTN_MAX_GROUPS + grp) * (HD + 2);
-#pragma unroll
-      for (int dt = 0; dt < HD / 8; ++dt)
-        *reinterpret_cast<float2*>(dst + 8 * dt + 2 * tq) = make_float2(o[dt][2 * half], o[dt][2 * half + 1]);
-      if (tq == 0) {
-        dst[HD] = m[half];
-        dst[HD + 1] = l[half];
-      }
-    }
+// let issued MMAs finish before TMEM is freed on an error path (bounded;
+// `bar` completes once, on the commit that follows them)
+__device__ __forceinline__ void attn_drain(uint64_t* bar) {
+  const uint32_t a = smem_u32(bar);
+  const long long t0 = clock64();
+  while (!mbar_try_wait(a, 0)) {
+    if (clock64() - t0 > 400000000ll) return;  // about 0.2 s
   }
 }
+
+struct AttnTcShape {
+  int M, Hq, Hkv, pos_base, gc;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const AttnTcShape sh, __nv_bfloat16* __restrict__ out,
+                   float* __restrict__ part, int* err) {
+  using C = AttnTcCfg<HD>;
+  constexpr float cexp = attn_c<HD>();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;        // 1
+  uint64_t* kv_full = bars + 1;   // 2
+  uint64_t* kv_empty = bars + 3;  // 2
+  uint64_t* s_full = bars + 5;    // 2
+  uint64_t* s_free = bars + 7;    // 2
+  uint64_t* p_full = bars + 9;    // 2
+  uint64_t* pv_done = bars + 11;  // 2
+  uint64_t* drain = bars + 13;    // 1, error path only
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = sh.Hq / sh.Hkv;
+  const int kvh = blockIdx.y, grp = blockIdx.z;
+  const int R0 = blockIdx.x * 128;
+  const int t0 = R0 / G;
+  const int t_last = min(sh.M - 1, (R0 + 127) / G);
+  const int last_ch = (sh.pos_base + t_last) / CHUNK;
+  const int ch_first = grp * sh.gc;
+  pdl_launch();
+  if (ch_first > last_ch) return;  // no keys of this group reach the block's rows
+  const int ch_end = min(last_ch, ch_first + sh.gc - 1);
+  const int n = ch_end - ch_first + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&kv_full[b], 1);
+      mbar_init(&kv_empty[b], 1);
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_free[b], 4);
+      mbar_init(&p_full[b], 4);
+      mbar_init(&pv_done[b], 1);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1 && lane == 0) {
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();
+
+  if (warp == 1) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      bool ok = true;
+      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+      for (int b = 0; b < C::NB; ++b) tma_load_3d(smem + b * (128 * 128), &tmQ, q_full, 64 * b, kvh * G, t0);
+      for (int j = 0; j < n && ok; ++j) {
+        const int s = j & 1;
+        if (j >= 2) ok = mbar_wait(&kv_empty[s], ((j - 2) >> 1) & 1, err, PF_DEV_TIMEOUT_PRODUCER);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&kv_full[s], 2 * C::KV_BYTES);
+        const int key0 = (ch_first + j) * CHUNK;
+        for (int b = 0; b < C::NB; ++b) {
+          tma_load_2d(smem + C::OFF_K + s * C::KV_BYTES + b * (CHUNK * 128), &tmK, &kv_full[s], kvh * HD + 64 * b,
+                      key0);
+          tma_load_2d(smem + C::OFF_V + s * C::KV_BYTES + b * (CHUNK * 128), &tmV, &kv_full[s], kvh * HD + 64 * b,
+                      key0);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 0) {
+    // ---------------- MMA issue
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_f16_f32(128, CHUNK, false);
+      constexpr uint32_t id_pv = idesc_f16_f32(128, HD, true);
+      const uint32_t sq = smem_u32(smem);
+      bool ok = mbar_wait(q_full, 0, err, PF_DEV_TIMEOUT_MMA);
+      bool issued = false;
+      // step i: S(i) = Q K(i)^T (if i < n), then O (+)= P(i-1) V(i-1)
+      for (int i = 0; i <= n && ok; ++i) {
+        if (i < n) {
+          const int s = i & 1;
+          ok = mbar_wait(&kv_full[s], (i >> 1) & 1, err, PF_DEV_TIMEOUT_MMA);
+          if (ok && i >= 2) ok = mbar_wait(&s_free[s], ((i - 2) >> 1) & 1, err, PF_DEV_TIMEOUT_MMA);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t sk = smem_u32(smem + C::OFF_K + s * C::KV_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const int b = kk >> 2, w = kk & 3;  // 64-dim box, 16-dim step within it
+            tc_mma_f16(tmem + C::TMEM_S + s * CHUNK, sdesc_sw128(sq + b * (128 * 128) + w * 32),
+                       sdesc_sw128(sk + b * (CHUNK * 128) + w * 32), id_qk, kk > 0 ? 1u : 0u);
+          }
+          issued = true;
+          tc_commit(&s_full[s]);
+        }
+        if (i >= 1) {
+          const int j = i - 1, s = j & 1;
+          ok = mbar_wait(&p_full[s], (j >> 1) & 1, err, PF_DEV_TIMEOUT_MMA);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t sp = smem_u32(smem + C::OFF_P + s * C::P_BYTES);
+          const uint32_t sv = smem_u32(smem + C::OFF_V + s * C::KV_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < CHUNK / 16; ++kk)  // 16 keys a step
+            tc_mma_f16(tmem + C::TMEM_O, sdesc_sw128(sp + kk * 32),
+                       sdesc_sw128_lbo_sbo(sv + kk * 16 * 128, CHUNK * 128, 1024), id_pv,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&pv_done[s]);
+          tc_commit(&kv_empty[s]);
+        }
+      }
+      if (!ok && issued) {
+        // the MMAs already issued finish before TMEM is freed
+        tc_commit(drain);
+        attn_drain(drain);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- rows (warps 2..5: TMEM lane quarter warp % 4)
+    const int qw = warp & 3;
+    const int r = 32 * qw + lane;
+    const int R = R0 + r;
+    const int t = R / G, head = kvh * G + R % G;
+    const int pos = t < sh.M ? sh.pos_base + t : -1;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * qw) << 16;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n && ok; ++j) {
+      const int s = j & 1;
+      const int ch = ch_first + j;
+      if (lane == 0) ok = mbar_wait(&s_full[s], (j >> 1) & 1, err, PF_DEV_TIMEOUT_EPILOGUE);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[2][32];
+      tmem_ld32(tmem + lane_base + C::TMEM_S + s * CHUNK, sr[0]);
+      tmem_ld32(tmem + lane_base + C::TMEM_S + s * CHUNK + 32, sr[1]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[s]);
+      // keys ch*64 + k visible to this row: k < nvis
+      const int nvis = pos < 0 ? 0 : min(CHUNK, pos - ch * CHUNK + 1);
+      float mj = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < CHUNK; ++k)
+        if (k < nvis) mj = fmaxf(mj, __uint_as_float(sr[k >> 5][k & 31]));
+      const float mn = fmaxf(m, mj);
+      float lc = 0.f;
+      uint32_t pw[32];  // 64 fp16 probabilities, two per word
+#pragma unroll
+      for (int k2 = 0; k2 < 32; ++k2) {
+        const int k = 2 * k2;
+        const float s0 = __uint_as_float(sr[k >> 5][k & 31]), s1 = __uint_as_float(sr[(k + 1) >> 5][(k + 1) & 31]);
+        const float p0 = k < nvis ? ex2_approx(__fmul_rn(__fsub_rn(s0, mn), cexp)) : 0.f;
+        const float p1 = k + 1 < nvis ? ex2_approx(__fmul_rn(__fsub_rn(s1, mn), cexp)) : 0.f;
+        const __half2 h = __floats2half2_rn(p0, p1);
+        pw[k2] = *reinterpret_cast<const uint32_t*>(&h);
+        lc = __fadd_rn(lc, __low2float(h));
+        lc = __fadd_rn(lc, __high2float(h));
+      }
+      const float scale = (mn != -INFINITY && m != -INFINITY) ? ex2_approx(__fmul_rn(__fsub_rn(m, mn), cexp)) : 1.f;
+      l = __fadd_rn(__fmul_rn(l, scale), lc);
+      m = mn;
+      // P(j) goes to buffer s once P V(j-2) has read it
+      if (j >= 2) {
+        if (lane == 0) ok = mbar_wait(&pv_done[s], ((j - 2) >> 1) & 1, err, PF_DEV_TIMEOUT_EPILOGUE);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+      uint8_t* prow = smem + C::OFF_P + s * C::P_BYTES + r * 128;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4*>(prow + ((q ^ (r & 7)) << 4)) =
+            make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+      fence_proxy_async_smem();
+      // O *= scale once P V(j-1) has landed (chunk 0 overwrites O)
+      if (j >= 1) {
+        if (lane == 0) ok = mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err, PF_DEV_TIMEOUT_EPILOGUE);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, scale != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t x[32];
+            tmem_ld32(tmem + lane_base + C::TMEM_O + 32 * c, x);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 32; ++q) x[q] = __float_as_uint(__fmul_rn(__uint_as_float(x[q]), scale));
+            tmem_st32(tmem + lane_base + C::TMEM_O + 32 * c, x);
+          }
+          tmem_st_wait();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[s]);
+    }
+    // the group's state of each row
+    if (ok) {
+      if (lane == 0) ok = mbar_wait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, err, PF_DEV_TIMEOUT_EPILOGUE);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+    if (ok) {
+      tc_fence_after();
+      const int n_g = pos >= 0 ? attn_row_groups(pos, sh.gc) : 0;
+      const bool final_row = pos >= 0 && n_g == 1;
+      const bool part_row = pos >= 0 && n_g > 1 && grp < n_g;
+      float* pdst = part_row ? part + (((size_t)t * sh.Hq + head) * ATTN_MAX_GROUPS + grp) * (HD + 2) : nullptr;
+      __nv_bfloat16* odst = final_row ? out + (size_t)t * sh.Hq * HD + (size_t)head * HD : nullptr;
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t x[32];
+        tmem_ld32(tmem + lane_base + C::TMEM_O + 32 * c, x);
+        tmem_ld_wait();
+        if (odst) {
+#pragma unroll
+          for (int q = 0; q < 32; q += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 h = __floats2bfloat162_rn(__fdiv_rn(__uint_as_float(x[q + 2 * e]), l),
+                                                             __fdiv_rn(__uint_as_float(x[q + 2 * e + 1]), l));
+              w[e] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(odst + 32 * c + q) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else if (pdst) {
+#pragma unroll
+          for (int q = 0; q < 32; q += 2)
+            *reinterpret_cast<float2*>(pdst + 32 * c + q) = make_float2(__uint_as_float(x[q]), __uint_as_float(x[q + 1]));
+        }
+      }
+      if (pdst) {
+        pdst[HD] = m;
+        pdst[HD + 1] = l;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// merge
 
 // Rows t0 .. M-1 (two or more groups): a warp per (row, query head) combines
 // the group states (m_g, l_g, o_g): m = max m_g, w_g = 2^((m_g - m) c),
@@ -361,7 +418,7 @@ template <int HD>
 __global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict__ part, int M, int Hq, int pos_base,
                                                          int gc, int t0, __nv_bfloat16* __restrict__ out) {
   constexpr int PER = HD / 32;
-  constexpr float c = 1.4426950408889634f / (HD == 256 ? 16.0f : HD == 128 ? 11.313708498984761f : 8.0f);
+  constexpr float c = attn_c<HD>();
   pdl_launch();
   pdl_wait();
   const int lane = threadIdx.x & 31;
@@ -418,44 +475,69 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict
 // ---------------------------------------------------------------------------
 // launchers
 
-template <int HD, int NW>
-static cudaError_t launch_prefill_t(const AttnArgs& a, float* part, cudaStream_t s) {
-  using C = PrefillCfg<HD, NW>;
+template <int HD>
+static cudaError_t launch_tc_t(const AttnArgs& a, float* part, cudaStream_t s) {
+  using C = AttnTcCfg<HD>;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel<HD, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   const int G = a.Hq / a.Hkv;
-  const int rows = a.M * G;
-  const int gc = attn_group_chunks(a.kv_len);
+  // Q viewed as [query][head][dim]; K and V as [key][Hkv*hd], keys past
+  // kv_len read as zeros
+  CUtensorMap tq, tk, tv;
+  std::string err;
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(HD), static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(a.M)};
+    const uint64_t st[2] = {static_cast<uint64_t>(HD) * 2, static_cast<uint64_t>(a.Hq) * HD * 2};
+    const uint32_t box[3] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(128 / G)};
+    if (!encode_fp16_sw128(&tq, a.q, 3, dims, st, box, &err)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(a.Hkv) * HD, static_cast<uint64_t>(a.kv_len)};
+    const uint64_t st[1] = {static_cast<uint64_t>(a.Hkv) * HD * 2};
+    const uint32_t box[2] = {64, CHUNK};
+    if (!encode_fp16_sw128(&tk, a.k, 2, dims, st, box, &err)) return cudaErrorInvalidValue;
+    if (!encode_fp16_sw128(&tv, a.v, 2, dims, st, box, &err)) return cudaErrorInvalidValue;
+  }
+  AttnTcShape sh;
+  sh.M = a.M;
+  sh.Hq = a.Hq;
+  sh.Hkv = a.Hkv;
+  sh.pos_base = a.pos_base;
+  sh.gc = attn_group_chunks(a.group_kv > 0 ? a.group_kv : a.kv_len);
   const int last_pos = a.pos_base + a.M - 1;
-  const int n_groups = attn_row_groups(last_pos, gc);
+  const int n_groups = attn_row_groups(last_pos, sh.gc);
   if (n_groups > 1 && !part) return cudaErrorInvalidValue;
-  dim3 grid((rows + C::ROWS - 1) / C::ROWS, a.Hkv, n_groups);
-  cudaError_t e = launch_k(attn_prefill_kernel<HD, NW>, grid, dim3(NW * 32), C::SMEM, s, 1, a, part, gc);
+  const int rows = a.M * G;
+  dim3 grid((rows + 127) / 128, a.Hkv, n_groups);
+  cudaError_t e =
+      launch_k(attn_tc_kernel<HD>, grid, dim3(C::THREADS), C::SMEM, s, 1, tq, tk, tv, sh, a.out, part, a.err);
   if (e != cudaSuccess || n_groups == 1) return e;
-  const int t0 = a.pos_base >= CHUNK * gc ? 0 : CHUNK * gc - a.pos_base;  // first row with two groups
+  const int t0 = a.pos_base >= CHUNK * sh.gc ? 0 : CHUNK * sh.gc - a.pos_base;  // first row with two groups
   const int pairs = (a.M - t0) * a.Hq;
   return launch_k(attn_merge_kernel<HD>, dim3((pairs + 3) / 4), dim3(128), 0, s, 1,
-                  static_cast<const float*>(part), a.M, a.Hq, a.pos_base, gc, t0, a.out);
+                  static_cast<const float*>(part), a.M, a.Hq, a.pos_base, sh.gc, t0, a.out);
 }
 
 static bool attn_shape_ok(const AttnArgs& a) {
-  if (a.Hkv <= 0 || a.Hq % a.Hkv != 0) return false;
+  if (a.Hkv <= 0 || a.Hq % a.Hkv != 0 || !a.err) return false;
   const int G = a.Hq / a.Hkv;
   if (G > 16 || (16 % G) != 0) return false;
   if (a.pos_base < 0 || a.pos_base + a.M > a.kv_len) return false;
+  // TMA bases must be 16-byte aligned
+  if ((reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k) | reinterpret_cast<uintptr_t>(a.v)) & 15)
+    return false;
   return a.hd == 64 || a.hd == 256;
 }
 
 cudaError_t launch_attn_prefill(const AttnArgs& a, float* partials, cudaStream_t s) {
   if (a.M <= 0) return cudaSuccess;
   if (!attn_shape_ok(a)) return cudaErrorInvalidValue;
-  if (a.hd == 256) return launch_prefill_t<256, 4>(a, partials, s);
-  return launch_prefill_t<64, 4>(a, partials, s);
+  if (a.hd == 256) return launch_tc_t<256>(a, partials, s);
+  return launch_tc_t<64>(a, partials, s);
 }
 
 cudaError_t launch_attn_split(const AttnArgs& a, float* partials, cudaStream_t s) {
@@ -465,7 +547,8 @@ cudaError_t launch_attn_split(const AttnArgs& a, float* partials, cudaStream_t s
 
 int attn_launch_count(const AttnArgs& a) {
   if (a.M <= 0) return 0;
-  return attn_row_groups(a.pos_base + a.M - 1, attn_group_chunks(a.kv_len)) > 1 ? 2 : 1;
+  return attn_row_groups(a.pos_base + a.M - 1, attn_group_chunks(a.group_kv > 0 ? a.group_kv : a.kv_len)) > 1 ? 2
+                                                                                                         : 1;
 }
 
 size_t attn_partials_floats(int M, int Hq, int hd, int kv_len) {

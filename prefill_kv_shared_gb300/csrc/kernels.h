@@ -72,6 +72,9 @@ struct ActMat {
 };
 
 bool make_act_map(ActMat& a, std::string* err);
+// fp16 tensor map with the 128-byte swizzle (rank 2..5; strides of dims 1..)
+bool encode_fp16_sw128(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box, std::string* err);
 bool make_weight_map(WeightMat& w, std::string* err);
 
 // k-splits (cluster size) for a weight shape, chosen from the shape and the
@@ -103,6 +106,10 @@ struct AttnArgs {
   int M = 0, Hq = 0, Hkv = 0, hd = 0;
   int pos_base = 0;  // position of row 0
   int kv_len = 0;    // keys [0, kv_len) exist in the cache
+  int group_kv = 0;  // key count that fixes the chunk-group size (0: kv_len); a
+                     // context passes its capacity, so that every launch over
+                     // its cache groups a row's keys the same way
+  int* err = nullptr;  // device error word (bounded waits that give up set it)
 };
 
 // Causal attention over (64-row block, chunk group) CTAs; rows whose keys span

@@ -19,7 +19,9 @@
 //     overlaps on the GPU race and give wrong results, so callers must order
 //     them (one stream, or events);
 //   - nothing in the array has to start at zero: each call writes every
-//     partial it later reads.
+//     partial it later reads;
+//   - its last four floats hold the call's device error word (reset by the
+//     call, read back after it).
 #include "../../include/prefill_ops.h"
 #include "common.cuh"
 #include "kernels.h"
@@ -70,7 +72,7 @@ extern "C" int pfop_attention_split_noalloc(const void* q_dev, const void* k_dev
   if (!q_dev || !k_dev || !v_dev || !out_dev || pos < 0 || pos >= kv_len || Hq < 1 || Hkv < 1)
     return fail(PF_E_ARG, "bad argument");
   const size_t need = pf::attn_partials_floats(1, Hq, hd, kv_len);
-  if (need > PF_NOALLOC_SCRATCH_FLOATS)
+  if (need > PF_NOALLOC_SCRATCH_FLOATS - 4)
     return fail(PF_E_ARG, "request needs " + std::to_string(need) + " scratch floats; the fixed array holds " +
                               std::to_string(PF_NOALLOC_SCRATCH_FLOATS));
   float* scratch = nullptr;
@@ -87,10 +89,18 @@ extern "C" int pfop_attention_split_noalloc(const void* q_dev, const void* k_dev
   a.hd = hd;
   a.pos_base = pos;
   a.kv_len = kv_len;
+  int* err_word = reinterpret_cast<int*>(scratch + PF_NOALLOC_SCRATCH_FLOATS - 4);
+  a.err = err_word;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = pf::launch_attn_split(a, scratch, s);
+  cudaError_t e = cudaMemsetAsync(err_word, 0, 16, s);
+  if (e != cudaSuccess) return fail(PF_E_CUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
+  e = pf::launch_attn_split(a, scratch, s);
   if (e != cudaSuccess) return fail(PF_E_CUDA, std::string("attention launch: ") + cudaGetErrorString(e));
   e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail(PF_E_CUDA, std::string("cudaStreamSynchronize: ") + cudaGetErrorString(e));
+  int h = 0;
+  e = cudaMemcpy(&h, err_word, 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(PF_E_CUDA, std::string("cudaMemcpy: ") + cudaGetErrorString(e));
+  if (h) return fail(PF_E_DEVICE_TIMEOUT, "attention gave up a bounded wait, code " + std::to_string(h));
   return PF_OK;
 }

@@ -297,13 +297,20 @@ extern "C" int pfop_attention(int32_t mode, const void* q_dev, const void* k_dev
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Scope sc;
   float* part = nullptr;
+  int* err = nullptr;
   OP_CUDA(sc.alloc(&part, attn_partials_floats(M, Hq, hd, kv_len) * 4));
+  OP_CUDA(sc.alloc(&err, 16));
+  OP_CUDA(cudaMemsetAsync(err, 0, 16, s));
+  a.err = err;
   if (mode == 0) {
     OP_CUDA(launch_attn_prefill(a, part, s));
   } else {
     OP_CUDA(launch_attn_split(a, part, s));
   }
   OP_CUDA(cudaStreamSynchronize(s));
+  int h = 0;
+  OP_CUDA(cudaMemcpy(&h, err, 4, cudaMemcpyDeviceToHost));
+  if (h) return op_fail(PF_E_DEVICE_TIMEOUT, "attention gave up a bounded wait, code " + std::to_string(h));
   return PF_OK;
 }
 
