@@ -6,8 +6,8 @@
 // the K/V tiles.  A CTA takes 128 rows (128/G queries) of one KV head.
 //
 // Keys are cut into absolute 64-key chunks, and the chunks into groups of gc
-// consecutive chunks, gc fixed by a key count (attn_group_chunks: at most
-// ATTN_MAX_GROUPS groups): a context's capacity, or the launch's keys.  A CTA handles one
+// consecutive chunks, gc fixed by the launch's key count (attn_group_chunks:
+// at most ATTN_MAX_GROUPS groups).  A CTA handles one
 // (128-row block, group) pair and runs the online softmax over the group's
 // chunks in ascending order:
 //     S = Q K^T (tcgen05.mma, TMEM), m' = max(m, max_k s_k),
@@ -20,10 +20,11 @@
 //
 // A row's result depends only on its own position, the keys and gc: the MMA
 // rows of a tile are independent and chunks past a row's position leave its
-// state unchanged.  A context fixes gc from its capacity, so the pruned output
-// row (M = 1, the KV-shared layers after pruning) is bit-identical to the
-// unpruned one, and a prompt gives the same bits however it is cut into
-// ubatches (a restored prefix plus a suffix included).
+// state unchanged.  gc comes from the launch's key count, which the ubatch's
+// last row shares whether the launch carries the whole ubatch (M = T) or that
+// row alone (M = 1, the KV-shared layers after pruning): the pruned output row
+// is bit-identical to the unpruned one.  (Rows of a prompt cut into ubatches
+// differently can see different gc, so such runs agree to rounding.)
 //
 // CTA roles: warp 1 lane 0 issues the TMA copies (Q once; K and V per chunk,
 // double-buffered); warp 0 allocates TMEM and its lane 0 issues the MMAs;

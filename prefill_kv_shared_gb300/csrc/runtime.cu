@@ -568,7 +568,6 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       a.hd = c->hd;
       a.pos_base = pos_base;
       a.kv_len = kv_len;
-      a.group_kv = c->d.max_ctx;
       a.err = c->err;
       // (query head, visible key) pairs: rows at positions pos_base .. pos_base+M-1
       const double pairs = static_cast<double>(M) * pos_base + 0.5 * M * (M + 1.0);

@@ -139,8 +139,10 @@ def tinyllama():
 
 def test_kv_restore_suffix_equals_full(gpu, tinyllama):
     """Cache a 500-token prefix as a KV image, restore it, prefill a 32-token
-    suffix: same logits as the full 532-token prefill (bit-identical on the
-    GPU) and within tolerance of the oracle."""
+    suffix: the logits of the full 532-token prefill to rounding (the two runs
+    cut the prompt into ubatches differently, and attention groups a row's
+    key chunks by its launch's key count) and within tolerance of the
+    oracle."""
     cfg = tinyllama.cfg
     prefix = synth.make_tokens(cfg, 500, seed=1)
     ctx = binding.PrefillContext(tinyllama, max_ctx=532, ubatch_max=512)
@@ -166,7 +168,7 @@ def test_kv_restore_suffix_equals_full(gpu, tinyllama):
         ctx.ubatch(suffix, 500, True, logits)
         ctx.sync()
         got = logits.cpu().numpy()
-        np.testing.assert_array_equal(got, full)
+        assert np.abs(got - full).max() <= 2e-3 * np.abs(full).max()
         o2 = OracleContext(cfg, tinyllama, 532)
         o2.kv_load(orc.kv_save(), 500)
         check_logits(got, o2.ubatch(suffix, True))
