@@ -13,7 +13,8 @@
 //     S = Q K^T (tcgen05.mma, TMEM), m' = max(m, max_k s_k),
 //     p_k = fp16(2^((s_k - m') c)), l' = l 2^((m - m') c) + sum_k p_k,
 //     O' = O 2^((m - m') c) + P V (the rescale in TMEM, P V by tcgen05.mma)
-// with c = log2(e)/sqrt(hd).  A row whose keys lie in one group writes O / l;
+// with c = log2(e)/sqrt(hd).  A row whose keys lie in one group writes
+// O * (1/l);
 // otherwise each group's (O, m, l) goes to a partials buffer and
 // attn_merge_kernel combines the row's group states.  So the causal work
 // spreads over many CTAs instead of piling up on those of the last rows.
@@ -366,6 +367,7 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
       const bool final_row = pos >= 0 && n_g == 1;
       const bool part_row = pos >= 0 && n_g > 1 && grp < n_g;
       float* pdst = part_row ? part + (((size_t)t * sh.Hq + head) * ATTN_MAX_GROUPS + grp) * (HD + 2) : nullptr;
+      const float inv_l = final_row ? __frcp_rn(l) : 0.f;  // out = O * (1/l)
       __nv_bfloat16* odst = final_row ? out + (size_t)t * sh.Hq * HD + (size_t)head * HD : nullptr;
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
@@ -378,8 +380,8 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const __nv_bfloat162 h = __floats2bfloat162_rn(__fdiv_rn(__uint_as_float(x[q + 2 * e]), l),
-                                                             __fdiv_rn(__uint_as_float(x[q + 2 * e + 1]), l));
+              const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(x[q + 2 * e]), inv_l),
+                                                             __fmul_rn(__uint_as_float(x[q + 2 * e + 1]), inv_l));
               w[e] = *reinterpret_cast<const uint32_t*>(&h);
             }
             *reinterpret_cast<uint4*>(odst + 32 * c + q) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -467,10 +469,11 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict
     }
   }
   __nv_bfloat16* dst = out + (size_t)t * Hq * HD + (size_t)head * HD + lane * PER;
+  const float inv_l = __frcp_rn(l);
 #pragma unroll
   for (int i = 0; i < PER; i += 2)
     *reinterpret_cast<__nv_bfloat162*>(dst + i) =
-        __floats2bfloat162_rn(__fdiv_rn(acc[i], l), __fdiv_rn(acc[i + 1], l));
+        __floats2bfloat162_rn(__fmul_rn(acc[i], inv_l), __fmul_rn(acc[i + 1], inv_l));
 }
 
 // ---------------------------------------------------------------------------
