@@ -117,6 +117,14 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                            int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+      "[%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
 
 // 32 lanes x 32 consecutive 32-bit columns from registers (thread i -> lane i)
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -208,20 +216,18 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
     // ---------------- TMA producer
     if (lane == 0) {
       bool ok = true;
+      // one copy per tile: the maps list the 64-dim box index last, so a
+      // copy lands as [box][rows][128 B]
       mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-      for (int b = 0; b < C::NB; ++b) tma_load_3d(smem + b * (128 * 128), &tmQ, q_full, 64 * b, kvh * G, t0);
+      tma_load_4d(smem, &tmQ, q_full, 0, kvh * G, t0, 0);
       for (int j = 0; j < n && ok; ++j) {
         const int s = j & 1;
         if (j >= 2) ok = mbar_wait(&kv_empty[s], ((j - 2) >> 1) & 1, err, PF_DEV_TIMEOUT_PRODUCER);
         if (!ok) break;
         mbar_arrive_expect_tx(&kv_full[s], 2 * C::KV_BYTES);
         const int key0 = (ch_first + j) * CHUNK;
-        for (int b = 0; b < C::NB; ++b) {
-          tma_load_2d(smem + C::OFF_K + s * C::KV_BYTES + b * (CHUNK * 128), &tmK, &kv_full[s], kvh * HD + 64 * b,
-                      key0);
-          tma_load_2d(smem + C::OFF_V + s * C::KV_BYTES + b * (CHUNK * 128), &tmV, &kv_full[s], kvh * HD + 64 * b,
-                      key0);
-        }
+        tma_load_3d(smem + C::OFF_K + s * C::KV_BYTES, &tmK, &kv_full[s], kvh * HD, key0, 0);
+        tma_load_3d(smem + C::OFF_V + s * C::KV_BYTES, &tmV, &kv_full[s], kvh * HD, key0, 0);
       }
     }
     __syncwarp();
@@ -489,22 +495,29 @@ static cudaError_t launch_tc_t(const AttnArgs& a, float* part, cudaStream_t s) {
     attr = true;
   }
   const int G = a.Hq / a.Hkv;
-  // Q viewed as [query][head][dim]; K and V as [key][Hkv*hd], keys past
-  // kv_len read as zeros
+  // Q viewed as [64-dim box][query][head][64 dims]; K and V as [64-dim
+  // box][key][64 dims] (the box dimension listed last, its stride 128 B), so
+  // that one copy brings a whole tile as [box][rows][128 B]; keys past kv_len
+  // read as zeros
   CUtensorMap tq, tk, tv;
   std::string err;
   {
-    const uint64_t dims[3] = {static_cast<uint64_t>(HD), static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(a.M)};
-    const uint64_t st[2] = {static_cast<uint64_t>(HD) * 2, static_cast<uint64_t>(a.Hq) * HD * 2};
-    const uint32_t box[3] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(128 / G)};
-    if (!encode_fp16_sw128(&tq, a.q, 3, dims, st, box, &err)) return cudaErrorInvalidValue;
+    const uint64_t dims[4] = {64, static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(a.M),
+                              static_cast<uint64_t>(HD / 64)};
+    const uint64_t st[3] = {static_cast<uint64_t>(HD) * 2, static_cast<uint64_t>(a.Hq) * HD * 2, 128};
+    const uint32_t box[4] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(128 / G),
+                             static_cast<uint32_t>(HD / 64)};
+    if (!encode_fp16_sw128(&tq, a.q, 4, dims, st, box, &err)) return cudaErrorInvalidValue;
   }
   {
-    const uint64_t dims[2] = {static_cast<uint64_t>(a.Hkv) * HD, static_cast<uint64_t>(a.kv_len)};
-    const uint64_t st[1] = {static_cast<uint64_t>(a.Hkv) * HD * 2};
-    const uint32_t box[2] = {64, CHUNK};
-    if (!encode_fp16_sw128(&tk, a.k, 2, dims, st, box, &err)) return cudaErrorInvalidValue;
-    if (!encode_fp16_sw128(&tv, a.v, 2, dims, st, box, &err)) return cudaErrorInvalidValue;
+    // the KV head's dims start at column kvh*HD: coordinate 0 of the
+    // innermost dimension spans the whole row so the head offset fits in it
+    const uint64_t dims[3] = {static_cast<uint64_t>(a.Hkv) * HD, static_cast<uint64_t>(a.kv_len),
+                              static_cast<uint64_t>(HD / 64)};
+    const uint64_t st[2] = {static_cast<uint64_t>(a.Hkv) * HD * 2, 128};
+    const uint32_t box[3] = {64, CHUNK, static_cast<uint32_t>(HD / 64)};
+    if (!encode_fp16_sw128(&tk, a.k, 3, dims, st, box, &err)) return cudaErrorInvalidValue;
+    if (!encode_fp16_sw128(&tv, a.v, 3, dims, st, box, &err)) return cudaErrorInvalidValue;
   }
   AttnTcShape sh;
   sh.M = a.M;
