@@ -95,7 +95,7 @@ int pfop_linear_bench(int32_t wtype, const void* w_host, int32_t N, int32_t K, i
    q fp16 [Hq*hd] at position pos; K/V fp16 [positions][Hkv*hd] with keys
    [0, kv_len) valid, pos < kv_len; out bf16 [Hq*hd].
    Scratch: one fixed device array of 2^21 floats (8 MiB) per GPU that loads
-   the library, kept until exit.  A call needs Hq*4*(hd+2) floats when the
+   the library, kept until exit.  A call needs Hq*4*(hd+4) floats when the
    row's keys span more than one chunk group (see pfop_attention), else none;
    larger requests return PF_E_ARG without touching the GPU.  All calls share
    the array, so calls that overlap on the GPU race: order them on one stream

@@ -50,9 +50,10 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// partials layout: [row t][query head][group (ATTN_MAX_GROUPS)][HD + 2] =
-// o[HD] (not normalised), m, l
+// partials layout: [row t][query head][group (ATTN_MAX_GROUPS)][HD + 4] =
+// o[HD] (not normalised), m, l, 2 pad (16-byte aligned rows)
 constexpr int ATTN_MAX_GROUPS = 4;
+__host__ __device__ constexpr int attn_part_stride(int hd) { return hd + 4; }
 
 int attn_group_chunks(int kv_len) {
   const int n_chunks = (kv_len + CHUNK - 1) / CHUNK;
@@ -368,40 +369,57 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
     }
     if (ok) {
+      // Each 32 x 32 block of O goes through a warp-private staging buffer
+      // in the (now idle) P tiles, so that the global stores cover whole row
+      // segments: lane l stores rows 4i + l/8, columns 4(l%8) .. +3.
       tc_fence_after();
+      // this lane's row: 0 = nothing to write, 1 = output row, 2 = group state
       const int n_g = pos >= 0 ? attn_row_groups(pos, sh.gc) : 0;
-      const bool final_row = pos >= 0 && n_g == 1;
-      const bool part_row = pos >= 0 && n_g > 1 && grp < n_g;
-      float* pdst = part_row ? part + (((size_t)t * sh.Hq + head) * ATTN_MAX_GROUPS + grp) * (HD + 2) : nullptr;
-      const float inv_l = final_row ? __frcp_rn(l) : 0.f;  // out = O * (1/l)
-      __nv_bfloat16* odst = final_row ? out + (size_t)t * sh.Hq * HD + (size_t)head * HD : nullptr;
+      const int kind_own = pos < 0 ? 0 : (n_g == 1 ? 1 : (grp < n_g ? 2 : 0));
+      const float inv_l = kind_own == 1 ? __frcp_rn(l) : 1.f;  // output rows: O * (1/l)
+      // destinations of the rows this lane writes in the transposed layout
+      // (rows 4i + lane/8), fetched once from the rows' own lanes
+      const size_t own_off = kind_own == 1 ? (size_t)t * sh.Hq * HD + (size_t)head * HD
+                                           : (((size_t)t * sh.Hq + head) * ATTN_MAX_GROUPS + grp) * attn_part_stride(HD);
+      const int rs = lane >> 3, pc = lane & 7;
+      size_t dst_off[8];
+      int dst_kind[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = 4 * i + rs;
+        dst_kind[i] = __shfl_sync(0xffffffffu, kind_own, rr);
+        const uint32_t lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(own_off), rr);
+        const uint32_t hi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(own_off >> 32), rr);
+        dst_off[i] = (static_cast<size_t>(hi) << 32) | lo;
+      }
+      uint8_t* stg = smem + C::OFF_P + qw * 4096;
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t x[32];
         tmem_ld32(tmem + lane_base + C::TMEM_O + 32 * c, x);
         tmem_ld_wait();
-        if (odst) {
 #pragma unroll
-          for (int q = 0; q < 32; q += 8) {
-            uint32_t w[4];
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4*>(stg + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+              make_float4(__fmul_rn(__uint_as_float(x[4 * q]), inv_l), __fmul_rn(__uint_as_float(x[4 * q + 1]), inv_l),
+                          __fmul_rn(__uint_as_float(x[4 * q + 2]), inv_l), __fmul_rn(__uint_as_float(x[4 * q + 3]), inv_l));
+        __syncwarp();
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(x[q + 2 * e]), inv_l),
-                                                             __fmul_rn(__uint_as_float(x[q + 2 * e + 1]), inv_l));
-              w[e] = *reinterpret_cast<const uint32_t*>(&h);
-            }
-            *reinterpret_cast<uint4*>(odst + 32 * c + q) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int i = 0; i < 8; ++i) {
+          const int rr = 4 * i + rs;
+          if (dst_kind[i] == 0) continue;
+          const float4 v = *reinterpret_cast<const float4*>(stg + rr * 128 + ((pc ^ (rr & 7)) << 4));
+          if (dst_kind[i] == 1) {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+            *reinterpret_cast<uint2*>(out + dst_off[i] + 32 * c + 4 * pc) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+          } else {
+            *reinterpret_cast<float4*>(part + dst_off[i] + 32 * c + 4 * pc) = v;
           }
-        } else if (pdst) {
-#pragma unroll
-          for (int q = 0; q < 32; q += 2)
-            *reinterpret_cast<float2*>(pdst + 32 * c + q) = make_float2(__uint_as_float(x[q]), __uint_as_float(x[q + 1]));
         }
+        __syncwarp();
       }
-      if (pdst) {
-        pdst[HD] = m;
-        pdst[HD + 1] = l;
-      }
+      if (kind_own == 2) *reinterpret_cast<float2*>(part + own_off + HD) = make_float2(m, l);
     }
   }
   tc_fence_before();
@@ -435,11 +453,11 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict
   const int t = t0 + pair / Hq, head = pair % Hq;
   if (t >= M) return;
   const int n_g = attn_row_groups(pos_base + t, gc);  // 2 .. ATTN_MAX_GROUPS
-  const float* base = part + ((size_t)t * Hq + head) * ATTN_MAX_GROUPS * (HD + 2);
+  const float* base = part + ((size_t)t * Hq + head) * ATTN_MAX_GROUPS * attn_part_stride(HD);
   // lane g < n_g fetches group g's (m, l)
   float mg = -INFINITY, lg = 0.f;
   if (lane < n_g) {
-    const float2 ml = *reinterpret_cast<const float2*>(base + (size_t)lane * (HD + 2) + HD);
+    const float2 ml = *reinterpret_cast<const float2*>(base + (size_t)lane * attn_part_stride(HD) + HD);
     mg = ml.x;
     lg = ml.y;
   }
@@ -455,7 +473,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict
     float oj[4][PER];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float* p = base + (size_t)(g0 + k) * (HD + 2) + lane * PER;
+      const float* p = base + (size_t)(g0 + k) * attn_part_stride(HD) + lane * PER;
 #pragma unroll
       for (int i = 0; i < PER; i += 2) {
         float2 v = make_float2(0.f, 0.f);
@@ -572,7 +590,7 @@ size_t attn_partials_floats(int M, int Hq, int hd, int kv_len) {
   const int gc = attn_group_chunks(kv_len > 0 ? kv_len : 1);
   const int n_groups = attn_row_groups(kv_len > 0 ? kv_len - 1 : 0, gc);
   if (n_groups <= 1) return 0;
-  return static_cast<size_t>(M > 0 ? M : 0) * Hq * ATTN_MAX_GROUPS * (hd + 2);
+  return static_cast<size_t>(M > 0 ? M : 0) * Hq * ATTN_MAX_GROUPS * attn_part_stride(hd);
 }
 
 }  // namespace pf

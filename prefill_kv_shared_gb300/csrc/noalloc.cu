@@ -12,7 +12,7 @@
 // Limits and sharing:
 //   - the array holds PF_NOALLOC_SCRATCH_FLOATS floats (8 MiB); every GPU
 //     that loads this library keeps it until the process exits;
-//   - a request needs n_head * 4 * (head_dim + 2) floats when the row's keys
+//   - a request needs n_head * 4 * (head_dim + 4) floats when the row's keys
 //     span more than one chunk group, none otherwise, and is refused
 //     (PF_E_ARG) when that is more than the array holds;
 //   - every call, on every stream, uses the same array: calls whose work

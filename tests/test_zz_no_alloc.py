@@ -49,8 +49,8 @@ def test_noalloc_matches_allocating_entry_point_twice(lib, Hq, Hkv, hd):
 def test_noalloc_refuses_requests_beyond_the_array(lib):
     q, k, v = _inputs(3, 8, 1, 256, 64)
     out = torch.empty((1, 8 * 256), dtype=torch.bfloat16, device="cuda")
-    # keys spanning several chunk groups need Hq * 4 * (hd + 2) floats:
-    # 2048 heads * 4 * 258 is beyond 2^21 floats (refused before any launch,
+    # keys spanning several chunk groups need Hq * 4 * (hd + 4) floats:
+    # 2048 heads * 4 * 260 is beyond 2^21 floats (refused before any launch,
     # so the small buffers are never read)
     rc = lib.pfop_attention_split_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), 2048, 128, 256, 1023, 1024,
                                           out.data_ptr(), None)
