@@ -41,6 +41,7 @@ def parse_args():
     ap.add_argument("--sweep-steps", type=int, default=5)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-hbm", action="store_true", help="skip the single-row attention / KV restore timings")
     ap.add_argument("--profile-passes", type=int, default=0,
                     help="run this many untimed prefill passes of the workload and exit (for ncu)")
     return ap.parse_args()
@@ -250,6 +251,67 @@ def run_reference(args, dist: Dist):
 
 
 # ---------------------------------------------------------------------------
+# HBM-bound kernels on their own: the single-row KV-shared attention and the
+# KV image restore, each cold (L2 scrubbed before every timed launch) and warm
+
+
+def hbm_kernels(dev, stream, peaks, iters: int = 20):
+    import ctypes as C
+
+    import torch
+
+    from prefill_kv_shared_gb300 import binding
+    lib = binding.load()
+    bw = peaks["hbm_gbs"]
+    scrub = torch.empty(512 << 20, dtype=torch.uint8, device=dev)  # 512 MB > L2 (129 MB)
+    sp = C.c_void_p(scrub.data_ptr())
+    us = C.c_float(0.0)
+    sh = C.c_void_p(stream.cuda_stream)
+    g = torch.Generator(device=dev)
+    g.manual_seed(3)
+    out = {"shared_attention": {}, "kv_restore": {}}
+    # (model, Hq, Hkv, hd, keys): the single-row attention of a KV-shared layer
+    for name, hq, hkv, hd, n in (("e2b", 8, 1, 256, 8192), ("e2b", 8, 1, 256, 32768),
+                                 ("e4b", 8, 2, 256, 8192), ("e4b", 8, 2, 256, 32768)):
+        q = torch.randn(hq * hd, generator=g, device=dev).half()
+        k = torch.randn(n, hkv * hd, generator=g, device=dev).half()
+        v = torch.randn(n, hkv * hd, generator=g, device=dev).half()
+        o = torch.empty(hq * hd, dtype=torch.bfloat16, device=dev)
+        algo = 2.0 * n * hkv * hd * 2  # K and V read once
+        row = {"keys": n, "bytes": algo}
+        for tag, sc in (("cold", sp), ("warm", None)):
+            rc = lib.pfop_attention_bench(1, q.data_ptr(), k.data_ptr(), v.data_ptr(), 1, hq, hkv, hd, n - 1, n,
+                                          o.data_ptr(), sc, scrub.numel() if sc else 0, 3, iters, C.byref(us), sh)
+            binding.check_op(rc)
+            gbs = algo / (us.value * 1e-6) / 1e9
+            row[tag] = {"us": us.value, "gbs": gbs, "frac": gbs / bw}
+        out["shared_attention"][f"{name}_{n}"] = row
+        del q, k, v, o
+    # (workload, writing layers, kv_dim, positions): kv_load of a KV image
+    for name, lw, kv, n in (("tinyllama_500", 22, 256, 500), ("e2b_8192", 16, 256, 8192),
+                            ("e4b_8192", 24, 512, 8192), ("e4b_32768", 24, 512, 32768)):
+        seg = n * kv * 2
+        image = torch.empty(16 + 2 * lw * seg, dtype=torch.uint8, device=dev)
+        cache = torch.empty(2 * lw * n * kv, dtype=torch.float16, device=dev)
+        algo = 2.0 * (2 * lw * seg)  # read the image body, write the cache
+        row = {"image_bytes": image.numel(), "bytes": algo}
+        for tag, sc in (("cold", sp), ("warm", None)):
+            rc = lib.pfop_kv_copy_bench(1, cache.data_ptr(), n * kv, image.data_ptr(), seg, 2 * lw, seg, sc,
+                                        scrub.numel() if sc else 0, 3, iters, C.byref(us), sh)
+            binding.check_op(rc)
+            gbs = algo / (us.value * 1e-6) / 1e9
+            row[tag] = {"us": us.value, "gbs": gbs, "frac": gbs / bw}
+        out["kv_restore"][name] = row
+        del image, cache
+    del scrub
+    torch.cuda.empty_cache()
+    out["peak_gbs"] = bw
+    out["note"] = ("bytes = algorithmic traffic (K and V read once; image read + cache written); "
+                   "cold: 512 MB written before every timed launch; mean of %d launches" % iters)
+    return out
+
+
+# ---------------------------------------------------------------------------
 # our arm
 
 
@@ -367,32 +429,48 @@ def run_ours(args, dist: Dist):
     assert np.isfinite(out_pinned.numpy()).all()
     ctx.close()
 
-    # pruning on/off at 512/2048/8192 (ubatches of 512), rank 0's GPU only
+    # pruning on/off: E2B at 512/2048/8192/32768 (ubatches of 512) and E4B at
+    # 8192 (ubatches of 1024), rank 0's GPU only
     sweep = None
     if not args.no_sweep and dist.rank == 0:
         sweep = {}
-        big = binding.PrefillContext(w, max_ctx=8192, ubatch_max=UB, prune=True, stream=stream)
-        for n in (512, 2048, 8192):
-            t = torch.from_numpy(synth.make_tokens(cfg, n)).to(dev)
+        models = {"e2b": w}
+        for mname, n, ub in (("e2b", 512, 512), ("e2b", 2048, 512), ("e2b", 8192, 512), ("e2b", 32768, 512),
+                             ("e4b", 8192, 1024)):
+            if mname not in models:
+                models.clear()  # one model's weights resident at a time
+                models[mname] = synth.make_weights(synth.config(mname))
+            wm = models[mname]
+            big = binding.PrefillContext(wm, max_ctx=n, ubatch_max=ub, prune=True, stream=stream)
+            lg = torch.empty(wm.cfg["vocab"], dtype=torch.float32, device=dev)
+            t = torch.from_numpy(synth.make_tokens(wm.cfg, n)).to(dev)
+            key = f"{n}" if mname == "e2b" else f"{mname}_{n}"
+            steps_n = args.sweep_steps if n <= 8192 else max(2, args.sweep_steps // 2)
             for prune in (True, False):
                 big.set_prune(prune)
 
                 def sweep_step():
                     big.reset()
-                    for i in range(0, n, UB):
-                        big.ubatch(t[i:i + UB], i, i + UB >= n, logits)
+                    for i in range(0, n, ub):
+                        big.ubatch(t[i:i + ub], i, i + ub >= n, lg)
                 sweep_step()
                 big.sync()
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-                for _ in range(args.sweep_steps):
+                for _ in range(steps_n):
                     sweep_step()
                 b.record(stream)
                 torch.cuda.synchronize(dev)
-                sms = a.elapsed_time(b) / args.sweep_steps
-                sweep[f"{n}_{'on' if prune else 'off'}"] = {"ms": sms, "tokens_per_s": n / (sms * 1e-3)}
-            sweep[f"{n}_speedup"] = sweep[f"{n}_off"]["ms"] / sweep[f"{n}_on"]["ms"]
-        big.close()
+                sms = a.elapsed_time(b) / steps_n
+                sweep[f"{key}_{'on' if prune else 'off'}"] = {"ms": sms, "tokens_per_s": n / (sms * 1e-3)}
+            sweep[f"{key}_speedup"] = sweep[f"{key}_off"]["ms"] / sweep[f"{key}_on"]["ms"]
+            big.close()
+            del t, lg
+        models.clear()
+
+    hbm = None
+    if not args.no_hbm and dist.rank == 0:
+        hbm = hbm_kernels(dev, stream, load_peaks()[0])
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
@@ -411,6 +489,7 @@ def run_ours(args, dist: Dist):
                        "l2": "inputs larger than L2 (488 MB of Q4_0 weights streamed every step)"},
             "gpu_launches": int(round(launches_per_step * args.steps)),
             "e2e": e2e, "roofline": roofline, "clocks": clk, "cpu_baseline": cpu, "sweep": sweep,
+            "hbm_kernels": hbm,
         }
         print(json.dumps(line), flush=True)
 

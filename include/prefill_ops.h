@@ -87,6 +87,28 @@ int pfop_linear_bench(int32_t wtype, const void* w_host, int32_t N, int32_t K, i
                       const void* a_dev, int32_t a_rows, int32_t M, float* out_dev, int32_t warmup, int32_t iters,
                       float* us, void* stream);
 
+/* Time the attention kernels of pfop_attention (same arguments and modes):
+   `warmup` untimed calls, then `iters` timed ones, each bracketed by its own
+   CUDA events on `stream`; *us = mean device time per call (the split or
+   prefill kernel plus the group-state merge when it runs).  If scrub_dev is
+   not NULL, scrub_bytes of it (a caller-owned device buffer larger than L2)
+   are overwritten before every timed call, outside the events, so that each
+   call reads K/V from HBM (cold L2).  Reading K/V once is the op's
+   algorithmic traffic: kv_len * Hkv * hd * 2 bytes for each of K and V.
+   Returns PF_E_DEVICE_TIMEOUT if a bounded wait gave up. */
+int pfop_attention_bench(int32_t mode, const void* q_dev, const void* k_dev, const void* v_dev, int32_t M, int32_t Hq,
+                         int32_t Hkv, int32_t hd, int32_t pos_base, int32_t kv_len, void* out_dev, void* scrub_dev,
+                         int64_t scrub_bytes, int32_t warmup, int32_t iters, float* us, void* stream);
+
+/* Time the KV image copy kernel of pfop_kv_copy (same layout arguments; the
+   image header written by dir 0 is all zeros here) like
+   pfop_attention_bench: mean device time per launch in *us, optional L2
+   scrub of scrub_dev before every timed launch.  The copy reads and writes
+   n_seg * copy_bytes bytes each. */
+int pfop_kv_copy_bench(int32_t dir, void* cache_dev, int64_t cache_seg_halves, void* image_dev, int64_t img_seg_bytes,
+                       int32_t n_seg, int64_t copy_bytes, void* scrub_dev, int64_t scrub_bytes, int32_t warmup,
+                       int32_t iters, float* us, void* stream);
+
 /* The single-row split-K attention of pfop_attention (mode 1) without any
    memory allocation, for callers that may not allocate device memory at this
    point (a fixed memory budget already handed out, a server that forbids

@@ -38,7 +38,7 @@ EXPORTS = (
     "prefill_kv_image_bytes_for", "prefill_set_timing", "prefill_get_stats", "prefill_reset_stats",
     "pfop_linear_f32", "pfop_linear_resid", "pfop_linear_glu", "pfop_linear_ple", "pfop_linear_qkv",
     "pfop_attention", "pfop_rmsnorm", "pfop_embed", "pfop_kv_copy", "pfop_last_error", "pfop_linear_bench",
-    "pfop_attention_split_noalloc",
+    "pfop_attention_split_noalloc", "pfop_attention_bench", "pfop_kv_copy_bench",
 )
 
 
@@ -127,6 +127,10 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "pfop_attention_split_noalloc": (C.c_int, [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
         "pfop_linear_bench": (C.c_int, [i32, vp, i32, i32, i32, i32, vp, i32, i32, vp, i32, i32,
                                         C.POINTER(C.c_float), vp]),
+        "pfop_attention_bench": (C.c_int, [i32, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, i64, i32, i32,
+                                           C.POINTER(C.c_float), vp]),
+        "pfop_kv_copy_bench": (C.c_int, [i32, vp, i64, vp, i64, i32, i64, vp, i64, i32, i32,
+                                         C.POINTER(C.c_float), vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

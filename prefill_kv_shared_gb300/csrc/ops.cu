@@ -378,3 +378,93 @@ extern "C" int pfop_kv_copy(int32_t dir, void* cache_dev, int64_t cache_seg_halv
   OP_CUDA(cudaStreamSynchronize(s));
   return PF_OK;
 }
+
+namespace {
+
+// Mean device time of `iters` timed repetitions of `launch` on s, each
+// bracketed by its own pair of events; with a scrub buffer, a memset of it
+// runs before every repetition (outside the events) so that the timed
+// kernels start with their operands evicted from L2.
+template <class F>
+int time_launches(F&& launch, void* scrub, int64_t scrub_bytes, int warmup, int iters, float* us, cudaStream_t s) {
+  for (int i = 0; i < warmup; ++i) OP_CUDA(launch());
+  std::vector<cudaEvent_t> ev(2 * static_cast<size_t>(iters), nullptr);
+  struct Ev {
+    std::vector<cudaEvent_t>& v;
+    ~Ev() {
+      for (cudaEvent_t e : v)
+        if (e) cudaEventDestroy(e);
+    }
+  } guard{ev};
+  for (auto& e : ev) OP_CUDA(cudaEventCreate(&e));
+  for (int i = 0; i < iters; ++i) {
+    if (scrub && scrub_bytes > 0) OP_CUDA(cudaMemsetAsync(scrub, i & 0xff, static_cast<size_t>(scrub_bytes), s));
+    OP_CUDA(cudaEventRecord(ev[2 * i], s));
+    OP_CUDA(launch());
+    OP_CUDA(cudaEventRecord(ev[2 * i + 1], s));
+  }
+  OP_CUDA(cudaStreamSynchronize(s));
+  double total = 0.0;
+  for (int i = 0; i < iters; ++i) {
+    float ms = 0.f;
+    OP_CUDA(cudaEventElapsedTime(&ms, ev[2 * i], ev[2 * i + 1]));
+    total += ms;
+  }
+  *us = static_cast<float>(total * 1000.0 / iters);
+  return PF_OK;
+}
+
+}  // namespace
+
+extern "C" int pfop_attention_bench(int32_t mode, const void* q_dev, const void* k_dev, const void* v_dev, int32_t M,
+                                    int32_t Hq, int32_t Hkv, int32_t hd, int32_t pos_base, int32_t kv_len,
+                                    void* out_dev, void* scrub_dev, int64_t scrub_bytes, int32_t warmup,
+                                    int32_t iters, float* us, void* stream) {
+  if (!q_dev || !k_dev || !v_dev || !out_dev || !us || M < 1 || pos_base < 0 || pos_base + M > kv_len || iters < 1 ||
+      warmup < 0 || scrub_bytes < 0)
+    return op_fail(PF_E_ARG, "bad argument");
+  if (mode != 0 && mode != 1) return op_fail(PF_E_ARG, "mode");
+  if (mode == 1 && M != 1) return op_fail(PF_E_ARG, "split mode takes one row");
+  AttnArgs a;
+  a.q = static_cast<const __half*>(q_dev);
+  a.k = static_cast<const __half*>(k_dev);
+  a.v = static_cast<const __half*>(v_dev);
+  a.out = static_cast<__nv_bfloat16*>(out_dev);
+  a.M = M;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.hd = hd;
+  a.pos_base = pos_base;
+  a.kv_len = kv_len;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Scope sc;
+  float* part = nullptr;
+  int* err = nullptr;
+  OP_CUDA(sc.alloc(&part, attn_partials_floats(M, Hq, hd, kv_len) * 4));
+  OP_CUDA(sc.alloc(&err, 16));
+  OP_CUDA(cudaMemsetAsync(err, 0, 16, s));
+  a.err = err;
+  int rc = time_launches([&] { return mode == 0 ? launch_attn_prefill(a, part, s) : launch_attn_split(a, part, s); },
+                         scrub_dev, scrub_bytes, warmup, iters, us, s);
+  if (rc) return rc;
+  int h = 0;
+  OP_CUDA(cudaMemcpy(&h, err, 4, cudaMemcpyDeviceToHost));
+  if (h) return op_fail(PF_E_DEVICE_TIMEOUT, "attention gave up a bounded wait, code " + std::to_string(h));
+  return PF_OK;
+}
+
+extern "C" int pfop_kv_copy_bench(int32_t dir, void* cache_dev, int64_t cache_seg_halves, void* image_dev,
+                                  int64_t img_seg_bytes, int32_t n_seg, int64_t copy_bytes, void* scrub_dev,
+                                  int64_t scrub_bytes, int32_t warmup, int32_t iters, float* us, void* stream) {
+  if (!cache_dev || !image_dev || !us || n_seg < 0 || copy_bytes < 0 || (dir != 0 && dir != 1) || iters < 1 ||
+      warmup < 0 || scrub_bytes < 0)
+    return op_fail(PF_E_ARG, "bad argument");
+  const int32_t hdr[4] = {0, 0, 0, 0};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return time_launches(
+      [&] {
+        return launch_kv_copy(dir, static_cast<__half*>(cache_dev), cache_seg_halves, static_cast<uint8_t*>(image_dev),
+                              img_seg_bytes, n_seg, copy_bytes, hdr, s);
+      },
+      scrub_dev, scrub_bytes, warmup, iters, us, s);
+}

@@ -114,7 +114,7 @@ def test_e2b_512_matches_oracle(gpu, e2b):
     check_logits(on, want)
 
 
-@pytest.mark.parametrize("n", [2048, 8192])
+@pytest.mark.parametrize("n", [2048, 8192, 32768])
 def test_e2b_prune_bit_identical(gpu, e2b, n):
     tok = synth.make_tokens(e2b.cfg, n)
     on = run_gpu(e2b, tok, 512, True)

@@ -290,3 +290,44 @@ def test_kv_copy_roundtrip(lib):
                                       None, None))
     assert torch.equal(back[:, :, :k], cache[:, :, :k])
     assert not back[:, :, k:].any()
+
+
+def test_attention_bench_runs_the_same_kernels(lib):
+    """The timing entry point leaves the same single-row output as the plain
+    call (bit for bit) and reports a positive time, with and without the L2
+    scrub."""
+    import ctypes as C
+    rng = np.random.default_rng(11)
+    Hq, Hkv, hd, kv_len = 8, 1, 256, 3000
+    q, k, v = _attn_inputs(rng, 1, Hq, Hkv, hd, kv_len)
+    tq, tk, tv = (torch.from_numpy(t).cuda() for t in (q, k, v))
+    ref = torch.empty((1, Hq * hd), dtype=torch.bfloat16, device="cuda")
+    binding.check_op(lib.pfop_attention(1, tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), 1, Hq, Hkv, hd, kv_len - 1,
+                                        kv_len, ref.data_ptr(), None))
+    scrub = torch.empty(1 << 24, dtype=torch.uint8, device="cuda")
+    for sc, nb in ((scrub.data_ptr(), scrub.numel()), (None, 0)):
+        out = torch.zeros_like(ref)
+        us = C.c_float(0.0)
+        binding.check_op(lib.pfop_attention_bench(1, tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), 1, Hq, Hkv, hd,
+                                                  kv_len - 1, kv_len, out.data_ptr(), sc, nb, 1, 3, C.byref(us),
+                                                  None))
+        assert us.value > 0
+        assert torch.equal(out, ref)
+    assert lib.pfop_attention_bench(1, tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), 2, Hq, Hkv, hd, kv_len - 2,
+                                    kv_len, ref.data_ptr(), None, 0, 0, 1, C.byref(us), None) == binding.PF_E_ARG
+
+
+def test_kv_copy_bench_restores_exactly(lib):
+    import ctypes as C
+    rng = np.random.default_rng(12)
+    L_w, n, kv = 4, 300, 256
+    seg = n * kv * 2
+    img = torch.from_numpy(rng.integers(0, 256, 16 + 2 * L_w * seg, dtype=np.uint8)).cuda()
+    cache = torch.zeros((2, L_w, n, kv), dtype=torch.float16, device="cuda")
+    scrub = torch.empty(1 << 24, dtype=torch.uint8, device="cuda")
+    us = C.c_float(0.0)
+    binding.check_op(lib.pfop_kv_copy_bench(1, cache.data_ptr(), n * kv, img.data_ptr(), seg, 2 * L_w, seg,
+                                            scrub.data_ptr(), scrub.numel(), 1, 2, C.byref(us), None))
+    assert us.value > 0
+    got = cache.cpu().numpy().view(np.uint8).reshape(-1)
+    np.testing.assert_array_equal(got, img[16:].cpu().numpy())
