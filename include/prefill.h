@@ -167,11 +167,13 @@ int kv_load(prefill_ctx* ctx, const void* src, size_t src_bytes, int64_t n_pos);
    at least).  With timing on, each launch is bracketed by CUDA events on
    the context's stream (this adds host overhead; use it on a separate run
    from throughput measurements). */
-#define PF_KC_GEMM 0  /* projections and the LM head (tcgen05) */
-#define PF_KC_ATTN 1  /* attention, chunk merge */
-#define PF_KC_NORM 2  /* RMSNorm (+ row gather) */
-#define PF_KC_OTHER 3 /* embedding gather, KV image copies */
-#define PF_KC_COUNT 4
+#define PF_KC_GEMM 0      /* projections of launches with more than 16 rows (tcgen05, tensor-bound) */
+#define PF_KC_ATTN 1      /* prefill attention and its group-state merge */
+#define PF_KC_NORM 2      /* RMSNorm (+ row gather) */
+#define PF_KC_OTHER 3     /* embedding gather, KV image copies */
+#define PF_KC_GEMM_ROW 4  /* projections of at most 16 rows: the pruned output row and the LM head (weight-bound) */
+#define PF_KC_ATTN_ROW 5  /* the single-row attention of the KV-shared layers after pruning */
+#define PF_KC_COUNT 6
 
 typedef struct prefill_stats {
   int64_t launches[PF_KC_COUNT];

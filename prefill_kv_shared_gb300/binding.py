@@ -60,13 +60,14 @@ class ModelDesc(C.Structure):
     ]
 
 
-KC_GEMM, KC_ATTN, KC_NORM, KC_OTHER = 0, 1, 2, 3
-KC_NAMES = ("gemm", "attention", "norm", "other")
+KC_GEMM, KC_ATTN, KC_NORM, KC_OTHER, KC_GEMM_ROW, KC_ATTN_ROW = 0, 1, 2, 3, 4, 5
+KC_NAMES = ("gemm", "attention", "norm", "other", "gemm_row", "attention_row")
+KC_COUNT = len(KC_NAMES)
 
 
 class Stats(C.Structure):
-    _fields_ = [("launches", C.c_int64 * 4), ("flops", C.c_double * 4), ("bytes", C.c_double * 4),
-                ("timed", C.c_int64 * 4), ("ms", C.c_double * 4)]
+    _fields_ = [("launches", C.c_int64 * KC_COUNT), ("flops", C.c_double * KC_COUNT),
+                ("bytes", C.c_double * KC_COUNT), ("timed", C.c_int64 * KC_COUNT), ("ms", C.c_double * KC_COUNT)]
 
 
 class LayerWeights(C.Structure):

@@ -265,6 +265,10 @@ cudaError_t counted(prefill_ctx* c, int kc, int n, double flops, double bytes, F
   return e;
 }
 
+// launch class of a projection: at most 16 rows stream the weights once and
+// are bound by them, more rows are bound by the tensor cores
+int gemm_class(int M) { return M <= 16 ? PF_KC_GEMM_ROW : PF_KC_GEMM; }
+
 double gemm_wbytes(const prefill_ctx* c, double n, double k) {
   return c->d.wtype == PF_W_Q4_0 ? n * k * 18.0 / 32.0 : n * k * 4.0;
 }
@@ -553,7 +557,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.k_cache = c->cache + static_cast<size_t>(il) * seg;
       e.v_cache = c->cache + static_cast<size_t>(c->L_w + il) * seg;
       const double n_out = c->q + 2.0 * e.kv_dim;
-      PF_CUDA(c, counted(c, PF_KC_GEMM, 1, 2.0 * M * n_out * D, M * D * 2.0 + gemm_wbytes(c, n_out, D) + M * n_out * 2.0,
+      PF_CUDA(c, counted(c, gemm_class(M), 1, 2.0 * M * n_out * D, M * D * 2.0 + gemm_wbytes(c, n_out, D) + M * n_out * 2.0,
                          [&] { return launch_gemm(c->a_y, M, W.qkv, e, c->err, s); }));
     }
     {
@@ -573,7 +577,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       const double pairs = static_cast<double>(M) * pos_base + 0.5 * M * (M + 1.0);
       const double aflops = pairs * c->Hq * 4.0 * c->hd;
       if (gathered)
-        PF_CUDA(c, counted(c, PF_KC_ATTN, attn_launch_count(a), aflops, kv_len * c->kv * 4.0 + M * c->q * 4.0,
+        PF_CUDA(c, counted(c, PF_KC_ATTN_ROW, attn_launch_count(a), aflops, kv_len * c->kv * 4.0 + M * c->q * 4.0,
                            [&] { return launch_attn_split(a, c->partials, s); }));
       else
         PF_CUDA(c, counted(c, PF_KC_ATTN, attn_launch_count(a), aflops, kv_len * c->kv * 4.0 + M * c->q * 4.0,
@@ -585,7 +589,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.N = D;
       e.out_f32 = xcur;
       e.ld_f32 = D;
-      PF_CUDA(c, counted(c, PF_KC_GEMM, 1, 2.0 * M * D * c->q, M * c->q * 2.0 + gemm_wbytes(c, D, c->q) + M * D * 8.0,
+      PF_CUDA(c, counted(c, gemm_class(M), 1, 2.0 * M * D * c->q, M * c->q * 2.0 + gemm_wbytes(c, D, c->q) + M * D * 8.0,
                          [&] { return launch_gemm(c->a_att, M, pick(W.o, W.o1, M), e, c->err, s); }));
     }
     PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, M * D * 6.0, [&] {
@@ -598,7 +602,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.out_bf16 = c->h;
       e.ld_bf16 = c->F;
       e.act = c->d.ffn_kind == PF_FFN_GEGLU ? 0 : 1;
-      PF_CUDA(c, counted(c, PF_KC_GEMM, 1, 4.0 * M * c->F * D, M * D * 2.0 + gemm_wbytes(c, 2.0 * c->F, D) + M * c->F * 2.0,
+      PF_CUDA(c, counted(c, gemm_class(M), 1, 4.0 * M * c->F * D, M * D * 2.0 + gemm_wbytes(c, 2.0 * c->F, D) + M * c->F * 2.0,
                          [&] { return launch_gemm(c->a_y, M, pick(W.gu, W.gu1, M), e, c->err, s); }));
     }
     {
@@ -611,7 +615,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
         e.out_bf16 = c->xb;
         e.ld_bf16 = D;
       }
-      PF_CUDA(c, counted(c, PF_KC_GEMM, 1, 2.0 * M * D * c->F, M * c->F * 2.0 + gemm_wbytes(c, D, c->F) + M * D * 8.0,
+      PF_CUDA(c, counted(c, gemm_class(M), 1, 2.0 * M * D * c->F, M * c->F * 2.0 + gemm_wbytes(c, D, c->F) + M * D * 8.0,
                          [&] { return launch_gemm(c->a_h, M, pick(W.down, W.down1, M), e, c->err, s); }));
     }
     if (c->P > 0) {
@@ -622,14 +626,14 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.ld_bf16 = c->P;
       e.ple = ple_view + static_cast<size_t>(il) * c->P;
       e.ple_stride = LP;
-      PF_CUDA(c, counted(c, PF_KC_GEMM, 1, 2.0 * M * c->P * D, M * D * 2.0 + gemm_wbytes(c, c->P, D) + M * c->P * 4.0,
+      PF_CUDA(c, counted(c, gemm_class(M), 1, 2.0 * M * c->P * D, M * D * 2.0 + gemm_wbytes(c, c->P, D) + M * c->P * 4.0,
                          [&] { return launch_gemm(c->a_xb, M, W.pg, e, c->err, s); }));
       EpiParams r;
       r.kind = EPI_RESID;
       r.N = D;
       r.out_f32 = xcur;
       r.ld_f32 = D;
-      PF_CUDA(c, counted(c, PF_KC_GEMM, 1, 2.0 * M * D * c->P, M * c->P * 2.0 + gemm_wbytes(c, D, c->P) + M * D * 8.0,
+      PF_CUDA(c, counted(c, gemm_class(M), 1, 2.0 * M * D * c->P, M * c->P * 2.0 + gemm_wbytes(c, D, c->P) + M * D * 8.0,
                          [&] { return launch_gemm(c->a_pg, M, pick(W.pp, W.pp1, M), r, c->err, s); }));
     }
   }
@@ -643,7 +647,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
     e.N = c->V;
     e.out_f32 = logits;
     e.ld_f32 = c->V;
-    PF_CUDA(c, counted(c, PF_KC_GEMM, 1, 2.0 * c->V * D, D * 2.0 + gemm_wbytes(c, c->V, D) + c->V * 4.0,
+    PF_CUDA(c, counted(c, gemm_class(1), 1, 2.0 * c->V * D, D * 2.0 + gemm_wbytes(c, c->V, D) + c->V * 4.0,
                        [&] { return launch_gemm(c->a_y, 1, c->head, e, c->err, s); }));
   }
   c->n_pos = kv_len;

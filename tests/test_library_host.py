@@ -94,3 +94,18 @@ def test_kv_header_check(lib):
     assert binding.kv_header_check(_hdr(500, 22, 256), 22, 256, 500, 499, size) == binding.PF_E_KV_RANGE
     assert binding.kv_header_check(_hdr(500, 22, 256), 22, 256, 500, 2048, size - 1) == binding.PF_E_KV_RANGE
     assert binding.kv_header_check(b"KV", 22, 256, 0, 2048, 2) == binding.PF_E_KV_MAGIC
+
+
+def test_stats_struct_matches_binding(tmp_path):
+    """The ctypes mirror of prefill_stats has the header's class count and size."""
+    import ctypes
+    src = tmp_path / "s.c"
+    src.write_text('#include <stdio.h>\n#include "prefill.h"\n'
+                   'int main(void){printf("%d %d\\n", (int)PF_KC_COUNT, (int)sizeof(prefill_stats));return 0;}\n')
+    exe = tmp_path / "s"
+    r = subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    n, size = map(int, subprocess.run([str(exe)], capture_output=True, text=True).stdout.split())
+    assert n == binding.KC_COUNT == len(binding.KC_NAMES)
+    assert size == ctypes.sizeof(binding.Stats)
