@@ -57,8 +57,13 @@ int pfop_linear_qkv(int32_t wtype, const void* wq_host, const void* wk_host, con
    Keys are folded in 64-key chunks, the chunks in groups of
    ceil(ceil(kv_len/64)/4); one CTA per (64-row block, group), then an
    ordered merge of the group states of rows whose keys span several groups.
-   mode 0: any M; mode 1: one row (M == 1), the KV-shared-layer form (the
-   same kernels; a row's result is the same in both modes). */
+   mode 0: any M.  mode 1: one row (M == 1) at position pos_base, the form
+   the KV-shared layers use for the output row (G4 section 1: after the
+   pruning those layers carry that row only): the keys [0, pos_base] are cut
+   into 64-key tiles and the tiles into ranges over about 148 CTAs, each CTA
+   streams its range once (online softmax, fp32 accumulation), and a merge
+   kernel combines the range states in a fixed order.  Its bits depend on
+   pos_base only, not on the launch; they differ from mode 0's in rounding. */
 int pfop_attention(int32_t mode, const void* q_dev, const void* k_dev, const void* v_dev, int32_t M, int32_t Hq,
                    int32_t Hkv, int32_t hd, int32_t pos_base, int32_t kv_len, void* out_dev, void* stream);
 
@@ -116,9 +121,10 @@ int pfop_kv_copy_bench(int32_t dir, void* cache_dev, int64_t cache_seg_halves, v
    The page set this library follows has no counterpart for this call.
    q fp16 [Hq*hd] at position pos; K/V fp16 [positions][Hkv*hd] with keys
    [0, kv_len) valid, pos < kv_len; out bf16 [Hq*hd].
-   Scratch: one fixed device array of 2^21 floats (8 MiB) per GPU that loads
-   the library, kept until exit.  A call needs Hq*4*(hd+4) floats when the
-   row's keys span more than one chunk group (see pfop_attention), else none;
+   Scratch: one fixed device array of 2^19 floats (2 MiB) per GPU that loads
+   the library, kept until exit.  A call needs Hq*R*(hd+4) floats, R being
+   the number of key ranges of pfop_attention's mode 1 (at most 148/Hkv), plus
+   4 for an error word: up to 8 query heads of 256 fit at any length;
    larger requests return PF_E_ARG without touching the GPU.  All calls share
    the array, so calls that overlap on the GPU race: order them on one stream
    or with events.  The first call on a device looks up the array's device

@@ -558,9 +558,397 @@ cudaError_t launch_attn_prefill(const AttnArgs& a, float* partials, cudaStream_t
   return launch_tc_t<64>(a, partials, s);
 }
 
+
+// ---------------------------------------------------------------------------
+// single-row attention: the output row of the KV-shared layers
+//
+// One query row at position pos reads keys [0, pos] of one layer's cache
+// once, so its cost is the K/V bytes (G4 section 1: after the pruning the
+// KV-shared layers carry only the output row).  The keys are cut into 64-key
+// tiles and the tiles of each KV head into `splits` consecutive ranges, sized
+// so that about ATTN_ROW_CTAS CTAs stream the cache together.  A CTA (range,
+// KV head) copies its K and V tiles through a TMA ring, forms the scores of
+// the KV head's G query heads and P V with mma.sync (m16n8k16: rows are the
+// G query heads, zero rows above G; fp32 accumulation), runs the online
+// softmax over its tiles and writes its state (o unnormalised, m, l) per
+// query head.  attn_row_merge_kernel combines a head's ranges in a fixed
+// reduction tree.  The range cut depends only on pos, so the row gets the
+// same bits from every pass that computes it.
+
+constexpr int ATTN_ROW_THREADS = 256;
+constexpr int ATTN_ROW_CTAS = 148;        // CTAs the ranges of all KV heads aim at
+constexpr int ATTN_ROW_MAX_SPLITS = 256;  // merge: one thread per range
+
+template <int HD>
+struct AttnRowCfg {
+  static constexpr int KV_BYTES = CHUNK * HD * 2;  // one 64-key K or V tile: [64-dim box][key][128 B]
+  static constexpr int STAGE = 2 * KV_BYTES;
+  static constexpr int NST = HD >= 256 ? 3 : 4;    // ring stages
+  static constexpr int S_LD = CHUNK + 4;           // score row stride, floats
+  static constexpr int P_LD = CHUNK + 8;           // P row stride, halves (conflict-free fragment loads)
+  static constexpr int OFF_S = NST * STAGE;
+  static constexpr int OFF_P = OFF_S + 16 * S_LD * 4;
+  static constexpr int OFF_H = OFF_P + 16 * P_LD * 2;  // per head: m, l, alpha
+  static constexpr int OFF_BAR = OFF_H + 3 * 16 * 4;
+  static constexpr int SMEM = OFF_BAR + NST * 8 + 1024;
+  static_assert(STAGE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static_assert(SMEM <= 232448, "shared memory");
+};
+
+struct AttnRowShape {
+  int Hq, Hkv, pos, n_tiles, tps, splits;
+};
+
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                              uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x2_trans(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
+// byte offset of (key r, dims d .. d+7) in a swizzled [64-dim box][64 keys][128 B] tile
+__device__ __forceinline__ uint32_t tile_off(int r, int d) {
+  return static_cast<uint32_t>((d >> 6) * (CHUNK * 128) + r * 128 + ((((d & 63) >> 3) ^ (r & 7)) << 4));
+}
+
+// bounded wait for a copy still in flight (error path: its shared memory
+// must not be released while the copy writes it)
+__device__ __forceinline__ void row_drain(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const long long t0 = clock64();
+  while (!mbar_try_wait(a, parity)) {
+    if (clock64() - t0 > 400000000ll) return;  // about 0.2 s
+  }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(ATTN_ROW_THREADS, 1)
+    attn_row_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const __half* __restrict__ q, const AttnRowShape sh, float* __restrict__ part, int* err) {
+  using C = AttnRowCfg<HD>;
+  constexpr float cexp = attn_c<HD>();
+  constexpr int KS = HD / 16;  // 16-dim steps of Q K^T
+  constexpr int NG = HD / 64;  // 8-dim column groups of P V per warp (the 8 warps split the dims)
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* sS = reinterpret_cast<float*>(smem + C::OFF_S);
+  __half* sP = reinterpret_cast<__half*>(smem + C::OFF_P);
+  float* sM = reinterpret_cast<float*>(smem + C::OFF_H);
+  float* sL = sM + 16;
+  float* sA = sL + 16;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int split = blockIdx.x, kvh = blockIdx.y;
+  const int G = sh.Hq / sh.Hkv;
+  const int tile0 = split * sh.tps;
+  const int nt = min(sh.n_tiles, tile0 + sh.tps) - tile0;
+
+  pdl_launch();
+  if (tid == 0) {
+    for (int i = 0; i < C::NST; ++i) mbar_init(&full[i], 1);
+    fence_mbar_init();
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  if (tid < 16) {
+    sM[tid] = -INFINITY;
+    sL[tid] = 0.f;
+    sA[tid] = 1.f;
+  }
+  for (int i = tid; i < 16 * C::P_LD / 2; i += ATTN_ROW_THREADS) reinterpret_cast<uint32_t*>(sP)[i] = 0u;
+  __syncthreads();
+  pdl_wait();
+  if (tid == 0) {
+    for (int i = 0; i < nt && i < C::NST; ++i) {
+      mbar_arrive_expect_tx(&full[i], C::STAGE);
+      tma_load_3d(smem + i * C::STAGE, &tmK, &full[i], kvh * HD, (tile0 + i) * CHUNK, 0);
+      tma_load_3d(smem + i * C::STAGE + C::KV_BYTES, &tmV, &full[i], kvh * HD, (tile0 + i) * CHUNK, 0);
+    }
+  }
+  // Q fragments (A of Q K^T): row g is query head kvh*G + g, row g + 8 head
+  // kvh*G + g + 8; rows past G are zero
+  uint32_t qa[KS][4];
+  {
+    const __half* q0 = q + (size_t)(kvh * G + g) * HD;
+    const __half* q1 = q + (size_t)(kvh * G + g + 8) * HD;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int d = ks * 16 + 2 * t4;
+      qa[ks][0] = g < G ? *reinterpret_cast<const uint32_t*>(q0 + d) : 0u;
+      qa[ks][1] = g + 8 < G ? *reinterpret_cast<const uint32_t*>(q1 + d) : 0u;
+      qa[ks][2] = g < G ? *reinterpret_cast<const uint32_t*>(q0 + d + 8) : 0u;
+      qa[ks][3] = g + 8 < G ? *reinterpret_cast<const uint32_t*>(q1 + d + 8) : 0u;
+    }
+  }
+  float o[NG][4];
+#pragma unroll
+  for (int n = 0; n < NG; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  const int dw = warp * (HD / 8);  // the warp's first P V column
+  int i = 0;
+  bool ok = true;
+  for (; i < nt; ++i) {
+    const int st = i % C::NST;
+    ok = mbar_wait(&full[st], (i / C::NST) & 1, err, PF_DEV_TIMEOUT_MMA);
+    ok = __syncthreads_and(ok);
+    if (!ok) break;
+    const uint8_t* kt = smem + st * C::STAGE;
+    const uint32_t vt = smem_u32(kt + C::KV_BYTES);
+    const int key0 = (tile0 + i) * CHUNK;
+    {
+      // scores of the warp's 8 keys (tile rows 8 warp .. +7)
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      const int r = warp * 8 + g;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int d = ks * 16 + 2 * t4;
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kt + tile_off(r, d) + (d & 7) * 2);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kt + tile_off(r, d + 8) + (d & 7) * 2);
+        mma_16816(c, qa[ks], b0, b1);
+      }
+      const int kc = warp * 8 + 2 * t4;  // tile column of c[0] / c[2]
+      const bool v0 = key0 + kc <= sh.pos, v1 = key0 + kc + 1 <= sh.pos;
+      *reinterpret_cast<float2*>(sS + g * C::S_LD + kc) = make_float2(v0 ? c[0] : -INFINITY, v1 ? c[1] : -INFINITY);
+      *reinterpret_cast<float2*>(sS + (g + 8) * C::S_LD + kc) =
+          make_float2(v0 ? c[2] : -INFINITY, v1 ? c[3] : -INFINITY);
+    }
+    __syncthreads();
+    // online softmax: warp w takes query heads w and w + 8 of the KV head
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int h = warp + 8 * hh;
+      if (h >= G) continue;
+      const float s0 = sS[h * C::S_LD + lane], s1 = sS[h * C::S_LD + lane + 32];
+      float mt = fmaxf(s0, s1);
+#pragma unroll
+      for (int x = 16; x > 0; x >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, x));
+      const float m_old = sM[h];
+      const float m_new = fmaxf(m_old, mt);
+      float p0 = 0.f, p1 = 0.f, alpha = 1.f;
+      if (m_new != -INFINITY) {
+        p0 = ex2_approx(__fmul_rn(__fsub_rn(s0, m_new), cexp));
+        p1 = ex2_approx(__fmul_rn(__fsub_rn(s1, m_new), cexp));
+        alpha = m_old == -INFINITY ? 0.f : ex2_approx(__fmul_rn(__fsub_rn(m_old, m_new), cexp));
+      }
+      const __half h0 = __float2half_rn(p0), h1 = __float2half_rn(p1);
+      float ps = __fadd_rn(__half2float(h0), __half2float(h1));  // the row sum adds the rounded values
+#pragma unroll
+      for (int x = 16; x > 0; x >>= 1) ps = __fadd_rn(ps, __shfl_xor_sync(0xffffffffu, ps, x));
+      sP[h * C::P_LD + lane] = h0;
+      sP[h * C::P_LD + lane + 32] = h1;
+      __syncwarp();
+      if (lane == 0) {
+        sL[h] = __fadd_rn(__fmul_rn(sL[h], alpha), ps);
+        sM[h] = m_new;
+        sA[h] = alpha;
+      }
+    }
+    __syncthreads();
+    {
+      // O = O * alpha + P V over the warp's columns
+      const float a0 = sA[g], a1 = sA[g + 8];
+#pragma unroll
+      for (int n = 0; n < NG; ++n) {
+        o[n][0] = __fmul_rn(o[n][0], a0);
+        o[n][1] = __fmul_rn(o[n][1], a0);
+        o[n][2] = __fmul_rn(o[n][2], a1);
+        o[n][3] = __fmul_rn(o[n][3], a1);
+      }
+#pragma unroll
+      for (int kk = 0; kk < CHUNK / 16; ++kk) {
+        uint32_t pa[4];
+        pa[0] = *reinterpret_cast<const uint32_t*>(sP + g * C::P_LD + kk * 16 + 2 * t4);
+        pa[1] = *reinterpret_cast<const uint32_t*>(sP + (g + 8) * C::P_LD + kk * 16 + 2 * t4);
+        pa[2] = *reinterpret_cast<const uint32_t*>(sP + g * C::P_LD + kk * 16 + 8 + 2 * t4);
+        pa[3] = *reinterpret_cast<const uint32_t*>(sP + (g + 8) * C::P_LD + kk * 16 + 8 + 2 * t4);
+        if constexpr (NG >= 2) {
+#pragma unroll
+          for (int n = 0; n < NG; n += 2) {
+            // matrices: (keys 0-7, cols d0), (keys 8-15, d0), (keys 0-7, d0+8), (keys 8-15, d0+8)
+            const int r = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int d = dw + 8 * n + (lane >> 4) * 8;
+            uint32_t v0, v1, v2, v3;
+            ldsm_x4_trans(vt + tile_off(r, d), v0, v1, v2, v3);
+            mma_16816(o[n], pa, v0, v1);
+            mma_16816(o[n + 1], pa, v2, v3);
+          }
+        } else {
+          const int r = kk * 16 + (lane & 15);
+          uint32_t v0, v1;
+          ldsm_x2_trans(vt + tile_off(r, dw), v0, v1);
+          mma_16816(o[0], pa, v0, v1);
+        }
+      }
+    }
+    __syncthreads();  // the stage, the scores and P are free
+    if (tid == 0 && i + C::NST < nt) {
+      mbar_arrive_expect_tx(&full[st], C::STAGE);
+      tma_load_3d(smem + st * C::STAGE, &tmK, &full[st], kvh * HD, (tile0 + i + C::NST) * CHUNK, 0);
+      tma_load_3d(smem + st * C::STAGE + C::KV_BYTES, &tmV, &full[st], kvh * HD, (tile0 + i + C::NST) * CHUNK, 0);
+    }
+  }
+  if (!ok) {
+    // copies issued for tiles i .. min(nt, i + NST) - 1 may still be landing
+    if (tid == 0)
+      for (int j = i; j < nt && j < i + C::NST; ++j) row_drain(&full[j % C::NST], (j / C::NST) & 1);
+    __syncthreads();
+    return;
+  }
+  // the range's state per query head: o (unnormalised), then m, l at HD
+  constexpr int STR = HD + 4;
+#pragma unroll
+  for (int n = 0; n < NG; ++n) {
+    const int d = dw + 8 * n + 2 * t4;
+    if (g < G)
+      *reinterpret_cast<float2*>(part + ((size_t)(kvh * G + g) * sh.splits + split) * STR + d) =
+          make_float2(o[n][0], o[n][1]);
+    if (g + 8 < G)
+      *reinterpret_cast<float2*>(part + ((size_t)(kvh * G + g + 8) * sh.splits + split) * STR + d) =
+          make_float2(o[n][2], o[n][3]);
+  }
+  if (tid < G)
+    *reinterpret_cast<float2*>(part + ((size_t)(kvh * G + tid) * sh.splits + split) * STR + HD) =
+        make_float2(sM[tid], sL[tid]);
+}
+
+// Combines the ranges of one query head (blockIdx.x) for 64 output columns
+// (blockIdx.y): thread s holds range s; m = max m_s, w_s = 2^((m_s - m) c),
+// out = sum w_s o_s / sum w_s l_s.  The sums run in a fixed tree (butterfly
+// within each warp, then the warps in order), so the bits do not depend on
+// timing.
+template <int HD>
+__global__ void __launch_bounds__(ATTN_ROW_THREADS) attn_row_merge_kernel(const float* __restrict__ part, int splits,
+                                                                          __nv_bfloat16* __restrict__ out) {
+  constexpr float c = attn_c<HD>();
+  constexpr int STR = HD + 4;
+  __shared__ float red[ATTN_ROW_THREADS / 32][68];
+  __shared__ float wmax[ATTN_ROW_THREADS / 32];
+  pdl_launch();
+  pdl_wait();
+  const int h = blockIdx.x, col0 = blockIdx.y * 64;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float m = -INFINITY, l = 0.f;
+  float v[65];
+  if (tid < splits) {
+    const float* p = part + ((size_t)h * splits + tid) * STR;
+    const float2 ml = *reinterpret_cast<const float2*>(p + HD);
+    m = ml.x;
+    l = ml.y;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float4 x = *reinterpret_cast<const float4*>(p + col0 + 4 * j);
+      v[4 * j] = x.x;
+      v[4 * j + 1] = x.y;
+      v[4 * j + 2] = x.z;
+      v[4 * j + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 64; ++j) v[j] = 0.f;
+  }
+  float mx = m;
+#pragma unroll
+  for (int x = 16; x > 0; x >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, x));
+  if (lane == 0) wmax[warp] = mx;
+  __syncthreads();
+  mx = wmax[0];
+#pragma unroll
+  for (int w = 1; w < ATTN_ROW_THREADS / 32; ++w) mx = fmaxf(mx, wmax[w]);
+  const float wgt = m == -INFINITY ? 0.f : ex2_approx(__fmul_rn(__fsub_rn(m, mx), c));
+#pragma unroll
+  for (int j = 0; j < 64; ++j) v[j] = __fmul_rn(v[j], wgt);
+  v[64] = __fmul_rn(l, wgt);
+#pragma unroll
+  for (int j = 0; j < 65; ++j) {
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) v[j] = __fadd_rn(v[j], __shfl_xor_sync(0xffffffffu, v[j], x));
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int j = 0; j < 65; ++j) red[warp][j] = v[j];
+  }
+  __syncthreads();
+  if (tid < 64) {
+    float o = red[0][tid], lt = red[0][64];
+#pragma unroll
+    for (int w = 1; w < ATTN_ROW_THREADS / 32; ++w) {
+      o = __fadd_rn(o, red[w][tid]);
+      lt = __fadd_rn(lt, red[w][64]);
+    }
+    out[(size_t)h * HD + col0 + tid] = __float2bfloat16_rn(__fmul_rn(o, __frcp_rn(lt)));
+  }
+}
+
+// tiles per range and ranges per KV head for a row at position pos
+static void attn_row_split(int pos, int Hkv, int* n_tiles, int* tps, int* splits) {
+  const int nt = pos / CHUNK + 1;
+  int per_head = ATTN_ROW_CTAS / (Hkv > 0 ? Hkv : 1);
+  if (per_head < 1) per_head = 1;
+  if (per_head > ATTN_ROW_MAX_SPLITS) per_head = ATTN_ROW_MAX_SPLITS;
+  const int t = (nt + per_head - 1) / per_head;
+  *n_tiles = nt;
+  *tps = t;
+  *splits = (nt + t - 1) / t;
+}
+
+size_t attn_split_partials_floats(int Hq, int Hkv, int hd, int pos) {
+  if (pos < 0 || Hkv < 1) return 0;
+  int nt = 0, tps = 0, splits = 0;
+  attn_row_split(pos, Hkv, &nt, &tps, &splits);
+  return static_cast<size_t>(Hq) * splits * (hd + 4);
+}
+
+template <int HD>
+static cudaError_t launch_row_t(const AttnArgs& a, float* part, cudaStream_t s) {
+  using C = AttnRowCfg<HD>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(attn_row_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  // K and V as [64-dim box][key][64 dims] (the box dimension last, stride
+  // 128 B): one copy brings a 64-key tile of one KV head as [box][key][128 B]
+  CUtensorMap tk, tv;
+  std::string err;
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(a.Hkv) * HD, static_cast<uint64_t>(a.kv_len),
+                              static_cast<uint64_t>(HD / 64)};
+    const uint64_t st[2] = {static_cast<uint64_t>(a.Hkv) * HD * 2, 128};
+    const uint32_t box[3] = {64, CHUNK, static_cast<uint32_t>(HD / 64)};
+    if (!encode_fp16_sw128(&tk, a.k, 3, dims, st, box, &err)) return cudaErrorInvalidValue;
+    if (!encode_fp16_sw128(&tv, a.v, 3, dims, st, box, &err)) return cudaErrorInvalidValue;
+  }
+  AttnRowShape sh;
+  sh.Hq = a.Hq;
+  sh.Hkv = a.Hkv;
+  sh.pos = a.pos_base;
+  attn_row_split(a.pos_base, a.Hkv, &sh.n_tiles, &sh.tps, &sh.splits);
+  cudaError_t e = launch_k(attn_row_kernel<HD>, dim3(sh.splits, a.Hkv), dim3(ATTN_ROW_THREADS), C::SMEM, s, 1, tk, tv,
+                           a.q, sh, part, a.err);
+  if (e != cudaSuccess) return e;
+  return launch_k(attn_row_merge_kernel<HD>, dim3(a.Hq, HD / 64), dim3(ATTN_ROW_THREADS), 0, s, 1,
+                  static_cast<const float*>(part), sh.splits, a.out);
+}
+
 cudaError_t launch_attn_split(const AttnArgs& a, float* partials, cudaStream_t s) {
-  if (a.M != 1) return cudaErrorInvalidValue;
-  return launch_attn_prefill(a, partials, s);
+  if (a.M != 1 || !partials) return cudaErrorInvalidValue;
+  if (!attn_shape_ok(a)) return cudaErrorInvalidValue;
+  if (a.hd == 256) return launch_row_t<256>(a, partials, s);
+  return launch_row_t<64>(a, partials, s);
 }
 
 int attn_launch_count(const AttnArgs& a) {

@@ -114,11 +114,15 @@ struct AttnArgs {
 
 // Causal attention over (64-row block, chunk group) CTAs; rows whose keys span
 // several groups go through the partials buffer (attn_partials_floats) and an
-// ordered merge.  launch_attn_split is the M == 1 form (same kernels).
+// ordered merge.  launch_attn_split is the single-row form of the KV-shared
+// layers (M == 1, position pos_base, keys [0, pos_base]): key ranges spread
+// over many CTAs, range states in `partials` (attn_split_partials_floats),
+// then a merge kernel; two launches.
 cudaError_t launch_attn_prefill(const AttnArgs& a, float* partials, cudaStream_t s);
 cudaError_t launch_attn_split(const AttnArgs& a, float* partials, cudaStream_t s);
 // floats of partials a launch of M rows over kv_len keys needs (0: none)
 size_t attn_partials_floats(int M, int Hq, int hd, int kv_len);
+size_t attn_split_partials_floats(int Hq, int Hkv, int hd, int pos);
 int attn_group_chunks(int kv_len);
 int attn_launch_count(const AttnArgs& a);  // kernels launch_attn_prefill starts (1 or 2)
 

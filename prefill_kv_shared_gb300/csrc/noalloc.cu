@@ -6,15 +6,16 @@
 // that memory use stays fixed and no call can fail with out-of-memory half
 // way through a request, and embedders whose own allocator owns the device.
 // For them this file keeps the scratch the split-K attention needs (the
-// per-chunk partials) in one fixed, file-scope device array instead of
+// per-range partial states) in one fixed, file-scope device array instead of
 // asking cudaMalloc for it.
 //
 // Limits and sharing:
-//   - the array holds PF_NOALLOC_SCRATCH_FLOATS floats (8 MiB); every GPU
+//   - the array holds PF_NOALLOC_SCRATCH_FLOATS floats (2 MiB); every GPU
 //     that loads this library keeps it until the process exits;
-//   - a request needs n_head * 4 * (head_dim + 4) floats when the row's keys
-//     span more than one chunk group, none otherwise, and is refused
-//     (PF_E_ARG) when that is more than the array holds;
+//   - a request needs n_head * R * (head_dim + 4) floats, R being the number
+//     of key ranges the row's keys are cut into (at most 148 / n_kv_head, so
+//     at most n_head * 148 * (head_dim + 4)), and is refused (PF_E_ARG) when
+//     that is more than the array holds;
 //   - every call, on every stream, uses the same array: calls whose work
 //     overlaps on the GPU race and give wrong results, so callers must order
 //     them (one stream, or events);
@@ -31,7 +32,7 @@
 
 namespace {
 
-constexpr size_t PF_NOALLOC_SCRATCH_FLOATS = size_t(1) << 21;
+constexpr size_t PF_NOALLOC_SCRATCH_FLOATS = size_t(1) << 19;
 
 // The scratch itself.  In host code this name is only a stand-in for the
 // device object; host code must use the address from cudaGetSymbolAddress.
@@ -71,7 +72,7 @@ extern "C" int pfop_attention_split_noalloc(const void* q_dev, const void* k_dev
                                             void* stream) {
   if (!q_dev || !k_dev || !v_dev || !out_dev || pos < 0 || pos >= kv_len || Hq < 1 || Hkv < 1)
     return fail(PF_E_ARG, "bad argument");
-  const size_t need = pf::attn_partials_floats(1, Hq, hd, kv_len);
+  const size_t need = pf::attn_split_partials_floats(Hq, Hkv, hd, pos);
   if (need > PF_NOALLOC_SCRATCH_FLOATS - 4)
     return fail(PF_E_ARG, "request needs " + std::to_string(need) + " scratch floats; the fixed array holds " +
                               std::to_string(PF_NOALLOC_SCRATCH_FLOATS));

@@ -298,7 +298,8 @@ extern "C" int pfop_attention(int32_t mode, const void* q_dev, const void* k_dev
   Scope sc;
   float* part = nullptr;
   int* err = nullptr;
-  OP_CUDA(sc.alloc(&part, attn_partials_floats(M, Hq, hd, kv_len) * 4));
+  OP_CUDA(sc.alloc(&part, (mode == 1 ? attn_split_partials_floats(Hq, Hkv, hd, pos_base)
+                                     : attn_partials_floats(M, Hq, hd, kv_len)) * 4));
   OP_CUDA(sc.alloc(&err, 16));
   OP_CUDA(cudaMemsetAsync(err, 0, 16, s));
   a.err = err;
@@ -440,7 +441,8 @@ extern "C" int pfop_attention_bench(int32_t mode, const void* q_dev, const void*
   Scope sc;
   float* part = nullptr;
   int* err = nullptr;
-  OP_CUDA(sc.alloc(&part, attn_partials_floats(M, Hq, hd, kv_len) * 4));
+  OP_CUDA(sc.alloc(&part, (mode == 1 ? attn_split_partials_floats(Hq, Hkv, hd, pos_base)
+                                     : attn_partials_floats(M, Hq, hd, kv_len)) * 4));
   OP_CUDA(sc.alloc(&err, 16));
   OP_CUDA(cudaMemsetAsync(err, 0, 16, s));
   a.err = err;

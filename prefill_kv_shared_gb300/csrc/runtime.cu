@@ -69,6 +69,7 @@ struct prefill_ctx {
   __nv_bfloat16 *y = nullptr, *att = nullptr, *h = nullptr, *xb = nullptr, *pg = nullptr, *ple = nullptr;
   __half* q16 = nullptr;
   float* partials = nullptr;
+  float* row_partials = nullptr;  // range states of the single-row attention
   __half* cache = nullptr;  // [2][L_w][max_ctx][kv]
   float2* rope = nullptr;
   int* err = nullptr;
@@ -400,6 +401,9 @@ extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weig
   }
   if ((rc = dev_alloc(C, &C->partials, attn_partials_floats(R, C->Hq, C->hd, C->d.max_ctx) * 4)))
     return fail(nullptr, rc, C->last_error);
+  if ((rc = dev_alloc(C, &C->row_partials,
+                      attn_split_partials_floats(C->Hq, C->Hkv, C->hd, static_cast<int>(C->d.max_ctx) - 1) * 4)))
+    return fail(nullptr, rc, C->last_error);
   if ((rc = dev_alloc(C, &C->cache, static_cast<size_t>(2) * C->L_w * C->d.max_ctx * C->kv * 2)))
     return fail(nullptr, rc, C->last_error);
   {
@@ -573,15 +577,31 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       a.pos_base = pos_base;
       a.kv_len = kv_len;
       a.err = c->err;
-      // (query head, visible key) pairs: rows at positions pos_base .. pos_base+M-1
-      const double pairs = static_cast<double>(M) * pos_base + 0.5 * M * (M + 1.0);
-      const double aflops = pairs * c->Hq * 4.0 * c->hd;
-      if (gathered)
-        PF_CUDA(c, counted(c, PF_KC_ATTN_ROW, attn_launch_count(a), aflops, kv_len * c->kv * 4.0 + M * c->q * 4.0,
-                           [&] { return launch_attn_split(a, c->partials, s); }));
-      else
-        PF_CUDA(c, counted(c, PF_KC_ATTN, attn_launch_count(a), aflops, kv_len * c->kv * 4.0 + M * c->q * 4.0,
-                           [&] { return launch_attn_prefill(a, c->partials, s); }));
+      // The output row of a KV-shared layer in the final ubatch goes through
+      // the single-row kernels in both modes (alone after the pruning, after
+      // the other rows without it), so its bits do not depend on the mode.
+      const bool out_row = !writes && is_last;
+      const int m_rest = out_row ? M - 1 : M;  // rows for the prefill kernels
+      if (m_rest > 0) {
+        AttnArgs r = a;
+        r.M = m_rest;
+        // (query head, visible key) pairs: rows at positions pos_base .. pos_base+m_rest-1
+        const double pairs = static_cast<double>(m_rest) * pos_base + 0.5 * m_rest * (m_rest + 1.0);
+        PF_CUDA(c, counted(c, PF_KC_ATTN, attn_launch_count(r), pairs * c->Hq * 4.0 * c->hd,
+                           kv_len * c->kv * 4.0 + m_rest * c->q * 4.0,
+                           [&] { return launch_attn_prefill(r, c->partials, s); }));
+      }
+      if (out_row) {
+        AttnArgs r = a;
+        r.M = 1;
+        r.q = c->q16 + static_cast<size_t>(M - 1) * c->q;
+        r.out = c->att + static_cast<size_t>(M - 1) * c->q;
+        r.pos_base = pos_base + M - 1;
+        const int n_keys = r.pos_base + 1;
+        PF_CUDA(c, counted(c, PF_KC_ATTN_ROW, 2, static_cast<double>(n_keys) * c->Hq * 4.0 * c->hd,
+                           n_keys * c->kv * 4.0 + c->q * 4.0,
+                           [&] { return launch_attn_split(r, c->row_partials, s); }));
+      }
     }
     {
       EpiParams e;

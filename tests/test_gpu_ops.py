@@ -209,26 +209,46 @@ def test_attention_prefill(lib, M, Hq, Hkv, hd, pos_base, kv_len):
     assert np.abs(got - want).max() < 1e-2
 
 
-@pytest.mark.parametrize("Hq,Hkv,hd,kv_len", [(8, 1, 256, 512), (8, 1, 256, 8192), (8, 2, 256, 1000),
-                                               (4, 1, 64, 64), (32, 4, 64, 532), (8, 1, 256, 1)])
-def test_attention_split_matches_and_is_bit_identical(lib, Hq, Hkv, hd, kv_len):
-    """One row through the split-K path equals the oracle, and is bit-identical
-    to the same row computed among all rows by the in-CTA fold."""
-    rng = np.random.default_rng(kv_len + hd)
-    M = min(kv_len, 96)
-    pos_base = kv_len - M
-    q, k, v = _attn_inputs(rng, M, Hq, Hkv, hd, kv_len)
+@pytest.mark.parametrize("Hq,Hkv,hd,kv_len,pos", [
+    (8, 1, 256, 512, 511), (8, 1, 256, 8192, 8191), (8, 2, 256, 1000, 999), (4, 1, 64, 64, 63),
+    (32, 4, 64, 532, 531), (8, 1, 256, 1, 0), (8, 1, 256, 3000, 1234), (8, 2, 256, 32768, 32767),
+    (8, 1, 256, 20000, 9500), (16, 1, 64, 200, 130)])
+def test_attention_split_matches_oracle(lib, Hq, Hkv, hd, kv_len, pos):
+    """The single-row form (the output row of the KV-shared layers): keys
+    [0, pos] of a cache holding kv_len positions, against the oracle, and the
+    same bits on a second call."""
+    rng = np.random.default_rng(kv_len + hd + pos)
+    q, k, v = _attn_inputs(rng, 1, Hq, Hkv, hd, kv_len)
     tq, tk, tv = (torch.from_numpy(t).cuda() for t in (q, k, v))
-    full = torch.empty((M, Hq * hd), dtype=torch.bfloat16, device="cuda")
-    binding.check_op(lib.pfop_attention(0, tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), M, Hq, Hkv, hd, pos_base,
-                                        kv_len, full.data_ptr(), None))
-    one = torch.empty((1, Hq * hd), dtype=torch.bfloat16, device="cuda")
-    q_last = tq[M - 1:M].contiguous()
-    binding.check_op(lib.pfop_attention(1, q_last.data_ptr(), tk.data_ptr(), tv.data_ptr(), 1, Hq, Hkv, hd,
-                                        kv_len - 1, kv_len, one.data_ptr(), None))
-    want = oracle.attention(q[M - 1:].astype(np.float32), k[:kv_len], v[:kv_len], np.array([kv_len - 1]))
-    assert np.abs(one.float().cpu().numpy().reshape(1, Hq, hd) - want).max() < 1e-2
-    assert torch.equal(one[0], full[M - 1])
+    outs = []
+    for _ in range(2):
+        one = torch.zeros((1, Hq * hd), dtype=torch.bfloat16, device="cuda")
+        binding.check_op(lib.pfop_attention(1, tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), 1, Hq, Hkv, hd, pos,
+                                            kv_len, one.data_ptr(), None))
+        outs.append(one)
+    want = oracle.attention(q.astype(np.float32), k[:kv_len], v[:kv_len], np.array([pos]))
+    got = outs[0].float().cpu().numpy().reshape(1, Hq, hd)
+    assert np.isfinite(got).all()
+    assert np.abs(got - want).max() < 1e-2
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_attention_split_ignores_keys_past_the_row(lib):
+    """Keys after the row's position change nothing, bit for bit."""
+    rng = np.random.default_rng(77)
+    Hq, Hkv, hd, kv_len, pos = 8, 1, 256, 4096, 2500
+    q, k, v = _attn_inputs(rng, 1, Hq, Hkv, hd, kv_len)
+    k2, v2 = k.copy(), v.copy()
+    k2[pos + 1:] = rng.normal(0, 3, k2[pos + 1:].shape).astype(np.float16)
+    v2[pos + 1:] = rng.normal(0, 3, v2[pos + 1:].shape).astype(np.float16)
+    res = []
+    for kk, vv in ((k, v), (k2, v2)):
+        tq, tk, tv = (torch.from_numpy(t).cuda() for t in (q, kk, vv))
+        one = torch.zeros((1, Hq * hd), dtype=torch.bfloat16, device="cuda")
+        binding.check_op(lib.pfop_attention(1, tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), 1, Hq, Hkv, hd, pos,
+                                            kv_len, one.data_ptr(), None))
+        res.append(one)
+    assert torch.equal(res[0], res[1])
 
 
 def test_rmsnorm_gather_and_copy(lib):

@@ -47,12 +47,14 @@ def test_noalloc_matches_allocating_entry_point_twice(lib, Hq, Hkv, hd):
 
 
 def test_noalloc_refuses_requests_beyond_the_array(lib):
-    q, k, v = _inputs(3, 8, 1, 256, 64)
-    out = torch.empty((1, 8 * 256), dtype=torch.bfloat16, device="cuda")
-    # keys spanning several chunk groups need Hq * 4 * (hd + 4) floats:
-    # 2048 heads * 4 * 260 is beyond 2^21 floats (refused before any launch,
-    # so the small buffers are never read)
-    rc = lib.pfop_attention_split_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), 2048, 128, 256, 1023, 1024,
+    # 16 query heads of 256 on one KV head, keys cut into 148 ranges: the
+    # range states need 16 * 148 * 260 floats, more than the 2^19 the array
+    # holds.  The buffers are full size for the request, so even a call that
+    # wrongly went ahead would stay inside them.
+    Hq, Hkv, hd, kv_len = 16, 1, 256, 148 * 64
+    q, k, v = _inputs(3, Hq, Hkv, hd, kv_len)
+    out = torch.empty((1, Hq * hd), dtype=torch.bfloat16, device="cuda")
+    rc = lib.pfop_attention_split_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), Hq, Hkv, hd, kv_len - 1, kv_len,
                                           out.data_ptr(), None)
     assert rc == binding.PF_E_ARG
     assert b"scratch" in lib.pfop_last_error()
