@@ -54,6 +54,7 @@ extern "C" {
 #define PF_E_DEVICE_TIMEOUT (-6) /* a kernel gave up a bounded wait; results are invalid */
 #define PF_E_DEVICE_TOKEN (-7)   /* a device-resident token id was out of range */
 #define PF_E_NOMEM (-8)          /* device allocation failed */
+#define PF_E_IO (-9)             /* a KV image file could not be opened, read or written */
 
 /* weight storage types */
 #define PF_W_F32 0  /* fp32 matrices (computed as bf16 on the GPU) */
@@ -159,6 +160,25 @@ int kv_save(prefill_ctx* ctx, void* dst, size_t dst_bytes);
    full prefill.  Whether the image was made from the same prompt prefix is
    the caller's contract (the image stores no tokens). */
 int kv_load(prefill_ctx* ctx, const void* src, size_t src_bytes, int64_t n_pos);
+
+/* ---- KV image files (PicoLM KV cache article, "usage" and "file") ----
+   A file holds exactly one KV image (the layout above).  kv_save_file
+   writes the cache's first prefill_n_pos() positions to `path` (created or
+   replaced; PF_E_IO when the file cannot be written).  kv_load_file checks
+   the file's header against this model and the file's size first
+   (PF_E_IO: cannot open or read; PF_E_KV_MAGIC / PF_E_KV_SHAPE /
+   PF_E_KV_RANGE: as kv_load) and only then restores its first n_pos
+   positions (n_pos < 0: all of them); any refusal leaves the cache and the
+   position count unchanged, so the caller falls back to a full prefill.
+   Both are synchronous and stage the image through host memory. */
+int kv_save_file(prefill_ctx* ctx, const char* path);
+int kv_load_file(prefill_ctx* ctx, const char* path, int64_t n_pos);
+
+/* Host-only check of a KV image file against a model (writing layers,
+   kv_dim) and a context length: PF_OK and *n_pos_out = the file's position
+   count, or the refusal kv_load_file would give.  No GPU needed. */
+int prefill_kv_file_check(const char* path, int32_t n_layers_written, int32_t kv_dim, int64_t max_ctx,
+                          int64_t* n_pos_out);
 
 /* ---- launch accounting and per-class kernel timing ----
    Every kernel the context launches is counted by class, with the

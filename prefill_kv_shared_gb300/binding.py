@@ -24,6 +24,7 @@ PF_E_CUDA = -5
 PF_E_DEVICE_TIMEOUT = -6
 PF_E_DEVICE_TOKEN = -7
 PF_E_NOMEM = -8
+PF_E_IO = -9
 
 PF_W_F32 = 0
 PF_W_Q4_0 = 2
@@ -39,6 +40,7 @@ EXPORTS = (
     "pfop_linear_f32", "pfop_linear_resid", "pfop_linear_glu", "pfop_linear_ple", "pfop_linear_qkv",
     "pfop_attention", "pfop_rmsnorm", "pfop_embed", "pfop_kv_copy", "pfop_last_error", "pfop_linear_bench",
     "pfop_attention_split_noalloc", "pfop_attention_bench", "pfop_kv_copy_bench",
+    "kv_save_file", "kv_load_file", "prefill_kv_file_check",
 )
 
 
@@ -106,6 +108,9 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "prefill_kv_image_bytes": (i64, [vp, i64]),
         "kv_save": (C.c_int, [vp, vp, sz]),
         "kv_load": (C.c_int, [vp, vp, sz, i64]),
+        "kv_save_file": (C.c_int, [vp, C.c_char_p]),
+        "kv_load_file": (C.c_int, [vp, C.c_char_p, i64]),
+        "prefill_kv_file_check": (C.c_int, [C.c_char_p, i32, i32, i64, C.POINTER(C.c_int64)]),
         "prefill_destroy": (None, [vp]),
         "prefill_last_error": (C.c_char_p, [vp]),
         "prefill_prune_predicate": (C.c_int, [C.POINTER(ModelDesc)]),
@@ -197,6 +202,35 @@ def kv_image_bytes_for(n_layers_written: int, n_pos: int, kv_dim: int) -> int:
     return int(load().prefill_kv_image_bytes_for(n_layers_written, n_pos, kv_dim))
 
 
+def kv_file_check(path: str, n_layers_written: int, kv_dim: int, max_ctx: int) -> tuple[int, int]:
+    """(status, positions) of a KV image file checked on the host only."""
+    n = C.c_int64(-1)
+    rc = load().prefill_kv_file_check(os.fsencode(path), n_layers_written, kv_dim, max_ctx, C.byref(n))
+    return rc, n.value
+
+
+def prefill_with_cache(ctx: "PrefillContext", tokens, ubatch: int, logits, path: str) -> int:
+    """The PicoLM flow for a fixed prompt prefix (KV cache article, "usage"):
+    if `path` holds a valid image of the prompt's first positions, restore it
+    and prefill only the rest; otherwise prefill everything and save the
+    cache to `path`.  Returns how many prompt positions came from the file.
+    Whether the file was made from the same prefix is the caller's contract
+    (the image stores no tokens)."""
+    n = len(tokens)
+    ctx.reset()
+    start = 0
+    if os.path.exists(path):
+        rc, n_file = kv_file_check(path, ctx.n_layers_written, ctx.kv_dim, ctx.max_ctx)
+        if rc == PF_OK and 0 < n_file < n and ctx.kv_load_file(path, n_file) == PF_OK:
+            start = n_file
+    for i in range(start, n, ubatch):
+        ctx.ubatch(tokens[i:i + ubatch], i, i + ubatch >= n, logits)
+    if start == 0:
+        ctx.sync()
+        ctx.kv_save_file(path)
+    return start
+
+
 def kv_header_check(header: bytes, n_layers_written: int, kv_dim: int, n_pos: int, max_ctx: int,
                     image_bytes: int) -> int:
     buf = (C.c_uint8 * 16).from_buffer_copy(header[:16].ljust(16, b"\0"))
@@ -238,6 +272,9 @@ class PrefillContext:
         self._h = h
         self._lib = lib
         self.vocab = cfg["vocab"]
+        self.max_ctx = max_ctx
+        self.n_layers_written = min(cfg["n_layer_kv_from_start"], cfg["n_layer"])
+        self.kv_dim = cfg["n_head_kv"] * cfg["head_dim"]
 
     def _check(self, rc):
         if rc != PF_OK:
@@ -279,6 +316,17 @@ class PrefillContext:
 
     def kv_load(self, src, nbytes: int, n_pos: int):
         self._check(self._lib.kv_load(self._h, _ptr(src), nbytes, n_pos))
+
+    def kv_save_file(self, path: str):
+        self._check(self._lib.kv_save_file(self._h, os.fsencode(path)))
+
+    def kv_load_file(self, path: str, n_pos: int = -1) -> int:
+        """Restore a KV image file; returns the status (0, or the refusal code,
+        in which case the cache is unchanged and a full prefill is due)."""
+        rc = self._lib.kv_load_file(self._h, os.fsencode(path), n_pos)
+        if rc not in (PF_OK, PF_E_KV_MAGIC, PF_E_KV_SHAPE, PF_E_KV_RANGE, PF_E_IO):
+            self._check(rc)
+        return rc
 
     def set_timing(self, enable: bool):
         self._check(self._lib.prefill_set_timing(self._h, 1 if enable else 0))

@@ -797,6 +797,99 @@ extern "C" int kv_load(prefill_ctx* c, const void* src, size_t src_bytes, int64_
   return PF_OK;
 }
 
+// ---------------------------------------------------------------------------
+// KV image files (PicoLM KV cache article, "usage", "file" and "rules"): one
+// image per file, written and read through host memory
+
+namespace {
+
+struct FileCloser {
+  std::FILE* f;
+  ~FileCloser() {
+    if (f) std::fclose(f);
+  }
+};
+
+// size of an open file, or -1
+int64_t file_size(std::FILE* f) {
+  if (std::fseek(f, 0, SEEK_END) != 0) return -1;
+  const long n = std::ftell(f);
+  if (n < 0 || std::fseek(f, 0, SEEK_SET) != 0) return -1;
+  return static_cast<int64_t>(n);
+}
+
+// header checks of kv_load_file; *n_img = the file's position count
+int check_file(std::FILE* f, int32_t n_layers_written, int32_t kv_dim, int64_t n_pos, int64_t max_ctx,
+               int64_t* n_img, int64_t* bytes) {
+  const int64_t size = file_size(f);
+  if (size < 0) return PF_E_IO;
+  uint8_t hdr[16] = {0};
+  if (size >= 16 && std::fread(hdr, 1, 16, f) != 16) return PF_E_IO;
+  int32_t n_file = 0;
+  std::memcpy(&n_file, hdr + 4, 4);
+  const int64_t want = n_pos < 0 ? n_file : n_pos;
+  const int rc = prefill_kv_header_check(hdr, n_layers_written, kv_dim, want, max_ctx, static_cast<size_t>(size));
+  if (rc != PF_OK) return rc;
+  *n_img = n_file;
+  *bytes = size;
+  return PF_OK;
+}
+
+}  // namespace
+
+extern "C" int prefill_kv_file_check(const char* path, int32_t n_layers_written, int32_t kv_dim, int64_t max_ctx,
+                                     int64_t* n_pos_out) {
+  if (!path) return PF_E_ARG;
+  FileCloser fc{std::fopen(path, "rb")};
+  if (!fc.f) return PF_E_IO;
+  int64_t n = 0, bytes = 0;
+  const int rc = check_file(fc.f, n_layers_written, kv_dim, -1, max_ctx, &n, &bytes);
+  if (rc == PF_OK && n_pos_out) *n_pos_out = n;
+  return rc;
+}
+
+extern "C" int kv_save_file(prefill_ctx* c, const char* path) {
+  if (!c || !path) return fail(c, PF_E_ARG, "null argument");
+  const int64_t bytes = prefill_kv_image_bytes(c, c->n_pos);
+  std::vector<uint8_t> img(static_cast<size_t>(bytes) + 16);
+  // 16-byte aligned staging inside the vector
+  uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(img.data()) + 15) & ~uintptr_t(15));
+  const int rc = kv_save(c, p, static_cast<size_t>(bytes));
+  if (rc != PF_OK) return rc;
+  FileCloser fc{std::fopen(path, "wb")};
+  if (!fc.f) return fail(c, PF_E_IO, std::string("cannot open ") + path + " for writing");
+  if (std::fwrite(p, 1, static_cast<size_t>(bytes), fc.f) != static_cast<size_t>(bytes))
+    return fail(c, PF_E_IO, std::string("short write to ") + path);
+  if (std::fclose(fc.f) != 0) {
+    fc.f = nullptr;
+    return fail(c, PF_E_IO, std::string("cannot close ") + path);
+  }
+  fc.f = nullptr;
+  return PF_OK;
+}
+
+extern "C" int kv_load_file(prefill_ctx* c, const char* path, int64_t n_pos) {
+  if (!c || !path) return fail(c, PF_E_ARG, "null argument");
+  FileCloser fc{std::fopen(path, "rb")};
+  if (!fc.f) return fail(c, PF_E_IO, std::string("cannot open ") + path);
+  int64_t n_img = 0, bytes = 0;
+  int rc = check_file(fc.f, c->L_w, c->kv, n_pos, c->d.max_ctx, &n_img, &bytes);
+  if (rc == PF_E_IO) return fail(c, rc, std::string("cannot read ") + path);
+  if (rc == PF_E_KV_MAGIC) return fail(c, rc, "not a KV image file (magic)");
+  if (rc == PF_E_KV_SHAPE) return fail(c, rc, "KV image file layers or kv_dim do not match the model");
+  if (rc != PF_OK) return fail(c, rc, "KV image file position count out of range");
+  const int64_t img_bytes = prefill_kv_image_bytes(c, n_img);
+  std::vector<uint8_t> img(static_cast<size_t>(img_bytes) + 16);
+  uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(img.data()) + 15) & ~uintptr_t(15));
+  if (std::fseek(fc.f, 0, SEEK_SET) != 0 ||
+      std::fread(p, 1, static_cast<size_t>(img_bytes), fc.f) != static_cast<size_t>(img_bytes))
+    return fail(c, PF_E_IO, std::string("cannot read ") + path);
+  rc = kv_load(c, p, static_cast<size_t>(img_bytes), n_pos < 0 ? n_img : n_pos);
+  if (rc != PF_OK) return rc;
+  PF_CUDA(c, cudaStreamSynchronize(c->stream));  // the staging buffer is released on return
+  return PF_OK;
+}
+
 extern "C" int prefill_prune_predicate(const prefill_model_desc* d) {
   if (!d) return PF_E_ARG;
   return predicate(*d, d->prune_shared_enable) ? 1 : 0;

@@ -5,6 +5,8 @@ same argmax (when the oracle's top two are further apart than twice that
 tolerance; otherwise the GPU's argmax must be one of the oracle's logits
 within the tolerance of the top), and the pruned pass bit-identical to the
 unpruned one."""
+import os
+
 import numpy as np
 import pytest
 
@@ -205,4 +207,57 @@ def test_errors_leave_state(gpu, tiny):
             ctx.kv_load(arr, len(arr), npos)
         assert e.value.code == code
         assert ctx.n_pos == 0
+    ctx.close()
+
+
+def test_kv_file_roundtrip_and_cached_prefill(gpu, tinyllama, tmp_path):
+    """A KV image written to a file restores the same cache as the in-memory
+    image (suffix logits bit for bit), and the cached-prefix flow (load when
+    the file is valid, else full prefill and save) gives the full prefill's
+    logits to rounding; a damaged file is refused with the state unchanged."""
+    cfg = tinyllama.cfg
+    prefix = synth.make_tokens(cfg, 500, seed=1)
+    suffix = synth.make_tokens(cfg, 32, seed=2)
+    logits = torch.empty(cfg["vocab"], dtype=torch.float32, device="cuda")
+    ctx = binding.PrefillContext(tinyllama, max_ctx=532, ubatch_max=512)
+    ctx.ubatch(prefix, 0, False)
+    path = str(tmp_path / "prefix.kvcp")
+    ctx.kv_save_file(path)
+    nbytes = ctx.kv_image_bytes(500)
+    assert os.path.getsize(path) == nbytes
+    img = np.empty(nbytes, dtype=np.uint8)
+    ctx.kv_save(img, nbytes)
+    assert open(path, "rb").read() == img.tobytes()
+    assert binding.kv_file_check(path, 22, 256, 532) == (binding.PF_OK, 500)
+    res = []
+    for how in ("memory", "file"):
+        ctx.reset()
+        if how == "memory":
+            ctx.kv_load(img, nbytes, 500)
+        else:
+            assert ctx.kv_load_file(path) == binding.PF_OK
+        assert ctx.n_pos == 500
+        ctx.ubatch(suffix, 500, True, logits)
+        ctx.sync()
+        res.append(logits.cpu().numpy().copy())
+    np.testing.assert_array_equal(res[0], res[1])
+    # a damaged file: refused, nothing changes
+    bad = str(tmp_path / "bad.kvcp")
+    with open(bad, "wb") as f:
+        f.write(b"KVCQ" + img[4:].tobytes())
+    ctx.reset()
+    assert ctx.kv_load_file(bad) == binding.PF_E_KV_MAGIC
+    assert ctx.n_pos == 0
+    assert ctx.kv_load_file(str(tmp_path / "missing.kvcp")) == binding.PF_E_IO
+    # the cached-prefix flow: first call prefills all and saves, second loads
+    prompt = np.concatenate([prefix, suffix])
+    cache = str(tmp_path / "flow.kvcp")
+    full = run_gpu(tinyllama, prompt, 512, True, max_ctx=532)
+    assert binding.prefill_with_cache(ctx, prompt[:500], 512, logits, cache) == 0
+    ctx.sync()
+    assert binding.kv_file_check(cache, 22, 256, 532)[1] == 500
+    assert binding.prefill_with_cache(ctx, prompt, 512, logits, cache) == 500
+    ctx.sync()
+    got = logits.cpu().numpy()
+    assert np.abs(got - full).max() <= 2e-3 * np.abs(full).max()
     ctx.close()

@@ -109,3 +109,30 @@ def test_stats_struct_matches_binding(tmp_path):
     n, size = map(int, subprocess.run([str(exe)], capture_output=True, text=True).stdout.split())
     assert n == binding.KC_COUNT == len(binding.KC_NAMES)
     assert size == ctypes.sizeof(binding.Stats)
+
+
+def test_kv_file_check_host_only(lib, tmp_path):
+    """The file form of the KV image header check (PicoLM KV cache article,
+    "file" and "rules"): a valid file gives its position count; a wrong
+    magic, a wrong shape, a short file, a count beyond the context and a
+    missing file are refused."""
+    import numpy as np
+    L_w, n, kv = 3, 40, 64
+    hdr = b"KVCP" + np.array([n, L_w, kv], dtype="<i4").tobytes()
+    body = bytes(2 * L_w * n * kv * 2)
+    cases = {
+        "ok": (hdr + body, binding.PF_OK),
+        "magic": (b"KVCQ" + hdr[4:] + body, binding.PF_E_KV_MAGIC),
+        "shape": (b"KVCP" + np.array([n, L_w + 1, kv], dtype="<i4").tobytes() + body, binding.PF_E_KV_SHAPE),
+        "short": (hdr + body[:-2], binding.PF_E_KV_RANGE),
+    }
+    for name, (blob, code) in cases.items():
+        p = tmp_path / (name + ".kvcp")
+        p.write_bytes(blob)
+        rc, npos = binding.kv_file_check(str(p), L_w, kv, 100)
+        assert rc == code, name
+        if code == binding.PF_OK:
+            assert npos == n
+    p = tmp_path / "ok.kvcp"
+    assert binding.kv_file_check(str(p), L_w, kv, 39)[0] == binding.PF_E_KV_RANGE  # beyond the context
+    assert binding.kv_file_check(str(tmp_path / "none.kvcp"), L_w, kv, 100)[0] == binding.PF_E_IO
