@@ -480,6 +480,35 @@ def run_ours(args, dist: Dist):
             big.close()
             del t, lg
         models.clear()
+        # generation after the prompt (llama-bench tg128): 128 one-token
+        # ubatches after a 512-token prefill, pruning on and off
+        dec = binding.PrefillContext(w, max_ctx=512 + 128, ubatch_max=UB, prune=True, stream=stream)
+        tg = torch.from_numpy(synth.make_tokens(cfg, 512 + 128)).to(dev)
+        for prune in (True, False):
+            dec.set_prune(prune)
+
+            def prefill_prompt():
+                dec.reset()
+                dec.ubatch(tg[:512], 0, True, logits)
+
+            def gen128():
+                for i in range(512, 512 + 128):
+                    dec.ubatch(tg[i:i + 1], i, True, logits)
+            prefill_prompt()
+            gen128()
+            dec.sync()
+            tot = 0.0
+            for _ in range(2):
+                prefill_prompt()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                gen128()
+                b.record(stream)
+                torch.cuda.synchronize(dev)
+                tot += a.elapsed_time(b)
+            gms = tot / 2
+            sweep[f"tg128_{'on' if prune else 'off'}"] = {"ms": gms, "tokens_per_s": 128 / (gms * 1e-3)}
+        dec.close()
 
     hbm = None
     if not args.no_hbm and dist.rank == 0:

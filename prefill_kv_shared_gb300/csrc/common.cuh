@@ -165,6 +165,41 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   }
 }
 
+// Non-suspending probe of a phase (test_wait never parks the thread, so a
+// spinning waiter sees the phase complete at once)
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// The bounded wait of mbar_wait as a pure spin on test_wait, for the single
+// thread whose issue rate paces a pipeline.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, int* err, int code) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_test_wait(a, parity)) return true;
+  long long t0 = 0;
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_wait(a, parity)) return true;
+    if ((i & 4095u) == 0u) {
+      const long long now = clock64();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > PF_WAIT_CYCLES) {
+        set_error(err, code);
+        return false;
+      }
+      if (read_error(err) != 0) return false;
+    }
+  }
+}
+
 // The same bounded wait for long waits (an epilogue warp waiting for a whole
 // main loop): between polls the thread sleeps about `ns` nanoseconds, so that
 // waiting warps do not take shared-memory and issue bandwidth from the warps

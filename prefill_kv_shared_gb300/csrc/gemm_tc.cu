@@ -757,8 +757,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const int kc = nkb - i * C::KS < C::KS ? nkb - i * C::KS : C::KS;
             const int sa = g % C::S_A;
             const int sb = C::Q4 ? g % C::NB : 0;
-            ok = mbar_wait(&full_a[sa], (g / C::S_A) & 1, err, PF_DEV_TIMEOUT_MMA);
-            if (ok && C::Q4) ok = mbar_wait(&bfull[sb], (g / C::NB) & 1, err, PF_DEV_TIMEOUT_MMA);
+            ok = mbar_wait_spin(&full_a[sa], (g / C::S_A) & 1, err, PF_DEV_TIMEOUT_MMA);
+            if (ok && C::Q4) ok = mbar_wait_spin(&bfull[sb], (g / C::NB) & 1, err, PF_DEV_TIMEOUT_MMA);
             if (!ok) break;
             tc_fence_after();
             const uint32_t a0 = smem_u32(a_ring + sa * C::A_STAGE);

@@ -580,7 +580,8 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       // The output row of a KV-shared layer in the final ubatch goes through
       // the single-row kernels in both modes (alone after the pruning, after
       // the other rows without it), so its bits do not depend on the mode.
-      const bool out_row = !writes && is_last;
+      // A one-row ubatch (a decode step) takes them in every layer.
+      const bool out_row = M == 1 || (!writes && is_last);
       const int m_rest = out_row ? M - 1 : M;  // rows for the prefill kernels
       if (m_rest > 0) {
         AttnArgs r = a;

@@ -261,3 +261,33 @@ def test_kv_file_roundtrip_and_cached_prefill(gpu, tinyllama, tmp_path):
     got = logits.cpu().numpy()
     assert np.abs(got - full).max() <= 2e-3 * np.abs(full).max()
     ctx.close()
+
+
+@pytest.mark.parametrize("name", ["tiny", "e2b"])
+def test_decode_steps_match_oracle(gpu, tiny, e2b, name):
+    """Generation after the prompt: one-token ubatches continue the cache
+    (every layer takes the single-row attention), within tolerance of the
+    oracle's continuation, and the same bits with pruning on and off."""
+    w = tiny if name == "tiny" else e2b
+    cfg = w.cfg
+    n0, steps = (40, 6) if name == "tiny" else (300, 3)
+    tok = synth.make_tokens(cfg, n0 + steps)
+    orc = OracleContext(cfg, w, n0 + steps)
+    orc.ubatch(tok[:n0], False)
+    outs = {}
+    for prune in (True, False):
+        ctx = binding.PrefillContext(w, max_ctx=n0 + steps, ubatch_max=n0, prune=prune)
+        logits = torch.empty(cfg["vocab"], dtype=torch.float32, device="cuda")
+        ctx.ubatch(tok[:n0], 0, True, logits)
+        got = []
+        for i in range(n0, n0 + steps):
+            ctx.ubatch(tok[i:i + 1], i, True, logits)
+            ctx.sync()
+            got.append(logits.cpu().numpy().copy())
+        outs[prune] = got
+        ctx.close()
+    for a, b in zip(outs[True], outs[False]):
+        np.testing.assert_array_equal(a, b)
+    for i in range(steps):
+        want = orc.ubatch(tok[n0 + i:n0 + i + 1], True)
+        check_logits(outs[True][i], want)
