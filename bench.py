@@ -42,6 +42,8 @@ def parse_args():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-hbm", action="store_true", help="skip the single-row attention / KV restore timings")
+    ap.add_argument("--hbm-only", action="store_true",
+                    help="run only the single-row attention / KV restore timings and print them (for ncu)")
     ap.add_argument("--profile-passes", type=int, default=0,
                     help="run this many untimed prefill passes of the workload and exit (for ncu)")
     return ap.parse_args()
@@ -326,6 +328,10 @@ def run_ours(args, dist: Dist):
     binding.load()
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
+    if args.hbm_only:
+        if dist.rank == 0:
+            print(json.dumps(hbm_kernels(dev, stream, load_peaks()[0])), flush=True)
+        return
     cfg = synth.config("e2b")
     w = synth.make_weights(cfg)
     N, UB = 512, 512

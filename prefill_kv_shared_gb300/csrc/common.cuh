@@ -14,9 +14,7 @@
 #include <stdint.h>
 
 #include <cstdlib>
-#include <mutex>
 #include <utility>
-#include <vector>
 
 namespace pf {
 
@@ -62,26 +60,11 @@ inline bool pdl_enabled() {
   return on;
 }
 
-// Every kernel asks for the largest shared-memory carve-out: the GEMM and
-// attention kernels need it, and an SM that alternates between kernels with
-// different carve-outs reconfigures its L1/shared split between them.  Set
-// once per kernel (thread-safe).
-inline void prefer_max_shared(const void* fn) {
-  static std::mutex mu;
-  static std::vector<const void*> done;
-  std::lock_guard<std::mutex> lock(mu);
-  for (const void* p : done)
-    if (p == fn) return;
-  cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-  done.push_back(fn);
-}
-
 // cudaLaunchKernelEx with programmatic stream serialization (and an optional
 // cluster size)
 template <class... KArgs, class... Args>
 inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                             int cluster, Args&&... args) {
-  prefer_max_shared(reinterpret_cast<const void*>(kernel));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
