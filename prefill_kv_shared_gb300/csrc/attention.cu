@@ -586,10 +586,12 @@ struct AttnRowCfg {
   static constexpr int NST = HD >= 256 ? 3 : 4;    // ring stages
   static constexpr int S_LD = CHUNK + 4;           // score row stride, floats
   static constexpr int P_LD = CHUNK + 8;           // P row stride, halves (conflict-free fragment loads)
+  // scores, P and the rescale factors are double-buffered by tile parity,
+  // so one tile's P V overlaps the next tile's scores
   static constexpr int OFF_S = NST * STAGE;
-  static constexpr int OFF_P = OFF_S + 16 * S_LD * 4;
-  static constexpr int OFF_H = OFF_P + 16 * P_LD * 2;  // per head: m, l, alpha
-  static constexpr int OFF_BAR = OFF_H + 3 * 16 * 4;
+  static constexpr int OFF_P = OFF_S + 2 * 16 * S_LD * 4;
+  static constexpr int OFF_H = OFF_P + 2 * 16 * P_LD * 2;  // per head: m, l, then alpha x 2
+  static constexpr int OFF_BAR = OFF_H + 4 * 16 * 4;
   static constexpr int SMEM = OFF_BAR + NST * 8 + 1024;
   static_assert(STAGE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static_assert(SMEM <= 232448, "shared memory");
@@ -643,11 +645,11 @@ __global__ void __launch_bounds__(ATTN_ROW_THREADS, 1)
   constexpr int NG = HD / 64;  // 8-dim column groups of P V per warp (the 8 warps split the dims)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* sS = reinterpret_cast<float*>(smem + C::OFF_S);
-  __half* sP = reinterpret_cast<__half*>(smem + C::OFF_P);
+  float* sS0 = reinterpret_cast<float*>(smem + C::OFF_S);
+  __half* sP0 = reinterpret_cast<__half*>(smem + C::OFF_P);
   float* sM = reinterpret_cast<float*>(smem + C::OFF_H);
   float* sL = sM + 16;
-  float* sA = sL + 16;
+  float* sA0 = sL + 16;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -667,9 +669,10 @@ __global__ void __launch_bounds__(ATTN_ROW_THREADS, 1)
   if (tid < 16) {
     sM[tid] = -INFINITY;
     sL[tid] = 0.f;
-    sA[tid] = 1.f;
+    sA0[tid] = 1.f;
+    sA0[tid + 16] = 1.f;
   }
-  for (int i = tid; i < 16 * C::P_LD / 2; i += ATTN_ROW_THREADS) reinterpret_cast<uint32_t*>(sP)[i] = 0u;
+  for (int i = tid; i < 2 * 16 * C::P_LD / 2; i += ATTN_ROW_THREADS) reinterpret_cast<uint32_t*>(sP0)[i] = 0u;
   __syncthreads();
   pdl_wait();
   if (tid == 0) {
@@ -702,23 +705,40 @@ __global__ void __launch_bounds__(ATTN_ROW_THREADS, 1)
   bool ok = true;
   for (; i < nt; ++i) {
     const int st = i % C::NST;
+    float* sS = sS0 + (i & 1) * 16 * C::S_LD;
+    __half* sP = sP0 + (i & 1) * 16 * C::P_LD;
+    float* sA = sA0 + (i & 1) * 16;
     ok = mbar_wait(&full[st], (i / C::NST) & 1, err, PF_DEV_TIMEOUT_MMA);
+    // every warp is past its P V of tile i-1: that tile's stage is free
     ok = __syncthreads_and(ok);
     if (!ok) break;
+    if (tid == 0 && i >= 1 && i - 1 + C::NST < nt) {
+      const int sp = (i - 1) % C::NST;
+      mbar_arrive_expect_tx(&full[sp], C::STAGE);
+      tma_load_3d(smem + sp * C::STAGE, &tmK, &full[sp], kvh * HD, (tile0 + i - 1 + C::NST) * CHUNK, 0);
+      tma_load_3d(smem + sp * C::STAGE + C::KV_BYTES, &tmV, &full[sp], kvh * HD, (tile0 + i - 1 + C::NST) * CHUNK,
+                  0);
+    }
     const uint8_t* kt = smem + st * C::STAGE;
     const uint32_t vt = smem_u32(kt + C::KV_BYTES);
     const int key0 = (tile0 + i) * CHUNK;
     {
-      // scores of the warp's 8 keys (tile rows 8 warp .. +7)
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      // scores of the warp's 8 keys (tile rows 8 warp .. +7): two
+      // accumulation chains (even and odd 16-dim steps), added at the end
+      float c[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
       const int r = warp * 8 + g;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const int d = ks * 16 + 2 * t4;
         const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kt + tile_off(r, d) + (d & 7) * 2);
         const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kt + tile_off(r, d + 8) + (d & 7) * 2);
-        mma_16816(c, qa[ks], b0, b1);
+        if (ks & 1)
+          mma_16816(c1, qa[ks], b0, b1);
+        else
+          mma_16816(c, qa[ks], b0, b1);
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) c[e] = __fadd_rn(c[e], c1[e]);
       const int kc = warp * 8 + 2 * t4;  // tile column of c[0] / c[2]
       const bool v0 = key0 + kc <= sh.pos, v1 = key0 + kc + 1 <= sh.pos;
       *reinterpret_cast<float2*>(sS + g * C::S_LD + kc) = make_float2(v0 ? c[0] : -INFINITY, v1 ? c[1] : -INFINITY);
@@ -793,17 +813,13 @@ __global__ void __launch_bounds__(ATTN_ROW_THREADS, 1)
         }
       }
     }
-    __syncthreads();  // the stage, the scores and P are free
-    if (tid == 0 && i + C::NST < nt) {
-      mbar_arrive_expect_tx(&full[st], C::STAGE);
-      tma_load_3d(smem + st * C::STAGE, &tmK, &full[st], kvh * HD, (tile0 + i + C::NST) * CHUNK, 0);
-      tma_load_3d(smem + st * C::STAGE + C::KV_BYTES, &tmV, &full[st], kvh * HD, (tile0 + i + C::NST) * CHUNK, 0);
-    }
   }
+  __syncthreads();  // the last tile's P V is done everywhere
   if (!ok) {
-    // copies issued for tiles i .. min(nt, i + NST) - 1 may still be landing
+    // copies issued for tiles i .. (i == 0 ? NST : i - 1 + NST) - 1 may still be landing
+    const int issued = i == 0 ? C::NST : i - 1 + C::NST;
     if (tid == 0)
-      for (int j = i; j < nt && j < i + C::NST; ++j) row_drain(&full[j % C::NST], (j / C::NST) & 1);
+      for (int j = i; j < nt && j < issued; ++j) row_drain(&full[j % C::NST], (j / C::NST) & 1);
     __syncthreads();
     return;
   }
