@@ -42,6 +42,8 @@ def parse_args():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-hbm", action="store_true", help="skip the single-row attention / KV restore timings")
+    ap.add_argument("--ref-tokens", type=int, default=0,
+                    help="reference arm: time passes over the first N prompt tokens (0: sized to ~2 minutes)")
     ap.add_argument("--hbm-only", action="store_true",
                     help="run only the single-row attention / KV restore timings and print them (for ncu)")
     ap.add_argument("--profile-passes", type=int, default=0,
@@ -219,14 +221,18 @@ def run_reference(args, dist: Dist):
     w = synth.make_weights(cfg)
     tok = synth.make_tokens(cfg, 512)
     ctx = OracleContext(cfg, w, 512)
-    t0 = time.perf_counter()
-    ctx.prefill(tok, 512, prune=True)  # decodes and caches the weights
-    ctx.reset()
-    t0 = time.perf_counter()
-    ctx.prefill(tok, 512, prune=True)
-    t512 = time.perf_counter() - t0
-    budget = 120.0
-    S = 512 if args.steps * t512 <= budget else max(16, int(512 * budget / (args.steps * t512)))
+    if args.ref_tokens > 0:
+        S = min(512, args.ref_tokens)
+        t512 = None
+        ctx.prefill(tok[:S], 512, prune=True)  # decodes and caches the weights
+    else:
+        ctx.prefill(tok, 512, prune=True)  # decodes and caches the weights
+        ctx.reset()
+        t0 = time.perf_counter()
+        ctx.prefill(tok, 512, prune=True)
+        t512 = time.perf_counter() - t0
+        budget = 120.0
+        S = 512 if args.steps * t512 <= budget else max(16, int(512 * budget / (args.steps * t512)))
     sample = tok[:S]
     for _ in range(args.warmup):
         ctx.reset()
@@ -239,7 +245,7 @@ def run_reference(args, dist: Dist):
     value = args.steps * S / el
     cores = cpu_threads()
     desc = (f"{args.steps} pruned prefill passes over the first {S} tokens of the 512-token prompt"
-            + ("" if S == 512 else f" (a full 512-token pass takes {t512:.2f} s)"))
+            + ("" if S == 512 or t512 is None else f" (a full 512-token pass takes {t512:.2f} s)"))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,

@@ -591,7 +591,8 @@ struct AttnRowCfg {
   static constexpr int OFF_S = NST * STAGE;
   static constexpr int OFF_P = OFF_S + 2 * 16 * S_LD * 4;
   static constexpr int OFF_H = OFF_P + 2 * 16 * P_LD * 2;  // per head: m, l, then alpha x 2
-  static constexpr int OFF_BAR = OFF_H + 4 * 16 * 4;
+  static constexpr int OFF_Q = OFF_H + 4 * 16 * 4;  // the KV head's query rows, fp16 [16][HD]
+  static constexpr int OFF_BAR = OFF_Q + 16 * HD * 2;
   static constexpr int SMEM = OFF_BAR + NST * 8 + 1024;
   static_assert(STAGE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static_assert(SMEM <= 232448, "shared memory");
@@ -683,18 +684,24 @@ __global__ void __launch_bounds__(ATTN_ROW_THREADS, 1)
     }
   }
   // Q fragments (A of Q K^T): row g is query head kvh*G + g, row g + 8 head
-  // kvh*G + g + 8; rows past G are zero
+  // kvh*G + g + 8; rows past G are zero.  The KV head's G query rows come
+  // in with one 16-byte load per thread and are read back from shared memory.
   uint32_t qa[KS][4];
   {
-    const __half* q0 = q + (size_t)(kvh * G + g) * HD;
-    const __half* q1 = q + (size_t)(kvh * G + g + 8) * HD;
+    __half* sQ = reinterpret_cast<__half*>(smem + C::OFF_Q);
+    const uint4* qg = reinterpret_cast<const uint4*>(q + (size_t)kvh * G * HD);
+    for (int i = tid; i < 16 * HD / 8; i += ATTN_ROW_THREADS)
+      reinterpret_cast<uint4*>(sQ)[i] = i < G * HD / 8 ? qg[i] : make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    const __half* q0 = sQ + g * HD;
+    const __half* q1 = sQ + (g + 8) * HD;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       const int d = ks * 16 + 2 * t4;
-      qa[ks][0] = g < G ? *reinterpret_cast<const uint32_t*>(q0 + d) : 0u;
-      qa[ks][1] = g + 8 < G ? *reinterpret_cast<const uint32_t*>(q1 + d) : 0u;
-      qa[ks][2] = g < G ? *reinterpret_cast<const uint32_t*>(q0 + d + 8) : 0u;
-      qa[ks][3] = g + 8 < G ? *reinterpret_cast<const uint32_t*>(q1 + d + 8) : 0u;
+      qa[ks][0] = *reinterpret_cast<const uint32_t*>(q0 + d);
+      qa[ks][1] = *reinterpret_cast<const uint32_t*>(q1 + d);
+      qa[ks][2] = *reinterpret_cast<const uint32_t*>(q0 + d + 8);
+      qa[ks][3] = *reinterpret_cast<const uint32_t*>(q1 + d + 8);
     }
   }
   float o[NG][4];
