@@ -21,11 +21,12 @@
 //
 // A row's result depends only on its own position, the keys and gc: the MMA
 // rows of a tile are independent and chunks past a row's position leave its
-// state unchanged.  gc comes from the launch's key count, which the ubatch's
-// last row shares whether the launch carries the whole ubatch (M = T) or that
-// row alone (M = 1, the KV-shared layers after pruning): the pruned output row
-// is bit-identical to the unpruned one.  (Rows of a prompt cut into ubatches
-// differently can see different gc, so such runs agree to rounding.)
+// state unchanged.  (Rows of a prompt cut into ubatches differently can see
+// different gc, so such runs agree to rounding.)  The output row of a
+// KV-shared layer does not come from this kernel in either pruning mode: the
+// single-row kernels at the end of this file (attn_row_kernel) compute it, so
+// that its bits are the same whether the layer carries one row or the whole
+// ubatch.
 //
 // CTA roles: warp 1 lane 0 issues the TMA copies (Q once; K and V per chunk,
 // double-buffered); warp 0 allocates TMEM and its lane 0 issues the MMAs;
@@ -232,11 +233,14 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
           if (!ok) break;
           tc_fence_after();
           const uint32_t sk = smem_u32(smem + C::OFF_K + s * C::KV_BYTES);
+          // descriptors built once per tile, constant offsets per step (the
+          // address field holds any shared-memory address: no carry)
+          const uint64_t qd0 = sdesc_sw128(sq), kd0 = sdesc_sw128(sk);
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
             const int b = kk >> 2, w = kk & 3;  // 64-dim box, 16-dim step within it
-            tc_mma_f16(tmem + C::TMEM_S + s * CHUNK, sdesc_sw128(sq + b * (128 * 128) + w * 32),
-                       sdesc_sw128(sk + b * (CHUNK * 128) + w * 32), id_qk, kk > 0 ? 1u : 0u);
+            tc_mma_f16(tmem + C::TMEM_S + s * CHUNK, qd0 + ((b * (128 * 128) + w * 32) >> 4),
+                       kd0 + ((b * (CHUNK * 128) + w * 32) >> 4), id_qk, kk > 0 ? 1u : 0u);
           }
           issued = true;
           tc_commit(&s_full[s]);
@@ -248,10 +252,10 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
           tc_fence_after();
           const uint32_t sp = smem_u32(smem + C::OFF_P + s * C::P_BYTES);
           const uint32_t sv = smem_u32(smem + C::OFF_V + s * C::KV_BYTES);
+          const uint64_t pd0 = sdesc_sw128(sp), vd0 = sdesc_sw128_lbo_sbo(sv, CHUNK * 128, 1024);
 #pragma unroll
           for (int kk = 0; kk < CHUNK / 16; ++kk)  // 16 keys a step
-            tc_mma_f16(tmem + C::TMEM_O, sdesc_sw128(sp + kk * 32),
-                       sdesc_sw128_lbo_sbo(sv + kk * 16 * 128, CHUNK * 128, 1024), id_pv,
+            tc_mma_f16(tmem + C::TMEM_O, pd0 + ((kk * 32) >> 4), vd0 + ((kk * 16 * 128) >> 4), id_pv,
                        (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&pv_done[s]);
           tc_commit(&kv_empty[s]);

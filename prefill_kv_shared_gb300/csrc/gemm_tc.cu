@@ -763,14 +763,29 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             tc_fence_after();
             const uint32_t a0 = smem_u32(a_ring + sa * C::A_STAGE);
             const uint32_t b0 = C::Q4 ? smem_u32(b_ring + sb * C::BT_BYTES) : a0 + C::A_BYTES;
-            for (int j = 0; j < kc; ++j) {
-              const int kbl = i * C::KS + j;  // k-block within the unit
-              for (int mt = 0; mt < mt_valid; ++mt) {
+            // The stage's descriptors are built once; an operand's address
+            // sits in the low bits (16-byte units, 14 bits) and every step
+            // adds a constant offset that cannot carry out of that field.
+            // A single issuing thread pays for every instruction between
+            // two MMAs, so the common full stage is unrolled completely.
+            const uint64_t ad0 = sdesc_sw128(a0), bd0 = sdesc_sw128(b0);
+            if (kc == C::KS && mt_valid == MT) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                  const uint64_t ad = sdesc_sw128(a0 + (j * MT + mt) * 128 * 128 + kk * 32);
-                  const uint64_t bd = sdesc_sw128(b0 + j * C::BT_KB + kk * 32);
-                  tc_mma_f16(tacc + mt * BN, ad, bd, idesc, (kbl | kk) != 0 ? 1u : 0u);
+              for (int j = 0; j < C::KS; ++j)
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                  for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_f16(tacc + mt * BN, ad0 + (((j * MT + mt) * 128 * 128 + kk * 32) >> 4),
+                               bd0 + ((j * C::BT_KB + kk * 32) >> 4), idesc, (i | j | kk) != 0 ? 1u : 0u);
+            } else {
+              for (int j = 0; j < kc; ++j) {
+                const int kbl = i * C::KS + j;  // k-block within the unit
+                for (int mt = 0; mt < mt_valid; ++mt) {
+#pragma unroll
+                  for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_f16(tacc + mt * BN, ad0 + (((j * MT + mt) * 128 * 128 + kk * 32) >> 4),
+                               bd0 + ((j * C::BT_KB + kk * 32) >> 4), idesc, (kbl | kk) != 0 ? 1u : 0u);
                 }
               }
             }
