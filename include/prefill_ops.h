@@ -84,6 +84,15 @@ int pfop_embed(int32_t wtype, const void* tok_host, const void* ple_host, int32_
 int pfop_kv_copy(int32_t dir, void* cache_dev, int64_t cache_seg_halves, void* image_dev, int64_t img_seg_bytes,
                  int32_t n_seg, int64_t copy_bytes, const int32_t* header4, void* stream);
 
+/* out[n] = sum_k a[k] W[n][k] (fp32 [N]) for ONE row a (bf16 [K]) with the
+   one-token projection kernel that a one-token ubatch uses (generation
+   after the prompt): CUDA cores stream W once (wtype as in pfop_linear_f32,
+   bn its tile width), fp32 dot products, k-part sums added in a fixed
+   order.  If iters > 0 the call is then repeated `iters` times and *us
+   receives the mean device time per launch (CUDA events on `stream`). */
+int pfop_linear_row(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn, const void* a_dev,
+                    float* out_dev, int32_t iters, float* us, void* stream);
+
 /* Time the GEMM kernel: upload W once, run `warmup` then `iters` launches of
    out = A W^T (fp32 [M][N]) and return the mean device time per launch in
    *us (CUDA events on `stream`).  split: k-splits (0 = the library's choice

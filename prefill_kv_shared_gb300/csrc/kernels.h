@@ -90,6 +90,15 @@ std::vector<const void*> qkv_tile_rows(const void* wq, const void* wk, const voi
 cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err_word,
                         cudaStream_t s);
 
+// One row (a one-token ubatch): out = A[0] W^T with the same fused epilogue,
+// streamed by CUDA cores over (tile, k-part) CTAs.  `sums` holds
+// gemv_scratch_floats(W) floats; `tickets` one int per tile, zero before the
+// first launch (each launch leaves them zero).  Launches sharing the
+// scratch must be stream-ordered.
+cudaError_t launch_gemv(const ActMat& A, const WeightMat& W, const EpiParams& ep, float* sums, int* tickets,
+                        cudaStream_t s);
+size_t gemv_scratch_floats(const WeightMat& W);
+
 // Host repack.  `rows[i]` points at the i-th stored row's source (Q4_0: K/32
 // blocks of 18 bytes; F32: K floats) or is null for a zero padding row.
 std::vector<uint8_t> repack_q4_tiles(const std::vector<const uint8_t*>& rows, int K, int BN);

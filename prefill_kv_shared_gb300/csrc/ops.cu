@@ -126,6 +126,49 @@ extern "C" int pfop_linear_f32(int32_t wtype, const void* w_host, int32_t N, int
   return run_gemm(sc, A, M, W, e, static_cast<cudaStream_t>(stream));
 }
 
+extern "C" int pfop_linear_row(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn,
+                               const void* a_dev, float* out_dev, int32_t iters, float* us, void* stream) {
+  if (!w_host || !a_dev || !out_dev || N < 1 || N % 4 || K % 64 || (bn != 64 && bn != 128 && bn != 256) ||
+      iters < 0 || (iters > 0 && !us))
+    return op_fail(PF_E_ARG, "bad argument");
+  Scope sc;
+  WeightMat W;
+  ActMat A;
+  int rc;
+  if ((rc = make_weight(sc, W, wtype, rows_of(w_host, N, K, wtype, bn), K, bn))) return rc;
+  A.dev = static_cast<const __nv_bfloat16*>(a_dev);
+  A.rows = 1;
+  A.K = K;
+  EpiParams e;
+  e.kind = EPI_F32;
+  e.N = N;
+  e.out_f32 = out_dev;
+  e.ld_f32 = N;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* sums = nullptr;
+  int* tickets = nullptr;
+  OP_CUDA(sc.alloc(&sums, gemv_scratch_floats(W) * 4));
+  OP_CUDA(sc.alloc(&tickets, static_cast<size_t>(W.N_rows / W.BN) * 4));
+  OP_CUDA(cudaMemsetAsync(tickets, 0, static_cast<size_t>(W.N_rows / W.BN) * 4, s));
+  OP_CUDA(launch_gemv(A, W, e, sums, tickets, s));
+  if (iters > 0) {
+    cudaEvent_t e0, e1;
+    OP_CUDA(cudaEventCreate(&e0));
+    OP_CUDA(cudaEventCreate(&e1));
+    OP_CUDA(cudaEventRecord(e0, s));
+    for (int i = 0; i < iters; ++i) OP_CUDA(launch_gemv(A, W, e, sums, tickets, s));
+    OP_CUDA(cudaEventRecord(e1, s));
+    OP_CUDA(cudaEventSynchronize(e1));
+    float ms = 0.f;
+    OP_CUDA(cudaEventElapsedTime(&ms, e0, e1));
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    *us = ms * 1000.f / iters;
+  }
+  OP_CUDA(cudaStreamSynchronize(s));
+  return PF_OK;
+}
+
 extern "C" int pfop_linear_bench(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn, int32_t split,
                                  const void* a_dev, int32_t a_rows, int32_t M, float* out_dev, int32_t warmup,
                                  int32_t iters, float* us, void* stream) {

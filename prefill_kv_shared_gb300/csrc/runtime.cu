@@ -70,6 +70,8 @@ struct prefill_ctx {
   __half* q16 = nullptr;
   float* partials = nullptr;
   float* row_partials = nullptr;  // range states of the single-row attention
+  float* gv_sums = nullptr;       // k-part sums of the one-token projections
+  int* gv_tickets = nullptr;      // per weight tile, zero between launches
   __half* cache = nullptr;  // [2][L_w][max_ctx][kv]
   float2* rope = nullptr;
   int* err = nullptr;
@@ -387,6 +389,20 @@ extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weig
     if ((rc = upload(C, &C->out_norm, w->out_norm, C->D * 4))) return fail(nullptr, rc, C->last_error);
   }
 
+  // scratch of the one-token projections: the largest matrix decides
+  {
+    size_t fl = gemv_scratch_floats(C->head);
+    int tiles = C->head.N_rows / C->head.BN;
+    for (const LayerW& L : C->layers)
+      for (const WeightMat* m : {&L.qkv, &L.o, &L.gu, &L.down, &L.pg, &L.pp, &L.o1, &L.gu1, &L.down1, &L.pp1}) {
+        if (!m->dev) continue;
+        fl = std::max(fl, gemv_scratch_floats(*m));
+        tiles = std::max(tiles, m->N_rows / m->BN);
+      }
+    if ((rc = dev_alloc(C, &C->gv_sums, fl * 4)) || (rc = dev_alloc(C, &C->gv_tickets, tiles * 4)))
+      return fail(nullptr, rc, C->last_error);
+  }
+
   // buffers
   const size_t R = C->rows_alloc;
   if ((rc = dev_alloc(C, &C->tok, R * 4)) || (rc = dev_alloc(C, &C->x, R * C->D * 4)) ||
@@ -526,6 +542,12 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
   int pos_base = static_cast<int>(pos0);
   const __nv_bfloat16* ple_view = c->ple;
   bool gathered = false;
+  // A one-token ubatch streams its projections (launch_gemv); larger ones
+  // use the tensor cores, also for the pruned output row, whose launches
+  // must match the unpruned ones.
+  auto proj = [&](const ActMat& A, int rows, const WeightMat& Wm, const EpiParams& e) {
+    return T == 1 ? launch_gemv(A, Wm, e, c->gv_sums, c->gv_tickets, s) : launch_gemm(A, rows, Wm, e, c->err, s);
+  };
 
   for (int il = 0; il < L; ++il) {
     const LayerW& W = c->layers[il];
@@ -562,7 +584,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.v_cache = c->cache + static_cast<size_t>(c->L_w + il) * seg;
       const double n_out = c->q + 2.0 * e.kv_dim;
       PF_CUDA(c, counted(c, gemm_class(M), 1, 2.0 * M * n_out * D, M * D * 2.0 + gemm_wbytes(c, n_out, D) + M * n_out * 2.0,
-                         [&] { return launch_gemm(c->a_y, M, W.qkv, e, c->err, s); }));
+                         [&] { return proj(c->a_y, M, W.qkv, e); }));
     }
     {
       AttnArgs a;
@@ -611,7 +633,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.out_f32 = xcur;
       e.ld_f32 = D;
       PF_CUDA(c, counted(c, gemm_class(M), 1, 2.0 * M * D * c->q, M * c->q * 2.0 + gemm_wbytes(c, D, c->q) + M * D * 8.0,
-                         [&] { return launch_gemm(c->a_att, M, pick(W.o, W.o1, M), e, c->err, s); }));
+                         [&] { return proj(c->a_att, M, pick(W.o, W.o1, M), e); }));
     }
     PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, M * D * 6.0, [&] {
                return launch_rmsnorm(xcur, 0, M, D, W.ffn_norm, c->d.rms_eps, c->y, nullptr, s);
@@ -624,7 +646,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.ld_bf16 = c->F;
       e.act = c->d.ffn_kind == PF_FFN_GEGLU ? 0 : 1;
       PF_CUDA(c, counted(c, gemm_class(M), 1, 4.0 * M * c->F * D, M * D * 2.0 + gemm_wbytes(c, 2.0 * c->F, D) + M * c->F * 2.0,
-                         [&] { return launch_gemm(c->a_y, M, pick(W.gu, W.gu1, M), e, c->err, s); }));
+                         [&] { return proj(c->a_y, M, pick(W.gu, W.gu1, M), e); }));
     }
     {
       EpiParams e;
@@ -637,7 +659,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
         e.ld_bf16 = D;
       }
       PF_CUDA(c, counted(c, gemm_class(M), 1, 2.0 * M * D * c->F, M * c->F * 2.0 + gemm_wbytes(c, D, c->F) + M * D * 8.0,
-                         [&] { return launch_gemm(c->a_h, M, pick(W.down, W.down1, M), e, c->err, s); }));
+                         [&] { return proj(c->a_h, M, pick(W.down, W.down1, M), e); }));
     }
     if (c->P > 0) {
       EpiParams e;
@@ -648,14 +670,14 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.ple = ple_view + static_cast<size_t>(il) * c->P;
       e.ple_stride = LP;
       PF_CUDA(c, counted(c, gemm_class(M), 1, 2.0 * M * c->P * D, M * D * 2.0 + gemm_wbytes(c, c->P, D) + M * c->P * 4.0,
-                         [&] { return launch_gemm(c->a_xb, M, W.pg, e, c->err, s); }));
+                         [&] { return proj(c->a_xb, M, W.pg, e); }));
       EpiParams r;
       r.kind = EPI_RESID;
       r.N = D;
       r.out_f32 = xcur;
       r.ld_f32 = D;
       PF_CUDA(c, counted(c, gemm_class(M), 1, 2.0 * M * D * c->P, M * c->P * 2.0 + gemm_wbytes(c, D, c->P) + M * D * 8.0,
-                         [&] { return launch_gemm(c->a_pg, M, pick(W.pp, W.pp1, M), r, c->err, s); }));
+                         [&] { return proj(c->a_pg, M, pick(W.pp, W.pp1, M), r); }));
     }
   }
   if (is_last) {
@@ -669,7 +691,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
     e.out_f32 = logits;
     e.ld_f32 = c->V;
     PF_CUDA(c, counted(c, gemm_class(1), 1, 2.0 * c->V * D, D * 2.0 + gemm_wbytes(c, c->V, D) + c->V * 4.0,
-                       [&] { return launch_gemm(c->a_y, 1, c->head, e, c->err, s); }));
+                       [&] { return launch_gemv(c->a_y, c->head, e, c->gv_sums, c->gv_tickets, s); }));
   }
   c->n_pos = kv_len;
   return PF_OK;

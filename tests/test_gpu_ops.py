@@ -351,3 +351,27 @@ def test_kv_copy_bench_restores_exactly(lib):
     assert us.value > 0
     got = cache.cpu().numpy().view(np.uint8).reshape(-1)
     np.testing.assert_array_equal(got, img[16:].cpu().numpy())
+
+
+@pytest.mark.parametrize("wtype,N,K,bn", [(Q4, 1536, 6144, 64), (Q4, 2560, 1536, 128), (Q4, 12288, 1536, 256),
+                                          (Q4, 200, 256, 64), (Q4, 32768, 1536, 128), (F32, 384, 512, 128),
+                                          (F32, 256, 1024, 256)])
+def test_linear_row_stream(lib, wtype, N, K, bn):
+    """The one-token projection (CUDA cores, fp32): against float64 on the
+    exact Q4_0 decode (its weights are exact in fp32, no bf16 rounding), the
+    same bits on a repeated call, ragged N included."""
+    rng = np.random.default_rng(N + K + bn)
+    w, w_gpu, w_exact = _weights(wtype, rng, N, K)
+    A = _A(rng, 1, K)
+    a = torch.from_numpy(A).cuda().bfloat16()
+    outs = []
+    for _ in range(2):
+        out = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+        binding.check_op(lib.pfop_linear_row(wtype, w.ctypes.data, N, K, bn, a.data_ptr(), out.data_ptr(), 0, None,
+                                             None))
+        outs.append(out)
+    got = outs[0].cpu().numpy()
+    ref = A.astype(np.float64)[0] @ (w_exact if wtype == Q4 else w_gpu).astype(np.float64).T
+    assert np.isfinite(got).all()
+    assert rel_err(got, ref) < 2e-5
+    assert torch.equal(outs[0], outs[1])
