@@ -23,10 +23,12 @@ Sources (web pages, by title and section):
   paragraph: layers / KV-dim mismatches are refused, the cached position count
   may not exceed the context length.
 
-Where the pages leave the architecture open, the oracle takes the readings
-listed in DESIGN.md ("Readings of the pages"); the model-level semantics that
-no page fixes (pre-norm layout, PLE block form, RoPE layout, GELU form) are
-"parity unpinned": nothing outside this oracle can confirm them.
+Where the pages leave the architecture open, the oracle takes the plainest
+readings the rest supports: a pre-norm decoder with RMSNorm gains (1 + g),
+half-split RoPE, GELU in its tanh form, the per-layer-embedding block
+x += W_pp (gelu(W_pg x) * ple) after the FFN, no embedding scale and a tied
+head.  Those model-level semantics are "parity unpinned": nothing outside
+this oracle can confirm them.
 """
 from .prefill import (  # noqa: F401
     OracleContext,
