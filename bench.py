@@ -48,6 +48,8 @@ def parse_args():
                     help="run only the single-row attention / KV restore timings and print them (for ncu)")
     ap.add_argument("--profile-passes", type=int, default=0,
                     help="run this many untimed prefill passes of the workload and exit (for ncu)")
+    ap.add_argument("--profile-prompt", type=int, default=512,
+                    help="prompt length of the --profile-passes passes (ubatches of 512)")
     return ap.parse_args()
 
 
@@ -351,10 +353,19 @@ def run_ours(args, dist: Dist):
         ctx.ubatch(tok, 0, True, logits)
 
     if args.profile_passes:
+        n = args.profile_prompt
+        pctx, ptok = ctx, tok
+        if n != N:
+            pctx = binding.PrefillContext(w, max_ctx=n, ubatch_max=UB, prune=True, stream=stream)
+            ptok = torch.from_numpy(synth.make_tokens(cfg, n)).to(dev)
         for _ in range(args.profile_passes):
-            step()
-            ctx.sync()
+            pctx.reset()
+            for i in range(0, n, UB):
+                pctx.ubatch(ptok[i:i + UB], i, i + UB >= n, logits)
+            pctx.sync()
         print("ok", float(logits.abs().max()), flush=True)
+        if pctx is not ctx:
+            pctx.close()
         ctx.close()
         return
 
