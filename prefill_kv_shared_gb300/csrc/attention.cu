@@ -529,7 +529,7 @@ static cudaError_t launch_tc_t(const AttnArgs& a, float* part, cudaStream_t s) {
   sh.Hq = a.Hq;
   sh.Hkv = a.Hkv;
   sh.pos_base = a.pos_base;
-  sh.gc = attn_group_chunks(a.group_kv > 0 ? a.group_kv : a.kv_len);
+  sh.gc = attn_group_chunks(a.kv_len);
   const int last_pos = a.pos_base + a.M - 1;
   const int n_groups = attn_row_groups(last_pos, sh.gc);
   if (n_groups > 1 && !part) return cudaErrorInvalidValue;
@@ -980,7 +980,7 @@ cudaError_t launch_attn_split(const AttnArgs& a, float* partials, cudaStream_t s
 
 int attn_launch_count(const AttnArgs& a) {
   if (a.M <= 0) return 0;
-  return attn_row_groups(a.pos_base + a.M - 1, attn_group_chunks(a.group_kv > 0 ? a.group_kv : a.kv_len)) > 1 ? 2
+  return attn_row_groups(a.pos_base + a.M - 1, attn_group_chunks(a.kv_len)) > 1 ? 2
                                                                                                          : 1;
 }
 

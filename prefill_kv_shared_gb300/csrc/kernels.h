@@ -115,9 +115,6 @@ struct AttnArgs {
   int M = 0, Hq = 0, Hkv = 0, hd = 0;
   int pos_base = 0;  // position of row 0
   int kv_len = 0;    // keys [0, kv_len) exist in the cache
-  int group_kv = 0;  // key count that fixes the chunk-group size (0: kv_len);
-                     // launches that pass the same value group a row's keys
-                     // the same way whatever their own key count
   int* err = nullptr;  // device error word (bounded waits that give up set it)
 };
 
