@@ -136,3 +136,55 @@ def test_kv_file_check_host_only(lib, tmp_path):
     p = tmp_path / "ok.kvcp"
     assert binding.kv_file_check(str(p), L_w, kv, 39)[0] == binding.PF_E_KV_RANGE  # beyond the context
     assert binding.kv_file_check(str(tmp_path / "none.kvcp"), L_w, kv, 100)[0] == binding.PF_E_IO
+
+
+def test_prefill_with_cache_flow_decisions(tmp_path):
+    """The cached-prefix flow (PicoLM KV cache article, "usage"): a missing or
+    refused file means a full prefill and a save; a valid file of the first
+    n positions means a restore and a prefill of the rest only."""
+    import numpy as np
+
+    class FakeCtx:
+        n_layers_written, kv_dim, max_ctx = 3, 64, 100
+
+        def __init__(self, load_rc):
+            self.calls, self.load_rc = [], load_rc
+
+        def reset(self):
+            self.calls.append(("reset",))
+
+        def kv_load_file(self, path, n):
+            self.calls.append(("load", n))
+            return self.load_rc
+
+        def ubatch(self, tok, pos0, is_last, logits):
+            self.calls.append(("ubatch", pos0, len(tok), bool(is_last)))
+
+        def sync(self):
+            pass
+
+        def kv_save_file(self, path):
+            self.calls.append(("save",))
+
+    tok = np.arange(50, dtype=np.int32)
+    path = str(tmp_path / "p.kvcp")
+    ctx = FakeCtx(binding.PF_OK)
+    assert binding.prefill_with_cache(ctx, tok, 32, None, path) == 0  # no file yet
+    assert ctx.calls == [("reset",), ("ubatch", 0, 32, False), ("ubatch", 32, 18, True), ("save",)]
+    # a valid 40-position image of this model
+    hdr = b"KVCP" + np.array([40, 3, 64], dtype="<i4").tobytes()
+    with open(path, "wb") as f:
+        f.write(hdr + bytes(2 * 3 * 40 * 64 * 2))
+    ctx = FakeCtx(binding.PF_OK)
+    assert binding.prefill_with_cache(ctx, tok, 32, None, path) == 40
+    assert ctx.calls == [("reset",), ("load", 40), ("ubatch", 40, 10, True)]
+    # the restore refused (e.g. the context changed): full prefill and save
+    ctx = FakeCtx(binding.PF_E_KV_RANGE)
+    assert binding.prefill_with_cache(ctx, tok, 32, None, path) == 0
+    assert ctx.calls[-1] == ("save",) and ("ubatch", 0, 32, False) in ctx.calls
+    # an image as long as the prompt cannot leave a row to prefill: ignored
+    with open(path, "wb") as f:
+        f.write(b"KVCP" + np.array([50, 3, 64], dtype="<i4").tobytes() + bytes(2 * 3 * 50 * 64 * 2))
+    ctx = FakeCtx(binding.PF_OK)
+    assert binding.prefill_with_cache(ctx, tok, 32, None, path) == 0
+    assert ("load", 50) not in ctx.calls
