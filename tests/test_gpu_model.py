@@ -192,7 +192,16 @@ def test_errors_leave_state(gpu, tiny):
     ctx.ubatch(tok[:20], 0, False)
     with pytest.raises(binding.PrefillError):
         ctx.ubatch(tok[20:30], 5, True, logits)   # pos0 gap
+    with pytest.raises(binding.PrefillError) as e:
+        ctx.ubatch(tok[:0], 20, True, logits)       # empty ubatch
+    assert e.value.code == binding.PF_E_ARG and ctx.n_pos == 20
+    with pytest.raises(binding.PrefillError) as e:
+        ctx.ubatch(tok[20:40], 20, True, None)      # last ubatch without logits
+    assert e.value.code == binding.PF_E_ARG and ctx.n_pos == 20
     ctx.ubatch(tok[20:40], 20, True, logits)
+    with pytest.raises(binding.PrefillError) as e:
+        ctx.ubatch(synth.make_tokens(cfg, 25), 40, True, logits)   # 40 + 25 > max_ctx 64
+    assert e.value.code == binding.PF_E_ARG and ctx.n_pos == 40
     ctx.sync()
     n = ctx.kv_image_bytes(40)
     img = np.empty(n, dtype=np.uint8)

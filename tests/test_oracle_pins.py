@@ -371,16 +371,30 @@ def test_pruned_row_equals_unpruned_row(tiny):
     np.testing.assert_allclose(a, b, rtol=0, atol=1e-5 * np.abs(a).max())
 
 
-def test_ubatch_split_invariance(tiny):
+@pytest.mark.parametrize("ub", [16, 7, 1])
+def test_ubatch_split_invariance(tiny, ub):
+    """The final row does not depend on how the prompt is cut into ubatches:
+    16 (even), 7 (a ragged last ubatch of one token) and 1 (token by token,
+    the form generation takes after the prompt)."""
     cfg, w = tiny
     tok = synth.make_tokens(cfg, 64)
     a = OracleContext(cfg, w, 128).prefill(tok, 64)
-    b = OracleContext(cfg, w, 128).prefill(tok, 16, prune=True)
-    c = OracleContext(cfg, w, 128).prefill(tok, 16, prune=False)
+    b = OracleContext(cfg, w, 128).prefill(tok, ub, prune=True)
+    c = OracleContext(cfg, w, 128).prefill(tok, ub, prune=False)
     # a different split rounds the fp32 sums differently, which can move an
     # FP16 cache entry by one unit: 1e-4 of the largest logit covers that
     np.testing.assert_allclose(a, b, rtol=0, atol=1e-4 * np.abs(a).max())
     np.testing.assert_allclose(a, c, rtol=0, atol=1e-4 * np.abs(a).max())
+
+
+def test_empty_or_oversized_ubatch_is_refused(tiny):
+    cfg, w = tiny
+    a = OracleContext(cfg, w, 16)
+    with pytest.raises(ValueError):
+        a.ubatch(np.zeros(0, dtype=np.int32), True)
+    with pytest.raises(ValueError):
+        a.ubatch(synth.make_tokens(cfg, 17), True)
+    assert a.n_pos == 0
 
 
 def test_kv_restore_then_suffix_equals_full(tiny):
