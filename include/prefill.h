@@ -53,7 +53,7 @@ extern "C" {
 #define PF_E_CUDA (-5)           /* a CUDA call failed */
 #define PF_E_DEVICE_TIMEOUT (-6) /* a kernel gave up a bounded wait; results are invalid */
 #define PF_E_DEVICE_TOKEN (-7)   /* a device-resident token id was out of range */
-#define PF_E_NOMEM (-8)          /* device allocation failed */
+#define PF_E_NOMEM (-8)          /* device memory exhausted (a cudaMalloc that failed for another reason is PF_E_CUDA) */
 #define PF_E_IO (-9)             /* a KV image file could not be opened, read or written */
 
 /* weight storage types */

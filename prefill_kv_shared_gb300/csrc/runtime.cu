@@ -118,7 +118,9 @@ template <class T>
 int dev_alloc(prefill_ctx* c, T** out, size_t bytes, bool zero = true) {
   void* p = nullptr;
   cudaError_t e = cudaMalloc(&p, bytes ? bytes : 16);
-  if (e != cudaSuccess) return fail(c, PF_E_NOMEM, std::string("cudaMalloc: ") + cudaGetErrorString(e));
+  if (e != cudaSuccess)  // out of memory is PF_E_NOMEM; no device or driver is a CUDA failure
+    return fail(c, e == cudaErrorMemoryAllocation ? PF_E_NOMEM : PF_E_CUDA,
+                std::string("cudaMalloc: ") + cudaGetErrorString(e));
   c->allocs.push_back(p);
   if (zero) {
     e = cudaMemset(p, 0, bytes ? bytes : 16);

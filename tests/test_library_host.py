@@ -188,3 +188,35 @@ def test_prefill_with_cache_flow_decisions(tmp_path):
     ctx = FakeCtx(binding.PF_OK)
     assert binding.prefill_with_cache(ctx, tok, 32, None, path) == 0
     assert ("load", 50) not in ctx.calls
+
+
+def test_product_package_never_touches_the_oracle():
+    """The library's Python side is marshalling only: no module of the
+    package imports the oracle (which is test infrastructure)."""
+    pkg = os.path.join(ROOT, "prefill_kv_shared_gb300")
+    for name in os.listdir(pkg):
+        if name.endswith(".py"):
+            src = open(os.path.join(pkg, name)).read()
+            assert not re.search(r"^\s*(from|import)\s+oracle\b", src, flags=re.M), name
+
+
+def test_missing_library_raises():
+    code = ("import sys; from prefill_kv_shared_gb300 import binding\n"
+            "try:\n    binding.load('/nonexistent/libprefill_kv_shared.so')\n"
+            "except RuntimeError as e:\n    print('raised', e)\n    sys.exit(0)\n"
+            "sys.exit(3)\n")
+    r = subprocess.run([os.sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "CUDA library not found" in r.stdout, r.stdout + r.stderr
+
+
+def test_no_gpu_means_an_error_not_a_fallback(lib):
+    """Without a CUDA device the context refuses to be created (PF_E_CUDA):
+    nothing of the pass runs on the host."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    cfg = synth.config("tiny")
+    w = synth.make_weights(cfg)
+    with pytest.raises(binding.PrefillError) as e:
+        binding.PrefillContext(w, max_ctx=64, ubatch_max=32)
+    assert e.value.code == binding.PF_E_CUDA
