@@ -707,7 +707,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const int kc = nkb - i * C::KS < C::KS ? nkb - i * C::KS : C::KS;
             const int sa = g % C::S_A;
             ok = mbar_wait(&empty_a[sa], ((g / C::S_A) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
-            const bool raw_now = C::Q4 && g + 1 > pre;  // g >= pre, without a vacuous compare when pre is 0
+            const bool raw_now = C::Q4 && g >= pre;
             const int sr = g % C::NR;
             if (ok && raw_now) ok = mbar_wait(&empty_r[sr], ((g / C::NR) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
             if (!ok) break;
