@@ -321,6 +321,98 @@ def hbm_kernels(dev, stream, peaks, iters: int = 20):
     return out
 
 
+# Reuse of a fixed prompt prefix through its KV image (PicoLM KV cache
+# article, "usage" and "measured": a system prompt is prefilled once and its
+# FP16 KV image restored for every later request).  TinyLlama shape: a
+# 500-token prefix, requests that each append a 32-token suffix.  full = the
+# whole prompt prefilled in ubatches of `ub`; reuse = restore the prefix's
+# positions from the image (device or host memory), then prefill the suffix.
+
+
+def prefix_reuse(ctx, prefix, suffixes, ub, logits, images, timer):
+    """ctx: a PrefillContext (or a stand-in with its methods); images:
+    {name: (image, nbytes)}; timer(fn) -> ms that one call of fn took on the
+    context's stream.  Returns ms per request for each way."""
+    import numpy as np
+    n0 = len(prefix)
+    prompts = [np.concatenate([prefix, s]) for s in suffixes]
+
+    def full():
+        for p in prompts:
+            ctx.reset()
+            for i in range(0, len(p), ub):
+                ctx.ubatch(p[i:i + ub], i, i + ub >= len(p), logits)
+
+    def reuse(img, nbytes):
+        for s in suffixes:
+            ctx.reset()
+            ctx.kv_load(img, nbytes, n0)
+            ctx.ubatch(s, n0, True, logits)
+
+    out = {"requests": len(suffixes), "prefix": n0, "suffix": len(suffixes[0]),
+           "full_ms": timer(full) / len(suffixes)}
+    for name, (img, nbytes) in images.items():
+        ms = timer(lambda: reuse(img, nbytes)) / len(suffixes)
+        out[f"reuse_{name}_ms"] = ms
+        out[f"speedup_{name}"] = out["full_ms"] / ms
+    return out
+
+
+def run_prefix_reuse(dev, stream):
+    """prefix_reuse on the GPU: the 500-token prefix of the TinyLlama-shaped
+    model (no KV-shared layers, so no pruning) cached once as a device image
+    and as a host (pageable) copy, 64 requests of 32 tokens (seeds 2..65)."""
+    import numpy as np
+    import torch
+
+    from prefill_kv_shared_gb300 import binding, synth
+    tl = synth.make_weights(synth.config("tinyllama"))
+    cfg = tl.cfg
+    ctx = binding.PrefillContext(tl, max_ctx=532, ubatch_max=512, stream=stream)
+    logits = torch.empty(cfg["vocab"], dtype=torch.float32, device=dev)
+    prefix = synth.make_tokens(cfg, 500, seed=1)
+    suffixes = [synth.make_tokens(cfg, 32, seed=2 + i) for i in range(64)]
+    ctx.ubatch(prefix, 0, False)
+    nbytes = ctx.kv_image_bytes(500)
+    img = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    ctx.kv_save(img, nbytes)
+    host_img = np.empty(nbytes, dtype=np.uint8)
+    ctx.kv_save(host_img, nbytes)
+    ctx.sync()
+
+    def timer(fn):
+        fn()  # warm-up
+        ctx.sync()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b)
+
+    out = prefix_reuse(ctx, prefix, suffixes, 512, logits, {"device": (img, nbytes), "host": (host_img, nbytes)},
+                       timer)
+    # the restored pass computes what the full pass computes (first request)
+    ctx.reset()
+    p = np.concatenate([prefix, suffixes[0]])
+    ctx.ubatch(p[:512], 0, False)
+    ctx.ubatch(p[512:], 512, True, logits)
+    ctx.sync()
+    want = logits.cpu().numpy().copy()
+    ctx.reset()
+    ctx.kv_load(img, nbytes, 500)
+    ctx.ubatch(suffixes[0], 500, True, logits)
+    ctx.sync()
+    got = logits.cpu().numpy()
+    out["max_rel_diff"] = float(np.abs(got - want).max() / np.abs(want).max())
+    out["image_bytes"] = nbytes
+    out["note"] = "CUDA events on the library's stream per request, tokens from host memory"
+    ctx.close()
+    del tl, img, logits
+    torch.cuda.empty_cache()
+    return out
+
+
 # ---------------------------------------------------------------------------
 # our arm
 
@@ -542,6 +634,12 @@ def run_ours(args, dist: Dist):
         rate, per, n = oracle_rate(cfg, w, tok_host, budget_s=10.0)
         cpu = {"value": rate, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
                "sample": f"{n} pruned prefill passes of the same 512-token prompt ({per:.2f} s each), weights decoded once before timing"}
+
+    if sweep is not None:
+        try:
+            sweep["prefix_reuse_tinyllama"] = run_prefix_reuse(dev, stream)
+        except Exception as e:  # recorded, never fatal to the line
+            sweep["prefix_reuse_tinyllama"] = {"error": f"{type(e).__name__}: {e}"}
 
     if dist.rank == 0:
         line = {
