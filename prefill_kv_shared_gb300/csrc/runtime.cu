@@ -90,6 +90,21 @@ struct prefill_ctx {
   };
   std::vector<Timed> timed;
   std::vector<cudaEvent_t> event_pool;
+
+  prefill_ctx() = default;
+  prefill_ctx(const prefill_ctx&) = delete;
+  prefill_ctx& operator=(const prefill_ctx&) = delete;
+  // Frees the events and device buffers the context holds.  Also runs when
+  // prefill_create gives up half way, so a failed create leaves no device
+  // memory behind.
+  ~prefill_ctx() {
+    for (auto& t : timed) {
+      cudaEventDestroy(t.e0);
+      cudaEventDestroy(t.e1);
+    }
+    for (cudaEvent_t e : event_pool) cudaEventDestroy(e);
+    for (void* p : allocs) cudaFree(p);
+  }
 };
 
 namespace {
@@ -487,12 +502,6 @@ extern "C" int prefill_reset_stats(prefill_ctx* c) {
 extern "C" void prefill_destroy(prefill_ctx* c) {
   if (!c) return;
   cudaStreamSynchronize(c->stream);
-  for (auto& t : c->timed) {
-    cudaEventDestroy(t.e0);
-    cudaEventDestroy(t.e1);
-  }
-  for (cudaEvent_t e : c->event_pool) cudaEventDestroy(e);
-  for (void* p : c->allocs) cudaFree(p);
   delete c;
 }
 
