@@ -110,7 +110,14 @@ typedef struct prefill_weights {
    uploads and repacks the weights, allocates the FP16 KV cache
    (2 x writing layers x max_ctx x kv_dim) and the activation buffers for
    ubatch_max rows.  cuda_stream: a cudaStream_t or NULL.  On failure *out is
-   NULL and the status says why. */
+   NULL, nothing stays allocated, and the status says why: PF_E_ARG for a
+   description outside the supported shapes (head_dim 64 or 256, n_head /
+   n_head_kv dividing 16, d_model / ffn_dim / ple_dim multiples of 64) or
+   too large to index with 32-bit integers (ubatch_max rounded up to 128
+   times the widest activation row, any weight matrix, or max_ctx x kv_dim
+   reaching 2^31 elements; ubatch_max above 2^20; max_ctx above 2^26),
+   checked before any CUDA call; PF_E_NOMEM when device memory runs out;
+   PF_E_CUDA for any other CUDA failure. */
 int prefill_create(const prefill_model_desc* desc, const prefill_weights* weights, void* cuda_stream,
                    prefill_ctx** out);
 

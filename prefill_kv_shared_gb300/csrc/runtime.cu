@@ -215,6 +215,23 @@ int check_desc(const prefill_model_desc* d, std::string* why) {
   if (d->ffn_kind != PF_FFN_GEGLU && d->ffn_kind != PF_FFN_SWIGLU) return bad("ffn_kind");
   if (d->wtype != PF_W_F32 && d->wtype != PF_W_Q4_0) return bad("wtype");
   if (d->max_ctx < 1 || d->ubatch_max < 1) return bad("max_ctx and ubatch_max must be >= 1");
+  // Sizes whose products the kernels index with 32-bit integers: a row of
+  // any activation, a weight matrix, and one layer's cache stay below 2^31
+  // elements (far above any model this library targets).
+  constexpr int64_t kMaxElems = int64_t(1) << 31;
+  if (d->n_layer > 4096 || d->n_head > 1024 || d->ubatch_max > (1 << 20) || d->max_ctx > (1 << 26))
+    return bad("n_layer, n_head, ubatch_max or max_ctx too large");
+  {
+    const int64_t rows = (int64_t(d->ubatch_max) + 127) / 128 * 128;
+    const int64_t kv = int64_t(d->n_head_kv) * d->head_dim, q = int64_t(d->n_head) * d->head_dim;
+    const int64_t width = std::max({int64_t(d->d_model), int64_t(d->ffn_dim), q, 2 * kv,
+                                    int64_t(d->n_layer) * d->ple_dim});
+    if (rows * width >= kMaxElems) return bad("ubatch_max times the widest activation reaches 2^31 elements");
+    if (int64_t(d->vocab) * d->d_model >= kMaxElems || 2 * int64_t(d->ffn_dim) * d->d_model >= kMaxElems ||
+        (q + 2 * kv) * d->d_model >= kMaxElems || int64_t(d->vocab) * d->n_layer * d->ple_dim >= kMaxElems)
+      return bad("a weight matrix reaches 2^31 elements");
+    if (int64_t(d->max_ctx) * kv >= kMaxElems) return bad("max_ctx times the KV width reaches 2^31 elements");
+  }
   if (!d->kv_src) return bad("kv_src is null");
   for (int il = 0; il < d->n_layer; ++il) {
     const int s = d->kv_src[il];

@@ -220,3 +220,20 @@ def test_no_gpu_means_an_error_not_a_fallback(lib):
     with pytest.raises(binding.PrefillError) as e:
         binding.PrefillContext(w, max_ctx=64, ubatch_max=32)
     assert e.value.code == binding.PF_E_CUDA
+
+
+@pytest.mark.parametrize("kw", [dict(ubatch_max=1 << 21), dict(max_ctx=1 << 27),
+                                dict(ubatch_max=1 << 20, cfg=dict(d_model=4096)),
+                                dict(max_ctx=1 << 24, cfg=dict(n_head=16, n_head_kv=16, head_dim=256))])
+def test_oversized_descriptions_refused_before_any_cuda_call(lib, kw):
+    """Sizes whose element counts would pass 2^31 (the kernels index rows,
+    weights and a layer's cache with 32-bit integers) are refused with
+    PF_E_ARG by the description check, which runs before the first CUDA
+    call (so this holds on a machine without a GPU too)."""
+    cfg = dict(synth.config("tiny"))
+    cfg.update(kw.get("cfg", {}))
+    w = synth.make_weights(synth.config("tiny"))
+    w.cfg = cfg
+    with pytest.raises(binding.PrefillError) as e:
+        binding.PrefillContext(w, max_ctx=kw.get("max_ctx", 64), ubatch_max=kw.get("ubatch_max", 32))
+    assert e.value.code == binding.PF_E_ARG, str(e.value)
