@@ -545,7 +545,7 @@ static cudaError_t launch_tc_t(const AttnArgs& a, float* part, cudaStream_t s) {
 }
 
 static bool attn_shape_ok(const AttnArgs& a) {
-  if (a.Hkv <= 0 || a.Hq % a.Hkv != 0 || !a.err) return false;
+  if (a.Hkv <= 0 || a.Hq <= 0 || a.Hq % a.Hkv != 0 || !a.err) return false;
   const int G = a.Hq / a.Hkv;
   if (G > 16 || (16 % G) != 0) return false;
   if (a.pos_base < 0 || a.pos_base + a.M > a.kv_len) return false;

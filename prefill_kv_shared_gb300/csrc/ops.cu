@@ -323,7 +323,7 @@ extern "C" int pfop_linear_qkv(int32_t wtype, const void* wq_host, const void* w
 extern "C" int pfop_attention(int32_t mode, const void* q_dev, const void* k_dev, const void* v_dev, int32_t M,
                               int32_t Hq, int32_t Hkv, int32_t hd, int32_t pos_base, int32_t kv_len, void* out_dev,
                               void* stream) {
-  if (!q_dev || !k_dev || !v_dev || !out_dev || M < 1 || pos_base < 0 || pos_base + M > kv_len)
+  if (!q_dev || !k_dev || !v_dev || !out_dev || M < 1 || Hq < 1 || Hkv < 1 || pos_base < 0 || pos_base + M > kv_len)
     return op_fail(PF_E_ARG, "bad argument");
   if (mode == 1 && M != 1) return op_fail(PF_E_ARG, "split mode takes one row");
   AttnArgs a;
@@ -464,7 +464,8 @@ extern "C" int pfop_attention_bench(int32_t mode, const void* q_dev, const void*
                                     int32_t Hq, int32_t Hkv, int32_t hd, int32_t pos_base, int32_t kv_len,
                                     void* out_dev, void* scrub_dev, int64_t scrub_bytes, int32_t warmup,
                                     int32_t iters, float* us, void* stream) {
-  if (!q_dev || !k_dev || !v_dev || !out_dev || !us || M < 1 || pos_base < 0 || pos_base + M > kv_len || iters < 1 ||
+  if (!q_dev || !k_dev || !v_dev || !out_dev || !us || M < 1 || Hq < 1 || Hkv < 1 || pos_base < 0 ||
+      pos_base + M > kv_len || iters < 1 ||
       warmup < 0 || scrub_bytes < 0)
     return op_fail(PF_E_ARG, "bad argument");
   if (mode != 0 && mode != 1) return op_fail(PF_E_ARG, "mode");

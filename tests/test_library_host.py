@@ -237,3 +237,17 @@ def test_oversized_descriptions_refused_before_any_cuda_call(lib, kw):
     with pytest.raises(binding.PrefillError) as e:
         binding.PrefillContext(w, max_ctx=kw.get("max_ctx", 64), ubatch_max=kw.get("ubatch_max", 32))
     assert e.value.code == binding.PF_E_ARG, str(e.value)
+
+
+def test_attention_entry_points_refuse_empty_head_counts(lib):
+    """Zero query or KV heads are argument errors (PF_E_ARG), found before
+    any CUDA call or any division by the head-group size."""
+    import ctypes as C
+    fake = C.c_void_p(256)  # never dereferenced: the argument check fails first
+    us = C.c_float(0.0)
+    for hq, hkv in ((0, 1), (8, 0), (0, 0)):
+        for mode in (0, 1):
+            assert lib.pfop_attention(mode, fake, fake, fake, 1, hq, hkv, 64, 0, 1, fake, None) == binding.PF_E_ARG
+            assert lib.pfop_attention_bench(mode, fake, fake, fake, 1, hq, hkv, 64, 0, 1, fake, None, 0, 0, 1,
+                                            C.byref(us), None) == binding.PF_E_ARG
+        assert lib.pfop_attention_split_noalloc(fake, fake, fake, hq, hkv, 64, 0, 1, fake, None) == binding.PF_E_ARG
