@@ -159,8 +159,9 @@ int64_t prefill_kv_image_bytes(const prefill_ctx* ctx, int64_t n_pos);
    prompt positions are ever in the cache. */
 int kv_save(prefill_ctx* ctx, void* dst, size_t dst_bytes);
 
-/* Restore the first n_pos positions of a KV image (device or host memory) and
-   set the position count to n_pos; the next ubatch continues at n_pos.  A
+/* Restore the first n_pos positions of a KV image (device or host memory; a
+   device image 16-byte aligned, else PF_E_ARG) and set the position count
+   to n_pos; the next ubatch continues at n_pos.  A
    wrong magic (PF_E_KV_MAGIC), a layer/kv_dim mismatch (PF_E_KV_SHAPE), or
    n_pos beyond the image's positions or max_ctx (PF_E_KV_RANGE) is refused
    and leaves the cache and position count unchanged: the caller then runs a

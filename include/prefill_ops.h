@@ -80,7 +80,10 @@ int pfop_embed(int32_t wtype, const void* tok_host, const void* ple_host, int32_
 /* The KV image copy kernel.  dir 0: cache -> image (writes the 16-byte header
    `header`, then n_seg segments of copy_bytes); dir 1: image -> cache.
    Segment s is at s*cache_seg_halves halves in the cache and at
-   16 + s*img_seg_bytes bytes in the image. */
+   16 + s*img_seg_bytes bytes in the image.  The kernel moves 16-byte
+   vectors: cache_dev and image_dev 16-byte aligned, cache_seg_halves a
+   multiple of 8, img_seg_bytes and copy_bytes multiples of 16, else
+   PF_E_ARG (checked before any CUDA call). */
 int pfop_kv_copy(int32_t dir, void* cache_dev, int64_t cache_seg_halves, void* image_dev, int64_t img_seg_bytes,
                  int32_t n_seg, int64_t copy_bytes, const int32_t* header4, void* stream);
 
@@ -114,11 +117,11 @@ int pfop_attention_bench(int32_t mode, const void* q_dev, const void* k_dev, con
                          int32_t Hkv, int32_t hd, int32_t pos_base, int32_t kv_len, void* out_dev, void* scrub_dev,
                          int64_t scrub_bytes, int32_t warmup, int32_t iters, float* us, void* stream);
 
-/* Time the KV image copy kernel of pfop_kv_copy (same layout arguments; the
-   image header written by dir 0 is all zeros here) like
-   pfop_attention_bench: mean device time per launch in *us, optional L2
-   scrub of scrub_dev before every timed launch.  The copy reads and writes
-   n_seg * copy_bytes bytes each. */
+/* Time the KV image copy kernel of pfop_kv_copy (same layout arguments and
+   alignment rules; the image header written by dir 0 is all zeros here)
+   like pfop_attention_bench: mean device time per launch in *us, optional
+   L2 scrub of scrub_dev before every timed launch.  The copy reads and
+   writes n_seg * copy_bytes bytes each. */
 int pfop_kv_copy_bench(int32_t dir, void* cache_dev, int64_t cache_seg_halves, void* image_dev, int64_t img_seg_bytes,
                        int32_t n_seg, int64_t copy_bytes, void* scrub_dev, int64_t scrub_bytes, int32_t warmup,
                        int32_t iters, float* us, void* stream);

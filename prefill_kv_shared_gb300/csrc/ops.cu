@@ -374,7 +374,8 @@ extern "C" int pfop_rmsnorm(const float* x_dev, int32_t row0, int32_t M, int32_t
 extern "C" int pfop_embed(int32_t wtype, const void* tok_host, const void* ple_host, int32_t vocab, int32_t D,
                           int32_t LP, float ple_scale, const int32_t* tok_dev, int32_t T, float* x_dev, void* ple_dev,
                           void* stream) {
-  if (!tok_host || !tok_dev || !x_dev || T < 1 || D % 32 || vocab < 1 || (ple_host && (!ple_dev || LP % 32 || LP < 32)))
+  if (!tok_host || !tok_dev || !x_dev || T < 1 || D < 32 || D % 32 || vocab < 1 ||
+      (ple_host && (!ple_dev || LP % 32 || LP < 32)))
     return op_fail(PF_E_ARG, "bad argument");
   Scope sc;
   void* tt = nullptr;
@@ -410,11 +411,22 @@ extern "C" int pfop_embed(int32_t wtype, const void* tok_host, const void* ple_h
   return PF_OK;
 }
 
+namespace {
+// the copy kernel moves 16-byte vectors on both sides
+bool kv_copy_layout_ok(const void* cache, int64_t cache_seg_halves, const void* image, int64_t img_seg_bytes,
+                       int64_t copy_bytes) {
+  return ((reinterpret_cast<uintptr_t>(cache) | reinterpret_cast<uintptr_t>(image)) % 16) == 0 &&
+         cache_seg_halves % 8 == 0 && img_seg_bytes % 16 == 0 && copy_bytes % 16 == 0;
+}
+}  // namespace
+
 extern "C" int pfop_kv_copy(int32_t dir, void* cache_dev, int64_t cache_seg_halves, void* image_dev,
                             int64_t img_seg_bytes, int32_t n_seg, int64_t copy_bytes, const int32_t* header4,
                             void* stream) {
   if (!cache_dev || !image_dev || n_seg < 0 || copy_bytes < 0 || (dir != 0 && dir != 1))
     return op_fail(PF_E_ARG, "bad argument");
+  if (!kv_copy_layout_ok(cache_dev, cache_seg_halves, image_dev, img_seg_bytes, copy_bytes))
+    return op_fail(PF_E_ARG, "KV copy layout not 16-byte aligned");
   const int32_t zero[4] = {0, 0, 0, 0};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   OP_CUDA(launch_kv_copy(dir, static_cast<__half*>(cache_dev), cache_seg_halves, static_cast<uint8_t*>(image_dev),
@@ -505,6 +517,8 @@ extern "C" int pfop_kv_copy_bench(int32_t dir, void* cache_dev, int64_t cache_se
   if (!cache_dev || !image_dev || !us || n_seg < 0 || copy_bytes < 0 || (dir != 0 && dir != 1) || iters < 1 ||
       warmup < 0 || scrub_bytes < 0)
     return op_fail(PF_E_ARG, "bad argument");
+  if (!kv_copy_layout_ok(cache_dev, cache_seg_halves, image_dev, img_seg_bytes, copy_bytes))
+    return op_fail(PF_E_ARG, "KV copy layout not 16-byte aligned");
   const int32_t hdr[4] = {0, 0, 0, 0};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return time_launches(

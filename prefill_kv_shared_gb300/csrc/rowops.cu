@@ -229,8 +229,9 @@ __global__ void __launch_bounds__(256) kv_copy_kernel(int dir, uint4* __restrict
 
 cudaError_t launch_kv_copy(int dir, __half* cache, int64_t cache_seg_stride, uint8_t* image, int64_t img_seg_bytes,
                            int n_seg, int64_t copy_bytes, const int32_t header[4], cudaStream_t s) {
+  // both sides move 16-byte vectors
   if (copy_bytes % 16 != 0 || img_seg_bytes % 16 != 0 || cache_seg_stride % 8 != 0 ||
-      reinterpret_cast<uintptr_t>(image) % 16 != 0)
+      ((reinterpret_cast<uintptr_t>(image) | reinterpret_cast<uintptr_t>(cache)) % 16) != 0)
     return cudaErrorInvalidValue;
   const int64_t copy_vec = copy_bytes / 16;
   const int64_t n_vec = copy_vec * n_seg;

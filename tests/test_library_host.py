@@ -251,3 +251,17 @@ def test_attention_entry_points_refuse_empty_head_counts(lib):
             assert lib.pfop_attention_bench(mode, fake, fake, fake, 1, hq, hkv, 64, 0, 1, fake, None, 0, 0, 1,
                                             C.byref(us), None) == binding.PF_E_ARG
         assert lib.pfop_attention_split_noalloc(fake, fake, fake, hq, hkv, 64, 0, 1, fake, None) == binding.PF_E_ARG
+
+
+@pytest.mark.parametrize("cache_off,img_off,cache_seg,img_seg,copy", [
+    (8, 0, 256, 512, 512), (0, 4, 256, 512, 512), (0, 0, 252, 512, 512), (0, 0, 256, 520, 512),
+    (0, 0, 256, 512, 504)])
+def test_kv_copy_refuses_unaligned_layouts(lib, cache_off, img_off, cache_seg, img_seg, copy):
+    """The KV copy kernel moves 16-byte vectors: misaligned pointers, cache
+    strides or byte counts are argument errors, found before any CUDA call."""
+    import ctypes as C
+    base = 1 << 20  # never dereferenced
+    us = C.c_float(0.0)
+    args = (C.c_void_p(base + cache_off), cache_seg, C.c_void_p(base + img_off), img_seg, 2, copy)
+    assert lib.pfop_kv_copy(1, *args, None, None) == binding.PF_E_ARG
+    assert lib.pfop_kv_copy_bench(1, *args, None, 0, 0, 1, C.byref(us), None) == binding.PF_E_ARG
