@@ -106,7 +106,10 @@ typedef struct prefill_weights {
   const prefill_layer_weights* layers; /* [n_layer] */
 } prefill_weights;
 
-/* Build a context on the current CUDA device: validates the description,
+/* Build a context on the current CUDA device.  All contexts of one process
+   must use the same device: the kernels' shared-memory opt-in is made once
+   per process, on the device of the first launch (run one process per GPU,
+   as the replicas do).  Validates the description,
    uploads and repacks the weights, allocates the FP16 KV cache
    (2 x writing layers x max_ctx x kv_dim) and the activation buffers for
    ubatch_max rows.  cuda_stream: a cudaStream_t or NULL.  On failure *out is
