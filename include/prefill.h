@@ -130,8 +130,8 @@ int prefill_create(const prefill_model_desc* desc, const prefill_weights* weight
    prefill_sync).  pos0 must equal the context's position count (ubatches
    continue the sequence), and pos0 + n_tokens <= max_ctx, 1 <= n_tokens <=
    ubatch_max.  is_last: this ubatch ends the prompt; its last row's logits
-   (fp32 [vocab], device memory) are written to `logits`, which may be NULL
-   otherwise.  With pruning active, a non-final ubatch runs only the writing
+   (fp32 [vocab]) are written to `logits`, which must then be device (or
+   managed) memory, else PF_E_ARG, and may be NULL otherwise.  With pruning active, a non-final ubatch runs only the writing
    layers.  Enqueue only: call prefill_sync to wait. */
 int prefill_ubatch(prefill_ctx* ctx, const int32_t* tokens, int32_t n_tokens, int64_t pos0, int32_t is_last,
                    float* logits);

@@ -536,6 +536,8 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
   if (pos0 != c->n_pos) return fail(c, PF_E_ARG, "pos0 must equal the cached position count");
   if (pos0 + T > c->d.max_ctx) return fail(c, PF_E_ARG, "positions would exceed max_ctx");
   if (is_last && !logits) return fail(c, PF_E_ARG, "logits is null on the last ubatch");
+  // the head kernel writes the logits: they must be device (or managed) memory
+  if (is_last && !is_device_ptr(logits)) return fail(c, PF_E_ARG, "logits is not device memory");
   cudaStream_t s = c->stream;
   if (is_device_ptr(tokens)) {
     PF_CUDA(c, cudaMemcpyAsync(c->tok, tokens, T * 4, cudaMemcpyDeviceToDevice, s));

@@ -198,6 +198,9 @@ def test_errors_leave_state(gpu, tiny):
     with pytest.raises(binding.PrefillError) as e:
         ctx.ubatch(tok[20:40], 20, True, None)      # last ubatch without logits
     assert e.value.code == binding.PF_E_ARG and ctx.n_pos == 20
+    with pytest.raises(binding.PrefillError) as e:   # logits in host memory
+        ctx.ubatch(tok[20:40], 20, True, np.empty(cfg["vocab"], dtype=np.float32))
+    assert e.value.code == binding.PF_E_ARG and ctx.n_pos == 20
     ctx.ubatch(tok[20:40], 20, True, logits)
     with pytest.raises(binding.PrefillError) as e:
         ctx.ubatch(synth.make_tokens(cfg, 25), 40, True, logits)   # 40 + 25 > max_ctx 64
