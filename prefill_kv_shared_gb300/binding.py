@@ -158,6 +158,26 @@ def _ptr(a) -> int | None:
     return a.data_ptr()
 
 
+def _buffer(a, what: str, dtype: str | None = None, min_elems: int = 0) -> int | None:
+    """Byte size of a numpy array or torch tensor handed to the library (None
+    for a raw address), after checking what the library cannot see behind a
+    pointer: contiguity, element type and element count."""
+    if a is None or isinstance(a, int):
+        return None
+    if isinstance(a, np.ndarray):
+        ok, n, dt, nbytes = a.flags["C_CONTIGUOUS"], a.size, str(a.dtype), a.nbytes
+    else:
+        ok, n, dt = a.is_contiguous(), a.numel(), str(a.dtype).replace("torch.", "")
+        nbytes = n * a.element_size()
+    if not ok:
+        raise ValueError(f"{what}: buffer must be contiguous")
+    if dtype is not None and dt != dtype:
+        raise ValueError(f"{what}: element type must be {dtype}, got {dt}")
+    if n < min_elems:
+        raise ValueError(f"{what}: needs at least {min_elems} elements, got {n}")
+    return nbytes
+
+
 def _stream(stream) -> int | None:
     if stream is None:
         return None
@@ -288,7 +308,10 @@ class PrefillContext:
             tokens = np.ascontiguousarray(tokens, dtype=np.int32)
             n = len(tokens)
         else:
+            _buffer(tokens, "tokens", "int32")
             n = tokens.numel()
+        if is_last:
+            _buffer(logits, "logits", "float32", self.cfg["vocab"])
         self._check(self._lib.prefill_ubatch(self._h, _ptr(tokens), n, pos0, 1 if is_last else 0,
                                              _ptr(logits)))
 
@@ -313,9 +336,15 @@ class PrefillContext:
         return int(self._lib.prefill_kv_image_bytes(self._h, n_pos))
 
     def kv_save(self, dst, nbytes: int):
+        size = _buffer(dst, "dst")
+        if size is not None and nbytes > size:
+            raise ValueError(f"dst: nbytes {nbytes} exceeds the buffer's {size} bytes")
         self._check(self._lib.kv_save(self._h, _ptr(dst), nbytes))
 
     def kv_load(self, src, nbytes: int, n_pos: int):
+        size = _buffer(src, "src")
+        if size is not None and nbytes > size:
+            raise ValueError(f"src: nbytes {nbytes} exceeds the buffer's {size} bytes")
         self._check(self._lib.kv_load(self._h, _ptr(src), nbytes, n_pos))
 
     def kv_save_file(self, path: str):

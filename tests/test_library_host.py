@@ -265,3 +265,19 @@ def test_kv_copy_refuses_unaligned_layouts(lib, cache_off, img_off, cache_seg, i
     args = (C.c_void_p(base + cache_off), cache_seg, C.c_void_p(base + img_off), img_seg, 2, copy)
     assert lib.pfop_kv_copy(1, *args, None, None) == binding.PF_E_ARG
     assert lib.pfop_kv_copy_bench(1, *args, None, 0, 0, 1, C.byref(us), None) == binding.PF_E_ARG
+
+
+def test_binding_checks_buffers_it_can_see():
+    """The binding refuses buffers the library could overrun behind a bare
+    pointer: wrong element type, too few elements, non-contiguous views."""
+    import numpy as np
+    import torch
+    assert binding._buffer(None, "x") is None and binding._buffer(4096, "x") is None
+    assert binding._buffer(np.zeros(10, np.float32), "x", "float32", 10) == 40
+    assert binding._buffer(torch.zeros(10, dtype=torch.int32), "x", "int32") == 40
+    bad = [(np.zeros(10, np.float64), "float32", 10), (np.zeros(9, np.float32), "float32", 10),
+           (np.zeros((4, 4), np.float32)[:, 0], "float32", 4), (torch.zeros(10, dtype=torch.int64), "int32", 0),
+           (torch.zeros(4, 4)[:, 1], "float32", 4)]
+    for arr, dt, n in bad:
+        with pytest.raises(ValueError):
+            binding._buffer(arr, "x", dt, n)
