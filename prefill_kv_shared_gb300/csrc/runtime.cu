@@ -12,6 +12,8 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
@@ -110,6 +112,16 @@ struct prefill_ctx {
 namespace {
 
 thread_local std::string g_last_error;
+
+// A named range for profilers (ncu --nvtx --nvtx-include, nsys): one per
+// ubatch, one per layer, one for the head and for each KV image copy.
+// Without a tool attached a push/pop is a cheap no-op.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 int fail(prefill_ctx* c, int code, const std::string& msg) {
   if (c)
@@ -538,6 +550,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
   if (is_last && !logits) return fail(c, PF_E_ARG, "logits is null on the last ubatch");
   // the head kernel writes the logits: they must be device (or managed) memory
   if (is_last && !is_device_ptr(logits)) return fail(c, PF_E_ARG, "logits is not device memory");
+  NvtxRange r_ubatch(is_last ? "ubatch (last)" : "ubatch");
   cudaStream_t s = c->stream;
   if (is_device_ptr(tokens)) {
     PF_CUDA(c, cudaMemcpyAsync(c->tok, tokens, T * 4, cudaMemcpyDeviceToDevice, s));
@@ -581,6 +594,9 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
 
   for (int il = 0; il < L; ++il) {
     const LayerW& W = c->layers[il];
+    char range_name[32];
+    std::snprintf(range_name, sizeof range_name, "layer %d", il);
+    NvtxRange r_layer(range_name);
     if (prune && il == S) {
       if (!is_last) {
         break;
@@ -711,6 +727,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
     }
   }
   if (is_last) {
+    NvtxRange r_head("head");
     const int row = gathered ? 0 : T - 1;
     PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, D * 6.0, [&] {
                return launch_rmsnorm(xcur, row, 1, D, c->out_norm, c->d.rms_eps, c->y, nullptr, s);
@@ -780,6 +797,7 @@ extern "C" int prefill_kv_header_check(const void* header16, int32_t n_layers_wr
 
 extern "C" int kv_save(prefill_ctx* c, void* dst, size_t dst_bytes) {
   if (!c || !dst) return fail(c, PF_E_ARG, "null argument");
+  NvtxRange r_save("kv_save");
   const int64_t n = c->n_pos;
   const int64_t need = prefill_kv_image_bytes(c, n);
   if (static_cast<int64_t>(dst_bytes) < need) return fail(c, PF_E_ARG, "destination smaller than the image");
@@ -810,6 +828,7 @@ extern "C" int kv_save(prefill_ctx* c, void* dst, size_t dst_bytes) {
 
 extern "C" int kv_load(prefill_ctx* c, const void* src, size_t src_bytes, int64_t n_pos) {
   if (!c || !src) return fail(c, PF_E_ARG, "null argument");
+  NvtxRange r_load("kv_load");
   const bool dev = is_device_ptr(src);
   uint8_t hdr[16] = {0};
   if (src_bytes >= 16) {
