@@ -414,6 +414,53 @@ def run_prefix_reuse(dev, stream):
 
 
 # ---------------------------------------------------------------------------
+# per-class roofline fractions from a run with CUDA events around every launch
+
+CLASS_BOUNDS = {"gemm": "tensor", "attention": "tensor", "norm": "hbm", "other": "hbm", "gemm_row": "hbm",
+                "attention_row": "hbm"}
+
+
+def class_fractions(stats, steps, peaks):
+    """Per launch class: launches and device ms per step, achieved rate and
+    its fraction of the measured peak (tensor classes: algorithmic FLOPs
+    against the burst bf16 peak, since every launch is timed on its own;
+    HBM classes: algorithmic bytes against the measured copy bandwidth)."""
+    peak_t = peaks["bf16_tflops"]
+    out = {}
+    for k, v in stats.items():
+        d = {"bound": CLASS_BOUNDS.get(k, "hbm"), "launches_per_step": v["launches"] / steps,
+             "ms_per_step": v["ms"] / steps,
+             "tflops": (v["flops"] / (v["ms"] * 1e-3) / 1e12) if v["ms"] > 0 and v["flops"] > 0 else None,
+             "gbs": (v["bytes"] / (v["ms"] * 1e-3) / 1e9) if v["ms"] > 0 else None}
+        if d["bound"] == "tensor":
+            d["frac"] = d["tflops"] / peak_t if d["tflops"] else None
+        else:
+            d["frac"] = d["gbs"] / peaks["hbm_gbs"] if d["gbs"] else None
+        out[k] = d
+    return out
+
+
+def pass_fraction(stats, steps, peaks, pass_ms):
+    """Whole-pass roofline fraction: the sum over launch classes of
+    max(FLOPs / bf16 peak, bytes / HBM bandwidth), over the measured pass."""
+    ideal_ms = sum(max(v["flops"] / (peaks["bf16_tflops"] * 1e12), v["bytes"] / (peaks["hbm_gbs"] * 1e9))
+                   for v in stats.values()) * 1e3 / steps
+    return ideal_ms / pass_ms
+
+
+def timed_classes(ctx, step, steps):
+    """Run `steps` steps with per-launch event timing; the context's stats."""
+    ctx.reset_stats()
+    ctx.set_timing(True)
+    for _ in range(steps):
+        step()
+    st = ctx.stats()
+    ctx.set_timing(False)
+    ctx.reset_stats()
+    return st
+
+
+# ---------------------------------------------------------------------------
 # our arm
 
 
@@ -490,13 +537,7 @@ def run_ours(args, dist: Dist):
 
     # the same steps again with CUDA events around every launch: per-class
     # device time and algorithmic work
-    ctx.reset_stats()
-    ctx.set_timing(True)
-    for _ in range(args.steps):
-        step()
-    st = ctx.stats()
-    ctx.set_timing(False)
-    ctx.reset_stats()
+    st = timed_classes(ctx, step, args.steps)
     launches_per_step = sum(v["launches"] for v in st.values()) / args.steps
 
     peaks, peak_src = load_peaks()
@@ -504,34 +545,18 @@ def run_ours(args, dist: Dist):
     gemm_ms_avg = g["ms"] / max(g["timed"], 1)
     gemm_flops_avg = g["flops"] / max(g["launches"], 1)
     achieved = gemm_flops_avg / (gemm_ms_avg * 1e-3) / 1e12 if gemm_ms_avg > 0 else None
-    peak = peaks["bf16_tflops_sustained"]
+    peak = peaks["bf16_tflops"]
     traffic = gemm_traffic()
-    bounds = {"gemm": "tensor", "attention": "tensor", "norm": "hbm", "other": "hbm", "gemm_row": "hbm",
-              "attention_row": "hbm"}
-
-    def cls(k, v):
-        d = {"bound": bounds.get(k, "hbm"), "launches_per_step": v["launches"] / args.steps,
-             "ms_per_step": v["ms"] / args.steps,
-             "tflops": (v["flops"] / (v["ms"] * 1e-3) / 1e12) if v["ms"] > 0 and v["flops"] > 0 else None,
-             "gbs": (v["bytes"] / (v["ms"] * 1e-3) / 1e9) if v["ms"] > 0 else None}
-        if d["bound"] == "tensor":
-            d["frac"] = d["tflops"] / peak if d["tflops"] else None
-        else:
-            d["frac"] = d["gbs"] / peaks["hbm_gbs"] if d["gbs"] else None
-        return d
-
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": (achieved / peak) if achieved else None, "traffic": traffic,
                 "kernel": "gemm_tc_kernel, projections of the 512-row ubatch (launches of more than 16 rows)",
-                "peak_source": f"{peak_src} bf16 sustained",
-                "classes": {k: cls(k, v) for k, v in st.items()},
+                "peak_source": f"{peak_src} bf16 burst (each launch timed on its own)",
+                "classes": class_fractions(st, args.steps, peaks),
                 "class_note": ("per-launch CUDA events around every launch (PDL overlap removed); gemm_row = the "
-                               "single-row projections after pruning and the LM head, bound by their weight bytes; "
-                               "attention_row = the single-row attention of the KV-shared layers")}
-    # whole-pass roofline: sum over classes of max(flops/P, bytes/BW)
-    ideal_ms = sum(max(v["flops"] / (peaks["bf16_tflops_sustained"] * 1e12),
-                       v["bytes"] / (peaks["hbm_gbs"] * 1e9)) for v in st.values()) * 1e3 / args.steps
-    roofline["pass_frac"] = ideal_ms / ms
+                               "one-row projections (the output row of the KV-shared layers and the LM head), "
+                               "bound by their weight bytes; attention_row = the single-row attention of the "
+                               "KV-shared layers")}
+    roofline["pass_frac"] = pass_fraction(st, args.steps, peaks, ms)
 
     # end to end through the C ABI with host buffers: tokens from pinned host
     # memory each step, logits read back to pinned host memory each step
@@ -558,13 +583,15 @@ def run_ours(args, dist: Dist):
     ctx.close()
 
     # pruning on/off: E2B at 512/2048/8192/32768 (ubatches of 512) and E4B at
-    # 8192 (ubatches of 1024), rank 0's GPU only
+    # 8192 and 32768 (ubatches of 1024), rank 0's GPU only; each entry with
+    # its class fractions from one more pass with every launch timed
     sweep = None
     if not args.no_sweep and dist.rank == 0:
         sweep = {}
         models = {"e2b": w}
+        peaks = load_peaks()[0]
         for mname, n, ub in (("e2b", 512, 512), ("e2b", 2048, 512), ("e2b", 8192, 512), ("e2b", 32768, 512),
-                             ("e4b", 8192, 1024)):
+                             ("e4b", 8192, 1024), ("e4b", 32768, 1024)):
             if mname not in models:
                 models.clear()  # one model's weights resident at a time
                 models[mname] = synth.make_weights(synth.config(mname))
@@ -590,7 +617,13 @@ def run_ours(args, dist: Dist):
                 b.record(stream)
                 torch.cuda.synchronize(dev)
                 sms = a.elapsed_time(b) / steps_n
-                sweep[f"{key}_{'on' if prune else 'off'}"] = {"ms": sms, "tokens_per_s": n / (sms * 1e-3)}
+                st_n = timed_classes(big, sweep_step, 1)
+                cl = class_fractions(st_n, 1, peaks)
+                sweep[f"{key}_{'on' if prune else 'off'}"] = {
+                    "ms": sms, "tokens_per_s": n / (sms * 1e-3), "ubatch": ub,
+                    "pass_frac": pass_fraction(st_n, 1, peaks, sms),
+                    "frac": {k: cl[k]["frac"] for k in ("gemm", "attention", "gemm_row", "attention_row", "norm")},
+                    "class_ms": {k: cl[k]["ms_per_step"] for k in cl}}
             sweep[f"{key}_speedup"] = sweep[f"{key}_off"]["ms"] / sweep[f"{key}_on"]["ms"]
             big.close()
             del t, lg

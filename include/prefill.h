@@ -106,7 +106,11 @@ typedef struct prefill_weights {
   const prefill_layer_weights* layers; /* [n_layer] */
 } prefill_weights;
 
-/* Build a context on the current CUDA device.  All contexts of one process
+/* Build a context on the current CUDA device.  (The model the pass runs:
+   "llama.cpp Gemma 4 prefill KV graph optimization", section 1: writing
+   layers below n_layer_kv_from_start, KV-shared layers from it up that
+   read kv_src's cache; the pruning condition of that section's listing is
+   evaluated from prune_shared_enable, n_seq_max and embeddings.)  All contexts of one process
    must use the same device: the kernels' shared-memory opt-in is made once
    per process, on the device of the first launch (run one process per GPU,
    as the replicas do).  Validates the description,
@@ -125,6 +129,10 @@ int prefill_create(const prefill_model_desc* desc, const prefill_weights* weight
                    prefill_ctx** out);
 
 /* Run one ubatch of n_tokens tokens at positions pos0 .. pos0+n_tokens-1.
+   ("llama.cpp Gemma 4 prefill KV graph optimization", section 1: every row
+   passes the writing layers; before the first KV-shared layer the rows no
+   output needs are dropped, so an intermediate ubatch stops there and the
+   final ubatch carries only its last row through the KV-shared layers.)
    tokens: host memory (validated on the host: PF_E_ARG on an id outside
    [0, vocab)) or device memory (validated on the device: PF_E_DEVICE_TOKEN at
    prefill_sync).  pos0 must equal the context's position count (ubatches
@@ -142,7 +150,9 @@ int prefill_sync(prefill_ctx* ctx);
 /* Positions currently in the cache. */
 int64_t prefill_n_pos(const prefill_ctx* ctx);
 
-/* Forget the sequence (position count 0); the cache memory is kept. */
+/* Forget the sequence (position count 0); the cache memory is kept.  (The
+   fallback of "PicoLM KV Cache persistence", "rules": a request whose
+   prefix cannot be restored starts from an empty cache.) */
 int prefill_reset(prefill_ctx* ctx);
 
 /* Switch pruning on or off for later ubatches (the A/B switch); the pruning
@@ -152,17 +162,28 @@ int prefill_set_prune(prefill_ctx* ctx, int32_t enable);
 int prefill_prune_active(const prefill_ctx* ctx);
 
 /* Size in bytes of a KV image of n_pos positions for this model:
-   16-byte header + 2 * writing_layers * n_pos * kv_dim * 2. */
+   16-byte header + 2 * writing_layers * n_pos * kv_dim * 2.  ("PicoLM KV
+   Cache persistence", "file": a header, then the FP16 keys and values of
+   the cached positions of every layer; 25 positions of a 22-layer,
+   kv_dim-256 model are about 550 KB.)  -1 for a NULL context or n_pos < 0. */
 int64_t prefill_kv_image_bytes(const prefill_ctx* ctx, int64_t n_pos);
 
-/* Write the cache's first prefill_n_pos() positions as a KV image to dst
+/* ("PicoLM KV Cache persistence", "usage" and "file": after the prompt
+   prefix has been prefilled its FP16 cache is saved, to be restored by
+   later runs with the same prefix; "rules": only prompt positions are
+   saved, never generated ones.)
+   Write the cache's first prefill_n_pos() positions as a KV image to dst
    (device or host memory, 16-byte aligned, dst_bytes >= the image size).
    Image: "KVCP", int32 n_pos, int32 writing layers, int32 kv_dim (little
    endian), then FP16 keys [layer][pos][kv_dim], then FP16 values.  Only
    prompt positions are ever in the cache. */
 int kv_save(prefill_ctx* ctx, void* dst, size_t dst_bytes);
 
-/* Restore the first n_pos positions of a KV image (device or host memory; a
+/* ("PicoLM KV Cache persistence", "usage": a saved prefix is restored and
+   its positions are skipped by the next prefill; "rules": the image must
+   match the model's layers and kv_dim, the restored count may not exceed
+   the image or the context, and a refused image means a full prefill.)
+   Restore the first n_pos positions of a KV image (device or host memory; a
    device image 16-byte aligned, else PF_E_ARG) and set the position count
    to n_pos; the next ubatch continues at n_pos.  A
    wrong magic (PF_E_KV_MAGIC), a layer/kv_dim mismatch (PF_E_KV_SHAPE), or
@@ -220,8 +241,14 @@ int prefill_set_timing(prefill_ctx* ctx, int32_t enable);
 int prefill_get_stats(prefill_ctx* ctx, prefill_stats* out);
 int prefill_reset_stats(prefill_ctx* ctx);
 
+/* Free the context: waits for its stream, then releases the weights, the
+   KV cache and every buffer it holds.  NULL is ignored.  (The library's
+   own resource handling; the pages describe no counterpart.) */
 void prefill_destroy(prefill_ctx* ctx);
 
+/* Message of the last failed call on ctx (or, with ctx NULL, of the last
+   failed prefill_create on this thread).  The returned string stays valid
+   until the next call on the same context. */
 const char* prefill_last_error(const prefill_ctx* ctx);
 
 /* ---- host-only helpers (no GPU needed) ---- */

@@ -137,7 +137,10 @@ int pfop_kv_copy_bench(int32_t dir, void* cache_dev, int64_t cache_seg_halves, v
    the library, kept until exit.  A call needs Hq*R*(hd+4) floats, R being
    the number of key ranges of pfop_attention's mode 1 (at most 148/Hkv), plus
    4 for an error word: up to 8 query heads of 256 fit at any length;
-   larger requests return PF_E_ARG without touching the GPU.  All calls share
+   larger requests return PF_E_ARG without touching the GPU, and so do
+   shapes the kernels do not take (head_dim other than 64 or 256, n_head not
+   a multiple of n_head_kv, a group size not dividing 16, q/k/v not 16-byte
+   aligned).  All calls share
    the array, so calls that overlap on the GPU race: order them on one stream
    or with events.  The first call on a device looks up the array's device
    address with that device current (cudaGetSymbolAddress); make that first

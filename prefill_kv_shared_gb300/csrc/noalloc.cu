@@ -72,6 +72,13 @@ extern "C" int pfop_attention_split_noalloc(const void* q_dev, const void* k_dev
                                             void* stream) {
   if (!q_dev || !k_dev || !v_dev || !out_dev || pos < 0 || pos >= kv_len || Hq < 1 || Hkv < 1)
     return fail(PF_E_ARG, "bad argument");
+  // the shapes and alignments the kernels take, refused here before any GPU work
+  if (hd != 64 && hd != 256) return fail(PF_E_ARG, "head_dim must be 64 or 256");
+  if (Hq % Hkv != 0 || Hq / Hkv > 16 || 16 % (Hq / Hkv) != 0)
+    return fail(PF_E_ARG, "n_head must be a multiple of n_head_kv with a group size dividing 16");
+  if ((reinterpret_cast<uintptr_t>(q_dev) | reinterpret_cast<uintptr_t>(k_dev) | reinterpret_cast<uintptr_t>(v_dev)) &
+      15)
+    return fail(PF_E_ARG, "q, k and v must be 16-byte aligned");
   const size_t need = pf::attn_split_partials_floats(Hq, Hkv, hd, pos);
   if (need > PF_NOALLOC_SCRATCH_FLOATS - 4)
     return fail(PF_E_ARG, "request needs " + std::to_string(need) + " scratch floats; the fixed array holds " +

@@ -1,10 +1,11 @@
 """Whole prefill through the C ABI against the CPU oracle.
 
-Acceptance: the output row's logits within 2e-2 * max|oracle logit| with the
-same argmax (when the oracle's top two are further apart than twice that
-tolerance; otherwise the GPU's argmax must be one of the oracle's logits
-within the tolerance of the top), and the pruned pass bit-identical to the
-unpruned one."""
+Acceptance: the output row's logits within 2e-2 * max|oracle logit| and the
+same argmax as the oracle, and the pruned pass bit-identical to the
+unpruned one.  Every model-level comparison records the GPU and oracle
+argmax, the oracle's top-two gap and the error (printed, and appended as a
+JSON line to the file named by PF_PARITY_LOG when that is set)."""
+import json
 import os
 
 import numpy as np
@@ -19,18 +20,23 @@ pytestmark = pytest.mark.gpu
 TOL = 2e-2
 
 
-def check_logits(got, want):
+def check_logits(got, want, case=""):
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
     assert np.isfinite(got).all()
     tol = TOL * np.abs(want).max()
     err = np.abs(got - want).max()
-    assert err <= tol, f"max|err| {err:.4g} > {tol:.4g}"
     top = np.sort(want)[::-1]
-    if top[0] - top[1] > 2 * tol:
-        assert int(np.argmax(got)) == int(np.argmax(want))
-    else:
-        assert want[int(np.argmax(got))] >= top[0] - tol
+    rec = {"case": case, "gpu_argmax": int(np.argmax(got)), "oracle_argmax": int(np.argmax(want)),
+           "oracle_top2_gap": float(top[0] - top[1]), "max_err": float(err), "tol": float(tol),
+           "gpu_logit_at_oracle_argmax": float(got[int(np.argmax(want))])}
+    print("parity", json.dumps(rec))
+    path = os.environ.get("PF_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(rec) + "\n")
+    assert err <= tol, f"max|err| {err:.4g} > {tol:.4g} ({rec})"
+    assert rec["gpu_argmax"] == rec["oracle_argmax"], f"argmax differs from the oracle's ({rec})"
     return err / np.abs(want).max()
 
 
@@ -76,7 +82,7 @@ def test_tiny_matches_oracle(gpu, tiny):
     want = OracleContext(tiny.cfg, tiny, 128).ubatch(tok, True)
     on = run_gpu(tiny, tok, 64, True)
     off = run_gpu(tiny, tok, 64, False)
-    check_logits(on, want)
+    check_logits(on, want, "tiny-64")
     np.testing.assert_array_equal(on, off)
 
 
@@ -85,7 +91,7 @@ def test_tiny_ubatches_and_ragged(gpu, tiny):
     want = OracleContext(tiny.cfg, tiny, 128).prefill(tok, 16)
     on = run_gpu(tiny, tok, 16, True, max_ctx=128)
     off = run_gpu(tiny, tok, 16, False, max_ctx=128)
-    check_logits(on, want)
+    check_logits(on, want, "tiny-61-ragged")
     np.testing.assert_array_equal(on, off)
 
 
@@ -113,7 +119,38 @@ def test_e2b_512_matches_oracle(gpu, e2b):
     off = run_gpu(e2b, tok, 512, False)
     np.testing.assert_array_equal(on, off)
     want = OracleContext(e2b.cfg, e2b, 512).ubatch(tok, True, prune=True)
-    check_logits(on, want)
+    check_logits(on, want, "e2b-512")
+
+
+def test_e2b_2048_matches_oracle(gpu, e2b):
+    """Four ubatches of 512: the first three stop before the KV-shared
+    layers, the last carries one row through them.  Against the oracle's
+    plain definition (every row through every layer), run once."""
+    tok = synth.make_tokens(e2b.cfg, 2048)
+    on = run_gpu(e2b, tok, 512, True)
+    want = OracleContext(e2b.cfg, e2b, 2048).prefill(tok, 512, prune=False)
+    check_logits(on, want, "e2b-2048")
+
+
+@pytest.fixture(scope="module")
+def e4b_scaled():
+    # full E4B widths (d_model 2560, 8/2 heads of 256, GeGLU 10240, vocab
+    # 32768, per-layer embedding 256), 6 layers: 0-3 write, 4 and 5 read
+    # the last writing layer of their parity (2 and 3)
+    return synth.make_weights(synth.scaled_config("e4b", n_layer=6, n_layer_kv_from_start=4))
+
+
+def test_e4b_scaled_matches_oracle(gpu, e4b_scaled):
+    """Two KV heads and the parity rule for the KV source, in ubatches of
+    1024 (the first stops before the KV-shared layers)."""
+    w = e4b_scaled
+    assert w.cfg["kv_src"] == [-1, -1, -1, -1, 2, 3]
+    tok = synth.make_tokens(w.cfg, 2048)
+    on = run_gpu(w, tok, 1024, True)
+    off = run_gpu(w, tok, 1024, False)
+    np.testing.assert_array_equal(on, off)
+    want = OracleContext(w.cfg, w, 2048).prefill(tok, 1024, prune=False)
+    check_logits(on, want, "e4b-scaled-6L-2048")
 
 
 @pytest.mark.parametrize("n", [2048, 8192, 32768])
@@ -125,11 +162,16 @@ def test_e2b_prune_bit_identical(gpu, e2b, n):
     np.testing.assert_array_equal(on, off)
 
 
-def test_e4b_8192_prune_bit_identical(gpu):
-    w = synth.make_weights(synth.config("e4b"))
-    tok = synth.make_tokens(w.cfg, 8192)
-    on = run_gpu(w, tok, 1024, True)
-    off = run_gpu(w, tok, 1024, False)
+@pytest.fixture(scope="module")
+def e4b():
+    return synth.make_weights(synth.config("e4b"))
+
+
+@pytest.mark.parametrize("n", [8192, 32768])
+def test_e4b_prune_bit_identical(gpu, e4b, n):
+    tok = synth.make_tokens(e4b.cfg, n)
+    on = run_gpu(e4b, tok, 1024, True)
+    off = run_gpu(e4b, tok, 1024, False)
     assert np.isfinite(on).all()
     np.testing.assert_array_equal(on, off)
 
@@ -173,8 +215,56 @@ def test_kv_restore_suffix_equals_full(gpu, tinyllama):
         assert np.abs(got - full).max() <= 2e-3 * np.abs(full).max()
         o2 = OracleContext(cfg, tinyllama, 532)
         o2.kv_load(orc.kv_save(), 500)
-        check_logits(got, o2.ubatch(suffix, True))
+        check_logits(got, o2.ubatch(suffix, True), f"tinyllama-500+32 suffix {i}")
     ctx.close()
+
+
+def test_kv_image_matches_oracle_image(gpu, tiny):
+    """The GPU's KV image of a prefill against the oracle's image of the same
+    prefill: the same header bytes, and a body whose FP16 keys and values
+    (layer, position, element in the image's order) agree within the
+    rounding the two computations differ by."""
+    cfg = tiny.cfg
+    tok = synth.make_tokens(cfg, 64)
+    ctx = binding.PrefillContext(tiny, max_ctx=64, ubatch_max=64)
+    ctx.ubatch(tok, 0, False)
+    ctx.sync()
+    n = ctx.kv_image_bytes(64)
+    img = np.empty(n, dtype=np.uint8)
+    ctx.kv_save(img, n)
+    ctx.close()
+    orc = OracleContext(cfg, tiny, 64)
+    orc.ubatch(tok, False)
+    want = np.frombuffer(orc.kv_save(), dtype=np.uint8)
+    assert len(want) == n
+    np.testing.assert_array_equal(img[:16], want[:16])
+    got_b = img[16:].view(np.float16).astype(np.float64)
+    want_b = want[16:].view(np.float16).astype(np.float64)
+    assert np.abs(got_b - want_b).max() <= 2e-2 * np.abs(want_b).max()
+
+
+def test_kv_partial_restore_matches_oracle_bytes(gpu, tiny):
+    """Restore the first 3 positions of a 5-position image and save again:
+    the GPU writes the same bytes as the oracle (a layout that put each
+    layer's keys and values together would pick other positions)."""
+    cfg = tiny.cfg
+    L_w, kv = cfg["n_layer_kv_from_start"], cfg["n_head_kv"] * cfg["head_dim"]
+    rng = np.random.default_rng(11)
+    body = rng.normal(0, 1, 2 * L_w * 5 * kv).astype(np.float16)
+    src = b"KVCP" + np.array([5, L_w, kv], dtype="<i4").tobytes() + body.tobytes()
+    orc = OracleContext(cfg, tiny, 16)
+    orc.kv_load(src, 3)
+    want = orc.kv_save()
+    ctx = binding.PrefillContext(tiny, max_ctx=16, ubatch_max=16)
+    arr = np.frombuffer(src, dtype=np.uint8).copy()
+    dev = torch.from_numpy(arr).cuda()
+    ctx.kv_load(dev, len(arr), 3)
+    n = ctx.kv_image_bytes(3)
+    out = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    ctx.kv_save(out, n)
+    ctx.sync()
+    ctx.close()
+    assert out.cpu().numpy().tobytes() == want
 
 
 def test_errors_leave_state(gpu, tiny):
@@ -302,4 +392,4 @@ def test_decode_steps_match_oracle(gpu, tiny, e2b, name):
         np.testing.assert_array_equal(a, b)
     for i in range(steps):
         want = orc.ubatch(tok[n0 + i:n0 + i + 1], True)
-        check_logits(outs[True][i], want)
+        check_logits(outs[True][i], want, f"{name} decode step {i}")

@@ -236,6 +236,47 @@ def test_kv_image_size_matches_article():
     assert round((got - 16) / 1024) == 550
 
 
+def _kv_fixture():
+    """The worked-example image of tests/golden/kv_image_small.txt, assembled
+    in the fixture's own row order, and its cache contents by position."""
+    rows = _golden_lines("kv_image_small.txt")
+    hdr = {r[0]: r[1] for r in rows if r[0] not in ("K", "V")}
+    n, L, kv = int(hdr["n_pos"]), int(hdr["n_layers"]), int(hdr["kv_dim"])
+    body = [r for r in rows if r[0] in ("K", "V")]
+    img = hdr["magic"].encode() + struct.pack("<iii", n, L, kv)
+    cache = {"K": np.zeros((L, n, kv)), "V": np.zeros((L, n, kv))}
+    for r in body:
+        vals = [float(x) for x in r[3:]]
+        assert len(vals) == kv
+        img += np.array(vals, dtype="<f2").tobytes()
+        cache[r[0]][int(r[1]), int(r[2])] = vals
+    return img, n, L, kv, cache
+
+
+def _kv_oracle(L, kv, max_ctx):
+    cfg = dict(n_layer=L + 1, n_layer_kv_from_start=L, n_head=2, n_head_kv=1, head_dim=kv)
+    return OracleContext(cfg, None, max_ctx)
+
+
+def test_kv_image_layout_matches_worked_example():
+    """The oracle's image is byte for byte the worked example (keys of every
+    layer and position first, then values), and restoring a prefix of it
+    reads back those positions."""
+    img, n, L, kv, cache = _kv_fixture()
+    o = _kv_oracle(L, kv, 8)
+    o.K[:, :n, 0, :] = cache["K"]
+    o.V[:, :n, 0, :] = cache["V"]
+    o.n_pos = n
+    assert o.kv_save() == img
+    assert len(img) == oracle.kv_image_bytes(L, n, kv)
+    r = _kv_oracle(L, kv, 8)
+    r.kv_load(img, 2)
+    assert r.n_pos == 2
+    np.testing.assert_array_equal(r.K[:, :2, 0, :].astype(np.float64), cache["K"][:, :2])
+    np.testing.assert_array_equal(r.V[:, :2, 0, :].astype(np.float64), cache["V"][:, :2])
+    assert not r.K[:, 2:].any() and not r.V[:, 2:].any()
+
+
 # ---------------------------------------------------------------------------
 # whole model on a micro configuration
 
