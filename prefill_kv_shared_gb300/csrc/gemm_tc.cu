@@ -1079,30 +1079,63 @@ constexpr int GV_WARPS = 8;
 constexpr int GV_THREADS = GV_WARPS * 32;
 constexpr int GV_TARGET_CTAS = 304;  // about two CTAs per SM
 
+// Two fp32 lanes in one 64-bit register pair, for the packed arithmetic
+// of sm_100-class SMs (sub.rn.f32x2 / fma.rn.f32x2: one instruction for two
+// independent fp32 operations, each rounded as its scalar form would be).
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(unsigned long long v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
 // sum over one 32-element Q4_0 block: byte j holds element j (low nibble)
 // and element j + 16 (high nibble); x: the block's 32 activations.  A
 // nibble n becomes the float 2^23 + n by placing it under the exponent byte
 // of 2^23 (one byte permute, no integer-to-float conversion), and
-// (2^23 + n) - (2^23 + 8) = n - 8 exactly.
+// (2^23 + n) - (2^23 + 8) = n - 8 exactly.  The subtraction and the
+// multiply-add run two elements per instruction (packed f32x2) on two
+// chains: the even and the odd elements of each group of four, added at
+// the end.
 __device__ __forceinline__ float q4_block_dot(uint4 nib, const float* x) {
   const uint32_t wds[4] = {nib.x, nib.y, nib.z, nib.w};
-  constexpr float bias = 8388616.0f;  // 2^23 + 8
-  float s = 0.f;
+  const unsigned long long bias = f2_pack(8388616.0f, 8388616.0f);  // 2^23 + 8
+  unsigned long long s = 0ull;  // (+0, +0)
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const float4 xl = *reinterpret_cast<const float4*>(x + 4 * q);
     const float4 xh = *reinterpret_cast<const float4*>(x + 16 + 4 * q);
     const uint32_t lo = wds[q] & 0x0F0F0F0Fu, hi = (wds[q] >> 4) & 0x0F0F0F0Fu;
-    s = fmaf(__int_as_float(__byte_perm(lo, 0x4B000000u, 0x7440)) - bias, xl.x, s);
-    s = fmaf(__int_as_float(__byte_perm(lo, 0x4B000000u, 0x7441)) - bias, xl.y, s);
-    s = fmaf(__int_as_float(__byte_perm(lo, 0x4B000000u, 0x7442)) - bias, xl.z, s);
-    s = fmaf(__int_as_float(__byte_perm(lo, 0x4B000000u, 0x7443)) - bias, xl.w, s);
-    s = fmaf(__int_as_float(__byte_perm(hi, 0x4B000000u, 0x7440)) - bias, xh.x, s);
-    s = fmaf(__int_as_float(__byte_perm(hi, 0x4B000000u, 0x7441)) - bias, xh.y, s);
-    s = fmaf(__int_as_float(__byte_perm(hi, 0x4B000000u, 0x7442)) - bias, xh.z, s);
-    s = fmaf(__int_as_float(__byte_perm(hi, 0x4B000000u, 0x7443)) - bias, xh.w, s);
+    const unsigned long long l01 = f2_pack(__int_as_float(__byte_perm(lo, 0x4B000000u, 0x7440)),
+                                           __int_as_float(__byte_perm(lo, 0x4B000000u, 0x7441)));
+    const unsigned long long l23 = f2_pack(__int_as_float(__byte_perm(lo, 0x4B000000u, 0x7442)),
+                                           __int_as_float(__byte_perm(lo, 0x4B000000u, 0x7443)));
+    const unsigned long long h01 = f2_pack(__int_as_float(__byte_perm(hi, 0x4B000000u, 0x7440)),
+                                           __int_as_float(__byte_perm(hi, 0x4B000000u, 0x7441)));
+    const unsigned long long h23 = f2_pack(__int_as_float(__byte_perm(hi, 0x4B000000u, 0x7442)),
+                                           __int_as_float(__byte_perm(hi, 0x4B000000u, 0x7443)));
+    s = f2_fma(f2_sub(l01, bias), f2_pack(xl.x, xl.y), s);
+    s = f2_fma(f2_sub(l23, bias), f2_pack(xl.z, xl.w), s);
+    s = f2_fma(f2_sub(h01, bias), f2_pack(xh.x, xh.y), s);
+    s = f2_fma(f2_sub(h23, bias), f2_pack(xh.z, xh.w), s);
   }
-  return s;
+  const float2 r = f2_unpack(s);
+  return r.x + r.y;
 }
 
 template <int WK, int BN>

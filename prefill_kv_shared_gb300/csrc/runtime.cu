@@ -35,18 +35,24 @@ struct DevBuf {
 struct LayerW {
   WeightMat qkv;  // writing layers: [Wq; Wk; Wv]; KV-shared layers: Wq
   WeightMat o, gu, down, pg, pp;
-  // KV-shared layers: the same matrices in 64-row tiles with the same k-split,
-  // for the single-row launches after pruning (more CTAs; a row's result
-  // does not depend on the tile width, so the pruned row keeps its bits)
-  WeightMat o1, gu1, down1, pp1;
   float* attn_norm = nullptr;
   float* ffn_norm = nullptr;
 };
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
-// the weight a launch of M rows uses: the single-row copy when there is one
-const WeightMat& pick(const WeightMat& full, const WeightMat& one, int M) { return M == 1 && one.dev ? one : full; }
+// The epilogue of a projection moved from its launch's row 0 to row r: the
+// outputs, the per-layer-embedding multipliers and the Q rows advance by r
+// rows, and the position (RoPE angle, K/V cache row) by r.
+EpiParams shift_rows(const EpiParams& e, int r) {
+  EpiParams s = e;
+  if (s.out_f32) s.out_f32 += static_cast<size_t>(r) * s.ld_f32;
+  if (s.out_bf16) s.out_bf16 += static_cast<size_t>(r) * s.ld_bf16;
+  if (s.ple) s.ple += static_cast<size_t>(r) * s.ple_stride;
+  if (s.q_out) s.q_out += static_cast<size_t>(r) * s.q_dim;
+  s.pos0 += r;
+  return s;
+}
 
 }  // namespace
 
@@ -376,12 +382,7 @@ extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weig
                                                     C->Hkv, C->hd, row_bytes(wt, C->D), QKV_BN);
       if ((rc = build_weight(C, L.qkv, rows, C->D, QKV_BN))) return fail(nullptr, rc, C->last_error);
     }
-    // KV-shared layers of a model that can prune also get 64-row copies
-    const bool single_row_copies = !writes && C->S > 0 && C->D % 64 == 0 && C->F % 32 == 0;
     if ((rc = build_weight(C, L.o, plain_rows(lw.wo, C->D, C->q, wt, 128), C->q, 128)))
-      return fail(nullptr, rc, C->last_error);
-    if (single_row_copies &&
-        (rc = build_weight(C, L.o1, plain_rows(lw.wo, C->D, C->q, wt, 64), C->q, 64, L.o.split)))
       return fail(nullptr, rc, C->last_error);
     {
       // gate/up interleaved per tile: BN/2 gate rows, then the same BN/2 up rows
@@ -397,13 +398,8 @@ extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weig
       };
       const int bn = C->F % 128 == 0 ? 256 : 128;
       if ((rc = build_weight(C, L.gu, gu_rows(bn), C->D, bn))) return fail(nullptr, rc, C->last_error);
-      if (single_row_copies && (rc = build_weight(C, L.gu1, gu_rows(64), C->D, 64, L.gu.split)))
-        return fail(nullptr, rc, C->last_error);
     }
     if ((rc = build_weight(C, L.down, plain_rows(lw.w_down, C->D, C->F, wt, 128), C->F, 128)))
-      return fail(nullptr, rc, C->last_error);
-    if (single_row_copies &&
-        (rc = build_weight(C, L.down1, plain_rows(lw.w_down, C->D, C->F, wt, 64), C->F, 64, L.down.split)))
       return fail(nullptr, rc, C->last_error);
     if (C->P > 0) {
       // the PLE gate has few output rows: 64-row tiles give it more CTAs
@@ -411,9 +407,6 @@ extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weig
       if ((rc = build_weight(C, L.pg, plain_rows(lw.ple_gate, C->P, C->D, wt, bn_pg), C->D, bn_pg)))
         return fail(nullptr, rc, C->last_error);
       if ((rc = build_weight(C, L.pp, plain_rows(lw.ple_proj, C->D, C->P, wt, 128), C->P, 128)))
-        return fail(nullptr, rc, C->last_error);
-      if (single_row_copies &&
-          (rc = build_weight(C, L.pp1, plain_rows(lw.ple_proj, C->D, C->P, wt, 64), C->P, 64, L.pp.split)))
         return fail(nullptr, rc, C->last_error);
     }
     if ((rc = upload(C, &L.attn_norm, lw.attn_norm, C->D * 4))) return fail(nullptr, rc, C->last_error);
@@ -440,7 +433,7 @@ extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weig
     size_t fl = gemv_scratch_floats(C->head);
     int tiles = C->head.N_rows / C->head.BN;
     for (const LayerW& L : C->layers)
-      for (const WeightMat* m : {&L.qkv, &L.o, &L.gu, &L.down, &L.pg, &L.pp, &L.o1, &L.gu1, &L.down1, &L.pp1}) {
+      for (const WeightMat* m : {&L.qkv, &L.o, &L.gu, &L.down, &L.pg, &L.pp}) {
         if (!m->dev) continue;
         fl = std::max(fl, gemv_scratch_floats(*m));
         tiles = std::max(tiles, m->N_rows / m->BN);
@@ -585,11 +578,29 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
   int pos_base = static_cast<int>(pos0);
   const __nv_bfloat16* ple_view = c->ple;
   bool gathered = false;
-  // A one-token ubatch streams its projections (launch_gemv); larger ones
-  // use the tensor cores, also for the pruned output row, whose launches
-  // must match the unpruned ones.
-  auto proj = [&](const ActMat& A, int rows, const WeightMat& Wm, const EpiParams& e) {
-    return T == 1 ? launch_gemv(A, Wm, e, c->gv_sums, c->gv_tickets, s) : launch_gemm(A, rows, Wm, e, c->err, s);
+  // One projection of a layer over the launch's `rows` rows.  With
+  // `out_row`, the last row streams through the one-row kernel
+  // (launch_gemv) and the rows before it (if any) take the tensor cores;
+  // otherwise every row takes the tensor cores.  The output row of a
+  // KV-shared layer in the final ubatch takes the one-row kernel in both
+  // pruning modes (alone after the pruning, beside the other rows without
+  // it), so its bits do not depend on the mode; a one-token ubatch (a decode
+  // step) takes it in every layer.  Work counted per row: flops_row FLOPs and
+  // io_row activation bytes, plus the weight bytes once per launch.
+  auto project = [&](const ActMat& A, int rows, bool out_row, const WeightMat& Wm, const EpiParams& e,
+                     double flops_row, double io_row, double wbytes) -> cudaError_t {
+    const int m_tc = out_row ? rows - 1 : rows;
+    if (m_tc > 0) {
+      const cudaError_t err = counted(c, gemm_class(m_tc), 1, flops_row * m_tc, wbytes + io_row * m_tc,
+                                      [&] { return launch_gemm(A, m_tc, Wm, e, c->err, s); });
+      if (err != cudaSuccess) return err;
+    }
+    if (!out_row) return cudaSuccess;
+    ActMat a1 = A;
+    a1.dev = A.dev + static_cast<size_t>(rows - 1) * A.K;
+    const EpiParams e1 = shift_rows(e, rows - 1);
+    return counted(c, PF_KC_GEMM_ROW, 1, flops_row, wbytes + io_row,
+                   [&] { return launch_gemv(a1, Wm, e1, c->gv_sums, c->gv_tickets, s); });
   };
 
   for (int il = 0; il < L; ++il) {
@@ -617,6 +628,9 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
     }
     const bool writes = il < S;
     const int src = writes ? il : c->kv_src[il];
+    // the output row of a KV-shared layer in the final ubatch, and the one
+    // row of a one-row launch, take the single-row kernels (see project)
+    const bool out_row = M == 1 || (!writes && is_last);
     {
       EpiParams e;
       e.kind = EPI_QKV;
@@ -629,8 +643,8 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.k_cache = c->cache + static_cast<size_t>(il) * seg;
       e.v_cache = c->cache + static_cast<size_t>(c->L_w + il) * seg;
       const double n_out = c->q + 2.0 * e.kv_dim;
-      PF_CUDA(c, counted(c, gemm_class(M), 1, 2.0 * M * n_out * D, M * D * 2.0 + gemm_wbytes(c, n_out, D) + M * n_out * 2.0,
-                         [&] { return proj(c->a_y, M, W.qkv, e); }));
+      PF_CUDA(c, project(c->a_y, M, out_row, W.qkv, e, 2.0 * n_out * D, D * 2.0 + n_out * 2.0,
+                         gemm_wbytes(c, n_out, D)));
     }
     {
       AttnArgs a;
@@ -645,11 +659,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       a.pos_base = pos_base;
       a.kv_len = kv_len;
       a.err = c->err;
-      // The output row of a KV-shared layer in the final ubatch goes through
-      // the single-row kernels in both modes (alone after the pruning, after
-      // the other rows without it), so its bits do not depend on the mode.
-      // A one-row ubatch (a decode step) takes them in every layer.
-      const bool out_row = M == 1 || (!writes && is_last);
+      // the output row takes the single-row attention, as in project()
       const int m_rest = out_row ? M - 1 : M;  // rows for the prefill kernels
       if (m_rest > 0) {
         AttnArgs r = a;
@@ -678,8 +688,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.N = D;
       e.out_f32 = xcur;
       e.ld_f32 = D;
-      PF_CUDA(c, counted(c, gemm_class(M), 1, 2.0 * M * D * c->q, M * c->q * 2.0 + gemm_wbytes(c, D, c->q) + M * D * 8.0,
-                         [&] { return proj(c->a_att, M, pick(W.o, W.o1, M), e); }));
+      PF_CUDA(c, project(c->a_att, M, out_row, W.o, e, 2.0 * D * c->q, c->q * 2.0 + D * 8.0, gemm_wbytes(c, D, c->q)));
     }
     PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, M * D * 6.0, [&] {
                return launch_rmsnorm(xcur, 0, M, D, W.ffn_norm, c->d.rms_eps, c->y, nullptr, s);
@@ -691,8 +700,8 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.out_bf16 = c->h;
       e.ld_bf16 = c->F;
       e.act = c->d.ffn_kind == PF_FFN_GEGLU ? 0 : 1;
-      PF_CUDA(c, counted(c, gemm_class(M), 1, 4.0 * M * c->F * D, M * D * 2.0 + gemm_wbytes(c, 2.0 * c->F, D) + M * c->F * 2.0,
-                         [&] { return proj(c->a_y, M, pick(W.gu, W.gu1, M), e); }));
+      PF_CUDA(c, project(c->a_y, M, out_row, W.gu, e, 4.0 * c->F * D, D * 2.0 + c->F * 2.0,
+                         gemm_wbytes(c, 2.0 * c->F, D)));
     }
     {
       EpiParams e;
@@ -704,8 +713,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
         e.out_bf16 = c->xb;
         e.ld_bf16 = D;
       }
-      PF_CUDA(c, counted(c, gemm_class(M), 1, 2.0 * M * D * c->F, M * c->F * 2.0 + gemm_wbytes(c, D, c->F) + M * D * 8.0,
-                         [&] { return proj(c->a_h, M, pick(W.down, W.down1, M), e); }));
+      PF_CUDA(c, project(c->a_h, M, out_row, W.down, e, 2.0 * D * c->F, c->F * 2.0 + D * 8.0, gemm_wbytes(c, D, c->F)));
     }
     if (c->P > 0) {
       EpiParams e;
@@ -715,15 +723,13 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.ld_bf16 = c->P;
       e.ple = ple_view + static_cast<size_t>(il) * c->P;
       e.ple_stride = LP;
-      PF_CUDA(c, counted(c, gemm_class(M), 1, 2.0 * M * c->P * D, M * D * 2.0 + gemm_wbytes(c, c->P, D) + M * c->P * 4.0,
-                         [&] { return proj(c->a_xb, M, W.pg, e); }));
+      PF_CUDA(c, project(c->a_xb, M, out_row, W.pg, e, 2.0 * c->P * D, D * 2.0 + c->P * 4.0, gemm_wbytes(c, c->P, D)));
       EpiParams r;
       r.kind = EPI_RESID;
       r.N = D;
       r.out_f32 = xcur;
       r.ld_f32 = D;
-      PF_CUDA(c, counted(c, gemm_class(M), 1, 2.0 * M * D * c->P, M * c->P * 2.0 + gemm_wbytes(c, D, c->P) + M * D * 8.0,
-                         [&] { return proj(c->a_pg, M, pick(W.pp, W.pp1, M), r); }));
+      PF_CUDA(c, project(c->a_pg, M, out_row, W.pp, r, 2.0 * D * c->P, c->P * 2.0 + D * 8.0, gemm_wbytes(c, D, c->P)));
     }
   }
   if (is_last) {
