@@ -413,6 +413,29 @@ def run_prefix_reuse(dev, stream):
     return out
 
 
+def run_cache_cli():
+    """The command-line cache-file flow (PicoLM KV cache article, "usage" and
+    "measured": a 25-token TinyLlama prompt, first run without the file,
+    then a run that restores it), 16 generated tokens each; wall-clock
+    seconds of each run after the weights are built (host work included)."""
+    import io
+    import tempfile
+
+    from prefill_kv_shared_gb300 import cli, synth
+    w = synth.make_weights(synth.config("tinyllama"))
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "prompt.kvcp")
+        args = cli.parse_args(["--prompt-tokens", "25", "--cache", path, "--gen", "16"])
+        cli.run(args, weights=w, out=io.StringIO())  # warm-up (writes the file)
+        os.remove(path)
+        full = cli.run(args, weights=w, out=io.StringIO())
+        cached = cli.run(args, weights=w, out=io.StringIO())
+    return {"prompt_tokens": 25, "generated": 16, "file_bytes": full.get("cache_bytes"),
+            "full_run_s": full["run_s"], "cached_run_s": cached["run_s"], "restored": cached["restored"],
+            "same_tokens": full["generated"] == cached["generated"],
+            "note": "wall clock of cli.run after the weights exist: create, restore or prefill, save, generation"}
+
+
 # ---------------------------------------------------------------------------
 # per-class roofline fractions from a run with CUDA events around every launch
 
@@ -584,7 +607,10 @@ def run_ours(args, dist: Dist):
 
     # pruning on/off: E2B at 512/2048/8192/32768 (ubatches of 512) and E4B at
     # 8192 and 32768 (ubatches of 1024), rank 0's GPU only; each entry with
-    # its class fractions from one more pass with every launch timed
+    # its class fractions from one more pass with every launch timed.  "off"
+    # keeps the output row of the KV-shared layers on the single-row kernels
+    # (logits bit-identical to "on"); "off_plain" runs every row through the
+    # prefill kernels (the fastest unpruned pass).
     sweep = None
     if not args.no_sweep and dist.rank == 0:
         sweep = {}
@@ -601,8 +627,9 @@ def run_ours(args, dist: Dist):
             t = torch.from_numpy(synth.make_tokens(wm.cfg, n)).to(dev)
             key = f"{n}" if mname == "e2b" else f"{mname}_{n}"
             steps_n = args.sweep_steps if n <= 8192 else max(2, args.sweep_steps // 2)
-            for prune in (True, False):
+            for prune in (True, False, binding.PF_PRUNE_OFF_PLAIN):
                 big.set_prune(prune)
+                tag = "off_plain" if prune is binding.PF_PRUNE_OFF_PLAIN else ("on" if prune else "off")
 
                 def sweep_step():
                     big.reset()
@@ -619,12 +646,13 @@ def run_ours(args, dist: Dist):
                 sms = a.elapsed_time(b) / steps_n
                 st_n = timed_classes(big, sweep_step, 1)
                 cl = class_fractions(st_n, 1, peaks)
-                sweep[f"{key}_{'on' if prune else 'off'}"] = {
+                sweep[f"{key}_{tag}"] = {
                     "ms": sms, "tokens_per_s": n / (sms * 1e-3), "ubatch": ub,
                     "pass_frac": pass_fraction(st_n, 1, peaks, sms),
                     "frac": {k: cl[k]["frac"] for k in ("gemm", "attention", "gemm_row", "attention_row", "norm")},
                     "class_ms": {k: cl[k]["ms_per_step"] for k in cl}}
             sweep[f"{key}_speedup"] = sweep[f"{key}_off"]["ms"] / sweep[f"{key}_on"]["ms"]
+            sweep[f"{key}_speedup_vs_plain"] = sweep[f"{key}_off_plain"]["ms"] / sweep[f"{key}_on"]["ms"]
             big.close()
             del t, lg
         models.clear()
@@ -673,6 +701,10 @@ def run_ours(args, dist: Dist):
             sweep["prefix_reuse_tinyllama"] = run_prefix_reuse(dev, stream)
         except Exception as e:  # recorded, never fatal to the line
             sweep["prefix_reuse_tinyllama"] = {"error": f"{type(e).__name__}: {e}"}
+        try:
+            sweep["cache_file_cli_tinyllama_25"] = run_cache_cli()
+        except Exception as e:  # recorded, never fatal to the line
+            sweep["cache_file_cli_tinyllama_25"] = {"error": f"{type(e).__name__}: {e}"}
 
     if dist.rank == 0:
         line = {

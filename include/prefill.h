@@ -157,7 +157,21 @@ int prefill_reset(prefill_ctx* ctx);
 
 /* Switch pruning on or off for later ubatches (the A/B switch); the pruning
    condition itself still has to hold.  prefill_prune_active() says whether
-   ubatches are pruned with the current settings. */
+   ubatches are pruned with the current settings.
+     PF_PRUNE_ON:        prune when the condition holds (the default when the
+                         description's prune_shared_enable is nonzero);
+     PF_PRUNE_OFF:       every row passes every layer; in the KV-shared layers
+                         of the final ubatch the output row takes the same
+                         single-row kernels as with pruning, so its logits are
+                         bit-identical to the pruned pass's;
+     PF_PRUNE_OFF_PLAIN: every row passes every layer through the prefill
+                         kernels (the fastest unpruned pass; the output row's
+                         logits then differ from the pruned pass's in
+                         rounding).
+   Any other value is PF_E_ARG. */
+#define PF_PRUNE_OFF 0
+#define PF_PRUNE_ON 1
+#define PF_PRUNE_OFF_PLAIN 2
 int prefill_set_prune(prefill_ctx* ctx, int32_t enable);
 int prefill_prune_active(const prefill_ctx* ctx);
 

@@ -26,6 +26,10 @@ PF_E_DEVICE_TOKEN = -7
 PF_E_NOMEM = -8
 PF_E_IO = -9
 
+PF_PRUNE_OFF = 0
+PF_PRUNE_ON = 1
+PF_PRUNE_OFF_PLAIN = 2
+
 PF_W_F32 = 0
 PF_W_Q4_0 = 2
 PF_FFN_GEGLU = 0
@@ -325,8 +329,10 @@ class PrefillContext:
     def n_pos(self) -> int:
         return int(self._lib.prefill_n_pos(self._h))
 
-    def set_prune(self, enable: bool):
-        self._check(self._lib.prefill_set_prune(self._h, 1 if enable else 0))
+    def set_prune(self, enable):
+        """True / PF_PRUNE_ON, False / PF_PRUNE_OFF, or PF_PRUNE_OFF_PLAIN."""
+        mode = enable if isinstance(enable, int) and not isinstance(enable, bool) else (1 if enable else 0)
+        self._check(self._lib.prefill_set_prune(self._h, mode))
 
     @property
     def prune_active(self) -> bool:

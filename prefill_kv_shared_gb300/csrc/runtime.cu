@@ -86,7 +86,7 @@ struct prefill_ctx {
   ActMat a_y, a_att, a_h, a_xb, a_pg;
 
   int64_t n_pos = 0;
-  int prune_enable = 1;
+  int prune_enable = 1;  // PF_PRUNE_ON / PF_PRUNE_OFF / PF_PRUNE_OFF_PLAIN
   std::string last_error;
 
   // launch accounting
@@ -553,7 +553,10 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
     PF_CUDA(c, cudaMemcpyAsync(c->tok, tokens, T * 4, cudaMemcpyHostToDevice, s));
   }
 
-  const bool prune = predicate(c->d, c->prune_enable);
+  const bool prune = predicate(c->d, c->prune_enable == PF_PRUNE_ON);
+  // the output row of the KV-shared layers takes the single-row kernels
+  // unless the plain unpruned pass was asked for
+  const bool row_kernels = c->prune_enable != PF_PRUNE_OFF_PLAIN;
   const int L = c->L, S = c->S, D = c->D, LP = L * c->P;
   const int kv_len = static_cast<int>(pos0) + T;
   const size_t seg = static_cast<size_t>(c->d.max_ctx) * c->kv;
@@ -630,7 +633,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
     const int src = writes ? il : c->kv_src[il];
     // the output row of a KV-shared layer in the final ubatch, and the one
     // row of a one-row launch, take the single-row kernels (see project)
-    const bool out_row = M == 1 || (!writes && is_last);
+    const bool out_row = M == 1 || (!writes && is_last && row_kernels);
     {
       EpiParams e;
       e.kind = EPI_QKV;
@@ -766,11 +769,15 @@ extern "C" int prefill_reset(prefill_ctx* c) {
 
 extern "C" int prefill_set_prune(prefill_ctx* c, int32_t enable) {
   if (!c) return fail(nullptr, PF_E_ARG, "null context");
-  c->prune_enable = enable ? 1 : 0;
+  if (enable != PF_PRUNE_OFF && enable != PF_PRUNE_ON && enable != PF_PRUNE_OFF_PLAIN)
+    return fail(c, PF_E_ARG, "pruning mode must be PF_PRUNE_OFF, PF_PRUNE_ON or PF_PRUNE_OFF_PLAIN");
+  c->prune_enable = enable;
   return PF_OK;
 }
 
-extern "C" int prefill_prune_active(const prefill_ctx* c) { return c ? (predicate(c->d, c->prune_enable) ? 1 : 0) : 0; }
+extern "C" int prefill_prune_active(const prefill_ctx* c) {
+  return c ? (predicate(c->d, c->prune_enable == PF_PRUNE_ON) ? 1 : 0) : 0;
+}
 
 // ---------------------------------------------------------------------------
 // KV image

@@ -41,10 +41,13 @@ def check_logits(got, want, case=""):
 
 
 def run_gpu(weights, tokens, ubatch, prune, max_ctx=None, ctx=None):
+    """prune: True, False or binding.PF_PRUNE_OFF_PLAIN."""
     cfg = weights.cfg
     own = ctx is None
     if own:
-        ctx = binding.PrefillContext(weights, max_ctx=max_ctx or len(tokens), ubatch_max=ubatch, prune=prune)
+        ctx = binding.PrefillContext(weights, max_ctx=max_ctx or len(tokens), ubatch_max=ubatch, prune=bool(prune))
+        if prune is binding.PF_PRUNE_OFF_PLAIN:
+            ctx.set_prune(prune)
     logits = torch.empty(cfg["vocab"], dtype=torch.float32, device="cuda")
     chunks = synth.split_ubatches(tokens, ubatch)
     pos = ctx.n_pos
@@ -120,6 +123,10 @@ def test_e2b_512_matches_oracle(gpu, e2b):
     np.testing.assert_array_equal(on, off)
     want = OracleContext(e2b.cfg, e2b, 512).ubatch(tok, True, prune=True)
     check_logits(on, want, "e2b-512")
+    # the plain unpruned pass (every row through the prefill kernels) meets
+    # the same acceptance; its bits may differ from the pruned pass's
+    plain = run_gpu(e2b, tok, 512, binding.PF_PRUNE_OFF_PLAIN)
+    check_logits(plain, want, "e2b-512 plain unpruned")
 
 
 def test_e2b_2048_matches_oracle(gpu, e2b):
@@ -393,3 +400,40 @@ def test_decode_steps_match_oracle(gpu, tiny, e2b, name):
     for i in range(steps):
         want = orc.ubatch(tok[n0 + i:n0 + i + 1], True)
         check_logits(outs[True][i], want, f"{name} decode step {i}")
+
+
+def test_cli_cache_file_flow(gpu, tinyllama, tmp_path):
+    """The command-line flow of the PicoLM cache article on the TinyLlama
+    shape with a 25-token prompt: the first run prefills and writes the
+    cache file, whose body is the article's 2 x 22 x 25 x 256 x 2 bytes
+    (tests/golden/kv_image_size.txt); the second run restores 24 positions
+    from it and prefills the last token, with the same first generated token
+    and logits to rounding; a damaged file is refused and rewritten."""
+    import io
+
+    from prefill_kv_shared_gb300 import cli
+    pin = {}
+    with open(os.path.join(os.path.dirname(__file__), "golden", "kv_image_size.txt")) as f:
+        for ln in f:
+            if ln.strip() and not ln.startswith("#"):
+                k, v = ln.split()
+                pin[k] = int(v)
+    path = str(tmp_path / "prompt.kvcp")
+    args = cli.parse_args(["--model", "tinyllama", "--prompt-tokens", str(pin["n_pos"]), "--cache", path,
+                           "--gen", "4"])
+    log = io.StringIO()
+    first = cli.run(args, weights=tinyllama, out=log)
+    assert first["restored"] == 0
+    assert os.path.getsize(path) - 16 == pin["body_bytes"]
+    second = cli.run(args, weights=tinyllama, out=log)
+    assert second["restored"] == pin["n_pos"] - 1
+    assert "restored 24 prompt positions" in log.getvalue()
+    assert second["first_token"] == first["first_token"]
+    assert second["generated"] == first["generated"]
+    a, b = first["logits"], second["logits"]
+    assert np.abs(a - b).max() <= 2e-3 * np.abs(a).max()
+    with open(path, "r+b") as f:
+        f.write(b"XXXX")
+    third = cli.run(args, weights=tinyllama, out=log)
+    assert third["restored"] == 0 and "refused" in log.getvalue()
+    assert os.path.getsize(path) - 16 == pin["body_bytes"]
