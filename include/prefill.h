@@ -89,7 +89,13 @@ typedef struct prefill_model_desc {
   int32_t prune_shared_enable; /* 1: prune before the first KV-shared layer when the
                                   condition holds; 0: every row passes every layer */
   int32_t n_seq_max;      /* sequences sharing the context; pruning needs 1 */
-  int32_t embeddings;     /* nonzero: an embeddings output is requested (disables pruning) */
+  int32_t embeddings;     /* nonzero: the embeddings output of every row is requested
+                             (PF_OUT_EMBD of prefill_set_output; disables pruning) */
+  const int32_t* embd_layer_inp; /* NULL, or [n_layer + 1] flags: nonzero at il requests the
+                                    hidden state entering layer il for every row (il ==
+                                    n_layer: the final hidden state, before the output
+                                    norm); copied at create.  A request at any il >=
+                                    n_layer_kv_from_start disables pruning. */
 } prefill_model_desc;
 
 /* host pointers; the library copies (and repacks) everything at create.
@@ -143,6 +149,22 @@ int prefill_create(const prefill_model_desc* desc, const prefill_weights* weight
    layers.  Enqueue only: call prefill_sync to wait. */
 int prefill_ubatch(prefill_ctx* ctx, const int32_t* tokens, int32_t n_tokens, int64_t pos0, int32_t is_last,
                    float* logits);
+
+/* Hidden-state outputs ("llama.cpp Gemma 4 prefill KV graph optimization",
+   section 1 listing: with embeddings requested, or a per-layer input
+   embedding requested for a layer from n_layer_kv_from_start up to the
+   final state, every row is needed there and the pruning is off).
+   which = PF_OUT_EMBD: the embeddings output, rmsnorm(final hidden
+   state) * (1 + out_norm) of every row, fp32 [n_tokens][d_model]; needs
+   desc.embeddings.  which = il in [0, n_layer]: the hidden state entering
+   layer il (il == n_layer: the final one, before the output norm), fp32
+   [n_tokens][d_model]; needs desc.embd_layer_inp[il].  dst: device memory
+   with room for ubatch_max rows (each later ubatch writes its rows from
+   dst[0]), or NULL to clear.  PF_E_ARG for an output the description did not
+   request or a dst that is not device memory; prefill_ubatch refuses
+   (PF_E_ARG) while a requested output has no buffer. */
+#define PF_OUT_EMBD (-1)
+int prefill_set_output(prefill_ctx* ctx, int32_t which, float* dst);
 
 /* Wait for the context's stream and report device-side errors. */
 int prefill_sync(prefill_ctx* ctx);
@@ -268,8 +290,9 @@ const char* prefill_last_error(const prefill_ctx* ctx);
 /* ---- host-only helpers (no GPU needed) ---- */
 
 /* The pruning condition for a description (n_seq_max == 1, no embeddings,
-   0 < n_layer_kv_from_start < n_layer, pruning enabled).  Returns 1 or 0, or
-   PF_E_ARG for a NULL description. */
+   no embd_layer_inp request at a layer from n_layer_kv_from_start to
+   n_layer, 0 < n_layer_kv_from_start < n_layer, pruning enabled).  Returns 1
+   or 0, or PF_E_ARG for a NULL description. */
 int prefill_prune_predicate(const prefill_model_desc* desc);
 
 /* Validate a 16-byte KV image header against a model (writing layers, kv_dim),

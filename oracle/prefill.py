@@ -231,14 +231,21 @@ class OracleContext:
         return x.astype(F32)
 
     # -- one ubatch ----------------------------------------------------------
-    def ubatch(self, tokens: np.ndarray, is_last: bool, prune: bool = False):
+    def ubatch(self, tokens: np.ndarray, is_last: bool, prune: bool = False, embeddings: bool = False,
+               embd_layer_inp=None, capture: dict | None = None):
         """Run one ubatch at positions n_pos .. n_pos+T-1.
 
         prune=False is the plain definition: every row passes every layer.
         prune=True is the pruned ordering: before layer n_layer_kv_from_start
         only the output row (the last row of the last ubatch) is kept, and an
-        intermediate ubatch stops there.  Returns fp32 logits [vocab] of the
-        last row when is_last, else None.
+        intermediate ubatch stops there -- when the pruning condition holds,
+        which embeddings (an embeddings output of every row) and
+        embd_layer_inp (n_layer + 1 flags: the hidden state entering layer il
+        of every row, il == n_layer the final one) can make false.  With
+        `capture` a dict, the requested outputs are stored in it: capture[il]
+        the rows entering layer il (fp32 [T, d_model]), capture["embd"] the
+        embeddings output rmsnorm(final hidden state) * (1 + g_out).  Returns
+        fp32 logits [vocab] of the last row when is_last, else None.
         """
         cfg = self.cfg
         tokens = np.asarray(tokens, dtype=np.int64)
@@ -255,16 +262,27 @@ class OracleContext:
         P = cfg["ple_dim"]
         if P > 0:
             ple = rows_f32(self.w.ple_embd, tokens).reshape(T, self.L, P) * F32(1.0 / math.sqrt(P))
-        pruning = prune and prune_shared(self.L, self.S)
+        pruning = prune and prune_shared(self.L, self.S, embeddings=embeddings,
+                                         embeddings_layer_inp=embd_layer_inp)
+        want = embd_layer_inp if embd_layer_inp is not None else [False] * (self.L + 1)
+        stopped = False
         for il in range(self.L):
             if pruning and il == self.S:
                 if not is_last:
+                    stopped = True
                     break
                 keep = [T - 1]
                 x, pos = x[keep], pos[keep]
                 ple = ple[keep] if ple is not None else None
+            if capture is not None and want[il]:
+                capture[il] = x.copy()
             x = self._layer(il, x, ple, pos, kv_len)
         self.n_pos = kv_len
+        if capture is not None and not stopped:
+            if want[self.L]:
+                capture[self.L] = x.copy()
+            if embeddings:
+                capture["embd"] = rmsnorm(x, self.w.out_norm, cfg["rms_eps"])
         if not is_last:
             return None
         y = rmsnorm(x[-1:], self.w.out_norm, cfg["rms_eps"])

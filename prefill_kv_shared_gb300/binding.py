@@ -26,6 +26,8 @@ PF_E_DEVICE_TOKEN = -7
 PF_E_NOMEM = -8
 PF_E_IO = -9
 
+PF_OUT_EMBD = -1
+
 PF_PRUNE_OFF = 0
 PF_PRUNE_ON = 1
 PF_PRUNE_OFF_PLAIN = 2
@@ -44,7 +46,7 @@ EXPORTS = (
     "pfop_linear_f32", "pfop_linear_resid", "pfop_linear_glu", "pfop_linear_ple", "pfop_linear_qkv",
     "pfop_attention", "pfop_rmsnorm", "pfop_embed", "pfop_kv_copy", "pfop_last_error", "pfop_linear_bench",
     "pfop_attention_split_noalloc", "pfop_attention_bench", "pfop_kv_copy_bench",
-    "kv_save_file", "kv_load_file", "prefill_kv_file_check", "pfop_linear_row",
+    "kv_save_file", "kv_load_file", "prefill_kv_file_check", "pfop_linear_row", "prefill_set_output",
 )
 
 
@@ -62,7 +64,7 @@ class ModelDesc(C.Structure):
         ("ffn_kind", C.c_int32), ("wtype", C.c_int32), ("rms_eps", C.c_float),
         ("rope_base", C.c_float), ("kv_src", C.POINTER(C.c_int32)), ("max_ctx", C.c_int32),
         ("ubatch_max", C.c_int32), ("prune_shared_enable", C.c_int32), ("n_seq_max", C.c_int32),
-        ("embeddings", C.c_int32),
+        ("embeddings", C.c_int32), ("embd_layer_inp", C.POINTER(C.c_int32)),
     ]
 
 
@@ -105,6 +107,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "prefill_create": (C.c_int, [C.POINTER(ModelDesc), C.POINTER(Weights), vp, C.POINTER(vp)]),
         "prefill_ubatch": (C.c_int, [vp, vp, i32, i64, i32, vp]),
         "prefill_sync": (C.c_int, [vp]),
+        "prefill_set_output": (C.c_int, [vp, i32, vp]),
         "prefill_n_pos": (i64, [vp]),
         "prefill_reset": (C.c_int, [vp]),
         "prefill_set_prune": (C.c_int, [vp, i32]),
@@ -200,8 +203,15 @@ def check_op(rc: int):
 
 
 def make_desc(cfg: dict, max_ctx: int, ubatch_max: int, prune: bool = True, n_seq_max: int = 1,
-              embeddings: bool = False):
+              embeddings: bool = False, layer_inp=None):
+    """layer_inp: None, or n_layer + 1 flags requesting the hidden state
+    entering each layer (the last one: the final hidden state)."""
     kv_src = (C.c_int32 * cfg["n_layer"])(*cfg["kv_src"])
+    inp = None
+    if layer_inp is not None:
+        if len(layer_inp) != cfg["n_layer"] + 1:
+            raise ValueError("layer_inp needs n_layer + 1 flags")
+        inp = (C.c_int32 * (cfg["n_layer"] + 1))(*[1 if f else 0 for f in layer_inp])
     d = ModelDesc(
         n_layer=cfg["n_layer"], n_layer_kv_from_start=cfg["n_layer_kv_from_start"],
         d_model=cfg["d_model"], n_head=cfg["n_head"], n_head_kv=cfg["n_head_kv"],
@@ -210,13 +220,15 @@ def make_desc(cfg: dict, max_ctx: int, ubatch_max: int, prune: bool = True, n_se
         wtype=PF_W_Q4_0 if cfg["wtype"] == "q4_0" else PF_W_F32, rms_eps=cfg["rms_eps"],
         rope_base=cfg["rope_base"], kv_src=C.cast(kv_src, C.POINTER(C.c_int32)), max_ctx=max_ctx,
         ubatch_max=ubatch_max, prune_shared_enable=1 if prune else 0, n_seq_max=n_seq_max,
-        embeddings=1 if embeddings else 0)
-    d._keep = kv_src
+        embeddings=1 if embeddings else 0,
+        embd_layer_inp=C.cast(inp, C.POINTER(C.c_int32)) if inp is not None else None)
+    d._keep = (kv_src, inp)
     return d
 
 
-def prune_predicate(cfg: dict, prune: bool = True, n_seq_max: int = 1, embeddings: bool = False) -> bool:
-    d = make_desc(cfg, 16, 16, prune, n_seq_max, embeddings)
+def prune_predicate(cfg: dict, prune: bool = True, n_seq_max: int = 1, embeddings: bool = False,
+                    layer_inp=None) -> bool:
+    d = make_desc(cfg, 16, 16, prune, n_seq_max, embeddings, layer_inp)
     rc = load().prefill_prune_predicate(C.byref(d))
     if rc < 0:
         raise PrefillError(rc, "bad description")
@@ -270,11 +282,11 @@ class PrefillContext:
     """One sequence on the current CUDA device (see prefill.h)."""
 
     def __init__(self, weights, max_ctx: int, ubatch_max: int, prune: bool = True, stream=None,
-                 n_seq_max: int = 1, embeddings: bool = False):
+                 n_seq_max: int = 1, embeddings: bool = False, layer_inp=None):
         lib = load()
         cfg = weights.cfg
         self.cfg = cfg
-        self._desc = make_desc(cfg, max_ctx, ubatch_max, prune, n_seq_max, embeddings)
+        self._desc = make_desc(cfg, max_ctx, ubatch_max, prune, n_seq_max, embeddings, layer_inp)
         keep = []
 
         def p(a):
@@ -318,6 +330,14 @@ class PrefillContext:
             _buffer(logits, "logits", "float32", self.cfg["vocab"])
         self._check(self._lib.prefill_ubatch(self._h, _ptr(tokens), n, pos0, 1 if is_last else 0,
                                              _ptr(logits)))
+
+    def set_output(self, which: int, dst):
+        """Hidden-state output buffer: which = PF_OUT_EMBD (the embeddings
+        output) or a layer index in [0, n_layer]; dst an fp32 device tensor
+        with ubatch_max x d_model elements, or None."""
+        if dst is not None:
+            _buffer(dst, "dst", "float32")
+        self._check(self._lib.prefill_set_output(self._h, which, _ptr(dst)))
 
     def sync(self):
         self._check(self._lib.prefill_sync(self._h))

@@ -149,9 +149,10 @@ struct EmbedArgs {
 };
 cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t s);
 
-// y[i] = rmsnorm(x[row0 + i]) * (1 + g) for i < M; optionally x_copy[i] = x[row0 + i]
+// y[i] = rmsnorm(x[row0 + i]) * (1 + g) for i < M as bf16 (y) and/or fp32
+// (y32); optionally x_copy[i] = x[row0 + i].  Null outputs are skipped.
 cudaError_t launch_rmsnorm(const float* x, int row0, int M, int D, const float* g, float eps,
-                           __nv_bfloat16* y, float* x_copy, cudaStream_t s);
+                           __nv_bfloat16* y, float* x_copy, cudaStream_t s, float* y32 = nullptr);
 
 // KV image body <-> cache.  n_seg segments (keys of each writing layer, then
 // values); each copies copy_bytes, from/to the cache at seg * cache_seg_stride

@@ -104,10 +104,12 @@ constexpr int NORM_THREADS = 128;
 // same either way.
 constexpr int NORM_VEC = 8;
 
+// Outputs (each optional): y bf16 (the next projection's operand), y32 fp32
+// (the embeddings output), x_copy (the input rows themselves).
 __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(const float* __restrict__ x, int row0, int D,
                                                                const float* __restrict__ gain, float eps,
                                                                __nv_bfloat16* __restrict__ y,
-                                                               float* __restrict__ x_copy) {
+                                                               float* __restrict__ x_copy, float* __restrict__ y32) {
   __shared__ float red[NORM_THREADS / 32];
   pdl_launch();
   pdl_wait();
@@ -150,15 +152,19 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(const float* __re
   for (int w = 1; w < NORM_THREADS / 32; ++w) tot = __fadd_rn(tot, red[w]);
   const float r = rsqrtf(__fadd_rn(__fdiv_rn(tot, static_cast<float>(D)), eps));
   const float4* g4 = reinterpret_cast<const float4*>(gain);
-  __nv_bfloat16* yr = y + (size_t)i * D;
   auto emit = [&](int v, const float4 a) {
     const float4 g = g4[v];
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * r * (1.f + g.x), a.y * r * (1.f + g.y));
-    const __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * r * (1.f + g.z), a.w * r * (1.f + g.w));
-    uint2 w;
-    w.x = *reinterpret_cast<const uint32_t*>(&lo);
-    w.y = *reinterpret_cast<const uint32_t*>(&hi);
-    reinterpret_cast<uint2*>(yr)[v] = w;
+    const float4 n = make_float4(a.x * r * (1.f + g.x), a.y * r * (1.f + g.y), a.z * r * (1.f + g.z),
+                                 a.w * r * (1.f + g.w));
+    if (y) {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(n.x, n.y);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(n.z, n.w);
+      uint2 w;
+      w.x = *reinterpret_cast<const uint32_t*>(&lo);
+      w.y = *reinterpret_cast<const uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(y + (size_t)i * D)[v] = w;
+    }
+    if (y32) reinterpret_cast<float4*>(y32 + (size_t)i * D)[v] = n;
     if (x_copy) reinterpret_cast<float4*>(x_copy + (size_t)i * D)[v] = a;
   };
   if (in_regs) {
@@ -174,10 +180,10 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(const float* __re
 }
 
 cudaError_t launch_rmsnorm(const float* x, int row0, int M, int D, const float* g, float eps, __nv_bfloat16* y,
-                           float* x_copy, cudaStream_t s) {
+                           float* x_copy, cudaStream_t s, float* y32) {
   if (M <= 0) return cudaSuccess;
   if (D % 4 != 0) return cudaErrorInvalidValue;
-  return launch_k(rmsnorm_kernel, dim3(M), dim3(NORM_THREADS), 0, s, 1, x, row0, D, g, eps, y, x_copy);
+  return launch_k(rmsnorm_kernel, dim3(M), dim3(NORM_THREADS), 0, s, 1, x, row0, D, g, eps, y, x_copy, y32);
 }
 
 // ---------------------------------------------------------------------------

@@ -59,6 +59,9 @@ EpiParams shift_rows(const EpiParams& e, int r) {
 struct prefill_ctx {
   prefill_model_desc d{};
   std::vector<int32_t> kv_src;
+  std::vector<int32_t> layer_inp;  // [n_layer + 1] requests of hidden-state outputs (empty: none)
+  std::vector<float*> layer_out;   // [n_layer + 1] their device buffers
+  float* embd_out = nullptr;       // the embeddings output's buffer
   int L = 0, S = 0, L_w = 0, D = 0, Hq = 0, Hkv = 0, hd = 0, q = 0, kv = 0, F = 0, V = 0, P = 0;
   int rows_alloc = 0;
   cudaStream_t stream = nullptr;
@@ -262,10 +265,19 @@ int check_desc(const prefill_model_desc* d, std::string* why) {
   return PF_OK;
 }
 
+// The pruning condition of the Gemma 4 prefill change (devotd.net news,
+// section 1 listing).  The NextN crop is always allowed here (no
+// multi-token-prediction head); a per-layer input embedding requested for
+// any layer from the first KV-shared one up to the final state (index
+// n_layer) needs every row there.
 bool predicate(const prefill_model_desc& d, int enable) {
-  // the NextN crop is always allowed here (no multi-token-prediction head)
-  return enable && d.n_layer_kv_from_start > 0 && d.n_layer_kv_from_start < d.n_layer && !d.embeddings &&
-         d.n_seq_max == 1;
+  if (!(enable && d.n_layer_kv_from_start > 0 && d.n_layer_kv_from_start < d.n_layer && !d.embeddings &&
+        d.n_seq_max == 1))
+    return false;
+  if (d.embd_layer_inp)
+    for (int il = d.n_layer_kv_from_start; il <= d.n_layer; ++il)
+      if (d.embd_layer_inp[il]) return false;
+  return true;
 }
 
 bool is_device_ptr(const void* p) {
@@ -347,6 +359,11 @@ extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weig
   C->d = *desc;
   C->kv_src.assign(desc->kv_src, desc->kv_src + desc->n_layer);
   C->d.kv_src = C->kv_src.data();
+  if (desc->embd_layer_inp) {
+    C->layer_inp.assign(desc->embd_layer_inp, desc->embd_layer_inp + desc->n_layer + 1);
+    C->d.embd_layer_inp = C->layer_inp.data();
+    C->layer_out.assign(desc->n_layer + 1, nullptr);
+  }
   C->L = desc->n_layer;
   C->S = desc->n_layer_kv_from_start;
   C->L_w = C->S;
@@ -543,6 +560,10 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
   if (is_last && !logits) return fail(c, PF_E_ARG, "logits is null on the last ubatch");
   // the head kernel writes the logits: they must be device (or managed) memory
   if (is_last && !is_device_ptr(logits)) return fail(c, PF_E_ARG, "logits is not device memory");
+  if (c->d.embeddings && !c->embd_out) return fail(c, PF_E_ARG, "the embeddings output has no buffer");
+  for (size_t il = 0; il < c->layer_inp.size(); ++il)
+    if (c->layer_inp[il] && !c->layer_out[il])
+      return fail(c, PF_E_ARG, "the hidden state of layer " + std::to_string(il) + " has no buffer");
   NvtxRange r_ubatch(is_last ? "ubatch (last)" : "ubatch");
   cudaStream_t s = c->stream;
   if (is_device_ptr(tokens)) {
@@ -625,8 +646,10 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       ple_view = c->ple + static_cast<size_t>(T - 1) * LP;
       gathered = true;
     } else {
-      PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, M * D * 6.0, [&] {
-                 return launch_rmsnorm(xcur, 0, M, D, W.attn_norm, c->d.rms_eps, c->y, nullptr, s);
+      // a requested hidden state entering this layer leaves as the norm's input copy
+      float* inp = c->layer_inp.empty() || !c->layer_inp[il] ? nullptr : c->layer_out[il];
+      PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, M * D * (6.0 + (inp ? 4.0 : 0.0)), [&] {
+                 return launch_rmsnorm(xcur, 0, M, D, W.attn_norm, c->d.rms_eps, c->y, inp, s);
                }));
     }
     const bool writes = il < S;
@@ -735,6 +758,16 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       PF_CUDA(c, project(c->a_pg, M, out_row, W.pp, r, 2.0 * D * c->P, c->P * 2.0 + D * 8.0, gemm_wbytes(c, D, c->P)));
     }
   }
+  {
+    // the final hidden state (index L) and the embeddings output of every
+    // row; requesting either turns the pruning off, so all T rows are here
+    float* fin = c->layer_inp.empty() || !c->layer_inp[L] ? nullptr : c->layer_out[L];
+    float* embd = c->d.embeddings ? c->embd_out : nullptr;
+    if ((fin || embd) && !gathered && !(prune && !is_last))
+      PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, M * D * (4.0 + (fin ? 4.0 : 0.0) + (embd ? 4.0 : 0.0)), [&] {
+                 return launch_rmsnorm(xcur, 0, M, D, c->out_norm, c->d.rms_eps, nullptr, fin, s, embd);
+               }));
+  }
   if (is_last) {
     NvtxRange r_head("head");
     const int row = gathered ? 0 : T - 1;
@@ -750,6 +783,20 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
                        [&] { return launch_gemv(c->a_y, c->head, e, c->gv_sums, c->gv_tickets, s); }));
   }
   c->n_pos = kv_len;
+  return PF_OK;
+}
+
+extern "C" int prefill_set_output(prefill_ctx* c, int32_t which, float* dst) {
+  if (!c) return fail(nullptr, PF_E_ARG, "null context");
+  if (dst && !is_device_ptr(dst)) return fail(c, PF_E_ARG, "output buffer is not device memory");
+  if (which == PF_OUT_EMBD) {
+    if (!c->d.embeddings) return fail(c, PF_E_ARG, "the description requests no embeddings output");
+    c->embd_out = dst;
+    return PF_OK;
+  }
+  if (which < 0 || which > c->L || c->layer_inp.empty() || !c->layer_inp[which])
+    return fail(c, PF_E_ARG, "the description requests no hidden state for that layer");
+  c->layer_out[which] = dst;
   return PF_OK;
 }
 

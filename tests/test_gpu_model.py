@@ -437,3 +437,56 @@ def test_cli_cache_file_flow(gpu, tinyllama, tmp_path):
     third = cli.run(args, weights=tinyllama, out=log)
     assert third["restored"] == 0 and "refused" in log.getvalue()
     assert os.path.getsize(path) - 16 == pin["body_bytes"]
+
+
+def test_hidden_state_outputs_match_oracle(gpu, tiny):
+    """Embeddings output and per-layer input hidden states (G4 section 1
+    listing: requesting them at or past the first KV-shared layer turns the
+    pruning off), ubatch by ubatch against the oracle; a request below the
+    first KV-shared layer keeps the pruning and leaves the logits' bits."""
+    cfg = tiny.cfg
+    L, D = cfg["n_layer"], cfg["d_model"]
+    tok = synth.make_tokens(cfg, 61, seed=5)
+    cuts = [(0, 32), (32, 61)]
+    req = [False, True, False, True, True]
+    ctx = binding.PrefillContext(tiny, max_ctx=64, ubatch_max=32, embeddings=True, layer_inp=req)
+    assert not ctx.prune_active
+    logits = torch.empty(cfg["vocab"], dtype=torch.float32, device="cuda")
+    with pytest.raises(binding.PrefillError) as e:
+        ctx.ubatch(tok[:32], 0, False)  # requested outputs without buffers
+    assert e.value.code == binding.PF_E_ARG
+    with pytest.raises(binding.PrefillError) as e:
+        ctx.set_output(2, torch.empty(32 * D, device="cuda"))  # layer 2 was not requested
+    assert e.value.code == binding.PF_E_ARG
+    bufs = {k: torch.full((32, D), float("nan"), device="cuda") for k in (1, 3, L, binding.PF_OUT_EMBD)}
+    for k, b in bufs.items():
+        ctx.set_output(k, b)
+    orc = OracleContext(cfg, tiny, 64)
+    for a, b in cuts:
+        cap = {}
+        want_logits = orc.ubatch(tok[a:b], b == 61, embeddings=True, embd_layer_inp=req, capture=cap)
+        ctx.ubatch(tok[a:b], a, b == 61, logits)
+        ctx.sync()
+        for k, buf in bufs.items():
+            got = buf[:b - a].cpu().numpy()
+            want = cap["embd" if k == binding.PF_OUT_EMBD else k]
+            assert got.shape == want.shape
+            assert np.abs(got - want).max() <= 2e-2 * np.abs(want).max(), (k, a)
+    check_logits(logits.cpu().numpy(), want_logits, "tiny-61 with hidden-state outputs")
+    ctx.close()
+    # a request below the first KV-shared layer: pruning stays on, logits unchanged
+    ref = run_gpu(tiny, tok, 32, True, max_ctx=64)
+    req1 = [False, True, False, False, False]
+    c1 = binding.PrefillContext(tiny, max_ctx=64, ubatch_max=32, layer_inp=req1)
+    assert c1.prune_active
+    buf = torch.empty((32, D), device="cuda")
+    c1.set_output(1, buf)
+    orc = OracleContext(cfg, tiny, 64)
+    for a, b in cuts:
+        cap = {}
+        orc.ubatch(tok[a:b], b == 61, prune=True, embd_layer_inp=req1, capture=cap)
+        c1.ubatch(tok[a:b], a, b == 61, logits)
+        c1.sync()
+        assert np.abs(buf[:b - a].cpu().numpy() - cap[1]).max() <= 2e-2 * np.abs(cap[1]).max()
+    np.testing.assert_array_equal(logits.cpu().numpy(), ref)
+    c1.close()

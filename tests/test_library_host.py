@@ -69,12 +69,15 @@ def test_prune_predicate_matches_listing(lib):
         if not ln.strip() or ln.startswith("#"):
             continue
         L, S, nseq, emb, idx, want = (int(v) for v in ln.split())
+        inp = None
         if idx >= 0:
-            continue  # the library exposes no per-layer embedding outputs
+            inp = [False] * (L + 1)
+            inp[idx] = True
         cfg = dict(base, n_layer=L, n_layer_kv_from_start=S,
                    kv_src=[-1 if i < S else max(S - 1, 0) for i in range(L)])
-        assert binding.prune_predicate(cfg, True, nseq, bool(emb)) == bool(want), ln
-        assert oracle.prune_shared(L, S, n_seq_max=nseq, embeddings=bool(emb)) == bool(want)
+        assert binding.prune_predicate(cfg, True, nseq, bool(emb), inp) == bool(want), ln
+        assert oracle.prune_shared(L, S, n_seq_max=nseq, embeddings=bool(emb),
+                                   embeddings_layer_inp=inp) == bool(want)
     assert binding.prune_predicate(base, prune=False) is False
 
 

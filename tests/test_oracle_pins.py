@@ -286,11 +286,13 @@ MICRO = dict(name="micro", n_layer=3, n_layer_kv_from_start=2, d_model=8, n_head
              rms_eps=1e-6, rope_base=10000.0, kv_src=[-1, -1, 1], wtype="f32")
 
 
-def _model_brute(cfg, w, tokens):
+def _model_brute(cfg, w, tokens, states=None):
     """Every step as float64 scalar loops, read straight from the method:
     pre-norm layers, Q/K/V projections, half-split RoPE, FP16 K/V, causal
     GQA attention over the own or the source layer's cache, output projection,
-    GeGLU feed-forward, then the per-layer-embedding block."""
+    GeGLU feed-forward, then the per-layer-embedding block.  With `states` a
+    dict, also the rows entering each layer (states[il]), the final rows
+    (states[n_layer]) and their output-normed form (states["embd"])."""
     D, L, S, P = cfg["d_model"], cfg["n_layer"], cfg["n_layer_kv_from_start"], cfg["ple_dim"]
     Hq, Hkv, hd, F = cfg["n_head"], cfg["n_head_kv"], cfg["head_dim"], cfg["ffn_dim"]
     T = len(tokens)
@@ -323,6 +325,8 @@ def _model_brute(cfg, w, tokens):
     cache = {}
     for il in range(L):
         lw = w.layers[il]
+        if states is not None:
+            states[il] = [list(r) for r in x]
         ys = [norm(x[t], lw["attn_norm"]) for t in range(T)]
         qs = []
         for t in range(T):
@@ -358,6 +362,9 @@ def _model_brute(cfg, w, tokens):
             gp = [gelu(gate[p]) * ple[t][il][p] for p in range(P)]
             pp = lin(lw["ple_proj"], gp)
             x[t] = [x[t][i] + pp[i] for i in range(D)]
+    if states is not None:
+        states[L] = [list(r) for r in x]
+        states["embd"] = [norm(r, w.out_norm) for r in x]
     y = norm(x[T - 1], w.out_norm)
     return np.array(lin(w.tok_embd, y))
 
@@ -382,6 +389,27 @@ def test_micro_model_matches_brute_force():
     got = ctx.ubatch(tokens, is_last=True)
     want = _model_brute(cfg, w, tokens)
     np.testing.assert_allclose(got, want, rtol=2e-4, atol=2e-4 * np.abs(want).max())
+
+
+def test_micro_model_hidden_states_match_brute_force():
+    """The hidden states the oracle hands out (the rows entering a layer, the
+    final rows, the embeddings output) against the float64 loops; asking
+    for a state at or past the first KV-shared layer keeps every row there
+    even with pruning asked for."""
+    cfg, w = _micro_weights()
+    tokens = np.array([3, 7, 0, 10, 5], dtype=np.int32)
+    states = {}
+    _model_brute(cfg, w, tokens, states)
+    L = cfg["n_layer"]
+    req = [False, True, True, True]
+    cap = {}
+    OracleContext(cfg, w, max_ctx=16).ubatch(tokens, is_last=True, prune=True, embeddings=True,
+                                             embd_layer_inp=req, capture=cap)
+    for key in (1, 2, L, "embd"):
+        want = np.array(states[key])
+        assert cap[key].shape == want.shape, key
+        np.testing.assert_allclose(cap[key], want, rtol=2e-4, atol=2e-4 * np.abs(want).max())
+    assert 0 not in cap
 
 
 def test_micro_model_brute_force_catches_planted_mistake(monkeypatch):
