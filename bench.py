@@ -156,8 +156,10 @@ def source_sha(paths):
 
 
 def gemm_traffic():
-    """DRAM bytes per GEMM launch from the committed ncu summary, or None when
-    the kernel source has changed since those counters were taken."""
+    """DRAM bytes per GEMM launch from the committed one-kernel ncu capture
+    (profiles/gemm_tc_e2b512_dram.json: the six projections of one writing
+    layer), or None when it is absent or the kernel source has changed since
+    those counters were taken."""
     path = os.path.join(ROOT, "profiles", "gemm_tc_e2b512_dram.json")
     try:
         with open(path) as f:
