@@ -96,6 +96,19 @@ int pfop_kv_copy(int32_t dir, void* cache_dev, int64_t cache_seg_halves, void* i
 int pfop_linear_row(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn, const void* a_dev,
                     float* out_dev, int32_t iters, float* us, void* stream);
 
+/* Check of the failure path of the bounded waits (the library's own error
+   convention; the pages have no counterpart).  Runs the GEMM of
+   pfop_linear_f32 (no k-split) with the copy producer of CTA 0 issuing
+   nothing from pipeline stage `withhold_stage` on, so no copy is left in
+   flight for the tensor-core and dequantisation warps that wait for that
+   stage: their waits give up after their bound (about 2 s of SM clock),
+   every warp unwinds (copies already issued are drained, TMEM is freed), and
+   the call returns PF_E_DEVICE_TIMEOUT with the GPU context still usable.
+   withhold_stage < 0 (or past the CTA's last stage) runs the plain GEMM and
+   returns PF_OK.  Synchronous on `stream`. */
+int pfop_linear_wait_test(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn, const void* a_dev,
+                          int32_t a_rows, int32_t M, float* out_dev, int32_t withhold_stage, void* stream);
+
 /* Time the GEMM kernel: upload W once, run `warmup` then `iters` launches of
    out = A W^T (fp32 [M][N]) and return the mean device time per launch in
    *us (CUDA events on `stream`).  split: k-splits (0 = the library's choice

@@ -47,6 +47,7 @@ EXPORTS = (
     "pfop_attention", "pfop_rmsnorm", "pfop_embed", "pfop_kv_copy", "pfop_last_error", "pfop_linear_bench",
     "pfop_attention_split_noalloc", "pfop_attention_bench", "pfop_kv_copy_bench",
     "kv_save_file", "kv_load_file", "prefill_kv_file_check", "pfop_linear_row", "prefill_set_output",
+    "pfop_linear_wait_test",
 )
 
 
@@ -145,6 +146,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "pfop_kv_copy_bench": (C.c_int, [i32, vp, i64, vp, i64, i32, i64, vp, i64, i32, i32,
                                          C.POINTER(C.c_float), vp]),
         "pfop_linear_row": (C.c_int, [i32, vp, i32, i32, i32, vp, vp, i32, C.POINTER(C.c_float), vp]),
+        "pfop_linear_wait_test": (C.c_int, [i32, vp, i32, i32, i32, vp, i32, i32, vp, i32, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -463,6 +463,10 @@ struct GemmShape {
   int M, K;
   int n_tiles, m_blocks, splits, kb_per_split, n_units;
   int a_box_rows;  // rows of A one TMA box brings (16 for launches of at most 16 rows, else 128)
+  // Failure-path check only (-1 otherwise): CTA 0's copy producer issues
+  // nothing from this pipeline stage on, so a consumer's bounded wait has to
+  // run out (no copy is left in flight for it).
+  int withhold_stage;
 };
 
 // Byte offset of (chunk c, row r, 16-byte piece q) in a split partial slot:
@@ -706,6 +710,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const int kb = ks * nkb + i * C::KS;  // first k-block of the stage
             const int kc = nkb - i * C::KS < C::KS ? nkb - i * C::KS : C::KS;
             const int sa = g % C::S_A;
+            if (blockIdx.x == 0 && static_cast<int>(g) == sh.withhold_stage) {
+              ok = false;  // stop issuing; the stages already issued are drained below
+              break;
+            }
             ok = mbar_wait(&empty_a[sa], ((g / C::S_A) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
             const bool raw_now = C::Q4 && g >= pre;
             const int sr = g % C::NR;
@@ -969,17 +977,20 @@ static size_t ring_bytes_mt1(int kind, int BN) {
 }
 
 int choose_split(int kind, int N_rows, int BN, int K, int max_rows) {
-  // Split the k-range over a cluster of CTAs while the split tile grid (one
-  // 128-row block per tile) still fits on the SMs at once.  Depends on the
+  // Split the k-range over a cluster of 2 or 3 CTAs while the split tile
+  // grid (one 128-row block per tile) still fits on the SMs at once, each
+  // part keeps at least 4 k-blocks, and rank 0's ring holds the other
+  // ranks' partial tiles; the largest such split wins.  Depends on the
   // matrix shape and the context's largest ubatch only, never on a launch's M.
   const int units1 = (N_rows / BN) * ((max_rows + 127) / 128);
   const int nkb = K / 64;
   const size_t ring = ring_bytes_mt1(kind, BN);
-  int s = 1;
-  while (units1 * 2 * s <= sm_count() && nkb % (2 * s) == 0 && nkb / (2 * s) >= 4 && 2 * s <= 2 &&
-         static_cast<size_t>(2 * s - 1) * 128 * BN * 4 <= ring)
-    s *= 2;
-  return s;
+  int best = 1;
+  for (int s = 2; s <= 3; ++s)
+    if (units1 * s <= sm_count() && nkb % s == 0 && nkb / s >= 4 &&
+        static_cast<size_t>(s - 1) * 128 * BN * 4 <= ring)
+      best = s;
+  return best;
 }
 
 std::vector<const void*> qkv_tile_rows(const void* wq, const void* wk, const void* wv, int Hq, int Hkv, int hd,
@@ -1009,7 +1020,7 @@ std::vector<const void*> qkv_tile_rows(const void* wq, const void* wk, const voi
 
 template <int WK, int BN, int MT>
 static cudaError_t launch_t(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err,
-                            cudaStream_t s) {
+                            cudaStream_t s, int withhold_stage) {
   using C = GemmCfg<WK, BN, MT>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -1031,6 +1042,7 @@ static cudaError_t launch_t(const ActMat& A, int M, const WeightMat& W, const Ep
   // rows that are never stored.
   const bool small = MT == 1 && M <= 16;
   sh.a_box_rows = small ? 16 : 128;
+  sh.withhold_stage = withhold_stage;
   if (W.split > 1 && static_cast<size_t>(W.split - 1) * 128 * BN * 4 > ring_bytes<WK, BN, MT>())
     return cudaErrorInvalidValue;
   const int cluster = W.split > 1 ? W.split : 1;
@@ -1039,7 +1051,8 @@ static cudaError_t launch_t(const ActMat& A, int M, const WeightMat& W, const Ep
                   small ? A.tmap_small : A.tmap, W.tmap, static_cast<const uint8_t*>(W.dev), sh, ep, err);
 }
 
-cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err, cudaStream_t s) {
+cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err, cudaStream_t s,
+                        int withhold_stage) {
   if (M <= 0) return cudaSuccess;
   if (A.K != W.K || W.K % 64 != 0 || W.N_rows % W.BN != 0 || M > A.rows || W.split < 1 ||
       (W.K / 64) % W.split != 0)
@@ -1050,7 +1063,8 @@ cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiPar
   const bool two = M > 128 && W.split == 1 && W.BN >= 256;
 #define PF_GEMM_CASE(WKV, BNV)                                                    \
   if (W.kind == WKV && W.BN == BNV)                                               \
-    return two ? launch_t<WKV, BNV, 2>(A, M, W, ep, err, s) : launch_t<WKV, BNV, 1>(A, M, W, ep, err, s);
+    return two ? launch_t<WKV, BNV, 2>(A, M, W, ep, err, s, withhold_stage)      \
+               : launch_t<WKV, BNV, 1>(A, M, W, ep, err, s, withhold_stage);
   PF_GEMM_CASE(W_Q4, 64)
   PF_GEMM_CASE(W_Q4, 128)
   PF_GEMM_CASE(W_Q4, 256)

@@ -87,8 +87,10 @@ constexpr int QKV_BN = 128;
 std::vector<const void*> qkv_tile_rows(const void* wq, const void* wk, const void* wv, int Hq, int Hkv, int hd,
                                        size_t row_bytes, int BN);
 
+// withhold_stage >= 0 only in the failure-path check (pfop_linear_wait_test):
+// CTA 0's copy producer issues nothing from that pipeline stage on.
 cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err_word,
-                        cudaStream_t s);
+                        cudaStream_t s, int withhold_stage = -1);
 
 // One row (a one-token ubatch): out = A[0] W^T with the same fused epilogue,
 // streamed by CUDA cores over (tile, k-part) CTAs.  `sums` holds

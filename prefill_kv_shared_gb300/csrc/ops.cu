@@ -213,6 +213,35 @@ extern "C" int pfop_linear_bench(int32_t wtype, const void* w_host, int32_t N, i
   return PF_OK;
 }
 
+extern "C" int pfop_linear_wait_test(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn,
+                                     const void* a_dev, int32_t a_rows, int32_t M, float* out_dev,
+                                     int32_t withhold_stage, void* stream) {
+  if (!w_host || !a_dev || !out_dev || N < 1 || N % 4 || M < 1 || M > a_rows || (bn != 64 && bn != 128 && bn != 256))
+    return op_fail(PF_E_ARG, "bad argument");
+  Scope sc;
+  WeightMat W;
+  ActMat A;
+  int rc;
+  if ((rc = make_weight(sc, W, wtype, rows_of(w_host, N, K, wtype, bn), K, bn))) return rc;
+  W.split = 1;  // no cluster: the withheld stage belongs to one CTA alone
+  if ((rc = make_act(A, a_dev, a_rows, K))) return rc;
+  EpiParams e;
+  e.kind = EPI_F32;
+  e.N = N;
+  e.out_f32 = out_dev;
+  e.ld_f32 = N;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* err = nullptr;
+  OP_CUDA(sc.alloc(&err, 16));
+  OP_CUDA(cudaMemsetAsync(err, 0, 16, s));
+  OP_CUDA(launch_gemm(A, M, W, e, err, s, withhold_stage < 0 ? -1 : withhold_stage));
+  OP_CUDA(cudaStreamSynchronize(s));
+  int h = 0;
+  OP_CUDA(cudaMemcpy(&h, err, 4, cudaMemcpyDeviceToHost));
+  if (h) return op_fail(PF_E_DEVICE_TIMEOUT, "GEMM gave up a bounded wait, code " + std::to_string(h));
+  return PF_OK;
+}
+
 extern "C" int pfop_linear_resid(int32_t wtype, const void* w_host, int32_t N, int32_t K, const void* a_dev,
                                  int32_t a_rows, int32_t M, float* x_dev, void* xb_dev, void* stream) {
   if (!w_host || !a_dev || !x_dev || N < 32 || N % 32 || M < 1 || M > a_rows) return op_fail(PF_E_ARG, "bad argument");
