@@ -187,8 +187,8 @@ cudaError_t launch_rmsnorm(const float* x, int row0, int M, int D, const float* 
 }
 
 // ---------------------------------------------------------------------------
-// KV image copy: a grid-stride loop over 16-byte vectors, four vectors in
-// flight per thread.  Segment s (s = kind * L_w + layer) is copy_vec vectors
+// KV image copy: a grid-stride loop over 16-byte vectors, up to four
+// vectors in flight per thread.  Segment s (s = kind * L_w + layer) is copy_vec vectors
 // long; it sits at s * cache_stride_vec in the cache and s * img_stride_vec
 // in the image body.
 
@@ -207,29 +207,28 @@ __global__ void __launch_bounds__(256) kv_copy_kernel(int dir, uint4* __restrict
   if (dir == 0 && blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int4*>(image) = header;
   uint4* body = reinterpret_cast<uint4*>(image + 16);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (; v + 3 * stride < n_vec; v += 4 * stride) {
+  // up to four vectors per thread in flight, the last group predicated, so
+  // that an image with only a few vectors per thread still issues all its
+  // loads before the first store
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n_vec; v += 4 * stride) {
     int64_t ci[4], ii[4];
     uint4 tmp[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) kv_vec_index(v + u * stride, copy_vec, cache_stride_vec, img_stride_vec, ci[u], ii[u]);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) tmp[u] = dir == 0 ? cache[ci[u]] : body[ii[u]];
+    for (int u = 0; u < 4; ++u) {
+      if (v + u * stride < n_vec) {
+        kv_vec_index(v + u * stride, copy_vec, cache_stride_vec, img_stride_vec, ci[u], ii[u]);
+        tmp[u] = dir == 0 ? cache[ci[u]] : body[ii[u]];
+      }
+    }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      if (dir == 0)
-        body[ii[u]] = tmp[u];
-      else
-        cache[ci[u]] = tmp[u];
+      if (v + u * stride < n_vec) {
+        if (dir == 0)
+          body[ii[u]] = tmp[u];
+        else
+          cache[ci[u]] = tmp[u];
+      }
     }
-  }
-  for (; v < n_vec; v += stride) {
-    int64_t ci, ii;
-    kv_vec_index(v, copy_vec, cache_stride_vec, img_stride_vec, ci, ii);
-    if (dir == 0)
-      body[ii] = cache[ci];
-    else
-      cache[ci] = body[ii];
   }
 }
 
