@@ -88,7 +88,8 @@ typedef struct prefill_model_desc {
   int32_t ubatch_max;     /* largest n_tokens per prefill_ubatch */
   int32_t prune_shared_enable; /* 1: prune before the first KV-shared layer when the
                                   condition holds; 0: every row passes every layer */
-  int32_t n_seq_max;      /* sequences sharing the context; pruning needs 1 */
+  int32_t n_seq_max;      /* sequences sharing the context (1 .. 128; see
+                             prefill_ubatch_seqs); the page's pruning needs 1 */
   int32_t embeddings;     /* nonzero: the embeddings output of every row is requested
                              (PF_OUT_EMBD of prefill_set_output; disables pruning) */
   const int32_t* embd_layer_inp; /* NULL, or [n_layer + 1] flags: nonzero at il requests the
@@ -166,13 +167,51 @@ int prefill_ubatch(prefill_ctx* ctx, const int32_t* tokens, int32_t n_tokens, in
 #define PF_OUT_EMBD (-1)
 int prefill_set_output(prefill_ctx* ctx, int32_t which, float* dst);
 
+/* ---- several sequences in one ubatch (unified KV cache) ----
+   ("llama.cpp Gemma 4 prefill KV graph optimization", section 5: the server
+   setting, where several sequences share one KV cache and one batch.)  A
+   context with n_seq_max > 1 gives every sequence q the cache cells
+   [q * max_ctx, (q + 1) * max_ctx) of each writing layer, and its own
+   position count.  A ubatch of several sequences is a list of runs: run k
+   holds runs[k].n_tokens consecutive tokens of sequence runs[k].seq_id
+   (each sequence at most once per ubatch, 0 <= seq_id < n_seq_max),
+   continuing it at prefill_seq_n_pos(seq_id); tokens holds the runs'
+   tokens one after another (host memory, validated on the host, or device
+   memory), at most ubatch_max in all.  Every row attends only to its own
+   sequence's cells.  A run with is_last nonzero ends its sequence's prompt:
+   its last row's logits go to row j of `logits` (fp32 [n_last][vocab],
+   device memory), j counting the is_last runs in order.
+   The page's pruning condition asks for one sequence, so with several
+   sequences it never holds; this call instead applies the variant the
+   server setting would need when pruning is on (PF_PRUNE_ON) and the rest
+   of the condition holds (a KV-shared split inside the model, no embeddings
+   or per-layer hidden-state outputs): before the first KV-shared layer only
+   the output rows (one per is_last run) are kept.  Pruned and unpruned
+   (PF_PRUNE_OFF) calls give bit-identical logits.  Enqueue only.
+   PF_E_ARG for a bad run list, positions past max_ctx, more than
+   ubatch_max tokens, or a missing/host logits buffer when a run ends. */
+typedef struct prefill_seq_run {
+  int32_t seq_id;
+  int32_t n_tokens;
+  int32_t is_last;
+} prefill_seq_run;
+int prefill_ubatch_seqs(prefill_ctx* ctx, const int32_t* tokens, const prefill_seq_run* runs, int32_t n_runs,
+                        float* logits);
+
+/* Positions of sequence seq_id in the cache (-1 for a bad id); forget one
+   sequence (prefill_reset forgets all of them).  prefill_n_pos, kv_save and
+   kv_load work on sequence 0. */
+int64_t prefill_seq_n_pos(const prefill_ctx* ctx, int32_t seq_id);
+int prefill_seq_reset(prefill_ctx* ctx, int32_t seq_id);
+
 /* Wait for the context's stream and report device-side errors. */
 int prefill_sync(prefill_ctx* ctx);
 
 /* Positions currently in the cache. */
 int64_t prefill_n_pos(const prefill_ctx* ctx);
 
-/* Forget the sequence (position count 0); the cache memory is kept.  (The
+/* Forget the sequence (position count 0; with several sequences, all of
+   them); the cache memory is kept.  (The
    fallback of "PicoLM KV Cache persistence", "rules": a request whose
    prefix cannot be restored starts from an empty cache.) */
 int prefill_reset(prefill_ctx* ctx);

@@ -47,7 +47,7 @@ EXPORTS = (
     "pfop_attention", "pfop_rmsnorm", "pfop_embed", "pfop_kv_copy", "pfop_last_error", "pfop_linear_bench",
     "pfop_attention_split_noalloc", "pfop_attention_bench", "pfop_kv_copy_bench",
     "kv_save_file", "kv_load_file", "prefill_kv_file_check", "pfop_linear_row", "prefill_set_output",
-    "pfop_linear_wait_test",
+    "pfop_linear_wait_test", "prefill_ubatch_seqs", "prefill_seq_n_pos", "prefill_seq_reset",
 )
 
 
@@ -84,6 +84,10 @@ class LayerWeights(C.Structure):
                                           "w_up", "w_down", "ple_gate", "ple_proj")]
 
 
+class SeqRun(C.Structure):
+    _fields_ = [("seq_id", C.c_int32), ("n_tokens", C.c_int32), ("is_last", C.c_int32)]
+
+
 class Weights(C.Structure):
     _fields_ = [("tok_embd", C.c_void_p), ("ple_embd", C.c_void_p), ("out_norm", C.c_void_p),
                 ("layers", C.POINTER(LayerWeights))]
@@ -109,6 +113,9 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "prefill_ubatch": (C.c_int, [vp, vp, i32, i64, i32, vp]),
         "prefill_sync": (C.c_int, [vp]),
         "prefill_set_output": (C.c_int, [vp, i32, vp]),
+        "prefill_ubatch_seqs": (C.c_int, [vp, vp, C.POINTER(SeqRun), i32, vp]),
+        "prefill_seq_n_pos": (i64, [vp, i32]),
+        "prefill_seq_reset": (C.c_int, [vp, i32]),
         "prefill_n_pos": (i64, [vp]),
         "prefill_reset": (C.c_int, [vp]),
         "prefill_set_prune": (C.c_int, [vp, i32]),
@@ -340,6 +347,27 @@ class PrefillContext:
         if dst is not None:
             _buffer(dst, "dst", "float32")
         self._check(self._lib.prefill_set_output(self._h, which, _ptr(dst)))
+
+    def ubatch_seqs(self, tokens, runs, logits=None):
+        """Several sequences in one ubatch: runs = [(seq_id, n_tokens,
+        is_last), ...] in the order of their tokens; tokens: numpy int32
+        (host) or an int32 device tensor holding the runs' tokens one after
+        another; logits: fp32 device tensor [number of is_last runs, vocab]."""
+        arr = (SeqRun * len(runs))(*[SeqRun(int(q), int(n), 1 if last else 0) for q, n, last in runs])
+        if isinstance(tokens, np.ndarray):
+            tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+        else:
+            _buffer(tokens, "tokens", "int32")
+        n_last = sum(1 for r in runs if r[2])
+        if n_last:
+            _buffer(logits, "logits", "float32", n_last * self.cfg["vocab"])
+        self._check(self._lib.prefill_ubatch_seqs(self._h, _ptr(tokens), arr, len(runs), _ptr(logits)))
+
+    def seq_n_pos(self, seq_id: int) -> int:
+        return int(self._lib.prefill_seq_n_pos(self._h, seq_id))
+
+    def seq_reset(self, seq_id: int):
+        self._check(self._lib.prefill_seq_reset(self._h, seq_id))
 
     def sync(self):
         self._check(self._lib.prefill_sync(self._h))

@@ -274,8 +274,8 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m0, int rv
         for (int i = 0; i < 8; ++i) {
           const int r = 4 * i + rs;
           if (r >= rv) continue;
-          const int pos = ep.pos0 + m0 + r;
-          *reinterpret_cast<uint2*>(ep.v_cache + (size_t)pos * ep.kv_dim + (n - k_end) + 4 * p) = h[i];
+          const int slot = ep.row_slot ? ep.row_slot[m0 + r] : ep.pos0 + m0 + r;
+          *reinterpret_cast<uint2*>(ep.v_cache + (size_t)slot * ep.kv_dim + (n - k_end) + 4 * p) = h[i];
         }
         continue;
       }
@@ -301,7 +301,8 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m0, int rv
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = 16 * hp + 4 * i + rs;
-          const int pos = ep.pos0 + m0 + (r < rv ? r : 0);
+          const int m = m0 + (r < rv ? r : 0);
+          const int pos = ep.row_pos ? ep.row_pos[m] : ep.pos0 + m;
           const float4* cs = reinterpret_cast<const float4*>(ep.rope + (size_t)pos * half + i0 + 4 * p);
           c01[i] = cs[0];
           c23[i] = cs[1];
@@ -332,9 +333,10 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m0, int rv
         for (int i = 0; i < 4; ++i) {
           const int r = 16 * hp + 4 * i + rs;
           if (r >= rv) continue;
-          const int m = m0 + r, pos = ep.pos0 + m;
+          const int m = m0 + r;
+          const int slot = ep.row_slot ? ep.row_slot[m] : ep.pos0 + m;
           __half* dst = is_q ? ep.q_out + (size_t)m * ep.q_dim + head * hd
-                             : ep.k_cache + (size_t)pos * ep.kv_dim + head * hd;
+                             : ep.k_cache + (size_t)slot * ep.kv_dim + head * hd;
           *reinterpret_cast<uint2*>(dst + i0 + 4 * p) = o1[i];
           *reinterpret_cast<uint2*>(dst + i0 + half + 4 * p) = o2[i];
         }
@@ -977,20 +979,17 @@ static size_t ring_bytes_mt1(int kind, int BN) {
 }
 
 int choose_split(int kind, int N_rows, int BN, int K, int max_rows) {
-  // Split the k-range over a cluster of 2 or 3 CTAs while the split tile
-  // grid (one 128-row block per tile) still fits on the SMs at once, each
-  // part keeps at least 4 k-blocks, and rank 0's ring holds the other
-  // ranks' partial tiles; the largest such split wins.  Depends on the
-  // matrix shape and the context's largest ubatch only, never on a launch's M.
+  // Split the k-range over a cluster of 2 CTAs while the split tile grid
+  // (one 128-row block per tile) still fits on the SMs at once, each part
+  // keeps at least 4 k-blocks, and rank 0's ring holds the other rank's
+  // partial tile.  (A 3-way split of the 1536 x 6144 down projection, which
+  // also fits one wave, made the E2B pass slower.)  Depends on the matrix
+  // shape and the context's largest ubatch only, never on a launch's M.
   const int units1 = (N_rows / BN) * ((max_rows + 127) / 128);
   const int nkb = K / 64;
   const size_t ring = ring_bytes_mt1(kind, BN);
-  int best = 1;
-  for (int s = 2; s <= 3; ++s)
-    if (units1 * s <= sm_count() && nkb % s == 0 && nkb / s >= 4 &&
-        static_cast<size_t>(s - 1) * 128 * BN * 4 <= ring)
-      best = s;
-  return best;
+  if (units1 * 2 <= sm_count() && nkb % 2 == 0 && nkb / 2 >= 4 && static_cast<size_t>(128) * BN * 4 <= ring) return 2;
+  return 1;
 }
 
 std::vector<const void*> qkv_tile_rows(const void* wq, const void* wk, const void* wv, int Hq, int Hkv, int hd,

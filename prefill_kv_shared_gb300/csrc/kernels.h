@@ -45,6 +45,10 @@ struct EpiParams {
   int q_dim = 0, kv_dim = 0, head_dim = 0;
   int pos0 = 0;                  // position of GEMM row 0
   const float2* rope = nullptr;  // [position][head_dim/2] = (cos, sin)
+  // rows of several sequences in one launch: row m's position (RoPE angle)
+  // and its K/V cache row; null: pos0 + m for both
+  const int* row_pos = nullptr;
+  const int* row_slot = nullptr;
 };
 
 // A weight matrix in device memory, in the GEMM's tile order.
@@ -151,10 +155,16 @@ struct EmbedArgs {
 };
 cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t s);
 
-// y[i] = rmsnorm(x[row0 + i]) * (1 + g) for i < M as bf16 (y) and/or fp32
-// (y32); optionally x_copy[i] = x[row0 + i].  Null outputs are skipped.
+// y[i] = rmsnorm(x[r_i]) * (1 + g) for i < M as bf16 (y) and/or fp32 (y32),
+// r_i = rows[i] when rows is given, else row0 + i; optionally x_copy[i] =
+// x[r_i].  Null outputs are skipped.
 cudaError_t launch_rmsnorm(const float* x, int row0, int M, int D, const float* g, float eps,
-                           __nv_bfloat16* y, float* x_copy, cudaStream_t s, float* y32 = nullptr);
+                           __nv_bfloat16* y, float* x_copy, cudaStream_t s, float* y32 = nullptr,
+                           const int* rows = nullptr);
+
+// dst[i] = src[rows[i]] for i < n, rows of row_bytes bytes (a multiple of 16,
+// both bases 16-byte aligned)
+cudaError_t launch_gather_rows(const void* src, void* dst, const int* rows, int n, size_t row_bytes, cudaStream_t s);
 
 // KV image body <-> cache.  n_seg segments (keys of each writing layer, then
 // values); each copies copy_bytes, from/to the cache at seg * cache_seg_stride

@@ -109,12 +109,14 @@ constexpr int NORM_VEC = 8;
 __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(const float* __restrict__ x, int row0, int D,
                                                                const float* __restrict__ gain, float eps,
                                                                __nv_bfloat16* __restrict__ y,
-                                                               float* __restrict__ x_copy, float* __restrict__ y32) {
+                                                               float* __restrict__ x_copy, float* __restrict__ y32,
+                                                               const int* __restrict__ rows) {
   __shared__ float red[NORM_THREADS / 32];
   pdl_launch();
   pdl_wait();
   const int i = blockIdx.x;
-  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)(row0 + i) * D);
+  const int src_row = rows ? rows[i] : row0 + i;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)src_row * D);
   const int nv = D / 4;
   const bool in_regs = nv <= NORM_THREADS * NORM_VEC;
   float4 keep[NORM_VEC];
@@ -180,10 +182,28 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(const float* __re
 }
 
 cudaError_t launch_rmsnorm(const float* x, int row0, int M, int D, const float* g, float eps, __nv_bfloat16* y,
-                           float* x_copy, cudaStream_t s, float* y32) {
+                           float* x_copy, cudaStream_t s, float* y32, const int* rows) {
   if (M <= 0) return cudaSuccess;
   if (D % 4 != 0) return cudaErrorInvalidValue;
-  return launch_k(rmsnorm_kernel, dim3(M), dim3(NORM_THREADS), 0, s, 1, x, row0, D, g, eps, y, x_copy, y32);
+  return launch_k(rmsnorm_kernel, dim3(M), dim3(NORM_THREADS), 0, s, 1, x, row0, D, g, eps, y, x_copy, y32, rows);
+}
+
+// one CTA per gathered row, 16-byte vectors
+__global__ void __launch_bounds__(128) gather_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                          const int* __restrict__ rows, int row_vec) {
+  pdl_launch();
+  pdl_wait();
+  const uint4* s = src + (size_t)rows[blockIdx.x] * row_vec;
+  uint4* d = dst + (size_t)blockIdx.x * row_vec;
+  for (int v = threadIdx.x; v < row_vec; v += blockDim.x) d[v] = s[v];
+}
+
+cudaError_t launch_gather_rows(const void* src, void* dst, const int* rows, int n, size_t row_bytes, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  if (row_bytes % 16 != 0 || ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) % 16) != 0)
+    return cudaErrorInvalidValue;
+  return launch_k(gather_rows_kernel, dim3(n), dim3(128), 0, s, 1, static_cast<const uint4*>(src),
+                  static_cast<uint4*>(dst), rows, static_cast<int>(row_bytes / 16));
 }
 
 // ---------------------------------------------------------------------------

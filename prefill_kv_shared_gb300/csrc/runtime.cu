@@ -50,6 +50,8 @@ EpiParams shift_rows(const EpiParams& e, int r) {
   if (s.out_bf16) s.out_bf16 += static_cast<size_t>(r) * s.ld_bf16;
   if (s.ple) s.ple += static_cast<size_t>(r) * s.ple_stride;
   if (s.q_out) s.q_out += static_cast<size_t>(r) * s.q_dim;
+  if (s.row_pos) s.row_pos += r;
+  if (s.row_slot) s.row_slot += r;
   s.pos0 += r;
   return s;
 }
@@ -88,7 +90,10 @@ struct prefill_ctx {
   int* err = nullptr;
   ActMat a_y, a_att, a_h, a_xb, a_pg;
 
-  int64_t n_pos = 0;
+  std::vector<int64_t> seq_pos;  // positions in the cache, per sequence
+  int* rowinfo = nullptr;        // several sequences: row positions, cache rows, output rows and positions
+  std::vector<int> rowinfo_host;
+  __nv_bfloat16* ple_g = nullptr;  // per-layer-embedding rows of the gathered output rows
   int prune_enable = 1;  // PF_PRUNE_ON / PF_PRUNE_OFF / PF_PRUNE_OFF_PLAIN
   std::string last_error;
 
@@ -236,6 +241,9 @@ int check_desc(const prefill_model_desc* d, std::string* why) {
   if (d->ffn_kind != PF_FFN_GEGLU && d->ffn_kind != PF_FFN_SWIGLU) return bad("ffn_kind");
   if (d->wtype != PF_W_F32 && d->wtype != PF_W_Q4_0) return bad("wtype");
   if (d->max_ctx < 1 || d->ubatch_max < 1) return bad("max_ctx and ubatch_max must be >= 1");
+  // the gathered output rows (one per finishing sequence) share the
+  // 128-row buffer of the pruned rows
+  if (d->n_seq_max < 1 || d->n_seq_max > 128) return bad("n_seq_max outside [1, 128]");
   // Sizes whose products the kernels index with 32-bit integers: a row of
   // any activation, a weight matrix, and one layer's cache stay below 2^31
   // elements (far above any model this library targets).
@@ -251,7 +259,8 @@ int check_desc(const prefill_model_desc* d, std::string* why) {
     if (int64_t(d->vocab) * d->d_model >= kMaxElems || 2 * int64_t(d->ffn_dim) * d->d_model >= kMaxElems ||
         (q + 2 * kv) * d->d_model >= kMaxElems || int64_t(d->vocab) * d->n_layer * d->ple_dim >= kMaxElems)
       return bad("a weight matrix reaches 2^31 elements");
-    if (int64_t(d->max_ctx) * kv >= kMaxElems) return bad("max_ctx times the KV width reaches 2^31 elements");
+    if (int64_t(d->max_ctx) * kv * (d->n_seq_max > 0 ? d->n_seq_max : 1) >= kMaxElems)
+      return bad("n_seq_max times max_ctx times the KV width reaches 2^31 elements");
   }
   if (!d->kv_src) return bad("kv_src is null");
   for (int il = 0; il < d->n_layer; ++il) {
@@ -476,7 +485,14 @@ extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weig
   if ((rc = dev_alloc(C, &C->row_partials,
                       attn_split_partials_floats(C->Hq, C->Hkv, C->hd, static_cast<int>(C->d.max_ctx) - 1) * 4)))
     return fail(nullptr, rc, C->last_error);
-  if ((rc = dev_alloc(C, &C->cache, static_cast<size_t>(2) * C->L_w * C->d.max_ctx * C->kv * 2)))
+  if ((rc = dev_alloc(C, &C->cache,
+                      static_cast<size_t>(2) * C->L_w * C->d.n_seq_max * C->d.max_ctx * C->kv * 2)))
+    return fail(nullptr, rc, C->last_error);
+  C->seq_pos.assign(C->d.n_seq_max, 0);
+  if ((rc = dev_alloc(C, &C->rowinfo, static_cast<size_t>(4) * C->rows_alloc * 4)))
+    return fail(nullptr, rc, C->last_error);
+  if (C->P > 0 && C->d.n_seq_max > 1 &&
+      (rc = dev_alloc(C, &C->ple_g, static_cast<size_t>(C->d.n_seq_max) * C->L * C->P * 2)))
     return fail(nullptr, rc, C->last_error);
   {
     // RoPE table: angle pos * base^(-2i/hd) in double, cos/sin rounded to fp32
@@ -551,36 +567,92 @@ extern "C" const char* prefill_last_error(const prefill_ctx* c) {
 // ---------------------------------------------------------------------------
 // the ubatch
 
-extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, int64_t pos0, int32_t is_last,
-                              float* logits) {
-  if (!c) return fail(nullptr, PF_E_ARG, "null context");
-  if (!tokens || T < 1 || T > c->d.ubatch_max) return fail(c, PF_E_ARG, "n_tokens outside [1, ubatch_max]");
-  if (pos0 != c->n_pos) return fail(c, PF_E_ARG, "pos0 must equal the cached position count");
-  if (pos0 + T > c->d.max_ctx) return fail(c, PF_E_ARG, "positions would exceed max_ctx");
-  if (is_last && !logits) return fail(c, PF_E_ARG, "logits is null on the last ubatch");
+namespace {
+
+// One run of a ubatch: n consecutive rows of sequence `seq`, continuing it at
+// position pos0; `last`: the run ends that sequence's prompt (its last row's
+// logits are an output).
+struct Run {
+  int seq = 0, n = 0, last = 0, row0 = 0;
+  int64_t pos0 = 0;
+};
+
+// The pruning condition without its single-sequence clause: a KV-shared
+// split inside the model and no output that needs every row there.  With
+// several sequences in a ubatch, this decides the per-sequence gather (one
+// row kept per finishing sequence), the variant of the page's pruning that
+// its server setting would need.
+bool gather_possible(const prefill_model_desc& d) {
+  prefill_model_desc one = d;
+  one.n_seq_max = 1;
+  return predicate(one, 1);
+}
+
+// The ubatch of one or more sequence runs (the runs' positions already
+// checked).  `multi`: the call came through prefill_ubatch_seqs; a single
+// run of sequence 0 then computes what prefill_ubatch computes, but takes the
+// tensor-core projections for its output row (the one-row stream kernel
+// serves single-sequence ubatches only).
+int run_ubatch(prefill_ctx* c, const int32_t* tokens, int T, std::vector<Run>& runs, bool multi, float* logits) {
+  int n_out = 0;
+  for (const Run& r : runs) n_out += r.last ? 1 : 0;
+  const bool is_last = n_out > 0;
+  if (is_last && !logits) return fail(c, PF_E_ARG, "logits is null for a ubatch that ends a prompt");
   // the head kernel writes the logits: they must be device (or managed) memory
   if (is_last && !is_device_ptr(logits)) return fail(c, PF_E_ARG, "logits is not device memory");
   if (c->d.embeddings && !c->embd_out) return fail(c, PF_E_ARG, "the embeddings output has no buffer");
   for (size_t il = 0; il < c->layer_inp.size(); ++il)
     if (c->layer_inp[il] && !c->layer_out[il])
       return fail(c, PF_E_ARG, "the hidden state of layer " + std::to_string(il) + " has no buffer");
-  NvtxRange r_ubatch(is_last ? "ubatch (last)" : "ubatch");
-  cudaStream_t s = c->stream;
-  if (is_device_ptr(tokens)) {
-    PF_CUDA(c, cudaMemcpyAsync(c->tok, tokens, T * 4, cudaMemcpyDeviceToDevice, s));
-  } else {
+  const bool dev_tokens = is_device_ptr(tokens);
+  if (!dev_tokens)
     for (int i = 0; i < T; ++i)
       if (tokens[i] < 0 || tokens[i] >= c->V) return fail(c, PF_E_ARG, "token id outside [0, vocab)");
-    PF_CUDA(c, cudaMemcpyAsync(c->tok, tokens, T * 4, cudaMemcpyHostToDevice, s));
-  }
+  NvtxRange r_ubatch(is_last ? "ubatch (last)" : "ubatch");
+  cudaStream_t s = c->stream;
+  PF_CUDA(c, cudaMemcpyAsync(c->tok, tokens, T * 4, dev_tokens ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, s));
 
-  const bool prune = predicate(c->d, c->prune_enable == PF_PRUNE_ON);
+  const int L = c->L, S = c->S, D = c->D, LP = L * c->P;
+  const int max_ctx = c->d.max_ctx;
+  // per layer the cache holds every sequence's cells: sequence q at rows
+  // [q * max_ctx, (q + 1) * max_ctx)
+  const size_t seg = static_cast<size_t>(c->d.n_seq_max) * max_ctx * c->kv;
+  const size_t seq_cells = static_cast<size_t>(max_ctx) * c->kv;
+  const bool prune = multi ? (c->prune_enable == PF_PRUNE_ON && gather_possible(c->d))
+                           : predicate(c->d, c->prune_enable == PF_PRUNE_ON);
   // the output row of the KV-shared layers takes the single-row kernels
   // unless the plain unpruned pass was asked for
   const bool row_kernels = c->prune_enable != PF_PRUNE_OFF_PLAIN;
-  const int L = c->L, S = c->S, D = c->D, LP = L * c->P;
-  const int kv_len = static_cast<int>(pos0) + T;
-  const size_t seg = static_cast<size_t>(c->d.max_ctx) * c->kv;
+  const int64_t pos0 = runs[0].pos0;
+  const int kv_len = static_cast<int>(pos0) + T;  // single-sequence ubatches
+
+  // several sequences: each row's position and cache row, the output rows
+  // and their positions, uploaded once for the ubatch
+  int* d_row_pos = c->rowinfo;
+  int* d_row_slot = c->rowinfo + c->rows_alloc;
+  int* d_out_rows = c->rowinfo + 2 * c->rows_alloc;
+  int* d_out_pos = c->rowinfo + 3 * c->rows_alloc;
+  std::vector<int> out_rows, out_pos, out_run;
+  for (size_t k = 0; k < runs.size(); ++k)
+    if (runs[k].last) {
+      out_rows.push_back(runs[k].row0 + runs[k].n - 1);
+      out_pos.push_back(static_cast<int>(runs[k].pos0) + runs[k].n - 1);
+      out_run.push_back(static_cast<int>(k));
+    }
+  if (multi) {
+    std::vector<int>& h = c->rowinfo_host;
+    h.assign(static_cast<size_t>(4) * c->rows_alloc, 0);
+    for (const Run& r : runs)
+      for (int i = 0; i < r.n; ++i) {
+        h[r.row0 + i] = static_cast<int>(r.pos0) + i;
+        h[c->rows_alloc + r.row0 + i] = r.seq * max_ctx + static_cast<int>(r.pos0) + i;
+      }
+    for (int j = 0; j < n_out; ++j) {
+      h[2 * c->rows_alloc + j] = out_rows[j];
+      h[3 * c->rows_alloc + j] = out_pos[j];
+    }
+    PF_CUDA(c, cudaMemcpyAsync(c->rowinfo, h.data(), h.size() * 4, cudaMemcpyHostToDevice, s));
+  }
 
   EmbedArgs ea;
   ea.tok = c->tok;
@@ -610,7 +682,10 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
   // pruning modes (alone after the pruning, beside the other rows without
   // it), so its bits do not depend on the mode; a one-token ubatch (a decode
   // step) takes it in every layer.  Work counted per row: flops_row FLOPs and
-  // io_row activation bytes, plus the weight bytes once per launch.
+  // io_row activation bytes, plus the weight bytes once per launch.  (The
+  // tensor-core kernel's rows are independent of each other bit for bit, so
+  // the rows of several sequences keep their bits whether the launch holds
+  // every row or only the gathered output rows.)
   auto project = [&](const ActMat& A, int rows, bool out_row, const WeightMat& Wm, const EpiParams& e,
                      double flops_row, double io_row, double wbytes) -> cudaError_t {
     const int m_tc = out_row ? rows - 1 : rows;
@@ -626,6 +701,35 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
     return counted(c, PF_KC_GEMM_ROW, 1, flops_row, wbytes + io_row,
                    [&] { return launch_gemv(a1, Wm, e1, c->gv_sums, c->gv_tickets, s); });
   };
+  // the single-row attention of one output row
+  auto row_attention = [&](const AttnArgs& base, int row, int seq, int pos) -> cudaError_t {
+    AttnArgs r = base;
+    r.M = 1;
+    r.q = c->q16 + static_cast<size_t>(row) * c->q;
+    r.out = c->att + static_cast<size_t>(row) * c->q;
+    r.k = base.k + static_cast<size_t>(seq) * seq_cells;
+    r.v = base.v + static_cast<size_t>(seq) * seq_cells;
+    r.pos_base = pos;
+    r.kv_len = pos + 1;
+    const int n_keys = pos + 1;
+    return counted(c, PF_KC_ATTN_ROW, 2, static_cast<double>(n_keys) * c->Hq * 4.0 * c->hd,
+                   n_keys * c->kv * 4.0 + c->q * 4.0, [&] { return launch_attn_split(r, c->row_partials, s); });
+  };
+  // the prefill attention of rows [row0, row0 + n) of sequence seq at positions pos .. pos + n - 1
+  auto rows_attention = [&](const AttnArgs& base, int row0, int n, int seq, int pos, int keys) -> cudaError_t {
+    AttnArgs r = base;
+    r.M = n;
+    r.q = c->q16 + static_cast<size_t>(row0) * c->q;
+    r.out = c->att + static_cast<size_t>(row0) * c->q;
+    r.k = base.k + static_cast<size_t>(seq) * seq_cells;
+    r.v = base.v + static_cast<size_t>(seq) * seq_cells;
+    r.pos_base = pos;
+    r.kv_len = keys;
+    // (query head, visible key) pairs: rows at positions pos .. pos+n-1
+    const double pairs = static_cast<double>(n) * pos + 0.5 * n * (n + 1.0);
+    return counted(c, PF_KC_ATTN, attn_launch_count(r), pairs * c->Hq * 4.0 * c->hd, keys * c->kv * 4.0 + n * c->q * 4.0,
+                   [&] { return launch_attn_prefill(r, c->partials, s); });
+  };
 
   for (int il = 0; il < L; ++il) {
     const LayerW& W = c->layers[il];
@@ -636,14 +740,29 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       if (!is_last) {
         break;
       }
-      // keep the output row only: gather it inside the norm
-      PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, D * 10.0, [&] {
-                 return launch_rmsnorm(c->x, T - 1, 1, D, W.attn_norm, c->d.rms_eps, c->y, c->xr, s);
-               }));
+      if (!multi) {
+        // keep the output row only: gather it inside the norm
+        PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, D * 10.0, [&] {
+                   return launch_rmsnorm(c->x, T - 1, 1, D, W.attn_norm, c->d.rms_eps, c->y, c->xr, s);
+                 }));
+        M = 1;
+        pos_base = static_cast<int>(pos0) + T - 1;
+        ple_view = c->ple + static_cast<size_t>(T - 1) * LP;
+      } else {
+        // keep one row per finishing sequence (the norm gathers them), and
+        // their per-layer-embedding rows
+        PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, n_out * D * 10.0, [&] {
+                   return launch_rmsnorm(c->x, 0, n_out, D, W.attn_norm, c->d.rms_eps, c->y, c->xr, s, nullptr,
+                                         d_out_rows);
+                 }));
+        if (c->P > 0)
+          PF_CUDA(c, counted(c, PF_KC_OTHER, 1, 0.0, n_out * LP * 4.0, [&] {
+                     return launch_gather_rows(c->ple, c->ple_g, d_out_rows, n_out, static_cast<size_t>(LP) * 2, s);
+                   }));
+        M = n_out;
+        ple_view = c->ple_g;
+      }
       xcur = c->xr;
-      M = 1;
-      pos_base = static_cast<int>(pos0) + T - 1;
-      ple_view = c->ple + static_cast<size_t>(T - 1) * LP;
       gathered = true;
     } else {
       // a requested hidden state entering this layer leaves as the norm's input copy
@@ -655,8 +774,9 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
     const bool writes = il < S;
     const int src = writes ? il : c->kv_src[il];
     // the output row of a KV-shared layer in the final ubatch, and the one
-    // row of a one-row launch, take the single-row kernels (see project)
-    const bool out_row = M == 1 || (!writes && is_last && row_kernels);
+    // row of a one-row launch, take the single-row kernels (see project);
+    // ubatches of several sequences keep every projection on the tensor cores
+    const bool out_row = !multi && (M == 1 || (!writes && is_last && row_kernels));
     {
       EpiParams e;
       e.kind = EPI_QKV;
@@ -668,9 +788,13 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       e.rope = c->rope;
       e.k_cache = c->cache + static_cast<size_t>(il) * seg;
       e.v_cache = c->cache + static_cast<size_t>(c->L_w + il) * seg;
-      const double n_out = c->q + 2.0 * e.kv_dim;
-      PF_CUDA(c, project(c->a_y, M, out_row, W.qkv, e, 2.0 * n_out * D, D * 2.0 + n_out * 2.0,
-                         gemm_wbytes(c, n_out, D)));
+      if (multi) {
+        e.row_pos = gathered ? d_out_pos : d_row_pos;
+        e.row_slot = gathered ? nullptr : d_row_slot;
+      }
+      const double n_out_cols = c->q + 2.0 * e.kv_dim;
+      PF_CUDA(c, project(c->a_y, M, out_row, W.qkv, e, 2.0 * n_out_cols * D, D * 2.0 + n_out_cols * 2.0,
+                         gemm_wbytes(c, n_out_cols, D)));
     }
     {
       AttnArgs a;
@@ -685,27 +809,24 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
       a.pos_base = pos_base;
       a.kv_len = kv_len;
       a.err = c->err;
-      // the output row takes the single-row attention, as in project()
-      const int m_rest = out_row ? M - 1 : M;  // rows for the prefill kernels
-      if (m_rest > 0) {
-        AttnArgs r = a;
-        r.M = m_rest;
-        // (query head, visible key) pairs: rows at positions pos_base .. pos_base+m_rest-1
-        const double pairs = static_cast<double>(m_rest) * pos_base + 0.5 * m_rest * (m_rest + 1.0);
-        PF_CUDA(c, counted(c, PF_KC_ATTN, attn_launch_count(r), pairs * c->Hq * 4.0 * c->hd,
-                           kv_len * c->kv * 4.0 + m_rest * c->q * 4.0,
-                           [&] { return launch_attn_prefill(r, c->partials, s); }));
-      }
-      if (out_row) {
-        AttnArgs r = a;
-        r.M = 1;
-        r.q = c->q16 + static_cast<size_t>(M - 1) * c->q;
-        r.out = c->att + static_cast<size_t>(M - 1) * c->q;
-        r.pos_base = pos_base + M - 1;
-        const int n_keys = r.pos_base + 1;
-        PF_CUDA(c, counted(c, PF_KC_ATTN_ROW, 2, static_cast<double>(n_keys) * c->Hq * 4.0 * c->hd,
-                           n_keys * c->kv * 4.0 + c->q * 4.0,
-                           [&] { return launch_attn_split(r, c->row_partials, s); }));
+      if (!multi) {
+        // the output row takes the single-row attention, as in project()
+        const int m_rest = out_row ? M - 1 : M;  // rows for the prefill kernels
+        if (m_rest > 0) PF_CUDA(c, rows_attention(a, 0, m_rest, 0, pos_base, kv_len));
+        if (out_row) PF_CUDA(c, row_attention(a, M - 1, 0, pos_base + M - 1));
+      } else if (gathered) {
+        for (int j = 0; j < n_out; ++j) PF_CUDA(c, row_attention(a, j, runs[out_run[j]].seq, out_pos[j]));
+      } else {
+        // each sequence attends to its own cells; the output row of a
+        // finishing sequence takes the single-row attention in the KV-shared
+        // layers, as it does after the gather
+        for (const Run& r : runs) {
+          const bool single = !writes && r.last && row_kernels;
+          const int n_pre = single ? r.n - 1 : r.n;
+          const int keys = static_cast<int>(r.pos0) + r.n;
+          if (n_pre > 0) PF_CUDA(c, rows_attention(a, r.row0, n_pre, r.seq, static_cast<int>(r.pos0), keys));
+          if (single) PF_CUDA(c, row_attention(a, r.row0 + r.n - 1, r.seq, keys - 1));
+        }
       }
     }
     {
@@ -768,7 +889,7 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
                  return launch_rmsnorm(xcur, 0, M, D, c->out_norm, c->d.rms_eps, nullptr, fin, s, embd);
                }));
   }
-  if (is_last) {
+  if (is_last && !multi) {
     NvtxRange r_head("head");
     const int row = gathered ? 0 : T - 1;
     PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, D * 6.0, [&] {
@@ -781,8 +902,80 @@ extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, 
     e.ld_f32 = c->V;
     PF_CUDA(c, counted(c, gemm_class(1), 1, 2.0 * c->V * D, D * 2.0 + gemm_wbytes(c, c->V, D) + c->V * 4.0,
                        [&] { return launch_gemv(c->a_y, c->head, e, c->gv_sums, c->gv_tickets, s); }));
+  } else if (is_last) {
+    // one logits row per finishing sequence, in run order: their rows are
+    // normed into y (gathered: rows 0 .. n_out-1 of xr; else picked out of x)
+    // and projected together on the tensor cores
+    NvtxRange r_head("head");
+    PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, n_out * D * 6.0, [&] {
+               return launch_rmsnorm(xcur, 0, n_out, D, c->out_norm, c->d.rms_eps, c->y, nullptr, s, nullptr,
+                                     gathered ? nullptr : d_out_rows);
+             }));
+    EpiParams e;
+    e.kind = EPI_F32;
+    e.N = c->V;
+    e.out_f32 = logits;
+    e.ld_f32 = c->V;
+    PF_CUDA(c, counted(c, gemm_class(n_out), 1, 2.0 * n_out * c->V * D,
+                       n_out * D * 2.0 + gemm_wbytes(c, c->V, D) + n_out * c->V * 4.0,
+                       [&] { return launch_gemm(c->a_y, n_out, c->head, e, c->err, s); }));
   }
-  c->n_pos = kv_len;
+  for (const Run& r : runs) c->seq_pos[r.seq] = r.pos0 + r.n;
+  return PF_OK;
+}
+
+}  // namespace
+
+extern "C" int prefill_ubatch(prefill_ctx* c, const int32_t* tokens, int32_t T, int64_t pos0, int32_t is_last,
+                              float* logits) {
+  if (!c) return fail(nullptr, PF_E_ARG, "null context");
+  if (!tokens || T < 1 || T > c->d.ubatch_max) return fail(c, PF_E_ARG, "n_tokens outside [1, ubatch_max]");
+  if (pos0 != c->seq_pos[0]) return fail(c, PF_E_ARG, "pos0 must equal the cached position count");
+  if (pos0 + T > c->d.max_ctx) return fail(c, PF_E_ARG, "positions would exceed max_ctx");
+  std::vector<Run> runs(1);
+  runs[0].seq = 0;
+  runs[0].n = T;
+  runs[0].last = is_last ? 1 : 0;
+  runs[0].row0 = 0;
+  runs[0].pos0 = pos0;
+  return run_ubatch(c, tokens, T, runs, false, logits);
+}
+
+extern "C" int prefill_ubatch_seqs(prefill_ctx* c, const int32_t* tokens, const prefill_seq_run* runs, int32_t n_runs,
+                                   float* logits) {
+  if (!c) return fail(nullptr, PF_E_ARG, "null context");
+  if (!tokens || !runs || n_runs < 1 || n_runs > c->d.n_seq_max)
+    return fail(c, PF_E_ARG, "n_runs outside [1, n_seq_max]");
+  std::vector<Run> rs(n_runs);
+  std::vector<char> seen(c->d.n_seq_max, 0);
+  int T = 0;
+  for (int k = 0; k < n_runs; ++k) {
+    const prefill_seq_run& r = runs[k];
+    if (r.seq_id < 0 || r.seq_id >= c->d.n_seq_max) return fail(c, PF_E_ARG, "seq_id outside [0, n_seq_max)");
+    if (seen[r.seq_id]) return fail(c, PF_E_ARG, "a sequence appears in two runs of one ubatch");
+    seen[r.seq_id] = 1;
+    if (r.n_tokens < 1) return fail(c, PF_E_ARG, "a run without tokens");
+    if (c->seq_pos[r.seq_id] + r.n_tokens > c->d.max_ctx) return fail(c, PF_E_ARG, "positions would exceed max_ctx");
+    rs[k].seq = r.seq_id;
+    rs[k].n = r.n_tokens;
+    rs[k].last = r.is_last ? 1 : 0;
+    rs[k].row0 = T;
+    rs[k].pos0 = c->seq_pos[r.seq_id];
+    T += r.n_tokens;
+    if (T > c->d.ubatch_max) return fail(c, PF_E_ARG, "the runs hold more than ubatch_max tokens");
+  }
+  return run_ubatch(c, tokens, T, rs, true, logits);
+}
+
+extern "C" int64_t prefill_seq_n_pos(const prefill_ctx* c, int32_t seq_id) {
+  if (!c || seq_id < 0 || seq_id >= c->d.n_seq_max) return -1;
+  return c->seq_pos[seq_id];
+}
+
+extern "C" int prefill_seq_reset(prefill_ctx* c, int32_t seq_id) {
+  if (!c) return fail(nullptr, PF_E_ARG, "null context");
+  if (seq_id < 0 || seq_id >= c->d.n_seq_max) return fail(c, PF_E_ARG, "seq_id outside [0, n_seq_max)");
+  c->seq_pos[seq_id] = 0;
   return PF_OK;
 }
 
@@ -806,11 +999,11 @@ extern "C" int prefill_sync(prefill_ctx* c) {
   return check_device_error(c);
 }
 
-extern "C" int64_t prefill_n_pos(const prefill_ctx* c) { return c ? c->n_pos : -1; }
+extern "C" int64_t prefill_n_pos(const prefill_ctx* c) { return c ? c->seq_pos[0] : -1; }
 
 extern "C" int prefill_reset(prefill_ctx* c) {
   if (!c) return fail(nullptr, PF_E_ARG, "null context");
-  c->n_pos = 0;
+  std::fill(c->seq_pos.begin(), c->seq_pos.end(), 0);
   return PF_OK;
 }
 
@@ -858,7 +1051,7 @@ extern "C" int prefill_kv_header_check(const void* header16, int32_t n_layers_wr
 extern "C" int kv_save(prefill_ctx* c, void* dst, size_t dst_bytes) {
   if (!c || !dst) return fail(c, PF_E_ARG, "null argument");
   NvtxRange r_save("kv_save");
-  const int64_t n = c->n_pos;
+  const int64_t n = c->seq_pos[0];
   const int64_t need = prefill_kv_image_bytes(c, n);
   if (static_cast<int64_t>(dst_bytes) < need) return fail(c, PF_E_ARG, "destination smaller than the image");
   if (reinterpret_cast<uintptr_t>(dst) % 16 != 0) return fail(c, PF_E_ARG, "destination not 16-byte aligned");
@@ -868,10 +1061,12 @@ extern "C" int kv_save(prefill_ctx* c, void* dst, size_t dst_bytes) {
   h4[2] = c->L_w;
   h4[3] = c->kv;
   const size_t seg_bytes = static_cast<size_t>(n) * c->kv * 2;
-  const size_t cache_pitch = static_cast<size_t>(c->d.max_ctx) * c->kv * 2;
+  // sequence 0's cells of each layer; a layer holds n_seq_max sequences' cells
+  const int64_t layer_halves = static_cast<int64_t>(c->d.n_seq_max) * c->d.max_ctx * c->kv;
+  const size_t cache_pitch = static_cast<size_t>(layer_halves) * 2;
   if (is_device_ptr(dst)) {
     PF_CUDA(c, counted(c, PF_KC_OTHER, 1, 0.0, 2.0 * seg_bytes * 2 * c->L_w, [&] {
-               return launch_kv_copy(0, c->cache, static_cast<int64_t>(c->d.max_ctx) * c->kv, static_cast<uint8_t*>(dst),
+               return launch_kv_copy(0, c->cache, layer_halves, static_cast<uint8_t*>(dst),
                                      static_cast<int64_t>(seg_bytes), 2 * c->L_w, static_cast<int64_t>(seg_bytes), h4,
                                      c->stream);
              }));
@@ -908,11 +1103,13 @@ extern "C" int kv_load(prefill_ctx* c, const void* src, size_t src_bytes, int64_
   std::memcpy(&n_img, hdr + 4, 4);
   const size_t img_seg = static_cast<size_t>(n_img) * c->kv * 2;
   const size_t copy = static_cast<size_t>(n_pos) * c->kv * 2;
-  const size_t cache_pitch = static_cast<size_t>(c->d.max_ctx) * c->kv * 2;
+  // sequence 0's cells of each layer; a layer holds n_seq_max sequences' cells
+  const int64_t layer_halves = static_cast<int64_t>(c->d.n_seq_max) * c->d.max_ctx * c->kv;
+  const size_t cache_pitch = static_cast<size_t>(layer_halves) * 2;
   if (copy > 0) {
     if (dev) {
       PF_CUDA(c, counted(c, PF_KC_OTHER, 1, 0.0, 2.0 * copy * 2 * c->L_w, [&] {
-                 return launch_kv_copy(1, c->cache, static_cast<int64_t>(c->d.max_ctx) * c->kv,
+                 return launch_kv_copy(1, c->cache, layer_halves,
                                        const_cast<uint8_t*>(static_cast<const uint8_t*>(src)),
                                        static_cast<int64_t>(img_seg), 2 * c->L_w, static_cast<int64_t>(copy),
                                        reinterpret_cast<const int32_t*>(hdr), c->stream);
@@ -922,7 +1119,7 @@ extern "C" int kv_load(prefill_ctx* c, const void* src, size_t src_bytes, int64_
                                    2 * c->L_w, cudaMemcpyHostToDevice, c->stream));
     }
   }
-  c->n_pos = n_pos;
+  c->seq_pos[0] = n_pos;
   if (std::getenv("PREFILL_LOG"))
     std::fprintf(stderr, "KV cache loaded: %lld positions; skipping %lld cached prompt tokens\n", (long long)n_pos,
                  (long long)n_pos);
@@ -982,7 +1179,7 @@ extern "C" int prefill_kv_file_check(const char* path, int32_t n_layers_written,
 
 extern "C" int kv_save_file(prefill_ctx* c, const char* path) {
   if (!c || !path) return fail(c, PF_E_ARG, "null argument");
-  const int64_t bytes = prefill_kv_image_bytes(c, c->n_pos);
+  const int64_t bytes = prefill_kv_image_bytes(c, c->seq_pos[0]);
   std::vector<uint8_t> img(static_cast<size_t>(bytes) + 16);
   // 16-byte aligned staging inside the vector
   uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(img.data()) + 15) & ~uintptr_t(15));

@@ -490,3 +490,82 @@ def test_hidden_state_outputs_match_oracle(gpu, tiny):
         assert np.abs(buf[:b - a].cpu().numpy() - cap[1]).max() <= 2e-2 * np.abs(cap[1]).max()
     np.testing.assert_array_equal(logits.cpu().numpy(), ref)
     c1.close()
+
+
+def _multi_seq_check(w, ubatches, n_seq, max_ctx, ubatch_max, case):
+    """ubatches: [[(seq, tokens, is_last), ...], ...].  Runs them through one
+    context with pruning on and off; every finishing sequence's logits must
+    match its own oracle run (each sequence alone), and the two modes must
+    agree bit for bit."""
+    cfg = w.cfg
+    outs = {}
+    for prune in (True, False):
+        ctx = binding.PrefillContext(w, max_ctx=max_ctx, ubatch_max=ubatch_max, n_seq_max=n_seq, prune=prune)
+        got = []
+        for ub in ubatches:
+            toks = np.concatenate([t for _, t, _ in ub]).astype(np.int32)
+            runs = [(q, len(t), last) for q, t, last in ub]
+            n_last = sum(1 for r in runs if r[2])
+            lg = torch.full((max(n_last, 1), cfg["vocab"]), float("nan"), device="cuda")
+            ctx.ubatch_seqs(toks, runs, lg if n_last else None)
+            ctx.sync()
+            got += [lg[j].cpu().numpy().copy() for j in range(n_last)]
+        outs[prune] = got
+        ctx.close()
+    for a, b in zip(outs[True], outs[False]):
+        np.testing.assert_array_equal(a, b)
+    oracles = {}
+    want = []
+    for ub in ubatches:
+        for q, t, last in ub:
+            o = oracles.setdefault(q, OracleContext(cfg, w, max_ctx))
+            r = o.ubatch(t, bool(last))
+            if last:
+                want.append(r)
+    assert len(want) == len(outs[True])
+    for j, (g, wnt) in enumerate(zip(outs[True], want)):
+        check_logits(g, wnt, f"{case} output {j}")
+
+
+def test_multi_sequence_ubatches_match_oracle(gpu, tiny):
+    """Three sequences sharing one cache and one ubatch (ragged runs, a
+    sequence that finishes in the first ubatch, two that finish in the
+    second): each finishing sequence's logits against the oracle run on that
+    sequence alone, and the per-sequence gather bit-identical to the
+    unpruned pass."""
+    cfg = tiny.cfg
+    a = synth.make_tokens(cfg, 20, seed=31)
+    b = synth.make_tokens(cfg, 14, seed=32)
+    c = synth.make_tokens(cfg, 25, seed=33)
+    ubatches = [[(1, b[:9], False), (0, a[:12], False), (2, c, True)],
+                [(0, a[12:], True), (1, b[9:], True)]]
+    _multi_seq_check(tiny, ubatches, 3, 32, 64, "tiny multi-sequence")
+
+
+def test_multi_sequence_e2b_4x128(gpu, e2b):
+    cfg = e2b.cfg
+    ubatches = [[(q, synth.make_tokens(cfg, 128, seed=40 + q), True) for q in range(4)]]
+    _multi_seq_check(e2b, ubatches, 4, 128, 512, "e2b 4x128 multi-sequence")
+
+
+def test_multi_sequence_refusals(gpu, tiny):
+    cfg = tiny.cfg
+    ctx = binding.PrefillContext(tiny, max_ctx=32, ubatch_max=40, n_seq_max=2)
+    t = synth.make_tokens(cfg, 30, seed=3)
+    lg = torch.empty((2, cfg["vocab"]), device="cuda")
+    for runs in ([(0, 5, True), (0, 5, True)],          # one sequence twice
+                 [(2, 5, True)],                        # seq_id past n_seq_max
+                 [(0, 25, False), (1, 20, True)],       # more than ubatch_max tokens
+                 [(0, 0, True)]):                       # an empty run
+        with pytest.raises(binding.PrefillError) as e:
+            ctx.ubatch_seqs(t[:sum(r[1] for r in runs)] if sum(r[1] for r in runs) <= 30 else
+                            np.concatenate([t, t])[:sum(r[1] for r in runs)], runs, lg)
+        assert e.value.code == binding.PF_E_ARG
+    ctx.ubatch_seqs(t[:30], [(1, 30, False)])
+    ctx.sync()
+    assert ctx.seq_n_pos(1) == 30 and ctx.seq_n_pos(0) == 0
+    with pytest.raises(binding.PrefillError):
+        ctx.ubatch_seqs(t[:5], [(1, 5, True)], lg)     # 30 + 5 > max_ctx 32
+    ctx.seq_reset(1)
+    assert ctx.seq_n_pos(1) == 0
+    ctx.close()
