@@ -415,6 +415,60 @@ def run_prefix_reuse(dev, stream):
     return out
 
 
+def run_multi_seq(w, dev, stream, steps: int = 10):
+    """Four E2B sequences of 128 tokens in one ubatch of 512 over a unified
+    KV cache (the server setting of the Gemma 4 prefill news, section 5):
+    the per-sequence gather (pruning on), the unpruned pass, and the same
+    four prompts as four one-sequence prefills; ms per batch of four."""
+    import numpy as np
+    import torch
+
+    from prefill_kv_shared_gb300 import binding, synth
+    cfg = w.cfg
+    toks = [synth.make_tokens(cfg, 128, seed=40 + q) for q in range(4)]
+    flat = torch.from_numpy(np.concatenate(toks)).to(dev)
+    runs = [(q, 128, True) for q in range(4)]
+    lg = torch.empty((4, cfg["vocab"]), dtype=torch.float32, device=dev)
+    out = {"sequences": 4, "tokens_per_sequence": 128}
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / steps
+
+    ctx = binding.PrefillContext(w, max_ctx=128, ubatch_max=512, n_seq_max=4, stream=stream)
+
+    def batch():
+        ctx.reset()
+        ctx.ubatch_seqs(flat, runs, lg)
+    res = {}
+    for name, mode in (("gathered", True), ("unpruned", False)):
+        ctx.set_prune(mode)
+        out[f"{name}_ms"] = timed(batch)
+        res[name] = lg.cpu().numpy().copy()
+    ctx.close()
+    one = binding.PrefillContext(w, max_ctx=128, ubatch_max=128, stream=stream)
+    d_toks = [torch.from_numpy(t).to(dev) for t in toks]
+
+    def separate():
+        for q in range(4):
+            one.reset()
+            one.ubatch(d_toks[q], 0, True, lg[q])
+    out["four_single_sequence_ms"] = timed(separate)
+    one.close()
+    out["gathered_tokens_per_s"] = 512 / (out["gathered_ms"] * 1e-3)
+    out["gathered_vs_unpruned"] = out["unpruned_ms"] / out["gathered_ms"]
+    out["gathered_vs_single_sequence"] = out["four_single_sequence_ms"] / out["gathered_ms"]
+    out["gathered_equals_unpruned"] = bool(np.array_equal(res["gathered"], res["unpruned"]))
+    return out
+
+
 def run_cache_cli():
     """The command-line cache-file flow (PicoLM KV cache article, "usage" and
     "measured": a 25-token TinyLlama prompt, first run without the file,
@@ -703,6 +757,10 @@ def run_ours(args, dist: Dist):
             sweep["prefix_reuse_tinyllama"] = run_prefix_reuse(dev, stream)
         except Exception as e:  # recorded, never fatal to the line
             sweep["prefix_reuse_tinyllama"] = {"error": f"{type(e).__name__}: {e}"}
+        try:
+            sweep["multi_sequence_e2b_4x128"] = run_multi_seq(w, dev, stream)
+        except Exception as e:  # recorded, never fatal to the line
+            sweep["multi_sequence_e2b_4x128"] = {"error": f"{type(e).__name__}: {e}"}
         try:
             sweep["cache_file_cli_tinyllama_25"] = run_cache_cli()
         except Exception as e:  # recorded, never fatal to the line
