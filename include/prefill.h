@@ -204,6 +204,23 @@ int prefill_ubatch_seqs(prefill_ctx* ctx, const int32_t* tokens, const prefill_s
 int64_t prefill_seq_n_pos(const prefill_ctx* ctx, int32_t seq_id);
 int prefill_seq_reset(prefill_ctx* ctx, int32_t seq_id);
 
+/* ---- a recorded ubatch (CUDA graph) ----
+   prefill_graph_capture records one prefill_ubatch call (same arguments;
+   tokens must be device memory) into a CUDA graph held by the context,
+   without running it; prefill_graph_launch replays it on the context's
+   stream.  A replay computes what the recorded call computes for the
+   current contents of the tokens buffer: the same positions (pos0 ..
+   pos0 + n_tokens - 1), the same logits buffer, the pruning mode and
+   outputs in force when it was recorded; it needs the context's position
+   count to be pos0 (PF_E_ARG otherwise) and advances it like the call.
+   One kernel launch sequence of ~250 kernels becomes one graph launch.
+   Recording needs a context created on a non-default stream and per-launch
+   timing off; the launch counts of prefill_get_stats do not include
+   replays.  A new recording replaces the previous one. */
+int prefill_graph_capture(prefill_ctx* ctx, const int32_t* tokens, int32_t n_tokens, int64_t pos0, int32_t is_last,
+                          float* logits);
+int prefill_graph_launch(prefill_ctx* ctx);
+
 /* Wait for the context's stream and report device-side errors. */
 int prefill_sync(prefill_ctx* ctx);
 

@@ -48,6 +48,7 @@ EXPORTS = (
     "pfop_attention_split_noalloc", "pfop_attention_bench", "pfop_kv_copy_bench",
     "kv_save_file", "kv_load_file", "prefill_kv_file_check", "pfop_linear_row", "prefill_set_output",
     "pfop_linear_wait_test", "prefill_ubatch_seqs", "prefill_seq_n_pos", "prefill_seq_reset",
+    "prefill_graph_capture", "prefill_graph_launch",
 )
 
 
@@ -116,6 +117,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "prefill_ubatch_seqs": (C.c_int, [vp, vp, C.POINTER(SeqRun), i32, vp]),
         "prefill_seq_n_pos": (i64, [vp, i32]),
         "prefill_seq_reset": (C.c_int, [vp, i32]),
+        "prefill_graph_capture": (C.c_int, [vp, vp, i32, i64, i32, vp]),
+        "prefill_graph_launch": (C.c_int, [vp]),
         "prefill_n_pos": (i64, [vp]),
         "prefill_reset": (C.c_int, [vp]),
         "prefill_set_prune": (C.c_int, [vp, i32]),
@@ -362,6 +365,17 @@ class PrefillContext:
         if n_last:
             _buffer(logits, "logits", "float32", n_last * self.cfg["vocab"])
         self._check(self._lib.prefill_ubatch_seqs(self._h, _ptr(tokens), arr, len(runs), _ptr(logits)))
+
+    def graph_capture(self, tokens, pos0: int, is_last: bool, logits=None):
+        """Record one ubatch (tokens: int32 device tensor) for graph_launch."""
+        _buffer(tokens, "tokens", "int32")
+        if is_last:
+            _buffer(logits, "logits", "float32", self.cfg["vocab"])
+        self._check(self._lib.prefill_graph_capture(self._h, _ptr(tokens), tokens.numel(), pos0,
+                                                    1 if is_last else 0, _ptr(logits)))
+
+    def graph_launch(self):
+        self._check(self._lib.prefill_graph_launch(self._h))
 
     def seq_n_pos(self, seq_id: int) -> int:
         return int(self._lib.prefill_seq_n_pos(self._h, seq_id))

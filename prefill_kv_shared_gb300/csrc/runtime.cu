@@ -95,6 +95,10 @@ struct prefill_ctx {
   std::vector<int> rowinfo_host;
   __nv_bfloat16* ple_g = nullptr;  // per-layer-embedding rows of the gathered output rows
   int prune_enable = 1;  // PF_PRUNE_ON / PF_PRUNE_OFF / PF_PRUNE_OFF_PLAIN
+  // a recorded ubatch (prefill_graph_capture) and the positions it covers
+  cudaGraphExec_t graph = nullptr;
+  int64_t graph_pos0 = -1;
+  int graph_T = 0;
   std::string last_error;
 
   // launch accounting
@@ -114,6 +118,7 @@ struct prefill_ctx {
   // prefill_create gives up half way, so a failed create leaves no device
   // memory behind.
   ~prefill_ctx() {
+    if (graph) cudaGraphExecDestroy(graph);
     for (auto& t : timed) {
       cudaEventDestroy(t.e0);
       cudaEventDestroy(t.e1);
@@ -965,6 +970,51 @@ extern "C" int prefill_ubatch_seqs(prefill_ctx* c, const int32_t* tokens, const 
     if (T > c->d.ubatch_max) return fail(c, PF_E_ARG, "the runs hold more than ubatch_max tokens");
   }
   return run_ubatch(c, tokens, T, rs, true, logits);
+}
+
+extern "C" int prefill_graph_capture(prefill_ctx* c, const int32_t* tokens, int32_t T, int64_t pos0,
+                                     int32_t is_last, float* logits) {
+  if (!c) return fail(nullptr, PF_E_ARG, "null context");
+  if (!c->stream) return fail(c, PF_E_ARG, "recording needs a context created on a non-default stream");
+  if (c->timing) return fail(c, PF_E_ARG, "per-launch timing is on");
+  if (!tokens || !is_device_ptr(tokens)) return fail(c, PF_E_ARG, "recorded tokens must be device memory");
+  if (c->graph) {
+    cudaGraphExecDestroy(c->graph);
+    c->graph = nullptr;
+  }
+  const std::vector<int64_t> saved = c->seq_pos;
+  const prefill_stats saved_stats = c->stats;
+  // relaxed: the host-side queries the call makes (pointer kinds, device
+  // attributes) are allowed while the stream records
+  PF_CUDA(c, cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeRelaxed));
+  const int rc = prefill_ubatch(c, tokens, T, pos0, is_last, logits);
+  cudaGraph_t g = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(c->stream, &g);
+  // recording runs nothing: the positions and the launch counts stay as they were
+  c->seq_pos = saved;
+  c->stats = saved_stats;
+  if (rc != PF_OK) {
+    if (g) cudaGraphDestroy(g);
+    return rc;
+  }
+  if (e != cudaSuccess) return cuda_fail(c, e, "cudaStreamEndCapture");
+  cudaGraphExec_t x = nullptr;
+  const cudaError_t ei = cudaGraphInstantiate(&x, g, 0);
+  cudaGraphDestroy(g);
+  if (ei != cudaSuccess) return cuda_fail(c, ei, "cudaGraphInstantiate");
+  c->graph = x;
+  c->graph_pos0 = pos0;
+  c->graph_T = T;
+  return PF_OK;
+}
+
+extern "C" int prefill_graph_launch(prefill_ctx* c) {
+  if (!c) return fail(nullptr, PF_E_ARG, "null context");
+  if (!c->graph) return fail(c, PF_E_ARG, "no recorded ubatch");
+  if (c->seq_pos[0] != c->graph_pos0) return fail(c, PF_E_ARG, "the recorded ubatch starts at another position");
+  PF_CUDA(c, cudaGraphLaunch(c->graph, c->stream));
+  c->seq_pos[0] = c->graph_pos0 + c->graph_T;
+  return PF_OK;
 }
 
 extern "C" int64_t prefill_seq_n_pos(const prefill_ctx* c, int32_t seq_id) {

@@ -569,3 +569,40 @@ def test_multi_sequence_refusals(gpu, tiny):
     ctx.seq_reset(1)
     assert ctx.seq_n_pos(1) == 0
     ctx.close()
+
+
+def test_graph_replay_matches_stream_launches(gpu, e2b):
+    """A recorded E2B-512 ubatch replayed as one CUDA graph gives the logits
+    of the stream launches bit for bit, replay after replay, for whatever
+    the recorded token buffer holds; replays need the recorded position."""
+    cfg = e2b.cfg
+    s = torch.cuda.Stream()
+    ctx = binding.PrefillContext(e2b, max_ctx=512, ubatch_max=512, stream=s)
+    toks = [torch.from_numpy(synth.make_tokens(cfg, 512, seed=q)).cuda() for q in (1, 9)]
+    logits = torch.empty(cfg["vocab"], dtype=torch.float32, device="cuda")
+    want = []
+    for t in toks:
+        ctx.reset()
+        ctx.ubatch(t, 0, True, logits)
+        ctx.sync()
+        want.append(logits.cpu().numpy().copy())
+    buf = toks[0].clone()
+    ctx.reset()
+    with pytest.raises(binding.PrefillError) as e:
+        ctx.graph_capture(torch.from_numpy(np.zeros(4, np.int32)), 0, True, logits)  # host tokens
+    assert e.value.code == binding.PF_E_ARG
+    ctx.graph_capture(buf, 0, True, logits)
+    assert ctx.n_pos == 0
+    for rep in range(2):
+        for q, t in enumerate(toks):
+            buf.copy_(t)
+            torch.cuda.synchronize()
+            ctx.reset()
+            ctx.graph_launch()
+            assert ctx.n_pos == 512
+            ctx.sync()
+            np.testing.assert_array_equal(logits.cpu().numpy(), want[q])
+    with pytest.raises(binding.PrefillError) as e:
+        ctx.graph_launch()  # the recorded ubatch starts at position 0
+    assert e.value.code == binding.PF_E_ARG
+    ctx.close()
