@@ -1151,26 +1151,47 @@ __device__ __forceinline__ float q4_block_dot(uint4 nib, const float* x) {
   return r.x + r.y;
 }
 
+// Shared memory of a CTA: the row as fp32 [K] (only the part's columns are
+// filled), then (Q4_0 weights) the CTA's weight slice: the tile's k-blocks
+// kb0 .. kb1-1, contiguous in the tile layout, brought in by one bulk copy
+// that is issued before the wait for the previous kernel (weights never
+// depend on it), so the fetch overlaps that kernel's tail.
 template <int WK, int BN>
 __global__ void __launch_bounds__(GV_THREADS) gemv_kernel(const __nv_bfloat16* __restrict__ a, int K,
                                                           const uint8_t* __restrict__ w, int parts,
                                                           float* __restrict__ sums, int* __restrict__ tickets,
-                                                          const EpiParams ep_in) {
+                                                          const EpiParams ep_in, int* err) {
   constexpr int RG = BN / 32;          // 32-row groups of a tile
   constexpr int KW = GV_WARPS / RG;    // warps along k inside the CTA
-  extern __shared__ float xs[];        // the row, fp32 [K]
+  constexpr int TILE = BN * 36;        // bytes of one (tile, k-block) of Q4_0
+  extern __shared__ __align__(16) float xs[];  // the row, fp32 [K]; then the weight slice
   __shared__ float part_s[GV_WARPS][32];
   __shared__ float yv[BN];
   __shared__ EpiParams ep;
   __shared__ int last;
+  __shared__ __align__(8) uint64_t wbar;
   __shared__ __align__(16) uint8_t stage[2][EPI_STAGE_BYTES];
   const int nt = blockIdx.x / parts, kp = blockIdx.x % parts;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nkb = K / 64;
+  const int kb0 = kp * nkb / parts, kb1 = (kp + 1) * nkb / parts;
+  uint8_t* wsl = reinterpret_cast<uint8_t*>(xs + K);
+  if constexpr (WK == W_Q4) {
+    if (tid == 0) {
+      mbar_init(&wbar, 1);
+      fence_mbar_init();
+      if (kb1 > kb0) {
+        const uint32_t bytes = static_cast<uint32_t>(kb1 - kb0) * TILE;
+        mbar_arrive_expect_tx(&wbar, bytes);
+        bulk_load(wsl, w + ((size_t)nt * nkb + kb0) * TILE, bytes, &wbar);
+      } else {
+        mbar_arrive(&wbar);
+      }
+    }
+  }
   pdl_launch();
   if (tid == 0) ep = ep_in;
   pdl_wait();
-  const int nkb = K / 64;
-  const int kb0 = kp * nkb / parts, kb1 = (kp + 1) * nkb / parts;
   for (int i = kb0 * 8 + tid; i < kb1 * 8; i += GV_THREADS) {  // the part's columns, 8 at a time
     const uint4 u = reinterpret_cast<const uint4*>(a)[i];
     *reinterpret_cast<float4*>(xs + 8 * i) = bf16x4_to_f32(make_uint2(u.x, u.y));
@@ -1183,16 +1204,20 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_kernel(const __nv_bfloat16* _
   const int c0 = kb0 + kw * nk / KW, c1 = kb0 + (kw + 1) * nk / KW;
   float acc = 0.f;
   if constexpr (WK == W_Q4) {
-    const uint8_t* t0 = w + (size_t)nt * nkb * (BN * 36);
+    // bounded: a copy that never lands flags the error word; the sums are
+    // then meaningless, but the launch still ends
+    const bool landed = mbar_wait(&wbar, 0, err, PF_DEV_TIMEOUT_PRODUCER);
+    if (landed) {
 #pragma unroll 4
-    for (int kb = c0; kb < c1; ++kb) {
-      const uint8_t* t = t0 + (size_t)kb * (BN * 36);
-      const uint4 n0 = *reinterpret_cast<const uint4*>(t + r * 16);
-      const uint4 n1 = *reinterpret_cast<const uint4*>(t + (BN + r) * 16);
-      const float d0 = __half2float(*reinterpret_cast<const __half*>(t + BN * 32 + r * 2));
-      const float d1 = __half2float(*reinterpret_cast<const __half*>(t + BN * 32 + (BN + r) * 2));
-      acc = fmaf(d0, q4_block_dot(n0, xs + kb * 64), acc);
-      acc = fmaf(d1, q4_block_dot(n1, xs + kb * 64 + 32), acc);
+      for (int kb = c0; kb < c1; ++kb) {
+        const uint8_t* t = wsl + (size_t)(kb - kb0) * TILE;
+        const uint4 n0 = *reinterpret_cast<const uint4*>(t + r * 16);
+        const uint4 n1 = *reinterpret_cast<const uint4*>(t + (BN + r) * 16);
+        const float d0 = __half2float(*reinterpret_cast<const __half*>(t + BN * 32 + r * 2));
+        const float d1 = __half2float(*reinterpret_cast<const __half*>(t + BN * 32 + (BN + r) * 2));
+        acc = fmaf(d0, q4_block_dot(n0, xs + kb * 64), acc);
+        acc = fmaf(d1, q4_block_dot(n1, xs + kb * 64 + 32), acc);
+      }
     }
   } else {
     const __nv_bfloat16* wr = reinterpret_cast<const __nv_bfloat16*>(w) + (size_t)(nt * BN + r) * K;
@@ -1251,28 +1276,39 @@ size_t gemv_scratch_floats(const WeightMat& W) {
   return static_cast<size_t>(W.N_rows / W.BN) * gemv_parts(W) * W.BN;
 }
 
+// dynamic shared memory of a launch: the row (K floats) and, for Q4_0, the
+// largest weight slice of a k-part
+static size_t gemv_smem(const WeightMat& W, int parts) {
+  const int nkb = W.K / 64;
+  const size_t slice = W.kind == W_Q4 ? static_cast<size_t>((nkb + parts - 1) / parts) * W.BN * 36 : 0;
+  return static_cast<size_t>(W.K) * 4 + slice;
+}
+
+constexpr size_t GV_SMEM_MAX = 160 * 1024;
+
 template <int WK, int BN>
 static cudaError_t launch_gemv_t(const ActMat& A, const WeightMat& W, const EpiParams& ep, float* sums, int* tickets,
-                                 cudaStream_t s) {
-  const size_t smem = static_cast<size_t>(W.K) * 4;
+                                 int* err, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemv_kernel<WK, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    attr_err = cudaFuncSetAttribute(gemv_kernel<WK, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(GV_SMEM_MAX));
   });
   if (attr_err != cudaSuccess) return attr_err;
-  if (smem > 160 * 1024) return cudaErrorInvalidValue;
   const int parts = gemv_parts(W);
+  const size_t smem = gemv_smem(W, parts);
+  if (smem > GV_SMEM_MAX) return cudaErrorInvalidValue;
   const int grid = (W.N_rows / BN) * parts;
   return launch_k(gemv_kernel<WK, BN>, dim3(grid), dim3(GV_THREADS), smem, s, 1, A.dev, W.K,
-                  static_cast<const uint8_t*>(W.dev), parts, sums, tickets, ep);
+                  static_cast<const uint8_t*>(W.dev), parts, sums, tickets, ep, err);
 }
 
 cudaError_t launch_gemv(const ActMat& A, const WeightMat& W, const EpiParams& ep, float* sums, int* tickets,
-                        cudaStream_t s) {
+                        int* err, cudaStream_t s) {
   if (A.K != W.K || W.K % 64 != 0 || W.N_rows % W.BN != 0 || !sums || !tickets) return cudaErrorInvalidValue;
 #define PF_GEMV_CASE(WKV, BNV) \
-  if (W.kind == WKV && W.BN == BNV) return launch_gemv_t<WKV, BNV>(A, W, ep, sums, tickets, s);
+  if (W.kind == WKV && W.BN == BNV) return launch_gemv_t<WKV, BNV>(A, W, ep, sums, tickets, err, s);
   PF_GEMV_CASE(W_Q4, 64)
   PF_GEMV_CASE(W_Q4, 128)
   PF_GEMV_CASE(W_Q4, 256)

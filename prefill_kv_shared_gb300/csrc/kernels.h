@@ -100,9 +100,10 @@ cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiPar
 // streamed by CUDA cores over (tile, k-part) CTAs.  `sums` holds
 // gemv_scratch_floats(W) floats; `tickets` one int per tile, zero before the
 // first launch (each launch leaves them zero).  Launches sharing the
-// scratch must be stream-ordered.
+// scratch must be stream-ordered.  err: device error word (a weight copy
+// that never lands flags it after the bounded wait).
 cudaError_t launch_gemv(const ActMat& A, const WeightMat& W, const EpiParams& ep, float* sums, int* tickets,
-                        cudaStream_t s);
+                        int* err, cudaStream_t s);
 size_t gemv_scratch_floats(const WeightMat& W);
 
 // Host repack.  `rows[i]` points at the i-th stored row's source (Q4_0: K/32

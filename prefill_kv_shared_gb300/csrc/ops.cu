@@ -147,16 +147,19 @@ extern "C" int pfop_linear_row(int32_t wtype, const void* w_host, int32_t N, int
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* sums = nullptr;
   int* tickets = nullptr;
+  int* err = nullptr;
   OP_CUDA(sc.alloc(&sums, gemv_scratch_floats(W) * 4));
   OP_CUDA(sc.alloc(&tickets, static_cast<size_t>(W.N_rows / W.BN) * 4));
+  OP_CUDA(sc.alloc(&err, 16));
   OP_CUDA(cudaMemsetAsync(tickets, 0, static_cast<size_t>(W.N_rows / W.BN) * 4, s));
-  OP_CUDA(launch_gemv(A, W, e, sums, tickets, s));
+  OP_CUDA(cudaMemsetAsync(err, 0, 16, s));
+  OP_CUDA(launch_gemv(A, W, e, sums, tickets, err, s));
   if (iters > 0) {
     cudaEvent_t e0, e1;
     OP_CUDA(cudaEventCreate(&e0));
     OP_CUDA(cudaEventCreate(&e1));
     OP_CUDA(cudaEventRecord(e0, s));
-    for (int i = 0; i < iters; ++i) OP_CUDA(launch_gemv(A, W, e, sums, tickets, s));
+    for (int i = 0; i < iters; ++i) OP_CUDA(launch_gemv(A, W, e, sums, tickets, err, s));
     OP_CUDA(cudaEventRecord(e1, s));
     OP_CUDA(cudaEventSynchronize(e1));
     float ms = 0.f;
@@ -166,6 +169,9 @@ extern "C" int pfop_linear_row(int32_t wtype, const void* w_host, int32_t N, int
     *us = ms * 1000.f / iters;
   }
   OP_CUDA(cudaStreamSynchronize(s));
+  int h = 0;
+  OP_CUDA(cudaMemcpy(&h, err, 4, cudaMemcpyDeviceToHost));
+  if (h) return op_fail(PF_E_DEVICE_TIMEOUT, "one-row projection gave up a bounded wait, code " + std::to_string(h));
   return PF_OK;
 }
 

@@ -704,7 +704,7 @@ int run_ubatch(prefill_ctx* c, const int32_t* tokens, int T, std::vector<Run>& r
     a1.dev = A.dev + static_cast<size_t>(rows - 1) * A.K;
     const EpiParams e1 = shift_rows(e, rows - 1);
     return counted(c, PF_KC_GEMM_ROW, 1, flops_row, wbytes + io_row,
-                   [&] { return launch_gemv(a1, Wm, e1, c->gv_sums, c->gv_tickets, s); });
+                   [&] { return launch_gemv(a1, Wm, e1, c->gv_sums, c->gv_tickets, c->err, s); });
   };
   // the single-row attention of one output row
   auto row_attention = [&](const AttnArgs& base, int row, int seq, int pos) -> cudaError_t {
@@ -906,7 +906,7 @@ int run_ubatch(prefill_ctx* c, const int32_t* tokens, int T, std::vector<Run>& r
     e.out_f32 = logits;
     e.ld_f32 = c->V;
     PF_CUDA(c, counted(c, gemm_class(1), 1, 2.0 * c->V * D, D * 2.0 + gemm_wbytes(c, c->V, D) + c->V * 4.0,
-                       [&] { return launch_gemv(c->a_y, c->head, e, c->gv_sums, c->gv_tickets, s); }));
+                       [&] { return launch_gemv(c->a_y, c->head, e, c->gv_sums, c->gv_tickets, c->err, s); }));
   } else if (is_last) {
     // one logits row per finishing sequence, in run order: their rows are
     // normed into y (gathered: rows 0 .. n_out-1 of xr; else picked out of x)
