@@ -298,7 +298,14 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
 #pragma unroll
       for (int k = 0; k < CHUNK; ++k)
         if (k < nvis) mj = fmaxf(mj, __uint_as_float(sr[k >> 5][k & 31]));
-      const float mn = fmaxf(m, mj);
+      // The running max moves only when this chunk's max passes it by more
+      // than 2^8 in the exponent (or on the row's first visible keys): then
+      // O and l are rescaled; otherwise P is taken against the old max
+      // (p <= 2^8, exact in fp16 range) and O needs no touch, so the P V of
+      // successive chunks go to the tensor cores back to back.  O / l is the
+      // same softmax either way.
+      const bool grow = mj != -INFINITY && (m == -INFINITY || __fmul_rn(__fsub_rn(mj, m), cexp) > 8.f);
+      const float mn = grow ? mj : m;
       float lc = 0.f;
       uint32_t pw[32];  // 64 fp16 probabilities, two per word
 #pragma unroll
@@ -312,7 +319,8 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
         lc = __fadd_rn(lc, __low2float(h));
         lc = __fadd_rn(lc, __high2float(h));
       }
-      const float scale = (mn != -INFINITY && m != -INFINITY) ? ex2_approx(__fmul_rn(__fsub_rn(m, mn), cexp)) : 1.f;
+      const bool resc = grow && m != -INFINITY;  // an earlier max to move away from
+      const float scale = resc ? ex2_approx(__fmul_rn(__fsub_rn(m, mn), cexp)) : 1.f;
       l = __fadd_rn(__fmul_rn(l, scale), lc);
       m = mn;
       // P(j) goes to buffer s once P V(j-2) has read it
@@ -327,24 +335,25 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
         *reinterpret_cast<uint4*>(prow + ((q ^ (r & 7)) << 4)) =
             make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
       fence_proxy_async_smem();
-      // O *= scale once P V(j-1) has landed (chunk 0 overwrites O)
-      if (j >= 1) {
+      // O *= scale once P V(j-1) has landed (chunk 0 overwrites O), only in
+      // the warps where a row moved its max.  (Skipping the wait elsewhere is
+      // safe: P V(j+1) cannot complete before P(j+1) is written, so the next
+      // wait on this barrier still finds the phase it expects.)
+      if (j >= 1 && __any_sync(0xffffffffu, resc)) {
         if (lane == 0) ok = mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err, PF_DEV_TIMEOUT_EPILOGUE);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, scale != 1.f)) {
 #pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t x[32];
-            tmem_ld32(tmem + lane_base + C::TMEM_O + 32 * c, x);
-            tmem_ld_wait();
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t x[32];
+          tmem_ld32(tmem + lane_base + C::TMEM_O + 32 * c, x);
+          tmem_ld_wait();
 #pragma unroll
-            for (int q = 0; q < 32; ++q) x[q] = __float_as_uint(__fmul_rn(__uint_as_float(x[q]), scale));
-            tmem_st32(tmem + lane_base + C::TMEM_O + 32 * c, x);
-          }
-          tmem_st_wait();
+          for (int q = 0; q < 32; ++q) x[q] = __float_as_uint(__fmul_rn(__uint_as_float(x[q]), scale));
+          tmem_st32(tmem + lane_base + C::TMEM_O + 32 * c, x);
         }
+        tmem_st_wait();
       }
       tc_fence_before();
       __syncwarp();
