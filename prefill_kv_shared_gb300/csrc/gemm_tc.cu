@@ -34,6 +34,7 @@
 // same split boundaries and the same split order) whatever M is, so a row's
 // result does not depend on how many rows the launch carries.
 #include "common.cuh"
+#include "epilogue.cuh"
 #include "kernels.h"
 
 #include <cstring>
@@ -138,288 +139,6 @@ __device__ __forceinline__ void dequant_block32(uint4 nib, __half d, uint8_t* ro
   *reinterpret_cast<uint4*>(row_ptr + (((4 * h + 1) ^ sw) << 4)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
   *reinterpret_cast<uint4*>(row_ptr + (((4 * h + 2) ^ sw) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
   *reinterpret_cast<uint4*>(row_ptr + (((4 * h + 3) ^ sw) << 4)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-}
-
-// ---------------------------------------------------------------------------
-// Epilogue.
-//
-// tcgen05.ld (32x32b) gives each thread one accumulator row: a warp holds a
-// 32-row x 32-column block, one row per lane.  Written to global memory in
-// that layout every 16-byte access of a warp instruction falls in a
-// different row, so a 128-byte row segment costs eight separate
-// transactions.  Each block therefore goes through a warp-private 4 KB
-// staging buffer in shared memory, and global memory is touched with lane l
-// at row 4i + l/8, columns 4(l%8) .. 4(l%8)+3 (i = 0..7): every instruction
-// covers four whole 128-byte (fp32) or 64-byte (16-bit) row segments.
-
-constexpr int EPI_STAGE_BYTES = 32 * 32 * 4;
-
-// Row r's 16-byte piece p (columns 4p .. 4p+3) sits at r*128 + 16*(p ^ (r & 7)):
-// both the row-per-lane writes and the transposed reads are free of bank
-// conflicts.
-__device__ __forceinline__ void stage_put(uint8_t* st, int r, const float (&v)[32]) {
-#pragma unroll
-  for (int p = 0; p < 8; ++p)
-    *reinterpret_cast<float4*>(st + r * 128 + ((p ^ (r & 7)) << 4)) =
-        make_float4(v[4 * p], v[4 * p + 1], v[4 * p + 2], v[4 * p + 3]);
-}
-__device__ __forceinline__ float4 stage_get(const uint8_t* st, int r, int p) {
-  return *reinterpret_cast<const float4*>(st + r * 128 + ((p ^ (r & 7)) << 4));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
-  __half2 v = __floats2half2_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-__device__ __forceinline__ uint2 pack_bf16x4(float4 a) {
-  return make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
-}
-__device__ __forceinline__ uint2 pack_half4(float4 a) { return make_uint2(pack_half2(a.x, a.y), pack_half2(a.z, a.w)); }
-__device__ __forceinline__ float comp(const float4& a, int e) { return e == 0 ? a.x : e == 1 ? a.y : e == 2 ? a.z : a.w; }
-__device__ __forceinline__ float4 bf16x4_to_f32(uint2 p) {
-  return make_float4(__uint_as_float(p.x << 16), __uint_as_float(p.x & 0xFFFF0000u), __uint_as_float(p.y << 16),
-                     __uint_as_float(p.y & 0xFFFF0000u));
-}
-
-// The fused epilogue for one warp's 32 rows of one tile: output rows
-// m0 .. m0+31, of which the first rv are real (warp-uniform).  load(c, v)
-// fills v with this lane's row (m0 + lane) of the tile's column chunk c
-// (columns 32c .. 32c+31) and is called in a warp-uniform way.  The two
-// epilogue warps of a lane quarter (ew = 0, 1) take alternate work items.
-// st: the warp's staging buffer.
-template <int BN, class Load>
-__device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m0, int rv, int n_tile, int ew, uint8_t* st,
-                                             Load&& load) {
-  constexpr int NCH = BN / 32;
-  if (rv <= 0) return;
-  const int lane = threadIdx.x & 31;
-  const int rs = lane >> 3, p = lane & 7;  // transposed position: rows 4i + rs, columns 4p .. 4p+3
-  const int n0 = n_tile * BN;
-  float v[32];
-  // Every kind below first computes all of a block's values into registers
-  // and only then stores them: a global load placed after a store in
-  // program order waits for it, which would put one memory round trip on
-  // every row of the block.
-
-  if (ep.kind == EPI_GLU) {
-    // gate chunk c and up chunk c + NCH/2 of the interleaved tile -> output
-    // columns f0 .. f0+31
-    constexpr int HALF_CH = NCH / 2;
-    for (int c = ew; c < HALF_CH; c += 2) {
-      const int f0 = n_tile * (BN / 2) + 32 * c;
-      if (f0 >= ep.N) break;
-      load(c, v);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = ep.act == 0 ? gelu_tanh_f(v[j]) : silu_f(v[j]);
-      {
-        float u[32];
-        load(c + HALF_CH, u);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] *= u[j];
-      }
-      stage_put(st, lane, v);
-      __syncwarp();
-      uint2 h[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) h[i] = pack_bf16x4(stage_get(st, 4 * i + rs, p));
-      __syncwarp();
-      const int col = f0 + 4 * p;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = 4 * i + rs;
-        if (r >= rv || col >= ep.N) continue;
-        __nv_bfloat16* dst = ep.out_bf16 + (size_t)(m0 + r) * ep.ld_bf16 + col;
-        if (col + 4 <= ep.N) {
-          *reinterpret_cast<uint2*>(dst) = h[i];
-        } else {
-          for (int e = 0; col + e < ep.N; ++e) {
-            const uint32_t w = e < 2 ? h[i].x : h[i].y;
-            dst[e] = __ushort_as_bfloat16(static_cast<unsigned short>(w >> (16 * (e & 1))));
-          }
-        }
-      }
-    }
-    return;
-  }
-
-  if (ep.kind == EPI_QKV) {
-    // Q | K | V columns; Q and K rotated (half-split RoPE at position
-    // pos0 + row) and written as fp16, V written as fp16 to the cache.  A
-    // rotated chunk is handled together with its partner half a head away:
-    // with whole heads in a tile (hd <= BN) the partner is half/32 chunks
-    // further; with heads wider than the tile, a tile holds BN/2 dims of the
-    // head's first half and the same BN/2 dims of its second half
-    // (qkv_tile_rows), and the partner is NCH/2 chunks further.
-    const int hd = ep.head_dim, half = hd / 2, pair_ch = half / 32;
-    const bool split_heads = hd > BN;
-    const int q_end = ep.q_dim, k_end = ep.q_dim + ep.kv_dim, v_end = ep.q_dim + 2 * ep.kv_dim;
-    int item = 0;
-    for (int c = 0; c < NCH; ++c) {
-      const int n = n0 + 32 * c;
-      if (n >= v_end) break;  // padding columns
-      if (n >= k_end) {       // V: no rotation
-        if ((item++ & 1) != ew) continue;
-        load(c, v);
-        stage_put(st, lane, v);
-        __syncwarp();
-        uint2 h[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) h[i] = pack_half4(stage_get(st, 4 * i + rs, p));
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = 4 * i + rs;
-          if (r >= rv) continue;
-          const int slot = ep.row_slot ? ep.row_slot[m0 + r] : ep.pos0 + m0 + r;
-          *reinterpret_cast<uint2*>(ep.v_cache + (size_t)slot * ep.kv_dim + (n - k_end) + 4 * p) = h[i];
-        }
-        continue;
-      }
-      const bool is_q = n < q_end;
-      const int rel = is_q ? n : n - q_end;
-      int i0, head, partner;
-      if (split_heads) {
-        const int tile = rel / BN, x = rel % BN;
-        if (x >= BN / 2) continue;  // handled together with its partner chunk
-        head = tile / (hd / BN);
-        i0 = (tile % (hd / BN)) * (BN / 2) + x;
-        partner = c + NCH / 2;
-      } else {
-        i0 = rel % hd;
-        if (i0 >= half) continue;  // handled together with its partner chunk
-        head = rel / hd;
-        partner = c + pair_ch;
-      }
-      if ((item++ & 1) != ew) continue;
-      // two passes of 16 rows each keep the transposed halves in registers
-      for (int hp = 0; hp < 2; ++hp) {
-        float4 c01[4], c23[4];  // (cos, sin) of columns i0+4p .. i0+4p+3 at each row's position
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = 16 * hp + 4 * i + rs;
-          const int m = m0 + (r < rv ? r : 0);
-          const int pos = ep.row_pos ? ep.row_pos[m] : ep.pos0 + m;
-          const float4* cs = reinterpret_cast<const float4*>(ep.rope + (size_t)pos * half + i0 + 4 * p);
-          c01[i] = cs[0];
-          c23[i] = cs[1];
-        }
-        float4 vt[4], ut[4];
-        load(c, v);
-        stage_put(st, lane, v);
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) vt[i] = stage_get(st, 16 * hp + 4 * i + rs, p);
-        __syncwarp();
-        load(partner, v);
-        stage_put(st, lane, v);
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) ut[i] = stage_get(st, 16 * hp + 4 * i + rs, p);
-        __syncwarp();
-        uint2 o1[4], o2[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 a = vt[i], b = ut[i], x = c01[i], y = c23[i];
-          o1[i] = pack_half4(make_float4(a.x * x.x - b.x * x.y, a.y * x.z - b.y * x.w, a.z * y.x - b.z * y.y,
-                                         a.w * y.z - b.w * y.w));
-          o2[i] = pack_half4(make_float4(a.x * x.y + b.x * x.x, a.y * x.w + b.y * x.z, a.z * y.y + b.z * y.x,
-                                         a.w * y.w + b.w * y.z));
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = 16 * hp + 4 * i + rs;
-          if (r >= rv) continue;
-          const int m = m0 + r;
-          const int slot = ep.row_slot ? ep.row_slot[m] : ep.pos0 + m;
-          __half* dst = is_q ? ep.q_out + (size_t)m * ep.q_dim + head * hd
-                             : ep.k_cache + (size_t)slot * ep.kv_dim + head * hd;
-          *reinterpret_cast<uint2*>(dst + i0 + 4 * p) = o1[i];
-          *reinterpret_cast<uint2*>(dst + i0 + half + 4 * p) = o2[i];
-        }
-        if (rv <= 16) break;
-      }
-    }
-    return;
-  }
-
-  // F32, RESID, PLE: one 32-column chunk at a time.  The chunk's global
-  // operand (RESID: the residual rows; PLE: the multipliers) is requested
-  // before the TMEM load so that its latency overlaps the staging.
-  for (int c = ew; c < NCH; c += 2) {
-    const int n = n0 + 32 * c;
-    if (n >= ep.N) break;
-    const int col = n + 4 * p;
-    const bool full = col + 4 <= ep.N;
-    float4 side[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int r = 4 * i + rs;
-      side[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (r >= rv || col >= ep.N) continue;
-      if (ep.kind == EPI_RESID) {
-        const float* xr = ep.out_f32 + (size_t)(m0 + r) * ep.ld_f32 + col;
-        if (full) {
-          side[i] = *reinterpret_cast<const float4*>(xr);
-        } else {
-          side[i].x = xr[0];
-          if (col + 1 < ep.N) side[i].y = xr[1];
-          if (col + 2 < ep.N) side[i].z = xr[2];
-        }
-      } else if (ep.kind == EPI_PLE) {
-        const __nv_bfloat16* pl = ep.ple + (size_t)(m0 + r) * ep.ple_stride + col;
-        if (full) {
-          side[i] = bf16x4_to_f32(*reinterpret_cast<const uint2*>(pl));
-        } else {
-          side[i].x = __bfloat162float(pl[0]);
-          if (col + 1 < ep.N) side[i].y = __bfloat162float(pl[1]);
-          if (col + 2 < ep.N) side[i].z = __bfloat162float(pl[2]);
-        }
-      }
-    }
-    load(c, v);
-    stage_put(st, lane, v);
-    __syncwarp();
-    // values of the block in the transposed layout (RESID: the new residual;
-    // PLE: gelu(acc) * multiplier, before rounding)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float4 a = stage_get(st, 4 * i + rs, p);
-      const float4 g = side[i];
-      if (ep.kind == EPI_RESID) {
-        side[i] = make_float4(g.x + a.x, g.y + a.y, g.z + a.z, g.w + a.w);
-      } else if (ep.kind == EPI_PLE) {
-        side[i] = make_float4(gelu_tanh_f(a.x) * g.x, gelu_tanh_f(a.y) * g.y, gelu_tanh_f(a.z) * g.z,
-                              gelu_tanh_f(a.w) * g.w);
-      } else {
-        side[i] = a;
-      }
-    }
-    __syncwarp();
-    if (col < ep.N) {
-      float* of = ep.kind != EPI_PLE ? ep.out_f32 : nullptr;                        // fp32 result
-      __nv_bfloat16* ob = ep.kind != EPI_F32 ? ep.out_bf16 : nullptr;               // bf16 result (RESID: optional copy)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = 4 * i + rs;
-        if (r >= rv) continue;
-        const size_t m = static_cast<size_t>(m0 + r);
-        const float4 a = side[i];
-        if (full) {
-          if (of) *reinterpret_cast<float4*>(of + m * ep.ld_f32 + col) = a;
-          if (ob) *reinterpret_cast<uint2*>(ob + m * ep.ld_bf16 + col) = pack_bf16x4(a);
-        } else {
-          for (int e = 0; col + e < ep.N; ++e) {
-            if (of) of[m * ep.ld_f32 + col + e] = comp(a, e);
-            if (ob) ob[m * ep.ld_bf16 + col + e] = __float2bfloat16_rn(comp(a, e));
-          }
-        }
-      }
-    }
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1071,251 +790,6 @@ cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiPar
   PF_GEMM_CASE(W_BF16, 128)
   PF_GEMM_CASE(W_BF16, 256)
 #undef PF_GEMM_CASE
-  return cudaErrorInvalidValue;
-}
-
-// ---------------------------------------------------------------------------
-// one-token projections
-//
-// A ubatch of one token (generation after the prompt) reads every weight
-// once for one row, which the tensor-core kernel serves badly (its MMAs are
-// 128 rows tall and it is bound per pipeline stage).  Here CTAs take
-// (tile, k-part) pairs of a weight matrix in the GEMM's tile layout: the
-// tile's BN rows over 32-row groups of lanes, the k-part's 64-wide k-blocks
-// over the remaining warps, plain 16-byte loads of the Q4_0 tiles (or bf16
-// rows), fp32 dot products (a Q4_0 value d*(n-8) is exact in fp32).  Each
-// CTA writes its part's row sums; the last CTA of a tile to finish adds the
-// parts in part order and runs the GEMM's fused epilogue on the tile's one
-// output row.  The bits depend only on the matrix shape and the part count
-// (a function of the shape), not on which CTA finishes last.
-constexpr int GV_WARPS = 8;
-constexpr int GV_THREADS = GV_WARPS * 32;
-constexpr int GV_TARGET_CTAS = 304;  // about two CTAs per SM
-
-// Two fp32 lanes in one 64-bit register pair, for the packed arithmetic
-// of sm_100-class SMs (sub.rn.f32x2 / fma.rn.f32x2: one instruction for two
-// independent fp32 operations, each rounded as its scalar form would be).
-__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ float2 f2_unpack(unsigned long long v) {
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-  return r;
-}
-__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {
-  unsigned long long r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
-                                                     unsigned long long c) {
-  unsigned long long r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-
-// sum over one 32-element Q4_0 block: byte j holds element j (low nibble)
-// and element j + 16 (high nibble); x: the block's 32 activations.  A
-// nibble n becomes the float 2^23 + n by placing it under the exponent byte
-// of 2^23 (one byte permute, no integer-to-float conversion), and
-// (2^23 + n) - (2^23 + 8) = n - 8 exactly.  The subtraction and the
-// multiply-add run two elements per instruction (packed f32x2) on two
-// chains: the even and the odd elements of each group of four, added at
-// the end.
-__device__ __forceinline__ float q4_block_dot(uint4 nib, const float* x) {
-  const uint32_t wds[4] = {nib.x, nib.y, nib.z, nib.w};
-  const unsigned long long bias = f2_pack(8388616.0f, 8388616.0f);  // 2^23 + 8
-  unsigned long long s = 0ull;  // (+0, +0)
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float4 xl = *reinterpret_cast<const float4*>(x + 4 * q);
-    const float4 xh = *reinterpret_cast<const float4*>(x + 16 + 4 * q);
-    const uint32_t lo = wds[q] & 0x0F0F0F0Fu, hi = (wds[q] >> 4) & 0x0F0F0F0Fu;
-    const unsigned long long l01 = f2_pack(__int_as_float(__byte_perm(lo, 0x4B000000u, 0x7440)),
-                                           __int_as_float(__byte_perm(lo, 0x4B000000u, 0x7441)));
-    const unsigned long long l23 = f2_pack(__int_as_float(__byte_perm(lo, 0x4B000000u, 0x7442)),
-                                           __int_as_float(__byte_perm(lo, 0x4B000000u, 0x7443)));
-    const unsigned long long h01 = f2_pack(__int_as_float(__byte_perm(hi, 0x4B000000u, 0x7440)),
-                                           __int_as_float(__byte_perm(hi, 0x4B000000u, 0x7441)));
-    const unsigned long long h23 = f2_pack(__int_as_float(__byte_perm(hi, 0x4B000000u, 0x7442)),
-                                           __int_as_float(__byte_perm(hi, 0x4B000000u, 0x7443)));
-    s = f2_fma(f2_sub(l01, bias), f2_pack(xl.x, xl.y), s);
-    s = f2_fma(f2_sub(l23, bias), f2_pack(xl.z, xl.w), s);
-    s = f2_fma(f2_sub(h01, bias), f2_pack(xh.x, xh.y), s);
-    s = f2_fma(f2_sub(h23, bias), f2_pack(xh.z, xh.w), s);
-  }
-  const float2 r = f2_unpack(s);
-  return r.x + r.y;
-}
-
-// Shared memory of a CTA: the row as fp32 [K] (only the part's columns are
-// filled), then (Q4_0 weights) the CTA's weight slice: the tile's k-blocks
-// kb0 .. kb1-1, contiguous in the tile layout, brought in by one bulk copy
-// that is issued before the wait for the previous kernel (weights never
-// depend on it), so the fetch overlaps that kernel's tail.
-template <int WK, int BN>
-__global__ void __launch_bounds__(GV_THREADS) gemv_kernel(const __nv_bfloat16* __restrict__ a, int K,
-                                                          const uint8_t* __restrict__ w, int parts,
-                                                          float* __restrict__ sums, int* __restrict__ tickets,
-                                                          const EpiParams ep_in, int* err) {
-  constexpr int RG = BN / 32;          // 32-row groups of a tile
-  constexpr int KW = GV_WARPS / RG;    // warps along k inside the CTA
-  constexpr int TILE = BN * 36;        // bytes of one (tile, k-block) of Q4_0
-  extern __shared__ __align__(16) float xs[];  // the row, fp32 [K]; then the weight slice
-  __shared__ float part_s[GV_WARPS][32];
-  __shared__ float yv[BN];
-  __shared__ EpiParams ep;
-  __shared__ int last;
-  __shared__ __align__(8) uint64_t wbar;
-  __shared__ __align__(16) uint8_t stage[2][EPI_STAGE_BYTES];
-  const int nt = blockIdx.x / parts, kp = blockIdx.x % parts;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nkb = K / 64;
-  const int kb0 = kp * nkb / parts, kb1 = (kp + 1) * nkb / parts;
-  uint8_t* wsl = reinterpret_cast<uint8_t*>(xs + K);
-  if constexpr (WK == W_Q4) {
-    if (tid == 0) {
-      mbar_init(&wbar, 1);
-      fence_mbar_init();
-      if (kb1 > kb0) {
-        const uint32_t bytes = static_cast<uint32_t>(kb1 - kb0) * TILE;
-        mbar_arrive_expect_tx(&wbar, bytes);
-        bulk_load(wsl, w + ((size_t)nt * nkb + kb0) * TILE, bytes, &wbar);
-      } else {
-        mbar_arrive(&wbar);
-      }
-    }
-  }
-  pdl_launch();
-  if (tid == 0) ep = ep_in;
-  pdl_wait();
-  for (int i = kb0 * 8 + tid; i < kb1 * 8; i += GV_THREADS) {  // the part's columns, 8 at a time
-    const uint4 u = reinterpret_cast<const uint4*>(a)[i];
-    *reinterpret_cast<float4*>(xs + 8 * i) = bf16x4_to_f32(make_uint2(u.x, u.y));
-    *reinterpret_cast<float4*>(xs + 8 * i + 4) = bf16x4_to_f32(make_uint2(u.z, u.w));
-  }
-  __syncthreads();
-  const int rg = warp % RG, kw = warp / RG;
-  const int r = rg * 32 + lane;
-  const int nk = kb1 - kb0;
-  const int c0 = kb0 + kw * nk / KW, c1 = kb0 + (kw + 1) * nk / KW;
-  float acc = 0.f;
-  if constexpr (WK == W_Q4) {
-    // bounded: a copy that never lands flags the error word; the sums are
-    // then meaningless, but the launch still ends
-    const bool landed = mbar_wait(&wbar, 0, err, PF_DEV_TIMEOUT_PRODUCER);
-    if (landed) {
-#pragma unroll 4
-      for (int kb = c0; kb < c1; ++kb) {
-        const uint8_t* t = wsl + (size_t)(kb - kb0) * TILE;
-        const uint4 n0 = *reinterpret_cast<const uint4*>(t + r * 16);
-        const uint4 n1 = *reinterpret_cast<const uint4*>(t + (BN + r) * 16);
-        const float d0 = __half2float(*reinterpret_cast<const __half*>(t + BN * 32 + r * 2));
-        const float d1 = __half2float(*reinterpret_cast<const __half*>(t + BN * 32 + (BN + r) * 2));
-        acc = fmaf(d0, q4_block_dot(n0, xs + kb * 64), acc);
-        acc = fmaf(d1, q4_block_dot(n1, xs + kb * 64 + 32), acc);
-      }
-    }
-  } else {
-    const __nv_bfloat16* wr = reinterpret_cast<const __nv_bfloat16*>(w) + (size_t)(nt * BN + r) * K;
-#pragma unroll 2
-    for (int k = c0 * 64; k < c1 * 64; k += 8) {
-      const uint4 u = *reinterpret_cast<const uint4*>(wr + k);
-      const float4 w0 = bf16x4_to_f32(make_uint2(u.x, u.y)), w1 = bf16x4_to_f32(make_uint2(u.z, u.w));
-      const float4 x0 = *reinterpret_cast<const float4*>(xs + k), x1 = *reinterpret_cast<const float4*>(xs + k + 4);
-      acc = fmaf(w0.x, x0.x, acc);
-      acc = fmaf(w0.y, x0.y, acc);
-      acc = fmaf(w0.z, x0.z, acc);
-      acc = fmaf(w0.w, x0.w, acc);
-      acc = fmaf(w1.x, x1.x, acc);
-      acc = fmaf(w1.y, x1.y, acc);
-      acc = fmaf(w1.z, x1.z, acc);
-      acc = fmaf(w1.w, x1.w, acc);
-    }
-  }
-  part_s[warp][lane] = acc;
-  __syncthreads();
-  if (tid < BN) {
-    const int g = tid >> 5, l = tid & 31;
-    float t = part_s[g][l];
-    for (int q = 1; q < KW; ++q) t += part_s[q * RG + g][l];
-    sums[((size_t)nt * parts + kp) * BN + tid] = t;
-  }
-  // the last CTA of the tile adds the parts in order and runs the epilogue
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) last = atomicAdd(&tickets[nt], 1) == parts - 1;
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  if (tid < BN) {
-    float t = __ldcg(sums + (size_t)nt * parts * BN + tid);
-    for (int q = 1; q < parts; ++q) t += __ldcg(sums + ((size_t)nt * parts + q) * BN + tid);
-    yv[tid] = t;
-  }
-  if (tid == 0) tickets[nt] = 0;  // ready for the next launch
-  __syncthreads();
-  if (warp < 2)
-    run_epilogue<BN>(ep, 0, 1, nt, warp, stage[warp], [&](int c, float(&v)[32]) {
-#pragma unroll
-      for (int q = 0; q < 32; ++q) v[q] = lane == 0 ? yv[32 * c + q] : 0.f;
-    });
-}
-
-int gemv_parts(const WeightMat& W) {
-  const int n_tiles = W.N_rows / W.BN, nkb = W.K / 64;
-  int p = (GV_TARGET_CTAS + n_tiles - 1) / n_tiles;
-  if (p > nkb) p = nkb;
-  return p < 1 ? 1 : p;
-}
-
-size_t gemv_scratch_floats(const WeightMat& W) {
-  return static_cast<size_t>(W.N_rows / W.BN) * gemv_parts(W) * W.BN;
-}
-
-// dynamic shared memory of a launch: the row (K floats) and, for Q4_0, the
-// largest weight slice of a k-part
-static size_t gemv_smem(const WeightMat& W, int parts) {
-  const int nkb = W.K / 64;
-  const size_t slice = W.kind == W_Q4 ? static_cast<size_t>((nkb + parts - 1) / parts) * W.BN * 36 : 0;
-  return static_cast<size_t>(W.K) * 4 + slice;
-}
-
-constexpr size_t GV_SMEM_MAX = 160 * 1024;
-
-template <int WK, int BN>
-static cudaError_t launch_gemv_t(const ActMat& A, const WeightMat& W, const EpiParams& ep, float* sums, int* tickets,
-                                 int* err, cudaStream_t s) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemv_kernel<WK, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(GV_SMEM_MAX));
-  });
-  if (attr_err != cudaSuccess) return attr_err;
-  const int parts = gemv_parts(W);
-  const size_t smem = gemv_smem(W, parts);
-  if (smem > GV_SMEM_MAX) return cudaErrorInvalidValue;
-  const int grid = (W.N_rows / BN) * parts;
-  return launch_k(gemv_kernel<WK, BN>, dim3(grid), dim3(GV_THREADS), smem, s, 1, A.dev, W.K,
-                  static_cast<const uint8_t*>(W.dev), parts, sums, tickets, ep, err);
-}
-
-cudaError_t launch_gemv(const ActMat& A, const WeightMat& W, const EpiParams& ep, float* sums, int* tickets,
-                        int* err, cudaStream_t s) {
-  if (A.K != W.K || W.K % 64 != 0 || W.N_rows % W.BN != 0 || !sums || !tickets) return cudaErrorInvalidValue;
-#define PF_GEMV_CASE(WKV, BNV) \
-  if (W.kind == WKV && W.BN == BNV) return launch_gemv_t<WKV, BNV>(A, W, ep, sums, tickets, err, s);
-  PF_GEMV_CASE(W_Q4, 64)
-  PF_GEMV_CASE(W_Q4, 128)
-  PF_GEMV_CASE(W_Q4, 256)
-  PF_GEMV_CASE(W_BF16, 64)
-  PF_GEMV_CASE(W_BF16, 128)
-  PF_GEMV_CASE(W_BF16, 256)
-#undef PF_GEMV_CASE
   return cudaErrorInvalidValue;
 }
 
