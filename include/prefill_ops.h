@@ -147,15 +147,17 @@ int pfop_kv_copy_bench(int32_t dir, void* cache_dev, int64_t cache_seg_halves, v
    q fp16 [Hq*hd] at position pos; K/V fp16 [positions][Hkv*hd] with keys
    [0, kv_len) valid, pos < kv_len; out bf16 [Hq*hd].
    Scratch: one fixed device array of 2^19 floats (2 MiB) per GPU that loads
-   the library, kept until exit.  A call needs Hq*R*(hd+4) floats, R being
-   the number of key ranges of pfop_attention's mode 1 (at most 148/Hkv), plus
-   4 for an error word: up to 8 query heads of 256 fit at any length;
-   larger requests return PF_E_ARG without touching the GPU, and so do
+   the library, kept until exit.  A call needs the merge tickets (Hkv ints,
+   rounded up to 4) and Hkv*C*(Hq/Hkv*hd + 32) floats of folded states, C
+   being the clusters of four key ranges per KV head (at most 36/Hkv, at
+   least 1), plus 4 for an error word: any shape of up to 1024 query heads
+   of 256 fits; larger requests return PF_E_ARG without touching the GPU,
+   and so do
    shapes the kernels do not take (head_dim other than 64 or 256, n_head not
    a multiple of n_head_kv, a group size not dividing 16, q/k/v not 16-byte
-   aligned).  All calls share
-   the array, so calls that overlap on the GPU race: order them on one stream
-   or with events.  The first call on a device looks up the array's device
+   aligned).  All calls share the array, so calls that overlap on the GPU
+   race: order them on one stream or with events.  Each call clears the
+   tickets it uses.  The first call on a device looks up the array's device
    address with that device current (cudaGetSymbolAddress); make that first
    call before capturing any stream.  Synchronous on `stream`. */
 int pfop_attention_split_noalloc(const void* q_dev, const void* k_dev, const void* v_dev, int32_t Hq, int32_t Hkv,

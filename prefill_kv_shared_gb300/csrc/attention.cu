@@ -579,18 +579,24 @@ cudaError_t launch_attn_prefill(const AttnArgs& a, float* partials, cudaStream_t
 // once, so its cost is the K/V bytes (G4 section 1: after the pruning the
 // KV-shared layers carry only the output row).  The keys are cut into 64-key
 // tiles and the tiles of each KV head into `splits` consecutive ranges, sized
-// so that about ATTN_ROW_CTAS CTAs stream the cache together.  A CTA (range,
+// so that the clusters that fit on the GPU at once stream the cache together.  A CTA (range,
 // KV head) copies its K and V tiles through a TMA ring, forms the scores of
 // the KV head's G query heads and P V with mma.sync (m16n8k16: rows are the
 // G query heads, zero rows above G; fp32 accumulation), runs the online
-// softmax over its tiles and writes its state (o unnormalised, m, l) per
-// query head.  attn_row_merge_kernel combines a head's ranges in a fixed
-// reduction tree.  The range cut depends only on pos, so the row gets the
+// softmax over its tiles and keeps its state (o unnormalised, m, l) per
+// query head.  The states are then combined inside the same launch: the
+// CTAs of a thread-block cluster (ATTN_ROW_CL consecutive ranges) fold their
+// states through distributed shared memory, each rank one slice of the
+// heads' dims, in rank order, into a cluster state in global memory; the
+// last cluster of a KV head to finish (a ticket) merges the cluster states
+// slice by slice, in cluster order, and writes the output row.  The range
+// cut depends only on pos and the fold order is fixed, so the row gets the
 // same bits from every pass that computes it.
 
 constexpr int ATTN_ROW_THREADS = 256;
-constexpr int ATTN_ROW_CTAS = 148;        // CTAs the ranges of all KV heads aim at
-constexpr int ATTN_ROW_MAX_SPLITS = 256;  // merge: one thread per range
+constexpr int ATTN_ROW_CL = 4;         // CTAs (ranges) per cluster
+constexpr int ATTN_ROW_CLUSTERS = 36;  // clusters of 4 resident at once with this kernel's shared memory
+                                       // (cudaOccupancyMaxActiveClusters on the GB300: 36)
 
 template <int HD>
 struct AttnRowCfg {
@@ -612,8 +618,39 @@ struct AttnRowCfg {
 };
 
 struct AttnRowShape {
-  int Hq, Hkv, pos, n_tiles, tps, splits;
+  int Hq, Hkv, pos, n_tiles, tps, splits;  // splits = n_cl * ATTN_ROW_CL ranges per KV head
+  int n_cl;                                // clusters per KV head
 };
+
+// Work buffer of the single-row attention (floats): a ticket per KV head
+// (ints, attn_row_ticket_words of them, zero before the first launch; every
+// launch leaves them zero), then per (KV head, cluster) a cluster state:
+// o [G][HD], then (m, l) per head, attn_row_cst_stride floats in all.
+__host__ __device__ __forceinline__ int attn_row_ticket_words(int Hkv) { return (Hkv + 3) / 4 * 4; }
+__host__ __device__ __forceinline__ int attn_row_cst_stride(int G, int HD) { return G * HD + 32; }
+
+__device__ __forceinline__ uint32_t row_cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void row_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// this CTA's shared-memory address as seen from cluster rank `rank`
+__device__ __forceinline__ uint32_t row_mapa(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float2 ld_cluster_f32x2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 
 __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -652,7 +689,8 @@ __device__ __forceinline__ void row_drain(uint64_t* bar, uint32_t parity) {
 template <int HD>
 __global__ void __launch_bounds__(ATTN_ROW_THREADS, 1)
     attn_row_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                    const __half* __restrict__ q, const AttnRowShape sh, float* __restrict__ part, int* err) {
+                    const __half* __restrict__ q, const AttnRowShape sh, float* __restrict__ work,
+                    __nv_bfloat16* __restrict__ out, int* err) {
   using C = AttnRowCfg<HD>;
   constexpr float cexp = attn_c<HD>();
   constexpr int KS = HD / 16;  // 16-dim steps of Q K^T
@@ -841,111 +879,136 @@ __global__ void __launch_bounds__(ATTN_ROW_THREADS, 1)
     if (tid == 0)
       for (int j = i; j < nt && j < issued; ++j) row_drain(&full[j % C::NST], (j / C::NST) & 1);
     __syncthreads();
-    return;
   }
-  // the range's state per query head: o (unnormalised), then m, l at HD
-  constexpr int STR = HD + 4;
+  // This range's state in shared memory (the K/V ring is free now): o
+  // [G][HD] (room for 16 heads), then (m, l) per head.  A range that gave up
+  // a wait, or holds no keys, adds nothing (m = -inf).  Every CTA takes part
+  // in the cluster steps below whatever happened before.
+  __shared__ int s_last;
+  float* sO = reinterpret_cast<float*>(smem);
+  float* sML = sO + 16 * HD;
 #pragma unroll
   for (int n = 0; n < NG; ++n) {
     const int d = dw + 8 * n + 2 * t4;
     if (g < G)
-      *reinterpret_cast<float2*>(part + ((size_t)(kvh * G + g) * sh.splits + split) * STR + d) =
-          make_float2(o[n][0], o[n][1]);
+      *reinterpret_cast<float2*>(sO + g * HD + d) = ok ? make_float2(o[n][0], o[n][1]) : make_float2(0.f, 0.f);
     if (g + 8 < G)
-      *reinterpret_cast<float2*>(part + ((size_t)(kvh * G + g + 8) * sh.splits + split) * STR + d) =
-          make_float2(o[n][2], o[n][3]);
+      *reinterpret_cast<float2*>(sO + (g + 8) * HD + d) = ok ? make_float2(o[n][2], o[n][3]) : make_float2(0.f, 0.f);
   }
-  if (tid < G)
-    *reinterpret_cast<float2*>(part + ((size_t)(kvh * G + tid) * sh.splits + split) * STR + HD) =
-        make_float2(sM[tid], sL[tid]);
-}
-
-// Combines the ranges of one query head (blockIdx.x) for 64 output columns
-// (blockIdx.y): thread s holds range s; m = max m_s, w_s = 2^((m_s - m) c),
-// out = sum w_s o_s / sum w_s l_s.  The sums run in a fixed tree (butterfly
-// within each warp, then the warps in order), so the bits do not depend on
-// timing.
-template <int HD>
-__global__ void __launch_bounds__(ATTN_ROW_THREADS) attn_row_merge_kernel(const float* __restrict__ part, int splits,
-                                                                          __nv_bfloat16* __restrict__ out) {
-  constexpr float c = attn_c<HD>();
-  constexpr int STR = HD + 4;
-  __shared__ float red[ATTN_ROW_THREADS / 32][68];
-  __shared__ float wmax[ATTN_ROW_THREADS / 32];
-  pdl_launch();
-  pdl_wait();
-  const int h = blockIdx.x, col0 = blockIdx.y * 64;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  float m = -INFINITY, l = 0.f;
-  float v[65];
-  if (tid < splits) {
-    const float* p = part + ((size_t)h * splits + tid) * STR;
-    const float2 ml = *reinterpret_cast<const float2*>(p + HD);
-    m = ml.x;
-    l = ml.y;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float4 x = *reinterpret_cast<const float4*>(p + col0 + 4 * j);
-      v[4 * j] = x.x;
-      v[4 * j + 1] = x.y;
-      v[4 * j + 2] = x.z;
-      v[4 * j + 3] = x.w;
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 64; ++j) v[j] = 0.f;
-  }
-  float mx = m;
-#pragma unroll
-  for (int x = 16; x > 0; x >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, x));
-  if (lane == 0) wmax[warp] = mx;
-  __syncthreads();
-  mx = wmax[0];
-#pragma unroll
-  for (int w = 1; w < ATTN_ROW_THREADS / 32; ++w) mx = fmaxf(mx, wmax[w]);
-  const float wgt = m == -INFINITY ? 0.f : ex2_approx(__fmul_rn(__fsub_rn(m, mx), c));
-#pragma unroll
-  for (int j = 0; j < 64; ++j) v[j] = __fmul_rn(v[j], wgt);
-  v[64] = __fmul_rn(l, wgt);
-#pragma unroll
-  for (int j = 0; j < 65; ++j) {
-#pragma unroll
-    for (int x = 16; x > 0; x >>= 1) v[j] = __fadd_rn(v[j], __shfl_xor_sync(0xffffffffu, v[j], x));
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int j = 0; j < 65; ++j) red[warp][j] = v[j];
+  if (tid < G) {
+    sML[2 * tid] = ok ? sM[tid] : -INFINITY;
+    sML[2 * tid + 1] = ok ? sL[tid] : 0.f;
   }
   __syncthreads();
-  if (tid < 64) {
-    float o = red[0][tid], lt = red[0][64];
+  row_cluster_sync();  // the cluster's range states are in shared memory
+  const uint32_t rank = row_cluster_rank();
+  const int cl = split / ATTN_ROW_CL;
+  const int GH = G * HD, SL = GH / ATTN_ROW_CL;  // rank r folds elements [r SL, (r+1) SL) of [G][HD]
+  const int CST = attn_row_cst_stride(G, HD);
+  float* cstates = work + attn_row_ticket_words(sh.Hkv);
+  {
+    float* cs = cstates + ((size_t)kvh * sh.n_cl + cl) * CST;
+    uint32_t ro[ATTN_ROW_CL], rml[ATTN_ROW_CL];
 #pragma unroll
-    for (int w = 1; w < ATTN_ROW_THREADS / 32; ++w) {
-      o = __fadd_rn(o, red[w][tid]);
-      lt = __fadd_rn(lt, red[w][64]);
+    for (int r = 0; r < ATTN_ROW_CL; ++r) {
+      ro[r] = row_mapa(smem_u32(sO), r);
+      rml[r] = row_mapa(smem_u32(sML), r);
     }
-    out[(size_t)h * HD + col0 + tid] = __float2bfloat16_rn(__fmul_rn(o, __frcp_rn(lt)));
+    for (int e = static_cast<int>(rank) * SL + 2 * tid; e < static_cast<int>(rank + 1) * SL;
+         e += 2 * ATTN_ROW_THREADS) {
+      const int h = e / HD;
+      float2 ml[ATTN_ROW_CL];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < ATTN_ROW_CL; ++r) {
+        ml[r] = ld_cluster_f32x2(rml[r] + 8u * h);
+        mx = fmaxf(mx, ml[r].x);
+      }
+      float2 acc = make_float2(0.f, 0.f);
+      float lacc = 0.f;
+#pragma unroll
+      for (int r = 0; r < ATTN_ROW_CL; ++r) {  // ranks in order
+        const float w = ml[r].x == -INFINITY ? 0.f : ex2_approx(__fmul_rn(__fsub_rn(ml[r].x, mx), cexp));
+        const float2 v = ld_cluster_f32x2(ro[r] + 4u * e);
+        acc.x = __fadd_rn(acc.x, __fmul_rn(w, v.x));
+        acc.y = __fadd_rn(acc.y, __fmul_rn(w, v.y));
+        lacc = __fadd_rn(lacc, __fmul_rn(w, ml[r].y));
+      }
+      *reinterpret_cast<float2*>(cs + e) = acc;
+      if (e % HD == 0) *reinterpret_cast<float2*>(cs + GH + 2 * h) = make_float2(mx, lacc);
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  row_cluster_sync();  // the cluster state is in global memory; no rank reads another's shared memory after this
+  if (rank == 0 && tid == 0) {
+    int* tickets = reinterpret_cast<int*>(work);
+    const int last = atomicAdd(&tickets[kvh], 1) == sh.n_cl - 1;
+    if (last) tickets[kvh] = 0;  // every cluster of this KV head has counted: ready for the next launch
+#pragma unroll
+    for (int r = 0; r < ATTN_ROW_CL; ++r) st_cluster_u32(row_mapa(smem_u32(&s_last), r), last ? 1u : 0u);
+  }
+  row_cluster_sync();  // every rank holds the flag
+  if (!s_last) return;
+  __threadfence();
+  // The last cluster: rank r merges slice r over the KV head's cluster
+  // states, in cluster order; (m, l) of the clusters first go to shared memory.
+  const float* cb = cstates + (size_t)kvh * sh.n_cl * CST;
+  float2* sCML = reinterpret_cast<float2*>(smem);  // [n_cl][G]
+  for (int i2 = tid; i2 < sh.n_cl * G; i2 += ATTN_ROW_THREADS) {
+    const int c = i2 / G, h = i2 % G;
+    sCML[i2] = __ldcg(reinterpret_cast<const float2*>(cb + (size_t)c * CST + GH + 2 * h));
+  }
+  __syncthreads();
+  for (int e = static_cast<int>(rank) * SL + 2 * tid; e < static_cast<int>(rank + 1) * SL; e += 2 * ATTN_ROW_THREADS) {
+    const int h = e / HD;
+    float mx = -INFINITY;
+    for (int c = 0; c < sh.n_cl; ++c) mx = fmaxf(mx, sCML[c * G + h].x);
+    float2 acc = make_float2(0.f, 0.f);
+    float lacc = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < sh.n_cl; ++c) {  // clusters in order
+      const float2 ml = sCML[c * G + h];
+      const float w = ml.x == -INFINITY ? 0.f : ex2_approx(__fmul_rn(__fsub_rn(ml.x, mx), cexp));
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(cb + (size_t)c * CST + e));
+      acc.x = __fadd_rn(acc.x, __fmul_rn(w, v.x));
+      acc.y = __fadd_rn(acc.y, __fmul_rn(w, v.y));
+      lacc = __fadd_rn(lacc, __fmul_rn(w, ml.y));
+    }
+    const float inv = __frcp_rn(lacc);
+    *reinterpret_cast<__nv_bfloat162*>(out + (size_t)kvh * GH + e) =
+        __floats2bfloat162_rn(__fmul_rn(acc.x, inv), __fmul_rn(acc.y, inv));
   }
 }
 
-// tiles per range and ranges per KV head for a row at position pos
-static void attn_row_split(int pos, int Hkv, int* n_tiles, int* tps, int* splits) {
+// tiles per range, ranges and clusters per KV head for a row at position
+// pos: the ranges of all KV heads aim at the clusters that fit at once
+static void attn_row_split(int pos, int Hkv, int* n_tiles, int* tps, int* splits, int* n_cl) {
   const int nt = pos / CHUNK + 1;
-  int per_head = ATTN_ROW_CTAS / (Hkv > 0 ? Hkv : 1);
-  if (per_head < 1) per_head = 1;
-  if (per_head > ATTN_ROW_MAX_SPLITS) per_head = ATTN_ROW_MAX_SPLITS;
+  int per_head = (ATTN_ROW_CLUSTERS / (Hkv > 0 ? Hkv : 1)) * ATTN_ROW_CL;
+  if (per_head < ATTN_ROW_CL) per_head = ATTN_ROW_CL;
   const int t = (nt + per_head - 1) / per_head;
+  const int ranges = (nt + t - 1) / t;
   *n_tiles = nt;
   *tps = t;
-  *splits = (nt + t - 1) / t;
+  *n_cl = (ranges + ATTN_ROW_CL - 1) / ATTN_ROW_CL;
+  *splits = *n_cl * ATTN_ROW_CL;
 }
 
+// Enough for a row at any position up to pos: a row's ranges are at most
+// its tile count and at most the per-head share, whatever the cut.
 size_t attn_split_partials_floats(int Hq, int Hkv, int hd, int pos) {
-  if (pos < 0 || Hkv < 1) return 0;
-  int nt = 0, tps = 0, splits = 0;
-  attn_row_split(pos, Hkv, &nt, &tps, &splits);
-  return static_cast<size_t>(Hq) * splits * (hd + 4);
+  if (pos < 0 || Hkv < 1 || Hq < Hkv) return 0;
+  const int nt = pos / CHUNK + 1;
+  int per_head = (ATTN_ROW_CLUSTERS / Hkv) * ATTN_ROW_CL;
+  if (per_head < ATTN_ROW_CL) per_head = ATTN_ROW_CL;
+  const int ranges_max = nt < per_head ? nt : per_head;
+  const int n_cl_max = (ranges_max + ATTN_ROW_CL - 1) / ATTN_ROW_CL;
+  return static_cast<size_t>(attn_row_ticket_words(Hkv)) +
+         static_cast<size_t>(Hkv) * n_cl_max * attn_row_cst_stride(Hq / Hkv, hd);
 }
+
+size_t attn_split_ticket_bytes(int Hkv) { return static_cast<size_t>(attn_row_ticket_words(Hkv)) * 4; }
 
 template <int HD>
 static cudaError_t launch_row_t(const AttnArgs& a, float* part, cudaStream_t s) {
@@ -972,12 +1035,9 @@ static cudaError_t launch_row_t(const AttnArgs& a, float* part, cudaStream_t s) 
   sh.Hq = a.Hq;
   sh.Hkv = a.Hkv;
   sh.pos = a.pos_base;
-  attn_row_split(a.pos_base, a.Hkv, &sh.n_tiles, &sh.tps, &sh.splits);
-  cudaError_t e = launch_k(attn_row_kernel<HD>, dim3(sh.splits, a.Hkv), dim3(ATTN_ROW_THREADS), C::SMEM, s, 1, tk, tv,
-                           a.q, sh, part, a.err);
-  if (e != cudaSuccess) return e;
-  return launch_k(attn_row_merge_kernel<HD>, dim3(a.Hq, HD / 64), dim3(ATTN_ROW_THREADS), 0, s, 1,
-                  static_cast<const float*>(part), sh.splits, a.out);
+  attn_row_split(a.pos_base, a.Hkv, &sh.n_tiles, &sh.tps, &sh.splits, &sh.n_cl);
+  return launch_k(attn_row_kernel<HD>, dim3(sh.splits, a.Hkv), dim3(ATTN_ROW_THREADS), C::SMEM, s, ATTN_ROW_CL, tk,
+                  tv, a.q, sh, part, a.out, a.err);
 }
 
 cudaError_t launch_attn_split(const AttnArgs& a, float* partials, cudaStream_t s) {

@@ -129,13 +129,16 @@ struct AttnArgs {
 // several groups go through the partials buffer (attn_partials_floats) and an
 // ordered merge.  launch_attn_split is the single-row form of the KV-shared
 // layers (M == 1, position pos_base, keys [0, pos_base]): key ranges spread
-// over many CTAs, range states in `partials` (attn_split_partials_floats),
-// then a merge kernel; two launches.
+// over clusters of CTAs, one launch; `partials` holds
+// attn_split_partials_floats floats (enough for any position up to the one
+// it was sized for), whose first attn_split_ticket_bytes bytes are tickets
+// that must be zero before the first launch (each launch leaves them zero).
 cudaError_t launch_attn_prefill(const AttnArgs& a, float* partials, cudaStream_t s);
 cudaError_t launch_attn_split(const AttnArgs& a, float* partials, cudaStream_t s);
 // floats of partials a launch of M rows over kv_len keys needs (0: none)
 size_t attn_partials_floats(int M, int Hq, int hd, int kv_len);
 size_t attn_split_partials_floats(int Hq, int Hkv, int hd, int pos);
+size_t attn_split_ticket_bytes(int Hkv);
 int attn_group_chunks(int kv_len);
 int attn_launch_count(const AttnArgs& a);  // kernels launch_attn_prefill starts (1 or 2)
 

@@ -12,15 +12,16 @@
 // Limits and sharing:
 //   - the array holds PF_NOALLOC_SCRATCH_FLOATS floats (2 MiB); every GPU
 //     that loads this library keeps it until the process exits;
-//   - a request needs n_head * R * (head_dim + 4) floats, R being the number
-//     of key ranges the row's keys are cut into (at most 148 / n_kv_head, so
-//     at most n_head * 148 * (head_dim + 4)), and is refused (PF_E_ARG) when
-//     that is more than the array holds;
+//   - a request needs the tickets of the kernel's last-cluster merge (one
+//     int per KV head, rounded up to four) and one folded state per (KV
+//     head, cluster of four key ranges): n_kv_head * C * (n_head / n_kv_head
+//     * head_dim + 32) floats, C being at most 36 / n_kv_head (at least 1);
+//     it is refused (PF_E_ARG) when that is more than the array holds;
 //   - every call, on every stream, uses the same array: calls whose work
 //     overlaps on the GPU race and give wrong results, so callers must order
 //     them (one stream, or events);
-//   - nothing in the array has to start at zero: each call writes every
-//     partial it later reads;
+//   - the call clears the tickets it uses before its launch; every state it
+//     reads is written by the same launch;
 //   - its last four floats hold the call's device error word (reset by the
 //     call, read back after it).
 #include "../../include/prefill_ops.h"
@@ -101,6 +102,7 @@ extern "C" int pfop_attention_split_noalloc(const void* q_dev, const void* k_dev
   a.err = err_word;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(err_word, 0, 16, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(scratch, 0, pf::attn_split_ticket_bytes(Hkv), s);
   if (e != cudaSuccess) return fail(PF_E_CUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
   e = pf::launch_attn_split(a, scratch, s);
   if (e != cudaSuccess) return fail(PF_E_CUDA, std::string("attention launch: ") + cudaGetErrorString(e));

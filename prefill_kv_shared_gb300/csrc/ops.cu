@@ -380,6 +380,7 @@ extern "C" int pfop_attention(int32_t mode, const void* q_dev, const void* k_dev
                                      : attn_partials_floats(M, Hq, hd, kv_len)) * 4));
   OP_CUDA(sc.alloc(&err, 16));
   OP_CUDA(cudaMemsetAsync(err, 0, 16, s));
+  if (mode == 1) OP_CUDA(cudaMemsetAsync(part, 0, attn_split_ticket_bytes(Hkv), s));  // the tickets start at zero
   a.err = err;
   if (mode == 0) {
     OP_CUDA(launch_attn_prefill(a, part, s));
@@ -536,6 +537,7 @@ extern "C" int pfop_attention_bench(int32_t mode, const void* q_dev, const void*
                                      : attn_partials_floats(M, Hq, hd, kv_len)) * 4));
   OP_CUDA(sc.alloc(&err, 16));
   OP_CUDA(cudaMemsetAsync(err, 0, 16, s));
+  if (mode == 1) OP_CUDA(cudaMemsetAsync(part, 0, attn_split_ticket_bytes(Hkv), s));  // the tickets start at zero
   a.err = err;
   int rc = time_launches([&] { return mode == 0 ? launch_attn_prefill(a, part, s) : launch_attn_split(a, part, s); },
                          scrub_dev, scrub_bytes, warmup, iters, us, s);

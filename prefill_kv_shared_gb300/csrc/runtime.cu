@@ -717,7 +717,7 @@ int run_ubatch(prefill_ctx* c, const int32_t* tokens, int T, std::vector<Run>& r
     r.pos_base = pos;
     r.kv_len = pos + 1;
     const int n_keys = pos + 1;
-    return counted(c, PF_KC_ATTN_ROW, 2, static_cast<double>(n_keys) * c->Hq * 4.0 * c->hd,
+    return counted(c, PF_KC_ATTN_ROW, 1, static_cast<double>(n_keys) * c->Hq * 4.0 * c->hd,
                    n_keys * c->kv * 4.0 + c->q * 4.0, [&] { return launch_attn_split(r, c->row_partials, s); });
   };
   // the prefill attention of rows [row0, row0 + n) of sequence seq at positions pos .. pos + n - 1

@@ -58,11 +58,11 @@ def test_noalloc_matches_allocating_entry_point_twice(lib, Hq, Hkv, hd):
 
 
 def test_noalloc_refuses_requests_beyond_the_array(lib):
-    # 16 query heads of 256 on one KV head, keys cut into 148 ranges: the
-    # range states need 16 * 148 * 260 floats, more than the 2^19 the array
-    # holds.  The buffers are full size for the request, so even a call that
-    # wrongly went ahead would stay inside them.
-    Hq, Hkv, hd, kv_len = 16, 1, 256, 148 * 64
+    # 4096 query heads of 256 over 256 KV heads: one cluster of key ranges
+    # per KV head, whose folded states need 256 * (16 * 256 + 32) floats,
+    # more than the 2^19 the array holds.  The buffers are full size for the
+    # request, so even a call that wrongly went ahead would stay inside them.
+    Hq, Hkv, hd, kv_len = 4096, 256, 256, 64
     q, k, v = (torch.from_numpy(t).cuda() for t in _inputs(3, Hq, Hkv, hd, kv_len))
     out = torch.empty((1, Hq * hd), dtype=torch.bfloat16, device="cuda")
     rc = lib.pfop_attention_split_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), Hq, Hkv, hd, kv_len - 1, kv_len,
