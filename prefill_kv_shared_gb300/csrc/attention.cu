@@ -966,14 +966,21 @@ __global__ void __launch_bounds__(ATTN_ROW_THREADS, 1)
     for (int c = 0; c < sh.n_cl; ++c) mx = fmaxf(mx, sCML[c * G + h].x);
     float2 acc = make_float2(0.f, 0.f);
     float lacc = 0.f;
-#pragma unroll 4
-    for (int c = 0; c < sh.n_cl; ++c) {  // clusters in order
-      const float2 ml = sCML[c * G + h];
-      const float w = ml.x == -INFINITY ? 0.f : ex2_approx(__fmul_rn(__fsub_rn(ml.x, mx), cexp));
-      const float2 v = __ldcg(reinterpret_cast<const float2*>(cb + (size_t)c * CST + e));
-      acc.x = __fadd_rn(acc.x, __fmul_rn(w, v.x));
-      acc.y = __fadd_rn(acc.y, __fmul_rn(w, v.y));
-      lacc = __fadd_rn(lacc, __fmul_rn(w, ml.y));
+    for (int c0 = 0; c0 < sh.n_cl; c0 += 8) {  // clusters in order, eight loads in flight
+      float2 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = c0 + u < sh.n_cl ? __ldcg(reinterpret_cast<const float2*>(cb + (size_t)(c0 + u) * CST + e))
+                                : make_float2(0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (c0 + u >= sh.n_cl) break;
+        const float2 ml = sCML[(c0 + u) * G + h];
+        const float w = ml.x == -INFINITY ? 0.f : ex2_approx(__fmul_rn(__fsub_rn(ml.x, mx), cexp));
+        acc.x = __fadd_rn(acc.x, __fmul_rn(w, v[u].x));
+        acc.y = __fadd_rn(acc.y, __fmul_rn(w, v[u].y));
+        lacc = __fadd_rn(lacc, __fmul_rn(w, ml.y));
+      }
     }
     const float inv = __frcp_rn(lacc);
     *reinterpret_cast<__nv_bfloat162*>(out + (size_t)kvh * GH + e) =
