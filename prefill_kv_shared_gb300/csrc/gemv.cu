@@ -94,7 +94,9 @@ template <int WK, int BN>
 __global__ void __launch_bounds__(GV_THREADS) gemv_kernel(const __nv_bfloat16* __restrict__ a, int K,
                                                           const uint8_t* __restrict__ w, int parts,
                                                           float* __restrict__ sums, int* __restrict__ tickets,
-                                                          const EpiParams ep_in, int* err) {
+                                                          const EpiParams ep_in, int* err,
+                                                          const float* __restrict__ nx, const float* __restrict__ ng,
+                                                          float eps) {
   constexpr int RG = BN / 32;          // 32-row groups of a tile
   constexpr int KW = GV_WARPS / RG;    // warps along k inside the CTA
   constexpr int TILE = BN * 36;        // bytes of one (tile, k-block) of Q4_0
@@ -126,10 +128,43 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_kernel(const __nv_bfloat16* _
   pdl_launch();
   if (tid == 0) ep = ep_in;
   pdl_wait();
-  for (int i = kb0 * 8 + tid; i < kb1 * 8; i += GV_THREADS) {  // the part's columns, 8 at a time
-    const uint4 u = reinterpret_cast<const uint4*>(a)[i];
-    *reinterpret_cast<float4*>(xs + 8 * i) = bf16x4_to_f32(make_uint2(u.x, u.y));
-    *reinterpret_cast<float4*>(xs + 8 * i + 4) = bf16x4_to_f32(make_uint2(u.z, u.w));
+  if (nx) {
+    // The row is the RMS norm of the residual row nx (fp32 [K]) with gain
+    // (1 + ng): every CTA forms it for itself (a fixed-order sum of squares,
+    // the same in every CTA and every launch) and rounds it to bf16 as the
+    // norm kernel would hand it over.
+    __shared__ float red[GV_WARPS];
+    const float4* x4 = reinterpret_cast<const float4*>(nx);
+    float ss = 0.f;
+    for (int v = tid; v < K / 4; v += GV_THREADS) {
+      const float4 q = x4[v];
+      ss = __fmaf_rn(q.x, q.x, ss);
+      ss = __fmaf_rn(q.y, q.y, ss);
+      ss = __fmaf_rn(q.z, q.z, ss);
+      ss = __fmaf_rn(q.w, q.w, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float tot = red[0];
+#pragma unroll
+    for (int w2 = 1; w2 < GV_WARPS; ++w2) tot = __fadd_rn(tot, red[w2]);
+    const float rr = rsqrtf(__fadd_rn(__fdiv_rn(tot, static_cast<float>(K)), eps));
+    const float4* g4 = reinterpret_cast<const float4*>(ng);
+    for (int v = kb0 * 16 + tid; v < kb1 * 16; v += GV_THREADS) {  // the part's columns, 4 at a time
+      const float4 q = x4[v], g = g4[v];
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(q.x * rr * (1.f + g.x), q.y * rr * (1.f + g.y));
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(q.z * rr * (1.f + g.z), q.w * rr * (1.f + g.w));
+      *reinterpret_cast<float4*>(xs + 4 * v) =
+          make_float4(__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi));
+    }
+  } else {
+    for (int i = kb0 * 8 + tid; i < kb1 * 8; i += GV_THREADS) {  // the part's columns, 8 at a time
+      const uint4 u = reinterpret_cast<const uint4*>(a)[i];
+      *reinterpret_cast<float4*>(xs + 8 * i) = bf16x4_to_f32(make_uint2(u.x, u.y));
+      *reinterpret_cast<float4*>(xs + 8 * i + 4) = bf16x4_to_f32(make_uint2(u.z, u.w));
+    }
   }
   __syncthreads();
   const int rg = warp % RG, kw = warp / RG;
@@ -222,7 +257,7 @@ constexpr size_t GV_SMEM_MAX = 160 * 1024;
 
 template <int WK, int BN>
 static cudaError_t launch_gemv_t(const ActMat& A, const WeightMat& W, const EpiParams& ep, float* sums, int* tickets,
-                                 int* err, cudaStream_t s) {
+                                 int* err, cudaStream_t s, const float* nx, const float* ng, float eps) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -235,14 +270,16 @@ static cudaError_t launch_gemv_t(const ActMat& A, const WeightMat& W, const EpiP
   if (smem > GV_SMEM_MAX) return cudaErrorInvalidValue;
   const int grid = (W.N_rows / BN) * parts;
   return launch_k(gemv_kernel<WK, BN>, dim3(grid), dim3(GV_THREADS), smem, s, 1, A.dev, W.K,
-                  static_cast<const uint8_t*>(W.dev), parts, sums, tickets, ep, err);
+                  static_cast<const uint8_t*>(W.dev), parts, sums, tickets, ep, err, nx, ng, eps);
 }
 
 cudaError_t launch_gemv(const ActMat& A, const WeightMat& W, const EpiParams& ep, float* sums, int* tickets,
-                        int* err, cudaStream_t s) {
+                        int* err, cudaStream_t s, const float* norm_x, const float* norm_g, float eps) {
   if (A.K != W.K || W.K % 64 != 0 || W.N_rows % W.BN != 0 || !sums || !tickets) return cudaErrorInvalidValue;
+  if (norm_x && (!norm_g || (reinterpret_cast<uintptr_t>(norm_x) | reinterpret_cast<uintptr_t>(norm_g)) % 16 != 0))
+    return cudaErrorInvalidValue;
 #define PF_GEMV_CASE(WKV, BNV) \
-  if (W.kind == WKV && W.BN == BNV) return launch_gemv_t<WKV, BNV>(A, W, ep, sums, tickets, err, s);
+  if (W.kind == WKV && W.BN == BNV) return launch_gemv_t<WKV, BNV>(A, W, ep, sums, tickets, err, s, norm_x, norm_g, eps);
   PF_GEMV_CASE(W_Q4, 64)
   PF_GEMV_CASE(W_Q4, 128)
   PF_GEMV_CASE(W_Q4, 256)

@@ -691,8 +691,12 @@ int run_ubatch(prefill_ctx* c, const int32_t* tokens, int T, std::vector<Run>& r
   // tensor-core kernel's rows are independent of each other bit for bit, so
   // the rows of several sequences keep their bits whether the launch holds
   // every row or only the gathered output rows.)
+  // norm_src / norm_gain: the projection's input is the RMS norm of these
+  // residual rows; the one-row kernel then forms its row's norm itself
+  // (the launch's A rows still serve the tensor-core part).
   auto project = [&](const ActMat& A, int rows, bool out_row, const WeightMat& Wm, const EpiParams& e,
-                     double flops_row, double io_row, double wbytes) -> cudaError_t {
+                     double flops_row, double io_row, double wbytes, const float* norm_src = nullptr,
+                     const float* norm_gain = nullptr) -> cudaError_t {
     const int m_tc = out_row ? rows - 1 : rows;
     if (m_tc > 0) {
       const cudaError_t err = counted(c, gemm_class(m_tc), 1, flops_row * m_tc, wbytes + io_row * m_tc,
@@ -703,8 +707,10 @@ int run_ubatch(prefill_ctx* c, const int32_t* tokens, int T, std::vector<Run>& r
     ActMat a1 = A;
     a1.dev = A.dev + static_cast<size_t>(rows - 1) * A.K;
     const EpiParams e1 = shift_rows(e, rows - 1);
-    return counted(c, PF_KC_GEMM_ROW, 1, flops_row, wbytes + io_row,
-                   [&] { return launch_gemv(a1, Wm, e1, c->gv_sums, c->gv_tickets, c->err, s); });
+    const float* nx = norm_src ? norm_src + static_cast<size_t>(rows - 1) * D : nullptr;
+    return counted(c, PF_KC_GEMM_ROW, 1, flops_row, wbytes + io_row, [&] {
+      return launch_gemv(a1, Wm, e1, c->gv_sums, c->gv_tickets, c->err, s, nx, norm_gain, c->d.rms_eps);
+    });
   };
   // the single-row attention of one output row
   auto row_attention = [&](const AttnArgs& base, int row, int seq, int pos) -> cudaError_t {
@@ -746,10 +752,10 @@ int run_ubatch(prefill_ctx* c, const int32_t* tokens, int T, std::vector<Run>& r
         break;
       }
       if (!multi) {
-        // keep the output row only: gather it inside the norm
-        PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, D * 10.0, [&] {
-                   return launch_rmsnorm(c->x, T - 1, 1, D, W.attn_norm, c->d.rms_eps, c->y, c->xr, s);
-                 }));
+        // keep the output row only: the rest of the pass works on row T-1 of
+        // the residual in place, and its one-row projections form their
+        // norms themselves
+        xcur = c->x + static_cast<size_t>(T - 1) * D;
         M = 1;
         pos_base = static_cast<int>(pos0) + T - 1;
         ple_view = c->ple + static_cast<size_t>(T - 1) * LP;
@@ -766,15 +772,17 @@ int run_ubatch(prefill_ctx* c, const int32_t* tokens, int T, std::vector<Run>& r
                    }));
         M = n_out;
         ple_view = c->ple_g;
+        xcur = c->xr;
       }
-      xcur = c->xr;
       gathered = true;
     } else {
-      // a requested hidden state entering this layer leaves as the norm's input copy
+      // a requested hidden state entering this layer leaves as the norm's
+      // input copy; a one-row launch needs the norm for nothing else
       float* inp = c->layer_inp.empty() || !c->layer_inp[il] ? nullptr : c->layer_out[il];
-      PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, M * D * (6.0 + (inp ? 4.0 : 0.0)), [&] {
-                 return launch_rmsnorm(xcur, 0, M, D, W.attn_norm, c->d.rms_eps, c->y, inp, s);
-               }));
+      if (multi || M > 1 || inp)
+        PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, M * D * (6.0 + (inp ? 4.0 : 0.0)), [&] {
+                   return launch_rmsnorm(xcur, 0, M, D, W.attn_norm, c->d.rms_eps, c->y, inp, s);
+                 }));
     }
     const bool writes = il < S;
     const int src = writes ? il : c->kv_src[il];
@@ -799,7 +807,7 @@ int run_ubatch(prefill_ctx* c, const int32_t* tokens, int T, std::vector<Run>& r
       }
       const double n_out_cols = c->q + 2.0 * e.kv_dim;
       PF_CUDA(c, project(c->a_y, M, out_row, W.qkv, e, 2.0 * n_out_cols * D, D * 2.0 + n_out_cols * 2.0,
-                         gemm_wbytes(c, n_out_cols, D)));
+                         gemm_wbytes(c, n_out_cols, D), xcur, W.attn_norm));
     }
     {
       AttnArgs a;
@@ -842,9 +850,10 @@ int run_ubatch(prefill_ctx* c, const int32_t* tokens, int T, std::vector<Run>& r
       e.ld_f32 = D;
       PF_CUDA(c, project(c->a_att, M, out_row, W.o, e, 2.0 * D * c->q, c->q * 2.0 + D * 8.0, gemm_wbytes(c, D, c->q)));
     }
-    PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, M * D * 6.0, [&] {
-               return launch_rmsnorm(xcur, 0, M, D, W.ffn_norm, c->d.rms_eps, c->y, nullptr, s);
-             }));
+    if (multi || M > 1)
+      PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, M * D * 6.0, [&] {
+                 return launch_rmsnorm(xcur, 0, M, D, W.ffn_norm, c->d.rms_eps, c->y, nullptr, s);
+               }));
     {
       EpiParams e;
       e.kind = EPI_GLU;
@@ -853,7 +862,7 @@ int run_ubatch(prefill_ctx* c, const int32_t* tokens, int T, std::vector<Run>& r
       e.ld_bf16 = c->F;
       e.act = c->d.ffn_kind == PF_FFN_GEGLU ? 0 : 1;
       PF_CUDA(c, project(c->a_y, M, out_row, W.gu, e, 4.0 * c->F * D, D * 2.0 + c->F * 2.0,
-                         gemm_wbytes(c, 2.0 * c->F, D)));
+                         gemm_wbytes(c, 2.0 * c->F, D), xcur, W.ffn_norm));
     }
     {
       EpiParams e;
@@ -895,18 +904,18 @@ int run_ubatch(prefill_ctx* c, const int32_t* tokens, int T, std::vector<Run>& r
                }));
   }
   if (is_last && !multi) {
+    // the head projects the output row's final norm, formed inside the launch
     NvtxRange r_head("head");
     const int row = gathered ? 0 : T - 1;
-    PF_CUDA(c, counted(c, PF_KC_NORM, 1, 0.0, D * 6.0, [&] {
-               return launch_rmsnorm(xcur, row, 1, D, c->out_norm, c->d.rms_eps, c->y, nullptr, s);
-             }));
+    const float* xrow = xcur + static_cast<size_t>(row) * D;
     EpiParams e;
     e.kind = EPI_F32;
     e.N = c->V;
     e.out_f32 = logits;
     e.ld_f32 = c->V;
-    PF_CUDA(c, counted(c, gemm_class(1), 1, 2.0 * c->V * D, D * 2.0 + gemm_wbytes(c, c->V, D) + c->V * 4.0,
-                       [&] { return launch_gemv(c->a_y, c->head, e, c->gv_sums, c->gv_tickets, c->err, s); }));
+    PF_CUDA(c, counted(c, gemm_class(1), 1, 2.0 * c->V * D, D * 4.0 + gemm_wbytes(c, c->V, D) + c->V * 4.0, [&] {
+      return launch_gemv(c->a_y, c->head, e, c->gv_sums, c->gv_tickets, c->err, s, xrow, c->out_norm, c->d.rms_eps);
+    }));
   } else if (is_last) {
     // one logits row per finishing sequence, in run order: their rows are
     // normed into y (gathered: rows 0 .. n_out-1 of xr; else picked out of x)
