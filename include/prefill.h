@@ -117,10 +117,10 @@ typedef struct prefill_weights {
    "llama.cpp Gemma 4 prefill KV graph optimization", section 1: writing
    layers below n_layer_kv_from_start, KV-shared layers from it up that
    read kv_src's cache; the pruning condition of that section's listing is
-   evaluated from prune_shared_enable, n_seq_max and embeddings.)  All contexts of one process
-   must use the same device: the kernels' shared-memory opt-in is made once
-   per process, on the device of the first launch (run one process per GPU,
-   as the replicas do).  Validates the description,
+   evaluated from prune_shared_enable, n_seq_max and embeddings.)  Contexts of
+   one process may sit on different devices (the kernels' shared-memory
+   opt-in is made once per kernel and device); each context's calls must be
+   made with its own device current.  Validates the description,
    uploads and repacks the weights, allocates the FP16 KV cache
    (2 x writing layers x max_ctx x kv_dim) and the activation buffers for
    ubatch_max rows.  cuda_stream: a cudaStream_t or NULL.  On failure *out is

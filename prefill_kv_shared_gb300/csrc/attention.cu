@@ -502,11 +502,9 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict
 template <int HD>
 static cudaError_t launch_tc_t(const AttnArgs& a, float* part, cudaStream_t s) {
   using C = AttnTcCfg<HD>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  {
+    const cudaError_t e = smem_opt_in<attn_tc_kernel<HD>>(C::SMEM);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const int G = a.Hq / a.Hkv;
   // Q viewed as [64-dim box][query][head][64 dims]; K and V as [64-dim
@@ -1020,11 +1018,9 @@ size_t attn_split_ticket_bytes(int Hkv) { return static_cast<size_t>(attn_row_ti
 template <int HD>
 static cudaError_t launch_row_t(const AttnArgs& a, float* part, cudaStream_t s) {
   using C = AttnRowCfg<HD>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_row_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  {
+    const cudaError_t e = smem_opt_in<attn_row_kernel<HD>>(C::SMEM);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   // K and V as [64-dim box][key][64 dims] (the box dimension last, stride
   // 128 B): one copy brings a 64-key tile of one KV head as [box][key][128 B]

@@ -14,6 +14,7 @@
 #include <stdint.h>
 
 #include <cstdlib>
+#include <mutex>
 #include <utility>
 
 namespace pf {
@@ -87,6 +88,27 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
   cfg.attrs = attr;
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// The dynamic shared-memory limit of a kernel above 48 KB is an attribute
+// of the kernel on each device: set it once per (kernel, device), for the
+// device current at the launch.
+template <auto Kernel>
+inline cudaError_t smem_opt_in(int bytes) {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static bool done[kMaxDev] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  std::lock_guard<std::mutex> g(mu);
+  if (!done[dev]) {
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
+  }
+  return cudaSuccess;
 }
 
 // ---------------------------------------------------------------------------

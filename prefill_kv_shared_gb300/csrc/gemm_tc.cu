@@ -674,15 +674,13 @@ bool make_weight_map(WeightMat& w, std::string* err) {
   return encode_2d_bf16(&w.tmap, w.dev, (uint64_t)w.K, (uint64_t)w.N_rows, 64, (uint32_t)w.BN, err);
 }
 
+// SM count of the current device (looked up per call: contexts of one
+// process may sit on different devices)
 static int sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
 }
 
 template <int WK, int BN, int MT>
@@ -740,13 +738,10 @@ template <int WK, int BN, int MT>
 static cudaError_t launch_t(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err,
                             cudaStream_t s, int withhold_stage) {
   using C = GemmCfg<WK, BN, MT>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<WK, BN, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    C::SMEM_BYTES);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+  {
+    const cudaError_t e = smem_opt_in<gemm_tc_kernel<WK, BN, MT>>(C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+  }
   GemmShape sh;
   sh.M = M;
   sh.K = W.K;

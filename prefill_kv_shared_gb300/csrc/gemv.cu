@@ -258,13 +258,10 @@ constexpr size_t GV_SMEM_MAX = 160 * 1024;
 template <int WK, int BN>
 static cudaError_t launch_gemv_t(const ActMat& A, const WeightMat& W, const EpiParams& ep, float* sums, int* tickets,
                                  int* err, cudaStream_t s, const float* nx, const float* ng, float eps) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemv_kernel<WK, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(GV_SMEM_MAX));
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+  {
+    const cudaError_t e = smem_opt_in<gemv_kernel<WK, BN>>(static_cast<int>(GV_SMEM_MAX));
+    if (e != cudaSuccess) return e;
+  }
   const int parts = gemv_parts(W);
   const size_t smem = gemv_smem(W, parts);
   if (smem > GV_SMEM_MAX) return cudaErrorInvalidValue;
