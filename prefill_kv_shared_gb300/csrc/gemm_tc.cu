@@ -770,10 +770,12 @@ cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiPar
   if (A.K != W.K || W.K % 64 != 0 || W.N_rows % W.BN != 0 || M > A.rows || W.split < 1 ||
       (W.K / 64) % W.split != 0)
     return cudaErrorInvalidValue;
-  // two 128-row M tiles per CTA for large M on wide tiles (not in split
-  // mode, whose partial slots hold one); narrow tiles keep one M tile so
-  // that more CTAs share the work
-  const bool two = M > 128 && W.split == 1 && W.BN >= 256;
+  // two 128-row M tiles per CTA for large M on wide tiles, and on narrower
+  // tiles when one M tile per CTA would need a second wave of CTAs (not in
+  // split mode, whose partial slots hold one); otherwise one M tile, so
+  // that more CTAs share the work.  A row's result does not depend on it.
+  const int units_one = (W.N_rows / W.BN) * ((M + 127) / 128);
+  const bool two = M > 128 && W.split == 1 && (W.BN >= 256 || (W.BN == 128 && units_one > sm_count()));
 #define PF_GEMM_CASE(WKV, BNV)                                                    \
   if (W.kind == WKV && W.BN == BNV)                                               \
     return two ? launch_t<WKV, BNV, 2>(A, M, W, ep, err, s, withhold_stage)      \

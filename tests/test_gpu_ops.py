@@ -50,6 +50,8 @@ GEMM_CASES = [
     (Q4, 512, 256, 1536, 64),
     (Q4, 3, 192, 512, 64),
     (F32, 100, 128, 256, 64),
+    (Q4, 1000, 2560, 256, 128),   # 160 tiles of 128 x 128: two M tiles per CTA
+    (F32, 1000, 2560, 128, 128),
 ]
 
 
@@ -69,17 +71,19 @@ def test_linear_f32(lib, wtype, M, N, K, bn):
     assert rel_err(got, ref_exact) < 2e-2
 
 
-@pytest.mark.parametrize("wtype,bn", [(Q4, 64), (Q4, 128), (Q4, 256), (F32, 128)])
-def test_linear_row_independent_of_m(lib, wtype, bn):
-    """A row's result is bit-identical whether the launch carries 512 rows or 1."""
+@pytest.mark.parametrize("wtype,bn,N,M", [(Q4, 64, 256, 512), (Q4, 128, 256, 512), (Q4, 256, 256, 512),
+                                          (F32, 128, 256, 512), (Q4, 128, 2560, 1024)])
+def test_linear_row_independent_of_m(lib, wtype, bn, N, M):
+    """A row's result is bit-identical whether the launch carries M rows or 1
+    (M = 1024 over 2560 columns takes two M tiles per CTA)."""
     rng = np.random.default_rng(3)
-    N, K = 256, 1536
+    K = 1536
     w, _, _ = _weights(wtype, rng, N, K)
-    A = _A(rng, 512, K)
+    A = _A(rng, M, K)
     a, R = padded_a(A)
-    full = torch.empty((512, N), dtype=torch.float32, device="cuda")
-    binding.check_op(lib.pfop_linear_f32(wtype, w.ctypes.data, N, K, bn, a.data_ptr(), R, 512, full.data_ptr(), None))
-    for row in (0, 129, 511):
+    full = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    binding.check_op(lib.pfop_linear_f32(wtype, w.ctypes.data, N, K, bn, a.data_ptr(), R, M, full.data_ptr(), None))
+    for row in (0, 129, M - 1):
         a1, R1 = padded_a(A[row:row + 1])
         one = torch.empty((1, N), dtype=torch.float32, device="cuda")
         binding.check_op(lib.pfop_linear_f32(wtype, w.ctypes.data, N, K, bn, a1.data_ptr(), R1, 1, one.data_ptr(), None))
