@@ -35,7 +35,9 @@ int pfop_linear_resid(int32_t wtype, const void* w_host, int32_t N, int32_t K, c
                       int32_t M, float* x_dev, void* xb_dev, void* stream);
 
 /* h[m][f] = act(A Wg^T)[m][f] * (A Wu^T)[m][f] (bf16 [M][F]); act 0 =
-   gelu_tanh (GeGLU), 1 = silu (SwiGLU).  F a multiple of 64. */
+   gelu_tanh (GeGLU), 1 = silu (SwiGLU).  F a multiple of 64.  Gate and up
+   rows are interleaved in tiles of 256 rows when F is a multiple of 128, of
+   192 (Q4_0) when F is a multiple of 96, else of 128. */
 int pfop_linear_glu(int32_t wtype, const void* wg_host, const void* wu_host, int32_t F, int32_t K, int32_t act,
                     const void* a_dev, int32_t a_rows, int32_t M, void* h_dev, void* stream);
 

@@ -82,8 +82,9 @@ struct GemmCfg {
   // The dequantised B ring bounds how far the dequant warps run ahead of the
   // MMAs (B stage k+S_B is written once the MMAs of stage k are done); the
   // A ring takes what the B and raw rings and the epilogue staging leave.
-  static constexpr int S_B = Q4 ? (BN >= 256 ? (MT == 2 ? 2 : 3) : KS == 2 ? (BN == 64 ? 4 : 2) : 4) : 0;
-  static constexpr int S_R = Q4 ? (BN >= 256 ? 3 : KS == 2 ? (BN == 64 ? 6 : 3) : 6) : 0;
+  static constexpr int S_B =
+      Q4 ? (BN >= 256 ? (MT == 2 ? 2 : 3) : BN == 192 ? 2 : KS == 2 ? (BN == 64 ? 4 : 2) : 4) : 0;
+  static constexpr int S_R = Q4 ? (BN >= 192 ? 3 : KS == 2 ? (BN == 64 ? 6 : 3) : 6) : 0;
   static constexpr int NB = S_B > 0 ? S_B : 1;  // ring moduli (the rings are unused without Q4)
   static constexpr int NR = S_R > 0 ? S_R : 1;
   static constexpr int RAW_RING = (S_R * RAW_BYTES + 1023) / 1024 * 1024;
@@ -691,7 +692,10 @@ static size_t ring_bytes() {
 
 static size_t ring_bytes_mt1(int kind, int BN) {
   if (kind == W_Q4)
-    return BN == 256 ? ring_bytes<W_Q4, 256, 1>() : BN == 64 ? ring_bytes<W_Q4, 64, 1>() : ring_bytes<W_Q4, 128, 1>();
+    return BN == 256   ? ring_bytes<W_Q4, 256, 1>()
+           : BN == 192 ? ring_bytes<W_Q4, 192, 1>()
+           : BN == 64  ? ring_bytes<W_Q4, 64, 1>()
+                       : ring_bytes<W_Q4, 128, 1>();
   return BN == 256 ? ring_bytes<W_BF16, 256, 1>() : BN == 64 ? ring_bytes<W_BF16, 64, 1>() : ring_bytes<W_BF16, 128, 1>();
 }
 
@@ -775,13 +779,14 @@ cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiPar
   // split mode, whose partial slots hold one); otherwise one M tile, so
   // that more CTAs share the work.  A row's result does not depend on it.
   const int units_one = (W.N_rows / W.BN) * ((M + 127) / 128);
-  const bool two = M > 128 && W.split == 1 && (W.BN >= 256 || (W.BN == 128 && units_one > sm_count()));
+  const bool two = M > 128 && W.split == 1 && (W.BN >= 192 || (W.BN == 128 && units_one > sm_count()));
 #define PF_GEMM_CASE(WKV, BNV)                                                    \
   if (W.kind == WKV && W.BN == BNV)                                               \
     return two ? launch_t<WKV, BNV, 2>(A, M, W, ep, err, s, withhold_stage)      \
                : launch_t<WKV, BNV, 1>(A, M, W, ep, err, s, withhold_stage);
   PF_GEMM_CASE(W_Q4, 64)
   PF_GEMM_CASE(W_Q4, 128)
+  PF_GEMM_CASE(W_Q4, 192)
   PF_GEMM_CASE(W_Q4, 256)
   PF_GEMM_CASE(W_BF16, 64)
   PF_GEMM_CASE(W_BF16, 128)

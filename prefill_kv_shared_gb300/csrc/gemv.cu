@@ -279,6 +279,7 @@ cudaError_t launch_gemv(const ActMat& A, const WeightMat& W, const EpiParams& ep
   if (W.kind == WKV && W.BN == BNV) return launch_gemv_t<WKV, BNV>(A, W, ep, sums, tickets, err, s, norm_x, norm_g, eps);
   PF_GEMV_CASE(W_Q4, 64)
   PF_GEMV_CASE(W_Q4, 128)
+  PF_GEMV_CASE(W_Q4, 192)
   PF_GEMV_CASE(W_Q4, 256)
   PF_GEMV_CASE(W_BF16, 64)
   PF_GEMV_CASE(W_BF16, 128)

@@ -276,7 +276,9 @@ extern "C" int pfop_linear_glu(int32_t wtype, const void* wg_host, const void* w
   ActMat A;
   int rc;
   const size_t rb = rbytes(wtype, K);
-  const int bn = F % 128 == 0 ? 256 : 128, half = bn / 2;
+  // tiles of 256 rows (128 gate + 128 up), of 192 for Q4_0 when F is a
+  // multiple of 96 but not of 128, else of 128
+  const int bn = F % 128 == 0 ? 256 : (wtype == PF_W_Q4_0 && F % 96 == 0) ? 192 : 128, half = bn / 2;
   std::vector<const void*> rows;
   for (int t = 0; t < F / half; ++t) {
     for (int i = 0; i < half; ++i) rows.push_back(static_cast<const uint8_t*>(wg_host) + (t * half + i) * rb);

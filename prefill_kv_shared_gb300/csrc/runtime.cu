@@ -427,7 +427,17 @@ extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weig
         }
         return rows;
       };
-      const int bn = C->F % 128 == 0 ? 256 : 128;
+      // Q4_0: 192-row tiles (96 gate + 96 up rows) when they give the
+      // ubatch's gate/up launch more CTAs than 256-row tiles and still fit
+      // one wave on the SMs (two 128-row M tiles per CTA); else 256 or 128
+      int bn = C->F % 128 == 0 ? 256 : 128;
+      if (wt == PF_W_Q4_0 && C->F % 96 == 0 && C->d.ubatch_max > 128) {
+        int sms = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, C->device);
+        const int pairs = (C->d.ubatch_max + 255) / 256;
+        const int u192 = (2 * C->F / 192) * pairs, u256 = C->F % 128 == 0 ? (2 * C->F / 256) * pairs : 0;
+        if (u192 > u256 && u192 <= sms) bn = 192;
+      }
       if ((rc = build_weight(C, L.gu, gu_rows(bn), C->D, bn))) return fail(nullptr, rc, C->last_error);
     }
     if ((rc = build_weight(C, L.down, plain_rows(lw.w_down, C->D, C->F, wt, 128), C->F, 128)))

@@ -108,8 +108,18 @@ def test_linear_resid_and_bf16_copy(lib):
 
 @pytest.mark.parametrize("act,wtype", [(0, Q4), (1, Q4), (0, F32)])
 def test_linear_glu(lib, act, wtype):
-    rng = np.random.default_rng(5 + act)
-    M, F, K = 140, 256, 512
+    _check_glu(lib, act, wtype, 140, 256, 512)
+
+
+@pytest.mark.parametrize("M", [100, 300])
+def test_linear_glu_192_row_tiles(lib, M):
+    """F = 576 (a multiple of 96, not of 128): Q4_0 gate/up interleaved in
+    192-row tiles; one and two 128-row M tiles per CTA."""
+    _check_glu(lib, 0, Q4, M, 576, 512)
+
+
+def _check_glu(lib, act, wtype, M, F, K):
+    rng = np.random.default_rng(5 + act + M)
     wg, wg_gpu, wg_exact = _weights(wtype, rng, F, K)
     wu, wu_gpu, wu_exact = _weights(wtype, rng, F, K)
     A = _A(rng, M, K, scale=8.0 if wtype == Q4 else 1.0)
