@@ -92,8 +92,8 @@ int pfop_kv_copy(int32_t dir, void* cache_dev, int64_t cache_seg_halves, void* i
 /* out[n] = sum_k a[k] W[n][k] (fp32 [N]) for ONE row a (bf16 [K]) with the
    one-token projection kernel that a one-token ubatch uses (generation
    after the prompt): CUDA cores stream W once (wtype as in pfop_linear_f32,
-   bn its tile width), fp32 dot products, k-part sums added in a fixed
-   order.  If iters > 0 the call is then repeated `iters` times and *us
+   bn its tile width: 64, 128, 256, or 192 for Q4_0), fp32 dot products,
+   k-part sums added in a fixed order.  If iters > 0 the call is then repeated `iters` times and *us
    receives the mean device time per launch (CUDA events on `stream`). */
 int pfop_linear_row(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn, const void* a_dev,
                     float* out_dev, int32_t iters, float* us, void* stream);

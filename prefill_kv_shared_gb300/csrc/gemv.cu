@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_kernel(const __nv_bfloat16* _
                                                           float eps) {
   constexpr int RG = BN / 32;          // 32-row groups of a tile
   constexpr int KW = GV_WARPS / RG;    // warps along k inside the CTA
+  static_assert(KW >= 1 && RG * KW <= GV_WARPS, "row groups x k-slices must fit the CTA's warps");
   constexpr int TILE = BN * 36;        // bytes of one (tile, k-block) of Q4_0
   extern __shared__ __align__(16) float xs[];  // the row, fp32 [K]; then the weight slice
   __shared__ float part_s[GV_WARPS][32];
@@ -170,7 +171,9 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_kernel(const __nv_bfloat16* _
   const int rg = warp % RG, kw = warp / RG;
   const int r = rg * 32 + lane;
   const int nk = kb1 - kb0;
-  const int c0 = kb0 + kw * nk / KW, c1 = kb0 + (kw + 1) * nk / KW;
+  // warps past RG * KW (BN = 192: six row groups, one k-slice, warps 6 and
+  // 7) take no k-blocks
+  const int c0 = kw < KW ? kb0 + kw * nk / KW : kb0, c1 = kw < KW ? kb0 + (kw + 1) * nk / KW : kb0;
   float acc = 0.f;
   if constexpr (WK == W_Q4) {
     // bounded: a copy that never lands flags the error word; the sums are

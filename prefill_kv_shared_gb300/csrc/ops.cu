@@ -128,8 +128,8 @@ extern "C" int pfop_linear_f32(int32_t wtype, const void* w_host, int32_t N, int
 
 extern "C" int pfop_linear_row(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn,
                                const void* a_dev, float* out_dev, int32_t iters, float* us, void* stream) {
-  if (!w_host || !a_dev || !out_dev || N < 1 || N % 4 || K % 64 || (bn != 64 && bn != 128 && bn != 256) ||
-      iters < 0 || (iters > 0 && !us))
+  if (!w_host || !a_dev || !out_dev || N < 1 || N % 4 || K % 64 ||
+      (bn != 64 && bn != 128 && bn != 256 && !(bn == 192 && wtype == PF_W_Q4_0)) || iters < 0 || (iters > 0 && !us))
     return op_fail(PF_E_ARG, "bad argument");
   Scope sc;
   WeightMat W;

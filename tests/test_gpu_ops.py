@@ -369,7 +369,7 @@ def test_kv_copy_bench_restores_exactly(lib):
 
 @pytest.mark.parametrize("wtype,N,K,bn", [(Q4, 1536, 6144, 64), (Q4, 2560, 1536, 128), (Q4, 12288, 1536, 256),
                                           (Q4, 200, 256, 64), (Q4, 32768, 1536, 128), (F32, 384, 512, 128),
-                                          (F32, 256, 1024, 256)])
+                                          (F32, 256, 1024, 256), (Q4, 12288, 1536, 192), (Q4, 500, 512, 192)])
 def test_linear_row_stream(lib, wtype, N, K, bn):
     """The one-token projection (CUDA cores, fp32): against float64 on the
     exact Q4_0 decode (its weights are exact in fp32, no bf16 rounding), the
