@@ -25,7 +25,8 @@ extern "C" {
 #endif
 
 /* out[m][n] = sum_k A[m][k] W[n][k] (fp32 [M][N]); W [N][K] in wtype
-   (PF_W_Q4_0 blocks or fp32, computed as bf16).  bn: N-tile, 64, 128 or 256. */
+   (PF_W_Q4_0 blocks or fp32, computed as bf16).  bn: N-tile, 64, 128 or 256
+   (192 with Q4_0). */
 int pfop_linear_f32(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn, const void* a_dev,
                     int32_t a_rows, int32_t M, float* out_dev, void* stream);
 
@@ -113,8 +114,10 @@ int pfop_linear_wait_test(int32_t wtype, const void* w_host, int32_t N, int32_t 
 
 /* Time the GEMM kernel: upload W once, run `warmup` then `iters` launches of
    out = A W^T (fp32 [M][N]) and return the mean device time per launch in
-   *us (CUDA events on `stream`).  split: k-splits (0 = the library's choice
-   for this shape). */
+   *us (CUDA events on `stream`).  split: k-splits on single CTAs (0 = the
+   library's choice for this shape; -1 = no split, 2-CTA pairs sharing
+   256-row tcgen05 MMAs, Q4_0 with bn 128, 192 or 256 only).  bn 192 takes
+   Q4_0 weights only. */
 int pfop_linear_bench(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn, int32_t split,
                       const void* a_dev, int32_t a_rows, int32_t M, float* out_dev, int32_t warmup, int32_t iters,
                       float* us, void* stream);
@@ -164,6 +167,13 @@ int pfop_kv_copy_bench(int32_t dir, void* cache_dev, int64_t cache_seg_halves, v
    call before capturing any stream.  Synchronous on `stream`. */
 int pfop_attention_split_noalloc(const void* q_dev, const void* k_dev, const void* v_dev, int32_t Hq, int32_t Hkv,
                                  int32_t hd, int32_t pos, int32_t kv_len, void* out_dev, void* stream);
+
+/* How the GEMMs of the pfop_* calls run (process-wide, for every later
+   call): 0 = as the library picks per matrix shape (the default), 1 = every
+   Q4_0 matrix with 128-, 192- or 256-row tiles in 2-CTA pairs (tcgen05
+   .cta_group::2, no k-split), -1 = never in pairs.  Lets the same checks run
+   on both forms; no effect on prefill contexts.  PF_E_ARG for other modes. */
+int pfop_set_gemm_pairs(int32_t mode);
 
 /* Last error message of a pfop_* call on this thread. */
 const char* pfop_last_error(void);

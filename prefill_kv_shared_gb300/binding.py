@@ -48,7 +48,7 @@ EXPORTS = (
     "pfop_attention_split_noalloc", "pfop_attention_bench", "pfop_kv_copy_bench",
     "kv_save_file", "kv_load_file", "prefill_kv_file_check", "pfop_linear_row", "prefill_set_output",
     "pfop_linear_wait_test", "prefill_ubatch_seqs", "prefill_seq_n_pos", "prefill_seq_reset",
-    "prefill_graph_capture", "prefill_graph_launch",
+    "prefill_graph_capture", "prefill_graph_launch", "pfop_set_gemm_pairs",
 )
 
 
@@ -157,6 +157,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
                                          C.POINTER(C.c_float), vp]),
         "pfop_linear_row": (C.c_int, [i32, vp, i32, i32, i32, vp, vp, i32, C.POINTER(C.c_float), vp]),
         "pfop_linear_wait_test": (C.c_int, [i32, vp, i32, i32, i32, vp, i32, i32, vp, i32, vp]),
+        "pfop_set_gemm_pairs": (C.c_int, [i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

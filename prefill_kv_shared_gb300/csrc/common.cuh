@@ -131,15 +131,27 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// CL: acquire at cluster scope, for phases that a peer CTA's release (a
+// remote arrive or a multicast tcgen05.commit) completes
+template <bool CL = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar_addr), "r"(parity)
-      : "memory");
+  if constexpr (CL)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
   return ok != 0;
 }
 
@@ -151,12 +163,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 #ifndef PF_WAIT_CYCLES
 #define PF_WAIT_CYCLES 4000000000ll  // about 2 s
 #endif
+template <bool CL = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  if (mbar_try_wait<CL>(a, parity)) return true;
   long long t0 = 0;
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (mbar_try_wait<CL>(a, parity)) return true;
     if ((i & 4095u) == 0u) {
       const long long now = clock64();
       if (t0 == 0) {
@@ -172,26 +185,37 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
 
 // Non-suspending probe of a phase (test_wait never parks the thread, so a
 // spinning waiter sees the phase complete at once)
+template <bool CL = false>
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar_addr, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar_addr), "r"(parity)
-      : "memory");
+  if constexpr (CL)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
   return ok != 0;
 }
 
 // The bounded wait of mbar_wait as a pure spin on test_wait, for the single
 // thread whose issue rate paces a pipeline.
+template <bool CL = false>
 __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, int* err, int code) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_test_wait(a, parity)) return true;
+  if (mbar_test_wait<CL>(a, parity)) return true;
   long long t0 = 0;
   for (uint32_t i = 1;; ++i) {
-    if (mbar_test_wait(a, parity)) return true;
+    if (mbar_test_wait<CL>(a, parity)) return true;
     if ((i & 4095u) == 0u) {
       const long long now = clock64();
       if (t0 == 0) {
@@ -209,13 +233,14 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, i
 // main loop): between polls the thread sleeps about `ns` nanoseconds, so that
 // waiting warps do not take shared-memory and issue bandwidth from the warps
 // that feed the tensor cores.  Wakes at most about `ns` late.
+template <bool CL = false>
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, int* err, int code, uint32_t ns) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  if (mbar_try_wait<CL>(a, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {
     __nanosleep(ns);
-    if (mbar_try_wait(a, parity)) return true;
+    if (mbar_try_wait<CL>(a, parity)) return true;
     if ((i & 255u) == 0u) {
       if (clock64() - t0 > PF_WAIT_CYCLES) {
         set_error(err, code);
@@ -312,6 +337,52 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
+}
+
+// ---- CTA pairs (tcgen05 .cta_group::2): one MMA covers 256 rows, rows
+// 0..127 of A and D in the even CTA of a 2-CTA cluster, rows 128..255 in the
+// odd one; B's N rows are split in two halves, one per CTA's shared memory
+// at the same offset.  Every tcgen05 instruction of a kernel that uses pairs
+// carries .cta_group::2.
+
+// collective over one warp in each CTA of the pair; both get the same address
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// issued by one thread of the even CTA
+__device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// arrive on the mbarrier at this shared-memory offset in every CTA of
+// cta_mask (bit r = cluster rank r) once the pair's tcgen05 ops issued so far
+// by this thread have completed
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// arrive (release at cluster scope) on an mbarrier given by its
+// shared::cluster address (mapa), in this CTA or a peer
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns; thread i of the warp gets lane

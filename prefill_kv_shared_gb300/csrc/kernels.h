@@ -62,6 +62,7 @@ struct WeightMat {
   int K = 0;
   int BN = 128;
   int split = 1;   // k-splits (fixed per matrix shape; K/64 divisible by it)
+  int pair = 0;    // 1: launches run in 2-CTA clusters sharing 256-row MMAs (Q4_0 only, split 1)
   void* dev = nullptr;
   size_t bytes = 0;
   CUtensorMap tmap;
@@ -84,6 +85,9 @@ bool make_weight_map(WeightMat& w, std::string* err);
 // k-splits (cluster size) for a weight shape, chosen from the shape and the
 // largest M the context runs; never from a launch's M
 int choose_split(int kind, int N_rows, int BN, int K, int max_rows);
+// 1 if the matrix's launches run in CTA pairs (tcgen05 .cta_group::2),
+// chosen like the split; a matrix with a k-split never does
+int choose_pair(int kind, int N_rows, int BN, int K, int max_rows, int split);
 // Q|K|V weight rows in GEMM tile order (128-row tiles; heads wider than a
 // tile are cut so that RoPE pairs share a tile; V in plain order), padded to
 // BN with NULL rows.  wk/wv may be NULL (a Q-only projection).
@@ -95,6 +99,10 @@ std::vector<const void*> qkv_tile_rows(const void* wq, const void* wk, const voi
 // CTA 0's copy producer issues nothing from that pipeline stage on.
 cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err_word,
                         cudaStream_t s, int withhold_stage = -1);
+// the CTA-pair launches of launch_gemm (W.pair set); two: two 256-row MMA
+// tiles per pair
+cudaError_t launch_gemm_pair(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err_word,
+                             cudaStream_t s, int withhold_stage, bool two);
 
 // One row (a one-token ubatch): out = A[0] W^T with the same fused epilogue,
 // streamed by CUDA cores over (tile, k-part) CTAs.  `sums` holds

@@ -4,6 +4,7 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <string>
@@ -14,6 +15,8 @@ using namespace pf;
 namespace {
 
 thread_local std::string g_err;
+// CTA pairs for the op entry points' GEMMs (pfop_set_gemm_pairs)
+std::atomic<int> g_pairs{0};
 
 int op_fail(int code, const std::string& m) {
   g_err = m;
@@ -52,7 +55,15 @@ int make_weight(Scope& sc, WeightMat& w, int wtype, const std::vector<const void
   w.N_rows = static_cast<int>(rows.size());
   // the split depends on the matrix shape only (as in a context with
   // ubatch_max = 512), so one row gives the same bits whatever M is
-  w.split = choose_split(wtype == PF_W_Q4_0 ? W_Q4 : W_BF16, w.N_rows, BN, K, 512);
+  const int kind = wtype == PF_W_Q4_0 ? W_Q4 : W_BF16;
+  w.split = choose_split(kind, w.N_rows, BN, K, 512);
+  const int pm = g_pairs.load();
+  if (pm > 0 && kind == W_Q4 && (BN == 128 || BN == 192 || BN == 256)) {
+    w.split = 1;
+    w.pair = 1;
+  } else {
+    w.pair = pm == 0 ? choose_pair(kind, w.N_rows, BN, K, 512, w.split) : 0;
+  }
   if (wtype == PF_W_Q4_0) {
     w.kind = W_Q4;
     std::vector<const uint8_t*> r(rows.size());
@@ -105,11 +116,18 @@ int run_gemm(Scope& sc, const ActMat& A, int M, const WeightMat& W, const EpiPar
 
 extern "C" const char* pfop_last_error(void) { return g_err.c_str(); }
 
+extern "C" int pfop_set_gemm_pairs(int32_t mode) {
+  if (mode < -1 || mode > 1) return op_fail(PF_E_ARG, "mode must be -1, 0 or 1");
+  g_pairs.store(mode);
+  return PF_OK;
+}
+
 void pf::set_op_error(const std::string& m) { g_err = m; }
 
 extern "C" int pfop_linear_f32(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn, const void* a_dev,
                                int32_t a_rows, int32_t M, float* out_dev, void* stream) {
-  if (!w_host || !a_dev || !out_dev || N < 1 || M < 1 || M > a_rows || (bn != 64 && bn != 128 && bn != 256))
+  if (!w_host || !a_dev || !out_dev || N < 1 || M < 1 || M > a_rows ||
+      (bn != 64 && bn != 128 && bn != 256 && !(bn == 192 && wtype == PF_W_Q4_0)))
     return op_fail(PF_E_ARG, "bad argument");
   Scope sc;
   WeightMat W;
@@ -178,8 +196,9 @@ extern "C" int pfop_linear_row(int32_t wtype, const void* w_host, int32_t N, int
 extern "C" int pfop_linear_bench(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn, int32_t split,
                                  const void* a_dev, int32_t a_rows, int32_t M, float* out_dev, int32_t warmup,
                                  int32_t iters, float* us, void* stream) {
-  if (!w_host || !a_dev || !out_dev || !us || N < 1 || N % 4 || M < 1 || M > a_rows || (bn != 64 && bn != 128 && bn != 256) ||
-      iters < 1 || warmup < 0 || split < 0)
+  if (!w_host || !a_dev || !out_dev || !us || N < 1 || N % 4 || M < 1 || M > a_rows ||
+      (bn != 64 && bn != 128 && bn != 256 && !(bn == 192 && wtype == PF_W_Q4_0)) || iters < 1 || warmup < 0 ||
+      split < -1 || (split == -1 && (wtype != PF_W_Q4_0 || bn == 64)))
     return op_fail(PF_E_ARG, "bad argument");
   Scope sc;
   WeightMat W;
@@ -189,6 +208,10 @@ extern "C" int pfop_linear_bench(int32_t wtype, const void* w_host, int32_t N, i
   if (split > 0) {
     if ((K / 64) % split) return op_fail(PF_E_ARG, "split must divide K/64");
     W.split = split;
+    W.pair = 0;
+  } else if (split == -1) {
+    W.split = 1;
+    W.pair = 1;
   }
   if ((rc = make_act(A, a_dev, a_rows, K))) return rc;
   EpiParams e;

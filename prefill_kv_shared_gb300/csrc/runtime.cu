@@ -193,8 +193,9 @@ int build_weight(prefill_ctx* c, WeightMat& w, const std::vector<const void*>& r
   w.BN = BN;
   w.N_rows = static_cast<int>(rows.size());
   if (w.N_rows % BN != 0 || K % 64 != 0) return fail(c, PF_E_ARG, "weight shape not tileable");
-  w.split = split_as > 0 ? split_as
-                         : choose_split(c->d.wtype == PF_W_Q4_0 ? W_Q4 : W_BF16, w.N_rows, BN, K, c->d.ubatch_max);
+  const int kind = c->d.wtype == PF_W_Q4_0 ? W_Q4 : W_BF16;
+  w.split = split_as > 0 ? split_as : choose_split(kind, w.N_rows, BN, K, c->d.ubatch_max);
+  w.pair = choose_pair(kind, w.N_rows, BN, K, c->d.ubatch_max, w.split);
   std::string err;
   if (c->d.wtype == PF_W_Q4_0) {
     w.kind = W_Q4;
