@@ -107,12 +107,19 @@ int choose_split(int kind, int N_rows, int BN, int K, int max_rows) {
 }
 
 int choose_pair(int kind, int N_rows, int BN, int K, int max_rows, int split) {
-  // CTA pairs halve each SM's B-operand traffic and MMA instructions; they
-  // need Q4_0 tiles of 128 rows or more (64 rows a CTA), no k-split, and
-  // ubatches of more than one 128-row tile.
+  // CTA pairs halve each SM's B-operand traffic, dequant work and MMA
+  // instructions, but on GB300 every measured projection shape (E2B and E4B
+  // QKV, O, gate/up, down at 512 and 1024 rows) ran 15-55 % slower in pairs
+  // than on single CTAs: the main loop waits on operand latency, not on B
+  // traffic, and a pair adds a cross-SM hop to every stage.  The library
+  // therefore never picks them; pfop_set_gemm_pairs runs them on request.
+  (void)kind;
   (void)N_rows;
+  (void)BN;
   (void)K;
-  return kind == W_Q4 && split == 1 && (BN == 128 || BN == 192 || BN == 256) && max_rows > 128 ? 1 : 0;
+  (void)max_rows;
+  (void)split;
+  return 0;
 }
 
 std::vector<const void*> qkv_tile_rows(const void* wq, const void* wk, const void* wv, int Hq, int Hkv, int hd,

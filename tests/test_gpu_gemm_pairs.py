@@ -2,10 +2,12 @@
 cluster stages its own 128 rows of A and half of the Q4_0 weight tile, and one
 MMA covers 256 rows.  Checked against float64 on the bf16 operands the tensor
 cores see and against the oracle's exact Q4_0 decode, bit for bit against the
-same GEMM on single CTAs (every output element comes from the same MMA
-sequence over k), and through every fused epilogue.  Shapes cover ragged M,
+same GEMM on single CTAs without a k-split (every output element comes from
+the same MMA sequence over k), and through every fused epilogue.  Shapes cover ragged M,
 one and two 256-row MMA tiles per pair, several work units per pair (the
 persistent loop and its accumulator buffers) and all three tile widths."""
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -43,6 +45,16 @@ def _gemm(lib, mode, w, N, K, bn, a, R, M):
     return out
 
 
+def _gemm_split(lib, split, w, N, K, bn, a, R, M):
+    """One launch through the timing entry point: split 1 = single CTAs
+    without a k-split, -1 = CTA pairs."""
+    out = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    us = ctypes.c_float()
+    binding.check_op(lib.pfop_linear_bench(Q4, w.ctypes.data, N, K, bn, split, a.data_ptr(), R, M, out.data_ptr(), 0,
+                                           1, ctypes.byref(us), None))
+    return out
+
+
 PAIR_CASES = [
     (1, 256, 512, 128),
     (7, 384, 1536, 256),
@@ -67,14 +79,16 @@ def test_pairs_match_single_ctas(lib, M, N, K, bn):
     a, R = padded_a(A)
     try:
         got = _gemm(lib, 1, w, N, K, bn, a, R, M)
-        one = _gemm(lib, -1, w, N, K, bn, a, R, M)
     finally:
         lib.pfop_set_gemm_pairs(0)
     g = got.cpu().numpy()
     assert np.isfinite(g).all()
     assert rel_err(g, A.astype(np.float64) @ gpu_q4_weights(w).astype(np.float64).T) < 2e-5
     assert rel_err(g, A.astype(np.float64) @ as_f32_matrix(w).astype(np.float64).T) < 2e-2
-    assert torch.equal(got, one)
+    # the same bits as single CTAs over the same k-order (no k-split), and as
+    # the timing entry point's pair launch
+    assert torch.equal(got, _gemm_split(lib, 1, w, N, K, bn, a, R, M))
+    assert torch.equal(got, _gemm_split(lib, -1, w, N, K, bn, a, R, M))
 
 
 def test_glu_in_pairs(lib, pairs):
