@@ -111,6 +111,20 @@ inline cudaError_t smem_opt_in(int bytes) {
   return cudaSuccess;
 }
 
+// One lane of a fully active warp (elect.sync: always the same lane for the
+// full mask).  Async issue (TMA, tcgen05.mma, tcgen05.commit) is done by the
+// elected lane inside loops the whole warp runs in step, so that the
+// issue's operands can stay in warp-uniform registers.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, e;\n\t}"
+      : "=r"(p));
+  return p != 0;
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier
 

@@ -73,8 +73,10 @@ bool make_act_map(ActMat& a, std::string* err) {
   }
   std::memset(&a.tmap, 0, sizeof(a.tmap));
   std::memset(&a.tmap_small, 0, sizeof(a.tmap_small));
+  std::memset(&a.tmap_wide, 0, sizeof(a.tmap_wide));
   return encode_2d_bf16(&a.tmap, a.dev, (uint64_t)a.K, (uint64_t)a.rows, 64, 128, err) &&
-         encode_2d_bf16(&a.tmap_small, a.dev, (uint64_t)a.K, (uint64_t)a.rows, 64, 16, err);
+         encode_2d_bf16(&a.tmap_small, a.dev, (uint64_t)a.K, (uint64_t)a.rows, 64, 16, err) &&
+         encode_2d_bf16(&a.tmap_wide, a.dev, (uint64_t)a.K, (uint64_t)a.rows, 64, 256, err);
 }
 
 bool make_weight_map(WeightMat& w, std::string* err) {

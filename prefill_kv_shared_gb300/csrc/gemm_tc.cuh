@@ -105,7 +105,10 @@ struct GemmCfg {
       !Q4    ? 0
       : PAIR ? (BT_BYTES >= 32768 ? 2 : 3)
              : (BN >= 256 ? (MT == 2 ? 2 : 3) : BN == 192 ? 2 : KS == 2 ? (BN == 64 ? 4 : 2) : 4);
-  static constexpr int S_R = !Q4 ? 0 : PAIR ? S_B + 1 : (BN >= 192 ? 3 : KS == 2 ? (BN == 64 ? 6 : 3) : 6);
+  // (192-row tiles over two M tiles: two raw stages leave room for a
+  // fourth A stage, which paces the main loop there)
+  static constexpr int S_R =
+      !Q4 ? 0 : PAIR ? S_B + 1 : (BN == 192 && MT == 2 ? 2 : BN >= 192 ? 3 : KS == 2 ? (BN == 64 ? 6 : 3) : 6);
   static constexpr int NB = S_B > 0 ? S_B : 1;  // ring moduli (the rings are unused without Q4)
   static constexpr int NR = S_R > 0 ? S_R : 1;
   static constexpr int RAW_RING = (S_R * RAW_BYTES + 1023) / 1024 * 1024;
@@ -222,8 +225,9 @@ __device__ __forceinline__ uint32_t slot_off(int c, int r, int q) {
 
 template <int WK, int BN, int MT, bool PAIR>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const uint8_t* __restrict__ wq4, const GemmShape sh_in, const EpiParams ep_in, int* err) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                   const __grid_constant__ CUtensorMap tmB, const uint8_t* __restrict__ wq4, const GemmShape sh_in,
+                   const EpiParams ep_in, int* err) {
   using C = GemmCfg<WK, BN, MT, PAIR>;
   // The launch parameters are read from shared-memory copies: fields of a
   // kernel parameter used through a reference are re-read from parameter
@@ -290,6 +294,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tmA);
+    if (MT == 2 && !PAIR) prefetch_tensormap(&tmA2);
     if (WK == W_BF16) prefetch_tensormap(&tmB);
   }
   if (warp == 1) {
@@ -482,8 +487,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       }
       __syncwarp();
       pdl_wait();
-      // The main loop runs in lane 0 alone: no warp-wide step per k-block.
-      if (lane == 0) {
+      // The whole warp runs the main loop in step (waits and decisions
+      // uniform); one elected lane issues the copies.
+      {
         uint32_t g = 0;
         bool ok = true;
         for (int u = unit0; u < sh.n_units && ok; u += ustep) {
@@ -504,21 +510,33 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const bool raw_now = C::Q4 && g >= pre;
             const int sr = g % C::NR;
             if (ok && raw_now) ok = mbar_wait(&empty_r[sr], ((g / C::NR) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
+            ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
-            uint8_t* st = a_ring + sa * C::A_STAGE;
-            mbar_arrive_expect_tx(&full_a[sa], kc * mt_valid * sh.a_box_rows * 128 + (C::Q4 ? 0 : C::BT_BYTES));
-            for (int j = 0; j < kc; ++j)
-              for (int mt = 0; mt < mt_valid; ++mt)
-                tma_load_2d(st + (j * MT + mt) * 128 * 128, &tmA, &full_a[sa], (kb + j) * 64,
-                            m_base + mt * C::MMA_M + static_cast<int>(rank) * 128);
-            if (raw_now) {
-              issue_raw(r_ring + sr * C::RAW_BYTES, nt, kb, kc, &full_r[sr]);
-            } else if (!C::Q4) {
-              tma_load_2d(st + C::A_BYTES, &tmB, &full_a[sa], kb * 64, nt * BN);
+            if (elect_one()) {
+              uint8_t* st = a_ring + sa * C::A_STAGE;
+              mbar_arrive_expect_tx(&full_a[sa], kc * mt_valid * sh.a_box_rows * 128 + (C::Q4 ? 0 : C::BT_BYTES));
+              // two adjacent 128-row M tiles come in one 256-row box (the
+              // same shared-memory layout as two boxes); every async copy
+              // costs the issuing thread a fixed amount
+              if (!PAIR && MT == 2 && mt_valid == 2) {
+                for (int j = 0; j < kc; ++j)
+                  tma_load_2d(st + j * MT * 128 * 128, &tmA2, &full_a[sa], (kb + j) * 64, m_base);
+              } else {
+                for (int j = 0; j < kc; ++j)
+                  for (int mt = 0; mt < mt_valid; ++mt)
+                    tma_load_2d(st + (j * MT + mt) * 128 * 128, &tmA, &full_a[sa], (kb + j) * 64,
+                                m_base + mt * C::MMA_M + static_cast<int>(rank) * 128);
+              }
+              if (raw_now) {
+                issue_raw(r_ring + sr * C::RAW_BYTES, nt, kb, kc, &full_r[sr]);
+              } else if (!C::Q4) {
+                tma_load_2d(st + C::A_BYTES, &tmB, &full_a[sa], kb * 64, nt * BN);
+              }
             }
+            __syncwarp();
           }
         }
-        if (!ok) {
+        if (!ok && elect_one()) {
           // the last S_A / S_R issues may still be in flight
           const uint32_t ga = g > (uint32_t)C::S_A ? g - C::S_A : 0;
           for (uint32_t x = ga; x < g; ++x) mbar_drain(&full_a[x % C::S_A], (x / C::S_A) & 1);
@@ -544,7 +562,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             mbar_arrive_cluster(issuer_bar(&full_a[sa]));
           }
       }
-      if (lane == 0 && issuer) {
+      if (issuer) {
+        // the whole warp runs the loop in step; one lane, elected once (its
+        // commits track the MMAs it issued), issues
+        const bool leader = elect_one();
         constexpr uint32_t idesc = idesc_bf16_f32(C::MMA_M, BN);
         uint32_t g = 0, j = 0;
         bool ok = true;
@@ -556,6 +577,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           const int buf = C::ACC_BUFS == 2 ? (j & 1) : 0;
           const uint32_t tacc = tmem_base + buf * C::ACC;
           ok = mbar_wait<PAIR>(&tempty[buf], ((j / C::ACC_BUFS) & 1) ^ 1, err, PF_DEV_TIMEOUT_MMA);
+          ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after();
           const int nst = (nkb + C::KS - 1) / C::KS;
@@ -565,6 +587,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const int sb = C::Q4 ? g % C::NB : 0;
             ok = mbar_wait_spin<PAIR>(&full_a[sa], (g / C::S_A) & 1, err, PF_DEV_TIMEOUT_MMA);
             if (ok && C::Q4) ok = mbar_wait_spin<PAIR>(&bfull[sb], (g / C::NB) & 1, err, PF_DEV_TIMEOUT_MMA);
+            ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
             const uint32_t a0 = smem_u32(a_ring + sa * C::A_STAGE);
@@ -572,8 +595,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             // The stage's descriptors are built once; an operand's address
             // sits in the low bits (16-byte units, 14 bits) and every step
             // adds a constant offset that cannot carry out of that field.
-            // A single issuing thread pays for every instruction between
-            // two MMAs, so the common full stage is unrolled completely.
             // With pairs the same descriptors address both CTAs' shared
             // memory (identical layouts).
             const uint64_t ad0 = sdesc_sw128(a0), bd0 = sdesc_sw128(b0);
@@ -583,42 +604,46 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               else
                 tc_mma_f16(d, a, b, idesc, acc);
             };
-            if (kc == C::KS && mt_valid == MT) {
+            if (leader) {
+              if (kc == C::KS && mt_valid == MT) {
 #pragma unroll
-              for (int j = 0; j < C::KS; ++j)
+                for (int j = 0; j < C::KS; ++j)
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
+                  for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                  for (int kk = 0; kk < 4; ++kk)
-                    mma(tacc + mt * BN, ad0 + (((j * MT + mt) * 128 * 128 + kk * 32) >> 4),
-                        bd0 + ((j * C::BT_KB + kk * 32) >> 4), (i | j | kk) != 0 ? 1u : 0u);
-            } else {
-              for (int j = 0; j < kc; ++j) {
-                const int kbl = i * C::KS + j;  // k-block within the unit
-                for (int mt = 0; mt < mt_valid; ++mt) {
+                    for (int kk = 0; kk < 4; ++kk)
+                      mma(tacc + mt * BN, ad0 + (((j * MT + mt) * 128 * 128 + kk * 32) >> 4),
+                          bd0 + ((j * C::BT_KB + kk * 32) >> 4), (i | j | kk) != 0 ? 1u : 0u);
+              } else {
+                for (int j = 0; j < kc; ++j) {
+                  const int kbl = i * C::KS + j;  // k-block within the unit
+                  for (int mt = 0; mt < mt_valid; ++mt) {
 #pragma unroll
-                  for (int kk = 0; kk < 4; ++kk)
-                    mma(tacc + mt * BN, ad0 + (((j * MT + mt) * 128 * 128 + kk * 32) >> 4),
-                        bd0 + ((j * C::BT_KB + kk * 32) >> 4), (kbl | kk) != 0 ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk)
+                      mma(tacc + mt * BN, ad0 + (((j * MT + mt) * 128 * 128 + kk * 32) >> 4),
+                          bd0 + ((j * C::BT_KB + kk * 32) >> 4), (kbl | kk) != 0 ? 1u : 0u);
+                  }
                 }
               }
+              if constexpr (PAIR) {
+                tc_commit_pair(&empty_a[sa], 3);
+                tc_commit_pair(&bempty[sb], 3);
+              } else {
+                tc_commit(&empty_a[sa]);
+                if (C::Q4) tc_commit(&bempty[sb]);
+              }
             }
-            if constexpr (PAIR) {
-              tc_commit_pair(&empty_a[sa], 3);
-              tc_commit_pair(&bempty[sb], 3);
-            } else {
-              tc_commit(&empty_a[sa]);
-              if (C::Q4) tc_commit(&bempty[sb]);
-            }
+            __syncwarp();
           }
-          if (ok) {  // the unit's accumulator is complete
+          if (ok && leader) {  // the unit's accumulator is complete
             if constexpr (PAIR)
               tc_commit_pair(&tfull[buf], 3);
             else
               tc_commit(&tfull[buf]);
           }
+          __syncwarp();
         }
-        if (!ok) {
+        if (!ok && leader) {
           // wait for the MMAs already issued before TMEM is freed (and,
           // with pairs, before the odd CTA may leave)
           if constexpr (PAIR)
@@ -790,7 +815,8 @@ inline cudaError_t launch_t(const ActMat& A, int M, const WeightMat& W, const Ep
     grid = sh.n_units < sm_count() ? sh.n_units : sm_count();
   }
   return launch_k(gemm_tc_kernel<WK, BN, MT, PAIR>, dim3(grid), dim3(GEMM_THREADS), C::SMEM_BYTES, s, cluster,
-                  small ? A.tmap_small : A.tmap, W.tmap, static_cast<const uint8_t*>(W.dev), sh, ep, err);
+                  small ? A.tmap_small : A.tmap, A.tmap_wide, W.tmap, static_cast<const uint8_t*>(W.dev), sh, ep,
+                  err);
 }
 
 }  // namespace pf

@@ -74,6 +74,7 @@ struct ActMat {
   int rows = 0, K = 0;
   CUtensorMap tmap;        // 128-row boxes
   CUtensorMap tmap_small;  // 16-row boxes, for launches of at most 16 rows
+  CUtensorMap tmap_wide;   // 256-row boxes: two 128-row M tiles in one copy
 };
 
 bool make_act_map(ActMat& a, std::string* err);
