@@ -269,7 +269,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int ustep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   // The issuing CTA's full_a, bfull and tempty also count the odd CTA's
-  // forwarded arrivals.
+  // forwarded arrivals (remote arrives, released at cluster scope): its MMA
+  // thread waits on them with cluster-scope acquire.  Barriers that only
+  // tcgen05.commit completes (empty_a, bempty, tfull, multicast to both
+  // CTAs) order the tensor cores' accesses by themselves and are waited on
+  // at CTA scope.
   const uint32_t peers = PAIR && issuer ? 2u : 1u;
 
   if (threadIdx.x == 0) {
@@ -339,7 +343,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         int mt_valid = (sh.M - m_base + C::MMA_M - 1) / C::MMA_M;
         if (mt_valid > MT) mt_valid = MT;
         const int buf = C::ACC_BUFS == 2 ? (j & 1) : 0;
-        bool ok = mbar_wait_sleep<PAIR>(&tfull[buf], (j / C::ACC_BUFS) & 1, err, PF_DEV_TIMEOUT_EPILOGUE, 128);
+        bool ok = mbar_wait_sleep(&tfull[buf], (j / C::ACC_BUFS) & 1, err, PF_DEV_TIMEOUT_EPILOGUE, 128);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
           epi_ok = false;
@@ -506,7 +510,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               ok = false;  // stop issuing; the stages already issued are drained below
               break;
             }
-            ok = mbar_wait<PAIR>(&empty_a[sa], ((g / C::S_A) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
+            ok = mbar_wait(&empty_a[sa], ((g / C::S_A) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
             const bool raw_now = C::Q4 && g >= pre;
             const int sr = g % C::NR;
             if (ok && raw_now) ok = mbar_wait(&empty_r[sr], ((g / C::NR) & 1) ^ 1, err, PF_DEV_TIMEOUT_PRODUCER);
@@ -666,7 +670,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           const int kc = nkb - i * C::KS < C::KS ? nkb - i * C::KS : C::KS;
           const int sr = g % C::NR, sb = g % C::NB;
           bool w_ok = mbar_wait(&full_r[sr], (g / C::NR) & 1, err, PF_DEV_TIMEOUT_DEQUANT);
-          if (w_ok) w_ok = mbar_wait<PAIR>(&bempty[sb], ((g / C::NB) & 1) ^ 1, err, PF_DEV_TIMEOUT_DEQUANT);
+          if (w_ok) w_ok = mbar_wait(&bempty[sb], ((g / C::NB) & 1) ^ 1, err, PF_DEV_TIMEOUT_DEQUANT);
           ok = __all_sync(0xffffffffu, w_ok);
           if (!ok) break;
           uint8_t* bt = b_ring + sb * C::BT_BYTES;
