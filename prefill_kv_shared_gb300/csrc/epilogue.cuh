@@ -57,13 +57,16 @@ __device__ __forceinline__ float4 bf16x4_to_f32(uint2 p) {
 // m0 .. m0+31, of which the first rv are real (warp-uniform).  load(c, v)
 // fills v with this lane's row (m0 + lane) of the tile's column chunk c
 // (columns 32c .. 32c+31) and is called in a warp-uniform way.  The two
-// epilogue warps of a lane quarter (ew = 0, 1) take alternate work items.
-// st: the warp's staging buffer.
+// epilogue warps of a lane quarter (ew = 0, 1) take alternate work items;
+// `par` (0 or 1) flips which of them takes the first, so that over the M
+// tiles of a unit (par = tile index & 1) an odd item count still splits
+// evenly.  st: the warp's staging buffer.
 template <int BN, class Load>
 __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m0, int rv, int n_tile, int ew, uint8_t* st,
-                                             Load&& load) {
+                                             int par, Load&& load) {
   constexpr int NCH = BN / 32;
   if (rv <= 0) return;
+  const int ew0 = ew ^ (par & 1);  // parity of this warp's items
   const int lane = threadIdx.x & 31;
   const int rs = lane >> 3, p = lane & 7;  // transposed position: rows 4i + rs, columns 4p .. 4p+3
   const int n0 = n_tile * BN;
@@ -77,7 +80,7 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m0, int rv
     // gate chunk c and up chunk c + NCH/2 of the interleaved tile -> output
     // columns f0 .. f0+31
     constexpr int HALF_CH = NCH / 2;
-    for (int c = ew; c < HALF_CH; c += 2) {
+    for (int c = ew0; c < HALF_CH; c += 2) {
       const int f0 = n_tile * (BN / 2) + 32 * c;
       if (f0 >= ep.N) break;
       load(c, v);
@@ -130,7 +133,7 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m0, int rv
       const int n = n0 + 32 * c;
       if (n >= v_end) break;  // padding columns
       if (n >= k_end) {       // V: no rotation
-        if ((item++ & 1) != ew) continue;
+        if ((item++ & 1) != ew0) continue;
         load(c, v);
         stage_put(st, lane, v);
         __syncwarp();
@@ -162,7 +165,7 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m0, int rv
         head = rel / hd;
         partner = c + pair_ch;
       }
-      if ((item++ & 1) != ew) continue;
+      if ((item++ & 1) != ew0) continue;
       // two passes of 16 rows each keep the transposed halves in registers
       for (int hp = 0; hp < 2; ++hp) {
         float4 c01[4], c23[4];  // (cos, sin) of columns i0+4p .. i0+4p+3 at each row's position
@@ -216,38 +219,45 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int m0, int rv
 
   // F32, RESID, PLE: one 32-column chunk at a time.  The chunk's global
   // operand (RESID: the residual rows; PLE: the multipliers) is requested
-  // before the TMEM load so that its latency overlaps the staging.
-  for (int c = ew; c < NCH; c += 2) {
+  // before the TMEM load so that its latency overlaps the staging.  (Asking
+  // for the next chunk's operand before this chunk's stores does not fit
+  // the registers: the epilogue then spills.)
+  auto load_side = [&](int c, float4(&sd)[8]) {
+    const int col = n0 + 32 * c + 4 * p;
+    const bool full = col + 4 <= ep.N;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = 4 * i + rs;
+      sd[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r >= rv || col >= ep.N) continue;
+      if (ep.kind == EPI_RESID) {
+        const float* xr = ep.out_f32 + (size_t)(m0 + r) * ep.ld_f32 + col;
+        if (full) {
+          sd[i] = *reinterpret_cast<const float4*>(xr);
+        } else {
+          sd[i].x = xr[0];
+          if (col + 1 < ep.N) sd[i].y = xr[1];
+          if (col + 2 < ep.N) sd[i].z = xr[2];
+        }
+      } else if (ep.kind == EPI_PLE) {
+        const __nv_bfloat16* pl = ep.ple + (size_t)(m0 + r) * ep.ple_stride + col;
+        if (full) {
+          sd[i] = bf16x4_to_f32(*reinterpret_cast<const uint2*>(pl));
+        } else {
+          sd[i].x = __bfloat162float(pl[0]);
+          if (col + 1 < ep.N) sd[i].y = __bfloat162float(pl[1]);
+          if (col + 2 < ep.N) sd[i].z = __bfloat162float(pl[2]);
+        }
+      }
+    }
+  };
+  for (int c = ew0; c < NCH; c += 2) {
     const int n = n0 + 32 * c;
     if (n >= ep.N) break;
     const int col = n + 4 * p;
     const bool full = col + 4 <= ep.N;
     float4 side[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int r = 4 * i + rs;
-      side[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (r >= rv || col >= ep.N) continue;
-      if (ep.kind == EPI_RESID) {
-        const float* xr = ep.out_f32 + (size_t)(m0 + r) * ep.ld_f32 + col;
-        if (full) {
-          side[i] = *reinterpret_cast<const float4*>(xr);
-        } else {
-          side[i].x = xr[0];
-          if (col + 1 < ep.N) side[i].y = xr[1];
-          if (col + 2 < ep.N) side[i].z = xr[2];
-        }
-      } else if (ep.kind == EPI_PLE) {
-        const __nv_bfloat16* pl = ep.ple + (size_t)(m0 + r) * ep.ple_stride + col;
-        if (full) {
-          side[i] = bf16x4_to_f32(*reinterpret_cast<const uint2*>(pl));
-        } else {
-          side[i].x = __bfloat162float(pl[0]);
-          if (col + 1 < ep.N) side[i].y = __bfloat162float(pl[1]);
-          if (col + 2 < ep.N) side[i].z = __bfloat162float(pl[2]);
-        }
-      }
-    }
+    load_side(c, side);
     load(c, v);
     stage_put(st, lane, v);
     __syncwarp();

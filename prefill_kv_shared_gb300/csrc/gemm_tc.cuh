@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           // they are all past M
           const int m0 = m_base + mt * C::MMA_M + static_cast<int>(rank) * 128 + 32 * qw;
           const int rv = sh.M - m0 < 32 ? sh.M - m0 : 32;
-          run_epilogue<BN>(ep, m0, rv, nt, ew, stage, [&](int c, float(&v)[32]) {
+          run_epilogue<BN>(ep, m0, rv, nt, ew, stage, mt, [&](int c, float(&v)[32]) {
             uint32_t x[32];
             tmem_ld32(tq + mt * BN + 32 * c, x);
             tmem_ld_wait();
@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           uint8_t* stage = epi_stage + (warp - EPI_WARP0) * EPI_STAGE_BYTES;
           const int m0 = m_base + 32 * qw;
           const int rv = sh.M - m0 < 32 ? sh.M - m0 : 32;
-          run_epilogue<BN>(ep, m0, rv, nt, ew, stage, [&](int c, float(&v)[32]) {
+          run_epilogue<BN>(ep, m0, rv, nt, ew, stage, 0, [&](int c, float(&v)[32]) {
             uint32_t x[32];
             tmem_ld32(tq + 32 * c, x);
             tmem_ld_wait();

@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_kernel(const __nv_bfloat16* _
   if (tid == 0) tickets[nt] = 0;  // ready for the next launch
   __syncthreads();
   if (warp < 2)
-    run_epilogue<BN>(ep, 0, 1, nt, warp, stage[warp], [&](int c, float(&v)[32]) {
+    run_epilogue<BN>(ep, 0, 1, nt, warp, stage[warp], 0, [&](int c, float(&v)[32]) {
 #pragma unroll
       for (int q = 0; q < 32; ++q) v[q] = lane == 0 ? yv[32 * c + q] : 0.f;
     });
