@@ -104,6 +104,12 @@ int choose_split(int kind, int N_rows, int BN, int K, int max_rows) {
   const int units1 = (N_rows / BN) * ((max_rows + 127) / 128);
   const int nkb = K / 64;
   const size_t ring = ring_bytes_mt1(kind, BN);
+  // Matrices with very few output tiles (the 256-row per-layer-embedding
+  // gate: 16 units at 512 rows) are bound by the length of each CTA's
+  // k-loop, not by tile counts: they take a 4-way split when it fits.
+  if (units1 <= 16 && units1 * 4 <= sm_count() && nkb % 4 == 0 && nkb / 4 >= 4 &&
+      static_cast<size_t>(3) * 128 * BN * 4 <= ring)
+    return 4;
   if (units1 * 2 <= sm_count() && nkb % 2 == 0 && nkb / 2 >= 4 && static_cast<size_t>(128) * BN * 4 <= ring) return 2;
   return 1;
 }
