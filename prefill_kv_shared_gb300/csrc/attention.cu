@@ -28,8 +28,11 @@
 // that its bits are the same whether the layer carries one row or the whole
 // ubatch.
 //
-// CTA roles: warp 1 lane 0 issues the TMA copies (Q once; K and V per chunk,
-// double-buffered); warp 0 allocates TMEM and its lane 0 issues the MMAs;
+// CTA roles: warp 1 lane 0 issues the TMA copies of Q (once) and of K, warp
+// 6 lane 0 those of V (K and V each double-buffered, on separate barriers:
+// a K buffer is free again once S = Q K^T has read it, a V buffer once P V
+// has, so the next K copies start a whole softmax earlier than with one
+// shared buffer); warp 0 allocates TMEM and its lane 0 issues the MMAs;
 // warps 2..5 own the 128 rows (thread = TMEM lane = row): softmax, the P tile
 // (fp16, 128-byte-swizzled K-major: the A operand of P V), the O rescale and
 // the output.  The MMA thread issues S(j+1) = Q K(j+1)^T before P(j) V(j), so
@@ -87,7 +90,7 @@ struct AttnTcCfg {
   static constexpr int TMEM_S = 0;                  // two S buffers of 64 columns
   static constexpr int TMEM_O = 2 * CHUNK;          // O: HD columns
   static constexpr int TMEM_COLS = (TMEM_O + HD) <= 256 ? 256 : 512;
-  static constexpr int THREADS = 192;
+  static constexpr int THREADS = 224;
   static_assert(SMEM <= 232448, "shared memory");
 };
 
@@ -150,14 +153,16 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;        // 1
-  uint64_t* kv_full = bars + 1;   // 2
-  uint64_t* kv_empty = bars + 3;  // 2
-  uint64_t* s_full = bars + 5;    // 2
-  uint64_t* s_free = bars + 7;    // 2
-  uint64_t* p_full = bars + 9;    // 2
-  uint64_t* pv_done = bars + 11;  // 2
-  uint64_t* drain = bars + 13;    // 1, error path only
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  uint64_t* k_full = bars + 1;    // 2
+  uint64_t* k_empty = bars + 3;   // 2
+  uint64_t* v_full = bars + 5;    // 2
+  uint64_t* v_empty = bars + 7;   // 2
+  uint64_t* s_full = bars + 9;    // 2
+  uint64_t* s_free = bars + 11;   // 2
+  uint64_t* p_full = bars + 13;   // 2
+  uint64_t* pv_done = bars + 15;  // 2
+  uint64_t* drain = bars + 17;    // 1, error path only
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = sh.Hq / sh.Hkv;
@@ -175,8 +180,10 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&kv_full[b], 1);
-      mbar_init(&kv_empty[b], 1);
+      mbar_init(&k_full[b], 1);
+      mbar_init(&k_empty[b], 1);
+      mbar_init(&v_full[b], 1);
+      mbar_init(&v_empty[b], 1);
       mbar_init(&s_full[b], 1);
       mbar_init(&s_free[b], 4);
       mbar_init(&p_full[b], 4);
@@ -197,22 +204,27 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   pdl_wait();
 
-  if (warp == 1) {
-    // ---------------- TMA producer
+  if (warp == 1 || warp == 6) {
+    // ---------------- TMA producers: Q and K (warp 1), V (warp 6)
     if (lane == 0) {
+      const bool is_k = warp == 1;
       bool ok = true;
       // one copy per tile: the maps list the 64-dim box index last, so a
       // copy lands as [box][rows][128 B]
-      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-      tma_load_4d(smem, &tmQ, q_full, 0, kvh * G, t0, 0);
+      if (is_k) {
+        mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+        tma_load_4d(smem, &tmQ, q_full, 0, kvh * G, t0, 0);
+      }
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      uint8_t* ring = smem + (is_k ? C::OFF_K : C::OFF_V);
+      const CUtensorMap* map = is_k ? &tmK : &tmV;
       for (int j = 0; j < n && ok; ++j) {
         const int s = j & 1;
-        if (j >= 2) ok = mbar_wait(&kv_empty[s], ((j - 2) >> 1) & 1, err, PF_DEV_TIMEOUT_PRODUCER);
+        if (j >= 2) ok = mbar_wait(&empty[s], ((j - 2) >> 1) & 1, err, PF_DEV_TIMEOUT_PRODUCER);
         if (!ok) break;
-        mbar_arrive_expect_tx(&kv_full[s], 2 * C::KV_BYTES);
-        const int key0 = (ch_first + j) * CHUNK;
-        tma_load_3d(smem + C::OFF_K + s * C::KV_BYTES, &tmK, &kv_full[s], kvh * HD, key0, 0);
-        tma_load_3d(smem + C::OFF_V + s * C::KV_BYTES, &tmV, &kv_full[s], kvh * HD, key0, 0);
+        mbar_arrive_expect_tx(&full[s], C::KV_BYTES);
+        tma_load_3d(ring + s * C::KV_BYTES, map, &full[s], kvh * HD, (ch_first + j) * CHUNK, 0);
       }
     }
     __syncwarp();
@@ -228,7 +240,7 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
       for (int i = 0; i <= n && ok; ++i) {
         if (i < n) {
           const int s = i & 1;
-          ok = mbar_wait(&kv_full[s], (i >> 1) & 1, err, PF_DEV_TIMEOUT_MMA);
+          ok = mbar_wait(&k_full[s], (i >> 1) & 1, err, PF_DEV_TIMEOUT_MMA);
           if (ok && i >= 2) ok = mbar_wait(&s_free[s], ((i - 2) >> 1) & 1, err, PF_DEV_TIMEOUT_MMA);
           if (!ok) break;
           tc_fence_after();
@@ -244,10 +256,12 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
           }
           issued = true;
           tc_commit(&s_full[s]);
+          tc_commit(&k_empty[s]);  // K(i) has been read
         }
         if (i >= 1) {
           const int j = i - 1, s = j & 1;
           ok = mbar_wait(&p_full[s], (j >> 1) & 1, err, PF_DEV_TIMEOUT_MMA);
+          if (ok) ok = mbar_wait(&v_full[s], (j >> 1) & 1, err, PF_DEV_TIMEOUT_MMA);
           if (!ok) break;
           tc_fence_after();
           const uint32_t sp = smem_u32(smem + C::OFF_P + s * C::P_BYTES);
@@ -258,7 +272,7 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
             tc_mma_f16(tmem + C::TMEM_O, pd0 + ((kk * 32) >> 4), vd0 + ((kk * 16 * 128) >> 4), id_pv,
                        (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&pv_done[s]);
-          tc_commit(&kv_empty[s]);
+          tc_commit(&v_empty[s]);
         }
       }
       if (!ok && issued) {
@@ -294,10 +308,17 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
       if (lane == 0) mbar_arrive(&s_free[s]);
       // keys ch*64 + k visible to this row: k < nvis
       const int nvis = pos < 0 ? 0 : min(CHUNK, pos - ch * CHUNK + 1);
-      float mj = -INFINITY;
+      // the chunk's max and sum over eight interleaved partials (fixed
+      // combination order): one thread owns the row, and a 64-long chain
+      // of dependent operations would set the softmax's pace
+      float mx[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) mx[q] = -INFINITY;
 #pragma unroll
       for (int k = 0; k < CHUNK; ++k)
-        if (k < nvis) mj = fmaxf(mj, __uint_as_float(sr[k >> 5][k & 31]));
+        if (k < nvis) mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(sr[k >> 5][k & 31]));
+      const float mj =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       // The running max moves only when this chunk's max passes it by more
       // than 2^8 in the exponent (or on the row's first visible keys): then
       // O and l are rescaled; otherwise P is taken against the old max
@@ -306,7 +327,7 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
       // same softmax either way.
       const bool grow = mj != -INFINITY && (m == -INFINITY || __fmul_rn(__fsub_rn(mj, m), cexp) > 8.f);
       const float mn = grow ? mj : m;
-      float lc = 0.f;
+      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       uint32_t pw[32];  // 64 fp16 probabilities, two per word
 #pragma unroll
       for (int k2 = 0; k2 < 32; ++k2) {
@@ -316,9 +337,10 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
         const float p1 = k + 1 < nvis ? ex2_approx(__fmul_rn(__fsub_rn(s1, mn), cexp)) : 0.f;
         const __half2 h = __floats2half2_rn(p0, p1);
         pw[k2] = *reinterpret_cast<const uint32_t*>(&h);
-        lc = __fadd_rn(lc, __low2float(h));
-        lc = __fadd_rn(lc, __high2float(h));
+        ls[k2 & 7] = __fadd_rn(ls[k2 & 7], __fadd_rn(__low2float(h), __high2float(h)));
       }
+      const float lc = __fadd_rn(__fadd_rn(__fadd_rn(ls[0], ls[1]), __fadd_rn(ls[2], ls[3])),
+                                 __fadd_rn(__fadd_rn(ls[4], ls[5]), __fadd_rn(ls[6], ls[7])));
       const bool resc = grow && m != -INFINITY;  // an earlier max to move away from
       const float scale = resc ? ex2_approx(__fmul_rn(__fsub_rn(m, mn), cexp)) : 1.f;
       l = __fadd_rn(__fmul_rn(l, scale), lc);
