@@ -17,14 +17,16 @@ namespace pf {
 // (tile, k-part) pairs of a weight matrix in the GEMM's tile layout: the
 // tile's BN rows over 32-row groups of lanes, the k-part's 64-wide k-blocks
 // over the remaining warps, plain 16-byte loads of the Q4_0 tiles (or bf16
-// rows), fp32 dot products (a Q4_0 value d*(n-8) is exact in fp32).  Each
-// CTA writes its part's row sums; the last CTA of a tile to finish adds the
-// parts in part order and runs the GEMM's fused epilogue on the tile's one
-// output row.  The bits depend only on the matrix shape and the part count
-// (a function of the shape), not on which CTA finishes last.
+// rows), fp32 dot products (a Q4_0 value d*(n-8) is exact in fp32).  The
+// k-parts of a tile form a thread-block cluster: after a cluster barrier,
+// rank 0 adds the parts' row sums in part order through distributed shared
+// memory and runs the GEMM's fused epilogue on the tile's one output row
+// (no global partials, fences or tickets on the path).  The bits depend
+// only on the matrix shape and the part count (a function of the shape).
 constexpr int GV_WARPS = 8;
 constexpr int GV_THREADS = GV_WARPS * 32;
 constexpr int GV_TARGET_CTAS = 304;  // about two CTAs per SM
+constexpr int GV_MAX_PARTS = 8;      // k-parts of a tile: one cluster, at most the portable cluster size
 
 // Two fp32 lanes in one 64-bit register pair, for the packed arithmetic
 // of sm_100-class SMs (sub.rn.f32x2 / fma.rn.f32x2: one instruction for two
@@ -93,7 +95,6 @@ __device__ __forceinline__ float q4_block_dot(uint4 nib, const float* x) {
 template <int WK, int BN>
 __global__ void __launch_bounds__(GV_THREADS) gemv_kernel(const __nv_bfloat16* __restrict__ a, int K,
                                                           const uint8_t* __restrict__ w, int parts,
-                                                          float* __restrict__ sums, int* __restrict__ tickets,
                                                           const EpiParams ep_in, int* err,
                                                           const float* __restrict__ nx, const float* __restrict__ ng,
                                                           float eps) {
@@ -103,9 +104,9 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_kernel(const __nv_bfloat16* _
   constexpr int TILE = BN * 36;        // bytes of one (tile, k-block) of Q4_0
   extern __shared__ __align__(16) float xs[];  // the row, fp32 [K]; then the weight slice
   __shared__ float part_s[GV_WARPS][32];
-  __shared__ float yv[BN];
+  __shared__ float yp[BN];  // this part's row sums
+  __shared__ float yv[BN];  // the tile's row (rank 0)
   __shared__ EpiParams ep;
-  __shared__ int last;
   __shared__ __align__(8) uint64_t wbar;
   __shared__ __align__(16) uint8_t stage[2][EPI_STAGE_BYTES];
   const int nt = blockIdx.x / parts, kp = blockIdx.x % parts;
@@ -214,21 +215,24 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_kernel(const __nv_bfloat16* _
     const int g = tid >> 5, l = tid & 31;
     float t = part_s[g][l];
     for (int q = 1; q < KW; ++q) t += part_s[q * RG + g][l];
-    sums[((size_t)nt * parts + kp) * BN + tid] = t;
+    yp[tid] = t;
   }
-  // the last CTA of the tile adds the parts in order and runs the epilogue
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) last = atomicAdd(&tickets[nt], 1) == parts - 1;
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  if (tid < BN) {
-    float t = __ldcg(sums + (size_t)nt * parts * BN + tid);
-    for (int q = 1; q < parts; ++q) t += __ldcg(sums + ((size_t)nt * parts + q) * BN + tid);
-    yv[tid] = t;
+  if (parts > 1) {
+    // the cluster's CTAs are the tile's k-parts, rank = part: rank 0 adds
+    // the parts in order once every rank's sums are in its shared memory,
+    // and the others stay until rank 0 has read them
+    cluster_sync_all();
+    if (kp == 0 && tid < BN) {
+      float t = yp[tid];
+      const uint32_t own = smem_u32(&yp[tid]);
+      for (int q = 1; q < parts; ++q) t += ld_cluster_f32(map_to_rank(own, static_cast<uint32_t>(q)));
+      yv[tid] = t;
+    }
+    cluster_sync_all();
+    if (kp != 0) return;
+  } else if (tid < BN) {
+    yv[tid] = yp[tid];
   }
-  if (tid == 0) tickets[nt] = 0;  // ready for the next launch
   __syncthreads();
   if (warp < 2)
     run_epilogue<BN>(ep, 0, 1, nt, warp, stage[warp], 0, [&](int c, float(&v)[32]) {
@@ -241,11 +245,8 @@ int gemv_parts(const WeightMat& W) {
   const int n_tiles = W.N_rows / W.BN, nkb = W.K / 64;
   int p = (GV_TARGET_CTAS + n_tiles - 1) / n_tiles;
   if (p > nkb) p = nkb;
+  if (p > GV_MAX_PARTS) p = GV_MAX_PARTS;
   return p < 1 ? 1 : p;
-}
-
-size_t gemv_scratch_floats(const WeightMat& W) {
-  return static_cast<size_t>(W.N_rows / W.BN) * gemv_parts(W) * W.BN;
 }
 
 // dynamic shared memory of a launch: the row (K floats) and, for Q4_0, the
@@ -259,8 +260,8 @@ static size_t gemv_smem(const WeightMat& W, int parts) {
 constexpr size_t GV_SMEM_MAX = 160 * 1024;
 
 template <int WK, int BN>
-static cudaError_t launch_gemv_t(const ActMat& A, const WeightMat& W, const EpiParams& ep, float* sums, int* tickets,
-                                 int* err, cudaStream_t s, const float* nx, const float* ng, float eps) {
+static cudaError_t launch_gemv_t(const ActMat& A, const WeightMat& W, const EpiParams& ep, int* err, cudaStream_t s,
+                                 const float* nx, const float* ng, float eps) {
   {
     const cudaError_t e = smem_opt_in<gemv_kernel<WK, BN>>(static_cast<int>(GV_SMEM_MAX));
     if (e != cudaSuccess) return e;
@@ -268,18 +269,18 @@ static cudaError_t launch_gemv_t(const ActMat& A, const WeightMat& W, const EpiP
   const int parts = gemv_parts(W);
   const size_t smem = gemv_smem(W, parts);
   if (smem > GV_SMEM_MAX) return cudaErrorInvalidValue;
-  const int grid = (W.N_rows / BN) * parts;
-  return launch_k(gemv_kernel<WK, BN>, dim3(grid), dim3(GV_THREADS), smem, s, 1, A.dev, W.K,
-                  static_cast<const uint8_t*>(W.dev), parts, sums, tickets, ep, err, nx, ng, eps);
+  const int grid = (W.N_rows / BN) * parts;  // clusters of `parts` CTAs: one tile each
+  return launch_k(gemv_kernel<WK, BN>, dim3(grid), dim3(GV_THREADS), smem, s, parts, A.dev, W.K,
+                  static_cast<const uint8_t*>(W.dev), parts, ep, err, nx, ng, eps);
 }
 
-cudaError_t launch_gemv(const ActMat& A, const WeightMat& W, const EpiParams& ep, float* sums, int* tickets,
-                        int* err, cudaStream_t s, const float* norm_x, const float* norm_g, float eps) {
-  if (A.K != W.K || W.K % 64 != 0 || W.N_rows % W.BN != 0 || !sums || !tickets) return cudaErrorInvalidValue;
+cudaError_t launch_gemv(const ActMat& A, const WeightMat& W, const EpiParams& ep, int* err, cudaStream_t s,
+                        const float* norm_x, const float* norm_g, float eps) {
+  if (A.K != W.K || W.K % 64 != 0 || W.N_rows % W.BN != 0) return cudaErrorInvalidValue;
   if (norm_x && (!norm_g || (reinterpret_cast<uintptr_t>(norm_x) | reinterpret_cast<uintptr_t>(norm_g)) % 16 != 0))
     return cudaErrorInvalidValue;
 #define PF_GEMV_CASE(WKV, BNV) \
-  if (W.kind == WKV && W.BN == BNV) return launch_gemv_t<WKV, BNV>(A, W, ep, sums, tickets, err, s, norm_x, norm_g, eps);
+  if (W.kind == WKV && W.BN == BNV) return launch_gemv_t<WKV, BNV>(A, W, ep, err, s, norm_x, norm_g, eps);
   PF_GEMV_CASE(W_Q4, 64)
   PF_GEMV_CASE(W_Q4, 128)
   PF_GEMV_CASE(W_Q4, 192)

@@ -106,18 +106,14 @@ cudaError_t launch_gemm_pair(const ActMat& A, int M, const WeightMat& W, const E
                              cudaStream_t s, int withhold_stage, bool two);
 
 // One row (a one-token ubatch): out = A[0] W^T with the same fused epilogue,
-// streamed by CUDA cores over (tile, k-part) CTAs.  `sums` holds
-// gemv_scratch_floats(W) floats; `tickets` one int per tile, zero before the
-// first launch (each launch leaves them zero).  Launches sharing the
-// scratch must be stream-ordered.  err: device error word (a weight copy
-// that never lands flags it after the bounded wait).  With norm_x (fp32
-// [K], 16-byte aligned) the row is not read from A: it is the RMS norm of
-// norm_x with gain (1 + norm_g) and eps, formed inside the launch and
-// rounded to bf16.
-cudaError_t launch_gemv(const ActMat& A, const WeightMat& W, const EpiParams& ep, float* sums, int* tickets,
-                        int* err, cudaStream_t s, const float* norm_x = nullptr, const float* norm_g = nullptr,
-                        float eps = 0.f);
-size_t gemv_scratch_floats(const WeightMat& W);
+// streamed by CUDA cores over (tile, k-part) CTAs, the k-parts of a tile
+// one thread-block cluster (no scratch memory).  err: device error word (a
+// weight copy that never lands flags it after the bounded wait).  With
+// norm_x (fp32 [K], 16-byte aligned) the row is not read from A: it is the
+// RMS norm of norm_x with gain (1 + norm_g) and eps, formed inside the
+// launch and rounded to bf16.
+cudaError_t launch_gemv(const ActMat& A, const WeightMat& W, const EpiParams& ep, int* err, cudaStream_t s,
+                        const float* norm_x = nullptr, const float* norm_g = nullptr, float eps = 0.f);
 
 // Host repack.  `rows[i]` points at the i-th stored row's source (Q4_0: K/32
 // blocks of 18 bytes; F32: K floats) or is null for a zero padding row.

@@ -163,21 +163,16 @@ extern "C" int pfop_linear_row(int32_t wtype, const void* w_host, int32_t N, int
   e.out_f32 = out_dev;
   e.ld_f32 = N;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float* sums = nullptr;
-  int* tickets = nullptr;
   int* err = nullptr;
-  OP_CUDA(sc.alloc(&sums, gemv_scratch_floats(W) * 4));
-  OP_CUDA(sc.alloc(&tickets, static_cast<size_t>(W.N_rows / W.BN) * 4));
   OP_CUDA(sc.alloc(&err, 16));
-  OP_CUDA(cudaMemsetAsync(tickets, 0, static_cast<size_t>(W.N_rows / W.BN) * 4, s));
   OP_CUDA(cudaMemsetAsync(err, 0, 16, s));
-  OP_CUDA(launch_gemv(A, W, e, sums, tickets, err, s));
+  OP_CUDA(launch_gemv(A, W, e, err, s));
   if (iters > 0) {
     cudaEvent_t e0, e1;
     OP_CUDA(cudaEventCreate(&e0));
     OP_CUDA(cudaEventCreate(&e1));
     OP_CUDA(cudaEventRecord(e0, s));
-    for (int i = 0; i < iters; ++i) OP_CUDA(launch_gemv(A, W, e, sums, tickets, err, s));
+    for (int i = 0; i < iters; ++i) OP_CUDA(launch_gemv(A, W, e, err, s));
     OP_CUDA(cudaEventRecord(e1, s));
     OP_CUDA(cudaEventSynchronize(e1));
     float ms = 0.f;

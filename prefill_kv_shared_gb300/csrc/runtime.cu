@@ -83,8 +83,6 @@ struct prefill_ctx {
   __half* q16 = nullptr;
   float* partials = nullptr;
   float* row_partials = nullptr;  // range states of the single-row attention
-  float* gv_sums = nullptr;       // k-part sums of the one-token projections
-  int* gv_tickets = nullptr;      // per weight tile, zero between launches
   __half* cache = nullptr;  // [2][L_w][max_ctx][kv]
   float2* rope = nullptr;
   int* err = nullptr;
@@ -470,20 +468,6 @@ extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weig
     if ((rc = upload(C, &C->out_norm, w->out_norm, C->D * 4))) return fail(nullptr, rc, C->last_error);
   }
 
-  // scratch of the one-token projections: the largest matrix decides
-  {
-    size_t fl = gemv_scratch_floats(C->head);
-    int tiles = C->head.N_rows / C->head.BN;
-    for (const LayerW& L : C->layers)
-      for (const WeightMat* m : {&L.qkv, &L.o, &L.gu, &L.down, &L.pg, &L.pp}) {
-        if (!m->dev) continue;
-        fl = std::max(fl, gemv_scratch_floats(*m));
-        tiles = std::max(tiles, m->N_rows / m->BN);
-      }
-    if ((rc = dev_alloc(C, &C->gv_sums, fl * 4)) || (rc = dev_alloc(C, &C->gv_tickets, tiles * 4)))
-      return fail(nullptr, rc, C->last_error);
-  }
-
   // buffers
   const size_t R = C->rows_alloc;
   if ((rc = dev_alloc(C, &C->tok, R * 4)) || (rc = dev_alloc(C, &C->x, R * C->D * 4)) ||
@@ -720,7 +704,7 @@ int run_ubatch(prefill_ctx* c, const int32_t* tokens, int T, std::vector<Run>& r
     const EpiParams e1 = shift_rows(e, rows - 1);
     const float* nx = norm_src ? norm_src + static_cast<size_t>(rows - 1) * D : nullptr;
     return counted(c, PF_KC_GEMM_ROW, 1, flops_row, wbytes + io_row, [&] {
-      return launch_gemv(a1, Wm, e1, c->gv_sums, c->gv_tickets, c->err, s, nx, norm_gain, c->d.rms_eps);
+      return launch_gemv(a1, Wm, e1, c->err, s, nx, norm_gain, c->d.rms_eps);
     });
   };
   // the single-row attention of one output row
@@ -925,7 +909,7 @@ int run_ubatch(prefill_ctx* c, const int32_t* tokens, int T, std::vector<Run>& r
     e.out_f32 = logits;
     e.ld_f32 = c->V;
     PF_CUDA(c, counted(c, gemm_class(1), 1, 2.0 * c->V * D, D * 4.0 + gemm_wbytes(c, c->V, D) + c->V * 4.0, [&] {
-      return launch_gemv(c->a_y, c->head, e, c->gv_sums, c->gv_tickets, c->err, s, xrow, c->out_norm, c->d.rms_eps);
+      return launch_gemv(c->a_y, c->head, e, c->err, s, xrow, c->out_norm, c->d.rms_eps);
     }));
   } else if (is_last) {
     // one logits row per finishing sequence, in run order: their rows are
