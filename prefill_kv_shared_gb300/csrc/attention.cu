@@ -29,13 +29,13 @@
 // ubatch.
 //
 // CTA roles: warp 1 lane 0 issues the TMA copies of Q (once) and of K, warp
-// 6 lane 0 those of V (K and V each double-buffered, on separate barriers:
-// a K buffer is free again once S = Q K^T has read it, a V buffer once P V
-// has, so the next K copies start a whole softmax earlier than with one
-// shared buffer); warp 0 allocates TMEM and its lane 0 issues the MMAs;
-// warps 2..5 own the 128 rows (thread = TMEM lane = row): softmax, the P tile
-// (fp16, 128-byte-swizzled K-major: the A operand of P V), the O rescale and
-// the output.  The MMA thread issues S(j+1) = Q K(j+1)^T before P(j) V(j), so
+// 6 lane 0 those of V (K on a 3-stage ring, V double-buffered, on separate
+// barriers: a K buffer is free again once S = Q K^T has read it, a V buffer
+// once P V has); warp 0 allocates TMEM and its lane 0 issues the MMAs;
+// warps 2..5 own the 128 rows (thread = TMEM lane = row): softmax, the P
+// tile (fp16, written to TMEM next to O: the A operand of P V comes from
+// TMEM, which leaves the shared memory of a P tile to the K ring), the O
+// rescale and the output.  The MMA thread issues S(j+1) = Q K(j+1)^T before P(j) V(j), so
 // the tensor cores work while the row warps run the softmax of chunk j.  All
 // waits are bounded (PF_WAIT_CYCLES); a timed-out wait flags the error word
 // and the CTA unwinds.
@@ -81,15 +81,16 @@ struct AttnTcCfg {
   static constexpr int NB = HD / 64;               // 64-dim (128-byte) boxes per row
   static constexpr int Q_BYTES = 128 * HD * 2;      // [box][128 rows][128 B]
   static constexpr int KV_BYTES = CHUNK * HD * 2;   // one K or V chunk: [box][64 keys][128 B]
-  static constexpr int P_BYTES = 128 * CHUNK * 2;   // [128 rows][64 keys fp16]
+  static constexpr int NK = 3;                      // K ring stages (V: 2)
   static constexpr int OFF_K = Q_BYTES;
-  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + barriers, + alignment slack
   static constexpr int TMEM_S = 0;                  // two S buffers of 64 columns
   static constexpr int TMEM_O = 2 * CHUNK;          // O: HD columns
-  static constexpr int TMEM_COLS = (TMEM_O + HD) <= 256 ? 256 : 512;
+  static constexpr int TMEM_P = TMEM_O + HD;        // two P buffers of 32 columns (64 fp16 a row)
+  static constexpr int TMEM_COLS = (TMEM_P + CHUNK) <= 256 ? 256 : 512;
+  static_assert(TMEM_P + CHUNK <= 512, "TMEM");
   static constexpr int THREADS = 224;
   static_assert(SMEM <= 232448, "shared memory");
 };
@@ -105,6 +106,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128_lbo_sbo(uint32_t saddr, uint32_t
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
   return d;
+}
+
+// D[tmem] (+)= A[tmem] * B[smem] (kind::f16), A in TMEM: its rows are the
+// TMEM lanes, two 16-bit elements of a row per 32-bit column (the lower k
+// in the low half), K = 16 per instruction (8 columns)
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 // kind::f16 instruction descriptor, fp16 A and B, fp32 accumulator; b_mn:
@@ -153,16 +167,17 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;        // 1
-  uint64_t* k_full = bars + 1;    // 2
-  uint64_t* k_empty = bars + 3;   // 2
-  uint64_t* v_full = bars + 5;    // 2
-  uint64_t* v_empty = bars + 7;   // 2
-  uint64_t* s_full = bars + 9;    // 2
-  uint64_t* s_free = bars + 11;   // 2
-  uint64_t* p_full = bars + 13;   // 2
-  uint64_t* pv_done = bars + 15;  // 2
-  uint64_t* drain = bars + 17;    // 1, error path only
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+  uint64_t* k_full = bars + 1;    // NK
+  uint64_t* k_empty = bars + 4;   // NK
+  uint64_t* v_full = bars + 7;    // 2
+  uint64_t* v_empty = bars + 9;   // 2
+  uint64_t* s_full = bars + 11;   // 2
+  uint64_t* s_free = bars + 13;   // 2
+  uint64_t* p_full = bars + 15;   // 2
+  uint64_t* pv_done = bars + 17;  // 2
+  uint64_t* drain = bars + 19;    // 1, error path only
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+  static_assert(C::NK == 3, "barrier layout");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = sh.Hq / sh.Hkv;
@@ -179,9 +194,11 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::NK; ++b) {
       mbar_init(&k_full[b], 1);
       mbar_init(&k_empty[b], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&v_full[b], 1);
       mbar_init(&v_empty[b], 1);
       mbar_init(&s_full[b], 1);
@@ -219,9 +236,10 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
       uint64_t* empty = is_k ? k_empty : v_empty;
       uint8_t* ring = smem + (is_k ? C::OFF_K : C::OFF_V);
       const CUtensorMap* map = is_k ? &tmK : &tmV;
+      const int ns = is_k ? C::NK : 2;  // ring stages
       for (int j = 0; j < n && ok; ++j) {
-        const int s = j & 1;
-        if (j >= 2) ok = mbar_wait(&empty[s], ((j - 2) >> 1) & 1, err, PF_DEV_TIMEOUT_PRODUCER);
+        const int s = j % ns;
+        if (j >= ns) ok = mbar_wait(&empty[s], ((j - ns) / ns) & 1, err, PF_DEV_TIMEOUT_PRODUCER);
         if (!ok) break;
         mbar_arrive_expect_tx(&full[s], C::KV_BYTES);
         tma_load_3d(ring + s * C::KV_BYTES, map, &full[s], kvh * HD, (ch_first + j) * CHUNK, 0);
@@ -239,12 +257,12 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
       // step i: S(i) = Q K(i)^T (if i < n), then O (+)= P(i-1) V(i-1)
       for (int i = 0; i <= n && ok; ++i) {
         if (i < n) {
-          const int s = i & 1;
-          ok = mbar_wait(&k_full[s], (i >> 1) & 1, err, PF_DEV_TIMEOUT_MMA);
+          const int s = i & 1, sk_i = i % C::NK;
+          ok = mbar_wait(&k_full[sk_i], (i / C::NK) & 1, err, PF_DEV_TIMEOUT_MMA);
           if (ok && i >= 2) ok = mbar_wait(&s_free[s], ((i - 2) >> 1) & 1, err, PF_DEV_TIMEOUT_MMA);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t sk = smem_u32(smem + C::OFF_K + s * C::KV_BYTES);
+          const uint32_t sk = smem_u32(smem + C::OFF_K + sk_i * C::KV_BYTES);
           // descriptors built once per tile, constant offsets per step (the
           // address field holds any shared-memory address: no carry)
           const uint64_t qd0 = sdesc_sw128(sq), kd0 = sdesc_sw128(sk);
@@ -256,7 +274,7 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
           }
           issued = true;
           tc_commit(&s_full[s]);
-          tc_commit(&k_empty[s]);  // K(i) has been read
+          tc_commit(&k_empty[sk_i]);  // K(i) has been read
         }
         if (i >= 1) {
           const int j = i - 1, s = j & 1;
@@ -264,13 +282,12 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
           if (ok) ok = mbar_wait(&v_full[s], (j >> 1) & 1, err, PF_DEV_TIMEOUT_MMA);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t sp = smem_u32(smem + C::OFF_P + s * C::P_BYTES);
           const uint32_t sv = smem_u32(smem + C::OFF_V + s * C::KV_BYTES);
-          const uint64_t pd0 = sdesc_sw128(sp), vd0 = sdesc_sw128_lbo_sbo(sv, CHUNK * 128, 1024);
+          const uint64_t vd0 = sdesc_sw128_lbo_sbo(sv, CHUNK * 128, 1024);
 #pragma unroll
-          for (int kk = 0; kk < CHUNK / 16; ++kk)  // 16 keys a step
-            tc_mma_f16(tmem + C::TMEM_O, pd0 + ((kk * 32) >> 4), vd0 + ((kk * 16 * 128) >> 4), id_pv,
-                       (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < CHUNK / 16; ++kk)  // 16 keys a step: 8 TMEM columns of P
+            tc_mma_f16_ts(tmem + C::TMEM_O, tmem + C::TMEM_P + s * (CHUNK / 2) + kk * 8,
+                          vd0 + ((kk * 16 * 128) >> 4), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&pv_done[s]);
           tc_commit(&v_empty[s]);
         }
@@ -351,12 +368,8 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
       }
-      uint8_t* prow = smem + C::OFF_P + s * C::P_BYTES + r * 128;
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<uint4*>(prow + ((q ^ (r & 7)) << 4)) =
-            make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
-      fence_proxy_async_smem();
+      tmem_st32(tmem + lane_base + C::TMEM_P + s * (CHUNK / 2), pw);
+      tmem_st_wait();
       // O *= scale once P V(j-1) has landed (chunk 0 overwrites O), only in
       // the warps where a row moved its max.  (Skipping the wait elsewhere is
       // safe: P V(j+1) cannot complete before P(j+1) is written, so the next
@@ -388,7 +401,7 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
     }
     if (ok) {
       // Each 32 x 32 block of O goes through a warp-private staging buffer
-      // in the (now idle) P tiles, so that the global stores cover whole row
+      // in the (now idle) K ring, so that the global stores cover whole row
       // segments: lane l stores rows 4i + l/8, columns 4(l%8) .. +3.
       tc_fence_after();
       // this lane's row: 0 = nothing to write, 1 = output row, 2 = group state
@@ -410,7 +423,7 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
         const uint32_t hi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(own_off >> 32), rr);
         dst_off[i] = (static_cast<size_t>(hi) << 32) | lo;
       }
-      uint8_t* stg = smem + C::OFF_P + qw * 4096;
+      uint8_t* stg = smem + C::OFF_K + qw * 4096;
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t x[32];
