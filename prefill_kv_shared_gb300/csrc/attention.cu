@@ -247,12 +247,17 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
     }
     __syncwarp();
   } else if (warp == 0) {
-    // ---------------- MMA issue
-    if (lane == 0) {
+    // ---------------- MMA issue: the whole warp runs the loop in step
+    // (waits and decisions warp-uniform), one lane elected once issues the
+    // MMAs and commits (its commits track the MMAs it issued); an issue
+    // from a lone lane's divergent loop costs several times as much
+    {
+      const bool leader = elect_one();
       constexpr uint32_t id_qk = idesc_f16_f32(128, CHUNK, false);
       constexpr uint32_t id_pv = idesc_f16_f32(128, HD, true);
       const uint32_t sq = smem_u32(smem);
       bool ok = mbar_wait(q_full, 0, err, PF_DEV_TIMEOUT_MMA);
+      ok = __all_sync(0xffffffffu, ok);
       bool issued = false;
       // step i: S(i) = Q K(i)^T (if i < n), then O (+)= P(i-1) V(i-1)
       for (int i = 0; i <= n && ok; ++i) {
@@ -260,39 +265,47 @@ __global__ void __launch_bounds__(AttnTcCfg<HD>::THREADS, 1)
           const int s = i & 1, sk_i = i % C::NK;
           ok = mbar_wait(&k_full[sk_i], (i / C::NK) & 1, err, PF_DEV_TIMEOUT_MMA);
           if (ok && i >= 2) ok = mbar_wait(&s_free[s], ((i - 2) >> 1) & 1, err, PF_DEV_TIMEOUT_MMA);
+          ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after();
           const uint32_t sk = smem_u32(smem + C::OFF_K + sk_i * C::KV_BYTES);
           // descriptors built once per tile, constant offsets per step (the
           // address field holds any shared-memory address: no carry)
           const uint64_t qd0 = sdesc_sw128(sq), kd0 = sdesc_sw128(sk);
+          if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            const int b = kk >> 2, w = kk & 3;  // 64-dim box, 16-dim step within it
-            tc_mma_f16(tmem + C::TMEM_S + s * CHUNK, qd0 + ((b * (128 * 128) + w * 32) >> 4),
-                       kd0 + ((b * (CHUNK * 128) + w * 32) >> 4), id_qk, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < HD / 16; ++kk) {
+              const int b = kk >> 2, w = kk & 3;  // 64-dim box, 16-dim step within it
+              tc_mma_f16(tmem + C::TMEM_S + s * CHUNK, qd0 + ((b * (128 * 128) + w * 32) >> 4),
+                         kd0 + ((b * (CHUNK * 128) + w * 32) >> 4), id_qk, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(&s_full[s]);
+            tc_commit(&k_empty[sk_i]);  // K(i) has been read
           }
+          __syncwarp();
           issued = true;
-          tc_commit(&s_full[s]);
-          tc_commit(&k_empty[sk_i]);  // K(i) has been read
         }
         if (i >= 1) {
           const int j = i - 1, s = j & 1;
           ok = mbar_wait(&p_full[s], (j >> 1) & 1, err, PF_DEV_TIMEOUT_MMA);
           if (ok) ok = mbar_wait(&v_full[s], (j >> 1) & 1, err, PF_DEV_TIMEOUT_MMA);
+          ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after();
           const uint32_t sv = smem_u32(smem + C::OFF_V + s * C::KV_BYTES);
           const uint64_t vd0 = sdesc_sw128_lbo_sbo(sv, CHUNK * 128, 1024);
+          if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < CHUNK / 16; ++kk)  // 16 keys a step: 8 TMEM columns of P
-            tc_mma_f16_ts(tmem + C::TMEM_O, tmem + C::TMEM_P + s * (CHUNK / 2) + kk * 8,
-                          vd0 + ((kk * 16 * 128) >> 4), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(&pv_done[s]);
-          tc_commit(&v_empty[s]);
+            for (int kk = 0; kk < CHUNK / 16; ++kk)  // 16 keys a step: 8 TMEM columns of P
+              tc_mma_f16_ts(tmem + C::TMEM_O, tmem + C::TMEM_P + s * (CHUNK / 2) + kk * 8,
+                            vd0 + ((kk * 16 * 128) >> 4), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(&pv_done[s]);
+            tc_commit(&v_empty[s]);
+          }
+          __syncwarp();
         }
       }
-      if (!ok && issued) {
+      if (!ok && issued && leader) {
         // the MMAs already issued finish before TMEM is freed
         tc_commit(drain);
         attn_drain(drain);
