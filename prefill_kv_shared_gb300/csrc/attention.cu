@@ -6,8 +6,9 @@
 // the K/V tiles.  A CTA takes 128 rows (128/G queries) of one KV head.
 //
 // Keys are cut into absolute 64-key chunks, and the chunks into groups of gc
-// consecutive chunks, gc fixed by the launch's key count (attn_group_chunks:
-// at most ATTN_MAX_GROUPS groups).  A CTA handles one
+// consecutive chunks, gc fixed by the launch's key count and its number of
+// row blocks (attn_group_chunks: at most ATTN_MAX_GROUPS groups, as many as
+// keep the launch to one wave, at least ATTN_GC_MIN chunks a group).  A CTA handles one
 // (128-row block, group) pair and runs the online softmax over the group's
 // chunks in ascending order:
 //     S = Q K^T (tcgen05.mma, TMEM), m' = max(m, max_k s_k),
@@ -59,11 +60,32 @@ __device__ __forceinline__ float ex2_approx(float x) {
 constexpr int ATTN_MAX_GROUPS = 4;
 __host__ __device__ constexpr int attn_part_stride(int hd) { return hd + 4; }
 
-int attn_group_chunks(int kv_len) {
-  const int n_chunks = (kv_len + CHUNK - 1) / CHUNK;
-  const int gc = (n_chunks + ATTN_MAX_GROUPS - 1) / ATTN_MAX_GROUPS;
-  return gc < 1 ? 1 : gc;
+// A group holds at least this many chunks: a group's partial state and its
+// merge cost more than a short chain of chunks (E2B, 512 rows over 512 keys:
+// two groups of four chunks 21.0 us, four groups of two 22.3 us).
+constexpr int ATTN_GC_MIN = 4;
+
+static int attn_sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
 }
+
+int attn_group_chunks(int kv_len, int row_ctas) {
+  const int n_chunks = (kv_len + CHUNK - 1) / CHUNK;
+  // as many groups as keep the launch to one wave of CTAs (E4B, 1024 rows
+  // over 1024 keys: 128 CTAs in two groups 26.9 us, 256 in four 36.0 us)
+  int groups = ATTN_MAX_GROUPS;
+  const int sms = attn_sm_count();
+  while (groups > 1 && row_ctas * groups > sms) --groups;
+  int gc = (n_chunks + groups - 1) / groups;
+  if (gc < ATTN_GC_MIN) gc = ATTN_GC_MIN;
+  return gc;
+}
+
+// CTAs over (128-row block, KV head) of a prefill launch
+static int attn_row_ctas(const AttnArgs& a) { return (a.M * (a.Hq / a.Hkv) + 127) / 128 * a.Hkv; }
 
 // groups that hold keys of the row at position pos
 __host__ __device__ __forceinline__ int attn_row_groups(int pos, int gc) { return (pos / CHUNK) / gc + 1; }
@@ -584,7 +606,7 @@ static cudaError_t launch_tc_t(const AttnArgs& a, float* part, cudaStream_t s) {
   sh.Hq = a.Hq;
   sh.Hkv = a.Hkv;
   sh.pos_base = a.pos_base;
-  sh.gc = attn_group_chunks(a.kv_len);
+  sh.gc = attn_group_chunks(a.kv_len, attn_row_ctas(a));
   const int last_pos = a.pos_base + a.M - 1;
   const int n_groups = attn_row_groups(last_pos, sh.gc);
   if (n_groups > 1 && !part) return cudaErrorInvalidValue;
@@ -1100,14 +1122,13 @@ cudaError_t launch_attn_split(const AttnArgs& a, float* partials, cudaStream_t s
 
 int attn_launch_count(const AttnArgs& a) {
   if (a.M <= 0) return 0;
-  return attn_row_groups(a.pos_base + a.M - 1, attn_group_chunks(a.kv_len)) > 1 ? 2
-                                                                                                         : 1;
+  return attn_row_groups(a.pos_base + a.M - 1, attn_group_chunks(a.kv_len, attn_row_ctas(a))) > 1 ? 2 : 1;
 }
 
 size_t attn_partials_floats(int M, int Hq, int hd, int kv_len) {
-  const int gc = attn_group_chunks(kv_len > 0 ? kv_len : 1);
-  const int n_groups = attn_row_groups(kv_len > 0 ? kv_len - 1 : 0, gc);
-  if (n_groups <= 1) return 0;
+  // a launch of up to M rows over up to kv_len keys: several groups are
+  // possible once the keys need more than one group of the minimum size
+  if (kv_len <= CHUNK * ATTN_GC_MIN) return 0;
   return static_cast<size_t>(M > 0 ? M : 0) * Hq * ATTN_MAX_GROUPS * attn_part_stride(hd);
 }
 

@@ -148,7 +148,7 @@ cudaError_t launch_attn_split(const AttnArgs& a, float* partials, cudaStream_t s
 size_t attn_partials_floats(int M, int Hq, int hd, int kv_len);
 size_t attn_split_partials_floats(int Hq, int Hkv, int hd, int pos);
 size_t attn_split_ticket_bytes(int Hkv);
-int attn_group_chunks(int kv_len);
+int attn_group_chunks(int kv_len, int row_ctas);  // row_ctas: (128-row block, KV head) pairs
 int attn_launch_count(const AttnArgs& a);  // kernels launch_attn_prefill starts (1 or 2)
 
 // ---------------------------------------------------------------------------
