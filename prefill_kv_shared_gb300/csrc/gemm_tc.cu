@@ -1,7 +1,8 @@
 // Host side of the tensor-core GEMM (the kernel and its configurations are
 // in gemm_tc.cuh): tensor maps, the k-split and CTA-pair choices, the QKV
-// tile order, launch dispatch for single CTAs (CTA pairs in gemm_pair.cu),
-// and the host repack of weights into tile order.
+// tile order, launch dispatch for single CTAs (one-unit launches in
+// gemm_solo.cu, CTA pairs in gemm_pair.cu), and the host repack of weights
+// into tile order.
 #include "gemm_tc.cuh"
 
 namespace pf {
@@ -173,6 +174,14 @@ cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiPar
     if (W.kind != W_Q4 || W.split != 1) return cudaErrorInvalidValue;
     const int units_pair = (W.N_rows / W.BN) * ((M + 255) / 256);
     return launch_gemm_pair(A, M, W, ep, err, s, withhold_stage, M > 256 && units_pair > sm_count() / 2);
+  }
+  if (W.kind == W_Q4) {
+    // one work unit per CTA: the epilogue stages in the B ring, and the A
+    // ring gets the room (gemm_solo.cu)
+    const int unit_rows = two ? 256 : 128;
+    const int units = (W.N_rows / W.BN) * ((M + unit_rows - 1) / unit_rows) * W.split;
+    if (units <= sm_count() && gemm_solo_fits(W.BN, two, W.split))
+      return launch_gemm_solo(A, M, W, ep, err, s, withhold_stage, two);
   }
 #define PF_GEMM_CASE(WKV, BNV)                                                        \
   if (W.kind == WKV && W.BN == BNV)                                                   \

@@ -80,10 +80,16 @@ constexpr int SMEM_LIMIT = 232448;
 
 __host__ __device__ constexpr int pow2_cols(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
 
-template <int WK, int BN, int MT, bool PAIR = false>
+// SOLO: a launch whose CTAs take one work unit each.  The epilogue then
+// stages in the dequantised-B ring, idle once the unit's last MMA has
+// completed, instead of a dedicated area, and the 32 KB go to the A ring
+// (one more A stage: the A operand's latency against the ring's depth paces
+// the main loop).
+template <int WK, int BN, int MT, bool PAIR = false, bool SOLO = false>
 struct GemmCfg {
   static constexpr bool Q4 = WK == W_Q4;
   static_assert(!PAIR || Q4, "CTA pairs take Q4_0 weights");
+  static_assert(!SOLO || (Q4 && !PAIR), "one-unit launches: Q4_0 weights on single CTAs");
   static constexpr int BNL = PAIR ? BN / 2 : BN;  // weight rows this CTA stages
   static constexpr int MMA_M = PAIR ? 256 : 128;  // rows of one MMA (over both CTAs of a pair)
   static constexpr int ROWS = MT * MMA_M;         // rows of A in one work unit
@@ -112,7 +118,9 @@ struct GemmCfg {
   static constexpr int NB = S_B > 0 ? S_B : 1;  // ring moduli (the rings are unused without Q4)
   static constexpr int NR = S_R > 0 ? S_R : 1;
   static constexpr int RAW_RING = (S_R * RAW_BYTES + 1023) / 1024 * 1024;
-  static constexpr int EPI_BYTES = EPI_WARPS * 32 * 32 * 4;  // one 4 KB staging buffer per epilogue warp
+  static constexpr int EPI_STAGING = EPI_WARPS * 32 * 32 * 4;  // one 4 KB staging buffer per epilogue warp
+  static constexpr int EPI_BYTES = SOLO ? 0 : EPI_STAGING;      // (SOLO: in the B ring)
+  static_assert(!SOLO || S_B * BT_BYTES >= EPI_STAGING, "the B ring holds the epilogue staging");
   static constexpr int FIXED = S_B * BT_BYTES + RAW_RING + EPI_BYTES + 1024 + 512;
   static constexpr int S_A_FIT = (SMEM_LIMIT - FIXED) / A_STAGE;
   static constexpr int S_A = S_A_FIT > 8 ? 8 : S_A_FIT;
@@ -210,12 +218,12 @@ __device__ __forceinline__ uint32_t slot_off(int c, int r, int q) {
   return static_cast<uint32_t>(((c * 128 + r) << 7) + ((q ^ (r & 7)) << 4));
 }
 
-template <int WK, int BN, int MT, bool PAIR>
+template <int WK, int BN, int MT, bool PAIR, bool SOLO>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB, const uint8_t* __restrict__ wq4, const GemmShape sh_in,
                    const EpiParams ep_in, int* err) {
-  using C = GemmCfg<WK, BN, MT, PAIR>;
+  using C = GemmCfg<WK, BN, MT, PAIR, SOLO>;
   // The launch parameters are read from shared-memory copies: fields of a
   // kernel parameter used through a reference are re-read from parameter
   // memory inside the loops, and a local copy of a struct this size lands in
@@ -234,8 +242,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint8_t* a_ring = smem;
   uint8_t* b_ring = a_ring + C::S_A * C::A_STAGE;
   uint8_t* r_ring = b_ring + C::S_B * C::BT_BYTES;
-  uint8_t* epi_stage = r_ring + C::RAW_RING;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + C::EPI_BYTES);
+  // one-unit launches stage the epilogue in the B ring: every MMA that read
+  // it has completed (tfull) before the epilogue writes there, and no
+  // dequant follows the unit's last stage
+  uint8_t* epi_stage = SOLO ? b_ring : r_ring + C::RAW_RING;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(r_ring + C::RAW_RING + C::EPI_BYTES);
   uint64_t* full_a = bars;
   uint64_t* empty_a = full_a + C::S_A;
   uint64_t* full_r = empty_a + C::S_A;
@@ -731,9 +742,9 @@ inline int sm_count() {
   return n > 0 ? n : 148;
 }
 
-template <int WK, int BN, int MT, bool PAIR = false>
+template <int WK, int BN, int MT, bool PAIR = false, bool SOLO = false>
 inline size_t ring_bytes() {
-  using C = GemmCfg<WK, BN, MT, PAIR>;
+  using C = GemmCfg<WK, BN, MT, PAIR, SOLO>;
   return static_cast<size_t>(C::S_A) * C::A_STAGE + static_cast<size_t>(C::S_B) * C::BT_BYTES + C::RAW_RING;
 }
 
@@ -769,12 +780,12 @@ inline int max_pairs(int smem_bytes) {
   return n_pairs[dev];
 }
 
-template <int WK, int BN, int MT, bool PAIR>
+template <int WK, int BN, int MT, bool PAIR, bool SOLO = false>
 inline cudaError_t launch_t(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err,
                             cudaStream_t s, int withhold_stage) {
-  using C = GemmCfg<WK, BN, MT, PAIR>;
+  using C = GemmCfg<WK, BN, MT, PAIR, SOLO>;
   {
-    const cudaError_t e = smem_opt_in<gemm_tc_kernel<WK, BN, MT, PAIR>>(C::SMEM_BYTES);
+    const cudaError_t e = smem_opt_in<gemm_tc_kernel<WK, BN, MT, PAIR, SOLO>>(C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
   }
   if (PAIR && W.split != 1) return cudaErrorInvalidValue;
@@ -792,11 +803,16 @@ inline cudaError_t launch_t(const ActMat& A, int M, const WeightMat& W, const Ep
   const bool small = !PAIR && MT == 1 && M <= 16;
   sh.a_box_rows = small ? 16 : 128;
   sh.withhold_stage = withhold_stage;
-  if (W.split > 1 && static_cast<size_t>(W.split - 1) * 128 * BN * 4 > ring_bytes<WK, BN, MT, PAIR>())
+  if (W.split > 1 && static_cast<size_t>(W.split - 1) * 128 * BN * 4 > ring_bytes<WK, BN, MT, PAIR, SOLO>())
+    return cudaErrorInvalidValue;
+  // one-unit launches: the split partials (A ring) must not reach the
+  // epilogue staging (B ring), and every CTA takes one unit
+  if (SOLO && (static_cast<size_t>(W.split - 1) * 128 * BN * 4 > static_cast<size_t>(C::S_A) * C::A_STAGE ||
+               sh.n_units > (W.split > 1 ? sh.n_units : sm_count())))
     return cudaErrorInvalidValue;
   int cluster = 1, grid = 0;
   if (PAIR) {  // persistent 2-CTA clusters, as many as fit at once
-    const int pairs = max_pairs<gemm_tc_kernel<WK, BN, MT, PAIR>>(C::SMEM_BYTES);
+    const int pairs = max_pairs<gemm_tc_kernel<WK, BN, MT, PAIR, SOLO>>(C::SMEM_BYTES);
     cluster = 2;
     grid = 2 * (sh.n_units < pairs ? sh.n_units : pairs);
   } else if (W.split > 1) {
@@ -805,7 +821,7 @@ inline cudaError_t launch_t(const ActMat& A, int M, const WeightMat& W, const Ep
   } else {
     grid = sh.n_units < sm_count() ? sh.n_units : sm_count();
   }
-  return launch_k(gemm_tc_kernel<WK, BN, MT, PAIR>, dim3(grid), dim3(GEMM_THREADS), C::SMEM_BYTES, s, cluster,
+  return launch_k(gemm_tc_kernel<WK, BN, MT, PAIR, SOLO>, dim3(grid), dim3(GEMM_THREADS), C::SMEM_BYTES, s, cluster,
                   small ? A.tmap_small : A.tmap, A.tmap_wide, W.tmap, static_cast<const uint8_t*>(W.dev), sh, ep,
                   err);
 }

@@ -100,6 +100,13 @@ std::vector<const void*> qkv_tile_rows(const void* wq, const void* wk, const voi
 // CTA 0's copy producer issues nothing from that pipeline stage on.
 cudaError_t launch_gemm(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err_word,
                         cudaStream_t s, int withhold_stage = -1);
+// the one-unit launches of launch_gemm (Q4_0, every CTA one work unit);
+// two: two 128-row M tiles per unit
+cudaError_t launch_gemm_solo(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err_word,
+                             cudaStream_t s, int withhold_stage, bool two);
+// whether a split's partial tiles fit the one-unit form's A ring (they must
+// stay clear of its epilogue staging in the B ring)
+bool gemm_solo_fits(int BN, bool two, int split);
 // the CTA-pair launches of launch_gemm (W.pair set); two: two 256-row MMA
 // tiles per pair
 cudaError_t launch_gemm_pair(const ActMat& A, int M, const WeightMat& W, const EpiParams& ep, int* err_word,
