@@ -68,6 +68,9 @@ constexpr int GEMM_THREADS = GEMM_WARPS * 32;
 constexpr int EPI_WARP0 = 4;  // warps 4..11: epilogue, two per TMEM lane quarter
 constexpr int EPI_WARPS = 8;
 constexpr int DQ_THREADS = 192;  // warps 2, 3, 12..15: Q4_0 dequant
+// one-unit launches: the eight epilogue warps dequantise too until the
+// unit's last stage (their epilogue cannot start before it)
+constexpr int DQ_THREADS_SOLO = DQ_THREADS + 256;
 constexpr int EPI_REGS = 176;
 constexpr int LEAN_REGS = 80;
 static_assert(2 * 128 * (EPI_REGS + LEAN_REGS) <= GEMM_THREADS * 128, "register split exceeds the launch's registers");
@@ -281,10 +284,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int s = 0; s < C::S_R; ++s) {
       mbar_init(&full_r[s], 1);
-      mbar_init(&empty_r[s], DQ_THREADS / 32);
+      mbar_init(&empty_r[s], (SOLO ? DQ_THREADS_SOLO : DQ_THREADS) / 32);
     }
     for (int s = 0; s < C::S_B; ++s) {
-      mbar_init(&bfull[s], peers * (DQ_THREADS / 32));
+      mbar_init(&bfull[s], peers * ((SOLO ? DQ_THREADS_SOLO : DQ_THREADS) / 32));
       mbar_init(&bempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -323,10 +326,62 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int rows = sh.M - mb * 128 < 128 ? sh.M - mb * 128 : 128;
     split_chunk_bytes = static_cast<uint32_t>(rows) * 128u;
   }
+  // Q4_0 -> bf16 over every stage of this CTA's units, by `nthreads` threads
+  // (t = this thread's index among them), each warp arriving on the ring
+  // barriers once per stage
+  constexpr int DQ_THREADS_ALL = SOLO ? DQ_THREADS_SOLO : DQ_THREADS;
+  auto dequant_loop = [&](const int t, const int nthreads) {
+    uint32_t g = 0;
+    bool ok = true;
+    const int nst = (nkb + C::KS - 1) / C::KS;
+    for (int u = unit0; u < sh.n_units && ok; u += ustep) {
+      for (int i = 0; i < nst; ++i, ++g) {
+        const int kc = nkb - i * C::KS < C::KS ? nkb - i * C::KS : C::KS;
+        const int sr = g % C::NR, sb = g % C::NB;
+        bool w_ok = mbar_wait(&full_r[sr], (g / C::NR) & 1, err, PF_DEV_TIMEOUT_DEQUANT);
+        if (w_ok) w_ok = mbar_wait(&bempty[sb], ((g / C::NB) & 1) ^ 1, err, PF_DEV_TIMEOUT_DEQUANT);
+        ok = __all_sync(0xffffffffu, w_ok);
+        if (!ok) break;
+        uint8_t* bt = b_ring + sb * C::BT_BYTES;
+        const uint8_t* raw = r_ring + sr * C::RAW_BYTES;
+        // items: (k-block j, half h, row rr); a thread takes two at a time
+        // so that their shared-memory loads overlap
+        constexpr int R = C::BNL;  // weight rows staged by this CTA
+        const int items = kc * R * 2;
+        for (int it = t; it < items; it += 2 * nthreads) {
+          const int it2 = it + nthreads;
+          const int j = it / (R * 2), rr = it % R, h = (it / R) & 1;
+          const uint8_t* rj = raw + j * C::RAW_KB;
+          const uint4 nib = *reinterpret_cast<const uint4*>(rj + (size_t)(h * R + rr) * 16);
+          const __half d = *reinterpret_cast<const __half*>(rj + R * 32 + (h * R + rr) * 2);
+          if (it2 < items) {
+            const int j2 = it2 / (R * 2), rr2 = it2 % R, h2 = (it2 / R) & 1;
+            const uint8_t* rj2 = raw + j2 * C::RAW_KB;
+            const uint4 nib2 = *reinterpret_cast<const uint4*>(rj2 + (size_t)(h2 * R + rr2) * 16);
+            const __half d2 = *reinterpret_cast<const __half*>(rj2 + R * 32 + (h2 * R + rr2) * 2);
+            dequant_block32(nib, d, bt + j * C::BT_KB + rr * 128, h, rr & 7);
+            dequant_block32(nib2, d2, bt + j2 * C::BT_KB + rr2 * 128, h2, rr2 & 7);
+          } else {
+            dequant_block32(nib, d, bt + j * C::BT_KB + rr * 128, h, rr & 7);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (PAIR)
+            mbar_arrive_cluster(issuer_bar(&bfull[sb]));
+          else
+            mbar_arrive(&bfull[sb]);
+          mbar_arrive(&empty_r[sr]);
+        }
+      }
+    }
+  };
   const int wg = warp >> 2;
   if (wg == 1 || wg == 2) {
     // ================ epilogue warpgroups
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPI_REGS));
+    if constexpr (SOLO) dequant_loop(DQ_THREADS + (warp - EPI_WARP0) * 32 + lane, DQ_THREADS_ALL);
     {
       // ---------------- epilogue
       pdl_wait();
@@ -659,52 +714,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       __syncwarp();
     } else if (C::Q4) {
       // ---------------- dequant
-      const int t = dq_index(warp, lane);
-      uint32_t g = 0;
-      bool ok = true;
-      const int nst = (nkb + C::KS - 1) / C::KS;
-      for (int u = unit0; u < sh.n_units && ok; u += ustep) {
-        for (int i = 0; i < nst; ++i, ++g) {
-          const int kc = nkb - i * C::KS < C::KS ? nkb - i * C::KS : C::KS;
-          const int sr = g % C::NR, sb = g % C::NB;
-          bool w_ok = mbar_wait(&full_r[sr], (g / C::NR) & 1, err, PF_DEV_TIMEOUT_DEQUANT);
-          if (w_ok) w_ok = mbar_wait(&bempty[sb], ((g / C::NB) & 1) ^ 1, err, PF_DEV_TIMEOUT_DEQUANT);
-          ok = __all_sync(0xffffffffu, w_ok);
-          if (!ok) break;
-          uint8_t* bt = b_ring + sb * C::BT_BYTES;
-          const uint8_t* raw = r_ring + sr * C::RAW_BYTES;
-          // items: (k-block j, half h, row rr); a thread takes two at a time
-          // so that their shared-memory loads overlap
-          constexpr int R = C::BNL;  // weight rows staged by this CTA
-          const int items = kc * R * 2;
-          for (int it = t; it < items; it += 2 * DQ_THREADS) {
-            const int it2 = it + DQ_THREADS;
-            const int j = it / (R * 2), rr = it % R, h = (it / R) & 1;
-            const uint8_t* rj = raw + j * C::RAW_KB;
-            const uint4 nib = *reinterpret_cast<const uint4*>(rj + (size_t)(h * R + rr) * 16);
-            const __half d = *reinterpret_cast<const __half*>(rj + R * 32 + (h * R + rr) * 2);
-            if (it2 < items) {
-              const int j2 = it2 / (R * 2), rr2 = it2 % R, h2 = (it2 / R) & 1;
-              const uint8_t* rj2 = raw + j2 * C::RAW_KB;
-              const uint4 nib2 = *reinterpret_cast<const uint4*>(rj2 + (size_t)(h2 * R + rr2) * 16);
-              const __half d2 = *reinterpret_cast<const __half*>(rj2 + R * 32 + (h2 * R + rr2) * 2);
-              dequant_block32(nib, d, bt + j * C::BT_KB + rr * 128, h, rr & 7);
-              dequant_block32(nib2, d2, bt + j2 * C::BT_KB + rr2 * 128, h2, rr2 & 7);
-            } else {
-              dequant_block32(nib, d, bt + j * C::BT_KB + rr * 128, h, rr & 7);
-            }
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            if constexpr (PAIR)
-              mbar_arrive_cluster(issuer_bar(&bfull[sb]));
-            else
-              mbar_arrive(&bfull[sb]);
-            mbar_arrive(&empty_r[sr]);
-          }
-        }
-      }
+      dequant_loop(dq_index(warp, lane), DQ_THREADS_ALL);
     }
     if (split_mode) {
       // the epilogue warpgroups run the cluster reduction; these warps
