@@ -446,7 +446,13 @@ extern "C" int prefill_create(const prefill_model_desc* desc, const prefill_weig
       const int bn_pg = C->P <= 512 ? 64 : 128;
       if ((rc = build_weight(C, L.pg, plain_rows(lw.ple_gate, C->P, C->D, wt, bn_pg), C->D, bn_pg)))
         return fail(nullptr, rc, C->last_error);
-      if ((rc = build_weight(C, L.pp, plain_rows(lw.ple_proj, C->D, C->P, wt, 128), C->P, 128)))
+      // the PLE projection (K = P, a few k-blocks) is bound by its epilogue:
+      // 64-row tiles halve each CTA's share of it when the launch still fits
+      // one wave
+      int sms_pp = 0;
+      cudaDeviceGetAttribute(&sms_pp, cudaDevAttrMultiProcessorCount, C->device);
+      const int bn_pp = (C->D % 64 == 0 && (C->D / 64) * ((C->d.ubatch_max + 127) / 128) <= sms_pp) ? 64 : 128;
+      if ((rc = build_weight(C, L.pp, plain_rows(lw.ple_proj, C->D, C->P, wt, bn_pp), C->P, bn_pp)))
         return fail(nullptr, rc, C->last_error);
     }
     if ((rc = upload(C, &L.attn_norm, lw.attn_norm, C->D * 4))) return fail(nullptr, rc, C->last_error);
