@@ -72,10 +72,11 @@ def test_linear_f32(lib, wtype, M, N, K, bn):
 
 
 @pytest.mark.parametrize("wtype,bn,N,M", [(Q4, 64, 256, 512), (Q4, 128, 256, 512), (Q4, 256, 256, 512),
-                                          (F32, 128, 256, 512), (Q4, 128, 2560, 1024)])
+                                          (F32, 128, 256, 512), (Q4, 128, 2560, 1024), (Q4, 128, 19200, 300)])
 def test_linear_row_independent_of_m(lib, wtype, bn, N, M):
     """A row's result is bit-identical whether the launch carries M rows or 1
-    (M = 1024 over 2560 columns takes two M tiles per CTA)."""
+    (M = 1024 over 2560 columns takes two M tiles per CTA; 300 rows over 150
+    tiles take the general persistent form, one row the one-unit form)."""
     rng = np.random.default_rng(3)
     K = 1536
     w, _, _ = _weights(wtype, rng, N, K)
