@@ -170,7 +170,7 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 }
 
 // CL: acquire at cluster scope, for phases that a peer CTA's release (a
-// remote arrive or a multicast tcgen05.commit) completes
+// remote arrive or a tcgen05.commit of the peer CTA) completes
 template <bool CL = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
   uint32_t ok;
@@ -406,15 +406,12 @@ __device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t adesc,
       : "memory");
 }
 
-// arrive on the mbarrier at this shared-memory offset in every CTA of
-// cta_mask (bit r = cluster rank r) once the pair's tcgen05 ops issued so far
-// by this thread have completed
-__device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
+// arrive on the mbarrier at shared::cluster address `cluster_addr` (this
+// CTA's or the peer's, from mapa) once the pair's tcgen05 ops issued so far
+// by this thread have completed; one commit per barrier to signal
+__device__ __forceinline__ void tc_commit_pair(uint32_t cluster_addr) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(cluster_addr)
+               : "memory");
 }
 
 // arrive (release at cluster scope) on an mbarrier given by its

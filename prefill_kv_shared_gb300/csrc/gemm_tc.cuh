@@ -41,7 +41,7 @@
 // unchanged tile layout and dequantised by its own warps), so per SM the
 // shared-memory operand traffic of B, the dequant work and the MMA
 // instructions per FLOP are halved.  The even CTA issues the MMAs and the
-// commits (multicast to both CTAs' barriers); the odd CTA forwards "my A
+// commits (one to each CTA's barrier); the odd CTA forwards "my A
 // stage has landed" and "my B stage is dequantised" to the even CTA's
 // barriers and returns "my accumulator is drained" from its epilogue.  Each
 // CTA's TMA and bulk copies complete on its own barriers only.
@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   // The issuing CTA's full_a, bfull and tempty also count the odd CTA's
   // forwarded arrivals (remote arrives, released at cluster scope): its MMA
   // thread waits on them with cluster-scope acquire.  Barriers that only
-  // tcgen05.commit completes (empty_a, bempty, tfull, multicast to both
+  // tcgen05.commit completes (empty_a, bempty, tfull, one commit to each of both
   // CTAs) order the tensor cores' accesses by themselves and are waited on
   // at CTA scope.
   const uint32_t peers = PAIR && issuer ? 2u : 1u;
@@ -682,9 +682,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                   }
                 }
               }
-              if constexpr (PAIR) {
-                tc_commit_pair(&empty_a[sa], 3);
-                tc_commit_pair(&bempty[sb], 3);
+              if constexpr (PAIR) {  // both CTAs' rings
+                for (uint32_t r2 = 0; r2 < 2; ++r2) {
+                  tc_commit_pair(map_to_rank(smem_u32(&empty_a[sa]), r2));
+                  tc_commit_pair(map_to_rank(smem_u32(&bempty[sb]), r2));
+                }
               } else {
                 tc_commit(&empty_a[sa]);
                 if (C::Q4) tc_commit(&bempty[sb]);
@@ -693,10 +695,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             __syncwarp();
           }
           if (ok && leader) {  // the unit's accumulator is complete
-            if constexpr (PAIR)
-              tc_commit_pair(&tfull[buf], 3);
-            else
+            if constexpr (PAIR) {
+              tc_commit_pair(map_to_rank(smem_u32(&tfull[buf]), 0));
+              tc_commit_pair(map_to_rank(smem_u32(&tfull[buf]), 1));
+            } else {
               tc_commit(&tfull[buf]);
+            }
           }
           __syncwarp();
         }
@@ -704,7 +708,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           // wait for the MMAs already issued before TMEM is freed (and,
           // with pairs, before the odd CTA may leave)
           if constexpr (PAIR)
-            tc_commit_pair(&tfull[0], 1);
+            tc_commit_pair(map_to_rank(smem_u32(&tfull[0]), 0));
           else
             tc_commit(&tfull[0]);
           mbar_drain(&tfull[0], 0);
