@@ -289,8 +289,10 @@ MICRO = dict(name="micro", n_layer=3, n_layer_kv_from_start=2, d_model=8, n_head
 def _model_brute(cfg, w, tokens, states=None):
     """Every step as float64 scalar loops, read straight from the method:
     pre-norm layers, Q/K/V projections, half-split RoPE, FP16 K/V, causal
-    GQA attention over the own or the source layer's cache, output projection,
-    GeGLU feed-forward, then the per-layer-embedding block.  With `states` a
+    GQA attention over the own or the source layer's cache (query head h
+    reads KV head h // (n_head / n_head_kv)), output projection, GeGLU or
+    SwiGLU feed-forward, then the per-layer-embedding block when the model
+    has one (ple_dim > 0).  With `states` a
     dict, also the rows entering each layer (states[il]), the final rows
     (states[n_layer]) and their output-normed form (states["embd"])."""
     D, L, S, P = cfg["d_model"], cfg["n_layer"], cfg["n_layer_kv_from_start"], cfg["ple_dim"]
@@ -318,10 +320,15 @@ def _model_brute(cfg, w, tokens, states=None):
     def gelu(a):
         return 0.5 * a * (1.0 + math.tanh(math.sqrt(2.0 / math.pi) * (a + 0.044715 * a ** 3)))
 
+    def silu(a):
+        return a / (1.0 + math.exp(-a))
+
+    act = gelu if cfg["ffn"] == "geglu" else silu
+
     f16 = lambda a: float(np.float16(a))
     x = [[float(w.tok_embd[t][i]) for i in range(D)] for t in tokens]
     ple = [[[float(w.ple_embd[t][il * P + p]) / math.sqrt(P) for p in range(P)]
-            for il in range(L)] for t in tokens]
+            for il in range(L)] for t in tokens] if P > 0 else None
     cache = {}
     for il in range(L):
         lw = w.layers[il]
@@ -355,9 +362,11 @@ def _model_brute(cfg, w, tokens, states=None):
         for t in range(T):
             y = norm(x[t], lw["ffn_norm"])
             gg = lin(lw["w_gate"], y); uu = lin(lw["w_up"], y)
-            h = [gelu(gg[f]) * uu[f] for f in range(F)]
+            h = [act(gg[f]) * uu[f] for f in range(F)]
             dn = lin(lw["w_down"], h)
             x[t] = [x[t][i] + dn[i] for i in range(D)]
+            if P == 0:
+                continue
             gate = lin(lw["ple_gate"], x[t])
             gp = [gelu(gate[p]) * ple[t][il][p] for p in range(P)]
             pp = lin(lw["ple_proj"], gp)
@@ -369,12 +378,13 @@ def _model_brute(cfg, w, tokens, states=None):
     return np.array(lin(w.tok_embd, y))
 
 
-def _micro_weights(scale=0.3):
-    cfg = dict(MICRO)
+def _micro_weights(scale=0.3, base=MICRO):
+    cfg = dict(base)
     w = synth.make_weights(cfg, seed=11)
     # larger weights so every term moves the output visibly
     w.tok_embd = w.tok_embd * 40
-    w.ple_embd = w.ple_embd * 40
+    if w.ple_embd is not None:
+        w.ple_embd = w.ple_embd * 40
     for lw in w.layers:
         for k, v in lw.items():
             if v is not None and v.ndim == 2:
@@ -419,6 +429,44 @@ def test_micro_model_brute_force_catches_planted_mistake(monkeypatch):
     bad = dict(cfg, kv_src=[-1, -1, 0])
     got = OracleContext(bad, w, max_ctx=16).ubatch(tokens, is_last=True)
     want = _model_brute(cfg, w, tokens)
+    assert np.abs(got - want).max() > 1e-2 * np.abs(want).max()
+
+
+# Two KV heads (query heads 0-1 read KV head 0, 2-3 read KV head 1),
+# SwiGLU, no per-layer embeddings, and KV-shared layers that read the last
+# writing layer of their own parity (layer 2 reads 0, layer 3 reads 1).
+MICRO_GQA = dict(name="micro-gqa", n_layer=4, n_layer_kv_from_start=2, d_model=16, n_head=4,
+                 n_head_kv=2, head_dim=4, ffn_dim=12, ffn="swiglu", vocab=13, ple_dim=0,
+                 rms_eps=1e-6, rope_base=10000.0, kv_src=[-1, -1, 0, 1], wtype="f32")
+
+
+def test_micro_gqa_swiglu_model_matches_brute_force():
+    cfg, w = _micro_weights(base=MICRO_GQA)
+    tokens = np.array([3, 12, 0, 7, 5, 9, 1], dtype=np.int32)
+    want = _model_brute(cfg, w, tokens)
+    got = OracleContext(cfg, w, max_ctx=16).ubatch(tokens, is_last=True)
+    np.testing.assert_allclose(got, want, rtol=2e-4, atol=2e-4 * np.abs(want).max())
+    # the pruned ordering over ragged ubatches (positions continue across
+    # them; the intermediate ubatches stop before the first KV-shared layer)
+    got = OracleContext(cfg, w, max_ctx=16).prefill(tokens, ubatch=3, prune=True)
+    np.testing.assert_allclose(got, want, rtol=2e-4, atol=2e-4 * np.abs(want).max())
+
+
+def test_micro_gqa_brute_force_catches_planted_head_mapping(monkeypatch):
+    """A planted error in the oracle (query head h reading KV head h % n_head_kv
+    instead of h // (n_head / n_head_kv)) must break the pin."""
+    import oracle.prefill as op
+    cfg, w = _micro_weights(base=MICRO_GQA)
+    tokens = np.array([3, 12, 0, 7, 5, 9, 1], dtype=np.int32)
+    want = _model_brute(cfg, w, tokens)
+    real = op.attention
+    perm = np.array([0, 2, 1, 3])  # its own inverse
+
+    def planted(q, k, v, pos):
+        return real(q[:, perm], k, v, pos)[:, perm]
+
+    monkeypatch.setattr(op, "attention", planted)
+    got = OracleContext(cfg, w, max_ctx=16).ubatch(tokens, is_last=True)
     assert np.abs(got - want).max() > 1e-2 * np.abs(want).max()
 
 
