@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import oracle
-from oracle.prefill import KVImageError, OracleContext, as_f32_matrix, rope_tables
+from oracle.prefill import KVImageError, OracleContext, as_f32_matrix, rope_tables, rows_f32
 from prefill_kv_shared_gb300 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -74,6 +74,23 @@ def test_q4_0_matrix_layout():
             j = c % 32
             n = (b[2 + j] & 0xF) if j < 16 else (b[2 + j - 16] >> 4)
             assert float(m[r, c]) == d * (int(n) - 8)
+
+
+def test_q4_0_row_gather():
+    """The embedding gather picks whole rows by token id (repeats and the
+    last row included), each decoded by the definition."""
+    rng = np.random.default_rng(8)
+    table = synth.draw_q4_0(rng, 5, 64)
+    ids = np.array([4, 0, 4, 2])
+    got = rows_f32(table, ids)
+    assert got.shape == (4, 64) and got.dtype == np.float32
+    for t, r in enumerate(ids):
+        for c in range(64):
+            b = table[r, c // 32]
+            d = _half_bits_to_f64(int(b[0]) | (int(b[1]) << 8))
+            j = c % 32
+            n = (b[2 + j] & 0xF) if j < 16 else (b[2 + j - 16] >> 4)
+            assert float(got[t, c]) == d * (int(n) - 8)
 
 
 # ---------------------------------------------------------------------------
