@@ -32,7 +32,8 @@
  *     default stream when NULL).  prefill_ubatch, kv_save and kv_load return
  *     once the work is enqueued; prefill_sync() waits for it and reports a
  *     device-side error (a bad token, a timed-out pipeline wait).
- *   - A context holds one sequence (n_seq_max == 1).
+ *   - A context holds one sequence, unless its description sets n_seq_max
+ *     above 1 (then prefill_ubatch_seqs feeds several; see there).
  */
 #ifndef PREFILL_KV_SHARED_H
 #define PREFILL_KV_SHARED_H
@@ -213,7 +214,7 @@ int prefill_seq_reset(prefill_ctx* ctx, int32_t seq_id);
    pos0 + n_tokens - 1), the same logits buffer, the pruning mode and
    outputs in force when it was recorded; it needs the context's position
    count to be pos0 (PF_E_ARG otherwise) and advances it like the call.
-   One kernel launch sequence of ~250 kernels becomes one graph launch.
+   The ubatch's few hundred kernel launches become one graph launch.
    Recording needs a context created on a non-default stream and per-launch
    timing off; the launch counts of prefill_get_stats do not include
    replays.  A new recording replaces the previous one. */
@@ -315,8 +316,10 @@ int prefill_kv_file_check(const char* path, int32_t n_layers_written, int32_t kv
 #define PF_KC_ATTN 1      /* prefill attention and its group-state merge */
 #define PF_KC_NORM 2      /* RMSNorm (+ row gather) */
 #define PF_KC_OTHER 3     /* embedding gather, KV image copies */
-#define PF_KC_GEMM_ROW 4  /* projections of at most 16 rows: the pruned output row and the LM head (weight-bound) */
-#define PF_KC_ATTN_ROW 5  /* the single-row attention of the KV-shared layers after pruning */
+#define PF_KC_GEMM_ROW 4  /* projections of at most 16 rows: the one-row stream projections of the output row and
+                           of one-token ubatches, the LM head (weight-bound) */
+#define PF_KC_ATTN_ROW 5  /* the single-row attention: the output row in the KV-shared layers, every layer of a
+                           one-token ubatch (HBM-bound) */
 #define PF_KC_COUNT 6
 
 typedef struct prefill_stats {
