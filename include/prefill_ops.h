@@ -57,16 +57,21 @@ int pfop_linear_qkv(int32_t wtype, const void* wq_host, const void* wk_host, con
 
 /* Causal GQA attention: q fp16 [M][Hq*hd] at positions pos_base+m, K/V fp16
    [positions][Hkv*hd] with keys [0, kv_len) valid; out bf16 [M][Hq*hd].
-   Keys are folded in 64-key chunks, the chunks in groups of
-   ceil(ceil(kv_len/64)/4); one CTA per (64-row block, group), then an
-   ordered merge of the group states of rows whose keys span several groups.
-   mode 0: any M.  mode 1: one row (M == 1) at position pos_base, the form
-   the KV-shared layers use for the output row (G4 section 1: after the
-   pruning those layers carry that row only): the keys [0, pos_base] are cut
-   into 64-key tiles and the tiles into ranges over about 148 CTAs, each CTA
-   streams its range once (online softmax, fp32 accumulation), and a merge
-   kernel combines the range states in a fixed order.  Its bits depend on
-   pos_base only, not on the launch; they differ from mode 0's in rounding. */
+   mode 0: any M.  The (query row, query head of a KV head's group) pairs
+   form 128-row blocks; keys are folded in 64-key chunks, the chunks in at
+   most four groups (as many as keep the launch to one wave of CTAs, at
+   least four chunks a group); one CTA per (row block, KV head, group),
+   then an ordered merge of the group states of rows whose keys span
+   several groups.
+   mode 1: one row (M == 1) at position pos_base, the form the KV-shared
+   layers use for the output row (G4 section 1: after the pruning those
+   layers carry that row only): the keys [0, pos_base] are cut into 64-key
+   tiles and the tiles into ranges over up to 144 CTAs in clusters of four;
+   each CTA streams its range once (online softmax, fp32 accumulation), a
+   cluster folds its four range states in rank order, and the last cluster
+   of each KV head merges the cluster states in cluster order, all in one
+   launch.  Its bits depend on pos_base only, not on the launch; they differ
+   from mode 0's in rounding. */
 int pfop_attention(int32_t mode, const void* q_dev, const void* k_dev, const void* v_dev, int32_t M, int32_t Hq,
                    int32_t Hkv, int32_t hd, int32_t pos_base, int32_t kv_len, void* out_dev, void* stream);
 
@@ -124,8 +129,8 @@ int pfop_linear_bench(int32_t wtype, const void* w_host, int32_t N, int32_t K, i
 
 /* Time the attention kernels of pfop_attention (same arguments and modes):
    `warmup` untimed calls, then `iters` timed ones, each bracketed by its own
-   CUDA events on `stream`; *us = mean device time per call (the split or
-   prefill kernel plus the group-state merge when it runs).  If scrub_dev is
+   CUDA events on `stream`; *us = mean device time per call (the single-row
+   kernel, or the prefill kernel plus the group-state merge when it runs).  If scrub_dev is
    not NULL, scrub_bytes of it (a caller-owned device buffer larger than L2)
    are overwritten before every timed call, outside the events, so that each
    call reads K/V from HBM (cold L2).  Reading K/V once is the op's
