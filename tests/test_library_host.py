@@ -99,6 +99,43 @@ def test_kv_header_check(lib):
     assert binding.kv_header_check(b"KV", 22, 256, 0, 2048, 2) == binding.PF_E_KV_MAGIC
 
 
+def test_kv_header_check_agrees_with_the_oracle(lib):
+    """The library's host check of a KV image and the oracle's restore refuse
+    the same images with the same class of error (PicoLM KV cache article,
+    "rules": wrong magic, a layer or KV-width mismatch, or a position count
+    beyond the image or the context), over 600 seeded cases that mix one or
+    two faults."""
+    import numpy as np
+    from oracle.prefill import KVImageError, OracleContext
+
+    L_w, kv = 2, 8
+    cfg = dict(n_layer=3, n_layer_kv_from_start=L_w, n_head=1, n_head_kv=1, head_dim=kv)
+    code = {"magic": binding.PF_E_KV_MAGIC, "shape": binding.PF_E_KV_SHAPE, "range": binding.PF_E_KV_RANGE}
+    rng = np.random.default_rng(12)
+    seen = set()
+    for _ in range(600):
+        n_img = int(rng.choice([-1, 0, 1, 5, 17]))
+        l_img = int(rng.choice([L_w, L_w, L_w, 1, 3]))
+        kv_img = int(rng.choice([kv, kv, kv, 4, 16]))
+        magic = bytes(rng.choice([b"KVCP", b"KVCP", b"KVCP", b"KVCQ", b"kvcp"]))
+        n_pos = int(rng.integers(-1, max(n_img, 0) + 3))
+        max_ctx = int(rng.choice([4, 16, 64]))
+        exact = 16 + 2 * max(l_img, 0) * max(n_img, 0) * max(kv_img, 0) * 2
+        size = int(rng.choice([exact, exact, exact - 1, exact + 16, 2]))
+        size = max(size, 0)
+        img = (magic + struct.pack("<iii", n_img, l_img, kv_img)).ljust(size, b"\0")[:size]
+        got = binding.kv_header_check(img, L_w, kv, n_pos, max_ctx, size)
+        o = OracleContext(cfg, None, max_ctx=max_ctx)
+        try:
+            o.kv_load(img, n_pos)
+            want = binding.PF_OK
+        except KVImageError as e:
+            want = code[e.code]
+        assert got == want, (magic, n_img, l_img, kv_img, n_pos, max_ctx, size)
+        seen.add(want)
+    assert seen == {binding.PF_OK, *code.values()}
+
+
 def test_stats_struct_matches_binding(tmp_path):
     """The ctypes mirror of prefill_stats has the header's class count and size."""
     import ctypes
