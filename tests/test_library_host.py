@@ -81,6 +81,31 @@ def test_prune_predicate_matches_listing(lib):
     assert binding.prune_predicate(base, prune=False) is False
 
 
+def test_prune_predicate_agrees_with_the_oracle(lib):
+    """The library's pruning condition and the oracle's agree on 500 seeded
+    descriptions (layer counts, the first KV-shared layer, sequences,
+    embeddings, sparse per-layer input requests, the on/off switch)."""
+    import numpy as np
+
+    base = synth.config("e2b")
+    rng = np.random.default_rng(21)
+    outcomes = set()
+    for _ in range(500):
+        L = int(rng.integers(1, 41))
+        S = int(rng.integers(1, L + 1))
+        nseq = int(rng.choice([1, 1, 1, 2, 3]))
+        emb = bool(rng.random() < 0.15)
+        inp = None if rng.random() < 0.5 else [bool(f) for f in rng.random(L + 1) < 0.04]
+        on = bool(rng.random() < 0.9)
+        cfg = dict(base, n_layer=L, n_layer_kv_from_start=S,
+                   kv_src=[-1 if i < S else S - 1 for i in range(L)])
+        got = binding.prune_predicate(cfg, on, nseq, emb, inp)
+        want = on and oracle.prune_shared(L, S, n_seq_max=nseq, embeddings=emb, embeddings_layer_inp=inp)
+        assert got == want, (L, S, nseq, emb, inp, on)
+        outcomes.add(got)
+    assert outcomes == {True, False}
+
+
 def _hdr(n, layers, kv, magic=b"KVCP"):
     return magic + struct.pack("<iii", n, layers, kv)
 
