@@ -27,8 +27,12 @@ Where the pages leave the architecture open, the oracle takes the plainest
 readings the rest supports: a pre-norm decoder with RMSNorm gains (1 + g),
 half-split RoPE, GELU in its tanh form, the per-layer-embedding block
 x += W_pp (gelu(W_pg x) * ple) after the FFN, no embedding scale and a tied
-head.  Those model-level semantics are "parity unpinned": nothing outside
-this oracle can confirm them.
+head.  Every function here is pinned by the tests to something outside it
+(hand-written values, closed forms, a published error bound, float64
+brute-force loops, the pages' worked size).  What no pin can confirm is the
+choice of those readings itself: the pages fix no architecture, so the
+brute-force models check that the oracle computes the readings correctly,
+not that a particular checkpoint would use them.
 """
 from .prefill import (  # noqa: F401
     OracleContext,
