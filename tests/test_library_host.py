@@ -41,6 +41,27 @@ def test_headers_are_plain_c():
         assert r.returncode == 0, r.stderr
 
 
+def test_plain_c_client(lib, tmp_path):
+    """A C99 program (tests/c_abi_client.c) compiled against include/prefill.h
+    and linked with the library: the host-only calls answer as the pages fix
+    them and, without a GPU, creating a context fails with PF_E_CUDA and a
+    message (no host fallback)."""
+    exe = str(tmp_path / "c_abi_client")
+    libdir = os.path.dirname(binding.LIB_PATH)
+    name = os.path.basename(binding.LIB_PATH)[3:-3]
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        os.path.join(ROOT, "tests", "c_abi_client.c"), "-L", libdir, "-l" + name,
+                        "-Wl,-rpath," + libdir, "-o", exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    args = [exe]
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        args.append("nogpu")
+    r = subprocess.run(args, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, f"check {r.returncode} failed: {r.stdout} {r.stderr}"
+    assert r.stdout.strip().endswith("ok")
+
+
 def test_every_declared_symbol_is_exported(lib):
     declared = _declared_functions()
     assert "prefill_ubatch" in declared and "kv_load" in declared and "pfop_attention" in declared
