@@ -145,12 +145,12 @@ def test_kv_header_check(lib):
     assert binding.kv_header_check(b"KV", 22, 256, 0, 2048, 2) == binding.PF_E_KV_MAGIC
 
 
-def test_kv_header_check_agrees_with_the_oracle(lib):
-    """The library's host check of a KV image and the oracle's restore refuse
-    the same images with the same class of error (PicoLM KV cache article,
-    "rules": wrong magic, a layer or KV-width mismatch, or a position count
-    beyond the image or the context), over 600 seeded cases that mix one or
-    two faults."""
+def test_kv_header_check_agrees_with_the_oracle(lib, tmp_path):
+    """The library's host checks of a KV image (in memory, and as a file
+    restored whole) and the oracle's restore refuse the same images with the
+    same class of error (PicoLM KV cache article, "rules": wrong magic, a
+    layer or KV-width mismatch, or a position count beyond the image or the
+    context), over 600 seeded cases that mix one or two faults."""
     import numpy as np
     from oracle.prefill import KVImageError, OracleContext
 
@@ -179,6 +179,18 @@ def test_kv_header_check_agrees_with_the_oracle(lib):
             want = code[e.code]
         assert got == want, (magic, n_img, l_img, kv_img, n_pos, max_ctx, size)
         seen.add(want)
+        path = str(tmp_path / "img.kvcp")
+        with open(path, "wb") as f:
+            f.write(img)
+        got_file, n_file = binding.kv_file_check(path, L_w, kv, max_ctx)
+        try:
+            OracleContext(cfg, None, max_ctx=max_ctx).kv_load(img, n_img)
+            want_file = binding.PF_OK
+        except KVImageError as e:
+            want_file = code[e.code]
+        assert got_file == want_file, ("file", magic, n_img, l_img, kv_img, max_ctx, size)
+        if want_file == binding.PF_OK:
+            assert n_file == n_img
     assert seen == {binding.PF_OK, *code.values()}
 
 
