@@ -180,6 +180,34 @@ int pfop_attention_split_noalloc(const void* q_dev, const void* k_dev, const voi
    on both forms; no effect on prefill contexts.  PF_E_ARG for other modes. */
 int pfop_set_gemm_pairs(int32_t mode);
 
+/* ---- host-only: the stored form of the weights (no GPU needed) ----
+   The library repacks every matrix at create into the order and layout its
+   kernels read; these two calls return that form so that it can be checked
+   on its own.
+
+   pfop_qkv_row_order: the stored row order of a layer's Q|K|V projection
+   (128-row tiles).  order[i] = the source row of stored row i, counting
+   rows of [Wq; Wk; Wv] (Wq: Hq*hd rows, then Wk and Wv: Hkv*hd rows each;
+   with_kv = 0: a Q-only projection), or -1 for a zero row padding the last
+   tile.  A Q or K head wider than a tile is cut into hd/128 tiles: tile j
+   of the head holds dims j*64 .. j*64+63 of each half of the head, so that
+   every RoPE pair (i, i + hd/2) lies in one tile; narrower heads and V rows
+   stay in order.  Returns the number of stored
+   rows (a multiple of 128), or PF_E_ARG (hd odd, hd above 128 and not a
+   multiple of it, cap too small).
+
+   pfop_repack_q4: a Q4_0 matrix [N][K] (K a multiple of 64) in tiles of bn
+   rows (64, 128, 192 or 256; N padded with zero rows to a multiple of bn).
+   Tile (t, kb), for t < ceil(N/bn) and 64-wide k-block kb < K/64, is bn*36
+   contiguous bytes at ((t * K/64) + kb) * bn*36: first the 16 nibble bytes
+   of 32-element block h (h = 0, 1: elements kb*64 + h*32 ..) of row r at
+   (h*bn + r)*16, then that block's fp16 scale at bn*32 + (h*bn + r)*2.
+   Padding rows hold nibble bytes 0x88 and scale 0 (value 0).  With dst NULL
+   returns the byte count; otherwise writes it to dst (host memory,
+   dst_bytes at least that) and returns it; PF_E_ARG for bad shapes. */
+int32_t pfop_qkv_row_order(int32_t Hq, int32_t Hkv, int32_t hd, int32_t with_kv, int32_t* order, int32_t cap);
+int64_t pfop_repack_q4(const void* w_host, int32_t N, int32_t K, int32_t bn, void* dst, int64_t dst_bytes);
+
 /* Last error message of a pfop_* call on this thread. */
 const char* pfop_last_error(void);
 

@@ -48,7 +48,8 @@ EXPORTS = (
     "pfop_attention_split_noalloc", "pfop_attention_bench", "pfop_kv_copy_bench",
     "kv_save_file", "kv_load_file", "prefill_kv_file_check", "pfop_linear_row", "prefill_set_output",
     "pfop_linear_wait_test", "prefill_ubatch_seqs", "prefill_seq_n_pos", "prefill_seq_reset",
-    "prefill_graph_capture", "prefill_graph_launch", "pfop_set_gemm_pairs",
+    "prefill_graph_capture", "prefill_graph_launch", "pfop_set_gemm_pairs", "pfop_qkv_row_order",
+    "pfop_repack_q4",
 )
 
 
@@ -158,6 +159,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "pfop_linear_row": (C.c_int, [i32, vp, i32, i32, i32, vp, vp, i32, C.POINTER(C.c_float), vp]),
         "pfop_linear_wait_test": (C.c_int, [i32, vp, i32, i32, i32, vp, i32, i32, vp, i32, vp]),
         "pfop_set_gemm_pairs": (C.c_int, [i32]),
+        "pfop_qkv_row_order": (i32, [i32, i32, i32, i32, vp, i32]),
+        "pfop_repack_q4": (i64, [vp, i32, i32, i32, vp, i64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -285,6 +288,34 @@ def kv_header_check(header: bytes, n_layers_written: int, kv_dim: int, n_pos: in
                     image_bytes: int) -> int:
     buf = (C.c_uint8 * 16).from_buffer_copy(header[:16].ljust(16, b"\0"))
     return int(load().prefill_kv_header_check(buf, n_layers_written, kv_dim, n_pos, max_ctx, image_bytes))
+
+
+def qkv_row_order(Hq: int, Hkv: int, hd: int, with_kv: bool = True):
+    """Stored row order of a Q|K|V projection (host only): the source row of
+    each stored row in [Wq; Wk; Wv], -1 for padding."""
+    import numpy as np
+    cap = ((Hq + 2 * Hkv) * hd + 127) // 128 * 128
+    out = np.empty(cap, dtype=np.int32)
+    n = int(load().pfop_qkv_row_order(Hq, Hkv, hd, 1 if with_kv else 0, out.ctypes.data, cap))
+    if n < 0:
+        raise PrefillError(n, load().pfop_last_error().decode())
+    return out[:n]
+
+
+def repack_q4(w, bn: int):
+    """A Q4_0 matrix [N][K/32][18] in the library's stored tile layout (host
+    only), as bytes."""
+    import numpy as np
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    N, K = w.shape[0], w.shape[1] * 32
+    need = int(load().pfop_repack_q4(w.ctypes.data, N, K, bn, None, 0))
+    if need < 0:
+        raise PrefillError(need, load().pfop_last_error().decode())
+    out = np.empty(need, dtype=np.uint8)
+    rc = int(load().pfop_repack_q4(w.ctypes.data, N, K, bn, out.ctypes.data, need))
+    if rc != need:
+        raise PrefillError(rc, load().pfop_last_error().decode())
+    return out
 
 
 # ---------------------------------------------------------------------------

@@ -124,6 +124,36 @@ extern "C" int pfop_set_gemm_pairs(int32_t mode) {
 
 void pf::set_op_error(const std::string& m) { g_err = m; }
 
+extern "C" int32_t pfop_qkv_row_order(int32_t Hq, int32_t Hkv, int32_t hd, int32_t with_kv, int32_t* order,
+                                      int32_t cap) {
+  if (Hq < 1 || Hkv < 1 || hd < 2 || hd % 2 || (hd > QKV_BN && hd % QKV_BN) || !order || cap < 0)
+    return op_fail(PF_E_ARG, "bad argument");
+  const size_t q = static_cast<size_t>(Hq) * hd, kv = static_cast<size_t>(Hkv) * hd;
+  // one byte per source row: a stored row's source is its offset from base
+  std::vector<uint8_t> base(q + 2 * kv);
+  const uint8_t* b = base.data();
+  const std::vector<const void*> rows =
+      qkv_tile_rows(b, with_kv ? b + q : nullptr, with_kv ? b + q + kv : nullptr, Hq, Hkv, hd, 1, QKV_BN);
+  if (rows.size() > static_cast<size_t>(cap)) return op_fail(PF_E_ARG, "order holds fewer than the stored rows");
+  for (size_t i = 0; i < rows.size(); ++i)
+    order[i] = rows[i] ? static_cast<int32_t>(static_cast<const uint8_t*>(rows[i]) - b) : -1;
+  return static_cast<int32_t>(rows.size());
+}
+
+extern "C" int64_t pfop_repack_q4(const void* w_host, int32_t N, int32_t K, int32_t bn, void* dst, int64_t dst_bytes) {
+  if (!w_host || N < 1 || K < 64 || K % 64 || (bn != 64 && bn != 128 && bn != 192 && bn != 256))
+    return op_fail(PF_E_ARG, "bad argument");
+  const size_t rb = static_cast<size_t>(K / 32) * 18;
+  std::vector<const uint8_t*> rows(static_cast<size_t>(rup(N, bn)), nullptr);
+  for (int n = 0; n < N; ++n) rows[n] = static_cast<const uint8_t*>(w_host) + n * rb;
+  const std::vector<uint8_t> t = repack_q4_tiles(rows, K, bn);
+  const int64_t need = static_cast<int64_t>(t.size());
+  if (!dst) return need;
+  if (dst_bytes < need) return op_fail(PF_E_ARG, "dst smaller than the stored matrix");
+  std::memcpy(dst, t.data(), t.size());
+  return need;
+}
+
 extern "C" int pfop_linear_f32(int32_t wtype, const void* w_host, int32_t N, int32_t K, int32_t bn, const void* a_dev,
                                int32_t a_rows, int32_t M, float* out_dev, void* stream) {
   if (!w_host || !a_dev || !out_dev || N < 1 || M < 1 || M > a_rows ||

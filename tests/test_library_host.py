@@ -194,6 +194,59 @@ def test_kv_header_check_agrees_with_the_oracle(lib, tmp_path):
     assert seen == {binding.PF_OK, *code.values()}
 
 
+@pytest.mark.parametrize("Hq,Hkv,hd,with_kv", [(8, 1, 256, True), (8, 2, 256, True), (8, 1, 256, False),
+                                             (4, 1, 64, True), (32, 4, 64, True), (2, 1, 128, True)])
+def test_qkv_row_order_keeps_rope_pairs_in_a_tile(lib, Hq, Hkv, hd, with_kv):
+    """The stored Q|K|V rows: every source row exactly once, the last tile
+    padded, every RoPE pair (i, i + hd/2) of a Q or K head inside one
+    128-row tile (the epilogue rotates a pair within its tile), V in order."""
+    import numpy as np
+    order = binding.qkv_row_order(Hq, Hkv, hd, with_kv)
+    q, kv = Hq * hd, Hkv * hd
+    n_src = q + (2 * kv if with_kv else 0)
+    assert len(order) == (n_src + 127) // 128 * 128
+    real = order[order >= 0]
+    assert sorted(real.tolist()) == list(range(n_src))
+    assert (order[len(real):] == -1).all()
+    tile_of = {int(src): i // 128 for i, src in enumerate(order) if src >= 0}
+    for src in range(q + (kv if with_kv else 0)):
+        head, i = divmod(src, hd)
+        partner = head * hd + (i + hd // 2) % hd
+        assert tile_of[src] == tile_of[partner], (src, partner)
+    if hd <= 128:
+        assert (real == np.arange(n_src)).all()
+    if with_kv:
+        v_pos = [i for i, src in enumerate(order) if src >= q + kv]
+        assert [int(order[i]) for i in v_pos] == list(range(q + kv, n_src))
+    with pytest.raises(binding.PrefillError):
+        binding.qkv_row_order(Hq, Hkv, 192, with_kv)
+
+
+@pytest.mark.parametrize("N,K,bn", [(200, 128, 128), (200, 128, 192), (64, 64, 64), (300, 256, 256)])
+def test_repack_q4_matches_documented_tile_layout(lib, N, K, bn):
+    """The stored Q4_0 tiles, read back by the layout include/prefill_ops.h
+    documents, decode to the source matrix (the oracle's decode), with zero
+    rows padding the last tile."""
+    import numpy as np
+    rng = np.random.default_rng(N + K + bn)
+    w = synth.draw_q4_0(rng, N, K)
+    stored = binding.repack_q4(w, bn)
+    n_tiles, nkb = (N + bn - 1) // bn, K // 64
+    assert stored.size == n_tiles * nkb * bn * 36
+    want = oracle.prefill.as_f32_matrix(w)
+    got = np.zeros((n_tiles * bn, K), dtype=np.float32)
+    for t in range(n_tiles):
+        for kb in range(nkb):
+            tile = stored[(t * nkb + kb) * bn * 36:(t * nkb + kb + 1) * bn * 36]
+            for h in range(2):
+                nib = tile[h * bn * 16:(h + 1) * bn * 16].reshape(bn, 16)
+                sc = tile[bn * 32 + h * bn * 2:bn * 32 + (h + 1) * bn * 2].reshape(bn, 2)
+                blocks = np.concatenate([sc, nib], axis=1).reshape(bn, 1, 18)
+                got[t * bn:(t + 1) * bn, kb * 64 + h * 32:kb * 64 + h * 32 + 32] = oracle.q4_0_decode(blocks)[:, :32]
+    np.testing.assert_array_equal(got[:N], want)
+    assert not got[N:].any()
+
+
 def test_stats_struct_matches_binding(tmp_path):
     """The ctypes mirror of prefill_stats has the header's class count and size."""
     import ctypes
